@@ -1,0 +1,130 @@
+"""Hybrid-precision prefill operator.
+
+Follows *HyQuant: Hybrid-Precision Quantization for LLM Attention*,
+§4.2 Eq. 6-7 and Appendix A.2, Algorithm 2:
+
+    O = Softmax( alpha Q K^_Q^T || alpha Q K_FP^T ) (V^_Q || V_FP),  alpha = 1/sqrt(d)
+
+where K_FP / V_FP are the vertical-line keys and the window (kept in BF16)
+and K^_Q / V^_Q the rest, quantised tile by tile with symmetric scales
+``s = max|x| / c_B`` (c_B = 127 for INT8, 448 for FP8 e4m3; Algorithm 2,
+stage 2), and the queries with a per-query-block scale ``s^Q``.
+
+Readings (the paper leaves these open):
+
+* the window is the last W keys of the sequence (Algorithm 2, "last W
+  keys"); vertical-line positions come from ``[0, L - W)``;
+* the causal mask ``j <= i`` applies in every segment (a query block in the
+  middle of the sequence must not see later keys);
+* key tiles are B_N = 64 consecutive entries of the quantised-prefix
+  positions taken in ascending order (the reordered layout of Algorithm 2,
+  stage 1); the last tile may be short;
+* K uses one scale per tile; V one scale per (tile, channel); Q one scale
+  per block of 128 query rows of one head;
+* INT8 codes are ``clamp(rint(x / s), -127, 127)``, FP8 codes are the e4m3
+  value nearest to ``x / s`` (saturating at +-448);
+* the softmax probabilities are *not* quantised here.  A kernel that feeds a
+  low-precision P to the PV product differs from this oracle by the P
+  rounding step only; that difference is covered by the test tolerance
+  (parity unpinned for that step).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+C_B = {"int8": 127.0, "fp8": 448.0}
+KEY_TILE = 64
+QUERY_BLOCK = 128
+
+
+def _codes(x: np.ndarray, s, dtype: str) -> np.ndarray:
+    """Low-bit codes of x / s (float64 in, float64 code values out)."""
+    s = np.asarray(s, dtype=np.float64)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        t = np.where(s > 0, x / np.where(s > 0, s, 1.0), 0.0)
+    if dtype == "int8":
+        return np.clip(np.rint(t), -127, 127)
+    if dtype == "fp8":
+        t = np.clip(t, -448.0, 448.0)
+        return torch.from_numpy(t).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    raise ValueError(dtype)
+
+
+def quantize_symmetric(x, axis, dtype: str):
+    """Symmetric quantisation with ``s = max|x| / c_B`` over ``axis``.
+    Returns (dequantised values, codes, scales)."""
+    x = np.asarray(x, dtype=np.float64)
+    s = np.abs(x).max(axis=axis, keepdims=True) / C_B[dtype]
+    c = _codes(x, s, dtype)
+    return c * s, c, s
+
+
+def hybrid_prefill(q, k, v, vl_idx, window: int, dtype: str = "int8",
+                   key_tile: int = KEY_TILE, query_block: int = QUERY_BLOCK):
+    """Eq. 7 with Algorithm 2's quantisation, causal, float64.
+
+    q [B, HQ, L, d]; k, v [B, HKV, L, d]; vl_idx [B, HKV, k] (positions in
+    [0, L - W), or None).  Returns o [B, HQ, L, d] float64.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    B, HQ, L, d = q.shape
+    HKV = k.shape[1]
+    g = HQ // HKV
+    alpha = 1.0 / math.sqrt(d)
+    P = max(0, L - window)
+    out = np.zeros_like(q)
+    for b in range(B):
+        for kh in range(HKV):
+            vl = (np.zeros(0, np.int64) if vl_idx is None
+                  else np.asarray(vl_idx[b, kh], np.int64))
+            qpos = np.setdiff1d(np.arange(P), vl)
+            # Effective key/value rows for the quantised prefix, tile by tile.
+            kq = np.zeros((len(qpos), d))
+            vq = np.zeros((len(qpos), d))
+            for t0 in range(0, len(qpos), key_tile):
+                j = qpos[t0:t0 + key_tile]
+                kq[t0:t0 + len(j)] = quantize_symmetric(k[b, kh, j], None, dtype)[0]
+                vq[t0:t0 + len(j)] = quantize_symmetric(v[b, kh, j], 0, dtype)[0]
+            fp = np.concatenate([vl, np.arange(P, L)])
+            pos = np.concatenate([qpos, fp])
+            Kall = np.concatenate([kq, k[b, kh, fp]])
+            Vall = np.concatenate([vq, v[b, kh, fp]])
+            nq = len(qpos)
+            for h in range(kh * g, (kh + 1) * g):
+                for r0 in range(0, L, query_block):
+                    rows = np.arange(r0, min(L, r0 + query_block))
+                    qb = q[b, h, rows]
+                    qhat = quantize_symmetric(qb, None, dtype)[0]
+                    # Quantised segment uses the quantised queries, the
+                    # full-precision segments the BF16 queries (Algorithm 2).
+                    lg = np.concatenate([alpha * qhat @ Kall[:nq].T,
+                                         alpha * qb @ Kall[nq:].T], axis=1)
+                    lg = np.where(pos[None, :] <= rows[:, None], lg, -np.inf)
+                    m = lg.max(axis=1, keepdims=True)
+                    e = np.exp(lg - m)
+                    out[b, h, rows] = (e @ Vall) / e.sum(axis=1, keepdims=True)
+    return out
+
+
+def causal_attention(q, k, v) -> np.ndarray:
+    """Exact causal softmax attention in float64 (the full-precision reference)."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    B, HQ, L, d = q.shape
+    g = HQ // k.shape[1]
+    alpha = 1.0 / math.sqrt(d)
+    out = np.zeros_like(q)
+    mask = np.tril(np.ones((L, L), dtype=bool))
+    for b in range(B):
+        for h in range(HQ):
+            lg = alpha * q[b, h] @ k[b, h // g].T
+            lg = np.where(mask, lg, -np.inf)
+            e = np.exp(lg - lg.max(axis=1, keepdims=True))
+            out[b, h] = (e @ v[b, h // g]) / e.sum(axis=1, keepdims=True)
+    return out

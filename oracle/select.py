@@ -1,0 +1,154 @@
+"""Vertical-line token identification (VTI).
+
+Follows *HyQuant: Hybrid-Precision Quantization for LLM Attention*,
+§4.1 Eq. 1-5 and Appendix A.1, Algorithm 1:
+
+* ``P = max(0, L_K - W)``: the local window is excluded; an empty prefix
+  selects nothing;
+* the proxy queries are summed (Algorithm 1 averages the tail queries; a sum
+  and a mean rank keys identically) and, for GQA, the g query heads that
+  share a KV head are summed too, so the score is computed once per KV head
+  without repeating K (the einsum form of Algorithm 1);
+* ``S(j) = u . k_j`` for j in the prefix -- raw dot products, no softmax and
+  no 1/sqrt(d) (Algorithm 1 takes TopK of ``Q_bar K_pre^T`` directly);
+* ``k = min(P, max(1, ceil(P * rho)))`` (Algorithm 1); with ``rho = 0`` the
+  set is empty (the pure low-bit special case);
+* TopK is taken with ties broken toward the lower position, and the set is
+  returned sorted ascending.
+
+``rho`` is carried as an integer number of parts per million so that
+``ceil(P * rho)`` is exact (5% = 50000 ppm).
+
+Readings: one set per KV head (the cache of Algorithm 4 is laid out per KV
+head, so a position can only leave the low-bit stream for the whole head);
+the proxy set is the most recent (at most 64) queries, per §5.5.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def prefix_len(L: int, window: int) -> int:
+    """``P = max(0, L - W)`` (Algorithm 1, first step)."""
+    return max(0, int(L) - int(window))
+
+
+def vl_count(P: int, rho_ppm: int) -> int:
+    """``k = min(P, max(1, ceil(P * rho)))``; 0 for an empty prefix or rho = 0."""
+    if P <= 0 or rho_ppm <= 0:
+        return 0
+    k = -((-P * int(rho_ppm)) // 1_000_000)   # exact integer ceil
+    return min(P, max(1, k))
+
+
+def proxy_sum(q_proxy, num_kv_heads: int) -> np.ndarray:
+    """Sum of proxy queries over time and over the query heads of each KV head.
+
+    q_proxy : [B, HQ, T, d]  ->  u : [B, HKV, d] (float64)
+    """
+    q = np.asarray(q_proxy, dtype=np.float64)
+    B, HQ, T, d = q.shape
+    g = HQ // num_kv_heads
+    return q.reshape(B, num_kv_heads, g, T, d).sum(axis=(2, 3))
+
+
+def scores(u, k_src, P: int) -> np.ndarray:
+    """``S(j) = u . k_j`` for j in [0, P).  u [B,HKV,d], k_src [B,HKV,>=P,d]."""
+    k = np.asarray(k_src, dtype=np.float64)[:, :, :P, :]
+    return np.einsum("bhd,bhpd->bhp", np.asarray(u, dtype=np.float64), k)
+
+
+def topk_ascending(S, k: int) -> np.ndarray:
+    """Indices of the k largest scores per row, ties to the lower index,
+    returned sorted ascending.  S [..., P] -> int64 [..., k]."""
+    S = np.asarray(S)
+    lead = S.shape[:-1]
+    P = S.shape[-1]
+    if k == 0 or P == 0:
+        return np.zeros(lead + (0,), dtype=np.int64)
+    flat = S.reshape(-1, P)
+    out = np.zeros((flat.shape[0], k), dtype=np.int64)
+    pos = np.arange(P)
+    for r in range(flat.shape[0]):
+        order = np.lexsort((pos, -flat[r]))   # primary: score desc, then index asc
+        out[r] = np.sort(order[:k])
+    return out.reshape(lead + (k,))
+
+
+def select_vertical(q_proxy, k_src, L: int, window: int, rho_ppm: int):
+    """Algorithm 1 end to end.  Returns (idx [B, HKV, k] ascending, S [B,HKV,P])."""
+    HKV = np.asarray(k_src).shape[1]
+    P = prefix_len(L, window)
+    k = vl_count(P, rho_ppm)
+    u = proxy_sum(q_proxy, HKV)
+    S = scores(u, k_src, P)
+    return topk_ascending(S, k), S
+
+
+# --- float32 error bounds used to judge a float32 implementation -----------
+
+def _gamma(n: int, unit: float = 2.0 ** -23) -> float:
+    # unit = 2^-23 (one float32 ulp, not half) so that the bound also covers
+    # accumulators that truncate instead of rounding to nearest.
+    return n * unit / (1.0 - n * unit)
+
+
+def score_error_bound(q_proxy, k_src, P: int) -> np.ndarray:
+    """A rigorous bound on |S32(j) - S(j)| for any float32 evaluation order.
+
+    The proxy sum u has n_u = T*g terms per component and the dot product d
+    terms; with gamma_n = n u / (1 - n u) (u = 2^-23) the standard
+    floating-point summation bounds give
+        |S32 - S| <= gamma_d * sum_i |u32_i k_ji| + sum_i |k_ji| * gamma_nu * U_i
+    where U_i = sum |q_i| over the summed queries, and |u32_i| <= |u_i| +
+    gamma_nu U_i.  Returned per (b, kvh, j) in float64.
+    """
+    q = np.asarray(q_proxy, dtype=np.float64)
+    k = np.abs(np.asarray(k_src, dtype=np.float64)[:, :, :P, :])
+    B, HQ, T, d = q.shape
+    HKV = k.shape[1]
+    g = HQ // HKV
+    n_u = T * g
+    u = np.abs(q.reshape(B, HKV, g, T, d).sum(axis=(2, 3)))
+    U = np.abs(q).reshape(B, HKV, g, T, d).sum(axis=(2, 3))
+    gu = _gamma(n_u)
+    u_hi = u + gu * U
+    return (_gamma(d) * np.einsum("bhd,bhpd->bhp", u_hi, k)
+            + gu * np.einsum("bhd,bhpd->bhp", U, k))
+
+
+def check_selection(S, bound, k: int, got) -> dict:
+    """Is ``got`` a valid top-k of scores known only to within ``bound``?
+
+    Keys whose whole interval [S-b, S+b] lies above the (k+1)-th largest
+    upper end must be selected; keys whose interval lies below the k-th
+    largest lower end must not be.  Keys in between are "ambiguous": either
+    outcome is valid.  Also checks size, uniqueness, order and range.
+    """
+    S = np.asarray(S, dtype=np.float64)
+    b = np.asarray(bound, dtype=np.float64)
+    got = np.asarray(got, dtype=np.int64)
+    P = S.shape[0]
+    res = dict(ok=True, ambiguous=0, reason="")
+    if got.shape != (k,):
+        return dict(ok=False, ambiguous=0, reason=f"size {got.shape} != ({k},)")
+    if k == 0:
+        return res
+    if np.any(np.diff(got) <= 0) or got.min() < 0 or got.max() >= P:
+        return dict(ok=False, ambiguous=0, reason="not strictly ascending / out of range")
+    hi = S + b
+    lo = S - b
+    hi_sorted = np.sort(hi)[::-1]
+    lo_sorted = np.sort(lo)[::-1]
+    tau_hi = hi_sorted[k] if k < P else -np.inf      # (k+1)-th largest upper end
+    tau_lo = lo_sorted[k - 1]                          # k-th largest lower end
+    must = lo > tau_hi
+    must_not = hi < tau_lo
+    sel = np.zeros(P, dtype=bool)
+    sel[got] = True
+    res["ambiguous"] = int(P - must.sum() - must_not.sum())
+    if np.any(must & ~sel):
+        res.update(ok=False, reason=f"missed {np.flatnonzero(must & ~sel)[:8].tolist()}")
+    elif np.any(must_not & sel):
+        res.update(ok=False, reason=f"wrongly chose {np.flatnonzero(must_not & sel)[:8].tolist()}")
+    return res

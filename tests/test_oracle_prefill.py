@@ -1,0 +1,95 @@
+"""Pins for the oracle's hybrid prefill operator (Eq. 6-7, Algorithm 2)."""
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+from gen import prefill_case
+from oracle.prefill import (C_B, causal_attention, hybrid_prefill, quantize_symmetric)
+from oracle.select import select_vertical
+
+
+def _np(c):
+    return c.q.double().numpy(), c.k.double().numpy(), c.v.double().numpy()
+
+
+def _sdpa_causal(q, k, v):
+    g = q.shape[1] // k.shape[1]
+    K = torch.from_numpy(k).repeat_interleave(g, 1)
+    V = torch.from_numpy(v).repeat_interleave(g, 1)
+    return F.scaled_dot_product_attention(torch.from_numpy(q), K, V, is_causal=True).numpy()
+
+
+def test_causal_reference_matches_torch():
+    q, k, v = _np(prefill_case(0, 1, 4, 2, 200, d=64))
+    np.testing.assert_allclose(causal_attention(q, k, v), _sdpa_causal(q, k, v), rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+def test_window_covering_sequence_is_exact(dtype):
+    q, k, v = _np(prefill_case(1, 1, 4, 2, 150, d=64))
+    o = hybrid_prefill(q, k, v, None, window=150, dtype=dtype)
+    np.testing.assert_allclose(o, _sdpa_causal(q, k, v), rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+def test_full_ratio_is_exact(dtype):
+    c = prefill_case(2, 1, 4, 2, 300, d=64, window=32)
+    q, k, v = _np(c)
+    idx = np.broadcast_to(np.arange(268), (1, 2, 268))
+    o = hybrid_prefill(q, k, v, idx, window=32, dtype=dtype)
+    np.testing.assert_allclose(o, _sdpa_causal(q, k, v), rtol=1e-12, atol=1e-13)
+
+
+def test_int8_codes_are_integers_with_max_at_127():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((64, 128))
+    xh, c, s = quantize_symmetric(x, None, "int8")
+    assert np.array_equal(c, np.rint(c)) and np.abs(c).max() == 127
+    assert np.abs(xh - x).max() <= s.max() / 2 + 1e-15
+    # integer tile products are exact in float64: the scaled product equals the
+    # product of dequantised operands
+    y = rng.standard_normal((16, 128))
+    yh, cy, sy = quantize_symmetric(y, None, "int8")
+    np.testing.assert_allclose((cy @ c.T) * (s * sy), yh @ xh.T, rtol=1e-12, atol=1e-12)
+
+
+def test_fp8_codes_are_e4m3_values_with_max_at_448():
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((64, 128)) * 3
+    xh, c, s = quantize_symmetric(x, 0, "fp8")          # per-channel scales
+    assert np.abs(c).max(axis=0).min() == 448.0
+    back = torch.from_numpy(c).to(torch.float8_e4m3fn).double().numpy()
+    assert np.array_equal(back, c)                      # representable exactly
+    rel = np.abs(xh - x) / np.maximum(np.abs(x), 1e-3)
+    assert np.median(rel) < 2 ** -4                     # 3-bit mantissa
+
+
+@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+def test_hybrid_beats_uniform_low_bit(dtype):
+    c = prefill_case(5, 1, 4, 2, 512, d=128, window=64, sink_frac=0.02, sink_gain=20.0, q_gain=4.0)
+    q, k, v = _np(c)
+    ex = causal_attention(q, k, v)
+    idx, _ = select_vertical(q[:, :, -64:], k, 512, 64, 50_000)
+    hyb = hybrid_prefill(q, k, v, idx, window=64, dtype=dtype)
+    uni = hybrid_prefill(q, k, v, None, window=0, dtype=dtype)
+    e_h = np.mean((hyb - ex) ** 2)
+    e_u = np.mean((uni - ex) ** 2)
+    assert e_h < e_u
+    assert e_h < 1e-3
+
+
+def test_causality():
+    c = prefill_case(6, 1, 2, 1, 256, d=64, window=32)
+    q, k, v = _np(c)
+    idx, _ = select_vertical(q[:, :, -32:], k, 256, 32, 50_000)
+    o1 = hybrid_prefill(q, k, v, idx, window=32)
+    k2, v2 = k.copy(), v.copy()
+    k2[:, :, 200:] += 5.0
+    v2[:, :, 200:] -= 3.0
+    o2 = hybrid_prefill(q, k2, v2, idx, window=32)
+    # rows before 200 see neither the changed keys nor values ...
+    # ... except through the per-tile quantisation scales of tiles that mix
+    # positions < 200 and >= 200, so compare only rows whose tiles are untouched.
+    assert np.array_equal(o1[:, :, :128], o2[:, :, :128])
+    assert not np.array_equal(o1[:, :, 230:], o2[:, :, 230:])

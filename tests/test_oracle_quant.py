@@ -1,0 +1,142 @@
+"""Pins for the oracle's asymmetric group quantiser (Algorithm 4 Quant, Eq. 9).
+
+Each test checks a property fixed by the definition of a uniform asymmetric
+grid over [min, max] of each contiguous group of 32 head_dim elements, not
+the oracle's own formula.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle.quant import QuantRangeError, dequantize, quantize, round_up_fp16
+
+
+def bf16_rows(seed, n, d=128, scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(n, d, generator=g) * scale
+    # give the four groups very different ranges so a wrong grouping axis shows
+    x = x * torch.tensor([0.01, 1.0, 30.0, 0.3]).repeat_interleave(d // 4)
+    return x.to(torch.bfloat16).double().numpy()
+
+
+def test_round_up_fp16_is_smallest_half_not_below():
+    rng = np.random.default_rng(0)
+    x = np.concatenate([rng.standard_normal(2000) * 10.0 ** rng.integers(-6, 4, 2000),
+                        [0.0, 1.0, 65504.0, 6e-8]])
+    h = round_up_fp16(x).astype(np.float64)
+    assert np.all(h >= x)
+    below = np.nextafter(round_up_fp16(x), np.float16(-np.inf)).astype(np.float64)
+    assert np.all(below < x)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_codes_are_nearest_grid_points_brute_force(bits):
+    x = bf16_rows(1, 64)
+    c, s, z = quantize(x, bits)
+    qmax = (1 << bits) - 1
+    xs = x.reshape(64, 4, 32)
+    sd = s.astype(np.float64)[..., None]
+    zd = z.astype(np.float64)[..., None]
+    grid = np.arange(qmax + 1)[None, None, None, :] * sd[..., None] + zd[..., None]
+    err = np.abs(xs[..., None] - grid)                       # every candidate code
+    best = err.min(axis=-1)
+    chosen = np.take_along_axis(err, c.reshape(64, 4, 32)[..., None].astype(np.int64), -1)[..., 0]
+    # the decision is taken in float32: allow a 1e-5 relative slack near ties
+    assert np.all(chosen <= best + 1e-5 * sd + 1e-12)
+    assert c.max() <= qmax and c.dtype == np.uint8
+
+
+def test_error_bound_half_step_over_contiguous_groups():
+    x = bf16_rows(2, 256)
+    xh = dequantize(*quantize(x))
+    xs = x.reshape(256, 4, 32)
+    rng_ = xs.max(-1) - xs.min(-1)
+    err = np.abs(x - xh).reshape(256, 4, 32).max(-1)
+    mn = xs.min(-1)
+    z_err = np.abs(mn - mn.astype(np.float16).astype(np.float64))
+    # half a grid step (range/15/2), widened by the fp16 rounding of the step
+    # (at most 2^-10 relative) and of the zero point.
+    assert np.all(err <= rng_ / 30.0 * (1 + 2 ** -9) + z_err + 1e-12)
+
+
+def test_grid_reaches_group_max_and_min():
+    x = bf16_rows(3, 128)
+    c, s, z = quantize(x)
+    xs = x.reshape(128, 4, 32)
+    top = 15 * s.astype(np.float64) + z.astype(np.float64)
+    assert np.all(top >= xs.max(-1) - 1e-12)
+    assert np.all(z.astype(np.float64) <= xs.min(-1) + np.abs(xs.min(-1)) * 2 ** -11 + 1e-30)
+
+
+def test_ties_round_half_to_even():
+    # group 0: min 0, max 15 -> s = 1, z = 0; x = k + 0.5 lands on exact ties
+    row = np.zeros(128)
+    row[0], row[1] = 0.0, 15.0
+    row[2:10] = [0.5, 1.5, 2.5, 3.5, 4.5, 5.5, 6.5, 14.5]
+    c, s, z = quantize(row[None])
+    assert float(s[0, 0]) == 1.0 and float(z[0, 0]) == 0.0
+    assert c[0, 2:10].tolist() == [0, 2, 2, 4, 4, 6, 6, 14]
+
+
+def test_constant_group_has_zero_scale_and_codes():
+    row = np.full((1, 128), 0.75)
+    row[0, 32:64] = np.linspace(-1, 1, 32).astype(np.float32)
+    row[0, 32:64] = torch.tensor(row[0, 32:64]).to(torch.bfloat16).double().numpy()
+    c, s, z = quantize(row)
+    assert float(s[0, 0]) == 0.0 and np.all(c[0, :32] == 0)
+    assert np.all(dequantize(c, s, z)[0, :32] == 0.75)
+    assert float(s[0, 1]) > 0
+
+
+def test_two_valued_group_reconstructs_min_and_max_exactly():
+    row = np.zeros((1, 128))
+    row[0, :32] = np.where(np.arange(32) % 3 == 0, -1.5, 6.0)   # (6+1.5)/15 = 0.5 exact
+    c, s, z = quantize(row)
+    xh = dequantize(c, s, z)
+    assert np.array_equal(xh[0, :32], row[0, :32])
+
+
+def test_power_of_two_scaling_equivariance():
+    x = bf16_rows(4, 32)
+    c1, s1, z1 = quantize(x)
+    c2, s2, z2 = quantize(x * 4.0)
+    assert np.array_equal(c1, c2)
+    assert np.array_equal(s1.astype(np.float64) * 4, s2.astype(np.float64))
+    assert np.array_equal(z1.astype(np.float64) * 4, z2.astype(np.float64))
+
+
+def test_groups_are_independent():
+    x = bf16_rows(5, 16)
+    y = x.copy()
+    y[:, 32:64] *= 8.0
+    c1, s1, z1 = quantize(x)
+    c2, s2, z2 = quantize(y)
+    for gi in (0, 2, 3):
+        sl = slice(32 * gi, 32 * gi + 32)
+        assert np.array_equal(c1[:, sl], c2[:, sl])
+        assert np.array_equal(s1[:, gi], s2[:, gi]) and np.array_equal(z1[:, gi], z2[:, gi])
+    assert not np.array_equal(s1[:, 1], s2[:, 1])
+
+
+def test_8bit_is_finer_than_4bit():
+    x = bf16_rows(6, 64)
+    e4 = np.abs(dequantize(*quantize(x, 4)) - x).mean()
+    e8 = np.abs(dequantize(*quantize(x, 8)) - x).mean()
+    assert e8 < e4 / 8
+
+
+@pytest.mark.parametrize("bad", [-70000.0, 1.0e6, np.nan])
+def test_out_of_range_is_an_error(bad):
+    # -70000: the zero point (group min) overflows float16;
+    # 1e6: the step (range / 15) overflows float16.
+    row = np.zeros((1, 128))
+    row[0, 5] = bad
+    with pytest.raises(QuantRangeError):
+        quantize(row)
+
+
+def test_large_but_representable_group_is_fine():
+    row = np.zeros((1, 128))
+    row[0, 5] = 70000.0          # step 4667 and zero 0 are finite float16
+    c, s, z = quantize(row)
+    assert c[0, 5] == 15 and np.all(c[0, :5] == 0)
