@@ -1,0 +1,196 @@
+"""ctypes binding of libhyq (include/hyq.h).
+
+Argument marshalling only: every function here converts torch tensors to
+device pointers and calls the C entry point of the same name; all the work
+runs in the library's CUDA kernels.  Loading fails loudly when the library is
+missing -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from ._build import LIB
+
+c_int32 = ctypes.c_int32
+c_size_t = ctypes.c_size_t
+c_void_p = ctypes.c_void_p
+
+HYQ_OK = 0
+STATUS = {0: "HYQ_OK", 1: "HYQ_ERR_INVALID_ARG", 2: "HYQ_ERR_UNSUPPORTED", 3: "HYQ_ERR_WORKSPACE",
+          4: "HYQ_ERR_CAPACITY", 5: "HYQ_ERR_CUDA", 6: "HYQ_ERR_DEVICE"}
+DEVERR_QUANT_RANGE = 0x1
+DEVERR_COUNT = 0x2
+DEVERR_INDEX = 0x4
+DEVERR_SCORE = 0x8
+DEVERR_TIMEOUT = 0x10
+
+QBLOCK_ROWS = 64
+QBLOCK_BYTES = 10240
+COUNTS = 8
+CNT_NQ, CNT_NVL, CNT_NTAIL, CNT_LEN, CNT_RING_N, CNT_RING_POS = range(6)
+LAYOUT_FIELDS = ("qblocks", "vl_k", "vl_v", "vl_idx", "tail_k", "tail_v", "q_ring", "counts", "err")
+OP_SELECT, OP_DECODE, OP_PREFILL = 1, 2, 3
+
+# Every symbol include/hyq.h declares.
+SYMBOLS = ("hyq_status_string", "hyq_config_check", "hyq_vl_count", "hyq_layout_sizes",
+           "hyq_workspace_size", "hyq_layout_reset", "hyq_quantize_append",
+           "hyq_select_vertical", "hyq_rebuild", "hyq_decode_append", "hyq_decode_attention",
+           "hyq_read_device_error")
+
+
+class HyqConfig(ctypes.Structure):
+    _fields_ = [("batch", c_int32), ("num_q_heads", c_int32), ("num_kv_heads", c_int32),
+                ("head_dim", c_int32), ("group", c_int32), ("window", c_int32),
+                ("period", c_int32), ("rho_ppm", c_int32), ("capacity", c_int32)]
+
+
+class HyqLayout(ctypes.Structure):
+    _fields_ = [(name, c_void_p) for name in LAYOUT_FIELDS]
+
+
+class HyqError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)}")
+
+
+_lib = None
+
+
+def lib_path() -> str:
+    return os.environ.get("HYQ_LIB", LIB)
+
+
+def load() -> ctypes.CDLL:
+    """Load libhyq.so (built by ``__graft_entry__.build()``); raises if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libhyq not built: {path} is missing (run __graft_entry__.build())")
+    lib = ctypes.CDLL(path)
+    P = ctypes.POINTER
+    sig = {
+        "hyq_status_string": (ctypes.c_char_p, [c_int32]),
+        "hyq_config_check": (c_int32, [P(HyqConfig)]),
+        "hyq_vl_count": (c_int32, [P(HyqConfig), c_int32]),
+        "hyq_layout_sizes": (c_int32, [P(HyqConfig), P(c_size_t)]),
+        "hyq_workspace_size": (c_size_t, [P(HyqConfig), ctypes.c_int, c_int32]),
+        "hyq_layout_reset": (c_int32, [P(HyqConfig), P(HyqLayout), c_void_p]),
+        "hyq_quantize_append": (c_int32, [P(HyqConfig), c_void_p, c_void_p, c_int32, P(HyqLayout), c_void_p]),
+        "hyq_select_vertical": (c_int32, [P(HyqConfig), c_void_p, c_int32, c_int32, c_void_p, c_int32,
+                                          c_int32, c_void_p, P(c_int32), c_void_p, c_size_t, c_void_p]),
+        "hyq_rebuild": (c_int32, [P(HyqConfig), c_void_p, c_void_p, c_int32, c_int32, c_void_p, c_int32,
+                                  P(HyqLayout), c_void_p]),
+        "hyq_decode_append": (c_int32, [P(HyqConfig), c_void_p, c_void_p, c_void_p, P(HyqLayout),
+                                        c_void_p, c_void_p, c_int32, c_void_p]),
+        "hyq_decode_attention": (c_int32, [P(HyqConfig), c_void_p, P(HyqLayout), c_void_p, c_int32,
+                                           c_void_p, c_size_t, c_void_p]),
+        "hyq_read_device_error": (c_int32, [c_void_p, P(c_int32), c_void_p]),
+    }
+    for name in SYMBOLS:
+        fn = getattr(lib, name)
+        fn.restype, fn.argtypes = sig[name]
+    _lib = lib
+    return lib
+
+
+def _check(fn: str, status: int):
+    if status != HYQ_OK:
+        raise HyqError(fn, status)
+
+
+def ptr(t) -> int | None:
+    """Device (or host) address of a tensor, None for None."""
+    return None if t is None else t.data_ptr()
+
+
+def stream_ptr(stream=None) -> int:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+# --- thin wrappers, same names as the C entry points ------------------------
+
+def hyq_status_string(status: int) -> str:
+    return load().hyq_status_string(status).decode()
+
+
+def hyq_config_check(cfg: HyqConfig) -> int:
+    return load().hyq_config_check(ctypes.byref(cfg))
+
+
+def hyq_vl_count(cfg: HyqConfig, P: int) -> int:
+    return load().hyq_vl_count(ctypes.byref(cfg), P)
+
+
+def hyq_layout_sizes(cfg: HyqConfig) -> list[int]:
+    out = (c_size_t * len(LAYOUT_FIELDS))()
+    _check("hyq_layout_sizes", load().hyq_layout_sizes(ctypes.byref(cfg), out))
+    return list(out)
+
+
+def hyq_workspace_size(cfg: HyqConfig, op: int, len_hint: int = 0) -> int:
+    return load().hyq_workspace_size(ctypes.byref(cfg), op, len_hint)
+
+
+def hyq_layout_reset(cfg, lay: HyqLayout, stream=None):
+    _check("hyq_layout_reset", load().hyq_layout_reset(ctypes.byref(cfg), ctypes.byref(lay), stream_ptr(stream)))
+
+
+def hyq_quantize_append(cfg, k_rows, v_rows, n_rows: int, lay: HyqLayout, stream=None):
+    _check("hyq_quantize_append", load().hyq_quantize_append(
+        ctypes.byref(cfg), ptr(k_rows), ptr(v_rows), n_rows, ctypes.byref(lay), stream_ptr(stream)))
+
+
+def row_ld(t) -> int:
+    """Leading dimension (rows per head) of a [B, H, rows, 128] view whose rows
+    are dense 128-element vectors and whose heads are evenly strided."""
+    if t.dim() != 4 or t.shape[3] != 128 or t.stride(3) != 1 or t.stride(2) != 128:
+        raise ValueError("expected a [B, H, rows, 128] tensor with dense rows")
+    if t.stride(1) % 128 or (t.shape[0] > 1 and t.stride(0) != t.shape[1] * t.stride(1)):
+        raise ValueError("heads must be evenly strided")
+    return t.stride(1) // 128
+
+
+def hyq_select_vertical(cfg, q_proxy, n_proxy: int, k_src, L: int, idx_out, ws, stream=None) -> int:
+    """q_proxy [B, HQ, T, 128] (a view; its first n_proxy rows are used);
+    k_src [B, HKV, ld, 128]; idx_out int32 [B, HKV, k] contiguous."""
+    k_out = c_int32(0)
+    _check("hyq_select_vertical", load().hyq_select_vertical(
+        ctypes.byref(cfg), ptr(q_proxy), n_proxy, row_ld(q_proxy), ptr(k_src), row_ld(k_src), L,
+        ptr(idx_out), ctypes.byref(k_out), ptr(ws), ws.numel() * ws.element_size(), stream_ptr(stream)))
+    return k_out.value
+
+
+def hyq_rebuild(cfg, k_src, v_src, L: int, idx, k: int, lay: HyqLayout, stream=None):
+    ld = row_ld(k_src)
+    if row_ld(v_src) != ld:
+        raise ValueError("k_src and v_src must share the leading dimension")
+    _check("hyq_rebuild", load().hyq_rebuild(
+        ctypes.byref(cfg), ptr(k_src), ptr(v_src), ld, L, ptr(idx), k,
+        ctypes.byref(lay), stream_ptr(stream)))
+
+
+def hyq_decode_append(cfg, q, k_new, v_new, lay: HyqLayout, k_src=None, v_src=None, stream=None):
+    ld = row_ld(k_src) if k_src is not None else 0
+    _check("hyq_decode_append", load().hyq_decode_append(
+        ctypes.byref(cfg), ptr(q), ptr(k_new), ptr(v_new), ctypes.byref(lay), ptr(k_src), ptr(v_src),
+        ld, stream_ptr(stream)))
+
+
+def hyq_decode_attention(cfg, q, lay: HyqLayout, out, ws, len_hint: int = 0, stream=None):
+    _check("hyq_decode_attention", load().hyq_decode_attention(
+        ctypes.byref(cfg), ptr(q), ctypes.byref(lay), ptr(out), len_hint, ptr(ws),
+        ws.numel() * ws.element_size(), stream_ptr(stream)))
+
+
+def hyq_read_device_error(err_dev, stream=None) -> int:
+    host = c_int32(0)
+    st = load().hyq_read_device_error(ptr(err_dev), ctypes.byref(host), stream_ptr(stream))
+    if st not in (0, 6):
+        raise HyqError("hyq_read_device_error", st)
+    return host.value

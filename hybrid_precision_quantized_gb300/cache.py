@@ -1,0 +1,223 @@
+"""Device buffers of a layer's hybrid cache and the per-step driver.
+
+PyTorch only allocates memory and provides the stream; every step runs in
+libhyq's kernels through the thin binding in ``_lib``.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import _lib as L
+from ._lib import HyqConfig, HyqLayout
+
+
+def make_config(batch, num_q_heads, num_kv_heads, capacity, window=128, period=64,
+                rho_ppm=50_000, head_dim=128, group=32) -> HyqConfig:
+    return HyqConfig(batch=batch, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
+                     head_dim=head_dim, group=group, window=window, period=period,
+                     rho_ppm=rho_ppm, capacity=capacity)
+
+
+class HybridLayer:
+    """One layer's hybrid cache: torch-owned device buffers + the C layout view."""
+
+    def __init__(self, cfg: HyqConfig, device="cuda"):
+        self.cfg = cfg
+        sizes = L.hyq_layout_sizes(cfg)
+        self.buf = {n: torch.zeros(s, dtype=torch.uint8, device=device)
+                    for n, s in zip(L.LAYOUT_FIELDS, sizes)}
+        self.c = HyqLayout(**{n: self.buf[n].data_ptr() for n in L.LAYOUT_FIELDS})
+        self.nbytes = sum(sizes)
+
+    # typed views -----------------------------------------------------------
+    def counts(self) -> torch.Tensor:
+        return self.buf["counts"].view(torch.int32)[: self.cfg.batch * L.COUNTS].view(self.cfg.batch, L.COUNTS)
+
+    def err(self) -> torch.Tensor:
+        return self.buf["err"].view(torch.int32)[:1]
+
+    def qblocks(self) -> torch.Tensor:
+        c = self.cfg
+        nblk = -(-c.capacity // L.QBLOCK_ROWS)
+        n = c.batch * c.num_kv_heads * nblk * L.QBLOCK_BYTES
+        return self.buf["qblocks"][:n].view(c.batch, c.num_kv_heads, nblk, L.QBLOCK_BYTES)
+
+    def cap_vl(self) -> int:
+        c = self.cfg
+        return max(1, L.hyq_vl_count(c, max(0, c.capacity - c.window)))
+
+    def cap_tail(self) -> int:
+        return self.cfg.window + self.cfg.period
+
+    def _bf16(self, name, rows):
+        c = self.cfg
+        n = c.batch * c.num_kv_heads * rows * 128
+        return self.buf[name].view(torch.bfloat16)[:n].view(c.batch, c.num_kv_heads, rows, 128)
+
+    def vl_k(self):
+        return self._bf16("vl_k", self.cap_vl())
+
+    def vl_v(self):
+        return self._bf16("vl_v", self.cap_vl())
+
+    def vl_idx(self):
+        c = self.cfg
+        n = c.batch * c.num_kv_heads * self.cap_vl()
+        return self.buf["vl_idx"].view(torch.int32)[:n].view(c.batch, c.num_kv_heads, self.cap_vl())
+
+    def tail_k(self):
+        return self._bf16("tail_k", self.cap_tail())
+
+    def tail_v(self):
+        return self._bf16("tail_v", self.cap_tail())
+
+    def q_ring(self):
+        c = self.cfg
+        n = c.batch * c.num_q_heads * c.period * 128
+        return self.buf["q_ring"].view(torch.bfloat16)[:n].view(c.batch, c.num_q_heads, c.period, 128)
+
+    def reset(self, stream=None):
+        L.hyq_layout_reset(self.cfg, self.c, stream)
+
+
+def workspace(cfg: HyqConfig, op: int, len_hint: int = 0, device="cuda") -> torch.Tensor:
+    """Zero-filled workspace for one operation."""
+    n = L.hyq_workspace_size(cfg, op, len_hint)
+    if n == 0:
+        raise ValueError("invalid config or operation")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+# --- block-format reader (documented layout of include/hyq.h) --------------
+
+def _tile_maps():
+    """For each of the 1024*2 nibbles of a code tile: (row, element) for the K
+    and the V fragment orders, indexed [byte_offset * 2 + (0 low | 1 high)]."""
+    krow = np.zeros(2048, np.int64)
+    kel = np.zeros(2048, np.int64)
+    vrow = np.zeros(2048, np.int64)
+    vel = np.zeros(2048, np.int64)
+    for u in range(8):
+        for lane in range(32):
+            base = 512 * (u // 4) + 16 * lane + 4 * (u % 4)
+            for n in range(8):
+                byte = base + n // 2
+                slot = 2 * byte + (n % 2)
+                krow[slot] = (8 if n & 1 else 0) + lane // 4
+                kel[slot] = 16 * u + 2 * (lane % 4) + (8 if n & 2 else 0) + (n >> 2)
+                vrow[slot] = 2 * (lane % 4) + (8 if n & 2 else 0) + (n >> 2)
+                vel[slot] = 16 * u + lane // 4 + (8 if n & 1 else 0)
+    return krow, kel, vrow, vel
+
+
+_MAPS = None
+
+
+def unpack_qblocks(blocks: np.ndarray, n_rows: int):
+    """Decode the first ``n_rows`` rows of a 4-bit stream.
+
+    blocks : uint8 [nblk, 10240] (one (batch, KV head) stream)
+    Returns k_codes, v_codes uint8 [n_rows, 128]; k_scale, k_zero, v_scale,
+    v_zero float16 [n_rows, 4].
+    """
+    global _MAPS
+    if _MAPS is None:
+        _MAPS = _tile_maps()
+    krow, kel, vrow, vel = _MAPS
+    blocks = np.asarray(blocks, dtype=np.uint8)
+    nblk = blocks.shape[0]
+    kc = np.zeros((nblk * 64, 128), np.uint8)
+    vc = np.zeros((nblk * 64, 128), np.uint8)
+    for bi in range(nblk):
+        blk = blocks[bi]
+        for tile in range(4):
+            for which, codes, rmap, emap in ((0, kc, krow, kel), (1, vc, vrow, vel)):
+                raw = blk[which * 4096 + tile * 1024: which * 4096 + (tile + 1) * 1024]
+                nib = np.stack([raw & 15, raw >> 4], axis=1).reshape(-1)
+                codes[bi * 64 + tile * 16 + rmap, emap] = nib
+    meta_k = blocks[:, 8192:9216].copy().view(np.float16).reshape(nblk * 64, 4, 2)
+    meta_v = blocks[:, 9216:10240].copy().view(np.float16).reshape(nblk * 64, 4, 2)
+    n = n_rows
+    return (kc[:n], vc[:n], meta_k[:n, :, 0], meta_k[:n, :, 1], meta_v[:n, :, 0], meta_v[:n, :, 1])
+
+
+def pack_qblocks(k_codes, v_codes, k_scale, k_zero, v_scale, v_zero) -> np.ndarray:
+    """Inverse of ``unpack_qblocks`` (rows padded with zeros to whole blocks)."""
+    global _MAPS
+    if _MAPS is None:
+        _MAPS = _tile_maps()
+    krow, kel, vrow, vel = _MAPS
+    n = k_codes.shape[0]
+    nblk = -(-n // 64)
+    out = np.zeros((nblk, 10240), np.uint8)
+
+    def pad(a, shape, dtype):
+        z = np.zeros(shape, dtype)
+        z[: a.shape[0]] = a
+        return z
+
+    kc = pad(np.asarray(k_codes), (nblk * 64, 128), np.uint8)
+    vc = pad(np.asarray(v_codes), (nblk * 64, 128), np.uint8)
+    for bi in range(nblk):
+        for tile in range(4):
+            for which, codes, rmap, emap in ((0, kc, krow, kel), (1, vc, vrow, vel)):
+                nib = codes[bi * 64 + tile * 16 + rmap, emap].reshape(1024, 2)
+                out[bi, which * 4096 + tile * 1024: which * 4096 + (tile + 1) * 1024] = nib[:, 0] | (nib[:, 1] << 4)
+    for off, s, z in ((8192, k_scale, k_zero), (9216, v_scale, v_zero)):
+        m = np.zeros((nblk * 64, 4, 2), np.float16)
+        m[:n, :, 0] = s
+        m[:n, :, 1] = z
+        out[:, off:off + 1024] = m.view(np.uint8).reshape(nblk, 1024)
+    return out
+
+
+class HybridDecoder:
+    """Decode-time driver of one layer (the re-selecting mode).
+
+    Every ``period`` steps the vertical-line set is chosen again from the
+    proxy ring against the caller's BF16 keys and the layout is rebuilt
+    (select + rebuild); every step appends the token and runs the fused
+    decode attention.
+    """
+
+    def __init__(self, cfg: HyqConfig, k_src: torch.Tensor, v_src: torch.Tensor, device="cuda"):
+        self.cfg = cfg
+        self.layer = HybridLayer(cfg, device)
+        self.k_src, self.v_src = k_src, v_src
+        self.ws_sel = workspace(cfg, L.OP_SELECT, cfg.capacity, device)
+        self.ws_dec = workspace(cfg, L.OP_DECODE, cfg.capacity, device)
+        kmax = max(1, L.hyq_vl_count(cfg, max(0, cfg.capacity - cfg.window)))
+        self.idx = torch.zeros(cfg.batch, cfg.num_kv_heads, kmax, dtype=torch.int32, device=device)
+        self.length = 0
+        self.since = 0
+        self.ring_n = 0
+
+    def freeze(self, L_ctx: int, q_tail: torch.Tensor, stream=None):
+        """Prefill -> decode (Algorithm 4): choose the vertical-line set from the
+        tail queries ``q_tail`` [B, HQ, T, 128] and build the layout for the
+        first ``L_ctx`` positions of k_src / v_src."""
+        self.layer.reset(stream)
+        self.maintain(L_ctx, q_tail, q_tail.shape[2], stream)
+        self.length = L_ctx
+        self.since = 0
+
+    def maintain(self, L_ctx: int, q_proxy, n_proxy: int, stream=None):
+        k = L.hyq_select_vertical(self.cfg, q_proxy, n_proxy, self.k_src, L_ctx,
+                                  self.idx, self.ws_sel, stream) if n_proxy > 0 else 0
+        if n_proxy == 0:
+            k = 0
+        L.hyq_rebuild(self.cfg, self.k_src, self.v_src, L_ctx, self.idx, k, self.layer.c, stream)
+        return k
+
+    def step(self, q, k_new, v_new, out, stream=None):
+        """Append this token, re-select every ``period`` steps, attend."""
+        L.hyq_decode_append(self.cfg, q, k_new, v_new, self.layer.c, self.k_src, self.v_src, stream)
+        self.length += 1
+        self.since += 1
+        self.ring_n = min(self.ring_n + 1, self.cfg.period)
+        if self.since == self.cfg.period:
+            self.maintain(self.length, self.layer.q_ring(), self.ring_n, stream)
+            self.since = 0
+        L.hyq_decode_attention(self.cfg, q, self.layer.c, out, self.ws_dec, self.cfg.capacity, stream)
+        return out

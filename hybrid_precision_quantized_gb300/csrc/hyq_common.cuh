@@ -1,0 +1,175 @@
+// Internal helpers shared by the libhyq kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/hyq.h"
+
+#define HYQ_D 128
+#define HYQ_G 32
+#define HYQ_NGROUPS 4
+#define HYQ_MAX_GQA 8
+#define HYQ_TILE_BYTES 1024
+#define HYQ_KMETA_OFF 8192
+#define HYQ_VMETA_OFF 9216
+#define HYQ_VCODE_OFF 4096
+#define HYQ_DEVERR_TIMEOUT 0x10  // internal: a bounded wait gave up
+
+// ---------------------------------------------------------------------------
+// Launch plumbing shared by the translation units (defined in hyq_api.cu).
+// ---------------------------------------------------------------------------
+int hyq_num_sms();
+int32_t hyq_cap_vl(const hyq_config* c);
+inline int32_t hyq_cap_tail(const hyq_config* c) { return c->window + c->period; }
+// Row stride of the vertical-line buffers (at least one row is allocated).
+inline int32_t hyq_vl_stride(const hyq_config* c) { return hyq_cap_vl(c) > 0 ? hyq_cap_vl(c) : 1; }
+inline int32_t hyq_nblk(const hyq_config* c) { return (c->capacity + HYQ_QBLOCK_ROWS - 1) / HYQ_QBLOCK_ROWS; }
+
+// Kernel launchers (return the launch's cudaError_t).
+cudaError_t hyq_launch_quantize_append(const hyq_config* c, const void* k, const void* v,
+                                       int32_t n_rows, const hyq_layout* lay, cudaStream_t s);
+cudaError_t hyq_launch_rebuild(const hyq_config* c, const void* k_src, const void* v_src,
+                               int32_t ld, int32_t L, const int32_t* idx, int32_t k,
+                               const hyq_layout* lay, cudaStream_t s);
+cudaError_t hyq_launch_select(const hyq_config* c, const void* q_proxy, int32_t n_proxy,
+                              int32_t n_proxy_ld, const void* k_src, int32_t ld, int32_t L,
+                              int32_t* idx_out, int32_t k, void* ws, cudaStream_t s);
+size_t hyq_select_ws_bytes(const hyq_config* c, int32_t L);
+cudaError_t hyq_launch_decode_append(const hyq_config* c, const void* q, const void* k_new,
+                                     const void* v_new, const hyq_layout* lay, void* k_src,
+                                     void* v_src, int32_t ld, cudaStream_t s);
+cudaError_t hyq_launch_decode(const hyq_config* c, const void* q, const hyq_layout* lay,
+                              void* out, int32_t len_hint, void* ws, cudaStream_t s);
+size_t hyq_decode_ws_bytes(const hyq_config* c, int32_t len_hint);
+
+// ---------------------------------------------------------------------------
+// Device helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void hyq_set_err(int32_t* err, int32_t bits) {
+  if (err) atomicOr(err, bits);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// D += A * B, m16n8k16, bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// D += A * B, m16n8k16, fp16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Transpose an 8x8 b16 matrix held one row-pair per thread.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(d) : "r"(a));
+  return d;
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                            uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                                  uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// Two 4-bit codes (nibbles sh and sh+16 of w) as a bf16 pair (128 + c).
+__device__ __forceinline__ uint32_t nib2_bf16(uint32_t w, int sh) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;\n" : "=r"(r) : "r"(w >> sh), "r"(0x000F000Fu), "r"(0x43004300u));
+  return r;
+}
+
+// Two 4-bit codes as an fp16 pair of subnormals c * 2^-24 (exact; the tensor
+// cores take fp16 subnormal operands at full precision).  Unlike an offset
+// encoding there is nothing to cancel afterwards, so rounding the other
+// operand to fp16 does not get amplified.
+__device__ __forceinline__ uint32_t nib2_f16_sub(uint32_t w, int sh) {
+  return (w >> sh) & 0x000F000Fu;
+}
+#define HYQ_F16_SUB_SCALE 16777216.0f  // 2^24: undoes the subnormal code scale
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float2 half2_to_float2(uint32_t u) {
+  __half2 h = *reinterpret_cast<__half2*>(&u);
+  return __half22float2(h);
+}
+
+// ----- mbarrier + bulk copy (non-tensor TMA) -------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::);
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// Bounded wait for the given phase parity; returns false if it gave up.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t addr = smem_u32(bar);
+  for (int it = 0; it < (1 << 22); ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+// Global -> shared bulk copy (16-byte aligned addresses, size a multiple of 16),
+// completion counted on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ float warp_max_xor(float v, int lanemask_start) {
+  for (int o = lanemask_start; o < 32; o <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}

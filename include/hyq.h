@@ -1,0 +1,261 @@
+/*
+ * hyq.h -- C ABI of libhyq: hybrid-precision (4-bit + BF16) KV-cache attention
+ * for one NVIDIA GB300 GPU (sm_103a).
+ *
+ * The method is the one of "HyQuant: Hybrid-Precision Quantization for LLM
+ * Attention": per layer and KV head, the key/value positions are split into a
+ * small set of vertical-line positions and a recent window, kept in BF16, and
+ * the remaining majority, stored as asymmetric 4-bit codes (§4.1 Eq. 1-3,
+ * §4.3 Eq. 8).  Decode attention dequantises the 4-bit rows inside one
+ * online-softmax pass (§4.3 Eq. 9, Appendix A.3 Algorithm 3).
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ *  - Pointers named "device" point to GPU global memory owned by the caller;
+ *    "host" pointers to CPU memory.  The library never allocates memory and
+ *    never synchronises the stream (except hyq_read_device_error).
+ *  - All calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream).
+ *  - Arguments are validated on the host first; an invalid call returns an
+ *    error status before anything is launched and leaves all buffers as they
+ *    were.  Errors that only the GPU can see (a value out of range, a count
+ *    over capacity) set bits in a device error word instead (HYQ_DEVERR_*),
+ *    which the caller reads with hyq_read_device_error; the kernels never
+ *    trap and never wait on another block.
+ *  - BF16 tensors are passed as `void*` and hold IEEE bfloat16 values;
+ *    FP16 metadata is IEEE binary16.  All arrays are row-major and densely
+ *    packed unless a leading dimension is given.
+ *  - Only head_dim = 128, group = 32 and 1 <= HQ/HKV <= 8 are supported.
+ */
+#ifndef HYQ_H
+#define HYQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *hyq_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  HYQ_OK = 0,
+  HYQ_ERR_INVALID_ARG = 1, /* null pointer, bad size or unsupported shape   */
+  HYQ_ERR_UNSUPPORTED = 2, /* valid request this build does not implement   */
+  HYQ_ERR_WORKSPACE = 3,   /* workspace null, misaligned or too small        */
+  HYQ_ERR_CAPACITY = 4,    /* a length exceeds what the layout was sized for */
+  HYQ_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed           */
+  HYQ_ERR_DEVICE = 6       /* the device error word is non-zero              */
+} hyq_status;
+
+/* Bits of the device error word (an int32 in device memory). */
+#define HYQ_DEVERR_QUANT_RANGE 0x1 /* a group's scale or zero is not a finite FP16, or NaN input */
+#define HYQ_DEVERR_COUNT 0x2       /* a device-side count exceeded the layout capacity */
+#define HYQ_DEVERR_INDEX 0x4       /* an index list was not strictly ascending in range */
+#define HYQ_DEVERR_SCORE 0x8       /* a selection score was NaN */
+
+/* Shape and method parameters of one attention layer. */
+typedef struct {
+  int32_t batch;        /* B >= 1                                               */
+  int32_t num_q_heads;  /* HQ                                                   */
+  int32_t num_kv_heads; /* HKV; HQ % HKV == 0 and g = HQ / HKV in [1, 8]         */
+  int32_t head_dim;     /* d; must be 128                                       */
+  int32_t group;        /* G, elements per quantisation group along d; must be 32 */
+  int32_t window;       /* W >= 0, BF16 window length (128 in the paper)        */
+  int32_t period;       /* re-selection period and proxy-query count (64)      */
+  int32_t rho_ppm;      /* vertical-line ratio rho in parts per million (5% = 50000) */
+  int32_t capacity;     /* largest context length L the layout must hold        */
+} hyq_config;
+
+/*
+ * 4-bit block format.  The 4-bit stream of one (batch, KV head) is an array of
+ * blocks of HYQ_QBLOCK_ROWS consecutive stream rows, HYQ_QBLOCK_BYTES each:
+ *
+ *   [0,    4096)  K codes: four 16-row tiles of 1024 bytes
+ *   [4096, 8192)  V codes: four 16-row tiles of 1024 bytes
+ *   [8192, 9216)  K metadata: 64 rows x 4 groups x (scale, zero) FP16 pairs
+ *   [9216,10240)  V metadata: same
+ *
+ * Metadata entry (row r, group q) of a block lives at byte 16*r + 4*q of its
+ * region: scale s then zero z.  The dequantised value of element e of group
+ * q is c * s + z with c the 4-bit code.
+ *
+ * Inside a 1024-byte code tile (16 rows, 128 elements) the codes are ordered
+ * for the register fragments of a 16x16 tensor-core tile: byte offset
+ *   512*(u/4) + 16*lane + 4*(u%4)
+ * holds a 32-bit word whose nibble n (bits 4n..4n+3, n = 0..7) is the code
+ *   K tile: row (n&1 ? 8 : 0) + lane/4,  element 16*u + 2*(lane%4) + (n&2 ? 8 : 0) + (n>>2)
+ *   V tile: row 2*(lane%4) + (n&2 ? 8 : 0) + (n>>2),  element 16*u + lane/4 + (n&1 ? 8 : 0)
+ * for u = 0..7 and lane = 0..31.  Rows past the stream length inside the
+ * last block have zero codes and zero metadata.
+ */
+#define HYQ_QBLOCK_ROWS 64
+#define HYQ_QBLOCK_BYTES 10240
+
+/*
+ * Device buffers of one layer's hybrid cache (§4.3 Eq. 8, Algorithm 4's four
+ * buffers, with the staging buffer and the window held as one BF16 tail).
+ * Sizes in bytes come from hyq_layout_sizes(); all pointers are device
+ * pointers, 256-byte aligned.
+ *
+ *   qblocks  [B][HKV][nblk][HYQ_QBLOCK_BYTES]  4-bit stream, positions of the
+ *            non-window prefix that are not vertical-line, ascending
+ *   vl_k/v   bf16 [B][HKV][cap_vl][128]  vertical-line rows, ascending position
+ *   vl_idx   int32 [B][HKV][cap_vl]      their positions
+ *   tail_k/v bf16 [B][HKV][cap_tail][128] positions [P, L) in order
+ *   q_ring   bf16 [B][HQ][period][128]   the `period` most recent queries
+ *   counts   int32 [B][HYQ_COUNTS]       see HYQ_CNT_*
+ *   err      int32 [1]                    device error word
+ * with nblk = ceil(capacity / 64), cap_vl = vertical-line count at
+ * capacity, cap_tail = window + period.
+ */
+typedef struct {
+  uint8_t *qblocks;
+  void *vl_k;
+  void *vl_v;
+  int32_t *vl_idx;
+  void *tail_k;
+  void *tail_v;
+  void *q_ring;
+  int32_t *counts;
+  int32_t *err;
+} hyq_layout;
+
+#define HYQ_COUNTS 8
+#define HYQ_CNT_NQ 0       /* rows in the 4-bit stream                     */
+#define HYQ_CNT_NVL 1      /* vertical-line rows                           */
+#define HYQ_CNT_NTAIL 2    /* BF16 tail rows                               */
+#define HYQ_CNT_LEN 3      /* context length L = NQ + NVL + NTAIL          */
+#define HYQ_CNT_RING_N 4   /* valid entries in q_ring (<= period)          */
+#define HYQ_CNT_RING_POS 5 /* next q_ring slot                             */
+
+#define HYQ_LAYOUT_FIELDS 9 /* qblocks vl_k vl_v vl_idx tail_k tail_v q_ring counts err */
+
+#define HYQ_OP_SELECT 1
+#define HYQ_OP_DECODE 2
+#define HYQ_OP_PREFILL 3
+
+#define HYQ_PREFILL_INT8 1
+#define HYQ_PREFILL_FP8 2
+
+/* Human-readable name of a status. */
+const char *hyq_status_string(hyq_status s);
+
+/* Validate a config; HYQ_OK when every entry point accepts it. */
+hyq_status hyq_config_check(const hyq_config *cfg);
+
+/* Vertical-line count for a prefix of P positions (Algorithm 1):
+ * k = min(P, max(1, ceil(P * rho))), and 0 when P <= 0 or rho = 0.
+ * Returns -1 for a null config. */
+int32_t hyq_vl_count(const hyq_config *cfg, int32_t P);
+
+/* Bytes of each layout field, in the order of HYQ_LAYOUT_FIELDS
+ * (out[HYQ_LAYOUT_FIELDS], host). */
+hyq_status hyq_layout_sizes(const hyq_config *cfg, size_t *out);
+
+/* Workspace bytes an operation needs (HYQ_OP_*); 0 on an invalid config.
+ * A workspace must be zero-filled before its first use; the kernels leave it
+ * ready for the next call.  `len_hint` is the largest context length the
+ * call will see (0 = capacity). */
+size_t hyq_workspace_size(const hyq_config *cfg, int op, int32_t len_hint);
+
+/* Zero the counters and the error word of a layout (the empty cache). */
+hyq_status hyq_layout_reset(const hyq_config *cfg, const hyq_layout *lay, hyq_stream_t stream);
+
+/*
+ * Quant_B(.; G) of Algorithm 4 (Appendix A.4) and the low-bit cache of §4.3
+ * Eq. 8: quantise n_rows new rows per (batch, KV head) of K and V and append
+ * them to the 4-bit stream after its current NQ rows.
+ *   k_rows, v_rows  device bf16 [B][HKV][n_rows][128]
+ * Per group of 32 elements along head_dim, with mn/mx the group min/max:
+ *   s = FP16 value of (mx - mn) / 15 (float64 quotient) rounded toward +inf,
+ *   z = FP16 value of mn rounded to nearest even,
+ *   c = clamp(rint((x - z) * r), 0, 15) in float32 with r = 1/s rounded to
+ *       nearest (c = 0 when s = 0).
+ * A group with a non-finite s or z gets zero codes, s = z = 0 and sets
+ * HYQ_DEVERR_QUANT_RANGE.  Rows that would pass the capacity are dropped and
+ * set HYQ_DEVERR_COUNT.  Updates NQ and LEN.
+ */
+hyq_status hyq_quantize_append(const hyq_config *cfg, const void *k_rows, const void *v_rows,
+                               int32_t n_rows, const hyq_layout *lay, hyq_stream_t stream);
+
+/*
+ * Vertical-line token identification, Eq. 4-5 and Algorithm 1 (Appendix A.1).
+ *   q_proxy  device bf16 [B][HQ][n_proxy_ld][128]; the first n_proxy query
+ *            rows of each head are used (order does not matter)
+ *   k_src    device bf16 [B][HKV][ld][128], the BF16 keys, ld >= L
+ *   idx_out  device int32 [B][HKV][k]: positions, strictly ascending
+ *   k_out    host int32: k = hyq_vl_count(cfg, max(0, L - window))
+ * Per KV head: u = sum over the n_proxy proxy queries and the g query heads
+ * of the group; S(j) = u . k_j for j < P = max(0, L - W) in float32; the k
+ * positions with the largest S, ties to the lower position.
+ * Workspace: hyq_workspace_size(cfg, HYQ_OP_SELECT, L).
+ */
+hyq_status hyq_select_vertical(const hyq_config *cfg, const void *q_proxy, int32_t n_proxy,
+                               int32_t n_proxy_ld, const void *k_src, int32_t ld, int32_t L,
+                               int32_t *idx_out, int32_t *k_out, void *ws, size_t ws_bytes,
+                               hyq_stream_t stream);
+
+/*
+ * Build a layer's hybrid cache for context length L (Algorithm 4, with the
+ * vertical-line set re-chosen): the 4-bit stream holds the positions of
+ * [0, P) \ idx in ascending order, quantised as in hyq_quantize_append; the
+ * vertical-line buffers hold the BF16 rows of idx; the tail holds [P, L).
+ *   k_src, v_src  device bf16 [B][HKV][ld][128]
+ *   idx           device int32 [B][HKV][k], strictly ascending in [0, P)
+ * Sets NQ = P - k, NVL = k, NTAIL = L - P, LEN = L.  Leaves q_ring alone.
+ * An idx list that is not strictly ascending within [0, P) sets
+ * HYQ_DEVERR_INDEX (the output is then unspecified but in bounds).
+ */
+hyq_status hyq_rebuild(const hyq_config *cfg, const void *k_src, const void *v_src, int32_t ld,
+                       int32_t L, const int32_t *idx, int32_t k, const hyq_layout *lay,
+                       hyq_stream_t stream);
+
+/*
+ * One decode step's bookkeeping (Algorithm 3 inputs, §5.5 query buffer):
+ * append this step's key/value row to the BF16 tail, store the query in the
+ * proxy ring, and (when k_src/v_src are non-null) write the row into the
+ * caller's BF16 cache at position LEN.  Updates NTAIL, LEN, RING_N, RING_POS.
+ *   q        device bf16 [B][HQ][128]
+ *   k_new    device bf16 [B][HKV][128];  v_new likewise
+ *   k_src    device bf16 [B][HKV][ld][128] or NULL;  v_src likewise
+ * A full tail (NTAIL = window + period) or LEN >= ld drops the row and sets
+ * HYQ_DEVERR_COUNT.
+ */
+hyq_status hyq_decode_append(const hyq_config *cfg, const void *q, const void *k_new,
+                             const void *v_new, const hyq_layout *lay, void *k_src,
+                             void *v_src, int32_t ld, hyq_stream_t stream);
+
+/*
+ * Hybrid-precision decode attention, §4.3 Eq. 8-9 and Algorithm 3 (Appendix
+ * A.3): for every query head h (KV head h / g)
+ *   out_h = sum_j exp(a q_h.k~_j - M) v~_j / sum_j exp(a q_h.k~_j - M),
+ * a = 1/sqrt(128), over the LEN positions of the layout, with k~, v~ the
+ * dequantised 4-bit rows (c*s + z) and the BF16 vertical-line and tail rows.
+ * The 4-bit stream is split along the sequence across thread blocks, the g
+ * query heads of a KV head are processed together, and the split partials
+ * are merged by log-sum-exp rescaling in the same launch.
+ *   q    device bf16 [B][HQ][128]
+ *   out  device bf16 [B][HQ][128] (zeros when LEN = 0)
+ *   len_hint  an upper bound of the current context lengths, used only to
+ *        size the launch (0 = capacity)
+ * Workspace: hyq_workspace_size(cfg, HYQ_OP_DECODE, len_hint), zero-filled
+ * before first use; one workspace must not be used by two calls at once.
+ */
+hyq_status hyq_decode_attention(const hyq_config *cfg, const void *q, const hyq_layout *lay,
+                                void *out, int32_t len_hint, void *ws, size_t ws_bytes,
+                                hyq_stream_t stream);
+
+/*
+ * Copy a device error word to the host (synchronises `stream`).
+ *   err_dev  device int32 [1];  err_host  host int32 [1]
+ * Returns HYQ_ERR_DEVICE when the word is non-zero, HYQ_OK otherwise.
+ */
+hyq_status hyq_read_device_error(const int32_t *err_dev, int32_t *err_host, hyq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HYQ_H */

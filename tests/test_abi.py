@@ -1,0 +1,158 @@
+"""The C ABI without a GPU: the library loads, exports every symbol the header
+declares, sizes buffers, and rejects invalid calls on the host before any
+launch.  Also the block-format reader/writer used by the tests."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import hybrid_precision_quantized_gb300 as hyq
+from hybrid_precision_quantized_gb300 import _lib as L
+from oracle.select import vl_count
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "hyq.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(L.lib_path()):
+        import __graft_entry__
+        __graft_entry__.build()
+    return hyq.load()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(hyq_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_what_the_binding_binds():
+    assert declared_symbols() == sorted(L.SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def cfg(**kw):
+    base = dict(batch=1, num_q_heads=32, num_kv_heads=8, capacity=32768)
+    base.update(kw)
+    return hyq.make_config(**base)
+
+
+def test_config_checks(lib):
+    assert hyq.hyq_config_check(cfg()) == 0
+    assert hyq.hyq_config_check(cfg(head_dim=64)) == 2          # unsupported
+    assert hyq.hyq_config_check(cfg(group=64)) == 2
+    assert hyq.hyq_config_check(cfg(num_q_heads=72)) == 2       # g = 9 > 8
+    assert hyq.hyq_config_check(cfg(num_q_heads=30)) == 1       # not a multiple
+    assert hyq.hyq_config_check(cfg(rho_ppm=-1)) == 1
+    assert hyq.hyq_config_check(cfg(rho_ppm=1_000_001)) == 1
+    assert hyq.hyq_config_check(cfg(window=-1)) == 1
+    assert hyq.hyq_config_check(cfg(capacity=0)) == 1
+    assert lib.hyq_config_check(None) == 1
+
+
+@pytest.mark.parametrize("ppm", [0, 20_000, 50_000, 100_000, 1_000_000, 333_333])
+def test_vl_count_matches_oracle(lib, ppm):
+    c = cfg(rho_ppm=ppm)
+    for P in [0, 1, 19, 20, 21, 896, 4000, 32640, 131072]:
+        assert hyq.hyq_vl_count(c, P) == vl_count(P, ppm)
+
+
+def test_layout_sizes(lib):
+    c = cfg()
+    s = hyq.hyq_layout_sizes(c)
+    assert len(s) == len(L.LAYOUT_FIELDS)
+    assert s[0] == 8 * 512 * 10240                    # 32768 rows = 512 blocks per head
+    assert s[1] == s[2] == -(-8 * 1632 * 256 // 256) * 256
+    assert s[4] == 8 * (128 + 64) * 256
+    assert s[6] == 32 * 64 * 256                      # proxy ring: 64 x HQ x d x 2 bytes (§5.5)
+    assert all(x % 256 == 0 for x in s)
+
+
+def test_workspace_sizes(lib):
+    c = cfg()
+    assert hyq.hyq_workspace_size(c, L.OP_DECODE, 32768) > 0
+    assert hyq.hyq_workspace_size(c, L.OP_SELECT, 32768) >= 8 * 32640 * 4
+    assert hyq.hyq_workspace_size(c, 99, 0) == 0
+    assert hyq.hyq_workspace_size(cfg(head_dim=64), L.OP_DECODE, 0) == 0
+
+
+def _null_layout():
+    return L.HyqLayout()
+
+
+def _no_gpu():
+    import torch
+    return not torch.cuda.is_available()
+
+
+# Fake device addresses are only ever passed where no GPU exists, so that a
+# validation gap could never turn into a launch that touches them.
+@pytest.mark.skipif(not _no_gpu(), reason="fake-pointer validation runs only without a GPU")
+def test_host_validation_rejects_before_launch(lib):
+    c = cfg()
+    lay = _null_layout()
+    P = ctypes.POINTER
+    # null layout pointers
+    assert lib.hyq_decode_attention(ctypes.byref(c), 256, ctypes.byref(lay), 256, 0, 256, 1 << 30, None) == 1
+    assert lib.hyq_rebuild(ctypes.byref(c), 256, 256, 100, 100, None, 0, ctypes.byref(lay), None) == 1
+    assert lib.hyq_layout_reset(ctypes.byref(c), ctypes.byref(lay), None) == 1
+    # a fake but aligned layout: argument checks that come after the layout check
+    fake = L.HyqLayout(**{n: 4096 * (i + 1) for i, n in enumerate(L.LAYOUT_FIELDS)})
+    assert lib.hyq_decode_attention(ctypes.byref(c), 256, ctypes.byref(fake), 256, 0, None, 0, None) == 3
+    assert lib.hyq_decode_attention(ctypes.byref(c), 256, ctypes.byref(fake), 256, 0, 256, 16, None) == 3
+    assert lib.hyq_decode_attention(ctypes.byref(c), 3, ctypes.byref(fake), 256, 0, 256, 1 << 30, None) == 1
+    assert lib.hyq_rebuild(ctypes.byref(c), 256, 256, 100, 40000, None, 0, ctypes.byref(fake), None) == 4
+    assert lib.hyq_rebuild(ctypes.byref(c), 256, 256, 99, 100, None, 0, ctypes.byref(fake), None) == 1
+    assert lib.hyq_rebuild(ctypes.byref(c), 256, 256, 1000, 1000, None, 5, ctypes.byref(fake), None) == 1
+    k_out = ctypes.c_int32(-1)
+    # L <= W: nothing to select, k = 0, no launch
+    assert lib.hyq_select_vertical(ctypes.byref(c), None, 0, 0, None, 100, 100, None,
+                                   ctypes.byref(k_out), None, 0, None) == 0 and k_out.value == 0
+    assert lib.hyq_select_vertical(ctypes.byref(c), 256, 64, 64, 256, 4096, 4096, 256,
+                                   ctypes.byref(k_out), None, 0, None) == 3
+    assert k_out.value == vl_count(4096 - 128, 50_000)
+    assert lib.hyq_quantize_append(ctypes.byref(c), 256, 256, -1, ctypes.byref(fake), None) == 1
+    assert lib.hyq_quantize_append(ctypes.byref(c), 256, 256, 0, ctypes.byref(fake), None) == 0
+    assert lib.hyq_decode_append(ctypes.byref(c), 256, 256, 256, ctypes.byref(fake), 256, None, 10, None) == 1
+    assert lib.hyq_read_device_error(None, None, None) == 1
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert hyq.hyq_status_string(s)
+
+
+def test_block_format_round_trip():
+    rng = np.random.default_rng(0)
+    n = 150
+    kc = rng.integers(0, 16, (n, 128), dtype=np.uint8)
+    vc = rng.integers(0, 16, (n, 128), dtype=np.uint8)
+    ks, kz, vs, vz = (rng.standard_normal((n, 4)).astype(np.float16) for _ in range(4))
+    blocks = hyq.pack_qblocks(kc, vc, ks, kz, vs, vz)
+    assert blocks.shape == (3, 10240)
+    out = hyq.unpack_qblocks(blocks, n)
+    for a, b in zip(out, (kc, vc, ks, kz, vs, vz)):
+        assert np.array_equal(a, b)
+    # every nibble slot of a tile is used exactly once by each fragment order
+    from hybrid_precision_quantized_gb300.cache import _tile_maps
+    krow, kel, vrow, vel = _tile_maps()
+    assert len(set(zip(krow.tolist(), kel.tolist()))) == 2048
+    assert len(set(zip(vrow.tolist(), vel.tolist()))) == 2048
+
+
+def test_block_format_fragment_order_examples():
+    """Spot values of the documented tile order: the first word of lane 0
+    holds K rows 0/8 elements 0,1,8,9 and V rows 0,1,8,9 of element 0/8."""
+    from hybrid_precision_quantized_gb300.cache import _tile_maps
+    krow, kel, vrow, vel = _tile_maps()
+    # nibble n of the word at byte 0: slot = 2*(n//2) + n%2 = n
+    assert [(krow[n], kel[n]) for n in range(8)] == [(0, 0), (8, 0), (0, 8), (8, 8), (0, 1), (8, 1), (0, 9), (8, 9)]
+    assert [(vrow[n], vel[n]) for n in range(8)] == [(0, 0), (0, 8), (8, 0), (8, 8), (1, 0), (1, 8), (9, 0), (9, 8)]

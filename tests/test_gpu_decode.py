@@ -1,0 +1,162 @@
+"""GPU parity of hybrid decode attention (Eq. 8-9, Algorithm 3) against the
+oracle's plain float64 softmax over the effective cache.
+
+The partition (vertical-line set) fed to the GPU is always the oracle's own
+selection, so the attention comparison does not depend on selection parity.
+Tolerance: |gpu - oracle| <= 2e-3 + 1e-2 |oracle| elementwise.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gen import decode_case, gen_for
+from hybrid_precision_quantized_gb300 import (HybridDecoder, HybridLayer, hyq_decode_append,
+                                              hyq_decode_attention, hyq_read_device_error,
+                                              hyq_rebuild, make_config, workspace)
+from hybrid_precision_quantized_gb300 import _lib as L
+from oracle.attention import hybrid_decode
+from oracle.select import check_selection, prefix_len, score_error_bound, select_vertical
+from tests.gpu_util import assert_attention_close, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def build_and_decode(c, Lc, W, ppm, capacity=None, len_hint=0, period=64):
+    B, HQ = c.q.shape[:2]
+    HKV = c.k.shape[1]
+    cfg = make_config(B, HQ, HKV, capacity=capacity or max(Lc, 1), window=W, rho_ppm=ppm, period=period)
+    layer = HybridLayer(cfg)
+    layer.reset()
+    qp = c.q_proxy.double().numpy()
+    k_np, v_np = c.k.double().numpy(), c.v.double().numpy()
+    idx_np, _ = select_vertical(qp, k_np, Lc, W, ppm)
+    k = idx_np.shape[-1]
+    idx = torch.from_numpy(idx_np).to(torch.int32).cuda().contiguous()
+    hyq_rebuild(cfg, c.k.cuda(), c.v.cuda(), Lc, idx, k, layer.c)
+    ws = workspace(cfg, L.OP_DECODE, len_hint)
+    out = torch.empty(B, HQ, 128, dtype=torch.bfloat16, device="cuda")
+    hyq_decode_attention(cfg, c.q.cuda(), layer.c, out, ws, len_hint)
+    torch.cuda.synchronize()
+    assert hyq_read_device_error(layer.err()) == 0
+    want = hybrid_decode(c.q.double().numpy(), k_np, v_np, Lc, prefix_len(Lc, W), idx_np)
+    return to_np(out), want, (cfg, layer, ws, out)
+
+
+@pytest.mark.parametrize("seed,B,HQ,HKV,Lc,W,ppm", [
+    (1000, 1, 4, 4, 1024, 128, 50_000),     # tiny decode workload
+    (1001, 1, 32, 8, 1024, 128, 50_000),    # Llama-3.1-8B-shaped, 1K
+    (1001, 1, 32, 8, 4096, 128, 50_000),    # 4K
+    (1003, 1, 64, 8, 2048, 128, 50_000),    # g = 8 (Qwen3-32B-shaped heads)
+    (5, 2, 8, 2, 777, 100, 50_000),         # two sequences, ragged 4-bit stream
+    (6, 1, 8, 8, 1111, 128, 20_000),        # MHA
+    (7, 1, 6, 2, 500, 128, 50_000),         # g = 3
+])
+def test_decode_parity(hyq, seed, B, HQ, HKV, Lc, W, ppm):
+    c = decode_case(seed, B, HQ, HKV, Lc, window=W, n_proxy=64, sink_frac=0.02, outlier_channels=3)
+    got, want, _ = build_and_decode(c, Lc, W, ppm)
+    assert_attention_close(got, want, what=f"L={Lc}")
+
+
+@pytest.mark.parametrize("Lc,W,ppm,what", [
+    (100, 128, 50_000, "context inside the window: no 4-bit rows"),
+    (1, 128, 50_000, "single position: output is its value"),
+    (600, 0, 0, "rho = 0, W = 0: pure 4-bit attention"),
+    (600, 64, 1_000_000, "rho = 100%: all BF16"),
+    (129, 128, 50_000, "P = 1"),
+    (192, 128, 0, "exactly one 4-bit block"),
+    (193, 128, 0, "one block plus one row"),
+    (1000, 990, 50_000, "tail nearly the whole context"),
+])
+def test_decode_edge_cases(hyq, Lc, W, ppm, what):
+    c = decode_case(31, 1, 8, 2, Lc, window=W, n_proxy=16, sink_frac=0.05)
+    got, want, _ = build_and_decode(c, Lc, W, ppm, capacity=Lc + 64, period=64 if W < 990 else 64)
+    assert_attention_close(got, want, what=what)
+    if Lc == 1:
+        np.testing.assert_array_equal(got[0, :4], c.v[0, 0, 0].double().numpy()[None].repeat(4, 0))
+
+
+def test_decode_split_count_does_not_change_result(hyq):
+    c = decode_case(41, 1, 32, 8, 3000, window=128, n_proxy=64, sink_frac=0.02)
+    a, want, _ = build_and_decode(c, 3000, 128, 50_000, capacity=3000, len_hint=0)
+    b, _, _ = build_and_decode(c, 3000, 128, 50_000, capacity=3000, len_hint=200)
+    assert_attention_close(a, want)
+    assert_attention_close(b, want)
+
+
+def test_decode_repeated_calls_reuse_workspace(hyq):
+    c = decode_case(42, 1, 8, 2, 900, window=128, n_proxy=16, sink_frac=0.02)
+    got, want, (cfg, layer, ws, out) = build_and_decode(c, 900, 128, 50_000)
+    for _ in range(3):
+        hyq_decode_attention(cfg, c.q.cuda(), layer.c, out, ws)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(to_np(out), got)   # deterministic, tickets reset
+
+
+def test_decode_full_size_llama_32k(hyq):
+    """Llama-3.1-8B-shaped layer at 32K context: every head against the oracle."""
+    c = decode_case(1001, 1, 32, 8, 32768, window=128, n_proxy=64, sink_frac=0.02, outlier_channels=3)
+    got, want, (cfg, layer, _, _) = build_and_decode(c, 32768, 128, 50_000, capacity=32768 + 64)
+    cnt = layer.counts()[0].tolist()
+    assert cnt[:4] == [32640 - 1632, 1632, 128, 32768]
+    assert_attention_close(got, want, what="32K")
+
+
+def test_decode_pipeline_with_reselection(hyq):
+    """Freeze, then 70 decode steps through HybridDecoder (append, proxy ring,
+    re-selection at step 64, fused attention) against the oracle step by step."""
+    B, HQ, HKV, W = 1, 8, 2, 128
+    L0, steps = 700, 70
+    cap = L0 + steps
+    c = decode_case(51, B, HQ, HKV, cap, window=W, n_proxy=64, sink_frac=0.03)
+    g = gen_for(51, "steps")
+    qs = (torch.randn(steps, B, HQ, 128, generator=g) + 2.0 * c.u.repeat_interleave(HQ // HKV, 1)[None]).to(torch.bfloat16)
+    k_all, v_all = c.k.clone(), c.v.clone()
+    cfg = make_config(B, HQ, HKV, capacity=cap, window=W)
+    k_src = torch.zeros(B, HKV, cap, 128, dtype=torch.bfloat16, device="cuda")
+    v_src = torch.zeros_like(k_src)
+    k_src[:, :, :L0] = k_all[:, :, :L0].cuda()
+    v_src[:, :, :L0] = v_all[:, :, :L0].cuda()
+    dec = HybridDecoder(cfg, k_src, v_src)
+    q_tail = c.q_proxy.cuda()
+    dec.freeze(L0, q_tail)
+    k_np, v_np = k_all.double().numpy(), v_all.double().numpy()
+    idx, _ = select_vertical(c.q_proxy.double().numpy(), k_np[:, :, :L0], L0, W, 50_000)
+    P = L0 - W
+    out = torch.empty(B, HQ, 128, dtype=torch.bfloat16, device="cuda")
+    for s in range(steps):
+        Lc = L0 + s + 1
+        dec.step(qs[s].cuda(), k_all[:, :, Lc - 1].cuda().contiguous(), v_all[:, :, Lc - 1].cuda().contiguous(), out)
+        if (s + 1) % 64 == 0:     # the decoder re-selected from the last 64 queries
+            ring = qs[s - 63:s + 1].permute(1, 2, 0, 3).double().numpy()
+            idx, S = select_vertical(ring, k_np[:, :, :Lc], Lc, W, 50_000)
+            P = Lc - W
+            got_idx = dec.layer.vl_idx()[:, :, :idx.shape[-1]].cpu().numpy()
+            bnd = score_error_bound(ring, k_np[:, :, :Lc], P)
+            for h in range(HKV):
+                r = check_selection(S[0, h], bnd[0, h], idx.shape[-1], got_idx[0, h])
+                assert r["ok"], r["reason"]
+                if r["ambiguous"] == 0:
+                    assert np.array_equal(got_idx[0, h], idx[0, h])
+        if s in (0, 1, 62, 63, 64, 69):
+            torch.cuda.synchronize()
+            want = hybrid_decode(qs[s].double().numpy(), k_np, v_np, Lc, P, idx)
+            assert_attention_close(to_np(out), want, what=f"step {s}")
+    assert hyq_read_device_error(dec.layer.err()) == 0
+    cnt = dec.layer.counts()[0].tolist()
+    assert cnt[L.CNT_LEN] == L0 + steps and cnt[L.CNT_NTAIL] == W + steps - 64
+
+
+def test_decode_append_full_tail_is_flagged(hyq):
+    cfg = make_config(1, 2, 1, capacity=400, window=4, period=2)
+    c = decode_case(61, 1, 2, 1, 10, window=4, n_proxy=2)
+    layer = HybridLayer(cfg)
+    layer.reset()
+    idx = torch.zeros(1, 1, 1, dtype=torch.int32, device="cuda")
+    hyq_rebuild(cfg, c.k.cuda(), c.v.cuda(), 10, idx, 0, layer.c)      # tail = 4 rows, capacity 6
+    q = c.q.cuda()
+    kn = c.k[:, :, 0].cuda().contiguous()
+    for _ in range(3):
+        hyq_decode_append(cfg, q, kn, kn, layer.c)
+    torch.cuda.synchronize()
+    assert layer.counts()[0, L.CNT_NTAIL].item() == 6
+    assert hyq_read_device_error(layer.err()) & L.DEVERR_COUNT

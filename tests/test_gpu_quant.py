@@ -1,0 +1,125 @@
+"""GPU parity of the 4-bit quantiser and the cache rebuild: codes, FP16 scales
+and zeros bit-exact with the oracle; vertical-line rows, tail rows and
+counters exact."""
+import numpy as np
+import pytest
+import torch
+
+from gen import decode_case
+from hybrid_precision_quantized_gb300 import (HybridLayer, hyq_quantize_append, hyq_read_device_error,
+                                              hyq_rebuild, make_config, unpack_qblocks)
+from hybrid_precision_quantized_gb300 import _lib as L
+from oracle.quant import quantize
+from oracle.select import prefix_len, select_vertical, vl_count
+from tests.gpu_util import mixed_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_stream(layer, b, h, n_rows, k_rows, v_rows):
+    blocks = layer.qblocks()[b, h].cpu().numpy()
+    kc, vc, ks, kz, vs, vz = unpack_qblocks(blocks, n_rows)
+    for got_c, got_s, got_z, rows in ((kc, ks, kz, k_rows), (vc, vs, vz, v_rows)):
+        c, s, z = quantize(rows)
+        assert np.array_equal(got_c, c), f"codes differ at {np.argwhere(got_c != c)[:5].tolist()}"
+        assert np.array_equal(got_s.view(np.uint16), s.view(np.uint16)), "scales differ"
+        assert np.array_equal(got_z.view(np.uint16), z.view(np.uint16)), "zeros differ"
+    # rows past the stream end inside the last block are zero
+    if n_rows % 64:
+        kc_all, vc_all, ks_all, *_ = unpack_qblocks(blocks, blocks.shape[0] * 64)
+        assert not kc_all[n_rows:(n_rows + 63) // 64 * 64].any()
+
+
+def test_quantize_append_bit_exact_two_appends(hyq):
+    B, HQ, HKV = 2, 4, 2
+    cfg = make_config(B, HQ, HKV, capacity=512, window=0)
+    layer = HybridLayer(cfg)
+    layer.reset()
+    k1, v1 = mixed_rows(1, (B, HKV, 150, 128)), mixed_rows(2, (B, HKV, 150, 128))
+    k2, v2 = mixed_rows(3, (B, HKV, 37, 128)), mixed_rows(4, (B, HKV, 37, 128))
+    hyq_quantize_append(cfg, k1.cuda(), v1.cuda(), 150, layer.c)
+    hyq_quantize_append(cfg, k2.cuda(), v2.cuda(), 37, layer.c)   # starts inside a block
+    torch.cuda.synchronize()
+    cnt = layer.counts().cpu().numpy()
+    assert cnt[:, L.CNT_NQ].tolist() == [187, 187] and cnt[:, L.CNT_LEN].tolist() == [187, 187]
+    assert hyq_read_device_error(layer.err()) == 0
+    for b in range(B):
+        for h in range(HKV):
+            kr = torch.cat([k1[b, h], k2[b, h]]).double().numpy()
+            vr = torch.cat([v1[b, h], v2[b, h]]).double().numpy()
+            _check_stream(layer, b, h, 187, kr, vr)
+
+
+def test_quantize_range_error_sets_device_word(hyq):
+    cfg = make_config(1, 1, 1, capacity=128, window=0)
+    layer = HybridLayer(cfg)
+    layer.reset()
+    k = mixed_rows(5, (1, 1, 4, 128))
+    k[0, 0, 2, 40] = -70000.0           # group 1 of row 2: zero point overflows FP16
+    v = mixed_rows(6, (1, 1, 4, 128))
+    hyq_quantize_append(cfg, k.cuda(), v.cuda(), 4, layer.c)
+    torch.cuda.synchronize()
+    assert hyq_read_device_error(layer.err()) & L.DEVERR_QUANT_RANGE
+    kc, vc, ks, kz, vs, vz = unpack_qblocks(layer.qblocks()[0, 0].cpu().numpy(), 4)
+    assert not kc[2, 32:64].any() and ks[2, 1] == 0 and kz[2, 1] == 0
+    c, s, z = quantize(k[0, 0, [0, 1, 3]].double().numpy())
+    assert np.array_equal(kc[[0, 1, 3]], c)
+
+
+def test_append_past_capacity_is_dropped_and_flagged(hyq):
+    cfg = make_config(1, 1, 1, capacity=64, window=0)
+    layer = HybridLayer(cfg)
+    layer.reset()
+    k = mixed_rows(7, (1, 1, 60, 128))
+    hyq_quantize_append(cfg, k.cuda(), k.cuda(), 60, layer.c)
+    hyq_quantize_append(cfg, k.cuda(), k.cuda(), 10, layer.c)   # only 4 rows fit
+    torch.cuda.synchronize()
+    assert layer.counts()[0, L.CNT_NQ].item() == 64
+    assert hyq_read_device_error(layer.err()) & L.DEVERR_COUNT
+
+
+@pytest.mark.parametrize("B,HQ,HKV,Lc,W,ppm", [
+    (1, 4, 4, 1024, 128, 50_000),     # tiny decode workload
+    (2, 8, 2, 777, 100, 50_000),      # ragged stream, two sequences
+    (1, 4, 1, 300, 128, 0),           # no vertical lines
+    (1, 4, 1, 300, 64, 1_000_000),    # everything in the prefix is vertical-line
+    (1, 4, 2, 100, 128, 50_000),      # context inside the window: empty stream
+])
+def test_rebuild_matches_partition(hyq, B, HQ, HKV, Lc, W, ppm):
+    c = decode_case(11, B, HQ, HKV, Lc, window=W, n_proxy=16, sink_frac=0.03)
+    cfg = make_config(B, HQ, HKV, capacity=Lc + 64, window=W, rho_ppm=ppm)
+    layer = HybridLayer(cfg)
+    layer.reset()
+    kq, vq = c.k.cuda(), c.v.cuda()
+    idx_np, _ = select_vertical(c.q_proxy.double().numpy(), c.k.double().numpy(), Lc, W, ppm)
+    k = idx_np.shape[-1]
+    P = prefix_len(Lc, W)
+    assert k == vl_count(P, ppm)
+    idx = torch.from_numpy(idx_np).to(torch.int32).cuda().contiguous()
+    hyq_rebuild(cfg, kq, vq, Lc, idx, k, layer.c)
+    torch.cuda.synchronize()
+    assert hyq_read_device_error(layer.err()) == 0
+    cnt = layer.counts().cpu().numpy()
+    assert cnt[:, :4].tolist() == [[P - k, k, Lc - P, Lc]] * B
+    for b in range(B):
+        for h in range(HKV):
+            qpos = np.setdiff1d(np.arange(P), idx_np[b, h])
+            if len(qpos):
+                _check_stream(layer, b, h, len(qpos), c.k[b, h, qpos].double().numpy(),
+                              c.v[b, h, qpos].double().numpy())
+            assert torch.equal(layer.vl_k()[b, h, :k].cpu(), c.k[b, h, idx_np[b, h]])
+            assert torch.equal(layer.vl_v()[b, h, :k].cpu(), c.v[b, h, idx_np[b, h]])
+            assert np.array_equal(layer.vl_idx()[b, h, :k].cpu().numpy(), idx_np[b, h])
+            assert torch.equal(layer.tail_k()[b, h, :Lc - P].cpu(), c.k[b, h, P:Lc])
+            assert torch.equal(layer.tail_v()[b, h, :Lc - P].cpu(), c.v[b, h, P:Lc])
+
+
+def test_rebuild_flags_unsorted_index_list(hyq):
+    c = decode_case(12, 1, 2, 1, 400, window=128, n_proxy=4)
+    cfg = make_config(1, 2, 1, capacity=512)
+    layer = HybridLayer(cfg)
+    layer.reset()
+    idx = torch.tensor([[[5, 3, 9]]], dtype=torch.int32).cuda()
+    hyq_rebuild(cfg, c.k.cuda(), c.v.cuda(), 400, idx, 3, layer.c)
+    torch.cuda.synchronize()
+    assert hyq_read_device_error(layer.err()) & L.DEVERR_INDEX
