@@ -36,7 +36,8 @@ OP_SELECT, OP_DECODE, OP_PREFILL = 1, 2, 3
 SYMBOLS = ("hyq_status_string", "hyq_config_check", "hyq_vl_count", "hyq_layout_sizes",
            "hyq_workspace_size", "hyq_layout_reset", "hyq_quantize_append",
            "hyq_select_vertical", "hyq_rebuild", "hyq_decode_append", "hyq_decode_attention",
-           "hyq_read_device_error")
+           "hyq_decode_attention_noalloc", "hyq_read_device_error")
+NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
 class HyqConfig(ctypes.Structure):
@@ -88,6 +89,8 @@ def load() -> ctypes.CDLL:
                                         c_void_p, c_void_p, c_int32, c_void_p]),
         "hyq_decode_attention": (c_int32, [P(HyqConfig), c_void_p, P(HyqLayout), c_void_p, c_int32,
                                            c_void_p, c_size_t, c_void_p]),
+        "hyq_decode_attention_noalloc": (c_int32, [P(HyqConfig), c_void_p, P(HyqLayout), c_void_p, c_int32,
+                                                   c_void_p]),
         "hyq_read_device_error": (c_int32, [c_void_p, P(c_int32), c_void_p]),
     }
     for name in SYMBOLS:
@@ -186,6 +189,14 @@ def hyq_decode_attention(cfg, q, lay: HyqLayout, out, ws, len_hint: int = 0, str
     _check("hyq_decode_attention", load().hyq_decode_attention(
         ctypes.byref(cfg), ptr(q), ctypes.byref(lay), ptr(out), len_hint, ptr(ws),
         ws.numel() * ws.element_size(), stream_ptr(stream)))
+
+
+def hyq_decode_attention_noalloc(cfg, q, lay: HyqLayout, out, len_hint: int = 0, stream=None):
+    """Decode attention with the library's own fixed scratch (no workspace):
+    for callers that cannot allocate device memory.  Calls that overlap on the
+    GPU race on the shared scratch."""
+    _check("hyq_decode_attention_noalloc", load().hyq_decode_attention_noalloc(
+        ctypes.byref(cfg), ptr(q), ctypes.byref(lay), ptr(out), len_hint, stream_ptr(stream)))
 
 
 def hyq_read_device_error(err_dev, stream=None) -> int:

@@ -537,3 +537,52 @@ cudaError_t hyq_launch_decode_append(const hyq_config* c, const void* q, const v
       static_cast<__nv_bfloat16*>(v_src), ld, c->num_q_heads, c->num_kv_heads, c->period, hyq_cap_tail(c));
   return cudaGetLastError();
 }
+
+// ---------------------------------------------------------------------------
+// Decode attention for callers that cannot allocate device memory: the split
+// partials and tickets live in this library-owned array instead of a
+// caller-provided workspace.  Host code never dereferences the symbol; it
+// looks up the array's device address once per device and passes that.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+static __device__ __align__(256) unsigned char g_hyq_noalloc_scratch[HYQ_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_addr[kMaxDevices] = {};
+
+bool ptr_ok(const void* p, size_t a) { return p && (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+}  // namespace
+
+extern "C" hyq_status hyq_decode_attention_noalloc(const hyq_config* c, const void* q,
+                                                   const hyq_layout* l, void* out, int32_t len_hint,
+                                                   hyq_stream_t s) {
+  hyq_status st = hyq_config_check(c);
+  if (st != HYQ_OK) return st;
+  if (!l || !ptr_ok(q, 16) || !ptr_ok(out, 16) || len_hint < 0) return HYQ_ERR_INVALID_ARG;
+  const void* ps[] = {l->qblocks, l->vl_k, l->vl_v, l->vl_idx, l->tail_k, l->tail_v, l->q_ring,
+                      l->counts, l->err};
+  for (const void* p : ps)
+    if (!ptr_ok(p, 256)) return HYQ_ERR_INVALID_ARG;
+  if (len_hint == 0 || len_hint > c->capacity) len_hint = c->capacity;
+  if (hyq_decode_ws_bytes(c, len_hint) > HYQ_NOALLOC_SCRATCH_BYTES) return HYQ_ERR_WORKSPACE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return HYQ_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return HYQ_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_addr[dev]) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_hyq_noalloc_scratch) != cudaSuccess || !p) return HYQ_ERR_CUDA;
+      g_noalloc_addr[dev] = p;
+    }
+    scratch = g_noalloc_addr[dev];
+  }
+  // The tickets at the front of the scratch must start at zero.
+  const size_t tickets = (size_t)c->batch * c->num_kv_heads * sizeof(int32_t);
+  if (cudaMemsetAsync(scratch, 0, tickets, s) != cudaSuccess) return HYQ_ERR_CUDA;
+  return hyq_launch_decode(c, q, l, out, len_hint, scratch, s) == cudaSuccess ? HYQ_OK : HYQ_ERR_CUDA;
+}

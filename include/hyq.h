@@ -248,6 +248,32 @@ hyq_status hyq_decode_attention(const hyq_config *cfg, const void *q, const hyq_
                                 hyq_stream_t stream);
 
 /*
+ * hyq_decode_attention without a caller-provided workspace.  The paper has
+ * no counterpart; this exists for callers that cannot allocate device
+ * memory: plugins and embedding runtimes that hand an attention op only its
+ * inputs and outputs (no workspace argument, no allocator) and hot loops that
+ * must not call cudaMalloc, which synchronises the device and can fail under
+ * memory pressure.
+ *
+ * Same arguments, result and layout as hyq_decode_attention, minus `ws`.
+ * The split partials and tickets live in a fixed library-owned device array
+ * of HYQ_NOALLOC_SCRATCH_BYTES (4 MiB), present on every GPU that loads the
+ * library until the process exits.  The call allocates nothing.
+ *  - The first call on a device looks up that array's device address (with
+ *    that device current) and caches it; make that first call before any
+ *    stream capture.
+ *  - A shape whose scratch need, hyq_workspace_size(cfg, HYQ_OP_DECODE,
+ *    len_hint), exceeds HYQ_NOALLOC_SCRATCH_BYTES is rejected with
+ *    HYQ_ERR_WORKSPACE before anything is launched.
+ *  - Every call on a device shares the one array and each call re-zeroes the
+ *    part that must start at zero; two calls that overlap on the GPU (other
+ *    streams, other threads) race on it and give wrong results.
+ */
+#define HYQ_NOALLOC_SCRATCH_BYTES (4u << 20)
+hyq_status hyq_decode_attention_noalloc(const hyq_config *cfg, const void *q, const hyq_layout *lay,
+                                        void *out, int32_t len_hint, hyq_stream_t stream);
+
+/*
  * Copy a device error word to the host (synchronises `stream`).
  *   err_dev  device int32 [1];  err_host  host int32 [1]
  * Returns HYQ_ERR_DEVICE when the word is non-zero, HYQ_OK otherwise.
