@@ -48,7 +48,39 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--layers", type=int, default=N_LAYERS)
     p.add_argument("--no-baseline", action="store_true", help="skip the CPU oracle timing")
+    p.add_argument("--case", default="period", choices=["period", "decode-layer"],
+                   help="decode-layer: one 32K layer, a few decode launches (a small profiling target)")
     return p.parse_args()
+
+
+def run_decode_layer_case(args, local):
+    """One Llama-shaped 32K layer (freeze, then 6 decode-attention launches);
+    prints the mean launch time.  Used as a small, self-contained ncu target."""
+    import torch
+    import hybrid_precision_quantized_gb300 as hyq
+    from hybrid_precision_quantized_gb300 import _lib as L
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    hyq.load()
+    cfg = hyq.make_config(B, HQ, HKV, capacity=CTX, window=WINDOW, period=PERIOD, rho_ppm=RHO_PPM)
+    k_srcs, v_srcs, q_tail, q_tok, _, _ = make_inputs(dev, 1)
+    layer = hyq.HybridLayer(cfg, dev)
+    layer.reset()
+    idx = torch.zeros(B, HKV, 1632, dtype=torch.int32, device=dev)
+    k = hyq.hyq_select_vertical(cfg, q_tail[0], 64, k_srcs[0], CTX, idx, hyq.workspace(cfg, L.OP_SELECT, CTX, dev))
+    hyq.hyq_rebuild(cfg, k_srcs[0], v_srcs[0], CTX, idx, k, layer.c)
+    ws = hyq.workspace(cfg, L.OP_DECODE, CTX, dev)
+    out = torch.empty(B, HQ, D, dtype=torch.bfloat16, device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(6):
+        if i == 2:
+            e0.record()
+        hyq.hyq_decode_attention(cfg, q_tok[0, 0], layer.c, out, ws, CTX)
+    e1.record()
+    torch.cuda.synchronize()
+    print(json.dumps({"case": "decode-layer", "us_per_launch_l2_warm": e0.elapsed_time(e1) * 1e3 / 4,
+                      "device_error_word": hyq.hyq_read_device_error(layer.err())}))
 
 
 def dist_setup(args):
@@ -360,7 +392,9 @@ def run_ours(args, rank, world, local):
 def main():
     args = parse()
     rank, world, local = dist_setup(args)
-    if args.impl == "reference":
+    if args.case == "decode-layer":
+        run_decode_layer_case(args, local)
+    elif args.impl == "reference":
         run_reference(args, rank, world)
     else:
         run_ours(args, rank, world, local)

@@ -89,87 +89,91 @@ def workspace(cfg: HyqConfig, op: int, len_hint: int = 0, device="cuda") -> torc
     return torch.zeros(n, dtype=torch.uint8, device=device)
 
 
-# --- block-format reader (documented layout of include/hyq.h) --------------
+# --- 4-bit stream reader/writer (documented format of include/hyq.h) -------
+
+TILE_BYTES = 2560
+
 
 def _tile_maps():
-    """For each of the 1024*2 nibbles of a code tile: (row, element) for the K
-    and the V fragment orders, indexed [byte_offset * 2 + (0 low | 1 high)]."""
+    """(row, element) of every nibble of a 1024-byte code region, for the K and
+    the V fragment orders, indexed [byte_offset * 2 + (0 low | 1 high nibble)]."""
     krow = np.zeros(2048, np.int64)
     kel = np.zeros(2048, np.int64)
     vrow = np.zeros(2048, np.int64)
     vel = np.zeros(2048, np.int64)
     for u in range(8):
         for lane in range(32):
+            g, t = lane // 4, lane % 4
             base = 512 * (u // 4) + 16 * lane + 4 * (u % 4)
             for n in range(8):
-                byte = base + n // 2
-                slot = 2 * byte + (n % 2)
-                krow[slot] = (8 if n & 1 else 0) + lane // 4
-                kel[slot] = 16 * u + 2 * (lane % 4) + (8 if n & 2 else 0) + (n >> 2)
-                vrow[slot] = 2 * (lane % 4) + (8 if n & 2 else 0) + (n >> 2)
-                vel[slot] = 16 * u + lane // 4 + (8 if n & 1 else 0)
+                a, b, c = n & 1, (n >> 1) & 1, n >> 2
+                slot = 2 * (base + n // 2) + (n % 2)
+                krow[slot] = g + 8 * a
+                kel[slot] = 8 * (t + 4 * (u // 2)) + 4 * (u % 2) + 2 * b + c
+                vrow[slot] = 2 * t + 8 * b + c
+                vel[slot] = 32 * (u // 2) + 4 * g + 2 * (u % 2) + a
     return krow, kel, vrow, vel
 
 
 _MAPS = None
 
 
-def unpack_qblocks(blocks: np.ndarray, n_rows: int):
-    """Decode the first ``n_rows`` rows of a 4-bit stream.
-
-    blocks : uint8 [nblk, 10240] (one (batch, KV head) stream)
-    Returns k_codes, v_codes uint8 [n_rows, 128]; k_scale, k_zero, v_scale,
-    v_zero float16 [n_rows, 4].
-    """
+def _maps():
     global _MAPS
     if _MAPS is None:
         _MAPS = _tile_maps()
-    krow, kel, vrow, vel = _MAPS
-    blocks = np.asarray(blocks, dtype=np.uint8)
-    nblk = blocks.shape[0]
-    kc = np.zeros((nblk * 64, 128), np.uint8)
-    vc = np.zeros((nblk * 64, 128), np.uint8)
-    for bi in range(nblk):
-        blk = blocks[bi]
-        for tile in range(4):
-            for which, codes, rmap, emap in ((0, kc, krow, kel), (1, vc, vrow, vel)):
-                raw = blk[which * 4096 + tile * 1024: which * 4096 + (tile + 1) * 1024]
-                nib = np.stack([raw & 15, raw >> 4], axis=1).reshape(-1)
-                codes[bi * 64 + tile * 16 + rmap, emap] = nib
-    meta_k = blocks[:, 8192:9216].copy().view(np.float16).reshape(nblk * 64, 4, 2)
-    meta_v = blocks[:, 9216:10240].copy().view(np.float16).reshape(nblk * 64, 4, 2)
+    return _MAPS
+
+
+def unpack_qblocks(blocks: np.ndarray, n_rows: int):
+    """Decode the first ``n_rows`` rows of a 4-bit stream.
+
+    blocks : uint8 [nblk, 10240] or [ntiles * 2560] (one (batch, KV head) stream)
+    Returns k_codes, v_codes uint8 [n_rows, 128]; k_scale, k_zero, v_scale,
+    v_zero float16 [n_rows, 4].
+    """
+    krow, kel, vrow, vel = _maps()
+    tiles = np.asarray(blocks, dtype=np.uint8).reshape(-1, TILE_BYTES)
+    nt = tiles.shape[0]
+    kc = np.zeros((nt * 16, 128), np.uint8)
+    vc = np.zeros((nt * 16, 128), np.uint8)
+    for ti in range(nt):
+        for off, codes, rmap, emap in ((0, kc, krow, kel), (1024, vc, vrow, vel)):
+            raw = tiles[ti, off:off + 1024]
+            nib = np.stack([raw & 15, raw >> 4], axis=1).reshape(-1)
+            codes[ti * 16 + rmap, emap] = nib
+    meta_k = tiles[:, 2048:2304].copy().view(np.float16).reshape(nt * 16, 4, 2)
+    meta_v = tiles[:, 2304:2560].copy().view(np.float16).reshape(nt * 16, 4, 2)
     n = n_rows
     return (kc[:n], vc[:n], meta_k[:n, :, 0], meta_k[:n, :, 1], meta_v[:n, :, 0], meta_v[:n, :, 1])
 
 
 def pack_qblocks(k_codes, v_codes, k_scale, k_zero, v_scale, v_zero) -> np.ndarray:
-    """Inverse of ``unpack_qblocks`` (rows padded with zeros to whole blocks)."""
-    global _MAPS
-    if _MAPS is None:
-        _MAPS = _tile_maps()
-    krow, kel, vrow, vel = _MAPS
+    """Inverse of ``unpack_qblocks``: rows padded with zeros to whole 64-row
+    blocks; returns uint8 [nblk, 10240]."""
+    krow, kel, vrow, vel = _maps()
     n = k_codes.shape[0]
     nblk = -(-n // 64)
-    out = np.zeros((nblk, 10240), np.uint8)
+    nt = 4 * nblk
+    tiles = np.zeros((nt, TILE_BYTES), np.uint8)
 
     def pad(a, shape, dtype):
         z = np.zeros(shape, dtype)
         z[: a.shape[0]] = a
         return z
 
-    kc = pad(np.asarray(k_codes), (nblk * 64, 128), np.uint8)
-    vc = pad(np.asarray(v_codes), (nblk * 64, 128), np.uint8)
-    for bi in range(nblk):
-        for tile in range(4):
-            for which, codes, rmap, emap in ((0, kc, krow, kel), (1, vc, vrow, vel)):
-                nib = codes[bi * 64 + tile * 16 + rmap, emap].reshape(1024, 2)
-                out[bi, which * 4096 + tile * 1024: which * 4096 + (tile + 1) * 1024] = nib[:, 0] | (nib[:, 1] << 4)
-    for off, s, z in ((8192, k_scale, k_zero), (9216, v_scale, v_zero)):
-        m = np.zeros((nblk * 64, 4, 2), np.float16)
-        m[:n, :, 0] = s
-        m[:n, :, 1] = z
-        out[:, off:off + 1024] = m.view(np.uint8).reshape(nblk, 1024)
-    return out
+    kc = pad(np.asarray(k_codes), (nt * 16, 128), np.uint8)
+    vc = pad(np.asarray(v_codes), (nt * 16, 128), np.uint8)
+    for ti in range(nt):
+        for off, codes, rmap, emap in ((0, kc, krow, kel), (1024, vc, vrow, vel)):
+            nib = codes[ti * 16 + rmap, emap].reshape(1024, 2)
+            tiles[ti, off:off + 1024] = nib[:, 0] | (nib[:, 1] << 4)
+    for off, sc, zr in ((2048, k_scale, k_zero), (2304, v_scale, v_zero)):
+        m = np.zeros((nt * 16, 4, 2), np.float16)
+        m[:n, :, 0] = sc
+        m[:n, :, 1] = zr
+        tiles[:, off:off + 256] = m.view(np.uint8).reshape(nt, 256)
+    return tiles.reshape(nblk, 10240)
 
 
 class HybridDecoder:

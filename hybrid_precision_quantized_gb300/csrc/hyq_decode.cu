@@ -2,76 +2,64 @@
 // for LLM Attention", §4.3 Eq. 8-9 and Appendix A.3 Algorithm 3) and the
 // per-step bookkeeping (append to the BF16 tail, proxy-query ring of §5.5).
 //
-// Work decomposition (one launch):
-//   grid.x = S_q + S_f thread blocks per (batch, KV head).  The first S_q
-//   blocks split the 4-bit stream along the sequence (Algorithm 3, segment 1
-//   "partition K^Q into S chunks"); the last S_f split the BF16 rows
-//   (vertical-line rows, then the tail).  Every block keeps one online
-//   softmax state (m, l, acc) per query head of the KV group (the g query
-//   heads are packed into one tensor-core tile, Algorithm 3 line "pack g GQA
-//   heads"), writes it to the workspace, and the last block to finish (an
-//   atomic ticket; nobody waits) merges all partials by log-sum-exp
-//   rescaling (ReduceSoftmax) and writes the BF16 output.
+// Work decomposition (one launch, grid S x HKV x B, 16 warps per block):
+//   the 4-bit stream of a (batch, KV head) is split along the sequence into
+//   S chunks (Algorithm 3, segment 1), and so are its BF16 rows (vertical-
+//   line rows, then the tail).  Inside a block every warp works alone on
+//   16-row tiles: BF16 tiles first, then 4-bit tiles streamed through its own
+//   ring of bulk copies (TMA, no block-wide barrier in the main loop).  Each
+//   warp keeps one online-softmax state (m, l, acc) for the g query heads of
+//   the KV group, packed into one tensor-core tile (Algorithm 3, "pack g GQA
+//   heads").  The block merges its warps, writes one partial per split, and
+//   the last block to finish (an atomic ticket; nobody waits) merges the S
+//   partials by log-sum-exp rescaling (ReduceSoftmax) into the BF16 output.
 //
-// 4-bit tiles (16 rows) are dequantised inside the dot products:
+// 4-bit tiles are dequantised inside the dot products:
 //   q.k~  = sum_q s_q (q_q . c_q) + z_q sum(q_q)     (per group q of 32)
 //   p v~  = sum_j (p_j s_jq) c_jd + p_j z_jq
-// The code products run on mma.sync m16n8k16 with the codes unpacked from
-// nibbles into register pairs by one lop3/and each: K codes as bf16 128 + c
-// (the offset is removed exactly through the per-group query sums, since q
-// and s enter unrounded), V codes as fp16 subnormals c * 2^-24 against the
-// fp16-rounded p * s (no offset, so the rounding of p * s is not amplified).
-// Scale/zero terms are applied in fp32.
+// on mma.sync m16n8k16: K codes as bf16 128 + c (the offset is removed
+// exactly through the per-group query sums, since q and s enter unrounded),
+// V codes as fp16 subnormals c * 2^-24 against the fp16-rounded p * s (no
+// offset, so the rounding of p * s is not amplified).  BF16 tiles are loaded
+// straight into fragment registers; the head_dim order of the K products and
+// of the V outputs is permuted (identically in both paths, see hyq.h) so that
+// those loads are 16- and 8-byte vectors.
 #include <math.h>
 
 #include "hyq_common.cuh"
 
 namespace {
 
-constexpr int kThreads = 128;  // 4 warps, one 16-row tile each
-constexpr int kWarps = 4;
-constexpr int kQStages = 4;      // 4-bit blocks in flight per CTA
-constexpr int kFRows = 64;       // BF16 rows per stage
-constexpr int kFStride = 272;    // padded BF16 row in shared memory (conflict-free ldmatrix)
-constexpr int kFStages = 2;
-constexpr int kStageFBytes = 2 * kFRows * kFStride;
-constexpr int kSmemBytes = (kQStages * HYQ_QBLOCK_BYTES > kFStages * kStageFBytes)
-                               ? kQStages * HYQ_QBLOCK_BYTES
-                               : kFStages * kStageFBytes;
-constexpr int kPart = 2 + HYQ_D;  // m, l, acc[128] per head
-constexpr int kMaxSplits = 512;
+constexpr int kWarps = 16;
+constexpr int kThreads = kWarps * 32;
+constexpr int kSlots = 4;                                     // tiles in flight per warp
+constexpr int kSmemBytes = kWarps * kSlots * HYQ_QTILE_BYTES; // 160 KiB ring
+constexpr int kPart = 2 + HYQ_D;                              // m, l, acc[128] per head
+constexpr int kMaxSplits = 1024;
 // log2(e) / sqrt(128): logits are kept in the base-2 domain.
 constexpr float kScale = 0.1275174307366466f;
+constexpr float kSubScale = 1.0f / HYQ_F16_SUB_SCALE;         // 2^-24
 
 size_t round_up(size_t x) { return (x + 255) / 256 * 256; }
 
-void decode_split(const hyq_config* c, int32_t len, int& sq, int& sf) {
+// Split count: about one block per SM over all (batch, KV head) pairs, and
+// not more blocks than there are 16-row tiles to share.
+int decode_split(const hyq_config* c, int32_t len) {
   const int bh = c->batch * c->num_kv_heads;
-  const int target = 2 * hyq_num_sms();
-  int per_bh = (target + bh - 1) / bh;
-  if (per_bh < 2) per_bh = 2;
+  int S = (hyq_num_sms() + bh / 2) / bh;
   int32_t P = len - c->window > 0 ? len - c->window : 0;
-  int32_t nvl = hyq_vl_count(c, P);
-  int64_t nq = P - nvl;
-  int64_t nf = (int64_t)nvl + (len < hyq_cap_tail(c) ? len : hyq_cap_tail(c));
-  double bq = 160.0 * nq, bf = 512.0 * nf;
-  sq = (int)(per_bh * bq / (bq + bf + 1.0) + 0.5);
-  int sq_max = (int)((nq + HYQ_QBLOCK_ROWS - 1) / HYQ_QBLOCK_ROWS);
-  if (sq > sq_max) sq = sq_max;
-  if (sq < 1) sq = 1;
-  sf = per_bh - sq;
-  int sf_max = (int)((nf + 2 * 16 - 1) / (2 * 16));  // at least ~32 rows per block
-  if (sf > sf_max) sf = sf_max;
-  if (sf < 1) sf = 1;
-  if (sq + sf > kMaxSplits) {
-    sq = kMaxSplits - sf;
-  }
+  int64_t tiles = (int64_t)(P + 15) / 16 + (hyq_vl_count(c, P) + hyq_cap_tail(c) + 15) / 16;
+  int64_t cap = tiles / 32;
+  if (S > cap) S = (int)cap;
+  if (S < 1) S = 1;
+  if (S > kMaxSplits) S = kMaxSplits;
+  return S;
 }
 
 struct State {
   float m[2], l[2];
-  float acc[8][4];
-  float zacc[2][4];
+  float acc[8][4];   // PV accumulators in units of 2^-24
+  float zacc[2][4];  // sum_j p_j z_jq per head (2t, 2t+1) and group q
 };
 
 // Online-softmax update of the two heads (2t, 2t+1) this thread owns with the
@@ -100,14 +88,12 @@ __device__ __forceinline__ void softmax_update(const float (&lg)[4], State& st, 
   }
 }
 
-// One 16-row tile of a 4-bit block (stage base `sb`, tile `w`), `vr` valid rows.
-__device__ __forceinline__ void q_tile(const uint8_t* sb, int w, int lane, int vr,
-                                       const uint32_t (&bq)[8][2], const float (&qs)[2][4],
-                                       State& st) {
+// One 16-row 4-bit tile (2560 bytes at `tb`), `vr` valid rows.
+__device__ __forceinline__ void q_tile(const uint8_t* tb, int lane, int vr, const uint32_t (&bq)[8][2],
+                                       const float (&qs)[2][4], State& st) {
   const int g = lane >> 2;
-  const uint8_t* kt = sb + w * HYQ_TILE_BYTES;
-  const uint4 kw0 = *reinterpret_cast<const uint4*>(kt + lane * 16);
-  const uint4 kw1 = *reinterpret_cast<const uint4*>(kt + 512 + lane * 16);
+  const uint4 kw0 = *reinterpret_cast<const uint4*>(tb + lane * 16);
+  const uint4 kw1 = *reinterpret_cast<const uint4*>(tb + 512 + lane * 16);
   const uint32_t kw[8] = {kw0.x, kw0.y, kw0.z, kw0.w, kw1.x, kw1.y, kw1.z, kw1.w};
   float C[4][4];
 #pragma unroll
@@ -116,7 +102,7 @@ __device__ __forceinline__ void q_tile(const uint8_t* sb, int w, int lane, int v
   for (int ks = 0; ks < 8; ++ks)
     mma_bf16(C[ks >> 1], nib2_bf16(kw[ks], 0), nib2_bf16(kw[ks], 4), nib2_bf16(kw[ks], 8),
              nib2_bf16(kw[ks], 12), bq[ks][0], bq[ks][1]);
-  const uint8_t* km = sb + HYQ_KMETA_OFF + w * 16 * 16;
+  const uint8_t* km = tb + 2048;
   float lg[4];
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
@@ -138,11 +124,10 @@ __device__ __forceinline__ void q_tile(const uint8_t* sb, int w, int lane, int v
   }
   float p[4];
   softmax_update(lg, st, p);
-  const uint8_t* vt = sb + HYQ_VCODE_OFF + w * HYQ_TILE_BYTES;
-  const uint4 vw0 = *reinterpret_cast<const uint4*>(vt + lane * 16);
-  const uint4 vw1 = *reinterpret_cast<const uint4*>(vt + 512 + lane * 16);
+  const uint4 vw0 = *reinterpret_cast<const uint4*>(tb + 1024 + lane * 16);
+  const uint4 vw1 = *reinterpret_cast<const uint4*>(tb + 1024 + 512 + lane * 16);
   const uint32_t vw[8] = {vw0.x, vw0.y, vw0.z, vw0.w, vw1.x, vw1.y, vw1.z, vw1.w};
-  const uint8_t* vm = sb + HYQ_VMETA_OFF + w * 16 * 16;
+  const uint8_t* vm = tb + 2304;
   const uint4 mv0 = *reinterpret_cast<const uint4*>(vm + g * 16);
   const uint4 mv1 = *reinterpret_cast<const uint4*>(vm + (g + 8) * 16);
   const uint32_t m0[4] = {mv0.x, mv0.y, mv0.z, mv0.w};
@@ -158,25 +143,41 @@ __device__ __forceinline__ void q_tile(const uint8_t* sb, int w, int lane, int v
     st.zacc[1][q] = fmaf(p[1], sz0.y, fmaf(p[3], sz1.y, st.zacc[1][q]));
 #pragma unroll
     for (int mm = 0; mm < 2; ++mm) {
-      const uint32_t x = vw[2 * q + mm];
-      // codes as c * 2^-24: acc collects 2^-24 * sum_j (p_j s_j) c_jd
+      const uint32_t x = vw[2 * q + mm];  // m-tile 2q + mm lies in group q
       mma_f16(st.acc[2 * q + mm], nib2_f16_sub(x, 0), nib2_f16_sub(x, 4), nib2_f16_sub(x, 8),
               nib2_f16_sub(x, 12), b0, b1);
     }
   }
 }
 
-// One 16-row tile of BF16 rows (K rows at Ks, V rows at Vs, padded stride).
-__device__ __forceinline__ void f_tile(const uint8_t* Ks, const uint8_t* Vs, int w, int lane, int vr,
-                                       const uint32_t (&bq)[8][2], State& st) {
-  const int g = lane >> 2, i4 = lane >> 3, rr = lane & 7;
+__device__ __forceinline__ uint32_t u4c(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// One 16-row tile of BF16 rows (rows row0.. of the vertical-line rows followed
+// by the tail), `vr` valid rows, loaded directly into fragment registers.
+__device__ __forceinline__ void f_tile(const __nv_bfloat16* vlk, const __nv_bfloat16* vlv,
+                                       const __nv_bfloat16* tk, const __nv_bfloat16* tv, int nvl,
+                                       int row0, int vr, int lane, const uint32_t (&bq)[8][2], State& st) {
+  const int g = lane >> 2, t = lane & 3;
   float S[4] = {0.f, 0.f, 0.f, 0.f};
+  {
+    // K rows g and g+8, chunks t + 4j: the permuted k order of the A fragments.
+    uint4 ka[2][4];
 #pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    uint32_t a0, a1, a2, a3;
-    ldmatrix_x4(smem_u32(Ks + (w * 16 + rr + 8 * (i4 & 1)) * kFStride + (16 * ks + 8 * (i4 >> 1)) * 2), a0,
-                a1, a2, a3);
-    mma_bf16(S, a0, a1, a2, a3, bq[ks][0], bq[ks][1]);
+    for (int a = 0; a < 2; ++a) {
+      const int rr = g + 8 * a, row = row0 + rr;
+      const __nv_bfloat16* src = row < nvl ? vlk + (size_t)row * HYQ_D : tk + (size_t)(row - nvl) * HYQ_D;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        ka[a][j] = rr < vr ? __ldg(reinterpret_cast<const uint4*>(src + 8 * (t + 4 * j))) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const int j = ks >> 1, sub = ks & 1;
+      mma_bf16(S, u4c(ka[0][j], 2 * sub), u4c(ka[1][j], 2 * sub), u4c(ka[0][j], 2 * sub + 1),
+               u4c(ka[1][j], 2 * sub + 1), bq[ks][0], bq[ks][1]);
+    }
   }
   float lg[4];
   lg[0] = g < vr ? S[0] * kScale : -INFINITY;
@@ -185,29 +186,42 @@ __device__ __forceinline__ void f_tile(const uint8_t* Ks, const uint8_t* Vs, int
   lg[3] = g + 8 < vr ? S[3] * kScale : -INFINITY;
   float p[4];
   softmax_update(lg, st, p);
-  const uint32_t b0 = movmatrix_trans(pack_bf16x2(p[0], p[1]));
-  const uint32_t b1 = movmatrix_trans(pack_bf16x2(p[2], p[3]));
+  // P^T (tokens x heads), scaled by 2^-24 like the 4-bit accumulators.
+  const uint32_t b0 = movmatrix_trans(pack_bf16x2(p[0] * kSubScale, p[1] * kSubScale));
+  const uint32_t b1 = movmatrix_trans(pack_bf16x2(p[2] * kSubScale, p[3] * kSubScale));
+  // V rows 2t + 8b + c, elements 32G + 4g .. +3 for the four groups G.
+  uint2 va[4][4];
 #pragma unroll
-  for (int mt = 0; mt < 8; ++mt) {
-    uint32_t a0, a1, a2, a3;
-    ldmatrix_x4_trans(smem_u32(Vs + (w * 16 + rr + 8 * (i4 >> 1)) * kFStride + (16 * mt + 8 * (i4 & 1)) * 2),
-                      a0, a1, a2, a3);
-    mma_bf16(st.acc[mt], a0, a1, a2, a3, b0, b1);
+  for (int tk4 = 0; tk4 < 4; ++tk4) {
+    const int rr = 2 * t + 8 * (tk4 >> 1) + (tk4 & 1), row = row0 + rr;
+    const __nv_bfloat16* src = row < nvl ? vlv + (size_t)row * HYQ_D : tv + (size_t)(row - nvl) * HYQ_D;
+#pragma unroll
+    for (int G = 0; G < 4; ++G)
+      va[tk4][G] = rr < vr ? __ldg(reinterpret_cast<const uint2*>(src + 32 * G + 4 * g)) : make_uint2(0, 0);
+  }
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int G = u >> 1, s2 = u & 1;
+    const uint32_t w0 = s2 ? va[0][G].y : va[0][G].x, w1 = s2 ? va[1][G].y : va[1][G].x;
+    const uint32_t w2 = s2 ? va[2][G].y : va[2][G].x, w3 = s2 ? va[3][G].y : va[3][G].x;
+    mma_bf16(st.acc[u], __byte_perm(w0, w1, 0x5410), __byte_perm(w0, w1, 0x7632),
+             __byte_perm(w2, w3, 0x5410), __byte_perm(w2, w3, 0x7632), b0, b1);
   }
 }
 
-__global__ void __launch_bounds__(kThreads) decode_kernel(
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(
     const __nv_bfloat16* __restrict__ q, hyq_layout lay, __nv_bfloat16* __restrict__ out,
     int32_t* __restrict__ tickets, float* __restrict__ part, int HQ, int gq, int nblk_cap,
-    int cap_vl, int cap_tail, int S_q, int S_f) {
+    int cap_vl, int cap_tail, int S) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(16) __nv_bfloat16 q_s[HYQ_MAX_GQA * HYQ_D];
   __shared__ float qsum_s[HYQ_MAX_GQA * 4];
-  __shared__ __align__(8) uint64_t bars[kQStages];
+  __shared__ __align__(8) uint64_t bars[kWarps * kSlots];
+  __shared__ float red_m[kWarps][HYQ_MAX_GQA], red_l[kWarps][HYQ_MAX_GQA], wts[kWarps][HYQ_MAX_GQA];
+  __shared__ float sM[HYQ_MAX_GQA], sL[HYQ_MAX_GQA];
   __shared__ int s_flag;
 
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z, HKV = gridDim.y;
-  const int S_tot = S_q + S_f;
   const size_t bh = (size_t)b * HKV + h;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
 
@@ -219,7 +233,29 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(
     nvl = min(max(nvl, 0), cap_vl);
     ntail = min(max(ntail, 0), cap_tail);
   }
+  // This block's share of the 4-bit tiles and of the BF16 tiles.
+  const int nt = (nq + 15) >> 4, nf = nvl + ntail, nft = (nf + 15) >> 4;
+  const int t0 = (int)((int64_t)split * nt / S), t1 = (int)((int64_t)(split + 1) * nt / S);
+  const int f0 = (int)((int64_t)split * nft / S), f1 = (int)((int64_t)(split + 1) * nft / S);
+  // 4-bit tiles go round-robin over the warps, starting after the warps that
+  // also take a BF16 tile.
+  const int ntc = t1 - t0, rot = (f1 - f0) % kWarps;
+  const int my0 = (warp - rot + kWarps) % kWarps;
+  const int nj = ntc > my0 ? (ntc - my0 + kWarps - 1) / kWarps : 0;
+  const uint8_t* tiles = lay.qblocks + bh * (size_t)nblk_cap * HYQ_QBLOCK_BYTES;
+  uint8_t* ring = smem + warp * kSlots * HYQ_QTILE_BYTES;
+  uint64_t* wb = bars + warp * kSlots;
 
+  if (lane == 0) {
+    for (int i = 0; i < kSlots; ++i) mbar_init(&wb[i], 1);
+    mbar_fence_init();
+    // Start this warp's 4-bit stream right away.
+    for (int j = 0; j < nj && j < kSlots; ++j) {
+      mbar_arrive_expect_tx(&wb[j], HYQ_QTILE_BYTES);
+      bulk_g2s(ring + j * HYQ_QTILE_BYTES, tiles + (size_t)(t0 + my0 + kWarps * j) * HYQ_QTILE_BYTES,
+               HYQ_QTILE_BYTES, &wb[j]);
+    }
+  }
   // Query tile of the KV group (rows past g are zero) and its per-group sums.
   for (int i = tid; i < HYQ_MAX_GQA * HYQ_D / 8; i += kThreads) {
     const int row = i >> 4, c8 = i & 15;
@@ -227,23 +263,22 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(
     if (row < gq) v = *reinterpret_cast<const uint4*>(q + ((size_t)b * HQ + (size_t)h * gq + row) * HYQ_D + 8 * c8);
     *reinterpret_cast<uint4*>(q_s + row * HYQ_D + 8 * c8) = v;
   }
-  if (tid == 0) {
-    for (int i = 0; i < kQStages; ++i) mbar_init(&bars[i], 1);
-    mbar_fence_init();
-  }
   __syncthreads();
   if (tid < 32) {
-    float s = 0.f;
+    float sacc = 0.f;
     const __nv_bfloat16* r = q_s + (tid >> 2) * HYQ_D + 32 * (tid & 3);
-    for (int i = 0; i < 32; ++i) s += __bfloat162float(r[i]);
-    qsum_s[tid] = s;
+    for (int i = 0; i < 32; ++i) sacc += __bfloat162float(r[i]);
+    qsum_s[tid] = sacc;
   }
   __syncthreads();
+  // B fragments of q in the permuted k order: kstep ks covers elements
+  // 8(t + 4(ks/2)) + 4(ks%2) + {0,1} and + {2,3}.
   uint32_t bq[8][2];
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
-    bq[ks][0] = *reinterpret_cast<const uint32_t*>(q_s + g * HYQ_D + 16 * ks + 2 * t);
-    bq[ks][1] = *reinterpret_cast<const uint32_t*>(q_s + g * HYQ_D + 16 * ks + 2 * t + 8);
+    const int e = 8 * (t + 4 * (ks >> 1)) + 4 * (ks & 1);
+    bq[ks][0] = *reinterpret_cast<const uint32_t*>(q_s + g * HYQ_D + e);
+    bq[ks][1] = *reinterpret_cast<const uint32_t*>(q_s + g * HYQ_D + e + 2);
   }
   float qs[2][4];
 #pragma unroll
@@ -259,105 +294,44 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(
 #pragma unroll
   for (int j = 0; j < 2; ++j) st.zacc[j][0] = st.zacc[j][1] = st.zacc[j][2] = st.zacc[j][3] = 0.f;
 
-  bool timed_out = false;
-  int pend_lo = 0, pend_hi = 0, pend_stages = 1;  // copies still in flight after a timeout
-  if (split < S_q) {
-    // ---- 4-bit stream: blocks [b0, b1) of this split ----------------------
-    const int nb = (nq + HYQ_QBLOCK_ROWS - 1) / HYQ_QBLOCK_ROWS;
-    const int b0 = (int)((int64_t)split * nb / S_q), b1 = (int)((int64_t)(split + 1) * nb / S_q);
-    const int n = b1 - b0;
-    const uint8_t* src = lay.qblocks + (bh * nblk_cap + b0) * (size_t)HYQ_QBLOCK_BYTES;
-    if (tid == 0) {
-      for (int i = 0; i < n && i < kQStages; ++i) {
-        mbar_arrive_expect_tx(&bars[i], HYQ_QBLOCK_BYTES);
-        bulk_g2s(smem + i * HYQ_QBLOCK_BYTES, src + (size_t)i * HYQ_QBLOCK_BYTES, HYQ_QBLOCK_BYTES, &bars[i]);
-      }
-    }
-    for (int i = 0; i < n; ++i) {
-      const int sidx = i % kQStages;
-      const bool ok = mbar_wait(&bars[sidx], (i / kQStages) & 1);
-      if (__syncthreads_or(!ok)) {
-        timed_out = true;
-        pend_lo = i;
-        pend_hi = min(n, i + kQStages);
-        pend_stages = kQStages;
-        break;
-      }
-      const int vr = min(HYQ_QBLOCK_ROWS, nq - (b0 + i) * HYQ_QBLOCK_ROWS) - 16 * warp;
-      if (vr > 0) q_tile(smem + sidx * HYQ_QBLOCK_BYTES, warp, lane, vr, bq, qs, st);
-      __syncthreads();
-      if (tid == 0 && i + kQStages < n) {
-        mbar_arrive_expect_tx(&bars[sidx], HYQ_QBLOCK_BYTES);
-        bulk_g2s(smem + sidx * HYQ_QBLOCK_BYTES, src + (size_t)(i + kQStages) * HYQ_QBLOCK_BYTES,
-                 HYQ_QBLOCK_BYTES, &bars[sidx]);
-      }
-    }
-  } else {
-    // ---- BF16 rows: vertical-line rows then tail rows ----------------------
-    const int nf = nvl + ntail;
-    const int sp = split - S_q;
-    const int r0 = (int)((int64_t)sp * nf / S_f), r1 = (int)((int64_t)(sp + 1) * nf / S_f);
-    const int nst = (r1 - r0 + kFRows - 1) / kFRows;
-    // Rows past the copied count must hold finite values: zero the stages once.
-    for (int i = tid; i < kFStages * kStageFBytes / 16; i += kThreads)
-      reinterpret_cast<uint4*>(smem)[i] = make_uint4(0, 0, 0, 0);
-    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-    __syncthreads();
+  // ---- BF16 tiles (vertical-line rows, then the tail) ----------------------
+  {
     const __nv_bfloat16* vlk = static_cast<const __nv_bfloat16*>(lay.vl_k) + bh * cap_vl * HYQ_D;
     const __nv_bfloat16* vlv = static_cast<const __nv_bfloat16*>(lay.vl_v) + bh * cap_vl * HYQ_D;
     const __nv_bfloat16* tk = static_cast<const __nv_bfloat16*>(lay.tail_k) + bh * cap_tail * HYQ_D;
     const __nv_bfloat16* tv = static_cast<const __nv_bfloat16*>(lay.tail_v) + bh * cap_tail * HYQ_D;
-    auto issue = [&](int stage, int rbase) {
-      const int nrows = min(kFRows, r1 - rbase);
-      uint8_t* Ks = smem + stage * kStageFBytes;
-      uint8_t* Vs = Ks + kFRows * kFStride;
-      if (lane == 0) mbar_arrive_expect_tx(&bars[stage], nrows * 2 * HYQ_D * 2);
+    for (int fi = f0 + warp; fi < f1; fi += kWarps)
+      f_tile(vlk, vlv, tk, tv, nvl, 16 * fi, min(16, nf - 16 * fi), lane, bq, st);
+  }
+  // ---- 4-bit tiles through the warp's ring ---------------------------------
+  bool timed_out = false;
+  for (int j = 0; j < nj; ++j) {
+    const int slot = j % kSlots;
+    const bool ok = mbar_wait(&wb[slot], (j / kSlots) & 1);
+    if (__any_sync(0xffffffffu, !ok)) {
+      // A copy did not arrive: flag it, and make sure none of this warp's
+      // copies is still in flight before the ring is reused below.
+      timed_out = true;
+      if (lane == 0) {
+        hyq_set_err(lay.err, HYQ_DEVERR_TIMEOUT);
+        for (int jj = j; jj < nj && jj < j + kSlots; ++jj) (void)mbar_wait(&wb[jj % kSlots], (jj / kSlots) & 1);
+      }
       __syncwarp();
-      for (int rr = lane; rr < nrows; rr += 32) {
-        const int row = rbase + rr;
-        const __nv_bfloat16* sk = row < nvl ? vlk + (size_t)row * HYQ_D : tk + (size_t)(row - nvl) * HYQ_D;
-        const __nv_bfloat16* sv = row < nvl ? vlv + (size_t)row * HYQ_D : tv + (size_t)(row - nvl) * HYQ_D;
-        bulk_g2s(Ks + rr * kFStride, sk, HYQ_D * 2, &bars[stage]);
-        bulk_g2s(Vs + rr * kFStride, sv, HYQ_D * 2, &bars[stage]);
-      }
-    };
-    if (warp == 0)
-      for (int i = 0; i < nst && i < kFStages; ++i) issue(i, r0 + i * kFRows);
-    for (int i = 0; i < nst; ++i) {
-      const int sidx = i % kFStages;
-      const bool ok = mbar_wait(&bars[sidx], (i / kFStages) & 1);
-      if (__syncthreads_or(!ok)) {
-        timed_out = true;
-        pend_lo = i;
-        pend_hi = min(nst, i + kFStages);
-        pend_stages = kFStages;
-        break;
-      }
-      const uint8_t* Ks = smem + sidx * kStageFBytes;
-      const int vr = min(kFRows, r1 - (r0 + i * kFRows)) - 16 * warp;
-      if (vr > 0) f_tile(Ks, Ks + kFRows * kFStride, warp, lane, vr, bq, st);
-      __syncthreads();
-      if (warp == 0 && i + kFStages < nst) issue(sidx, r0 + (i + kFStages) * kFRows);
+      break;
+    }
+    const int tile = t0 + my0 + kWarps * j;
+    q_tile(ring + slot * HYQ_QTILE_BYTES, lane, min(16, nq - 16 * tile), bq, qs, st);
+    __syncwarp();
+    if (lane == 0 && j + kSlots < nj) {
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+      mbar_arrive_expect_tx(&wb[slot], HYQ_QTILE_BYTES);
+      bulk_g2s(ring + slot * HYQ_QTILE_BYTES, tiles + (size_t)(tile + kWarps * kSlots) * HYQ_QTILE_BYTES,
+               HYQ_QTILE_BYTES, &wb[slot]);
     }
   }
-  if (timed_out) {
-    // A bulk copy did not arrive: report it and make sure none is still in
-    // flight into this block's shared memory before the block exits.
-    if (tid == 0) {
-      hyq_set_err(lay.err, HYQ_DEVERR_TIMEOUT);
-      for (int i = pend_lo; i < pend_hi; ++i) (void)mbar_wait(&bars[i % pend_stages], (i / pend_stages) & 1);
-    }
-    __syncthreads();
-    return;
-  }
+  (void)timed_out;
 
-  if (split < S_q) {  // the 4-bit PV products were taken on codes scaled by 2^-24
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-      for (int ci = 0; ci < 4; ++ci) st.acc[mt][ci] *= HYQ_F16_SUB_SCALE;
-  }
-  // ---- reduce the thread-partial sums over the 8 lanes sharing t ----------
+  // ---- warp partials -> block partial --------------------------------------
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
 #pragma unroll
@@ -367,34 +341,33 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(
 #pragma unroll
       for (int o = 4; o < 32; o <<= 1) st.zacc[j][qq] += __shfl_xor_sync(0xffffffffu, st.zacc[j][qq], o);
   }
-  __syncthreads();  // stage memory is free from here on
-  float* red = reinterpret_cast<float*>(smem);           // [warp][head][128]
-  float* red_m = red + kWarps * HYQ_MAX_GQA * HYQ_D;     // [warp][head]
-  float* red_l = red_m + kWarps * HYQ_MAX_GQA;
-  float* wts = red_l + kWarps * HYQ_MAX_GQA;             // [warp][head]
+  __syncthreads();  // every warp is done with its ring: reuse shared memory
+  float* red = reinterpret_cast<float*>(smem);  // [warp][head][128]
+  // Accumulator (m-tile u, ci) of thread (g, t): element 32(u/2) + 4g + 2(u%2)
+  // + (ci >> 1), head 2t + (ci & 1).
 #pragma unroll
-  for (int mt = 0; mt < 8; ++mt)
+  for (int u = 0; u < 8; ++u)
 #pragma unroll
     for (int ci = 0; ci < 4; ++ci) {
-      const int d = 16 * mt + g + 8 * (ci >> 1), hd = 2 * t + (ci & 1);
-      red[(warp * HYQ_MAX_GQA + hd) * HYQ_D + d] = st.acc[mt][ci] + st.zacc[ci & 1][mt >> 1];
+      const int d = 32 * (u >> 1) + 4 * g + 2 * (u & 1) + (ci >> 1), hd = 2 * t + (ci & 1);
+      red[(warp * HYQ_MAX_GQA + hd) * HYQ_D + d] = fmaf(st.acc[u][ci], HYQ_F16_SUB_SCALE, st.zacc[ci & 1][u >> 1]);
     }
   if (g == 0)
     for (int j = 0; j < 2; ++j) {
-      red_m[warp * HYQ_MAX_GQA + 2 * t + j] = st.m[j];
-      red_l[warp * HYQ_MAX_GQA + 2 * t + j] = st.l[j];
+      red_m[warp][2 * t + j] = st.m[j];
+      red_l[warp][2 * t + j] = st.l[j];
     }
   __syncthreads();
-  float* pp = part + (bh * S_tot + split) * (size_t)(HYQ_MAX_GQA * kPart);
+  float* pp = part + (bh * S + split) * (size_t)(HYQ_MAX_GQA * kPart);
   if (tid < gq) {
     float M = -INFINITY;
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w * HYQ_MAX_GQA + tid]);
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w][tid]);
     const float Ms = (M == -INFINITY) ? 0.f : M;
     float Lsum = 0.f;
     for (int w = 0; w < kWarps; ++w) {
-      const float wt = exp2f(red_m[w * HYQ_MAX_GQA + tid] - Ms);
-      wts[w * HYQ_MAX_GQA + tid] = wt;
-      Lsum = fmaf(red_l[w * HYQ_MAX_GQA + tid], wt, Lsum);
+      const float wt = exp2f(red_m[w][tid] - Ms);
+      wts[w][tid] = wt;
+      Lsum = fmaf(red_l[w][tid], wt, Lsum);
     }
     pp[tid * kPart + 0] = M;
     pp[tid * kPart + 1] = Lsum;
@@ -403,45 +376,47 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(
   for (int i = tid; i < gq * HYQ_D; i += kThreads) {
     const int hd = i >> 7, d = i & (HYQ_D - 1);
     float a = 0.f;
-    for (int w = 0; w < kWarps; ++w) a = fmaf(red[(w * HYQ_MAX_GQA + hd) * HYQ_D + d], wts[w * HYQ_MAX_GQA + hd], a);
+#pragma unroll 4
+    for (int w = 0; w < kWarps; ++w) a = fmaf(red[(w * HYQ_MAX_GQA + hd) * HYQ_D + d], wts[w][hd], a);
     pp[hd * kPart + 2 + d] = a;
   }
   __threadfence();
   __syncthreads();
-  if (tid == 0) s_flag = (atomicAdd(&tickets[bh], 1) == S_tot - 1);
+  if (tid == 0) s_flag = (atomicAdd(&tickets[bh], 1) == S - 1);
   __syncthreads();
   if (!s_flag) return;
   __threadfence();
 
-  // ---- last block: ReduceSoftmax over the S_tot partials -------------------
-  const float* pb = part + bh * S_tot * (size_t)(HYQ_MAX_GQA * kPart);
-  float* sM = red;                       // [head]
-  float* sL = sM + HYQ_MAX_GQA;          // [head]
-  float* sw = sL + HYQ_MAX_GQA;          // [split][head]
+  // ---- last block of this (batch, KV head): ReduceSoftmax over S splits ----
+  const float* pb = part + bh * S * (size_t)(HYQ_MAX_GQA * kPart);
+  float* sm_m = red;                         // [S][8]
+  float* sm_w = red + kMaxSplits * HYQ_MAX_GQA;  // [S][8]
+  for (int i = tid; i < S * gq; i += kThreads) {
+    const int s2 = i / gq, hd = i % gq;
+    sm_m[s2 * HYQ_MAX_GQA + hd] = __ldcg(pb + (size_t)s2 * HYQ_MAX_GQA * kPart + hd * kPart);
+    sm_w[s2 * HYQ_MAX_GQA + hd] = __ldcg(pb + (size_t)s2 * HYQ_MAX_GQA * kPart + hd * kPart + 1);
+  }
+  __syncthreads();
   if (tid < gq) {
     float M = -INFINITY;
-    for (int s2 = 0; s2 < S_tot; ++s2) M = fmaxf(M, __ldcg(pb + (size_t)s2 * HYQ_MAX_GQA * kPart + tid * kPart));
-    sM[tid] = (M == -INFINITY) ? 0.f : M;
-  }
-  __syncthreads();
-  for (int i = tid; i < S_tot * gq; i += kThreads) {
-    const int s2 = i / gq, hd = i % gq;
-    const float* e = pb + (size_t)s2 * HYQ_MAX_GQA * kPart + hd * kPart;
-    sw[s2 * HYQ_MAX_GQA + hd] = exp2f(__ldcg(e) - sM[hd]);
-  }
-  __syncthreads();
-  if (tid < gq) {
+    for (int s2 = 0; s2 < S; ++s2) M = fmaxf(M, sm_m[s2 * HYQ_MAX_GQA + tid]);
+    const float Ms = (M == -INFINITY) ? 0.f : M;
     float Lsum = 0.f;
-    for (int s2 = 0; s2 < S_tot; ++s2)
-      Lsum = fmaf(__ldcg(pb + (size_t)s2 * HYQ_MAX_GQA * kPart + tid * kPart + 1), sw[s2 * HYQ_MAX_GQA + tid], Lsum);
+    for (int s2 = 0; s2 < S; ++s2) {
+      const float wt = exp2f(sm_m[s2 * HYQ_MAX_GQA + tid] - Ms);
+      Lsum = fmaf(sm_w[s2 * HYQ_MAX_GQA + tid], wt, Lsum);
+      sm_w[s2 * HYQ_MAX_GQA + tid] = wt;     // l_s no longer needed: keep the weight
+    }
+    sM[tid] = Ms;
     sL[tid] = Lsum;
   }
   __syncthreads();
   for (int i = tid; i < gq * HYQ_D; i += kThreads) {
     const int hd = i >> 7, d = i & (HYQ_D - 1);
+    const float* e = pb + hd * kPart + 2 + d;
     float a = 0.f;
-    for (int s2 = 0; s2 < S_tot; ++s2)
-      a = fmaf(__ldcg(pb + (size_t)s2 * HYQ_MAX_GQA * kPart + hd * kPart + 2 + d), sw[s2 * HYQ_MAX_GQA + hd], a);
+#pragma unroll 8
+    for (int s2 = 0; s2 < S; ++s2) a = fmaf(__ldcg(e + (size_t)s2 * HYQ_MAX_GQA * kPart), sm_w[s2 * HYQ_MAX_GQA + hd], a);
     const float Lh = sL[hd];
     out[((size_t)b * HQ + (size_t)h * gq + hd) * HYQ_D + d] = __float2bfloat16_rn(Lh > 0.f ? a / Lh : 0.f);
   }
@@ -502,10 +477,9 @@ __global__ void decode_append_kernel(const __nv_bfloat16* __restrict__ q, const 
 }  // namespace
 
 size_t hyq_decode_ws_bytes(const hyq_config* c, int32_t len_hint) {
-  int sq, sf;
-  decode_split(c, len_hint, sq, sf);
+  const int S = decode_split(c, len_hint);
   size_t bh = (size_t)c->batch * c->num_kv_heads;
-  return round_up(bh * 4) + round_up(bh * (size_t)(sq + sf) * HYQ_MAX_GQA * kPart * 4);
+  return round_up(bh * 4) + round_up(bh * (size_t)S * HYQ_MAX_GQA * kPart * 4);
 }
 
 cudaError_t hyq_launch_decode(const hyq_config* c, const void* q, const hyq_layout* lay, void* out,
@@ -516,15 +490,14 @@ cudaError_t hyq_launch_decode(const hyq_config* c, const void* q, const hyq_layo
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  int sq, sf;
-  decode_split(c, len_hint, sq, sf);
+  const int S = decode_split(c, len_hint);
   size_t bh = (size_t)c->batch * c->num_kv_heads;
   int32_t* tickets = static_cast<int32_t*>(ws);
   float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + round_up(bh * 4));
-  dim3 grid(sq + sf, c->num_kv_heads, c->batch);
+  dim3 grid(S, c->num_kv_heads, c->batch);
   decode_kernel<<<grid, kThreads, kSmemBytes, s>>>(
       static_cast<const __nv_bfloat16*>(q), *lay, static_cast<__nv_bfloat16*>(out), tickets, part,
-      c->num_q_heads, c->num_q_heads / c->num_kv_heads, hyq_nblk(c), hyq_vl_stride(c), hyq_cap_tail(c), sq, sf);
+      c->num_q_heads, c->num_q_heads / c->num_kv_heads, hyq_nblk(c), hyq_vl_stride(c), hyq_cap_tail(c), S);
   return cudaGetLastError();
 }
 

@@ -5,114 +5,182 @@
 // Freeze re-organisation of the cache into a 4-bit stream, vertical-line rows
 // and a BF16 tail (§4.3 Eq. 8).
 //
-// A CTA builds one 64-row block image of the 4-bit stream in shared memory
-// (codes placed directly in the tensor-core fragment order documented in
-// hyq.h) and writes it out with 16-byte stores.  One warp quantises one
-// 128-element row: lane l holds elements 4l..4l+3, lanes 8q..8q+7 form group q.
+// A CTA builds one 64-row block of the 4-bit stream: the BF16 rows are staged
+// in shared memory with each group's min / max, one thread per group derives
+// the FP16 step and zero point, and each thread then assembles whole 32-bit
+// code words in the tensor-core fragment order documented in hyq.h and
+// stores them directly (no atomics, no float64).
 #include "hyq_common.cuh"
 
 namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr int kRows = HYQ_QBLOCK_ROWS;  // 64 stream rows per block
+constexpr int kChunks = HYQ_D / 8;      // 16 chunks of 8 elements per row
 
-// Position of the nibble of (row tt of a 16-row tile, element e) in the K tile.
-__device__ __forceinline__ void k_nibble(int tt, int e, int& word, int& shift) {
-  int ks = e >> 4, c = e & 15;
-  int ch = c >> 3, t = (c & 7) >> 1, lo_hi = c & 1;
-  int g = tt & 7, rh = tt >> 3;
-  int n = rh + 2 * ch + 4 * lo_hi;
-  int lane = 4 * g + t;
-  word = (512 * (ks >> 2) + 16 * lane + 4 * (ks & 3)) >> 2;
-  shift = 4 * n;
+// Shared image of one 64-row block being built.
+struct BuildSmem {
+  __nv_bfloat16 x[2][kRows][HYQ_D];  // K and V rows (zero for padding / kept rows)
+  float mn[2][kRows][4], mx[2][kRows][4];
+  float s[2][kRows][4], z[2][kRows][4], r[2][kRows][4];
+  int32_t pos[kRows];      // source row of each slot, -1 for none
+  uint8_t keep[kRows];     // slot already holds a stream row (append)
+  uint8_t nan[2][kRows][4];
+};
+
+__device__ __forceinline__ uint32_t code_of(float x, float s, float z, float r) {
+  if (s == 0.f) return 0u;
+  float t = rintf(__fmul_rn(__fsub_rn(x, z), r));
+  t = fminf(fmaxf(t, 0.f), 15.f);
+  return (uint32_t)t;
 }
 
-// Same for the V tile (rows of the tensor-core A operand are elements).
-__device__ __forceinline__ void v_nibble(int tt, int e, int& word, int& shift) {
-  int mt = e >> 4, rr = e & 15;
-  int g = rr & 7, rh = rr >> 3;
-  int ch = tt >> 3, t = (tt & 7) >> 1, lo_hi = tt & 1;
-  int n = rh + 2 * ch + 4 * lo_hi;
-  int lane = 4 * g + t;
-  word = (512 * (mt >> 2) + 16 * lane + 4 * (mt & 3)) >> 2;
-  shift = 4 * n;
+__device__ __forceinline__ void unpack8(uint4 v, float (&f)[8]) {
+  const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 t = __bfloat1622float2(p[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
 }
 
-// Quantise one row held by a warp; returns this lane's 4 codes and the
-// (scale, zero) of its group as an FP16 pair (scale in the low half).
-__device__ __forceinline__ void quant_row(const float x[4], uint32_t c[4], uint32_t& sz,
-                                          bool& bad) {
-  float mn = fminf(fminf(x[0], x[1]), fminf(x[2], x[3]));
-  float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-  int nan = isnan(x[0]) | isnan(x[1]) | isnan(x[2]) | isnan(x[3]);
+// Build one 64-row block of the 4-bit stream at `dst` (10240 bytes, global).
+// sm.pos / sm.keep must be set.  Rows with keep = 1 keep their existing
+// codes and metadata; rows with pos < 0 become zero padding.
+__device__ void build_block(BuildSmem& sm, const __nv_bfloat16* kbase, const __nv_bfloat16* vbase,
+                            uint8_t* dst, bool any_keep, int32_t* err) {
+  const int tid = threadIdx.x;
+  // Pass 1: load the rows, per-group min / max (4 chunks of 8 per group are
+  // on 4 consecutive lanes).
+  for (int f = tid; f < 2 * kRows * kChunks; f += kThreads) {
+    const int T = f >> 10, row = (f >> 4) & (kRows - 1), c = f & (kChunks - 1);
+    const int32_t p = sm.pos[row];
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (p >= 0 && !sm.keep[row])
+      v = *reinterpret_cast<const uint4*>((T ? vbase : kbase) + (size_t)p * HYQ_D + 8 * c);
+    *reinterpret_cast<uint4*>(&sm.x[T][row][8 * c]) = v;
+    float e[8];
+    unpack8(v, e);
+    float mn = e[0], mx = e[0];
+    int nan = isnan(e[0]);
 #pragma unroll
-  for (int o = 1; o < 8; o <<= 1) {
-    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    nan |= __shfl_xor_sync(0xffffffffu, nan, o);
-  }
-  // s = (mx - mn) / 15 in float64, rounded up to FP16 (float64 -> float32 ->
-  // FP16, both rounding up, which equals one rounding up); z = FP16(mn), RN.
-  double q = ((double)mx - (double)mn) / 15.0;
-  __half s = __float2half_ru(__double2float_ru(q));
-  __half z = __float2half_rn(mn);
-  float s32 = __half2float(s), z32 = __half2float(z);
-  bad = nan || isinf(s32) || isinf(z32);
-  if (bad) {
-    s32 = 0.f;
-    s = __float2half_rn(0.f);
-    z = s;
-  }
-  if (s32 == 0.f) {
+    for (int i = 1; i < 8; ++i) {
+      mn = fminf(mn, e[i]);
+      mx = fmaxf(mx, e[i]);
+      nan |= isnan(e[i]);
+    }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) c[i] = 0;
-  } else {
-    float r = __frcp_rn(s32);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float t = rintf(__fmul_rn(__fsub_rn(x[i], z32), r));
-      t = fminf(fmaxf(t, 0.f), 15.f);
-      c[i] = (uint32_t)t;
+    for (int o = 1; o < 4; o <<= 1) {
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      nan |= __shfl_xor_sync(0xffffffffu, nan, o);
+    }
+    if ((c & 3) == 0) {
+      sm.mn[T][row][c >> 2] = mn;
+      sm.mx[T][row][c >> 2] = mx;
+      sm.nan[T][row][c >> 2] = (uint8_t)nan;
     }
   }
-  sz = (uint32_t)__half_as_ushort(s) | ((uint32_t)__half_as_ushort(z) << 16);
-}
-
-// Quantise K and V row `src_row` (or a zero padding row when src is null)
-// into slot `tau` (0..63) of the shared block image `img`.
-__device__ __forceinline__ void quant_into_block(uint32_t* img, int tau, const __nv_bfloat16* srck,
-                                                 const __nv_bfloat16* srcv, int lane, int32_t* err) {
-#pragma unroll
-  for (int tensor = 0; tensor < 2; ++tensor) {
-    const __nv_bfloat16* src = tensor ? srcv : srck;
-    uint2 raw = *reinterpret_cast<const uint2*>(src + 4 * lane);
-    __nv_bfloat162 p0 = *reinterpret_cast<__nv_bfloat162*>(&raw.x);
-    __nv_bfloat162 p1 = *reinterpret_cast<__nv_bfloat162*>(&raw.y);
-    float x[4] = {__low2float(p0), __high2float(p0), __low2float(p1), __high2float(p1)};
-    uint32_t c[4], sz;
-    bool bad;
-    quant_row(x, c, sz, bad);
-    if (bad && (lane & 7) == 0) hyq_set_err(err, HYQ_DEVERR_QUANT_RANGE);
-    int tile = tau >> 4, tt = tau & 15;
-    uint32_t* codes = img + ((tensor ? HYQ_VCODE_OFF : 0) + tile * HYQ_TILE_BYTES) / 4;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      int w, sh;
-      if (tensor) v_nibble(tt, 4 * lane + i, w, sh);
-      else k_nibble(tt, 4 * lane + i, w, sh);
-      if (c[i]) atomicOr(codes + w, c[i] << sh);
+  __syncthreads();
+  // Pass 2: one thread per group: step s = smallest FP16 with 15 s >= mx - mn
+  // (the subtraction, the division and the FP16 conversion all round up,
+  // which gives exactly that value); zero z = FP16(mn) to nearest.
+  for (int i = tid; i < 2 * kRows * 4; i += kThreads) {
+    const int T = i >> 8, row = (i >> 2) & (kRows - 1), q = i & 3;
+    if (sm.keep[row]) continue;
+    const float mn = sm.mn[T][row][q], mx = sm.mx[T][row][q];
+    __half sh = __float2half_ru(__fdiv_ru(__fsub_ru(mx, mn), 15.f));
+    __half zh = __float2half_rn(mn);
+    float s32 = __half2float(sh), z32 = __half2float(zh);
+    if (sm.nan[T][row][q] || isinf(s32) || isinf(z32)) {
+      hyq_set_err(err, HYQ_DEVERR_QUANT_RANGE);
+      sh = zh = __float2half_rn(0.f);
+      s32 = z32 = 0.f;
     }
-    if ((lane & 7) == 0) {
-      uint32_t* meta = img + ((tensor ? HYQ_VMETA_OFF : HYQ_KMETA_OFF) + tau * 16) / 4;
-      meta[lane >> 3] = sz;
-    }
+    sm.s[T][row][q] = s32;
+    sm.z[T][row][q] = z32;
+    sm.r[T][row][q] = s32 > 0.f ? __frcp_rn(s32) : 0.f;
+    const uint32_t w = (uint32_t)__half_as_ushort(sh) | ((uint32_t)__half_as_ushort(zh) << 16);
+    *reinterpret_cast<uint32_t*>(dst + (row >> 4) * HYQ_QTILE_BYTES + 2048 + T * 256 + (row & 15) * 16 + 4 * q) = w;
   }
-}
-
-__device__ __forceinline__ void store_block(uint8_t* dst, const uint32_t* img) {
-  const uint4* s = reinterpret_cast<const uint4*>(img);
-  uint4* d = reinterpret_cast<uint4*>(dst);
-  for (int i = threadIdx.x; i < HYQ_QBLOCK_BYTES / 16; i += kThreads) d[i] = s[i];
+  __syncthreads();
+  // Pass 3a: K code words.  Job (tile, g, chunk cc): rows g and g+8 of the
+  // tile, elements 8cc..8cc+7 -> the two words u = 2(cc/4) + {0,1} of lane 4g + cc%4.
+  for (int j = tid; j < 4 * 8 * kChunks; j += kThreads) {
+    const int tile = j >> 7, g = (j >> 4) & 7, cc = j & 15;
+    const int q = cc >> 2, t = cc & 3;
+    uint8_t* wp = dst + tile * HYQ_QTILE_BYTES + 512 * (cc >> 3) + 16 * (4 * g + t) + 4 * (2 * (q & 1));
+    uint32_t w[2] = {0u, 0u};
+    uint2 old = make_uint2(0, 0);
+    if (any_keep) old = *reinterpret_cast<const uint2*>(wp);
+#pragma unroll
+    for (int a = 0; a < 2; ++a) {
+      const int row = 16 * tile + g + 8 * a;
+      if (sm.keep[row]) {
+        const uint32_t mm = 0x0F0F0F0Fu << (4 * a);  // this row's nibbles a + 2b + 4c
+        w[0] |= old.x & mm;
+        w[1] |= old.y & mm;
+        continue;
+      }
+      float e[8];
+      unpack8(*reinterpret_cast<const uint4*>(&sm.x[0][row][8 * cc]), e);
+      const float s = sm.s[0][row][q], z = sm.z[0][row][q], r = sm.r[0][row][q];
+#pragma unroll
+      for (int sub = 0; sub < 2; ++sub)
+#pragma unroll
+        for (int b = 0; b < 2; ++b)
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+            w[sub] |= code_of(e[4 * sub + 2 * b + c], s, z, r) << (4 * (a + 2 * b + 4 * c));
+    }
+    *reinterpret_cast<uint2*>(wp) = make_uint2(w[0], w[1]);
+  }
+  // Pass 3b: V code words.  Job (tile, t, chunk cc): rows 2t + 8b + c,
+  // elements 8cc..8cc+7 = 32q + 4g + 2s + a with q = cc/4 and g = 2(cc%4) + gl
+  // -> the words (lane 4g + t, u = 2q + s) for gl, s in {0, 1}; the two s
+  // words of one lane are adjacent.
+  for (int j = tid; j < 4 * 4 * kChunks; j += kThreads) {
+    const int tile = j >> 6, t = (j >> 4) & 3, cc = j & 15;
+    const int q = cc >> 2;
+    uint8_t* wp[2];
+    uint32_t w[2][2] = {{0u, 0u}, {0u, 0u}};
+    uint2 old[2] = {make_uint2(0, 0), make_uint2(0, 0)};
+#pragma unroll
+    for (int gl = 0; gl < 2; ++gl) {
+      const int g = 2 * (cc & 3) + gl;
+      wp[gl] = dst + tile * HYQ_QTILE_BYTES + 1024 + 512 * (cc >> 3) + 16 * (4 * g + t) + 8 * (q & 1);
+      if (any_keep) old[gl] = *reinterpret_cast<const uint2*>(wp[gl]);
+    }
+#pragma unroll
+    for (int b = 0; b < 2; ++b)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int row = 16 * tile + 2 * t + 8 * b + c;
+        if (sm.keep[row]) {
+          const uint32_t mm = 0xFFu << (4 * (2 * b + 4 * c));  // nibbles a + 2b + 4c, a = 0, 1
+#pragma unroll
+          for (int gl = 0; gl < 2; ++gl) {
+            w[gl][0] |= old[gl].x & mm;
+            w[gl][1] |= old[gl].y & mm;
+          }
+          continue;
+        }
+        float e[8];
+        unpack8(*reinterpret_cast<const uint4*>(&sm.x[1][row][8 * cc]), e);
+        const float s = sm.s[1][row][q], z = sm.z[1][row][q], r = sm.r[1][row][q];
+#pragma unroll
+        for (int gl = 0; gl < 2; ++gl)
+#pragma unroll
+          for (int ss = 0; ss < 2; ++ss)
+#pragma unroll
+            for (int a = 0; a < 2; ++a)
+              w[gl][ss] |= code_of(e[4 * gl + 2 * ss + a], s, z, r) << (4 * (a + 2 * b + 4 * c));
+      }
+#pragma unroll
+    for (int gl = 0; gl < 2; ++gl) *reinterpret_cast<uint2*>(wp[gl]) = make_uint2(w[gl][0], w[gl][1]);
+  }
 }
 
 // Source position of stream row r: the r-th position of [0, P) not in idx
@@ -128,20 +196,18 @@ __device__ __forceinline__ int32_t stream_pos(int32_t r, const int32_t* idx, int
   return r + lo;
 }
 
-// grid (nblocks of the new stream, HKV, B)
+// grid (blocks of the new stream, HKV, B)
 __global__ void __launch_bounds__(kThreads) rebuild_blocks_kernel(
     const __nv_bfloat16* __restrict__ k_src, const __nv_bfloat16* __restrict__ v_src, int32_t ld,
     int32_t P, const int32_t* __restrict__ idx, int32_t k, uint8_t* __restrict__ qblocks,
     int32_t nblk_cap, int32_t* err) {
-  __shared__ __align__(16) uint32_t img[HYQ_QBLOCK_BYTES / 4];
-  __shared__ int32_t pos[HYQ_QBLOCK_ROWS];
+  __shared__ __align__(16) BuildSmem sm;
   const int bi = blockIdx.x, h = blockIdx.y, b = blockIdx.z, HKV = gridDim.y;
   const size_t bh = (size_t)b * HKV + h;
   const int32_t nq = P - k;
   const int32_t* idx_bh = idx ? idx + bh * k : nullptr;
-  for (int i = threadIdx.x; i < HYQ_QBLOCK_BYTES / 4; i += kThreads) img[i] = 0;
-  if (threadIdx.x < HYQ_QBLOCK_ROWS) {
-    int32_t r = bi * HYQ_QBLOCK_ROWS + threadIdx.x;
+  if (threadIdx.x < kRows) {
+    const int32_t r = bi * kRows + threadIdx.x;
     int32_t p = -1;
     if (r < nq) {
       p = k > 0 ? stream_pos(r, idx_bh, k) : r;
@@ -150,19 +216,12 @@ __global__ void __launch_bounds__(kThreads) rebuild_blocks_kernel(
         p = min(max(p, 0), P - 1);
       }
     }
-    pos[threadIdx.x] = p;
+    sm.pos[threadIdx.x] = p;
+    sm.keep[threadIdx.x] = 0;
   }
   __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const __nv_bfloat16* kb = k_src + bh * ld * HYQ_D;
-  const __nv_bfloat16* vb = v_src + bh * ld * HYQ_D;
-  for (int tau = warp; tau < HYQ_QBLOCK_ROWS; tau += kWarps) {
-    int32_t p = pos[tau];
-    if (p < 0) continue;  // padding row: zero codes, zero metadata
-    quant_into_block(img, tau, kb + (size_t)p * HYQ_D, vb + (size_t)p * HYQ_D, lane, err);
-  }
-  __syncthreads();
-  store_block(qblocks + (bh * nblk_cap + bi) * HYQ_QBLOCK_BYTES, img);
+  build_block(sm, k_src + bh * ld * HYQ_D, v_src + bh * ld * HYQ_D,
+              qblocks + (bh * nblk_cap + bi) * (size_t)HYQ_QBLOCK_BYTES, false, err);
 }
 
 // Vertical-line gather, BF16 tail copy and counters.  One warp per row:
@@ -212,11 +271,11 @@ __global__ void __launch_bounds__(kThreads) rebuild_gather_kernel(
 __global__ void __launch_bounds__(kThreads) append_blocks_kernel(
     const __nv_bfloat16* __restrict__ k_rows, const __nv_bfloat16* __restrict__ v_rows, int32_t n,
     hyq_layout lay, int32_t nblk_cap) {
-  __shared__ __align__(16) uint32_t img[HYQ_QBLOCK_BYTES / 4];
+  __shared__ __align__(16) BuildSmem sm;
   const int h = blockIdx.y, b = blockIdx.z, HKV = gridDim.y;
   const size_t bh = (size_t)b * HKV + h;
   const int32_t nq0 = lay.counts[(size_t)b * HYQ_COUNTS + HYQ_CNT_NQ];
-  const int32_t cap_rows = nblk_cap * HYQ_QBLOCK_ROWS;
+  const int32_t cap_rows = nblk_cap * kRows;
   if (nq0 < 0 || nq0 > cap_rows) {
     if (threadIdx.x == 0) hyq_set_err(lay.err, HYQ_DEVERR_COUNT);
     return;
@@ -224,26 +283,16 @@ __global__ void __launch_bounds__(kThreads) append_blocks_kernel(
   const int32_t end = min(nq0 + n, cap_rows);
   if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0 && nq0 + n > cap_rows)
     hyq_set_err(lay.err, HYQ_DEVERR_COUNT);
-  const int32_t bi = nq0 / HYQ_QBLOCK_ROWS + blockIdx.x;
-  const int32_t r0 = max(bi * HYQ_QBLOCK_ROWS, nq0);
-  const int32_t r1 = min((bi + 1) * HYQ_QBLOCK_ROWS, end);
-  if (r0 >= r1) return;
-  uint8_t* dst = lay.qblocks + (bh * nblk_cap + bi) * HYQ_QBLOCK_BYTES;
-  if (bi * HYQ_QBLOCK_ROWS < nq0) {
-    const uint4* s = reinterpret_cast<const uint4*>(dst);
-    uint4* d = reinterpret_cast<uint4*>(img);
-    for (int i = threadIdx.x; i < HYQ_QBLOCK_BYTES / 16; i += kThreads) d[i] = s[i];
-  } else {
-    for (int i = threadIdx.x; i < HYQ_QBLOCK_BYTES / 4; i += kThreads) img[i] = 0;
+  const int32_t bi = nq0 / kRows + blockIdx.x;
+  if (max(bi * kRows, nq0) >= min((bi + 1) * kRows, end)) return;  // uniform across the block
+  if (threadIdx.x < kRows) {
+    const int32_t row = bi * kRows + threadIdx.x;
+    sm.keep[threadIdx.x] = row < nq0;
+    sm.pos[threadIdx.x] = (row >= nq0 && row < end) ? row - nq0 : -1;
   }
   __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int32_t r = r0 + warp; r < r1; r += kWarps) {
-    size_t src = (bh * n + (r - nq0)) * HYQ_D;
-    quant_into_block(img, r - bi * HYQ_QBLOCK_ROWS, k_rows + src, v_rows + src, lane, lay.err);
-  }
-  __syncthreads();
-  store_block(dst, img);
+  build_block(sm, k_rows + bh * n * HYQ_D, v_rows + bh * n * HYQ_D,
+              lay.qblocks + (bh * nblk_cap + bi) * (size_t)HYQ_QBLOCK_BYTES, bi * kRows < nq0, lay.err);
 }
 
 __global__ void append_counts_kernel(hyq_layout lay, int32_t n, int32_t cap_rows) {

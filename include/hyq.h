@@ -69,29 +69,34 @@ typedef struct {
 } hyq_config;
 
 /*
- * 4-bit block format.  The 4-bit stream of one (batch, KV head) is an array of
- * blocks of HYQ_QBLOCK_ROWS consecutive stream rows, HYQ_QBLOCK_BYTES each:
+ * 4-bit stream format.  The 4-bit stream of one (batch, KV head) is an array
+ * of 16-row tiles of HYQ_QTILE_BYTES each, tile i holding stream rows
+ * 16i..16i+15; four consecutive tiles form a block of HYQ_QBLOCK_ROWS rows,
+ * the unit the stream is allocated in.  A tile is
  *
- *   [0,    4096)  K codes: four 16-row tiles of 1024 bytes
- *   [4096, 8192)  V codes: four 16-row tiles of 1024 bytes
- *   [8192, 9216)  K metadata: 64 rows x 4 groups x (scale, zero) FP16 pairs
- *   [9216,10240)  V metadata: same
+ *   [0,    1024)  K codes
+ *   [1024, 2048)  V codes
+ *   [2048, 2304)  K metadata: 16 rows x 4 groups x (scale, zero) FP16 pairs
+ *   [2304, 2560)  V metadata: same
  *
- * Metadata entry (row r, group q) of a block lives at byte 16*r + 4*q of its
- * region: scale s then zero z.  The dequantised value of element e of group
- * q is c * s + z with c the 4-bit code.
+ * Metadata entry (row r, group q) lives at byte 16*r + 4*q of its region:
+ * scale s then zero z.  The dequantised value of element e (group q = e/32)
+ * is c * s + z with c the 4-bit code.
  *
- * Inside a 1024-byte code tile (16 rows, 128 elements) the codes are ordered
- * for the register fragments of a 16x16 tensor-core tile: byte offset
- *   512*(u/4) + 16*lane + 4*(u%4)
+ * Inside a 1024-byte code region the 16 x 128 codes are ordered for the
+ * register fragments of 16x16 tensor-core tiles: byte offset
+ *   512*(u/4) + 16*lane + 4*(u%4)          (u = 0..7, lane = 0..31)
  * holds a 32-bit word whose nibble n (bits 4n..4n+3, n = 0..7) is the code
- *   K tile: row (n&1 ? 8 : 0) + lane/4,  element 16*u + 2*(lane%4) + (n&2 ? 8 : 0) + (n>>2)
- *   V tile: row 2*(lane%4) + (n&2 ? 8 : 0) + (n>>2),  element 16*u + lane/4 + (n&1 ? 8 : 0)
- * for u = 0..7 and lane = 0..31.  Rows past the stream length inside the
- * last block have zero codes and zero metadata.
+ * of, with g = lane/4, t = lane%4, a = n&1, b = (n>>1)&1, c = n>>2,
+ *   K: row g + 8a,          element 8*(t + 4*(u/2)) + 4*(u%2) + 2b + c
+ *   V: row 2t + 8b + c,     element 32*(u/2) + 4g + 2*(u%2) + a
+ * Rows past the stream length inside the last block have zero codes and
+ * zero metadata.
  */
 #define HYQ_QBLOCK_ROWS 64
 #define HYQ_QBLOCK_BYTES 10240
+#define HYQ_QTILE_ROWS 16
+#define HYQ_QTILE_BYTES 2560
 
 /*
  * Device buffers of one layer's hybrid cache (§4.3 Eq. 8, Algorithm 4's four

@@ -8,9 +8,9 @@ form nor the rounding; the readings adopted here are:
 
 * groups are G = 32 consecutive elements along head_dim, for K and for V;
 * asymmetric affine form ``x ~ c * s + z`` with codes c in [0, 2^bits - 1];
-* ``s = RU_fp16((max - min) / (2^bits - 1))`` -- the division in float64,
-  the result rounded *up* to float16 so that the top code still reaches the
-  group maximum;
+* ``s`` = the smallest float16 value with ``(2^bits - 1) * s >= max - min``
+  in exact arithmetic: the step of the 2^bits-level grid rounded *up* to
+  float16, so that the top code still reaches the group maximum;
 * ``z = RN_fp16(min)``;
 * the code decision is taken in float32 (the kernel's precision):
   ``r = fl32(1 / s)``, ``c = clamp(rint(fl32(fl32(x - z) * r)), 0, qmax)``
@@ -44,6 +44,39 @@ def round_up_fp16(x: np.ndarray) -> np.ndarray:
     return h
 
 
+def min_step_fp16(mx, mn, qmax: int) -> np.ndarray:
+    """Smallest float16 h with qmax * h >= mx - mn, exactly (as float16).
+
+    A float64 quotient gives a candidate that is at most one float16 step
+    off; the candidate and its neighbours are then tested with the exact
+    sign of qmax*h - mx + mn (a three-term float64 sum, decided with
+    math.fsum where plain float64 arithmetic is not conclusive).
+    """
+    import math
+    mx = np.asarray(mx, dtype=np.float64)
+    mn = np.asarray(mn, dtype=np.float64)
+    with np.errstate(over="ignore", invalid="ignore"):
+        cand = round_up_fp16((mx - mn) / float(qmax))
+    h = cand.astype(np.float64)
+    lo = np.nextafter(cand, np.float16(-np.inf)).astype(np.float64)
+    hi = np.nextafter(cand, np.float16(np.inf)).astype(np.float64)
+
+    def covers(v):
+        """Exact test qmax*v - mx + mn >= 0 (qmax*v is exact in float64)."""
+        with np.errstate(over="ignore", invalid="ignore"):
+            r = (qmax * v - mx) + mn
+        bound = 4 * np.finfo(np.float64).eps * np.maximum.reduce(
+            [np.abs(qmax * v), np.abs(mx), np.abs(mn)])
+        out = r >= 0
+        unsure = ~(np.abs(r) > bound) & np.isfinite(v)
+        for i in zip(*np.nonzero(unsure)):
+            out[i] = math.fsum([qmax * float(v[i]), -float(mx[i]), float(mn[i])]) >= 0
+        return out | np.isinf(v) & (v > 0)
+
+    res = np.where(covers(lo) & (lo >= 0), lo, np.where(covers(h), h, hi))
+    return res.astype(np.float16)
+
+
 def quantize(x, bits: int = 4, group: int = GROUP):
     """Quantise rows of ``x`` (values exactly representable in BF16).
 
@@ -67,8 +100,8 @@ def quantize(x, bits: int = 4, group: int = GROUP):
         raise QuantRangeError("NaN input")
     mn = xg.min(axis=-1)
     mx = xg.max(axis=-1)
+    scale = min_step_fp16(mx, mn, qmax)
     with np.errstate(over="ignore", invalid="ignore"):
-        scale = round_up_fp16((mx - mn) / float(qmax))
         zero = mn.astype(np.float16)
     if not (np.isfinite(scale).all() and np.isfinite(zero).all()):
         raise QuantRangeError("group range exceeds the float16 metadata range")

@@ -149,10 +149,17 @@ def test_block_format_round_trip():
 
 
 def test_block_format_fragment_order_examples():
-    """Spot values of the documented tile order: the first word of lane 0
-    holds K rows 0/8 elements 0,1,8,9 and V rows 0,1,8,9 of element 0/8."""
+    """Spot values of the documented code order: the first word of lane 0
+    holds K rows 0/8 elements 0,1,2,3 and V rows 0,1,8,9 of elements 0/1;
+    lane 5 (g=1, t=1), u=3 holds K elements 8*(1+4)+4+.. = 44..47 of rows 1/9."""
     from hybrid_precision_quantized_gb300.cache import _tile_maps
     krow, kel, vrow, vel = _tile_maps()
     # nibble n of the word at byte 0: slot = 2*(n//2) + n%2 = n
-    assert [(krow[n], kel[n]) for n in range(8)] == [(0, 0), (8, 0), (0, 8), (8, 8), (0, 1), (8, 1), (0, 9), (8, 9)]
-    assert [(vrow[n], vel[n]) for n in range(8)] == [(0, 0), (0, 8), (8, 0), (8, 8), (1, 0), (1, 8), (9, 0), (9, 8)]
+    assert [(krow[n], kel[n]) for n in range(8)] == [(0, 0), (8, 0), (0, 2), (8, 2), (0, 1), (8, 1), (0, 3), (8, 3)]
+    assert [(vrow[n], vel[n]) for n in range(8)] == [(0, 0), (0, 1), (8, 0), (8, 1), (1, 0), (1, 1), (9, 0), (9, 1)]
+    base = 2 * (512 * 0 + 16 * 5 + 4 * 3)
+    assert [(krow[base + n], kel[base + n]) for n in range(8)] == [
+        (1, 44), (9, 44), (1, 46), (9, 46), (1, 45), (9, 45), (1, 47), (9, 47)]
+    # V: element 32*(3//2) + 4*1 + 2*(3%2) + a = 38 + a
+    assert [(vrow[base + n], vel[base + n]) for n in range(8)] == [
+        (2, 38), (2, 39), (10, 38), (10, 39), (3, 38), (3, 39), (11, 38), (11, 39)]

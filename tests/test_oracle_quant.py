@@ -59,13 +59,42 @@ def test_error_bound_half_step_over_contiguous_groups():
     assert np.all(err <= rng_ / 30.0 * (1 + 2 ** -9) + z_err + 1e-12)
 
 
-def test_grid_reaches_group_max_and_min():
+def _exact_min_step_check(x, s):
+    """s is the smallest float16 with 15 s >= max - min, in exact arithmetic."""
+    from fractions import Fraction
+    xs = x.reshape(-1, 4, 32)
+    sf = s.reshape(-1, 4)
+    for i in range(xs.shape[0]):
+        for q in range(4):
+            rng_ = Fraction(float(xs[i, q].max())) - Fraction(float(xs[i, q].min()))
+            h = sf[i, q]
+            assert 15 * Fraction(float(h)) >= rng_
+            if float(h) > 0:
+                below = np.nextafter(h, np.float16(-np.inf))
+                assert 15 * Fraction(float(below)) < rng_
+
+
+def test_step_is_smallest_fp16_covering_the_range():
     x = bf16_rows(3, 128)
     c, s, z = quantize(x)
+    _exact_min_step_check(x, s)
     xs = x.reshape(128, 4, 32)
-    top = 15 * s.astype(np.float64) + z.astype(np.float64)
-    assert np.all(top >= xs.max(-1) - 1e-12)
     assert np.all(z.astype(np.float64) <= xs.min(-1) + np.abs(xs.min(-1)) * 2 ** -11 + 1e-30)
+
+
+def test_step_is_exact_for_extreme_spans():
+    """Groups whose range is a tiny amount above 15 * (a float16 value): a
+    float64 quotient would round down onto that value, the exact step is the
+    next float16 up."""
+    rows = np.zeros((6, 128))
+    for i, (hi, tiny) in enumerate([(15.0, 2.0 ** -80), (7.5, 2.0 ** -90), (30.0, 2.0 ** -70),
+                                    (15.0, 0.0), (3.0, 2.0 ** -100), (1.5, 2.0 ** -60)]):
+        rows[i, 0] = hi
+        rows[i, 1] = -tiny          # min is a tiny negative bf16 value
+    c, s, z = quantize(rows)
+    _exact_min_step_check(rows, s)
+    assert float(s[0, 0]) == float(np.nextafter(np.float16(1.0), np.float16(2)))
+    assert float(s[3, 0]) == 1.0
 
 
 def test_ties_round_half_to_even():
