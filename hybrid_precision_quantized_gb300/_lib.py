@@ -36,7 +36,7 @@ OP_SELECT, OP_DECODE, OP_PREFILL = 1, 2, 3
 SYMBOLS = ("hyq_status_string", "hyq_config_check", "hyq_vl_count", "hyq_layout_sizes",
            "hyq_workspace_size", "hyq_layout_reset", "hyq_quantize_append",
            "hyq_select_vertical", "hyq_rebuild", "hyq_decode_append", "hyq_decode_attention",
-           "hyq_decode_attention_noalloc", "hyq_read_device_error")
+           "hyq_decode_attention_noalloc", "hyq_read_device_error", "hyq_set_decode_plan")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -92,6 +92,7 @@ def load() -> ctypes.CDLL:
         "hyq_decode_attention_noalloc": (c_int32, [P(HyqConfig), c_void_p, P(HyqLayout), c_void_p, c_int32,
                                                    c_void_p]),
         "hyq_read_device_error": (c_int32, [c_void_p, P(c_int32), c_void_p]),
+        "hyq_set_decode_plan": (c_int32, [c_int32, c_int32]),
     }
     for name in SYMBOLS:
         fn = getattr(lib, name)
@@ -197,6 +198,14 @@ def hyq_decode_attention_noalloc(cfg, q, lay: HyqLayout, out, len_hint: int = 0,
     GPU race on the shared scratch."""
     _check("hyq_decode_attention_noalloc", load().hyq_decode_attention_noalloc(
         ctypes.byref(cfg), ptr(q), ctypes.byref(lay), ptr(out), len_hint, stream_ptr(stream)))
+
+
+DECODE_PLAN_AUTO, DECODE_PLAN_DIRECT, DECODE_PLAN_CLUSTER, DECODE_PLAN_GLOBAL = range(4)
+
+
+def hyq_set_decode_plan(merge: int, splits: int = 0):
+    """Override the decode split / merge plan (process-wide); 0 = automatic."""
+    _check("hyq_set_decode_plan", load().hyq_set_decode_plan(merge, splits))
 
 
 def hyq_read_device_error(err_dev, stream=None) -> int:

@@ -10,9 +10,10 @@
 //   ring of bulk copies (TMA, no block-wide barrier in the main loop).  Each
 //   warp keeps one online-softmax state (m, l, acc) for the g query heads of
 //   the KV group, packed into one tensor-core tile (Algorithm 3, "pack g GQA
-//   heads").  The block merges its warps, writes one partial per split, and
-//   the last block to finish (an atomic ticket; nobody waits) merges the S
-//   partials by log-sum-exp rescaling (ReduceSoftmax) into the BF16 output.
+//   heads").  The block merges its warps; the S block partials are merged by
+//   log-sum-exp rescaling (ReduceSoftmax) either inside a thread-block
+//   cluster through distributed shared memory, or through the workspace by
+//   the last block to finish (an atomic ticket; nobody waits).
 //
 // 4-bit tiles are dequantised inside the dot products:
 //   q.k~  = sum_q s_q (q_q . c_q) + z_q sum(q_q)     (per group q of 32)
@@ -24,16 +25,25 @@
 // straight into fragment registers; the head_dim order of the K products and
 // of the V outputs is permuted (identically in both paths, see hyq.h) so that
 // those loads are 16- and 8-byte vectors.
+#include <cooperative_groups.h>
 #include <math.h>
 
 #include "hyq_common.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace {
 
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
-constexpr int kSlots = 4;                                     // tiles in flight per warp
-constexpr int kSmemBytes = kWarps * kSlots * HYQ_QTILE_BYTES; // 160 KiB ring
+constexpr int kSlots = 3;                                     // 4-bit tiles in flight per warp
+constexpr int kRingBytes = kWarps * kSlots * HYQ_QTILE_BYTES; // 120 KiB of rings
+// BF16 tiles staged in shared memory by bulk copies, one row per copy, with
+// padded row strides that make the fragment loads bank-conflict free.
+constexpr int kFKStride = 320, kFVStride = 272;
+constexpr int kFTileBytes = 16 * kFKStride + 16 * kFVStride;  // 9472
+constexpr int kFStaged = 7;                                     // staged BF16 tiles per block
+constexpr int kSmemBytes = kRingBytes + kFStaged * kFTileBytes;
 constexpr int kPart = 2 + HYQ_D;                              // m, l, acc[128] per head
 constexpr int kMaxSplits = 1024;
 // log2(e) / sqrt(128): logits are kept in the base-2 domain.
@@ -42,18 +52,51 @@ constexpr float kSubScale = 1.0f / HYQ_F16_SUB_SCALE;         // 2^-24
 
 size_t round_up(size_t x) { return (x + 255) / 256 * 256; }
 
-// Split count: about one block per SM over all (batch, KV head) pairs, and
-// not more blocks than there are 16-row tiles to share.
-int decode_split(const hyq_config* c, int32_t len) {
+// Merge modes of the split partials of one (batch, KV head):
+//   kDirect  S = 1: the block writes the output itself;
+//   kCluster the S blocks form a thread-block cluster and merge through
+//            distributed shared memory (no global traffic, no last-block tail);
+//   kGlobal  partials go to the workspace and the last block to finish (an
+//            atomic ticket; nobody waits) merges them.
+enum MergeMode { kDirect = 0, kCluster = 1, kGlobal = 2 };
+
+struct DecodePlan {
+  int S;     // blocks per (batch, KV head)
+  int mode;  // MergeMode
+};
+
+// About one block per SM over all (batch, KV head) pairs, and not more
+// blocks than there are 16-row tiles to share; one block per pair when even
+// two would not fit in one wave.
+int g_plan_merge = 0;   // hyq_set_decode_plan override (0 = automatic)
+int g_plan_splits = 0;
+
+DecodePlan decode_plan(const hyq_config* c, int32_t len) {
   const int bh = c->batch * c->num_kv_heads;
-  int S = (hyq_num_sms() + bh / 2) / bh;
+  const int sms = hyq_num_sms();
   int32_t P = len - c->window > 0 ? len - c->window : 0;
   int64_t tiles = (int64_t)(P + 15) / 16 + (hyq_vl_count(c, P) + hyq_cap_tail(c) + 15) / 16;
-  int64_t cap = tiles / 32;
-  if (S > cap) S = (int)cap;
-  if (S < 1) S = 1;
-  if (S > kMaxSplits) S = kMaxSplits;
-  return S;
+  int cap = (int)(tiles / 32 > 0 ? tiles / 32 : 1);
+  DecodePlan p;
+  if (g_plan_merge != 0) {
+    p.mode = g_plan_merge - 1;
+    p.S = p.mode == kDirect ? 1 : g_plan_splits;
+    return p;
+  }
+  if (2 * bh > sms || cap < 2) {  // even two blocks per pair would not fit in one wave
+    p.S = 1;
+    p.mode = kDirect;
+    return p;
+  }
+  // Measured on GB300 (152 SMs, 8 KV heads, 32K context): the workspace merge
+  // at one block per SM beats 16-block clusters, which cannot all be resident
+  // with a 185 KiB block each.
+  int S = (sms + bh / 2) / bh;
+  if (S > cap) S = cap;
+  if (S < 2) S = 2;
+  p.S = S;
+  p.mode = kGlobal;
+  return p;
 }
 
 struct State {
@@ -63,8 +106,12 @@ struct State {
 };
 
 // Online-softmax update of the two heads (2t, 2t+1) this thread owns with the
-// logits of tokens (g, g+8); returns the probabilities p[2r + j].
+// logits of tokens (g, g+8); returns the probabilities p[2r + j].  The
+// accumulators are rescaled only when some head's running max moved (the
+// factor is exactly 1 otherwise).
 __device__ __forceinline__ void softmax_update(const float (&lg)[4], State& st, float (&p)[4]) {
+  float corr[2];
+  bool moved = false;
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     float tm = fmaxf(lg[j], lg[2 + j]);
@@ -73,18 +120,24 @@ __device__ __forceinline__ void softmax_update(const float (&lg)[4], State& st, 
     tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 16));
     const float mn = fmaxf(st.m[j], tm);
     const float ms = (mn == -INFINITY) ? 0.f : mn;
-    const float corr = exp2f(st.m[j] - ms);
+    moved |= mn != st.m[j];
+    corr[j] = exp2f(st.m[j] - ms);
     p[j] = exp2f(lg[j] - ms);
     p[2 + j] = exp2f(lg[2 + j] - ms);
-    st.l[j] = fmaf(st.l[j], corr, p[j] + p[2 + j]);
+    st.l[j] = fmaf(st.l[j], corr[j], p[j] + p[2 + j]);
     st.m[j] = mn;
+  }
+  if (__any_sync(0xffffffffu, moved)) {
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      st.acc[mt][j] *= corr;
-      st.acc[mt][2 + j] *= corr;
+    for (int j = 0; j < 2; ++j) {
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        st.acc[mt][j] *= corr[j];
+        st.acc[mt][2 + j] *= corr[j];
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) st.zacc[j][q] *= corr[j];
     }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) st.zacc[j][q] *= corr;
   }
 }
 
@@ -209,6 +262,55 @@ __device__ __forceinline__ void f_tile(const __nv_bfloat16* vlk, const __nv_bflo
   }
 }
 
+// The same BF16 tile from shared memory (K rows at stride kFKStride, V rows
+// at kFVStride); rows at or past `vr` are masked (their contents are undefined).
+__device__ __forceinline__ void f_tile_smem(const uint8_t* Ks, const uint8_t* Vs, int vr, int lane,
+                                            const uint32_t (&bq)[8][2], State& st) {
+  const int g = lane >> 2, t = lane & 3;
+  float S[4] = {0.f, 0.f, 0.f, 0.f};
+  {
+    uint4 ka[2][4];
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        ka[a][j] = *reinterpret_cast<const uint4*>(Ks + (g + 8 * a) * kFKStride + 16 * (t + 4 * j));
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const int j = ks >> 1, sub = ks & 1;
+      mma_bf16(S, u4c(ka[0][j], 2 * sub), u4c(ka[1][j], 2 * sub), u4c(ka[0][j], 2 * sub + 1),
+               u4c(ka[1][j], 2 * sub + 1), bq[ks][0], bq[ks][1]);
+    }
+  }
+  float lg[4];
+  lg[0] = g < vr ? S[0] * kScale : -INFINITY;
+  lg[1] = g < vr ? S[1] * kScale : -INFINITY;
+  lg[2] = g + 8 < vr ? S[2] * kScale : -INFINITY;
+  lg[3] = g + 8 < vr ? S[3] * kScale : -INFINITY;
+  float p[4];
+  softmax_update(lg, st, p);
+  const uint32_t b0 = movmatrix_trans(pack_bf16x2(p[0] * kSubScale, p[1] * kSubScale));
+  const uint32_t b1 = movmatrix_trans(pack_bf16x2(p[2] * kSubScale, p[3] * kSubScale));
+  uint2 va[4][4];
+#pragma unroll
+  for (int tk4 = 0; tk4 < 4; ++tk4) {
+    const int rr = 2 * t + 8 * (tk4 >> 1) + (tk4 & 1);
+#pragma unroll
+    for (int G = 0; G < 4; ++G)
+      va[tk4][G] = rr < vr ? *reinterpret_cast<const uint2*>(Vs + rr * kFVStride + 2 * (32 * G + 4 * g))
+                           : make_uint2(0, 0);
+  }
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int G = u >> 1, s2 = u & 1;
+    const uint32_t w0 = s2 ? va[0][G].y : va[0][G].x, w1 = s2 ? va[1][G].y : va[1][G].x;
+    const uint32_t w2 = s2 ? va[2][G].y : va[2][G].x, w3 = s2 ? va[3][G].y : va[3][G].x;
+    mma_bf16(st.acc[u], __byte_perm(w0, w1, 0x5410), __byte_perm(w0, w1, 0x7632),
+             __byte_perm(w2, w3, 0x5410), __byte_perm(w2, w3, 0x7632), b0, b1);
+  }
+}
+
+template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
     const __nv_bfloat16* __restrict__ q, hyq_layout lay, __nv_bfloat16* __restrict__ out,
     int32_t* __restrict__ tickets, float* __restrict__ part, int HQ, int gq, int nblk_cap,
@@ -217,6 +319,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
   __shared__ __align__(16) __nv_bfloat16 q_s[HYQ_MAX_GQA * HYQ_D];
   __shared__ float qsum_s[HYQ_MAX_GQA * 4];
   __shared__ __align__(8) uint64_t bars[kWarps * kSlots];
+  __shared__ __align__(8) uint64_t fbars[kFStaged];
+  __shared__ __align__(8) uint64_t qbar;
   __shared__ float red_m[kWarps][HYQ_MAX_GQA], red_l[kWarps][HYQ_MAX_GQA], wts[kWarps][HYQ_MAX_GQA];
   __shared__ float sM[HYQ_MAX_GQA], sL[HYQ_MAX_GQA];
   __shared__ int s_flag;
@@ -225,6 +329,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
   const size_t bh = (size_t)b * HKV + h;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
 
+  // The query rows of the KV group go first in this SM's copy queue.
+  if (tid == 0) {
+    mbar_init(&qbar, 1);
+    mbar_fence_init();
+    mbar_arrive_expect_tx(&qbar, gq * HYQ_D * 2);
+    bulk_g2s(q_s, q + ((size_t)b * HQ + (size_t)h * gq) * HYQ_D, gq * HYQ_D * 2, &qbar);
+  }
   const int32_t* cnt = lay.counts + (size_t)b * HYQ_COUNTS;
   int32_t nq = cnt[HYQ_CNT_NQ], nvl = cnt[HYQ_CNT_NVL], ntail = cnt[HYQ_CNT_NTAIL];
   if (nq < 0 || nq > nblk_cap * HYQ_QBLOCK_ROWS || nvl < 0 || nvl > cap_vl || ntail < 0 || ntail > cap_tail) {
@@ -245,25 +356,43 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
   const uint8_t* tiles = lay.qblocks + bh * (size_t)nblk_cap * HYQ_QBLOCK_BYTES;
   uint8_t* ring = smem + warp * kSlots * HYQ_QTILE_BYTES;
   uint64_t* wb = bars + warp * kSlots;
-
+  const __nv_bfloat16* vlk = static_cast<const __nv_bfloat16*>(lay.vl_k) + bh * cap_vl * HYQ_D;
+  const __nv_bfloat16* vlv = static_cast<const __nv_bfloat16*>(lay.vl_v) + bh * cap_vl * HYQ_D;
+  const __nv_bfloat16* tk = static_cast<const __nv_bfloat16*>(lay.tail_k) + bh * cap_tail * HYQ_D;
+  const __nv_bfloat16* tv = static_cast<const __nv_bfloat16*>(lay.tail_v) + bh * cap_tail * HYQ_D;
+  // The first kFStaged BF16 tiles of this block are fetched by bulk copies,
+  // one row per lane, by the warp that will use them (before its 4-bit ring).
+  const int n_staged = min(f1 - f0, kFStaged);
+  uint8_t* fstage = smem + kRingBytes + warp * kFTileBytes;
+  if (warp < n_staged) {
+    const int row0 = 16 * (f0 + warp), nrows = min(16, nf - row0);
+    if (lane == 0) {
+      mbar_init(&fbars[warp], 1);
+      mbar_fence_init();
+      mbar_arrive_expect_tx(&fbars[warp], nrows * 2 * HYQ_D * 2);
+    }
+    __syncwarp();
+    const int rr = lane & 15, row = row0 + rr;
+    if (rr < nrows) {
+      const bool v = lane >= 16;
+      const __nv_bfloat16* src = row < nvl ? (v ? vlv : vlk) + (size_t)row * HYQ_D
+                                           : (v ? tv : tk) + (size_t)(row - nvl) * HYQ_D;
+      bulk_g2s(fstage + (v ? 16 * kFKStride + rr * kFVStride : rr * kFKStride), src, HYQ_D * 2, &fbars[warp]);
+    }
+  }
   if (lane == 0) {
     for (int i = 0; i < kSlots; ++i) mbar_init(&wb[i], 1);
     mbar_fence_init();
-    // Start this warp's 4-bit stream right away.
     for (int j = 0; j < nj && j < kSlots; ++j) {
       mbar_arrive_expect_tx(&wb[j], HYQ_QTILE_BYTES);
       bulk_g2s(ring + j * HYQ_QTILE_BYTES, tiles + (size_t)(t0 + my0 + kWarps * j) * HYQ_QTILE_BYTES,
                HYQ_QTILE_BYTES, &wb[j]);
     }
   }
-  // Query tile of the KV group (rows past g are zero) and its per-group sums.
-  for (int i = tid; i < HYQ_MAX_GQA * HYQ_D / 8; i += kThreads) {
-    const int row = i >> 4, c8 = i & 15;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (row < gq) v = *reinterpret_cast<const uint4*>(q + ((size_t)b * HQ + (size_t)h * gq + row) * HYQ_D + 8 * c8);
-    *reinterpret_cast<uint4*>(q_s + row * HYQ_D + 8 * c8) = v;
-  }
+  for (int i = gq * HYQ_D / 8 + tid; i < HYQ_MAX_GQA * HYQ_D / 8; i += kThreads)
+    reinterpret_cast<uint4*>(q_s)[i] = make_uint4(0, 0, 0, 0);  // query rows past g
   __syncthreads();
+  if (!mbar_wait(&qbar, 0) && tid == 0) hyq_set_err(lay.err, HYQ_DEVERR_TIMEOUT);
   if (tid < 32) {
     float sacc = 0.f;
     const __nv_bfloat16* r = q_s + (tid >> 2) * HYQ_D + 32 * (tid & 3);
@@ -295,23 +424,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
   for (int j = 0; j < 2; ++j) st.zacc[j][0] = st.zacc[j][1] = st.zacc[j][2] = st.zacc[j][3] = 0.f;
 
   // ---- BF16 tiles (vertical-line rows, then the tail) ----------------------
-  {
-    const __nv_bfloat16* vlk = static_cast<const __nv_bfloat16*>(lay.vl_k) + bh * cap_vl * HYQ_D;
-    const __nv_bfloat16* vlv = static_cast<const __nv_bfloat16*>(lay.vl_v) + bh * cap_vl * HYQ_D;
-    const __nv_bfloat16* tk = static_cast<const __nv_bfloat16*>(lay.tail_k) + bh * cap_tail * HYQ_D;
-    const __nv_bfloat16* tv = static_cast<const __nv_bfloat16*>(lay.tail_v) + bh * cap_tail * HYQ_D;
-    for (int fi = f0 + warp; fi < f1; fi += kWarps)
-      f_tile(vlk, vlv, tk, tv, nvl, 16 * fi, min(16, nf - 16 * fi), lane, bq, st);
+  if (warp < n_staged) {
+    const bool ok = mbar_wait(&fbars[warp], 0);
+    if (__any_sync(0xffffffffu, !ok)) {
+      if (lane == 0) {
+        hyq_set_err(lay.err, HYQ_DEVERR_TIMEOUT);
+        (void)mbar_wait(&fbars[warp], 0);
+      }
+      __syncwarp();
+    } else {
+      f_tile_smem(fstage, fstage + 16 * kFKStride, min(16, nf - 16 * (f0 + warp)), lane, bq, st);
+    }
   }
+  for (int fi = f0 + kFStaged + warp; fi < f1; fi += kWarps)  // tiles past the staged ones
+    f_tile(vlk, vlv, tk, tv, nvl, 16 * fi, min(16, nf - 16 * fi), lane, bq, st);
   // ---- 4-bit tiles through the warp's ring ---------------------------------
-  bool timed_out = false;
   for (int j = 0; j < nj; ++j) {
     const int slot = j % kSlots;
     const bool ok = mbar_wait(&wb[slot], (j / kSlots) & 1);
     if (__any_sync(0xffffffffu, !ok)) {
       // A copy did not arrive: flag it, and make sure none of this warp's
-      // copies is still in flight before the ring is reused below.
-      timed_out = true;
+      // copies is still in flight before shared memory is reused below.
       if (lane == 0) {
         hyq_set_err(lay.err, HYQ_DEVERR_TIMEOUT);
         for (int jj = j; jj < nj && jj < j + kSlots; ++jj) (void)mbar_wait(&wb[jj % kSlots], (jj / kSlots) & 1);
@@ -329,9 +462,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
                HYQ_QTILE_BYTES, &wb[slot]);
     }
   }
-  (void)timed_out;
 
-  // ---- warp partials -> block partial --------------------------------------
+  // ---- warp partials -> block partial (m, l, acc) in shared memory ---------
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
 #pragma unroll
@@ -342,7 +474,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
       for (int o = 4; o < 32; o <<= 1) st.zacc[j][qq] += __shfl_xor_sync(0xffffffffu, st.zacc[j][qq], o);
   }
   __syncthreads();  // every warp is done with its ring: reuse shared memory
-  float* red = reinterpret_cast<float*>(smem);  // [warp][head][128]
+  float* red = reinterpret_cast<float*>(smem);                    // [warp][head][128]
+  float* blk = red + kWarps * HYQ_MAX_GQA * HYQ_D;                  // [head][2 + 128]
   // Accumulator (m-tile u, ci) of thread (g, t): element 32(u/2) + 4g + 2(u%2)
   // + (ci >> 1), head 2t + (ci & 1).
 #pragma unroll
@@ -358,7 +491,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
       red_l[warp][2 * t + j] = st.l[j];
     }
   __syncthreads();
-  float* pp = part + (bh * S + split) * (size_t)(HYQ_MAX_GQA * kPart);
   if (tid < gq) {
     float M = -INFINITY;
     for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w][tid]);
@@ -369,8 +501,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
       wts[w][tid] = wt;
       Lsum = fmaf(red_l[w][tid], wt, Lsum);
     }
-    pp[tid * kPart + 0] = M;
-    pp[tid * kPart + 1] = Lsum;
+    blk[tid * kPart + 0] = M;
+    blk[tid * kPart + 1] = Lsum;
   }
   __syncthreads();
   for (int i = tid; i < gq * HYQ_D; i += kThreads) {
@@ -378,18 +510,70 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
     float a = 0.f;
 #pragma unroll 4
     for (int w = 0; w < kWarps; ++w) a = fmaf(red[(w * HYQ_MAX_GQA + hd) * HYQ_D + d], wts[w][hd], a);
-    pp[hd * kPart + 2 + d] = a;
+    if (kMode == kDirect) {
+      const float Lh = blk[hd * kPart + 1];
+      out[((size_t)b * HQ + (size_t)h * gq + hd) * HYQ_D + d] = __float2bfloat16_rn(Lh > 0.f ? a / Lh : 0.f);
+    } else {
+      blk[hd * kPart + 2 + d] = a;
+    }
   }
+  if (kMode == kDirect) return;
+
+  if (kMode == kCluster) {
+    // ---- ReduceSoftmax across the cluster through distributed shared memory
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();  // every block's partial is in its shared memory
+    float* rm = red;                         // [S][8] remote m, then weights
+    float* rl = red + 16 * HYQ_MAX_GQA;      // [S][8] remote l
+    for (int i = tid; i < S * gq; i += kThreads) {
+      const int r = i / gq, hd = i % gq;
+      const float* rb = cluster.map_shared_rank(blk, r);
+      rm[r * HYQ_MAX_GQA + hd] = rb[hd * kPart + 0];
+      rl[r * HYQ_MAX_GQA + hd] = rb[hd * kPart + 1];
+    }
+    __syncthreads();
+    if (tid < gq) {
+      float M = -INFINITY;
+      for (int r = 0; r < S; ++r) M = fmaxf(M, rm[r * HYQ_MAX_GQA + tid]);
+      const float Ms = (M == -INFINITY) ? 0.f : M;
+      float Lsum = 0.f;
+      for (int r = 0; r < S; ++r) {
+        const float wt = exp2f(rm[r * HYQ_MAX_GQA + tid] - Ms);
+        rm[r * HYQ_MAX_GQA + tid] = wt;
+        Lsum = fmaf(rl[r * HYQ_MAX_GQA + tid], wt, Lsum);
+      }
+      sL[tid] = Lsum;
+    }
+    __syncthreads();
+    // Block `split` of the cluster writes its share of the (head, element) outputs.
+    const int items = gq * HYQ_D, per = (items + S - 1) / S;
+    for (int i = split * per + tid; i < min(items, (split + 1) * per); i += kThreads) {
+      const int hd = i >> 7, d = i & (HYQ_D - 1);
+      float a = 0.f;
+#pragma unroll 4
+      for (int r = 0; r < S; ++r) {
+        const float* rb = cluster.map_shared_rank(blk, r);
+        a = fmaf(rb[hd * kPart + 2 + d], rm[r * HYQ_MAX_GQA + hd], a);
+      }
+      const float Lh = sL[hd];
+      out[((size_t)b * HQ + (size_t)h * gq + hd) * HYQ_D + d] = __float2bfloat16_rn(Lh > 0.f ? a / Lh : 0.f);
+    }
+    cluster.sync();  // no block leaves while another still reads its shared memory
+    return;
+  }
+
+  // ---- kGlobal: partials to the workspace, the last block merges -----------
+  __syncthreads();  // blk was written by other threads
+  float* pp = part + (bh * S + split) * (size_t)(HYQ_MAX_GQA * kPart);
+  for (int i = tid; i < gq * kPart; i += kThreads) pp[i] = blk[i];
   __threadfence();
   __syncthreads();
   if (tid == 0) s_flag = (atomicAdd(&tickets[bh], 1) == S - 1);
   __syncthreads();
   if (!s_flag) return;
   __threadfence();
-
-  // ---- last block of this (batch, KV head): ReduceSoftmax over S splits ----
   const float* pb = part + bh * S * (size_t)(HYQ_MAX_GQA * kPart);
-  float* sm_m = red;                         // [S][8]
+  float* sm_m = red;                             // [S][8]
   float* sm_w = red + kMaxSplits * HYQ_MAX_GQA;  // [S][8]
   for (int i = tid; i < S * gq; i += kThreads) {
     const int s2 = i / gq, hd = i % gq;
@@ -405,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
     for (int s2 = 0; s2 < S; ++s2) {
       const float wt = exp2f(sm_m[s2 * HYQ_MAX_GQA + tid] - Ms);
       Lsum = fmaf(sm_w[s2 * HYQ_MAX_GQA + tid], wt, Lsum);
-      sm_w[s2 * HYQ_MAX_GQA + tid] = wt;     // l_s no longer needed: keep the weight
+      sm_w[s2 * HYQ_MAX_GQA + tid] = wt;
     }
     sM[tid] = Ms;
     sL[tid] = Lsum;
@@ -415,8 +599,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
     const int hd = i >> 7, d = i & (HYQ_D - 1);
     const float* e = pb + hd * kPart + 2 + d;
     float a = 0.f;
-#pragma unroll 8
-    for (int s2 = 0; s2 < S; ++s2) a = fmaf(__ldcg(e + (size_t)s2 * HYQ_MAX_GQA * kPart), sm_w[s2 * HYQ_MAX_GQA + hd], a);
+    for (int s0 = 0; s0 < S; s0 += 32) {  // all loads of a chunk in flight at once
+      float v[32];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) v[k] = s0 + k < S ? __ldcg(e + (size_t)(s0 + k) * HYQ_MAX_GQA * kPart) : 0.f;
+#pragma unroll
+      for (int k = 0; k < 32; ++k)
+        if (s0 + k < S) a = fmaf(v[k], sm_w[(s0 + k) * HYQ_MAX_GQA + hd], a);
+    }
     const float Lh = sL[hd];
     out[((size_t)b * HQ + (size_t)h * gq + hd) * HYQ_D + d] = __float2bfloat16_rn(Lh > 0.f ? a / Lh : 0.f);
   }
@@ -477,28 +667,92 @@ __global__ void decode_append_kernel(const __nv_bfloat16* __restrict__ q, const 
 }  // namespace
 
 size_t hyq_decode_ws_bytes(const hyq_config* c, int32_t len_hint) {
-  const int S = decode_split(c, len_hint);
+  // Enough for the global merge at the plan's split count (the fallback when
+  // a cluster cannot be resident); the cluster and direct merges use none.
+  const DecodePlan p = decode_plan(c, len_hint);
   size_t bh = (size_t)c->batch * c->num_kv_heads;
-  return round_up(bh * 4) + round_up(bh * (size_t)S * HYQ_MAX_GQA * kPart * 4);
+  return round_up(bh * 4) + round_up(bh * (size_t)p.S * HYQ_MAX_GQA * kPart * 4);
+}
+
+template <int kMode>
+cudaError_t set_attrs() {
+  static bool done = false;
+  if (done) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e == cudaSuccess && kMode == kCluster)
+    e = cudaFuncSetAttribute(decode_kernel<kMode>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess) done = true;
+  return e;
+}
+
+// Can one cluster of S decode blocks be resident on this device?
+bool cluster_fits(int S) {
+  static int cached[17] = {0};  // 0 unknown, 1 yes, 2 no
+  if (S < 2 || S > 16) return false;
+  if (cached[S]) return cached[S] == 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(S, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = S;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  bool ok = cudaOccupancyMaxActiveClusters(&n, decode_kernel<kCluster>, &cfg) == cudaSuccess && n >= 1;
+  cudaGetLastError();
+  cached[S] = ok ? 1 : 2;
+  return ok;
+}
+
+extern "C" hyq_status hyq_set_decode_plan(int32_t merge, int32_t splits) {
+  if (merge < 0 || merge > 3) return HYQ_ERR_INVALID_ARG;
+  if (merge == 2 && (splits < 2 || splits > 16)) return HYQ_ERR_INVALID_ARG;
+  if (merge == 3 && (splits < 1 || splits > kMaxSplits)) return HYQ_ERR_INVALID_ARG;
+  g_plan_merge = merge;
+  g_plan_splits = splits;
+  return HYQ_OK;
 }
 
 cudaError_t hyq_launch_decode(const hyq_config* c, const void* q, const hyq_layout* lay, void* out,
                               int32_t len_hint, void* ws, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  const int S = decode_split(c, len_hint);
+  cudaError_t e = set_attrs<kDirect>();
+  if (e == cudaSuccess) e = set_attrs<kCluster>();
+  if (e == cudaSuccess) e = set_attrs<kGlobal>();
+  if (e != cudaSuccess) return e;
+  DecodePlan p = decode_plan(c, len_hint);
+  if (p.mode == kCluster && !cluster_fits(p.S)) p.mode = kGlobal;  // same S, workspace merge
   size_t bh = (size_t)c->batch * c->num_kv_heads;
   int32_t* tickets = static_cast<int32_t*>(ws);
   float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + round_up(bh * 4));
-  dim3 grid(S, c->num_kv_heads, c->batch);
-  decode_kernel<<<grid, kThreads, kSmemBytes, s>>>(
-      static_cast<const __nv_bfloat16*>(q), *lay, static_cast<__nv_bfloat16*>(out), tickets, part,
-      c->num_q_heads, c->num_q_heads / c->num_kv_heads, hyq_nblk(c), hyq_vl_stride(c), hyq_cap_tail(c), S);
-  return cudaGetLastError();
+  const int gq = c->num_q_heads / c->num_kv_heads;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.S, c->num_kv_heads, c->batch);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = p.S;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  const __nv_bfloat16* qq = static_cast<const __nv_bfloat16*>(q);
+  __nv_bfloat16* oo = static_cast<__nv_bfloat16*>(out);
+  const int nblk = hyq_nblk(c), cvl = hyq_vl_stride(c), ct = hyq_cap_tail(c);
+  if (p.mode == kCluster) {
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_kernel<kCluster>, qq, *lay, oo, tickets, part, c->num_q_heads, gq,
+                              nblk, cvl, ct, p.S);
+  }
+  if (p.mode == kDirect)
+    return cudaLaunchKernelEx(&cfg, decode_kernel<kDirect>, qq, *lay, oo, tickets, part, c->num_q_heads, gq,
+                              nblk, cvl, ct, p.S);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<kGlobal>, qq, *lay, oo, tickets, part, c->num_q_heads, gq,
+                            nblk, cvl, ct, p.S);
 }
 
 cudaError_t hyq_launch_decode_append(const hyq_config* c, const void* q, const void* k_new,

@@ -253,6 +253,17 @@ hyq_status hyq_decode_attention(const hyq_config *cfg, const void *q, const hyq_
                                 hyq_stream_t stream);
 
 /*
+ * Override how hyq_decode_attention splits and merges its work (process-
+ * wide; for tuning and testing).  merge: 0 automatic (the default), 1 one
+ * block per (batch, KV head) and no merge, 2 `splits` blocks (2..16) merged
+ * inside a thread-block cluster, 3 `splits` blocks (1..1024) merged through
+ * the workspace by the last block to finish.  The workspace size reported by
+ * hyq_workspace_size follows the override.  Returns HYQ_ERR_INVALID_ARG for
+ * values out of range and leaves the previous setting.
+ */
+hyq_status hyq_set_decode_plan(int32_t merge, int32_t splits);
+
+/*
  * hyq_decode_attention without a caller-provided workspace.  The paper has
  * no counterpart; this exists for callers that cannot allocate device
  * memory: plugins and embedding runtimes that hand an attention op only its

@@ -83,6 +83,27 @@ def test_decode_split_count_does_not_change_result(hyq):
     assert_attention_close(b, want)
 
 
+@pytest.mark.parametrize("merge,splits", [(1, 0), (2, 2), (2, 5), (2, 16), (3, 3), (3, 19)])
+def test_decode_every_merge_plan(hyq, merge, splits):
+    """Direct (one block per KV head), cluster and workspace merges all give the
+    oracle's result."""
+    from hybrid_precision_quantized_gb300 import hyq_set_decode_plan
+    c = decode_case(43, 1, 16, 4, 5000, window=128, n_proxy=64, sink_frac=0.02)
+    hyq_set_decode_plan(merge, splits)
+    try:
+        got, want, _ = build_and_decode(c, 5000, 128, 50_000)
+    finally:
+        hyq_set_decode_plan(0, 0)
+    assert_attention_close(got, want, what=f"plan {merge}/{splits}")
+
+
+def test_decode_many_heads_direct_plan(hyq):
+    """Enough (batch, KV head) pairs that the automatic plan uses one block each."""
+    c = decode_case(44, 12, 16, 8, 700, window=128, n_proxy=16, sink_frac=0.02)
+    got, want, _ = build_and_decode(c, 700, 128, 50_000)
+    assert_attention_close(got, want, what="B=12 x 8 KV heads")
+
+
 def test_decode_repeated_calls_reuse_workspace(hyq):
     c = decode_case(42, 1, 8, 2, 900, window=128, n_proxy=16, sink_frac=0.02)
     got, want, (cfg, layer, ws, out) = build_and_decode(c, 900, 128, 50_000)
