@@ -18,13 +18,14 @@
 // 4-bit tiles are dequantised inside the dot products:
 //   q.k~  = sum_q s_q (q_q . c_q) + z_q sum(q_q)     (per group q of 32)
 //   p v~  = sum_j (p_j s_jq) c_jd + p_j z_jq
-// on mma.sync m16n8k16: K codes as bf16 128 + c (the offset is removed
-// exactly through the per-group query sums, since q and s enter unrounded),
-// V codes as fp16 subnormals c * 2^-24 against the fp16-rounded p * s (no
-// offset, so the rounding of p * s is not amplified).  BF16 tiles are loaded
-// straight into fragment registers; the head_dim order of the K products and
-// of the V outputs is permuted (identically in both paths, see hyq.h) so that
-// those loads are 16- and 8-byte vectors.
+// on fp16 mma.sync m16n8k16 with the codes as fp16 subnormals (c * 2^-24,
+// one AND per register pair: no offset to cancel, so the fp16 rounding of the
+// other operand is not amplified), against the query scaled by an exact power
+// of two into fp16 (QK) and against p * s in fp16 (PV); scales, zeros and the
+// per-group query sums are applied in fp32.  BF16 tiles are staged by bulk
+// copies (or loaded straight into fragment registers); the head_dim order of
+// the K products and of the V outputs is permuted (identically in both paths,
+// see hyq.h) so that those loads are 16- and 8-byte vectors.
 #include <cooperative_groups.h>
 #include <math.h>
 
@@ -38,10 +39,10 @@ constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 constexpr int kSlots = 3;                                     // 4-bit tiles in flight per warp
 constexpr int kRingBytes = kWarps * kSlots * HYQ_QTILE_BYTES; // 120 KiB of rings
-// BF16 tiles staged in shared memory by bulk copies, one row per copy, with
-// padded row strides that make the fragment loads bank-conflict free.
-constexpr int kFKStride = 320, kFVStride = 272;
-constexpr int kFTileBytes = 16 * kFKStride + 16 * kFVStride;  // 9472
+// BF16 tiles staged in shared memory by a few contiguous bulk copies (K rows,
+// then V rows, 256 bytes each): a handful of copies instead of one per row.
+constexpr int kFKStride = 256, kFVStride = 256;
+constexpr int kFTileBytes = 16 * kFKStride + 16 * kFVStride;  // 8192
 constexpr int kFStaged = 7;                                     // staged BF16 tiles per block
 constexpr int kSmemBytes = kRingBytes + kFStaged * kFTileBytes;
 constexpr int kPart = 2 + HYQ_D;                              // m, l, acc[128] per head
@@ -141,9 +142,20 @@ __device__ __forceinline__ void softmax_update(const float (&lg)[4], State& st, 
   }
 }
 
-// One 16-row 4-bit tile (2560 bytes at `tb`), `vr` valid rows.
+// Per-block constants of the 4-bit path.
+struct QConst {
+  float ksc[2];   // logit factor of the code products for tokens g (x1) and g+8 (x16 codes)
+  float qs[2][4]; // per-group query sums of heads 2t, 2t+1, times log2(e)/sqrt(d)
+};
+
+// One 16-row 4-bit tile (2560 bytes at `tb`), `vr` valid rows.  The codes
+// enter the fp16 MMAs as subnormals: the low nibble of a byte as c * 2^-24,
+// the high nibble, masked in place, as 16 c * 2^-24.  In both code orders the
+// high nibbles are exactly fragment rows g+8 (K: tokens g+8; V: output rows
+// g+8), so the factor 16 is a per-row constant: folded into ksc[1] for K and
+// into the epilogue for V.  bq holds the query as fp16, scaled by 2^e.
 __device__ __forceinline__ void q_tile(const uint8_t* tb, int lane, int vr, const uint32_t (&bq)[8][2],
-                                       const float (&qs)[2][4], State& st) {
+                                       const QConst& qc, State& st) {
   const int g = lane >> 2;
   const uint4 kw0 = *reinterpret_cast<const uint4*>(tb + lane * 16);
   const uint4 kw1 = *reinterpret_cast<const uint4*>(tb + 512 + lane * 16);
@@ -152,28 +164,29 @@ __device__ __forceinline__ void q_tile(const uint8_t* tb, int lane, int vr, cons
 #pragma unroll
   for (int q = 0; q < 4; ++q) C[q][0] = C[q][1] = C[q][2] = C[q][3] = 0.f;
 #pragma unroll
-  for (int ks = 0; ks < 8; ++ks)
-    mma_bf16(C[ks >> 1], nib2_bf16(kw[ks], 0), nib2_bf16(kw[ks], 4), nib2_bf16(kw[ks], 8),
-             nib2_bf16(kw[ks], 12), bq[ks][0], bq[ks][1]);
+  for (int ks = 0; ks < 8; ++ks) {
+    const uint32_t w = kw[ks], w8 = w >> 8;
+    mma_f16(C[ks >> 1], w & 0x000F000Fu, w & 0x00F000F0u, w8 & 0x000F000Fu, w8 & 0x00F000F0u, bq[ks][0],
+            bq[ks][1]);
+  }
   const uint8_t* km = tb + 2048;
   float lg[4];
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
     const uint4 mk = *reinterpret_cast<const uint4*>(km + (g + 8 * r) * 16);
     const uint32_t mw[4] = {mk.x, mk.y, mk.z, mk.w};
-    float a0 = 0.f, a1 = 0.f;
+    float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const float2 sz = half2_to_float2(mw[q]);
-      const float zz = fmaf(-128.f, sz.x, sz.y);  // zero minus the bf16 code offset
       a0 = fmaf(sz.x, C[q][2 * r], a0);
-      a0 = fmaf(zz, qs[0][q], a0);
       a1 = fmaf(sz.x, C[q][2 * r + 1], a1);
-      a1 = fmaf(zz, qs[1][q], a1);
+      b0 = fmaf(sz.y, qc.qs[0][q], b0);
+      b1 = fmaf(sz.y, qc.qs[1][q], b1);
     }
     const bool valid = g + 8 * r < vr;
-    lg[2 * r] = valid ? a0 * kScale : -INFINITY;
-    lg[2 * r + 1] = valid ? a1 * kScale : -INFINITY;
+    lg[2 * r] = valid ? fmaf(a0, qc.ksc[r], b0) : -INFINITY;
+    lg[2 * r + 1] = valid ? fmaf(a1, qc.ksc[r], b1) : -INFINITY;
   }
   float p[4];
   softmax_update(lg, st, p);
@@ -185,22 +198,32 @@ __device__ __forceinline__ void q_tile(const uint8_t* tb, int lane, int vr, cons
   const uint4 mv1 = *reinterpret_cast<const uint4*>(vm + (g + 8) * 16);
   const uint32_t m0[4] = {mv0.x, mv0.y, mv0.z, mv0.w};
   const uint32_t m1[4] = {mv1.x, mv1.y, mv1.z, mv1.w};
+  const __half2 p0 = __floats2half2_rn(p[0], p[1]), p1 = __floats2half2_rn(p[2], p[3]);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const float2 sz0 = half2_to_float2(m0[q]);
-    const float2 sz1 = half2_to_float2(m1[q]);
-    // B operand (tokens x heads) of group q: p * s, transposed into place.
-    const uint32_t b0 = movmatrix_trans(pack_f16x2(p[0] * sz0.x, p[1] * sz0.x));
-    const uint32_t b1 = movmatrix_trans(pack_f16x2(p[2] * sz1.x, p[3] * sz1.x));
-    st.zacc[0][q] = fmaf(p[0], sz0.y, fmaf(p[2], sz1.y, st.zacc[0][q]));
-    st.zacc[1][q] = fmaf(p[1], sz0.y, fmaf(p[3], sz1.y, st.zacc[1][q]));
+    // B operand (tokens x heads) of group q: p * s in packed fp16, transposed into place.
+    const uint32_t s0 = __byte_perm(m0[q], 0, 0x1010), s1 = __byte_perm(m1[q], 0, 0x1010);
+    const __half2 x0 = __hmul2(p0, *reinterpret_cast<const __half2*>(&s0));
+    const __half2 x1 = __hmul2(p1, *reinterpret_cast<const __half2*>(&s1));
+    const uint32_t b0 = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&x0));
+    const uint32_t b1 = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&x1));
+    const float z0 = __high2float(*reinterpret_cast<const __half2*>(&m0[q]));
+    const float z1 = __high2float(*reinterpret_cast<const __half2*>(&m1[q]));
+    st.zacc[0][q] = fmaf(p[0], z0, fmaf(p[2], z1, st.zacc[0][q]));
+    st.zacc[1][q] = fmaf(p[1], z0, fmaf(p[3], z1, st.zacc[1][q]));
 #pragma unroll
     for (int mm = 0; mm < 2; ++mm) {
-      const uint32_t x = vw[2 * q + mm];  // m-tile 2q + mm lies in group q
-      mma_f16(st.acc[2 * q + mm], nib2_f16_sub(x, 0), nib2_f16_sub(x, 4), nib2_f16_sub(x, 8),
-              nib2_f16_sub(x, 12), b0, b1);
+      const uint32_t x = vw[2 * q + mm], x8 = x >> 8;  // m-tile 2q + mm lies in group q
+      mma_f16(st.acc[2 * q + mm], x & 0x000F000Fu, x & 0x00F000F0u, x8 & 0x000F000Fu, x8 & 0x00F000F0u, b0, b1);
     }
   }
+}
+
+// 16 x a bf16 pair (exact: a power of two).
+__device__ __forceinline__ uint32_t times16_bf16x2(uint32_t x) {
+  __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&x);
+  v = __hmul2(v, __floats2bfloat162_rn(16.f, 16.f));
+  return *reinterpret_cast<uint32_t*>(&v);
 }
 
 __device__ __forceinline__ uint32_t u4c(const uint4& v, int i) {
@@ -211,8 +234,9 @@ __device__ __forceinline__ uint32_t u4c(const uint4& v, int i) {
 // by the tail), `vr` valid rows, loaded directly into fragment registers.
 __device__ __forceinline__ void f_tile(const __nv_bfloat16* vlk, const __nv_bfloat16* vlv,
                                        const __nv_bfloat16* tk, const __nv_bfloat16* tv, int nvl,
-                                       int row0, int vr, int lane, const uint32_t (&bq)[8][2], State& st) {
+                                       int row0, int vr, int lane, const __nv_bfloat16* q_s, State& st) {
   const int g = lane >> 2, t = lane & 3;
+
   float S[4] = {0.f, 0.f, 0.f, 0.f};
   {
     // K rows g and g+8, chunks t + 4j: the permuted k order of the A fragments.
@@ -228,8 +252,10 @@ __device__ __forceinline__ void f_tile(const __nv_bfloat16* vlk, const __nv_bflo
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
       const int j = ks >> 1, sub = ks & 1;
+      const __nv_bfloat16* qe = q_s + g * HYQ_D + 8 * (t + 4 * j) + 4 * sub;  // permuted k order
       mma_bf16(S, u4c(ka[0][j], 2 * sub), u4c(ka[1][j], 2 * sub), u4c(ka[0][j], 2 * sub + 1),
-               u4c(ka[1][j], 2 * sub + 1), bq[ks][0], bq[ks][1]);
+               u4c(ka[1][j], 2 * sub + 1), *reinterpret_cast<const uint32_t*>(qe),
+               *reinterpret_cast<const uint32_t*>(qe + 2));
     }
   }
   float lg[4];
@@ -257,16 +283,20 @@ __device__ __forceinline__ void f_tile(const __nv_bfloat16* vlk, const __nv_bflo
     const int G = u >> 1, s2 = u & 1;
     const uint32_t w0 = s2 ? va[0][G].y : va[0][G].x, w1 = s2 ? va[1][G].y : va[1][G].x;
     const uint32_t w2 = s2 ? va[2][G].y : va[2][G].x, w3 = s2 ? va[3][G].y : va[3][G].x;
-    mma_bf16(st.acc[u], __byte_perm(w0, w1, 0x5410), __byte_perm(w0, w1, 0x7632),
-             __byte_perm(w2, w3, 0x5410), __byte_perm(w2, w3, 0x7632), b0, b1);
+    // rows g+8 carry the same factor 16 as the 4-bit high-nibble rows
+    mma_bf16(st.acc[u], __byte_perm(w0, w1, 0x5410), times16_bf16x2(__byte_perm(w0, w1, 0x7632)),
+             __byte_perm(w2, w3, 0x5410), times16_bf16x2(__byte_perm(w2, w3, 0x7632)), b0, b1);
   }
 }
 
 // The same BF16 tile from shared memory (K rows at stride kFKStride, V rows
 // at kFVStride); rows at or past `vr` are masked (their contents are undefined).
+// The unpadded rows cost 2-way (K) and 4-way (V) bank conflicts on these few
+// loads, against 32 single-row copies per tile otherwise.
 __device__ __forceinline__ void f_tile_smem(const uint8_t* Ks, const uint8_t* Vs, int vr, int lane,
-                                            const uint32_t (&bq)[8][2], State& st) {
+                                            const __nv_bfloat16* q_s, State& st) {
   const int g = lane >> 2, t = lane & 3;
+
   float S[4] = {0.f, 0.f, 0.f, 0.f};
   {
     uint4 ka[2][4];
@@ -278,8 +308,10 @@ __device__ __forceinline__ void f_tile_smem(const uint8_t* Ks, const uint8_t* Vs
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
       const int j = ks >> 1, sub = ks & 1;
+      const __nv_bfloat16* qe = q_s + g * HYQ_D + 8 * (t + 4 * j) + 4 * sub;  // permuted k order
       mma_bf16(S, u4c(ka[0][j], 2 * sub), u4c(ka[1][j], 2 * sub), u4c(ka[0][j], 2 * sub + 1),
-               u4c(ka[1][j], 2 * sub + 1), bq[ks][0], bq[ks][1]);
+               u4c(ka[1][j], 2 * sub + 1), *reinterpret_cast<const uint32_t*>(qe),
+               *reinterpret_cast<const uint32_t*>(qe + 2));
     }
   }
   float lg[4];
@@ -305,8 +337,9 @@ __device__ __forceinline__ void f_tile_smem(const uint8_t* Ks, const uint8_t* Vs
     const int G = u >> 1, s2 = u & 1;
     const uint32_t w0 = s2 ? va[0][G].y : va[0][G].x, w1 = s2 ? va[1][G].y : va[1][G].x;
     const uint32_t w2 = s2 ? va[2][G].y : va[2][G].x, w3 = s2 ? va[3][G].y : va[3][G].x;
-    mma_bf16(st.acc[u], __byte_perm(w0, w1, 0x5410), __byte_perm(w0, w1, 0x7632),
-             __byte_perm(w2, w3, 0x5410), __byte_perm(w2, w3, 0x7632), b0, b1);
+    // rows g+8 carry the same factor 16 as the 4-bit high-nibble rows
+    mma_bf16(st.acc[u], __byte_perm(w0, w1, 0x5410), times16_bf16x2(__byte_perm(w0, w1, 0x7632)),
+             __byte_perm(w2, w3, 0x5410), times16_bf16x2(__byte_perm(w2, w3, 0x7632)), b0, b1);
   }
 }
 
@@ -360,39 +393,45 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
   const __nv_bfloat16* vlv = static_cast<const __nv_bfloat16*>(lay.vl_v) + bh * cap_vl * HYQ_D;
   const __nv_bfloat16* tk = static_cast<const __nv_bfloat16*>(lay.tail_k) + bh * cap_tail * HYQ_D;
   const __nv_bfloat16* tv = static_cast<const __nv_bfloat16*>(lay.tail_v) + bh * cap_tail * HYQ_D;
-  // The first kFStaged BF16 tiles of this block are fetched by bulk copies,
-  // one row per lane, by the warp that will use them (before its 4-bit ring).
   const int n_staged = min(f1 - f0, kFStaged);
   uint8_t* fstage = smem + kRingBytes + warp * kFTileBytes;
-  if (warp < n_staged) {
-    const int row0 = 16 * (f0 + warp), nrows = min(16, nf - row0);
-    if (lane == 0) {
-      mbar_init(&fbars[warp], 1);
-      mbar_fence_init();
-      mbar_arrive_expect_tx(&fbars[warp], nrows * 2 * HYQ_D * 2);
-    }
-    __syncwarp();
-    const int rr = lane & 15, row = row0 + rr;
-    if (rr < nrows) {
-      const bool v = lane >= 16;
-      const __nv_bfloat16* src = row < nvl ? (v ? vlv : vlk) + (size_t)row * HYQ_D
-                                           : (v ? tv : tk) + (size_t)(row - nvl) * HYQ_D;
-      bulk_g2s(fstage + (v ? 16 * kFKStride + rr * kFVStride : rr * kFKStride), src, HYQ_D * 2, &fbars[warp]);
-    }
-  }
   if (lane == 0) {
     for (int i = 0; i < kSlots; ++i) mbar_init(&wb[i], 1);
+    if (warp < n_staged) mbar_init(&fbars[warp], 1);
     mbar_fence_init();
+  }
+  for (int i = gq * HYQ_D / 8 + tid; i < HYQ_MAX_GQA * HYQ_D / 8; i += kThreads)
+    reinterpret_cast<uint4*>(q_s)[i] = make_uint4(0, 0, 0, 0);  // query rows past g
+  __syncthreads();
+  // Nothing else is requested until the query has arrived: a flood of tile
+  // copies ahead of it would delay the start of all compute by the flood's
+  // service time.
+  if (!mbar_wait(&qbar, 0) && tid == 0) hyq_set_err(lay.err, HYQ_DEVERR_TIMEOUT);
+  if (lane == 0) {
+    // The first kFStaged BF16 tiles of this block: the rows of a tile are
+    // contiguous in the vertical-line buffer and in the tail, so a tile takes
+    // one K and one V copy per buffer it touches.  Used after the 4-bit loop.
+    if (warp < n_staged) {
+      const int row0 = 16 * (f0 + warp), nrows = min(16, nf - row0);
+      mbar_arrive_expect_tx(&fbars[warp], nrows * 2 * HYQ_D * 2);
+      const int na = max(0, min(row0 + nrows, nvl) - row0);  // rows in the vertical-line buffer
+      if (na > 0) {
+        bulk_g2s(fstage, vlk + (size_t)row0 * HYQ_D, na * HYQ_D * 2, &fbars[warp]);
+        bulk_g2s(fstage + 16 * kFKStride, vlv + (size_t)row0 * HYQ_D, na * HYQ_D * 2, &fbars[warp]);
+      }
+      if (nrows > na) {
+        const int tr = row0 + na - nvl;  // first tail row
+        bulk_g2s(fstage + na * kFKStride, tk + (size_t)tr * HYQ_D, (nrows - na) * HYQ_D * 2, &fbars[warp]);
+        bulk_g2s(fstage + 16 * kFKStride + na * kFVStride, tv + (size_t)tr * HYQ_D, (nrows - na) * HYQ_D * 2,
+                 &fbars[warp]);
+      }
+    }
     for (int j = 0; j < nj && j < kSlots; ++j) {
       mbar_arrive_expect_tx(&wb[j], HYQ_QTILE_BYTES);
       bulk_g2s(ring + j * HYQ_QTILE_BYTES, tiles + (size_t)(t0 + my0 + kWarps * j) * HYQ_QTILE_BYTES,
                HYQ_QTILE_BYTES, &wb[j]);
     }
   }
-  for (int i = gq * HYQ_D / 8 + tid; i < HYQ_MAX_GQA * HYQ_D / 8; i += kThreads)
-    reinterpret_cast<uint4*>(q_s)[i] = make_uint4(0, 0, 0, 0);  // query rows past g
-  __syncthreads();
-  if (!mbar_wait(&qbar, 0) && tid == 0) hyq_set_err(lay.err, HYQ_DEVERR_TIMEOUT);
   if (tid < 32) {
     float sacc = 0.f;
     const __nv_bfloat16* r = q_s + (tid >> 2) * HYQ_D + 32 * (tid & 3);
@@ -400,20 +439,43 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
     qsum_s[tid] = sacc;
   }
   __syncthreads();
+  // The query in fp16 for the 4-bit path, scaled by 2^e (exact) so that its
+  // largest element is below 2^14; e = 14 - (binary exponent of max |q|).
+  float amax = 0.f;
+  for (int i = lane; i < gq * HYQ_D / 8; i += 32) {
+    const uint4 v = reinterpret_cast<const uint4*>(q_s)[i];
+    const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __bfloat1622float2(p2[k]);
+      amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+  }
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  int ex = 0;
+  if (amax > 0.f && isfinite(amax)) (void)frexpf(amax, &ex);
+  const int qe = 14 - ex;
+  const float qscale = ldexpf(1.f, qe);
   // B fragments of q in the permuted k order: kstep ks covers elements
   // 8(t + 4(ks/2)) + 4(ks%2) + {0,1} and + {2,3}.
   uint32_t bq[8][2];
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
     const int e = 8 * (t + 4 * (ks >> 1)) + 4 * (ks & 1);
-    bq[ks][0] = *reinterpret_cast<const uint32_t*>(q_s + g * HYQ_D + e);
-    bq[ks][1] = *reinterpret_cast<const uint32_t*>(q_s + g * HYQ_D + e + 2);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(q_s + g * HYQ_D + e + 2 * hh));
+      bq[ks][hh] = pack_f16x2(f.x * qscale, f.y * qscale);
+    }
   }
-  float qs[2][4];
+  QConst qc;
+  qc.ksc[0] = ldexpf(kScale, 24 - qe);
+  qc.ksc[1] = ldexpf(kScale, 20 - qe);
 #pragma unroll
   for (int j = 0; j < 2; ++j)
 #pragma unroll
-    for (int qq = 0; qq < 4; ++qq) qs[j][qq] = qsum_s[(2 * t + j) * 4 + qq];
+    for (int qq = 0; qq < 4; ++qq) qc.qs[j][qq] = qsum_s[(2 * t + j) * 4 + qq] * kScale;
 
   State st;
   st.m[0] = st.m[1] = -INFINITY;
@@ -423,21 +485,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
 #pragma unroll
   for (int j = 0; j < 2; ++j) st.zacc[j][0] = st.zacc[j][1] = st.zacc[j][2] = st.zacc[j][3] = 0.f;
 
-  // ---- BF16 tiles (vertical-line rows, then the tail) ----------------------
-  if (warp < n_staged) {
-    const bool ok = mbar_wait(&fbars[warp], 0);
-    if (__any_sync(0xffffffffu, !ok)) {
-      if (lane == 0) {
-        hyq_set_err(lay.err, HYQ_DEVERR_TIMEOUT);
-        (void)mbar_wait(&fbars[warp], 0);
-      }
-      __syncwarp();
-    } else {
-      f_tile_smem(fstage, fstage + 16 * kFKStride, min(16, nf - 16 * (f0 + warp)), lane, bq, st);
-    }
-  }
-  for (int fi = f0 + kFStaged + warp; fi < f1; fi += kWarps)  // tiles past the staged ones
-    f_tile(vlk, vlv, tk, tv, nvl, 16 * fi, min(16, nf - 16 * fi), lane, bq, st);
   // ---- 4-bit tiles through the warp's ring ---------------------------------
   for (int j = 0; j < nj; ++j) {
     const int slot = j % kSlots;
@@ -453,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
       break;
     }
     const int tile = t0 + my0 + kWarps * j;
-    q_tile(ring + slot * HYQ_QTILE_BYTES, lane, min(16, nq - 16 * tile), bq, qs, st);
+    q_tile(ring + slot * HYQ_QTILE_BYTES, lane, min(16, nq - 16 * tile), bq, qc, st);
     __syncwarp();
     if (lane == 0 && j + kSlots < nj) {
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
@@ -462,6 +509,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
                HYQ_QTILE_BYTES, &wb[slot]);
     }
   }
+
+  // ---- BF16 tiles (vertical-line rows, then the tail): the staged ones have
+  // long arrived by now -----------------------------------------------------
+  if (warp < n_staged) {
+    const bool ok = mbar_wait(&fbars[warp], 0);
+    if (__any_sync(0xffffffffu, !ok)) {
+      if (lane == 0) {
+        hyq_set_err(lay.err, HYQ_DEVERR_TIMEOUT);
+        (void)mbar_wait(&fbars[warp], 0);
+      }
+      __syncwarp();
+    } else {
+      f_tile_smem(fstage, fstage + 16 * kFKStride, min(16, nf - 16 * (f0 + warp)), lane, q_s, st);
+    }
+  }
+  for (int fi = f0 + kFStaged + warp; fi < f1; fi += kWarps)  // tiles past the staged ones
+    f_tile(vlk, vlv, tk, tv, nvl, 16 * fi, min(16, nf - 16 * fi), lane, q_s, st);
 
   // ---- warp partials -> block partial (m, l, acc) in shared memory ---------
 #pragma unroll
@@ -483,7 +547,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
 #pragma unroll
     for (int ci = 0; ci < 4; ++ci) {
       const int d = 32 * (u >> 1) + 4 * g + 2 * (u & 1) + (ci >> 1), hd = 2 * t + (ci & 1);
-      red[(warp * HYQ_MAX_GQA + hd) * HYQ_D + d] = fmaf(st.acc[u][ci], HYQ_F16_SUB_SCALE, st.zacc[ci & 1][u >> 1]);
+      red[(warp * HYQ_MAX_GQA + hd) * HYQ_D + d] =
+          fmaf(st.acc[u][ci], ci < 2 ? HYQ_F16_SUB_SCALE : HYQ_F16_SUB_SCALE / 16.f, st.zacc[ci & 1][u >> 1]);
     }
   if (g == 0)
     for (int j = 0; j < 2; ++j) {
@@ -505,6 +570,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
     blk[tid * kPart + 1] = Lsum;
   }
   __syncthreads();
+  // kGlobal writes the block partial straight to its workspace slot.
+  float* pp = part + (bh * S + split) * (size_t)(HYQ_MAX_GQA * kPart);
+  if (kMode == kGlobal && tid < gq) {
+    pp[tid * kPart + 0] = blk[tid * kPart + 0];
+    pp[tid * kPart + 1] = blk[tid * kPart + 1];
+  }
   for (int i = tid; i < gq * HYQ_D; i += kThreads) {
     const int hd = i >> 7, d = i & (HYQ_D - 1);
     float a = 0.f;
@@ -513,8 +584,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
     if (kMode == kDirect) {
       const float Lh = blk[hd * kPart + 1];
       out[((size_t)b * HQ + (size_t)h * gq + hd) * HYQ_D + d] = __float2bfloat16_rn(Lh > 0.f ? a / Lh : 0.f);
-    } else {
+    } else if (kMode == kCluster) {
       blk[hd * kPart + 2 + d] = a;
+    } else {
+      pp[hd * kPart + 2 + d] = a;
     }
   }
   if (kMode == kDirect) return;
@@ -562,16 +635,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
     return;
   }
 
-  // ---- kGlobal: partials to the workspace, the last block merges -----------
-  __syncthreads();  // blk was written by other threads
-  float* pp = part + (bh * S + split) * (size_t)(HYQ_MAX_GQA * kPart);
-  for (int i = tid; i < gq * kPart; i += kThreads) pp[i] = blk[i];
-  __threadfence();
+  // ---- kGlobal: the last block to finish merges the workspace partials -----
+  // The barrier orders every thread's partial writes before thread 0's
+  // release; its acquire (in the last block) orders them before the reads.
   __syncthreads();
-  if (tid == 0) s_flag = (atomicAdd(&tickets[bh], 1) == S - 1);
+  if (tid == 0) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;\n" : "=r"(old) : "l"(tickets + bh) : "memory");
+    s_flag = (old == S - 1);
+  }
   __syncthreads();
   if (!s_flag) return;
-  __threadfence();
   const float* pb = part + bh * S * (size_t)(HYQ_MAX_GQA * kPart);
   float* sm_m = red;                             // [S][8]
   float* sm_w = red + kMaxSplits * HYQ_MAX_GQA;  // [S][8]
@@ -579,6 +653,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
     const int s2 = i / gq, hd = i % gq;
     sm_m[s2 * HYQ_MAX_GQA + hd] = __ldcg(pb + (size_t)s2 * HYQ_MAX_GQA * kPart + hd * kPart);
     sm_w[s2 * HYQ_MAX_GQA + hd] = __ldcg(pb + (size_t)s2 * HYQ_MAX_GQA * kPart + hd * kPart + 1);
+  }
+  // This thread's first output element: its partial accumulators are loaded
+  // now, in the same round trip as the (m, l) above.
+  float v0[32];
+  {
+    const int i = tid, hd = i >> 7, d = i & (HYQ_D - 1);
+    const float* e = pb + hd * kPart + 2 + d;
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+      v0[k] = (i < gq * HYQ_D && k < S) ? __ldcg(e + (size_t)k * HYQ_MAX_GQA * kPart) : 0.f;
   }
   __syncthreads();
   if (tid < gq) {
@@ -601,8 +685,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
     float a = 0.f;
     for (int s0 = 0; s0 < S; s0 += 32) {  // all loads of a chunk in flight at once
       float v[32];
+      if (i == tid && s0 == 0) {
 #pragma unroll
-      for (int k = 0; k < 32; ++k) v[k] = s0 + k < S ? __ldcg(e + (size_t)(s0 + k) * HYQ_MAX_GQA * kPart) : 0.f;
+        for (int k = 0; k < 32; ++k) v[k] = v0[k];
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) v[k] = s0 + k < S ? __ldcg(e + (size_t)(s0 + k) * HYQ_MAX_GQA * kPart) : 0.f;
+      }
 #pragma unroll
       for (int k = 0; k < 32; ++k)
         if (s0 + k < S) a = fmaf(v[k], sm_w[(s0 + k) * HYQ_MAX_GQA + hd], a);
