@@ -19,10 +19,15 @@ Readings (the paper leaves these open):
 * key tiles are B_N = 64 consecutive entries of the quantised-prefix
   positions taken in ascending order (the reordered layout of Algorithm 2,
   stage 1); the last tile may be short;
-* K uses one scale per tile; V one scale per (tile, channel); Q one scale
-  per block of 128 query rows of one head;
-* INT8 codes are ``clamp(rint(x / s), -127, 127)``, FP8 codes are the e4m3
-  value nearest to ``x / s`` (saturating at +-448);
+* K and V each use one scale per tile (Algorithm 2, stage 2 states the rule
+  ``s_T = max|K_T| / c_B`` for K; Eq. 7 quantises V_Q as well and names no
+  other rule, so V takes the same one); Q uses one scale per block of 128
+  query rows of one head (``s^Q``, Algorithm 2 line 13);
+* scales and codes are decided in float32, the kernel's precision (the
+  paper fixes none): ``s = fl32(max|x| / c_B)`` and ``t = fl32(x / s)``;
+  INT8 codes are ``clamp(rint(t), -127, 127)`` (ties to even), FP8 codes the
+  e4m3 value nearest to ``t`` (ties to even, saturating at +-448); a block
+  of zeros gets ``s = 0`` and zero codes;
 * the softmax probabilities are *not* quantised here.  A kernel that feeds a
   low-precision P to the PV product differs from this oracle by the P
   rounding step only; that difference is covered by the test tolerance
@@ -41,25 +46,30 @@ QUERY_BLOCK = 128
 
 
 def _codes(x: np.ndarray, s, dtype: str) -> np.ndarray:
-    """Low-bit codes of x / s (float64 in, float64 code values out)."""
-    s = np.asarray(s, dtype=np.float64)
+    """Low-bit codes of ``fl32(x / s)`` (float32 in, float64 code values out)."""
+    x = np.asarray(x, dtype=np.float32)
+    s = np.asarray(s, dtype=np.float32)
     with np.errstate(divide="ignore", invalid="ignore"):
-        t = np.where(s > 0, x / np.where(s > 0, s, 1.0), 0.0)
+        t = np.where(s > 0, x / np.where(s > 0, s, np.float32(1.0)), np.float32(0.0)).astype(np.float32)
     if dtype == "int8":
-        return np.clip(np.rint(t), -127, 127)
+        return np.clip(np.rint(t), -127, 127).astype(np.float64)
     if dtype == "fp8":
-        t = np.clip(t, -448.0, 448.0)
+        t = np.clip(t, np.float32(-448.0), np.float32(448.0))
         return torch.from_numpy(t).to(torch.float8_e4m3fn).to(torch.float64).numpy()
     raise ValueError(dtype)
 
 
 def quantize_symmetric(x, axis, dtype: str):
-    """Symmetric quantisation with ``s = max|x| / c_B`` over ``axis``.
-    Returns (dequantised values, codes, scales)."""
+    """Symmetric quantisation with ``s = fl32(max|x| / c_B)`` over ``axis``
+    (``None`` = one scale for the whole block).  ``x`` holds BF16 values, so
+    ``max|x|`` and ``x`` are exact in float32.
+    Returns (dequantised values, codes, scales), all float64."""
     x = np.asarray(x, dtype=np.float64)
-    s = np.abs(x).max(axis=axis, keepdims=True) / C_B[dtype]
-    c = _codes(x, s, dtype)
-    return c * s, c, s
+    amax = np.abs(x).max(axis=axis, keepdims=True).astype(np.float32)
+    s = (amax / np.float32(C_B[dtype])).astype(np.float32)
+    c = _codes(x.astype(np.float32), s, dtype)
+    s64 = s.astype(np.float64)
+    return c * s64, c, s64
 
 
 def hybrid_prefill(q, k, v, vl_idx, window: int, dtype: str = "int8",
@@ -89,7 +99,7 @@ def hybrid_prefill(q, k, v, vl_idx, window: int, dtype: str = "int8",
             for t0 in range(0, len(qpos), key_tile):
                 j = qpos[t0:t0 + key_tile]
                 kq[t0:t0 + len(j)] = quantize_symmetric(k[b, kh, j], None, dtype)[0]
-                vq[t0:t0 + len(j)] = quantize_symmetric(v[b, kh, j], 0, dtype)[0]
+                vq[t0:t0 + len(j)] = quantize_symmetric(v[b, kh, j], None, dtype)[0]
             fp = np.concatenate([vl, np.arange(P, L)])
             pos = np.concatenate([qpos, fp])
             Kall = np.concatenate([kq, k[b, kh, fp]])

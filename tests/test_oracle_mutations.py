@@ -65,6 +65,10 @@ MUTATIONS = [
      "BF16 branch uses quantised queries"),
     ("prefill", "return np.clip(np.rint(t), -127, 127)", "return np.clip(np.trunc(t), -127, 127)",
      "INT8 codes truncated"),
+    ("prefill", "vq[t0:t0 + len(j)] = quantize_symmetric(v[b, kh, j], None, dtype)[0]",
+     "vq[t0:t0 + len(j)] = quantize_symmetric(v[b, kh, j], 0, dtype)[0]", "V scales per channel"),
+    ("prefill", "s = (amax / np.float32(C_B[dtype])).astype(np.float32)",
+     "s = (amax / np.float32(C_B[dtype] + 1)).astype(np.float32)", "c_B off by one"),
     ("accounting", "return d // 2 + ((d // group) * 4 if with_meta else 0)",
      "return d // 2 + ((d // group) * 2 if with_meta else 0)", "metadata bytes halved"),
 ]

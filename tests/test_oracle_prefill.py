@@ -93,3 +93,64 @@ def test_causality():
     # positions < 200 and >= 200, so compare only rows whose tiles are untouched.
     assert np.array_equal(o1[:, :, :128], o2[:, :, :128])
     assert not np.array_equal(o1[:, :, 230:], o2[:, :, 230:])
+
+
+def _e4m3_values():
+    """All finite e4m3 (fn) values from the format's definition: 1 sign bit,
+    4 exponent bits (bias 7), 3 mantissa bits, subnormals at exponent 0, the
+    all-ones pattern (S.1111.111) is NaN, no infinities; max 448."""
+    vals = {}
+    for bits in range(256):
+        s, e, m = bits >> 7, (bits >> 3) & 0xF, bits & 7
+        if e == 15 and m == 7:
+            continue
+        mag = (m / 8.0) * 2.0 ** -6 if e == 0 else (1.0 + m / 8.0) * 2.0 ** (e - 7)
+        vals[bits] = -mag if s else mag
+    return vals
+
+
+def test_fp8_codes_are_nearest_e4m3_ties_to_even():
+    vals = _e4m3_values()
+    pos = sorted((v, b) for b, v in vals.items() if v >= 0 and not (v == 0 and b & 0x80))
+    grid = np.array([v for v, _ in pos])
+    mant_even = np.array([(b & 1) == 0 for _, b in pos])
+    rng = np.random.default_rng(11)
+    t = np.concatenate([rng.uniform(0, 448, 4000), rng.uniform(0, 0.05, 2000),
+                        (grid[:-1] + grid[1:]) / 2])          # exact midpoints: ties
+    t = t.astype(np.float32).astype(np.float64)
+    x = np.concatenate([t, -t, [448.0]])
+    _, c, s = quantize_symmetric(x.reshape(1, -1), None, "fp8")
+    tt = (x.astype(np.float32) / np.float32(s.item())).astype(np.float64)
+    a = np.abs(tt)
+    i = np.clip(np.searchsorted(grid, a), 1, len(grid) - 1)
+    lo, hi = grid[i - 1], grid[i]
+    pick_hi = (a - lo > hi - a) | ((a - lo == hi - a) & mant_even[i])
+    want = np.where(pick_hi, hi, lo) * np.sign(tt)
+    np.testing.assert_array_equal(c.ravel(), want)
+
+
+def test_int8_scale_and_codes_in_float32():
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((64, 128)).astype(np.float32).astype(np.float64)
+    _, c, s = quantize_symmetric(x, None, "int8")
+    s32 = np.float32(np.abs(x).max()) / np.float32(127.0)
+    assert s.item() == float(np.float32(s32))
+    t = (x.astype(np.float32) / np.float32(s32)).astype(np.float64)
+    assert np.all(np.abs(t - c) <= 0.5)
+    half = np.abs(np.abs(t - c) - 0.5) == 0
+    assert np.all(c[half] % 2 == 0)
+
+
+def test_value_tiles_share_one_scale():
+    """One scale per key tile for V too: a huge channel in every value row
+    drives the other channels' INT8 codes to zero, so rows that attend only
+    to quantised keys get exactly zero in those channels."""
+    L, W = 200, 8
+    rng = np.random.default_rng(13)
+    q = rng.standard_normal((1, 2, L, 64))
+    k = rng.standard_normal((1, 1, L, 64))
+    v = rng.uniform(-1, 1, (1, 1, L, 64)).astype(np.float32).astype(np.float64)
+    v[..., 0] = 1000.0
+    o = hybrid_prefill(q, k, v, None, window=W, dtype="int8")
+    assert np.all(o[:, :, :L - W, 1:] == 0.0)
+    assert np.all(o[:, :, L - W:, 1:] != 0.0)
