@@ -31,12 +31,14 @@ COUNTS = 8
 CNT_NQ, CNT_NVL, CNT_NTAIL, CNT_LEN, CNT_RING_N, CNT_RING_POS = range(6)
 LAYOUT_FIELDS = ("qblocks", "vl_k", "vl_v", "vl_idx", "tail_k", "tail_v", "q_ring", "counts", "err")
 OP_SELECT, OP_DECODE, OP_PREFILL = 1, 2, 3
+PREFILL_INT8, PREFILL_FP8 = 1, 2
 
 # Every symbol include/hyq.h declares.
 SYMBOLS = ("hyq_status_string", "hyq_config_check", "hyq_vl_count", "hyq_layout_sizes",
            "hyq_workspace_size", "hyq_layout_reset", "hyq_quantize_append",
            "hyq_select_vertical", "hyq_rebuild", "hyq_decode_append", "hyq_decode_attention",
-           "hyq_decode_attention_noalloc", "hyq_read_device_error", "hyq_set_decode_plan")
+           "hyq_decode_attention_noalloc", "hyq_read_device_error", "hyq_set_decode_plan",
+           "hyq_prefill_attention")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -93,6 +95,9 @@ def load() -> ctypes.CDLL:
                                                    c_void_p]),
         "hyq_read_device_error": (c_int32, [c_void_p, P(c_int32), c_void_p]),
         "hyq_set_decode_plan": (c_int32, [c_int32, c_int32]),
+        "hyq_prefill_attention": (c_int32, [P(HyqConfig), c_int32, c_void_p, c_int32, c_void_p, c_void_p,
+                                            c_int32, c_int32, c_void_p, c_int32, c_void_p, c_void_p,
+                                            c_void_p, c_size_t, c_void_p]),
     }
     for name in SYMBOLS:
         fn = getattr(lib, name)
@@ -198,6 +203,20 @@ def hyq_decode_attention_noalloc(cfg, q, lay: HyqLayout, out, len_hint: int = 0,
     GPU race on the shared scratch."""
     _check("hyq_decode_attention_noalloc", load().hyq_decode_attention_noalloc(
         ctypes.byref(cfg), ptr(q), ctypes.byref(lay), ptr(out), len_hint, stream_ptr(stream)))
+
+
+def hyq_prefill_attention(cfg, dtype: int, q, k, v, L: int, vl_idx, kvl: int, out, ws, err=None,
+                          stream=None):
+    """q [B, HQ, ldq, 128]; k, v [B, HKV, ldk, 128] (bf16 views with dense
+    rows); vl_idx int32 [B, HKV, kvl] contiguous (or None when kvl = 0);
+    out bf16 [B, HQ, L, 128] contiguous; err int32 [1] device or None."""
+    ldk = row_ld(k)
+    if row_ld(v) != ldk:
+        raise ValueError("k and v must share the leading dimension")
+    _check("hyq_prefill_attention", load().hyq_prefill_attention(
+        ctypes.byref(cfg), dtype, ptr(q), row_ld(q), ptr(k), ptr(v), ldk, L,
+        ptr(vl_idx) if kvl > 0 else None, kvl, ptr(out), ptr(err), ptr(ws),
+        ws.numel() * ws.element_size(), stream_ptr(stream)))
 
 
 DECODE_PLAN_AUTO, DECODE_PLAN_DIRECT, DECODE_PLAN_CLUSTER, DECODE_PLAN_GLOBAL = range(4)

@@ -253,6 +253,41 @@ hyq_status hyq_decode_attention(const hyq_config *cfg, const void *q, const hyq_
                                 hyq_stream_t stream);
 
 /*
+ * Hybrid-precision prefill attention, §4.2 Eq. 6-7 and Algorithm 2 (Appendix
+ * A.2), causal, for every query row i < L and query head h (KV head h / g):
+ *   out_{h,i} = softmax_j(x_j) . v_j over j <= i, a = 1/sqrt(128), where for
+ *   j in the full-precision set (the vertical lines vl_idx and the last W
+ *   positions [P, L), P = max(0, L - W)) x_j = a q_i . k_j and v_j are the BF16
+ *   rows, and for the other positions of [0, P) (the quantised prefix)
+ *   x_j = a q^_i . k^_j and v_j = v^_j, with
+ *   - the quantised-prefix positions taken in ascending order and cut into
+ *     tiles of 64 (the last one may be shorter); per tile one scale for K
+ *     and one for V: s = fl32(max|x| / c) over the tile, c = 127 (INT8) or
+ *     448 (FP8 e4m3);
+ *   - one scale for Q per block of 128 consecutive rows of one head
+ *     (rows 128m .. 128m+127, those < L);
+ *   - codes of t = fl32(x / s): INT8 rint (ties to even) clamped to +-127,
+ *     FP8 the nearest e4m3 value (ties to even, saturating); x^ = code * s.
+ *   dtype  HYQ_PREFILL_INT8 or HYQ_PREFILL_FP8
+ *   q      device bf16 [B][HQ][ldq][128]; rows 0..L-1 are used
+ *   k, v   device bf16 [B][HKV][ldk][128]
+ *   vl_idx device int32 [B][HKV][kvl], strictly ascending in [0, P)
+ *          (e.g. from hyq_select_vertical); kvl may be 0
+ *   out    device bf16 [B][HQ][L][128]
+ *   err    device int32 [1] or NULL: HYQ_DEVERR_INDEX for an invalid vl_idx
+ *          (the output is then unspecified), HYQ_DEVERR_TIMEOUT
+ * The softmax probabilities enter the P.V product rounded to BF16 (the value
+ * scale folded in); all products accumulate in float32.
+ * Workspace: hyq_workspace_size(cfg, HYQ_OP_PREFILL, L) covers every call
+ * with context length <= L and kvl <= hyq_vl_count(cfg, P); it needs no
+ * zero fill.  L > capacity returns HYQ_ERR_CAPACITY.
+ */
+hyq_status hyq_prefill_attention(const hyq_config *cfg, int32_t dtype, const void *q, int32_t ldq,
+                                 const void *k, const void *v, int32_t ldk, int32_t L,
+                                 const int32_t *vl_idx, int32_t kvl, void *out, int32_t *err,
+                                 void *ws, size_t ws_bytes, hyq_stream_t stream);
+
+/*
  * Override how hyq_decode_attention splits and merges its work (process-
  * wide; for tuning and testing).  merge: 0 automatic (the default), 1 one
  * block per (batch, KV head) and no merge, 2 `splits` blocks (2..16) merged

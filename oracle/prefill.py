@@ -73,11 +73,19 @@ def quantize_symmetric(x, axis, dtype: str):
 
 
 def hybrid_prefill(q, k, v, vl_idx, window: int, dtype: str = "int8",
-                   key_tile: int = KEY_TILE, query_block: int = QUERY_BLOCK):
+                   key_tile: int = KEY_TILE, query_block: int = QUERY_BLOCK,
+                   query_blocks=None, heads=None, return_abs: bool = False):
     """Eq. 7 with Algorithm 2's quantisation, causal, float64.
 
     q [B, HQ, L, d]; k, v [B, HKV, L, d]; vl_idx [B, HKV, k] (positions in
     [0, L - W), or None).  Returns o [B, HQ, L, d] float64.
+    ``query_blocks`` / ``heads`` (optional lists) restrict which 128-row query
+    blocks and query heads are computed (the others stay zero); each block's
+    result does not depend on the others.
+    With ``return_abs`` the function also returns ``a = sum_j p_j |v_j| /
+    sum_j p_j`` (the same softmax weights applied to the magnitudes of the
+    effective values): ``2^-8 a`` bounds what rounding the probabilities to
+    BF16 (unit roundoff 2^-8) before the P.V product can change in ``o``.
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -88,6 +96,7 @@ def hybrid_prefill(q, k, v, vl_idx, window: int, dtype: str = "int8",
     alpha = 1.0 / math.sqrt(d)
     P = max(0, L - window)
     out = np.zeros_like(q)
+    mag = np.zeros_like(q)
     for b in range(B):
         for kh in range(HKV):
             vl = (np.zeros(0, np.int64) if vl_idx is None
@@ -106,7 +115,11 @@ def hybrid_prefill(q, k, v, vl_idx, window: int, dtype: str = "int8",
             Vall = np.concatenate([vq, v[b, kh, fp]])
             nq = len(qpos)
             for h in range(kh * g, (kh + 1) * g):
+                if heads is not None and h not in heads:
+                    continue
                 for r0 in range(0, L, query_block):
+                    if query_blocks is not None and r0 // query_block not in query_blocks:
+                        continue
                     rows = np.arange(r0, min(L, r0 + query_block))
                     qb = q[b, h, rows]
                     qhat = quantize_symmetric(qb, None, dtype)[0]
@@ -118,7 +131,9 @@ def hybrid_prefill(q, k, v, vl_idx, window: int, dtype: str = "int8",
                     m = lg.max(axis=1, keepdims=True)
                     e = np.exp(lg - m)
                     out[b, h, rows] = (e @ Vall) / e.sum(axis=1, keepdims=True)
-    return out
+                    if return_abs:
+                        mag[b, h, rows] = (e @ np.abs(Vall)) / e.sum(axis=1, keepdims=True)
+    return (out, mag) if return_abs else out
 
 
 def causal_attention(q, k, v) -> np.ndarray:

@@ -39,3 +39,23 @@ def mixed_rows(seed, shape):
             flat[s, 2, 0], flat[s, 2, 1] = 0.0, 15.0
             flat[s, 3, 32:64] = 1e-6 * torch.randn(32, generator=g)  # subnormal-size step
     return x.to(torch.bfloat16)
+
+
+# Prefill: the probabilities enter the P.V product rounded to BF16 (unit
+# roundoff 2^-8), which can move an output element by at most 2^-8 times the
+# softmax-weighted mean of |v| over its keys (``a`` from the oracle).
+P_ROUND = 2.0 ** -8
+
+
+def assert_prefill_close(got, want, a, what=""):
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    a = np.asarray(a, dtype=np.float64)
+    assert got.shape == want.shape == a.shape
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    err = np.abs(got - want)
+    bound = ATOL + RTOL * np.abs(want) + P_ROUND * a
+    bad = err > bound
+    assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} outside tolerance; "
+                           f"max abs err {err.max():.3e}, worst excess {(err - bound).max():.3e}")
+    return float(err.max())

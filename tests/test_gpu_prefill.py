@@ -1,0 +1,120 @@
+"""GPU parity of the hybrid prefill operator (Eq. 6-7, Algorithm 2) against
+the oracle's float64 restatement, INT8 and FP8 main paths.
+
+The vertical-line set fed to the GPU is the oracle's own selection from the
+last min(64, L) queries, so the attention comparison does not depend on
+selection parity.  Tolerance: |gpu - oracle| <= 2e-3 + 1e-2 |oracle| + 2^-8 a,
+where a = sum_j p_j |v_j| / sum_j p_j from the oracle: the last term bounds
+the kernel's rounding of the probabilities to BF16 before the P.V product
+(unit roundoff 2^-8), a step the oracle does not take.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gen import prefill_case
+from hybrid_precision_quantized_gb300 import _lib as L
+from hybrid_precision_quantized_gb300 import hyq_prefill_attention, hyq_read_device_error, make_config, workspace
+from oracle.prefill import hybrid_prefill
+from oracle.select import select_vertical
+from tests.gpu_util import assert_prefill_close, to_np
+
+pytestmark = pytest.mark.gpu
+
+DT = {"int8": L.PREFILL_INT8, "fp8": L.PREFILL_FP8}
+
+
+def vl_for(c, Lc, W, ppm):
+    q = c.q.double().numpy()
+    n_proxy = min(64, Lc)
+    idx, _ = select_vertical(q[:, :, Lc - n_proxy:Lc], c.k.double().numpy(), Lc, W, ppm)
+    return idx
+
+
+def run_gpu(c, Lc, W, ppm, dtype, idx, ws_len=None):
+    B, HQ = c.q.shape[:2]
+    HKV = c.k.shape[1]
+    cfg = make_config(B, HQ, HKV, capacity=max(Lc, ws_len or 0, 1), window=W, rho_ppm=ppm)
+    kvl = idx.shape[-1]
+    vl = torch.from_numpy(np.ascontiguousarray(idx)).to(torch.int32).cuda() if kvl else None
+    ws = workspace(cfg, L.OP_PREFILL, ws_len or Lc)
+    out = torch.full((B, HQ, Lc, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    hyq_prefill_attention(cfg, DT[dtype], c.q.cuda(), c.k.cuda(), c.v.cuda(), Lc, vl, kvl, out, ws, err)
+    torch.cuda.synchronize()
+    assert hyq_read_device_error(err) == 0
+    return to_np(out)
+
+
+@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+@pytest.mark.parametrize("seed,B,HQ,HKV,Lc,W,ppm", [
+    (1, 1, 4, 2, 300, 64, 50_000),      # a few tiles, ragged tails in both lists
+    (2, 1, 8, 2, 1000, 128, 50_000),
+    (3, 2, 4, 4, 515, 128, 20_000),     # two sequences, MHA
+    (4, 1, 16, 2, 777, 100, 50_000),    # g = 8
+    (5, 1, 6, 2, 1100, 128, 100_000),   # g = 3, more vertical lines
+])
+def test_prefill_parity(hyq, dtype, seed, B, HQ, HKV, Lc, W, ppm):
+    c = prefill_case(seed, B, HQ, HKV, Lc, window=W, sink_frac=0.02)
+    idx = vl_for(c, Lc, W, ppm)
+    got = run_gpu(c, Lc, W, ppm, dtype, idx)
+    want, a = hybrid_prefill(c.q.double().numpy(), c.k.double().numpy(), c.v.double().numpy(), idx, W, dtype,
+                             return_abs=True)
+    assert_prefill_close(got, want, a, what=f"{dtype} L={Lc}")
+
+
+@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+@pytest.mark.parametrize("Lc,W,ppm,what", [
+    (1, 128, 50_000, "single position"),
+    (100, 128, 50_000, "sequence inside the window: all BF16"),
+    (129, 128, 50_000, "P = 1"),
+    (600, 0, 0, "rho = 0, W = 0: all quantised"),
+    (600, 64, 1_000_000, "rho = 100%: no quantised keys"),
+    (256, 64, 0, "exactly one quantised MMA tile and a window"),
+    (257, 0, 0, "two query blocks, one row in the second"),
+])
+def test_prefill_edge_cases(hyq, dtype, Lc, W, ppm, what):
+    c = prefill_case(21, 1, 4, 2, Lc, window=W, sink_frac=0.03)
+    idx = vl_for(c, Lc, W, ppm) if W < Lc else np.zeros((1, 2, 0), np.int64)
+    got = run_gpu(c, Lc, W, ppm, dtype, idx)
+    want, a = hybrid_prefill(c.q.double().numpy(), c.k.double().numpy(), c.v.double().numpy(),
+                             idx if idx.shape[-1] else None, W, dtype, return_abs=True)
+    assert_prefill_close(got, want, a, what=what)
+
+
+def test_prefill_workspace_reuse_and_larger_hint(hyq):
+    """A workspace sized for a longer context serves a shorter call; two calls
+    give identical bits."""
+    c = prefill_case(31, 1, 8, 2, 700, window=128)
+    idx = vl_for(c, 700, 128, 50_000)
+    a = run_gpu(c, 700, 128, 50_000, "fp8", idx, ws_len=2048)
+    b = run_gpu(c, 700, 128, 50_000, "fp8", idx)
+    np.testing.assert_array_equal(a, b)
+
+
+def test_prefill_bad_vertical_lines_flagged(hyq):
+    c = prefill_case(32, 1, 4, 2, 400, window=64)
+    cfg = make_config(1, 4, 2, capacity=400, window=64, rho_ppm=50_000)
+    vl = torch.tensor([[[5, 3, 9]] * 2], dtype=torch.int32, device="cuda")   # not ascending
+    ws = workspace(cfg, L.OP_PREFILL, 400)
+    out = torch.empty(1, 4, 400, 128, dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    hyq_prefill_attention(cfg, L.PREFILL_FP8, c.q.cuda(), c.k.cuda(), c.v.cuda(), 400, vl, 3, out, ws, err)
+    torch.cuda.synchronize()
+    assert hyq_read_device_error(err) & L.DEVERR_INDEX
+
+
+@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+def test_prefill_llama_shaped_8k_sampled(hyq, dtype):
+    """Llama-3.1-8B-shaped heads at 8K: every head of four query blocks (first,
+    two middle, last) against the oracle."""
+    Lc, W, ppm = 8192, 128, 50_000
+    c = prefill_case(1005, 1, 32, 8, Lc, window=W, sink_frac=0.02)
+    idx = vl_for(c, Lc, W, ppm)
+    got = run_gpu(c, Lc, W, ppm, dtype, idx)
+    blocks = [0, 17, 40, Lc // 128 - 1]
+    want, a = hybrid_prefill(c.q.double().numpy(), c.k.double().numpy(), c.v.double().numpy(), idx, W, dtype,
+                             query_blocks=blocks, return_abs=True)
+    for blk in blocks:
+        rows = slice(128 * blk, 128 * blk + 128)
+        assert_prefill_close(got[:, :, rows], want[:, :, rows], a[:, :, rows], what=f"{dtype} block {blk}")

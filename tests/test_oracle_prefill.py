@@ -154,3 +154,30 @@ def test_value_tiles_share_one_scale():
     o = hybrid_prefill(q, k, v, None, window=W, dtype="int8")
     assert np.all(o[:, :, :L - W, 1:] == 0.0)
     assert np.all(o[:, :, L - W:, 1:] != 0.0)
+
+
+def test_restricted_blocks_equal_full_computation():
+    c = prefill_case(7, 1, 4, 2, 300, d=64, window=32)
+    q, k, v = _np(c)
+    idx, _ = select_vertical(q[:, :, -32:], k, 300, 32, 50_000)
+    full = hybrid_prefill(q, k, v, idx, window=32, dtype="fp8")
+    part = hybrid_prefill(q, k, v, idx, window=32, dtype="fp8", query_blocks=[0, 2], heads=[1, 2])
+    for h in (1, 2):
+        for blk in (0, 2):
+            rows = slice(128 * blk, min(300, 128 * blk + 128))
+            np.testing.assert_array_equal(part[0, h, rows], full[0, h, rows])
+    assert np.all(part[0, 0] == 0) and np.all(part[0, 1, 128:256] == 0)
+
+
+@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+def test_abs_weighted_values(dtype):
+    """``a`` is the operator applied to |V| (symmetric quantisation commutes
+    with |.|), and bounds |o| by the triangle inequality."""
+    c = prefill_case(8, 1, 4, 2, 260, d=64, window=32)
+    q, k, v = _np(c)
+    idx, _ = select_vertical(q[:, :, -32:], k, 260, 32, 50_000)
+    o, a = hybrid_prefill(q, k, v, idx, window=32, dtype=dtype, return_abs=True)
+    np.testing.assert_array_equal(o, hybrid_prefill(q, k, v, idx, window=32, dtype=dtype))
+    np.testing.assert_allclose(a, hybrid_prefill(q, k, np.abs(v), idx, window=32, dtype=dtype),
+                               rtol=1e-13, atol=1e-15)
+    assert np.all(a >= np.abs(o) - 1e-15)
