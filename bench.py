@@ -48,8 +48,12 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--layers", type=int, default=N_LAYERS)
     p.add_argument("--no-baseline", action="store_true", help="skip the CPU oracle timing")
-    p.add_argument("--case", default="period", choices=["period", "decode-layer"],
-                   help="decode-layer: one 32K layer, a few decode launches (a small profiling target)")
+    p.add_argument("--case", default="period", choices=["period", "decode-layer", "prefill"],
+                   help="decode-layer: one 32K layer, a few decode launches (a small profiling target); "
+                        "prefill: the hybrid prefill operator alone")
+    p.add_argument("--prefill-len", type=int, nargs="*", default=None,
+                   help="sequence lengths for --case prefill (default 8192 32768)")
+    p.add_argument("--prefill-reps", type=int, default=5)
     return p.parse_args()
 
 
@@ -81,6 +85,96 @@ def run_decode_layer_case(args, local):
     torch.cuda.synchronize()
     print(json.dumps({"case": "decode-layer", "us_per_launch_l2_warm": e0.elapsed_time(e1) * 1e3 / 4,
                       "device_error_word": hyq.hyq_read_device_error(layer.err())}))
+
+
+def measured_tensor_peaks():
+    """Dense BF16 burst peak (measured) and the FP8 figure derived from it
+    with the nominal FP8/BF16 ratio (4.5 / 2.25 PFLOP/s = 2)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            bf16 = float(json.load(f)["bf16_tflops"])
+        kind = "measured bf16 burst"
+    except Exception:
+        bf16, kind = 1900.0, "fallback bf16"
+    return {"bf16": bf16, "fp8": 2.0 * bf16, "source": kind}
+
+
+def prefill_inputs(dev, Lc, seed=1005):
+    """Llama-shaped causal prefill inputs on the device: N(0,1) K/V, 2% planted
+    vertical-line keys (4u + noise), queries N(0,1) + 2u."""
+    import torch
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    P = max(0, Lc - WINDOW)
+    u = torch.randn(B, HKV, D, generator=g, device=dev)
+    u = u / u.norm(dim=-1, keepdim=True)
+    k = torch.randn(B, HKV, Lc, D, generator=g, device=dev)
+    ns = int(0.02 * P)
+    for h in range(HKV):
+        pos = torch.randperm(P, generator=g, device=dev)[:ns]
+        k[0, h, pos] += 4.0 * u[0, h]
+    v = torch.randn(B, HKV, Lc, D, generator=g, device=dev)
+    uq = u.repeat_interleave(HQ // HKV, dim=1)
+    q = torch.randn(B, HQ, Lc, D, generator=g, device=dev) + 2.0 * uq[:, :, None]
+    return q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16)
+
+
+def prefill_measure(dev, lengths, reps=5, warmup=3):
+    """Time hyq_prefill_attention (pack + main kernel) per length and dtype with
+    CUDA events, L2 flushed (a 256 MB write) before every timed call.  The
+    vertical-line set comes from hyq_select_vertical on the last 64 queries."""
+    import torch
+    import hybrid_precision_quantized_gb300 as hyq
+    from hybrid_precision_quantized_gb300 import _lib as L
+    peaks = measured_tensor_peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    res = []
+    for Lc in lengths:
+        cfg = hyq.make_config(B, HQ, HKV, capacity=Lc, window=WINDOW, rho_ppm=RHO_PPM)
+        q, k, v = prefill_inputs(dev, Lc)
+        kmax = max(1, hyq.hyq_vl_count(cfg, max(0, Lc - WINDOW)))
+        idx = torch.zeros(B, HKV, kmax, dtype=torch.int32, device=dev)
+        kvl = hyq.hyq_select_vertical(cfg, q[:, :, Lc - 64:], 64, k, Lc, idx,
+                                      hyq.workspace(cfg, L.OP_SELECT, Lc, dev))
+        ws = hyq.workspace(cfg, L.OP_PREFILL, Lc, dev)
+        out = torch.empty(B, HQ, Lc, D, dtype=torch.bfloat16, device=dev)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        flops = 4.0 * D * HQ * Lc * (Lc + 1) / 2
+        for name, dt in (("fp8", L.PREFILL_FP8), ("int8", L.PREFILL_INT8)):
+            for _ in range(warmup):
+                hyq.hyq_prefill_attention(cfg, dt, q, k, v, Lc, idx, kvl, out, ws, err)
+            times = []
+            for _ in range(reps):
+                flush.fill_(1)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                hyq.hyq_prefill_attention(cfg, dt, q, k, v, Lc, idx, kvl, out, ws, err)
+                e1.record()
+                torch.cuda.synchronize()
+                times.append(e0.elapsed_time(e1))
+            ms = statistics.median(times)
+            tf = flops / (ms * 1e-3) / 1e12
+            peak = peaks["fp8"] if name == "fp8" else peaks["bf16"]
+            res.append({"seq_len": Lc, "dtype": name, "ms": ms, "tflops": tf,
+                        "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
+                                     "frac": tf / peak,
+                                     "peak_source": (peaks["source"] + (" x 2 (nominal fp8/bf16)" if name == "fp8"
+                                                                        else " (INT8 codes run on the bf16 pipe)"))},
+                        "device_error_word": hyq.hyq_read_device_error(err)})
+        del q, k, v, out, ws
+    return res
+
+
+def run_prefill_case(args, local):
+    import torch
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import hybrid_precision_quantized_gb300 as hyq
+    hyq.load()
+    lengths = args.prefill_len or [8192, 32768]
+    print(json.dumps({"case": "prefill", "workload": "llama3.1-8b-shaped causal prefill, B1, 32/8 heads, d128, "
+                                                     "W128, rho 5%",
+                      "flops": "4 d HQ L(L+1)/2", "results": prefill_measure(dev, lengths, args.prefill_reps)}))
 
 
 def dist_setup(args):
@@ -394,6 +488,8 @@ def main():
     rank, world, local = dist_setup(args)
     if args.case == "decode-layer":
         run_decode_layer_case(args, local)
+    elif args.case == "prefill":
+        run_prefill_case(args, local)
     elif args.impl == "reference":
         run_reference(args, rank, world)
     else:

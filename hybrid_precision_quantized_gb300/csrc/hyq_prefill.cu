@@ -15,11 +15,12 @@
 //     main kernel moves each 128-key tile with one bulk copy.  Values are
 //     stored transposed (dims x keys) for the P.V product.
 //  2. prefill_kernel (stage 3): one CTA per (query block of 128 rows, query
-//     head).  Warp 4 streams key/value tiles (bulk copies, 2-stage rings);
-//     warp 5 issues tcgen05.mma: S = Q K^T into TMEM (double buffer), then
-//     O += P V into TMEM; warps 0-3 (one thread per query row = TMEM lane)
-//     read S, scale, mask, run the online softmax and write P back to shared
-//     memory.  The quantised segment uses e4m3 codes (kind::f8f6f4) or INT8
+//     head).  Warps 8 and 9 stream key and value tiles (bulk copies, one
+//     2-stage ring each); warp 10 issues tcgen05.mma: S = Q K^T into TMEM (double buffer), then
+//     O_h += P_h V_h into TMEM for the two 64-key halves h of each tile;
+//     warps 0-7 (one thread per query row = TMEM lane and key half) read S,
+//     scale, mask, run an online softmax per half and write P back to
+//     shared memory; the two halves' (max, sum, O) merge once at the end.  The quantised segment uses e4m3 codes (kind::f8f6f4) or INT8
 //     codes held exactly as BF16 integers (kind::f16; sm_103a has no integer
 //     tensor-core MMA); the full-precision segment uses BF16.  P.V runs in
 //     BF16 with the value codes (exact in BF16) and the value scale folded
@@ -42,10 +43,12 @@ constexpr int kScaleTile = 64;       // keys per quantisation scale (B_N)
 constexpr int kRegion = 16384;       // 128 rows x 128 bytes, swizzled
 constexpr int kImg16 = 2 * kRegion;  // 128 x 128 16-bit operand image
 constexpr int kImg8 = kRegion;       // 128 x 128 8-bit operand image
-constexpr int kSoft = 128;           // softmax threads (warps 0-3)
-constexpr int kThreads = 192;        // + copy warp (4) + MMA warp (5)
+constexpr int kSoft = 256;           // softmax threads (warps 0-7)
+constexpr int kCopyWarp = 8, kMmaWarp = 10;  // copy warps 8 (keys) and 9 (values)
+constexpr int kThreads = 352;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+// TMEM columns: S double buffer, then one O accumulator per key half.
+constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Shared-memory map (offsets from a 1024-byte aligned base).
@@ -55,7 +58,7 @@ constexpr int kOffK = kOffQc + kImg16;     // 2 key stages
 constexpr int kOffV = kOffK + 2 * kImg16;  // 2 value stages (transposed)
 constexpr int kOffP = kOffV + 2 * kImg16;  // probabilities, BF16 image
 constexpr int kOffBar = kOffP + kImg16;
-constexpr int kNumBars = 16;
+constexpr int kNumBars = 18;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemUsed = kOffMisc + 64;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // room to align the base
@@ -129,6 +132,33 @@ __device__ __forceinline__ int count_le(const int32_t* a, int n, int32_t x) {
     else hi = mid;
   }
   return lo;
+}
+
+// Warp-cooperative count of the entries <= x in the ascending a[0..n): 32
+// probes per round, so a 32K-entry list takes 3-4 dependent loads.
+__device__ __forceinline__ int warp_count_le(const int32_t* a, int n, int32_t x, int lane) {
+  int lo = 0, hi = n;  // invariant: a[i] <= x for i < lo, a[i] > x for i >= hi
+  while (lo < hi) {
+    const int step = (hi - lo + 31) >> 5;
+    const int idx = lo + lane * step;
+    const bool le = idx < hi && __ldg(a + idx) <= x;
+    const int cnt = __popc(__ballot_sync(0xffffffffu, le));
+    if (cnt == 0) {
+      hi = lo;
+    } else {
+      const int nlo = lo + (cnt - 1) * step + 1;
+      hi = min(hi, lo + cnt * step);
+      lo = nlo;
+    }
+  }
+  return lo;
+}
+
+// 2^x on the special-function unit (flushes subnormal results to zero).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ float block_max(float v, float* red, int nwarps) {
@@ -315,13 +345,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   uint64_t* vempty = bars + 7;  // [2]
   uint64_t* sfull = bars + 9;   // [2]
   uint64_t* sfree = bars + 11;  // [2]
-  uint64_t* pfull = bars + 13;
-  uint64_t* pvdone = bars + 14;
-  uint64_t* mmadone = bars + 15;
+  uint64_t* pfull = bars + 13;  // [2], one per key half
+  uint64_t* pvdone = bars + 15; // [2]
+  uint64_t* mmadone = bars + 17;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kOffMisc + 4);
-  int* ntiles = reinterpret_cast<int*>(sm + kOffMisc + 8);  // [2]
-  float* red = reinterpret_cast<float*>(sm + kOffMisc + 32);  // [4]
+  int* ntiles = reinterpret_cast<int*>(sm + kOffMisc + 8);     // [4]
+  float* red = reinterpret_cast<float*>(sm + kOffMisc + 32);   // [8]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.x, b = blockIdx.z;
@@ -344,51 +374,70 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       mbar_init(vempty + i, 1);
       mbar_init(sfull + i, 1);
       mbar_init(sfree + i, kSoft);
+      mbar_init(pfull + i, kSoft / 2);
+      mbar_init(pvdone + i, 1);
     }
-    mbar_init(pfull, kSoft);
-    mbar_init(pvdone, 1);
     mbar_init(mmadone, 1);
     mbar_fence_init();
     *abort_flag = 0;
-    ntiles[0] = (count_le(kpos, p.ntq * kKeys, rlast) + kKeys - 1) / kKeys;
-    ntiles[1] = (count_le(fpos, p.ntf * kKeys, rlast) + kKeys - 1) / kKeys;
   }
-  if (warp == 5) tc_alloc(tslot, kTmemCols);
+  if (warp == kCopyWarp) {
+    const int cq1 = warp_count_le(kpos, p.ntq * kKeys, rlast, lane);
+    const int cf1 = warp_count_le(fpos, p.ntf * kKeys, rlast, lane);
+    const int cq0 = warp_count_le(kpos, p.ntq * kKeys, r0, lane);
+    const int cf0 = warp_count_le(fpos, p.ntf * kKeys, r0, lane);
+    if (lane == 0) {
+      ntiles[0] = (cq1 + kKeys - 1) / kKeys;
+      ntiles[1] = (cf1 + kKeys - 1) / kKeys;
+      // tiles before these hold only keys <= r0 (no mask needed for any row)
+      ntiles[2] = cq0 / kKeys;
+      ntiles[3] = cf0 / kKeys;
+    }
+  }
+  if (warp == kMmaWarp) tc_alloc(tslot, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tslot;
   const int nqt = ntiles[0], nt = ntiles[0] + ntiles[1];
+  const int mask_q = ntiles[2], mask_f = ntiles[3];
 
   if (tid < kSoft) {
     // ---------------- softmax / epilogue warps --------------------------
-    const int row = r0 + tid;
+    // Thread = (query row, key half): warps 0-3 take keys 0-63 of every
+    // tile, warps 4-7 keys 64-127, each half with its own online-softmax
+    // state and its own O accumulator in TMEM; the halves merge at the end.
+    const int hf = tid >> 7;           // key half
+    const int rr = tid & (kRows - 1);  // row in the block = TMEM lane
+    const int row = r0 + rr;
     const bool rvalid = row <= rlast;
     auto fail = [&]() {
       *abort_flag = 1;
       hyq_set_err(p.err, HYQ_DEVERR_TIMEOUT);
     };
-    // Query row -> BF16 image and code image.
-    uint4 qv[16];
-    const uint4* qrow =
-        reinterpret_cast<const uint4*>(p.q + (((size_t)b * p.HQ + h) * p.ldq + (rvalid ? row : 0)) * HYQ_D);
+    // Query row (dims 64hf .. 64hf+63) -> BF16 image and code image.
+    uint4 qv[8];
+    const uint4* qrow = reinterpret_cast<const uint4*>(
+        p.q + (((size_t)b * p.HQ + h) * p.ldq + (rvalid ? row : 0)) * HYQ_D + 64 * hf);
 #pragma unroll
-    for (int c = 0; c < 16; ++c) qv[c] = rvalid ? __ldg(qrow + c) : make_uint4(0, 0, 0, 0);
+    for (int c = 0; c < 8; ++c) qv[c] = rvalid ? __ldg(qrow + c) : make_uint4(0, 0, 0, 0);
     float amax = 0.f;
 #pragma unroll
-    for (int c = 0; c < 16; ++c) {
+    for (int c = 0; c < 8; ++c) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(bf16_at(qv[c], e)));
-      *reinterpret_cast<uint4*>(sm + kOffQ + (c >> 3) * kRegion + swz(tid, c & 7)) = qv[c];
+      *reinterpret_cast<uint4*>(sm + kOffQ + hf * kRegion + swz(rr, c)) = qv[c];
     }
     amax = warp_max_xor(amax, 1);
     if (lane == 0) red[warp] = amax;
-    asm volatile("bar.sync 1, 128;\n" ::: "memory");
-    amax = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    asm volatile("bar.sync 1, 256;\n" ::: "memory");
+    amax = red[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[w]);
     const float sq = __fdiv_rn(amax, kFp8 ? 448.f : 127.f);
     if (kFp8) {
 #pragma unroll
-      for (int c16 = 0; c16 < 8; ++c16) {
+      for (int c16 = 0; c16 < 4; ++c16) {  // 16 codes per chunk: chunks 4hf .. 4hf+3
         uint32_t w[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -402,11 +451,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           }
           w[u] = acc;
         }
-        *reinterpret_cast<uint4*>(sm + kOffQc + swz(tid, c16)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(sm + kOffQc + swz(rr, 4 * hf + c16)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
     } else {
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
+      for (int c = 0; c < 8; ++c) {
         uint32_t w[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -415,19 +464,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           const float t1 = sq > 0.f ? __fdiv_rn(x1, sq) : 0.f;
           w[e] = pack_bf16x2(code_i8(t0), code_i8(t1));
         }
-        *reinterpret_cast<uint4*>(sm + kOffQc + (c >> 3) * kRegion + swz(tid, c & 7)) =
-            make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(sm + kOffQc + hf * kRegion + swz(rr, c)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
     fence_proxy_async_smem();
     mbar_arrive(qready);
 
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const float* skp = p.sk + bh * p.ntq * 2;
-    const float* svp = p.sv + bh * p.ntq * 2;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tO = tbase + lane_off + (hf ? kColO1 : kColO0);
+    const float* skp = p.sk + bh * p.ntq * 2 + hf;
+    const float* svp = p.sv + bh * p.ntq * 2 + hf;
     const float qfac = p.alpha_log2e * sq;
     float m_used = -INFINITY, l_sum = 0.f;
     bool ok = true;
+    // this half's scales for the current tile, loaded a tile ahead
+    float2 sc = nqt > 0 ? make_float2(__ldg(skp), __ldg(svp)) : make_float2(0.f, 1.f);
     for (int j = 0; j < nt; ++j) {
       const int s = j & 1;
       const bool quant = j < nqt;
@@ -437,46 +488,32 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         break;
       }
       tc_fence_after();
-      float x[128];
+      float x[64];
       {
-        uint32_t r0v[32], r1v[32], r2v[32], r3v[32];
-        const uint32_t ts = tbase + lane_off + (s ? kColS1 : kColS0);
-        tc_ld32(ts + 0, r0v);
-        tc_ld32(ts + 32, r1v);
-        tc_ld32(ts + 64, r2v);
-        tc_ld32(ts + 96, r3v);
+        uint32_t ra[32], rb[32];
+        const uint32_t ts = tbase + lane_off + (s ? kColS1 : kColS0) + 64 * hf;
+        tc_ld32(ts, ra);
+        tc_ld32(ts + 32, rb);
         tc_wait_ld();
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          x[i] = __uint_as_float(r0v[i]);
-          x[32 + i] = __uint_as_float(r1v[i]);
-          x[64 + i] = __uint_as_float(r2v[i]);
-          x[96 + i] = __uint_as_float(r3v[i]);
+          x[i] = __uint_as_float(ra[i]);
+          x[32 + i] = __uint_as_float(rb[i]);
         }
       }
       tc_fence_before();
       mbar_arrive(sfree + s);
 
-      const int32_t* tpos = quant ? kpos + j * kKeys : fpos + (j - nqt) * kKeys;
-      float cs0, cs1, vf0, vf1;
-      if (quant) {
-        cs0 = qfac * __ldg(skp + 2 * j);
-        cs1 = qfac * __ldg(skp + 2 * j + 1);
-        vf0 = __ldg(svp + 2 * j);
-        vf1 = __ldg(svp + 2 * j + 1);
-      } else {
-        cs0 = cs1 = p.alpha_log2e;
-        vf0 = vf1 = 1.f;
-      }
+      // A scale is 0 only when every code it multiplies is 0; keeping it
+      // positive changes no score and makes masked (-inf) keys give 0.
+      const float cs = quant ? fmaxf(qfac * sc.x, 1.17549435e-38f) : p.alpha_log2e;
+      const float vf = quant ? sc.y : 1.f;
+      if (j + 1 < nqt) sc = make_float2(__ldg(skp + 2 * j + 2), __ldg(svp + 2 * j + 2));
+      const bool masked = quant ? j >= mask_q : j - nqt >= mask_f;  // some key after some row
+      if (masked) {
+        const int4* pp = reinterpret_cast<const int4*>((quant ? kpos + j * kKeys : fpos + (j - nqt) * kKeys) + 64 * hf);
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        x[i] *= cs0;
-        x[64 + i] *= cs1;
-      }
-      if (__ldg(tpos + kKeys - 1) > r0) {  // some key of this tile is after some row
-        const int4* pp = reinterpret_cast<const int4*>(tpos);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
+        for (int c = 0; c < 16; ++c) {
           const int4 q4 = __ldg(pp + c);
           if (q4.x > row) x[4 * c] = -INFINITY;
           if (q4.y > row) x[4 * c + 1] = -INFINITY;
@@ -484,25 +521,32 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           if (q4.w > row) x[4 * c + 3] = -INFINITY;
         }
       }
-      float tmax = -INFINITY;
+      float a[8];
 #pragma unroll
-      for (int i = 0; i < 128; ++i) tmax = fmaxf(tmax, x[i]);
+      for (int u = 0; u < 8; ++u) a[u] = x[u];
+#pragma unroll
+      for (int i = 8; i < 64; ++i) a[i & 7] = fmaxf(a[i & 7], x[i]);
+      const float hmax = fmaxf(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])), fmaxf(fmaxf(a[4], a[5]), fmaxf(a[6], a[7])));
+      const float tmax = hmax == -INFINITY ? -INFINITY : hmax * cs;
       // Lazy maximum: rescale only when the row maximum grew by more than 2^8.
       const bool grow = tmax > m_used + 8.f;
       const float m_new = grow ? tmax : m_used;
-      const float fac = grow ? exp2f(m_used - m_new) : 1.f;
+      const float fac = grow ? fast_exp2(m_used - m_new) : 1.f;
       const float mb = (m_new == -INFINITY) ? 0.f : m_new;
-      float rs = 0.f;
+      float ps[8];
 #pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        x[i] = exp2f(x[i] - mb);
-        rs += x[i];
+      for (int u = 0; u < 8; ++u) ps[u] = 0.f;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        x[i] = fast_exp2(fmaf(x[i], cs, -mb));
+        ps[i & 7] += x[i];
       }
+      const float rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       l_sum = l_sum * fac + rs;
       m_used = m_new;
 
-      if (j > 0) {  // P.V of the previous tile done: O stable, P buffer free
-        if (!mbar_wait_or_abort(pvdone, (j - 1) & 1, abort_flag)) {
+      if (j > 0) {  // this half's P.V of the previous tile is done: O stable, P free
+        if (!mbar_wait_or_abort(pvdone + hf, (j - 1) & 1, abort_flag)) {
           fail();
           ok = false;
           break;
@@ -512,98 +556,112 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             uint32_t o[32];
-            const uint32_t to = tbase + lane_off + kColO + 32 * c;
-            tc_ld32(to, o);
+            tc_ld32(tO + 32 * c, o);
             tc_wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * fac);
-            tc_st32(to, o);
+            tc_st32(tO + 32 * c, o);
           }
           tc_wait_st();
         }
       }
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const float f = c < 8 ? vf0 : vf1;
-        const uint4 u = make_uint4(pack_bf16x2(x[8 * c] * f, x[8 * c + 1] * f),
-                                   pack_bf16x2(x[8 * c + 2] * f, x[8 * c + 3] * f),
-                                   pack_bf16x2(x[8 * c + 4] * f, x[8 * c + 5] * f),
-                                   pack_bf16x2(x[8 * c + 6] * f, x[8 * c + 7] * f));
-        *reinterpret_cast<uint4*>(sm + kOffP + (c >> 3) * kRegion + swz(tid, c & 7)) = u;
+      for (int c = 0; c < 8; ++c) {
+        const uint4 u = make_uint4(pack_bf16x2(x[8 * c] * vf, x[8 * c + 1] * vf),
+                                   pack_bf16x2(x[8 * c + 2] * vf, x[8 * c + 3] * vf),
+                                   pack_bf16x2(x[8 * c + 4] * vf, x[8 * c + 5] * vf),
+                                   pack_bf16x2(x[8 * c + 6] * vf, x[8 * c + 7] * vf));
+        *reinterpret_cast<uint4*>(sm + kOffP + hf * kRegion + swz(rr, c)) = u;
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(pfull);
+      mbar_arrive(pfull + hf);
     }
-    if (ok && nt > 0) {
-      if (!mbar_wait_or_abort(pvdone, (nt - 1) & 1, abort_flag)) {
-        fail();
-      } else {
-        tc_fence_after();
-        const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
-        uint4* orow = reinterpret_cast<uint4*>(p.out + (((size_t)b * p.HQ + h) * p.L + row) * HYQ_D);
+    // Merge the two halves.  Each half waits for its own last P.V, leaves
+    // (m, l) in its own P region (free from then on), and the named barrier
+    // makes both halves' accumulators and (m, l) visible to every thread;
+    // each thread then writes dims 64hf .. 64hf+63 of its row.
+    bool done = ok && nt > 0;
+    if (done && !mbar_wait_or_abort(pvdone + hf, (nt - 1) & 1, abort_flag)) {
+      fail();
+      done = false;
+    }
+    float* xch_own = reinterpret_cast<float*>(sm + kOffP + hf * kRegion);
+    const float* xch_oth = reinterpret_cast<const float*>(sm + kOffP + (hf ^ 1) * kRegion);
+    if (done) {
+      xch_own[rr] = m_used;
+      xch_own[kRows + rr] = l_sum;
+    }
+    tc_fence_before();
+    asm volatile("bar.sync 1, 256;\n" ::: "memory");
+    if (done && !*abort_flag) {
+      tc_fence_after();
+      const float ma = hf ? xch_oth[rr] : m_used, la = hf ? xch_oth[kRows + rr] : l_sum;
+      const float mb2 = hf ? m_used : xch_oth[rr], lb = hf ? l_sum : xch_oth[kRows + rr];
+      const float m = fmaxf(ma, mb2);
+      const float wa = ma == -INFINITY ? 0.f : fast_exp2(ma - m);
+      const float wb = mb2 == -INFINITY ? 0.f : fast_exp2(mb2 - m);
+      const float l = la * wa + lb * wb;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float fa = wa * inv, fb = wb * inv;
+      uint4* orow = reinterpret_cast<uint4*>(p.out + (((size_t)b * p.HQ + h) * p.L + row) * HYQ_D + 64 * hf);
+      const uint32_t ta = tbase + lane_off + kColO0 + 64 * hf, tb = tbase + lane_off + kColO1 + 64 * hf;
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t o[32];
-          tc_ld32(tbase + lane_off + kColO + 32 * c, o);
-          tc_wait_ld();
-          if (rvalid) {
+      for (int c = 0; c < 2; ++c) {
+        uint32_t oa[32], ob[32];
+        tc_ld32(ta + 32 * c, oa);
+        tc_ld32(tb + 32 * c, ob);
+        tc_wait_ld();
+        if (rvalid) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const float* f = reinterpret_cast<const float*>(o) + 8 * u;
-              orow[4 * c + u] = make_uint4(pack_bf16x2(f[0] * inv, f[1] * inv), pack_bf16x2(f[2] * inv, f[3] * inv),
-                                           pack_bf16x2(f[4] * inv, f[5] * inv), pack_bf16x2(f[6] * inv, f[7] * inv));
-            }
+          for (int u = 0; u < 4; ++u) {
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              f[e] = __uint_as_float(oa[8 * u + e]) * fa + __uint_as_float(ob[8 * u + e]) * fb;
+            orow[4 * c + u] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                                         pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
           }
         }
       }
     }
-  } else if (warp == 4) {
-    // ---------------- copy warp ----------------------------------------
+  } else if (warp == kCopyWarp || warp == kCopyWarp + 1) {
+    // ---------------- copy warps: keys (8) and values (9), each its own
+    // 2-stage ring, so that key tiles are not held back by value tiles ---
     if (lane == 0) {
-      const uint8_t* kq = p.kq + bh * p.ntq * (size_t)kKImg;
-      const uint8_t* vq = p.vq + bh * p.ntq * (size_t)kImg16;
-      const uint8_t* kf = p.kf + bh * p.ntf * (size_t)kImg16;
-      const uint8_t* vf = p.vf + bh * p.ntf * (size_t)kImg16;
-      int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};
+      const bool is_v = warp != kCopyWarp;
+      uint64_t* full = is_v ? vfull : kfull;
+      uint64_t* empty = is_v ? vempty : kempty;
+      const int qimg = is_v ? kImg16 : kKImg;
+      const uint8_t* qsrc = is_v ? p.vq + bh * p.ntq * (size_t)kImg16 : p.kq + bh * p.ntq * (size_t)kKImg;
+      const uint8_t* fsrc = (is_v ? p.vf : p.kf) + bh * p.ntf * (size_t)kImg16;
+      uint8_t* dst = sm + (is_v ? kOffV : kOffK);
+      int last_j = -1;
       bool ok = true;
       for (int j = 0; j < nt; ++j) {
         const int s = j & 1;
-        const uint32_t prev = ((j >> 1) & 1) ^ 1;
+        if (j >= 2 && !mbar_wait_or_abort(empty + s, ((j >> 1) & 1) ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
         const bool quant = j < nqt;
-        if (j >= 2 && !mbar_wait_or_abort(kempty + s, prev, abort_flag)) {
-          ok = false;
-          break;
-        }
-        const uint32_t kb = quant ? kKImg : kImg16;
-        mbar_arrive_expect_tx(kfull + s, kb);
-        bulk_g2s(sm + kOffK + s * kImg16, quant ? kq + (size_t)j * kKImg : kf + (size_t)(j - nqt) * kImg16, kb,
-                 kfull + s);
-        last_k[s] = j;
-        if (j >= 2 && !mbar_wait_or_abort(vempty + s, prev, abort_flag)) {
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(vfull + s, kImg16);
-        bulk_g2s(sm + kOffV + s * kImg16, quant ? vq + (size_t)j * kImg16 : vf + (size_t)(j - nqt) * kImg16,
-                 kImg16, vfull + s);
-        last_v[s] = j;
+        const uint32_t bytes = quant ? qimg : kImg16;
+        mbar_arrive_expect_tx(full + s, bytes);
+        bulk_g2s(dst + s * kImg16, quant ? qsrc + (size_t)j * qimg : fsrc + (size_t)(j - nqt) * kImg16, bytes,
+                 full + s);
+        last_j = j;
       }
       if (!ok) {
         *abort_flag = 1;
         hyq_set_err(p.err, HYQ_DEVERR_TIMEOUT);
-        // let the copies in flight land before the CTA's shared memory goes away
-        for (int s = 0; s < 2; ++s) {
-          if (last_k[s] >= 0) mbar_wait(kfull + s, (last_k[s] >> 1) & 1);
-          if (last_v[s] >= 0) mbar_wait(vfull + s, (last_v[s] >> 1) & 1);
-        }
+        // let the copies in flight (the last two tiles') land before the
+        // CTA's shared memory goes away
+        for (int j = max(0, last_j - 1); j <= last_j; ++j) mbar_wait(full + (j & 1), (j >> 1) & 1);
       }
     }
   } else {
     // ---------------- MMA warp -----------------------------------------
     if (lane == 0) {
-      const uint32_t tS[2] = {tbase + kColS0, tbase + kColS1};
-      const uint32_t tO = tbase + kColO;
       const uint32_t aQ = smem_u32(sm + kOffQ), aQc = smem_u32(sm + kOffQc), aP = smem_u32(sm + kOffP);
       bool ok = mbar_wait_or_abort(qready, 0, abort_flag);
       tc_fence_after();
@@ -618,31 +676,35 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           if (kFp8 && j < nqt) {
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-              tc_mma_f8(tS[s], tc_desc_sw128(aQc + 32 * ks), tc_desc_sw128(aK + 32 * ks), kIdescE4M3, ks > 0);
+              tc_mma_f8(tbase + (s ? kColS1 : kColS0), tc_desc_sw128(aQc + 32 * ks), tc_desc_sw128(aK + 32 * ks), kIdescE4M3, ks > 0);
           } else {
             const uint32_t aA = j < nqt ? aQc : aQ;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
               const uint32_t off = (ks >> 2) * kRegion + (ks & 3) * 32;
-              tc_mma_f16(tS[s], tc_desc_sw128(aA + off), tc_desc_sw128(aK + off), kIdescBF16, ks > 0);
+              tc_mma_f16(tbase + (s ? kColS1 : kColS0), tc_desc_sw128(aA + off), tc_desc_sw128(aK + off), kIdescBF16, ks > 0);
             }
           }
           tc_commit(sfull + s);
           tc_commit(kempty + s);
         }
-        if (j >= 1) {  // O += P V for tile i = j - 1
+        if (j >= 1) {  // O_h += P_h V_h for tile i = j - 1, one key half at a time
           const int i = j - 1, s = i & 1;
-          ok = mbar_wait_or_abort(pfull, i & 1, abort_flag);
-          if (ok) ok = mbar_wait_or_abort(vfull + s, (i >> 1) & 1, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
+          ok = mbar_wait_or_abort(vfull + s, (i >> 1) & 1, abort_flag);
           const uint32_t aV = smem_u32(sm + kOffV + s * kImg16);
+          for (int hf = 0; ok && hf < 2; ++hf) {
+            ok = mbar_wait_or_abort(pfull + hf, i & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t off = (ks >> 2) * kRegion + (ks & 3) * 32;
-            tc_mma_f16(tO, tc_desc_sw128(aP + off), tc_desc_sw128(aV + off), kIdescBF16, (i > 0 || ks > 0) ? 1u : 0u);
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint32_t off = hf * kRegion + ks * 32;
+              tc_mma_f16(tbase + (hf ? kColO1 : kColO0), tc_desc_sw128(aP + off), tc_desc_sw128(aV + off), kIdescBF16,
+                         (i > 0 || ks > 0) ? 1u : 0u);
+            }
+            tc_commit(pvdone + hf);
           }
-          tc_commit(pvdone);
+          if (!ok) break;
           tc_commit(vempty + s);
         }
       }
@@ -657,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tc_dealloc(tbase, kTmemCols);
   }
