@@ -48,6 +48,7 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--layers", type=int, default=N_LAYERS)
     p.add_argument("--no-baseline", action="store_true", help="skip the CPU oracle timing")
+    p.add_argument("--no-prefill", action="store_true", help="skip the prefill measurement")
     p.add_argument("--case", default="period", choices=["period", "decode-layer", "prefill"],
                    help="decode-layer: one 32K layer, a few decode launches (a small profiling target); "
                         "prefill: the hybrid prefill operator alone")
@@ -458,6 +459,7 @@ def run_ours(args, rank, world, local):
     achieved = bytes_per / (dec_us * 1e-6) / 1e9
     peak, peak_kind = measured_peaks()
     base = None if args.no_baseline else cpu_baseline()
+    prefill = None if args.no_prefill else prefill_measure(dev, [CTX], reps=5)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": False,
@@ -479,6 +481,10 @@ def run_ours(args, rank, world, local):
                 "d2h_bytes_per_step": d2h},
         "clocks": clk.summary(),
         "cpu_baseline": base,
+        "prefill": ({"workload": "llama3.1-8b-shaped causal prefill, B1, 32/8 heads, d128, 32K, W128, rho 5% "
+                                 "(hyq_prefill_attention: pack + main kernel)",
+                     "flops": "4 d HQ L(L+1)/2", "l2": "256 MB flush before every timed call",
+                     "results": prefill} if prefill is not None else None),
     }
     print(json.dumps(line))
 
