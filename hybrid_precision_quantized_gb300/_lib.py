@@ -38,7 +38,7 @@ SYMBOLS = ("hyq_status_string", "hyq_config_check", "hyq_vl_count", "hyq_layout_
            "hyq_workspace_size", "hyq_layout_reset", "hyq_quantize_append",
            "hyq_select_vertical", "hyq_rebuild", "hyq_decode_append", "hyq_decode_attention",
            "hyq_decode_attention_noalloc", "hyq_read_device_error", "hyq_set_decode_plan",
-           "hyq_prefill_attention")
+           "hyq_prefill_attention", "hyq_decode_step")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -95,6 +95,8 @@ def load() -> ctypes.CDLL:
                                                    c_void_p]),
         "hyq_read_device_error": (c_int32, [c_void_p, P(c_int32), c_void_p]),
         "hyq_set_decode_plan": (c_int32, [c_int32, c_int32]),
+        "hyq_decode_step": (c_int32, [P(HyqConfig), c_void_p, c_void_p, c_void_p, P(HyqLayout), c_void_p,
+                                      c_void_p, c_int32, c_void_p, c_int32, c_void_p, c_size_t, c_void_p]),
         "hyq_prefill_attention": (c_int32, [P(HyqConfig), c_int32, c_void_p, c_int32, c_void_p, c_void_p,
                                             c_int32, c_int32, c_void_p, c_int32, c_void_p, c_void_p,
                                             c_void_p, c_size_t, c_void_p]),
@@ -195,6 +197,16 @@ def hyq_decode_attention(cfg, q, lay: HyqLayout, out, ws, len_hint: int = 0, str
     _check("hyq_decode_attention", load().hyq_decode_attention(
         ctypes.byref(cfg), ptr(q), ctypes.byref(lay), ptr(out), len_hint, ptr(ws),
         ws.numel() * ws.element_size(), stream_ptr(stream)))
+
+
+def hyq_decode_step(cfg, q, k_new, v_new, lay: HyqLayout, out, ws, k_src=None, v_src=None, len_hint: int = 0,
+                    stream=None):
+    """Append this token (as hyq_decode_append) and attend over the cache
+    including it (as hyq_decode_attention), in one launch."""
+    ld = row_ld(k_src) if k_src is not None else 0
+    _check("hyq_decode_step", load().hyq_decode_step(
+        ctypes.byref(cfg), ptr(q), ptr(k_new), ptr(v_new), ctypes.byref(lay), ptr(k_src), ptr(v_src), ld,
+        ptr(out), len_hint, ptr(ws), ws.numel() * ws.element_size(), stream_ptr(stream)))
 
 
 def hyq_decode_attention_noalloc(cfg, q, lay: HyqLayout, out, len_hint: int = 0, stream=None):

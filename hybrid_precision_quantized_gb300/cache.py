@@ -215,13 +215,17 @@ class HybridDecoder:
         return k
 
     def step(self, q, k_new, v_new, out, stream=None):
-        """Append this token, re-select every ``period`` steps, attend."""
-        L.hyq_decode_append(self.cfg, q, k_new, v_new, self.layer.c, self.k_src, self.v_src, stream)
+        """Append this token, re-select every ``period`` steps, attend.  Steps
+        without maintenance run as one fused launch (hyq_decode_step)."""
         self.length += 1
         self.since += 1
         self.ring_n = min(self.ring_n + 1, self.cfg.period)
-        if self.since == self.cfg.period:
-            self.maintain(self.length, self.layer.q_ring(), self.ring_n, stream)
-            self.since = 0
+        if self.since < self.cfg.period:
+            L.hyq_decode_step(self.cfg, q, k_new, v_new, self.layer.c, out, self.ws_dec, self.k_src, self.v_src,
+                              self.cfg.capacity, stream)
+            return out
+        L.hyq_decode_append(self.cfg, q, k_new, v_new, self.layer.c, self.k_src, self.v_src, stream)
+        self.maintain(self.length, self.layer.q_ring(), self.ring_n, stream)
+        self.since = 0
         L.hyq_decode_attention(self.cfg, q, self.layer.c, out, self.ws_dec, self.cfg.capacity, stream)
         return out

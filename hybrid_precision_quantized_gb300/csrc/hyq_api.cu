@@ -194,6 +194,22 @@ extern "C" hyq_status hyq_decode_attention(const hyq_config* c, const void* q,
   return from_cuda(hyq_launch_decode(c, q, l, out, len_hint, ws, s));
 }
 
+extern "C" hyq_status hyq_decode_step(const hyq_config* c, const void* q, const void* k_new,
+                                      const void* v_new, const hyq_layout* l, void* k_src, void* v_src,
+                                      int32_t ld, void* out, int32_t len_hint, void* ws, size_t ws_bytes,
+                                      hyq_stream_t s) {
+  hyq_status st = hyq_config_check(c);
+  if (st != HYQ_OK) return st;
+  if (!layout_ok(l) || !q || !k_new || !v_new || !out || len_hint < 0) return HYQ_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(out, 16))
+    return HYQ_ERR_INVALID_ARG;
+  if ((k_src == nullptr) != (v_src == nullptr)) return HYQ_ERR_INVALID_ARG;
+  if (k_src && (ld < 1 || !aligned(k_src, 16) || !aligned(v_src, 16))) return HYQ_ERR_INVALID_ARG;
+  if (len_hint == 0 || len_hint > c->capacity) len_hint = c->capacity;
+  if (!ws || !aligned(ws, kAlign) || ws_bytes < hyq_decode_ws_bytes(c, len_hint)) return HYQ_ERR_WORKSPACE;
+  return from_cuda(hyq_launch_decode(c, q, l, out, len_hint, ws, s, k_new, v_new, k_src, v_src, ld));
+}
+
 extern "C" hyq_status hyq_prefill_attention(const hyq_config* c, int32_t dtype, const void* q,
                                             int32_t ldq, const void* k, const void* v, int32_t ldk,
                                             int32_t L, const int32_t* vl_idx, int32_t kvl, void* out,

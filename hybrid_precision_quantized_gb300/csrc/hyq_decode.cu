@@ -100,6 +100,59 @@ DecodePlan decode_plan(const hyq_config* c, int32_t len) {
   return p;
 }
 
+// One decode step's append, fused into the attention launch (hyq_decode_step);
+// k_new == nullptr for attention only.
+struct StepArgs {
+  const __nv_bfloat16* k_new;  // [B][HKV][128]
+  const __nv_bfloat16* v_new;
+  __nv_bfloat16* k_src;        // [B][HKV][ld][128] or nullptr
+  __nv_bfloat16* v_src;
+  int32_t ld, period;
+  int32_t* tickets_b;          // [B] per-sequence ticket of the counter update
+};
+
+// The fused step's writes and counter update, at the end of a block: the
+// block that holds the new row stores it to the tail (and the caller's BF16
+// cache) and the group's queries to the proxy ring -- nothing in this launch
+// reads those slots -- and the last block of the sequence to get here
+// advances the counters (every block read them at its start).
+__device__ __forceinline__ void finish_step(const StepArgs& sa, const hyq_layout& lay,
+                                            const __nv_bfloat16* q, bool owner, bool app, size_t bh, int b,
+                                            int h, int HQ, int gq, int cap_tail, int ntail, int len, int rpos,
+                                            int rn, int nblocks) {
+  const int tid = threadIdx.x;
+  if (owner) {
+    for (int i = tid; i < 32 + 16 * gq; i += blockDim.x) {
+      const int c8 = i & 15;
+      if (i < 32) {
+        const bool isv = i >= 16;
+        const uint4 x = __ldg(reinterpret_cast<const uint4*>((isv ? sa.v_new : sa.k_new) + bh * HYQ_D) + c8);
+        __nv_bfloat16* tb = static_cast<__nv_bfloat16*>(isv ? lay.tail_v : lay.tail_k);
+        reinterpret_cast<uint4*>(tb + (bh * cap_tail + ntail) * HYQ_D)[c8] = x;
+        if (sa.k_src) reinterpret_cast<uint4*>((isv ? sa.v_src : sa.k_src) + (bh * sa.ld + len) * HYQ_D)[c8] = x;
+      } else {
+        const size_t hq = (size_t)b * HQ + (size_t)h * gq + ((i - 32) >> 4);
+        const uint4 x = __ldg(reinterpret_cast<const uint4*>(q + hq * HYQ_D) + c8);
+        reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(lay.q_ring) + (hq * sa.period + rpos) * HYQ_D)[c8] = x;
+      }
+    }
+  }
+  if (tid == 0) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;\n" : "=r"(old) : "l"(sa.tickets_b + b) : "memory");
+    if (old == nblocks - 1) {
+      if (app) {
+        int32_t* wc = lay.counts + (size_t)b * HYQ_COUNTS;
+        wc[HYQ_CNT_NTAIL] = ntail + 1;
+        wc[HYQ_CNT_LEN] = len + 1;
+        wc[HYQ_CNT_RING_POS] = (rpos + 1) % sa.period;
+        wc[HYQ_CNT_RING_N] = min(rn + 1, sa.period);
+      }
+      sa.tickets_b[b] = 0;
+    }
+  }
+}
+
 struct State {
   float m[2], l[2];
   float acc[8][4];   // PV accumulators in units of 2^-24
@@ -231,9 +284,11 @@ __device__ __forceinline__ uint32_t u4c(const uint4& v, int i) {
 }
 
 // One 16-row tile of BF16 rows (rows row0.. of the vertical-line rows followed
-// by the tail), `vr` valid rows, loaded directly into fragment registers.
+// by the tail), `vr` valid rows, loaded directly into fragment registers; row
+// `rnew` (a fused step's new row) is read from knew/vnew.
 __device__ __forceinline__ void f_tile(const __nv_bfloat16* vlk, const __nv_bfloat16* vlv,
                                        const __nv_bfloat16* tk, const __nv_bfloat16* tv, int nvl,
+                                       int rnew, const __nv_bfloat16* knew, const __nv_bfloat16* vnew,
                                        int row0, int vr, int lane, const __nv_bfloat16* q_s, State& st) {
   const int g = lane >> 2, t = lane & 3;
 
@@ -244,7 +299,8 @@ __device__ __forceinline__ void f_tile(const __nv_bfloat16* vlk, const __nv_bflo
 #pragma unroll
     for (int a = 0; a < 2; ++a) {
       const int rr = g + 8 * a, row = row0 + rr;
-      const __nv_bfloat16* src = row < nvl ? vlk + (size_t)row * HYQ_D : tk + (size_t)(row - nvl) * HYQ_D;
+      const __nv_bfloat16* src =
+          row == rnew ? knew : row < nvl ? vlk + (size_t)row * HYQ_D : tk + (size_t)(row - nvl) * HYQ_D;
 #pragma unroll
       for (int j = 0; j < 4; ++j)
         ka[a][j] = rr < vr ? __ldg(reinterpret_cast<const uint4*>(src + 8 * (t + 4 * j))) : make_uint4(0, 0, 0, 0);
@@ -273,7 +329,8 @@ __device__ __forceinline__ void f_tile(const __nv_bfloat16* vlk, const __nv_bflo
 #pragma unroll
   for (int tk4 = 0; tk4 < 4; ++tk4) {
     const int rr = 2 * t + 8 * (tk4 >> 1) + (tk4 & 1), row = row0 + rr;
-    const __nv_bfloat16* src = row < nvl ? vlv + (size_t)row * HYQ_D : tv + (size_t)(row - nvl) * HYQ_D;
+    const __nv_bfloat16* src =
+        row == rnew ? vnew : row < nvl ? vlv + (size_t)row * HYQ_D : tv + (size_t)(row - nvl) * HYQ_D;
 #pragma unroll
     for (int G = 0; G < 4; ++G)
       va[tk4][G] = rr < vr ? __ldg(reinterpret_cast<const uint2*>(src + 32 * G + 4 * g)) : make_uint2(0, 0);
@@ -347,7 +404,7 @@ template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
     const __nv_bfloat16* __restrict__ q, hyq_layout lay, __nv_bfloat16* __restrict__ out,
     int32_t* __restrict__ tickets, float* __restrict__ part, int HQ, int gq, int nblk_cap,
-    int cap_vl, int cap_tail, int S) {
+    int cap_vl, int cap_tail, int S, const StepArgs sa) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(16) __nv_bfloat16 q_s[HYQ_MAX_GQA * HYQ_D];
   __shared__ float qsum_s[HYQ_MAX_GQA * 4];
@@ -377,8 +434,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
     nvl = min(max(nvl, 0), cap_vl);
     ntail = min(max(ntail, 0), cap_tail);
   }
+  // Fused step: this token's K/V row becomes tail row `ntail` (when it fits).
+  const bool step = sa.k_new != nullptr;
+  int32_t len = 0, rpos = 0, rn = 0;
+  bool app = false;
+  if (step) {
+    len = cnt[HYQ_CNT_LEN];
+    rpos = cnt[HYQ_CNT_RING_POS];
+    rn = cnt[HYQ_CNT_RING_N];
+    app = ntail < cap_tail && len >= 0 && rpos >= 0 && rpos < sa.period && (sa.k_src == nullptr || len < sa.ld);
+    if (!app && tid == 0 && split == 0 && h == 0) hyq_set_err(lay.err, HYQ_DEVERR_COUNT);
+  }
   // This block's share of the 4-bit tiles and of the BF16 tiles.
-  const int nt = (nq + 15) >> 4, nf = nvl + ntail, nft = (nf + 15) >> 4;
+  const int nt = (nq + 15) >> 4, nf = nvl + ntail + (app ? 1 : 0), nft = (nf + 15) >> 4;
   const int t0 = (int)((int64_t)split * nt / S), t1 = (int)((int64_t)(split + 1) * nt / S);
   const int f0 = (int)((int64_t)split * nft / S), f1 = (int)((int64_t)(split + 1) * nft / S);
   // 4-bit tiles go round-robin over the warps, starting after the warps that
@@ -413,17 +481,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
     // one K and one V copy per buffer it touches.  Used after the 4-bit loop.
     if (warp < n_staged) {
       const int row0 = 16 * (f0 + warp), nrows = min(16, nf - row0);
-      mbar_arrive_expect_tx(&fbars[warp], nrows * 2 * HYQ_D * 2);
+      // the new row of a fused step (if in this tile) comes from the input instead
+      const int rnew = app ? nvl + ntail - row0 : -1;
+      const int ncopy = nrows - ((rnew >= 0 && rnew < nrows) ? 1 : 0);
+      mbar_arrive_expect_tx(&fbars[warp], ncopy * 2 * HYQ_D * 2);
       const int na = max(0, min(row0 + nrows, nvl) - row0);  // rows in the vertical-line buffer
       if (na > 0) {
         bulk_g2s(fstage, vlk + (size_t)row0 * HYQ_D, na * HYQ_D * 2, &fbars[warp]);
         bulk_g2s(fstage + 16 * kFKStride, vlv + (size_t)row0 * HYQ_D, na * HYQ_D * 2, &fbars[warp]);
       }
-      if (nrows > na) {
+      const int ntr = min(nrows - na, ntail - max(0, row0 + na - nvl));  // stored tail rows (not the new one)
+      if (ntr > 0) {
         const int tr = row0 + na - nvl;  // first tail row
-        bulk_g2s(fstage + na * kFKStride, tk + (size_t)tr * HYQ_D, (nrows - na) * HYQ_D * 2, &fbars[warp]);
-        bulk_g2s(fstage + 16 * kFKStride + na * kFVStride, tv + (size_t)tr * HYQ_D, (nrows - na) * HYQ_D * 2,
-                 &fbars[warp]);
+        bulk_g2s(fstage + na * kFKStride, tk + (size_t)tr * HYQ_D, ntr * HYQ_D * 2, &fbars[warp]);
+        bulk_g2s(fstage + 16 * kFKStride + na * kFVStride, tv + (size_t)tr * HYQ_D, ntr * HYQ_D * 2, &fbars[warp]);
       }
     }
     for (int j = 0; j < nj && j < kSlots; ++j) {
@@ -521,11 +592,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
       }
       __syncwarp();
     } else {
+      const int rnew = app ? nvl + ntail - 16 * (f0 + warp) : -1;
+      if (rnew >= 0 && rnew < 16) {  // the fused step's new row, from the input
+        const __nv_bfloat16* src = (lane < 16 ? sa.k_new : sa.v_new) + bh * HYQ_D;
+        reinterpret_cast<uint4*>(fstage + (lane < 16 ? 0 : 16 * kFKStride) + rnew * kFKStride)[lane & 15] =
+            __ldg(reinterpret_cast<const uint4*>(src) + (lane & 15));
+        __syncwarp();
+      }
       f_tile_smem(fstage, fstage + 16 * kFKStride, min(16, nf - 16 * (f0 + warp)), lane, q_s, st);
     }
   }
   for (int fi = f0 + kFStaged + warp; fi < f1; fi += kWarps)  // tiles past the staged ones
-    f_tile(vlk, vlv, tk, tv, nvl, 16 * fi, min(16, nf - 16 * fi), lane, q_s, st);
+    f_tile(vlk, vlv, tk, tv, nvl, app ? nvl + ntail : -1, sa.k_new + bh * HYQ_D, sa.v_new + bh * HYQ_D, 16 * fi,
+           min(16, nf - 16 * fi), lane, q_s, st);
 
   // ---- warp partials -> block partial (m, l, acc) in shared memory ---------
 #pragma unroll
@@ -590,7 +669,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
       pp[hd * kPart + 2 + d] = a;
     }
   }
-  if (kMode == kDirect) return;
+  const bool owner = app && (nvl + ntail) >> 4 >= f0 && (nvl + ntail) >> 4 < f1;
+#define HYQ_FINISH_STEP() \
+  if (step) finish_step(sa, lay, q, owner, app, bh, b, h, HQ, gq, cap_tail, ntail, len, rpos, rn, S * HKV)
+  if (kMode == kDirect) {
+    HYQ_FINISH_STEP();
+    return;
+  }
 
   if (kMode == kCluster) {
     // ---- ReduceSoftmax across the cluster through distributed shared memory
@@ -632,10 +717,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
       out[((size_t)b * HQ + (size_t)h * gq + hd) * HYQ_D + d] = __float2bfloat16_rn(Lh > 0.f ? a / Lh : 0.f);
     }
     cluster.sync();  // no block leaves while another still reads its shared memory
+    HYQ_FINISH_STEP();
     return;
   }
 
   // ---- kGlobal: the last block to finish merges the workspace partials -----
+  HYQ_FINISH_STEP();
+#undef HYQ_FINISH_STEP
   // The barrier orders every thread's partial writes before thread 0's
   // release; its acquire (in the last block) orders them before the reads.
   __syncthreads();
@@ -760,7 +848,7 @@ size_t hyq_decode_ws_bytes(const hyq_config* c, int32_t len_hint) {
   // a cluster cannot be resident); the cluster and direct merges use none.
   const DecodePlan p = decode_plan(c, len_hint);
   size_t bh = (size_t)c->batch * c->num_kv_heads;
-  return round_up(bh * 4) + round_up(bh * (size_t)p.S * HYQ_MAX_GQA * kPart * 4);
+  return round_up(bh * 4) + round_up((size_t)c->batch * 4) + round_up(bh * (size_t)p.S * HYQ_MAX_GQA * kPart * 4);
 }
 
 template <int kMode>
@@ -807,7 +895,8 @@ extern "C" hyq_status hyq_set_decode_plan(int32_t merge, int32_t splits) {
 }
 
 cudaError_t hyq_launch_decode(const hyq_config* c, const void* q, const hyq_layout* lay, void* out,
-                              int32_t len_hint, void* ws, cudaStream_t s) {
+                              int32_t len_hint, void* ws, cudaStream_t s, const void* k_new, const void* v_new,
+                              void* k_src, void* v_src, int32_t ld) {
   cudaError_t e = set_attrs<kDirect>();
   if (e == cudaSuccess) e = set_attrs<kCluster>();
   if (e == cudaSuccess) e = set_attrs<kGlobal>();
@@ -816,7 +905,10 @@ cudaError_t hyq_launch_decode(const hyq_config* c, const void* q, const hyq_layo
   if (p.mode == kCluster && !cluster_fits(p.S)) p.mode = kGlobal;  // same S, workspace merge
   size_t bh = (size_t)c->batch * c->num_kv_heads;
   int32_t* tickets = static_cast<int32_t*>(ws);
-  float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + round_up(bh * 4));
+  StepArgs sa{static_cast<const __nv_bfloat16*>(k_new), static_cast<const __nv_bfloat16*>(v_new),
+              static_cast<__nv_bfloat16*>(k_src), static_cast<__nv_bfloat16*>(v_src), ld, c->period,
+              reinterpret_cast<int32_t*>(static_cast<char*>(ws) + round_up(bh * 4))};
+  float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + round_up(bh * 4) + round_up((size_t)c->batch * 4));
   const int gq = c->num_q_heads / c->num_kv_heads;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.S, c->num_kv_heads, c->batch);
@@ -835,13 +927,13 @@ cudaError_t hyq_launch_decode(const hyq_config* c, const void* q, const hyq_layo
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, decode_kernel<kCluster>, qq, *lay, oo, tickets, part, c->num_q_heads, gq,
-                              nblk, cvl, ct, p.S);
+                              nblk, cvl, ct, p.S, sa);
   }
   if (p.mode == kDirect)
     return cudaLaunchKernelEx(&cfg, decode_kernel<kDirect>, qq, *lay, oo, tickets, part, c->num_q_heads, gq,
-                              nblk, cvl, ct, p.S);
+                              nblk, cvl, ct, p.S, sa);
   return cudaLaunchKernelEx(&cfg, decode_kernel<kGlobal>, qq, *lay, oo, tickets, part, c->num_q_heads, gq,
-                            nblk, cvl, ct, p.S);
+                            nblk, cvl, ct, p.S, sa);
 }
 
 cudaError_t hyq_launch_decode_append(const hyq_config* c, const void* q, const void* k_new,

@@ -2,9 +2,11 @@
 layers, captured as CUDA graphs so that host overhead does not gate the
 kernels.
 
-For every token t of the period two graphs are captured: the appends of all
-layers (plus, at the last token, the re-selection and rebuild of every layer)
-and the fused decode attention of all layers.  A reset graph restores the
+For every token t of the period but the last, one graph holds the fused
+decode step (append + attention, hyq_decode_step) of every layer.  At the
+last token two graphs are captured: the appends of all layers with the
+re-selection and rebuild of every layer, then the decode attention of all
+layers (maintenance sits between the append and the attention).  A reset graph restores the
 layer counters to the start of the period, so a period can be replayed any
 number of times on the same synthetic inputs (the work of every replay is
 identical: the same positions are re-appended and the same layout rebuilt).
@@ -81,6 +83,15 @@ class PeriodRunner:
             L.hyq_decode_attention(self.cfg, self.q_tok[t, li], lay.c, self.out[t, li], self.ws_dec, self.L_end)
         return self.n_layers
 
+    def _steps(self, t):
+        for li, lay in enumerate(self.layers):
+            L.hyq_decode_step(self.cfg, self.q_tok[t, li], self.k_tok[t, li], self.v_tok[t, li], lay.c,
+                              self.out[t, li], self.ws_dec, self.k_srcs[li], self.v_srcs[li], self.L_end)
+        return self.n_layers
+
+    def _fused(self, t):
+        return t < self.cfg.period - 1
+
     def capture(self):
         """Run one period eagerly (warm-up, attributes), then capture graphs."""
         s = torch.cuda.Stream()
@@ -88,8 +99,11 @@ class PeriodRunner:
         with torch.cuda.stream(s):
             self._reset()
             for t in range(self.cfg.period):
-                self._appends(t)
-                self._decodes(t)
+                if self._fused(t):
+                    self._steps(t)
+                else:
+                    self._appends(t)
+                    self._decodes(t)
         torch.cuda.synchronize()
         self.g_reset = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.g_reset):
@@ -97,11 +111,17 @@ class PeriodRunner:
         self.g_app, self.g_dec = [], []
         n = 0
         for t in range(self.cfg.period):
-            ga, gd = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-            with torch.cuda.graph(ga):
-                n += self._appends(t)
-            with torch.cuda.graph(gd):
-                n += self._decodes(t)
+            gd = torch.cuda.CUDAGraph()
+            if self._fused(t):
+                ga = None
+                with torch.cuda.graph(gd):
+                    n += self._steps(t)
+            else:
+                ga = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(ga):
+                    n += self._appends(t)
+                with torch.cuda.graph(gd):
+                    n += self._decodes(t)
             self.g_app.append(ga)
             self.g_dec.append(gd)
         self.launches_per_period = n
@@ -110,10 +130,12 @@ class PeriodRunner:
     def run_period(self, dec_events=None):
         """Replay one period.  ``dec_events`` (optional) is a list of
         (start, end) CUDA event pairs, one per token, recorded around the
-        decode-attention graph of that token."""
+        decode graph of that token (fused steps, or the attention alone at
+        the maintenance token)."""
         self.g_reset.replay()
         for t in range(self.cfg.period):
-            self.g_app[t].replay()
+            if self.g_app[t] is not None:
+                self.g_app[t].replay()
             if dec_events is not None:
                 dec_events[t][0].record()
             self.g_dec[t].replay()
@@ -129,6 +151,7 @@ class PeriodRunner:
             self.q_tok[t].copy_(q_host[t], non_blocking=True)
             self.k_tok[t].copy_(k_host[t], non_blocking=True)
             self.v_tok[t].copy_(v_host[t], non_blocking=True)
-            self.g_app[t].replay()
+            if self.g_app[t] is not None:
+                self.g_app[t].replay()
             self.g_dec[t].replay()
             out_host[t].copy_(self.out[t], non_blocking=True)

@@ -288,6 +288,23 @@ hyq_status hyq_prefill_attention(const hyq_config *cfg, int32_t dtype, const voi
                                  void *ws, size_t ws_bytes, hyq_stream_t stream);
 
 /*
+ * One decode step in one launch: hyq_decode_append followed by
+ * hyq_decode_attention (§4.3 Eq. 8-9, Algorithm 3; §5.5 query buffer).  The
+ * token's K/V row becomes the newest tail row (and row LEN of the caller's
+ * BF16 cache when k_src/v_src are non-null), its query goes to the proxy
+ * ring, the counters advance as in hyq_decode_append, and `out` is the
+ * attention of q over the LEN + 1 positions, the new row included.
+ * Arguments as in those two calls; len_hint bounds LEN + 1.  A full tail (or
+ * LEN >= ld) sets HYQ_DEVERR_COUNT, leaves the layout unchanged and attends
+ * over the LEN existing positions.  Workspace: hyq_workspace_size(cfg,
+ * HYQ_OP_DECODE, len_hint), zero-filled before first use.
+ */
+hyq_status hyq_decode_step(const hyq_config *cfg, const void *q, const void *k_new,
+                           const void *v_new, const hyq_layout *lay, void *k_src, void *v_src,
+                           int32_t ld, void *out, int32_t len_hint, void *ws, size_t ws_bytes,
+                           hyq_stream_t stream);
+
+/*
  * Override how hyq_decode_attention splits and merges its work (process-
  * wide; for tuning and testing).  merge: 0 automatic (the default), 1 one
  * block per (batch, KV head) and no merge, 2 `splits` blocks (2..16) merged

@@ -181,3 +181,97 @@ def test_decode_append_full_tail_is_flagged(hyq):
     torch.cuda.synchronize()
     assert layer.counts()[0, L.CNT_NTAIL].item() == 6
     assert hyq_read_device_error(layer.err()) & L.DEVERR_COUNT
+
+
+def _two_layers(c, Lc, W, ppm, capacity):
+    """Two identical layouts at context Lc (oracle partition) plus their inputs."""
+    B, HQ = c.q.shape[:2]
+    HKV = c.k.shape[1]
+    cfg = make_config(B, HQ, HKV, capacity=capacity, window=W, rho_ppm=ppm)
+    k_np = c.k.double().numpy()
+    idx_np, _ = select_vertical(c.q_proxy.double().numpy(), k_np[:, :, :Lc], Lc, W, ppm)
+    idx = torch.from_numpy(idx_np).to(torch.int32).cuda().contiguous()
+    layers = []
+    for _ in range(2):
+        lay = HybridLayer(cfg)
+        lay.reset()
+        hyq_rebuild(cfg, c.k[:, :, :Lc].contiguous().cuda(), c.v[:, :, :Lc].contiguous().cuda(), Lc, idx,
+                    idx_np.shape[-1], lay.c)
+        layers.append(lay)
+    return cfg, layers, idx_np
+
+
+@pytest.mark.parametrize("plan", [(0, 0), (1, 0), (2, 4), (3, 7)])
+@pytest.mark.parametrize("B,HQ,HKV", [(1, 8, 2), (2, 6, 2)])
+def test_decode_step_equals_append_then_attention(hyq, plan, B, HQ, HKV):
+    """The fused step leaves the same counters, tail, proxy ring and BF16 source
+    rows as hyq_decode_append (bit-exact), and its output matches the oracle's
+    attention over the cache with the new row, under every merge plan."""
+    from hybrid_precision_quantized_gb300 import hyq_decode_step, hyq_set_decode_plan
+    L0, W, ppm, steps = 900, 128, 50_000, 5
+    cap = L0 + steps
+    c = decode_case(71, B, HQ, HKV, cap, window=W, n_proxy=16, sink_frac=0.02)
+    cfg, (la, lb), idx_np = _two_layers(c, L0, W, ppm, cap)
+    srcs = []
+    for _ in range(2):
+        ks = torch.zeros(B, HKV, cap, 128, dtype=torch.bfloat16, device="cuda")
+        vs = torch.zeros_like(ks)
+        ks[:, :, :L0] = c.k[:, :, :L0].cuda()
+        vs[:, :, :L0] = c.v[:, :, :L0].cuda()
+        srcs.append((ks, vs))
+    g = gen_for(71, "q-steps")
+    qs = torch.randn(steps, B, HQ, 128, generator=g).to(torch.bfloat16)
+    oa = torch.empty(B, HQ, 128, dtype=torch.bfloat16, device="cuda")
+    ob = torch.empty_like(oa)
+    k_np, v_np = c.k.double().numpy(), c.v.double().numpy()
+    hyq_set_decode_plan(*plan)
+    try:
+        wsa, wsb = workspace(cfg, L.OP_DECODE, cap), workspace(cfg, L.OP_DECODE, cap)   # sized for the plan
+        for s in range(steps):
+            q = qs[s].cuda()
+            kn = c.k[:, :, L0 + s].contiguous().cuda()
+            vn = c.v[:, :, L0 + s].contiguous().cuda()
+            hyq_decode_append(cfg, q, kn, vn, la.c, srcs[0][0], srcs[0][1])
+            hyq_decode_attention(cfg, q, la.c, oa, wsa, cap)
+            hyq_decode_step(cfg, q, kn, vn, lb.c, ob, wsb, srcs[1][0], srcs[1][1], cap)
+            torch.cuda.synchronize()
+            want = hybrid_decode(qs[s].double().numpy(), k_np, v_np, L0 + s + 1, L0 - W, idx_np)
+            assert_attention_close(to_np(ob), want, what=f"fused step {s}, plan {plan}")
+            assert_attention_close(to_np(oa), want, what=f"two calls step {s}")
+    finally:
+        hyq_set_decode_plan(0, 0)
+    assert hyq_read_device_error(la.err()) == 0 and hyq_read_device_error(lb.err()) == 0
+    assert torch.equal(la.counts(), lb.counts())
+    n = la.counts()[0, L.CNT_NTAIL].item()
+    assert n == W + steps
+    assert torch.equal(la.tail_k()[:, :, :n], lb.tail_k()[:, :, :n])
+    assert torch.equal(la.tail_v()[:, :, :n], lb.tail_v()[:, :, :n])
+    assert torch.equal(la.q_ring()[:, :, :steps], lb.q_ring()[:, :, :steps])
+    assert torch.equal(srcs[0][0], srcs[1][0]) and torch.equal(srcs[0][1], srcs[1][1])
+
+
+def test_decode_step_full_tail_is_flagged(hyq):
+    """A fused step with a full tail flags the error, leaves the layout alone
+    and attends over the existing positions."""
+    from hybrid_precision_quantized_gb300 import hyq_decode_step
+    cfg = make_config(1, 2, 1, capacity=400, window=4, period=2)
+    c = decode_case(62, 1, 2, 1, 12, window=4, n_proxy=2)
+    layer = HybridLayer(cfg)
+    layer.reset()
+    idx = torch.zeros(1, 1, 1, dtype=torch.int32, device="cuda")
+    hyq_rebuild(cfg, c.k[:, :, :10].contiguous().cuda(), c.v[:, :, :10].contiguous().cuda(), 10, idx, 0, layer.c)
+    ws = workspace(cfg, L.OP_DECODE, 400)
+    out = torch.empty(1, 2, 128, dtype=torch.bfloat16, device="cuda")
+    q = c.q.cuda()
+    for s in range(2):   # tail 4 -> 6 rows = capacity
+        hyq_decode_step(cfg, q, c.k[:, :, 10 + s].contiguous().cuda(), c.v[:, :, 10 + s].contiguous().cuda(),
+                        layer.c, out, ws)
+    torch.cuda.synchronize()
+    assert hyq_read_device_error(layer.err()) == 0
+    before = layer.counts().clone()
+    hyq_decode_step(cfg, q, c.k[:, :, 11].contiguous().cuda(), c.v[:, :, 11].contiguous().cuda(), layer.c, out, ws)
+    torch.cuda.synchronize()
+    assert hyq_read_device_error(layer.err()) & L.DEVERR_COUNT
+    assert torch.equal(layer.counts(), before)
+    want = hybrid_decode(c.q.double().numpy(), c.k.double().numpy(), c.v.double().numpy(), 12, 6, np.zeros((1, 1, 0), np.int64))
+    assert_attention_close(to_np(out), want, what="full tail")
