@@ -111,46 +111,29 @@ struct StepArgs {
   int32_t* tickets_b;          // [B] per-sequence ticket of the counter update
 };
 
-// The fused step's writes and counter update, at the end of a block: the
-// block that holds the new row stores it to the tail (and the caller's BF16
-// cache) and the group's queries to the proxy ring -- nothing in this launch
-// reads those slots -- and the last block of the sequence to get here
-// advances the counters (every block read them at its start).
-__device__ __forceinline__ void finish_step(const StepArgs& sa, const hyq_layout& lay,
-                                            const __nv_bfloat16* q, bool owner, bool app, size_t bh, int b,
-                                            int h, int HQ, int gq, int cap_tail, int ntail, int len, int rpos,
-                                            int rn, int nblocks) {
-  const int tid = threadIdx.x;
-  if (owner) {
-    for (int i = tid; i < 32 + 16 * gq; i += blockDim.x) {
-      const int c8 = i & 15;
-      if (i < 32) {
-        const bool isv = i >= 16;
-        const uint4 x = __ldg(reinterpret_cast<const uint4*>((isv ? sa.v_new : sa.k_new) + bh * HYQ_D) + c8);
-        __nv_bfloat16* tb = static_cast<__nv_bfloat16*>(isv ? lay.tail_v : lay.tail_k);
-        reinterpret_cast<uint4*>(tb + (bh * cap_tail + ntail) * HYQ_D)[c8] = x;
-        if (sa.k_src) reinterpret_cast<uint4*>((isv ? sa.v_src : sa.k_src) + (bh * sa.ld + len) * HYQ_D)[c8] = x;
-      } else {
-        const size_t hq = (size_t)b * HQ + (size_t)h * gq + ((i - 32) >> 4);
-        const uint4 x = __ldg(reinterpret_cast<const uint4*>(q + hq * HYQ_D) + c8);
-        reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(lay.q_ring) + (hq * sa.period + rpos) * HYQ_D)[c8] = x;
-      }
-    }
+// The fused step's counter update: one ticket per (sequence, KV head), taken
+// by the block that finishes that pair; the last of the sequence's KV heads
+// advances the counters (every block read them at its start, before its own
+// pair's ticket).  The increment is a release, so the issuing thread does not
+// wait for it; the result is used (with an acquire fence) only at the end.
+__device__ __forceinline__ int step_ticket_issue(const StepArgs& sa, int b) {
+  int old;
+  asm volatile("atom.release.gpu.global.add.s32 %0, [%1], 1;\n" : "=r"(old) : "l"(sa.tickets_b + b) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ void step_ticket_finish(int old, const StepArgs& sa, const hyq_layout& lay, int b,
+                                                   int HKV, bool app, int ntail, int len, int rpos, int rn) {
+  if (old != HKV - 1) return;
+  asm volatile("fence.acq_rel.gpu;\n" ::: "memory");
+  if (app) {
+    int32_t* wc = lay.counts + (size_t)b * HYQ_COUNTS;
+    wc[HYQ_CNT_NTAIL] = ntail + 1;
+    wc[HYQ_CNT_LEN] = len + 1;
+    wc[HYQ_CNT_RING_POS] = (rpos + 1) % sa.period;
+    wc[HYQ_CNT_RING_N] = min(rn + 1, sa.period);
   }
-  if (tid == 0) {
-    int old;
-    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;\n" : "=r"(old) : "l"(sa.tickets_b + b) : "memory");
-    if (old == nblocks - 1) {
-      if (app) {
-        int32_t* wc = lay.counts + (size_t)b * HYQ_COUNTS;
-        wc[HYQ_CNT_NTAIL] = ntail + 1;
-        wc[HYQ_CNT_LEN] = len + 1;
-        wc[HYQ_CNT_RING_POS] = (rpos + 1) % sa.period;
-        wc[HYQ_CNT_RING_N] = min(rn + 1, sa.period);
-      }
-      sa.tickets_b[b] = 0;
-    }
-  }
+  sa.tickets_b[b] = 0;
 }
 
 struct State {
@@ -462,6 +445,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
   const __nv_bfloat16* tk = static_cast<const __nv_bfloat16*>(lay.tail_k) + bh * cap_tail * HYQ_D;
   const __nv_bfloat16* tv = static_cast<const __nv_bfloat16*>(lay.tail_v) + bh * cap_tail * HYQ_D;
   const int n_staged = min(f1 - f0, kFStaged);
+  // Fused step: the block holding the new row stores it (tail, caller's BF16
+  // cache) and the group's queries (proxy ring) at its end; nothing in this
+  // launch reads those slots.  Warp 2 loads the row now, off the critical path.
+  const bool owner = app && (nvl + ntail) >> 4 >= f0 && (nvl + ntail) >> 4 < f1;
+  uint4 nrow = make_uint4(0, 0, 0, 0);
+  if (owner && warp == 2)
+    nrow = __ldg(reinterpret_cast<const uint4*>((lane >= 16 ? sa.v_new : sa.k_new) + bh * HYQ_D) + (lane & 15));
   uint8_t* fstage = smem + kRingBytes + warp * kFTileBytes;
   if (lane == 0) {
     for (int i = 0; i < kSlots; ++i) mbar_init(&wb[i], 1);
@@ -475,6 +465,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
   // copies ahead of it would delay the start of all compute by the flood's
   // service time.
   if (!mbar_wait(&qbar, 0) && tid == 0) hyq_set_err(lay.err, HYQ_DEVERR_TIMEOUT);
+  if (owner && warp == 2) {
+    // the new row into its staging slot (the tile's bulk copies skip it); the
+    // barrier before the main loop orders this for the warp that reads it
+    const int fw = ((nvl + ntail) >> 4) - f0, rin = (nvl + ntail) & 15;
+    if (fw < n_staged)
+      reinterpret_cast<uint4*>(smem + kRingBytes + fw * kFTileBytes + (lane >= 16 ? 16 * kFKStride : 0) +
+                               rin * kFKStride)[lane & 15] = nrow;
+  }
   if (lane == 0) {
     // The first kFStaged BF16 tiles of this block: the rows of a tile are
     // contiguous in the vertical-line buffer and in the tail, so a tile takes
@@ -592,13 +590,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
       }
       __syncwarp();
     } else {
-      const int rnew = app ? nvl + ntail - 16 * (f0 + warp) : -1;
-      if (rnew >= 0 && rnew < 16) {  // the fused step's new row, from the input
-        const __nv_bfloat16* src = (lane < 16 ? sa.k_new : sa.v_new) + bh * HYQ_D;
-        reinterpret_cast<uint4*>(fstage + (lane < 16 ? 0 : 16 * kFKStride) + rnew * kFKStride)[lane & 15] =
-            __ldg(reinterpret_cast<const uint4*>(src) + (lane & 15));
-        __syncwarp();
-      }
       f_tile_smem(fstage, fstage + 16 * kFKStride, min(16, nf - 16 * (f0 + warp)), lane, q_s, st);
     }
   }
@@ -669,11 +660,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
       pp[hd * kPart + 2 + d] = a;
     }
   }
-  const bool owner = app && (nvl + ntail) >> 4 >= f0 && (nvl + ntail) >> 4 < f1;
-#define HYQ_FINISH_STEP() \
-  if (step) finish_step(sa, lay, q, owner, app, bh, b, h, HQ, gq, cap_tail, ntail, len, rpos, rn, S * HKV)
+  if (owner) {
+    if (warp == 2) {
+      const size_t row = (bh * cap_tail + ntail) * HYQ_D;
+      reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(lane >= 16 ? lay.tail_v : lay.tail_k) + row)[lane & 15] = nrow;
+      if (sa.k_src)
+        reinterpret_cast<uint4*>((lane >= 16 ? sa.v_src : sa.k_src) + (bh * sa.ld + len) * HYQ_D)[lane & 15] = nrow;
+    } else if (tid >= 96 && tid < 96 + 16 * gq) {
+      const int r = (tid - 96) >> 4, c8 = tid & 15;
+      const size_t hq = (size_t)b * HQ + (size_t)h * gq + r;
+      reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(lay.q_ring) + (hq * sa.period + rpos) * HYQ_D)[c8] =
+          reinterpret_cast<const uint4*>(q_s + r * HYQ_D)[c8];
+    }
+  }
+  const bool ticket_thread = step && tid == kThreads - 1;
   if (kMode == kDirect) {
-    HYQ_FINISH_STEP();
+    if (ticket_thread) step_ticket_finish(step_ticket_issue(sa, b), sa, lay, b, HKV, app, ntail, len, rpos, rn);
     return;
   }
 
@@ -717,13 +719,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
       out[((size_t)b * HQ + (size_t)h * gq + hd) * HYQ_D + d] = __float2bfloat16_rn(Lh > 0.f ? a / Lh : 0.f);
     }
     cluster.sync();  // no block leaves while another still reads its shared memory
-    HYQ_FINISH_STEP();
+    if (ticket_thread && split == 0)
+      step_ticket_finish(step_ticket_issue(sa, b), sa, lay, b, HKV, app, ntail, len, rpos, rn);
     return;
   }
 
   // ---- kGlobal: the last block to finish merges the workspace partials -----
-  HYQ_FINISH_STEP();
-#undef HYQ_FINISH_STEP
   // The barrier orders every thread's partial writes before thread 0's
   // release; its acquire (in the last block) orders them before the reads.
   __syncthreads();
@@ -734,6 +735,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
   }
   __syncthreads();
   if (!s_flag) return;
+  const int tk_old = ticket_thread ? step_ticket_issue(sa, b) : 0;  // overlaps the merge
   const float* pb = part + bh * S * (size_t)(HYQ_MAX_GQA * kPart);
   float* sm_m = red;                             // [S][8]
   float* sm_w = red + kMaxSplits * HYQ_MAX_GQA;  // [S][8]
@@ -788,6 +790,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
     out[((size_t)b * HQ + (size_t)h * gq + hd) * HYQ_D + d] = __float2bfloat16_rn(Lh > 0.f ? a / Lh : 0.f);
   }
   if (tid == 0) tickets[bh] = 0;
+  if (ticket_thread) step_ticket_finish(tk_old, sa, lay, b, HKV, app, ntail, len, rpos, rn);
 }
 
 // One step's append: BF16 tail row, proxy ring slot, optional BF16 source row.
