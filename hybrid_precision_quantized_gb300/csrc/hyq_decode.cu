@@ -626,18 +626,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
       red_l[warp][2 * t + j] = st.l[j];
     }
   __syncthreads();
-  if (tid < gq) {
-    float M = -INFINITY;
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w][tid]);
+  if (warp < gq) {  // warp = head, lane = warp of the block
+    const int hd = warp;
+    const float mw = lane < kWarps ? red_m[lane][hd] : -INFINITY;
+    float M = mw;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     const float Ms = (M == -INFINITY) ? 0.f : M;
-    float Lsum = 0.f;
-    for (int w = 0; w < kWarps; ++w) {
-      const float wt = exp2f(red_m[w][tid] - Ms);
-      wts[w][tid] = wt;
-      Lsum = fmaf(red_l[w][tid], wt, Lsum);
+    const float wt = lane < kWarps ? exp2f(mw - Ms) : 0.f;
+    if (lane < kWarps) wts[lane][hd] = wt;
+    float Lsum = lane < kWarps ? red_l[lane][hd] * wt : 0.f;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, o);
+    if (lane == 0) {
+      blk[hd * kPart + 0] = M;
+      blk[hd * kPart + 1] = Lsum;
     }
-    blk[tid * kPart + 0] = M;
-    blk[tid * kPart + 1] = Lsum;
   }
   __syncthreads();
   // kGlobal writes the block partial straight to its workspace slot.
@@ -755,18 +759,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
       v0[k] = (i < gq * HYQ_D && k < S) ? __ldcg(e + (size_t)k * HYQ_MAX_GQA * kPart) : 0.f;
   }
   __syncthreads();
-  if (tid < gq) {
+  if (warp < gq) {  // warp = head, lanes over the splits
+    const int hd = warp;
     float M = -INFINITY;
-    for (int s2 = 0; s2 < S; ++s2) M = fmaxf(M, sm_m[s2 * HYQ_MAX_GQA + tid]);
+    for (int s2 = lane; s2 < S; s2 += 32) M = fmaxf(M, sm_m[s2 * HYQ_MAX_GQA + hd]);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     const float Ms = (M == -INFINITY) ? 0.f : M;
     float Lsum = 0.f;
-    for (int s2 = 0; s2 < S; ++s2) {
-      const float wt = exp2f(sm_m[s2 * HYQ_MAX_GQA + tid] - Ms);
-      Lsum = fmaf(sm_w[s2 * HYQ_MAX_GQA + tid], wt, Lsum);
-      sm_w[s2 * HYQ_MAX_GQA + tid] = wt;
+    for (int s2 = lane; s2 < S; s2 += 32) {
+      const float wt = exp2f(sm_m[s2 * HYQ_MAX_GQA + hd] - Ms);
+      Lsum = fmaf(sm_w[s2 * HYQ_MAX_GQA + hd], wt, Lsum);
+      sm_w[s2 * HYQ_MAX_GQA + hd] = wt;
     }
-    sM[tid] = Ms;
-    sL[tid] = Lsum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, o);
+    if (lane == 0) {
+      sM[hd] = Ms;
+      sL[hd] = Lsum;
+    }
   }
   __syncthreads();
   for (int i = tid; i < gq * HYQ_D; i += kThreads) {
