@@ -49,6 +49,8 @@ def parse():
     p.add_argument("--layers", type=int, default=N_LAYERS)
     p.add_argument("--no-baseline", action="store_true", help="skip the CPU oracle timing")
     p.add_argument("--no-prefill", action="store_true", help="skip the prefill measurement")
+    p.add_argument("--overlap", action="store_true",
+                   help="launch decode steps with programmatic dependent launch")
     p.add_argument("--case", default="period", choices=["period", "decode-layer", "prefill"],
                    help="decode-layer: one 32K layer, a few decode launches (a small profiling target); "
                         "prefill: the hybrid prefill operator alone")
@@ -397,6 +399,10 @@ def run_ours(args, rank, world, local):
     nl = args.layers
     cfg = hyq.make_config(B, HQ, HKV, capacity=CTX, window=WINDOW, period=PERIOD, rho_ppm=RHO_PPM)
     k_srcs, v_srcs, q_tail, q_tok, k_tok, v_tok = make_inputs(dev, nl, seed=1001 + rank)
+    # consecutive decode launches belong to different layers, so each may
+    # overlap the one before it (programmatic dependent launch); measured
+    # slower inside CUDA graphs on GB300, hence off unless asked for
+    hyq.hyq_set_decode_overlap(args.overlap)
     run = PeriodRunner(cfg, k_srcs, v_srcs, L0, dev)
     run.q_tok.copy_(q_tok)
     run.k_tok.copy_(k_tok)
@@ -468,7 +474,8 @@ def run_ours(args, rank, world, local):
         "config": {"workload": "llama3.1-8b-shaped decode layer, B1, 32/8 heads, d128, 32K ctx, W128, "
                                "rho 5%, K4V4 G32; 32 distinct layers; step = 64-token re-selection period",
                    "context": CTX, "layers": nl, "tokens_per_step": PERIOD,
-                   "l2": "no flush: the 32 layers' caches (~1.6 GB) exceed L2 between reuses"},
+                   "l2": "no flush: the 32 layers' caches (~1.6 GB) exceed L2 between reuses",
+                   "launch_overlap": args.overlap},
         "gpu_launches": run.launches_per_period * args.steps,
         "decode_kernel_us": dec_us,
         "us_per_token_all_layers": value * nl,

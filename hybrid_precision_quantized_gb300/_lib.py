@@ -38,7 +38,7 @@ SYMBOLS = ("hyq_status_string", "hyq_config_check", "hyq_vl_count", "hyq_layout_
            "hyq_workspace_size", "hyq_layout_reset", "hyq_quantize_append",
            "hyq_select_vertical", "hyq_rebuild", "hyq_decode_append", "hyq_decode_attention",
            "hyq_decode_attention_noalloc", "hyq_read_device_error", "hyq_set_decode_plan",
-           "hyq_prefill_attention", "hyq_decode_step")
+           "hyq_prefill_attention", "hyq_decode_step", "hyq_set_decode_overlap")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -95,6 +95,7 @@ def load() -> ctypes.CDLL:
                                                    c_void_p]),
         "hyq_read_device_error": (c_int32, [c_void_p, P(c_int32), c_void_p]),
         "hyq_set_decode_plan": (c_int32, [c_int32, c_int32]),
+        "hyq_set_decode_overlap": (c_int32, [c_int32]),
         "hyq_decode_step": (c_int32, [P(HyqConfig), c_void_p, c_void_p, c_void_p, P(HyqLayout), c_void_p,
                                       c_void_p, c_int32, c_void_p, c_int32, c_void_p, c_size_t, c_void_p]),
         "hyq_prefill_attention": (c_int32, [P(HyqConfig), c_int32, c_void_p, c_int32, c_void_p, c_void_p,
@@ -237,6 +238,13 @@ DECODE_PLAN_AUTO, DECODE_PLAN_DIRECT, DECODE_PLAN_CLUSTER, DECODE_PLAN_GLOBAL = 
 def hyq_set_decode_plan(merge: int, splits: int = 0):
     """Override the decode split / merge plan (process-wide); 0 = automatic."""
     _check("hyq_set_decode_plan", load().hyq_set_decode_plan(merge, splits))
+
+
+def hyq_set_decode_overlap(enable: bool):
+    """Programmatic dependent launch of decode calls (process-wide).  Only for
+    streams where the kernel before each decode call does not write that
+    call's layout (see include/hyq.h)."""
+    _check("hyq_set_decode_overlap", load().hyq_set_decode_overlap(1 if enable else 0))
 
 
 def hyq_read_device_error(err_dev, stream=None) -> int:

@@ -70,6 +70,7 @@ struct DecodePlan {
 // blocks than there are 16-row tiles to share; one block per pair when even
 // two would not fit in one wave.
 int g_plan_merge = 0;   // hyq_set_decode_plan override (0 = automatic)
+int g_overlap = 0;      // hyq_set_decode_overlap
 int g_plan_splits = 0;
 
 DecodePlan decode_plan(const hyq_config* c, int32_t len) {
@@ -109,6 +110,7 @@ struct StepArgs {
   __nv_bfloat16* v_src;
   int32_t ld, period;
   int32_t* tickets_b;          // [B] per-sequence ticket of the counter update
+  int32_t overlap;             // launched as a programmatic dependent (hyq_set_decode_overlap)
 };
 
 // The fused step's counter update: one ticket per (sequence, KV head), taken
@@ -402,12 +404,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
   const size_t bh = (size_t)b * HKV + h;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
 
+  // With overlap this launch reads only the cache layout before
+  // griddepcontrol.wait (the caller guarantees the preceding kernel does not
+  // write it), and the query, the new row and every output after it; it lets
+  // the next launch start only once that wait has returned, so that every
+  // kernel but the immediately preceding one has finished whenever a launch
+  // starts.
+  const bool ovl = sa.overlap != 0;
   // The query rows of the KV group go first in this SM's copy queue.
   if (tid == 0) {
     mbar_init(&qbar, 1);
     mbar_fence_init();
-    mbar_arrive_expect_tx(&qbar, gq * HYQ_D * 2);
-    bulk_g2s(q_s, q + ((size_t)b * HQ + (size_t)h * gq) * HYQ_D, gq * HYQ_D * 2, &qbar);
+    if (!ovl) {
+      mbar_arrive_expect_tx(&qbar, gq * HYQ_D * 2);
+      bulk_g2s(q_s, q + ((size_t)b * HQ + (size_t)h * gq) * HYQ_D, gq * HYQ_D * 2, &qbar);
+    }
   }
   const int32_t* cnt = lay.counts + (size_t)b * HYQ_COUNTS;
   int32_t nq = cnt[HYQ_CNT_NQ], nvl = cnt[HYQ_CNT_NVL], ntail = cnt[HYQ_CNT_NTAIL];
@@ -450,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
   // launch reads those slots.  Warp 2 loads the row now, off the critical path.
   const bool owner = app && (nvl + ntail) >> 4 >= f0 && (nvl + ntail) >> 4 < f1;
   uint4 nrow = make_uint4(0, 0, 0, 0);
-  if (owner && warp == 2)
+  if (owner && warp == 2 && !ovl)
     nrow = __ldg(reinterpret_cast<const uint4*>((lane >= 16 ? sa.v_new : sa.k_new) + bh * HYQ_D) + (lane & 15));
   uint8_t* fstage = smem + kRingBytes + warp * kFTileBytes;
   if (lane == 0) {
@@ -461,18 +472,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
   for (int i = gq * HYQ_D / 8 + tid; i < HYQ_MAX_GQA * HYQ_D / 8; i += kThreads)
     reinterpret_cast<uint4*>(q_s)[i] = make_uint4(0, 0, 0, 0);  // query rows past g
   __syncthreads();
-  // Nothing else is requested until the query has arrived: a flood of tile
-  // copies ahead of it would delay the start of all compute by the flood's
-  // service time.
-  if (!mbar_wait(&qbar, 0) && tid == 0) hyq_set_err(lay.err, HYQ_DEVERR_TIMEOUT);
-  if (owner && warp == 2) {
-    // the new row into its staging slot (the tile's bulk copies skip it); the
-    // barrier before the main loop orders this for the warp that reads it
-    const int fw = ((nvl + ntail) >> 4) - f0, rin = (nvl + ntail) & 15;
-    if (fw < n_staged)
-      reinterpret_cast<uint4*>(smem + kRingBytes + fw * kFTileBytes + (lane >= 16 ? 16 * kFKStride : 0) +
-                               rin * kFKStride)[lane & 15] = nrow;
-  }
+  // Without overlap nothing else is requested until the query has arrived:
+  // a flood of tile copies ahead of it would delay the start of all compute
+  // by the flood's service time.
+  if (!ovl && !mbar_wait(&qbar, 0) && tid == 0) hyq_set_err(lay.err, HYQ_DEVERR_TIMEOUT);
   if (lane == 0) {
     // The first kFStaged BF16 tiles of this block: the rows of a tile are
     // contiguous in the vertical-line buffer and in the tail, so a tile takes
@@ -500,6 +503,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
       bulk_g2s(ring + j * HYQ_QTILE_BYTES, tiles + (size_t)(t0 + my0 + kWarps * j) * HYQ_QTILE_BYTES,
                HYQ_QTILE_BYTES, &wb[j]);
     }
+  }
+  if (ovl) {
+    // The layout copies are in flight; now wait for the preceding kernel and
+    // fetch what it may have produced.
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    if (tid == 0) {
+      mbar_arrive_expect_tx(&qbar, gq * HYQ_D * 2);
+      bulk_g2s(q_s, q + ((size_t)b * HQ + (size_t)h * gq) * HYQ_D, gq * HYQ_D * 2, &qbar);
+    }
+    if (owner && warp == 2)
+      nrow = __ldg(reinterpret_cast<const uint4*>((lane >= 16 ? sa.v_new : sa.k_new) + bh * HYQ_D) + (lane & 15));
+    if (!mbar_wait(&qbar, 0) && tid == 0) hyq_set_err(lay.err, HYQ_DEVERR_TIMEOUT);
+  }
+  if (owner && warp == 2) {
+    // the new row into its staging slot (the tile's bulk copies skip it); the
+    // barrier before the main loop orders this for the warp that reads it
+    const int fw = ((nvl + ntail) >> 4) - f0, rin = (nvl + ntail) & 15;
+    if (fw < n_staged)
+      reinterpret_cast<uint4*>(smem + kRingBytes + fw * kFTileBytes + (lane >= 16 ? 16 * kFKStride : 0) +
+                               rin * kFKStride)[lane & 15] = nrow;
   }
   if (tid < 32) {
     float sacc = 0.f;
@@ -899,6 +923,12 @@ bool cluster_fits(int S) {
   return ok;
 }
 
+extern "C" hyq_status hyq_set_decode_overlap(int32_t enable) {
+  if (enable != 0 && enable != 1) return HYQ_ERR_INVALID_ARG;
+  g_overlap = enable;
+  return HYQ_OK;
+}
+
 extern "C" hyq_status hyq_set_decode_plan(int32_t merge, int32_t splits) {
   if (merge < 0 || merge > 3) return HYQ_ERR_INVALID_ARG;
   if (merge == 2 && (splits < 2 || splits > 16)) return HYQ_ERR_INVALID_ARG;
@@ -921,7 +951,7 @@ cudaError_t hyq_launch_decode(const hyq_config* c, const void* q, const hyq_layo
   int32_t* tickets = static_cast<int32_t*>(ws);
   StepArgs sa{static_cast<const __nv_bfloat16*>(k_new), static_cast<const __nv_bfloat16*>(v_new),
               static_cast<__nv_bfloat16*>(k_src), static_cast<__nv_bfloat16*>(v_src), ld, c->period,
-              reinterpret_cast<int32_t*>(static_cast<char*>(ws) + round_up(bh * 4))};
+              reinterpret_cast<int32_t*>(static_cast<char*>(ws) + round_up(bh * 4)), g_overlap};
   float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + round_up(bh * 4) + round_up((size_t)c->batch * 4));
   const int gq = c->num_q_heads / c->num_kv_heads;
   cudaLaunchConfig_t cfg = {};
@@ -929,17 +959,20 @@ cudaError_t hyq_launch_decode(const hyq_config* c, const void* q, const hyq_layo
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeClusterDimension;
-  attr.val.clusterDim.x = p.S;
-  attr.val.clusterDim.y = 1;
-  attr.val.clusterDim.z = 1;
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[0].val.programmaticStreamSerializationAllowed = 1;
+  attrs[1].id = cudaLaunchAttributeClusterDimension;
+  attrs[1].val.clusterDim.x = p.S;
+  attrs[1].val.clusterDim.y = 1;
+  attrs[1].val.clusterDim.z = 1;
+  cfg.attrs = g_overlap ? attrs : attrs + 1;
+  cfg.numAttrs = g_overlap ? 1 : 0;
   const __nv_bfloat16* qq = static_cast<const __nv_bfloat16*>(q);
   __nv_bfloat16* oo = static_cast<__nv_bfloat16*>(out);
   const int nblk = hyq_nblk(c), cvl = hyq_vl_stride(c), ct = hyq_cap_tail(c);
   if (p.mode == kCluster) {
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs += 1;
     return cudaLaunchKernelEx(&cfg, decode_kernel<kCluster>, qq, *lay, oo, tickets, part, c->num_q_heads, gq,
                               nblk, cvl, ct, p.S, sa);
   }

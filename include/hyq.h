@@ -305,6 +305,22 @@ hyq_status hyq_decode_step(const hyq_config *cfg, const void *q, const void *k_n
                            hyq_stream_t stream);
 
 /*
+ * Let hyq_decode_attention and hyq_decode_step launches overlap the kernel
+ * launched before them on the same stream (programmatic dependent launch;
+ * process-wide, off by default).  With it on, every such launch lets the next
+ * launch on its stream start once the kernel before it has finished; it
+ * reads the layer's layout (counters, 4-bit stream, vertical-line and tail
+ * rows) before the preceding kernel has finished, and the query, the new
+ * K/V row, the workspace and every output only after.  The caller guarantees
+ * that the kernel launched immediately before each decode call on its stream
+ * does not write that call's layout: true in a transformer decode step (that
+ * kernel produces q, k, v) and between calls on different layers; false for
+ * consecutive calls on the same layer, which must run with it off.
+ * Returns HYQ_ERR_INVALID_ARG unless enable is 0 or 1.
+ */
+hyq_status hyq_set_decode_overlap(int32_t enable);
+
+/*
  * Override how hyq_decode_attention splits and merges its work (process-
  * wide; for tuning and testing).  merge: 0 automatic (the default), 1 one
  * block per (batch, KV head) and no merge, 2 `splits` blocks (2..16) merged

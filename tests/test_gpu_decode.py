@@ -275,3 +275,57 @@ def test_decode_step_full_tail_is_flagged(hyq):
     assert torch.equal(layer.counts(), before)
     want = hybrid_decode(c.q.double().numpy(), c.k.double().numpy(), c.v.double().numpy(), 12, 6, np.zeros((1, 1, 0), np.int64))
     assert_attention_close(to_np(out), want, what="full tail")
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_decode_overlap_across_layers(hyq, fused):
+    """With programmatic dependent launch on, calls alternating over two layers
+    (the kernel before each call belongs to the other layer) give the same bits
+    as with it off, fused step or attention alone, in a CUDA graph too."""
+    from hybrid_precision_quantized_gb300 import hyq_decode_step, hyq_set_decode_overlap
+    L0, W, ppm, steps = 1500, 128, 50_000, 4
+    cap = L0 + steps
+    cases = [decode_case(81 + i, 1, 8, 2, cap, window=W, n_proxy=16, sink_frac=0.02) for i in range(2)]
+    g = gen_for(81, "q-steps")
+    qs = torch.randn(steps, 2, 1, 8, 128, generator=g).to(torch.bfloat16).cuda()
+
+    def run(overlap, graph):
+        layers, outs = [], torch.zeros(steps, 2, 1, 8, 128, dtype=torch.bfloat16, device="cuda")
+        cfg = None
+        for c in cases:
+            cfg, (la, _), _ = _two_layers(c, L0, W, ppm, cap)
+            layers.append(la)
+        ws = workspace(cfg, L.OP_DECODE, cap)
+        kn = [[c.k[:, :, L0 + s].contiguous().cuda() for s in range(steps)] for c in cases]
+        vn = [[c.v[:, :, L0 + s].contiguous().cuda() for s in range(steps)] for c in cases]
+
+        def body():
+            for s in range(steps):
+                for i in range(2):
+                    if fused:
+                        hyq_decode_step(cfg, qs[s, i], kn[i][s], vn[i][s], layers[i].c, outs[s, i], ws, None, None, cap)
+                    else:
+                        hyq_decode_attention(cfg, qs[s, i], layers[i].c, outs[s, i], ws, cap)
+        hyq_set_decode_overlap(overlap)
+        try:
+            if graph:
+                st = torch.cuda.Stream()
+                st.wait_stream(torch.cuda.current_stream())
+                gr = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gr, stream=st):
+                    body()
+                gr.replay()
+            else:
+                body()
+            torch.cuda.synchronize()
+        finally:
+            hyq_set_decode_overlap(False)
+        for la in layers:
+            assert hyq_read_device_error(la.err()) == 0
+        return outs.cpu(), [la.counts().cpu() for la in layers]
+
+    ref, cref = run(False, False)
+    for graph in (False, True):
+        got, cgot = run(True, graph)
+        assert torch.equal(got, ref), f"overlap changed the result (graph={graph})"
+        assert all(torch.equal(a, b) for a, b in zip(cgot, cref))
