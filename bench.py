@@ -49,6 +49,7 @@ def parse():
     p.add_argument("--layers", type=int, default=N_LAYERS)
     p.add_argument("--no-baseline", action="store_true", help="skip the CPU oracle timing")
     p.add_argument("--no-prefill", action="store_true", help="skip the prefill measurement")
+    p.add_argument("--no-batched", action="store_true", help="skip the batch-16 decode measurement")
     p.add_argument("--overlap", action="store_true",
                    help="launch decode steps with programmatic dependent launch")
     p.add_argument("--case", default="period", choices=["period", "decode-layer", "prefill"],
@@ -61,8 +62,9 @@ def parse():
 
 
 def run_decode_layer_case(args, local):
-    """One Llama-shaped 32K layer (freeze, then 6 decode-attention launches);
-    prints the mean launch time.  Used as a small, self-contained ncu target."""
+    """One Llama-shaped 32K layer: freeze at 32K - 64 positions, then 6 fused
+    decode steps (hyq_decode_step, the call the benchmark times); prints the
+    mean launch time.  Used as a small, self-contained ncu target."""
     import torch
     import hybrid_precision_quantized_gb300 as hyq
     from hybrid_precision_quantized_gb300 import _lib as L
@@ -71,19 +73,19 @@ def run_decode_layer_case(args, local):
     dev = torch.device("cuda", local)
     hyq.load()
     cfg = hyq.make_config(B, HQ, HKV, capacity=CTX, window=WINDOW, period=PERIOD, rho_ppm=RHO_PPM)
-    k_srcs, v_srcs, q_tail, q_tok, _, _ = make_inputs(dev, 1)
+    k_srcs, v_srcs, q_tail, q_tok, k_tok, v_tok = make_inputs(dev, 1)
     layer = hyq.HybridLayer(cfg, dev)
     layer.reset()
-    idx = torch.zeros(B, HKV, 1632, dtype=torch.int32, device=dev)
-    k = hyq.hyq_select_vertical(cfg, q_tail[0], 64, k_srcs[0], CTX, idx, hyq.workspace(cfg, L.OP_SELECT, CTX, dev))
-    hyq.hyq_rebuild(cfg, k_srcs[0], v_srcs[0], CTX, idx, k, layer.c)
+    idx = torch.zeros(B, HKV, hyq.hyq_vl_count(cfg, L0 - WINDOW), dtype=torch.int32, device=dev)
+    k = hyq.hyq_select_vertical(cfg, q_tail[0], 64, k_srcs[0], L0, idx, hyq.workspace(cfg, L.OP_SELECT, CTX, dev))
+    hyq.hyq_rebuild(cfg, k_srcs[0], v_srcs[0], L0, idx, k, layer.c)
     ws = hyq.workspace(cfg, L.OP_DECODE, CTX, dev)
     out = torch.empty(B, HQ, D, dtype=torch.bfloat16, device=dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for i in range(6):
         if i == 2:
             e0.record()
-        hyq.hyq_decode_attention(cfg, q_tok[0, 0], layer.c, out, ws, CTX)
+        hyq.hyq_decode_step(cfg, q_tok[i, 0], k_tok[i, 0], v_tok[i, 0], layer.c, out, ws, k_srcs[0], v_srcs[0], CTX)
     e1.record()
     torch.cuda.synchronize()
     print(json.dumps({"case": "decode-layer", "us_per_launch_l2_warm": e0.elapsed_time(e1) * 1e3 / 4,
@@ -166,6 +168,69 @@ def prefill_measure(dev, lengths, reps=5, warmup=3):
                         "device_error_word": hyq.hyq_read_device_error(err)})
         del q, k, v, out, ws
     return res
+
+
+def batched_measure(dev, batch=16, n_layers=4, reps=5, warmup=3, seed=1003):
+    """Decode attention at batch 16 (Qwen3-8B-shaped heads: 32 query / 8 KV,
+    d 128, 32K context, W 128, rho 5%): per-call time over n_layers distinct
+    layers (~3 GB of hybrid caches, far beyond L2), CUDA events.  Each layer
+    is built from device-generated BF16 (2% planted vertical lines) that is
+    freed once the layer's hybrid cache is built."""
+    import torch
+    import hybrid_precision_quantized_gb300 as hyq
+    from hybrid_precision_quantized_gb300 import _lib as L
+    Bb = batch
+    cfg = hyq.make_config(Bb, HQ, HKV, capacity=CTX, window=WINDOW, period=PERIOD, rho_ppm=RHO_PPM)
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    P = CTX - WINDOW
+    k_vl = hyq.hyq_vl_count(cfg, P)
+    layers = []
+    for _ in range(n_layers):
+        u = torch.randn(Bb, HKV, D, generator=g, device=dev)
+        u = u / u.norm(dim=-1, keepdim=True)
+        k = torch.randn(Bb, HKV, CTX, D, generator=g, device=dev, dtype=torch.bfloat16)
+        ns = int(0.02 * P)
+        pos = torch.randint(0, P, (Bb, HKV, ns), generator=g, device=dev)
+        bi = torch.arange(Bb, device=dev)[:, None, None].expand_as(pos)
+        hi = torch.arange(HKV, device=dev)[None, :, None].expand_as(pos)
+        k[bi, hi, pos] += (4.0 * u[:, :, None, :]).to(torch.bfloat16).expand(Bb, HKV, ns, D)
+        v = torch.randn(Bb, HKV, CTX, D, generator=g, device=dev, dtype=torch.bfloat16)
+        qt = (torch.randn(Bb, HQ, 64, D, generator=g, device=dev)
+              + 2.0 * u.repeat_interleave(HQ // HKV, 1)[:, :, None]).to(torch.bfloat16)
+        lay = hyq.HybridLayer(cfg, dev)
+        lay.reset()
+        idx = torch.zeros(Bb, HKV, k_vl, dtype=torch.int32, device=dev)
+        kk = hyq.hyq_select_vertical(cfg, qt, 64, k, CTX, idx, hyq.workspace(cfg, L.OP_SELECT, CTX, dev))
+        hyq.hyq_rebuild(cfg, k, v, CTX, idx, kk, lay.c)
+        torch.cuda.synchronize()
+        del k, v
+        layers.append(lay)
+    q = (torch.randn(n_layers, Bb, HQ, D, generator=g, device=dev)).to(torch.bfloat16)
+    out = torch.empty(Bb, HQ, D, dtype=torch.bfloat16, device=dev)
+    ws = hyq.workspace(cfg, L.OP_DECODE, CTX, dev)
+    for _ in range(warmup):
+        for li in range(n_layers):
+            hyq.hyq_decode_attention(cfg, q[li], layers[li].c, out, ws, CTX)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        for li in range(n_layers):
+            hyq.hyq_decode_attention(cfg, q[li], layers[li].c, out, ws, CTX)
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (reps * n_layers)
+    nbytes = Bb * (HKV * ((P - k_vl) * 160 + (k_vl + WINDOW) * 512) + 2 * HQ * D * 2)
+    peak, kind = measured_peaks()
+    gbs = nbytes / (us * 1e-6) / 1e9
+    err = max(hyq.hyq_read_device_error(l.err()) for l in layers)
+    return {"workload": "qwen3-8b-shaped batched decode attention, B16, 32/8 heads, d128, 32K ctx, W128, rho 5%, "
+                        "K4V4 G32; 4 distinct layers", "us_per_call": us, "us_per_token_36_layers": us * 36 / Bb,
+            "algorithmic_bytes_per_call": nbytes,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                         "peak_source": f"{kind} hbm_gbs"},
+            "device_error_word": err}
 
 
 def run_prefill_case(args, local):
@@ -466,6 +531,7 @@ def run_ours(args, rank, world, local):
     peak, peak_kind = measured_peaks()
     base = None if args.no_baseline else cpu_baseline()
     prefill = None if args.no_prefill else prefill_measure(dev, [CTX], reps=5)
+    batched = None if args.no_batched else batched_measure(dev)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": False,
@@ -488,6 +554,7 @@ def run_ours(args, rank, world, local):
                 "d2h_bytes_per_step": d2h},
         "clocks": clk.summary(),
         "cpu_baseline": base,
+        "batched": batched,
         "prefill": ({"workload": "llama3.1-8b-shaped causal prefill, B1, 32/8 heads, d128, 32K, W128, rho 5% "
                                  "(hyq_prefill_attention: pack + main kernel)",
                      "flops": "4 d HQ L(L+1)/2", "l2": "256 MB flush before every timed call",
