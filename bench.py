@@ -255,6 +255,24 @@ def dist_setup(args):
     return rank, world, local
 
 
+def reduce_timing(ms, world, device):
+    """Max over ranks of a per-rank elapsed time: the slowest rank sets the
+    job's time (weak scaling, no data-path collective)."""
+    if world <= 1:
+        return float(ms)
+    import torch
+    import torch.distributed as dist
+    tt = torch.tensor([float(ms)], device=device, dtype=torch.float64)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_value(ms_total, steps, units_per_rank, world):
+    """Microseconds per unit for the whole job: the job's time per step over
+    the units every rank processed in that step."""
+    return ms_total / steps * 1e3 / (units_per_rank * world)
+
+
 def algorithmic_bytes(n_q, n_vl, n_tail):
     """Bytes one decode-attention call must move (B=1 layer): 160 per 4-bit
     row (K+V codes, FP16 scale+zero), 512 per BF16 row (K+V), q and out."""
@@ -492,13 +510,10 @@ def run_ours(args, rank, world, local):
     ms = t0.elapsed_time(t1)
     dec_ms = sum(a.elapsed_time(b) for row in ev for a, b in row)
     err = max(hyq.hyq_read_device_error(l.err()) for l in run.layers)
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = reduce_timing(ms, world, dev)
     ms_per_step = ms / args.steps
     tokens_layers = PERIOD * nl * world
-    value = ms_per_step * 1e3 / tokens_layers
+    value = job_value(ms, args.steps, PERIOD * nl, world)
 
     # end to end: same periods with every token's inputs in pinned host memory
     q_h = q_tok.cpu().pin_memory()
@@ -515,10 +530,7 @@ def run_ours(args, rank, world, local):
     e1.record()
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = reduce_timing(e2e_ms, world, dev)
     h2d = q_h.numel() * 2 + k_h.numel() * 2 + v_h.numel() * 2
     d2h = o_h.numel() * 2
 
