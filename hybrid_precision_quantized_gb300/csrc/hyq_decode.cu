@@ -476,33 +476,37 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
   // a flood of tile copies ahead of it would delay the start of all compute
   // by the flood's service time.
   if (!ovl && !mbar_wait(&qbar, 0) && tid == 0) hyq_set_err(lay.err, HYQ_DEVERR_TIMEOUT);
-  if (lane == 0) {
+  if (warp < n_staged) {
     // The first kFStaged BF16 tiles of this block: the rows of a tile are
     // contiguous in the vertical-line buffer and in the tail, so a tile takes
-    // one K and one V copy per buffer it touches.  Used after the 4-bit loop.
-    if (warp < n_staged) {
-      const int row0 = 16 * (f0 + warp), nrows = min(16, nf - row0);
-      // the new row of a fused step (if in this tile) comes from the input instead
-      const int rnew = app ? nvl + ntail - row0 : -1;
-      const int ncopy = nrows - ((rnew >= 0 && rnew < nrows) ? 1 : 0);
-      mbar_arrive_expect_tx(&fbars[warp], ncopy * 2 * HYQ_D * 2);
-      const int na = max(0, min(row0 + nrows, nvl) - row0);  // rows in the vertical-line buffer
-      if (na > 0) {
-        bulk_g2s(fstage, vlk + (size_t)row0 * HYQ_D, na * HYQ_D * 2, &fbars[warp]);
-        bulk_g2s(fstage + 16 * kFKStride, vlv + (size_t)row0 * HYQ_D, na * HYQ_D * 2, &fbars[warp]);
-      }
-      const int ntr = min(nrows - na, ntail - max(0, row0 + na - nvl));  // stored tail rows (not the new one)
-      if (ntr > 0) {
-        const int tr = row0 + na - nvl;  // first tail row
-        bulk_g2s(fstage + na * kFKStride, tk + (size_t)tr * HYQ_D, ntr * HYQ_D * 2, &fbars[warp]);
-        bulk_g2s(fstage + 16 * kFKStride + na * kFVStride, tv + (size_t)tr * HYQ_D, ntr * HYQ_D * 2, &fbars[warp]);
-      }
+    // one K and one V copy per buffer it touches, issued by lanes 4 and 5
+    // (not by the ring lanes).  Used after the 4-bit loop.
+    const int row0 = 16 * (f0 + warp), nrows = min(16, nf - row0);
+    // the new row of a fused step (if in this tile) comes from the input instead
+    const int rnew = app ? nvl + ntail - row0 : -1;
+    const int ncopy = nrows - ((rnew >= 0 && rnew < nrows) ? 1 : 0);
+    const int na = max(0, min(row0 + nrows, nvl) - row0);  // rows in the vertical-line buffer
+    const int ntr = min(nrows - na, ntail - max(0, row0 + na - nvl));  // stored tail rows (not the new one)
+    if (lane == 4) mbar_arrive_expect_tx(&fbars[warp], ncopy * 2 * HYQ_D * 2);
+    __syncwarp();
+    if (lane == 4 && na > 0) {
+      bulk_g2s(fstage, vlk + (size_t)row0 * HYQ_D, na * HYQ_D * 2, &fbars[warp]);
+      bulk_g2s(fstage + 16 * kFKStride, vlv + (size_t)row0 * HYQ_D, na * HYQ_D * 2, &fbars[warp]);
     }
-    for (int j = 0; j < nj && j < kSlots; ++j) {
-      mbar_arrive_expect_tx(&wb[j], HYQ_QTILE_BYTES);
-      bulk_g2s(ring + j * HYQ_QTILE_BYTES, tiles + (size_t)(t0 + my0 + kWarps * j) * HYQ_QTILE_BYTES,
-               HYQ_QTILE_BYTES, &wb[j]);
+    if (lane == 5 && ntr > 0) {
+      const int tr = row0 + na - nvl;  // first tail row
+      bulk_g2s(fstage + na * kFKStride, tk + (size_t)tr * HYQ_D, ntr * HYQ_D * 2, &fbars[warp]);
+      bulk_g2s(fstage + 16 * kFKStride + na * kFVStride, tv + (size_t)tr * HYQ_D, ntr * HYQ_D * 2, &fbars[warp]);
     }
+  }
+  // Ring slot i is always filled by lane i: the bulk copies one thread issues
+  // complete one after another, so one issuing lane per slot keeps all of a
+  // warp's slots in flight at once.
+  if (lane < kSlots && lane < nj) {
+    const int j = lane;
+    mbar_arrive_expect_tx(&wb[j], HYQ_QTILE_BYTES);
+    bulk_g2s(ring + j * HYQ_QTILE_BYTES, tiles + (size_t)(t0 + my0 + kWarps * j) * HYQ_QTILE_BYTES,
+             HYQ_QTILE_BYTES, &wb[j]);
   }
   if (ovl) {
     // The layout copies are in flight; now wait for the preceding kernel and
@@ -595,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
     const int tile = t0 + my0 + kWarps * j;
     q_tile(ring + slot * HYQ_QTILE_BYTES, lane, min(16, nq - 16 * tile), bq, qc, st);
     __syncwarp();
-    if (lane == 0 && j + kSlots < nj) {
+    if (lane == slot && j + kSlots < nj) {
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
       mbar_arrive_expect_tx(&wb[slot], HYQ_QTILE_BYTES);
       bulk_g2s(ring + slot * HYQ_QTILE_BYTES, tiles + (size_t)(tile + kWarps * kSlots) * HYQ_QTILE_BYTES,

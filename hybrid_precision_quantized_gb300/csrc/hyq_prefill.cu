@@ -19,8 +19,9 @@
 //     2-stage ring each); warp 10 issues tcgen05.mma: S = Q K^T into TMEM (double buffer), then
 //     O_h += P_h V_h into TMEM for the two 64-key halves h of each tile;
 //     warps 0-7 (one thread per query row = TMEM lane and key half) read S,
-//     scale, mask, run an online softmax per half and write P back to
-//     shared memory; the two halves' (max, sum, O) merge once at the end.  The quantised segment uses e4m3 codes (kind::f8f6f4) or INT8
+//     scale, mask, run an online softmax per half and write P as BF16 over
+//     the S columns they have read, where the P.V MMA takes its A operand
+//     from tensor memory; the two halves' (max, sum, O) merge once at the end.  The quantised segment uses e4m3 codes (kind::f8f6f4) or INT8
 //     codes held exactly as BF16 integers (kind::f16; sm_103a has no integer
 //     tensor-core MMA); the full-precision segment uses BF16.  P.V runs in
 //     BF16 with the value codes (exact in BF16) and the value scale folded
@@ -47,18 +48,22 @@ constexpr int kSoft = 256;           // softmax threads (warps 0-7)
 constexpr int kCopyWarp = 8, kMmaWarp = 10;  // copy warps 8 (keys) and 9 (values)
 constexpr int kThreads = 352;
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: S double buffer, then one O accumulator per key half.
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 384;
+// TMEM columns: S (one 128-key tile, FP32), P (two tiles in flight, BF16
+// pairs: 64 columns per tile, 32 per key half), one O accumulator per key half.
+constexpr uint32_t kColS = 0, kColP = 128, kColO0 = 256, kColO1 = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Shared-memory map (offsets from a 1024-byte aligned base).
 constexpr int kOffQ = 0;                   // Q, BF16 image
 constexpr int kOffQc = kOffQ + kImg16;     // Q codes image (8- or 16-bit)
-constexpr int kOffK = kOffQc + kImg16;     // 2 key stages
-constexpr int kOffV = kOffK + 2 * kImg16;  // 2 value stages (transposed)
-constexpr int kOffP = kOffV + 2 * kImg16;  // probabilities, BF16 image
-constexpr int kOffBar = kOffP + kImg16;
-constexpr int kNumBars = 18;
+constexpr int kOffK = kOffQc + kImg16;     // key stages
+#ifndef HYQ_PREFILL_KSTAGES
+#define HYQ_PREFILL_KSTAGES 3
+#endif
+constexpr int kKStages = HYQ_PREFILL_KSTAGES, kVStages = 5 - HYQ_PREFILL_KSTAGES;
+constexpr int kOffV = kOffK + kKStages * kImg16;  // value stages (transposed)
+constexpr int kOffBar = kOffV + kVStages * kImg16;
+constexpr int kNumBars = 24;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemUsed = kOffMisc + 64;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // room to align the base
@@ -339,15 +344,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                                            ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
   uint64_t* qready = bars + 0;
-  uint64_t* kfull = bars + 1;   // [2]
-  uint64_t* kempty = bars + 3;  // [2]
-  uint64_t* vfull = bars + 5;   // [2]
-  uint64_t* vempty = bars + 7;  // [2]
-  uint64_t* sfull = bars + 9;   // [2]
-  uint64_t* sfree = bars + 11;  // [2]
-  uint64_t* pfull = bars + 13;  // [2], one per key half
-  uint64_t* pvdone = bars + 15; // [2]
-  uint64_t* mmadone = bars + 17;
+  uint64_t* kfull = bars + 18;  // [kKStages]
+  uint64_t* kempty = bars + 21; // [kKStages]
+  uint64_t* sfull = bars + 5;   // S of the current tile is in TMEM
+  uint64_t* sfree = bars + 6;   // every softmax thread has read it
+  uint64_t* pfull = bars + 7;   // [2], one per key half
+  uint64_t* pvdone = bars + 9;  // [2]
+  uint64_t* mmadone = bars + 11;
+  uint64_t* vfull = bars + 12;  // [kVStages]
+  uint64_t* vempty = bars + 15; // [kVStages]
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kOffMisc + 4);
   int* ntiles = reinterpret_cast<int*>(sm + kOffMisc + 8);     // [4]
@@ -367,17 +372,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 
   if (tid == 0) {
     mbar_init(qready, kSoft);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(kfull + i, 1);
-      mbar_init(kempty + i, 1);
+    for (int i = 0; i < kVStages; ++i) {
       mbar_init(vfull + i, 1);
       mbar_init(vempty + i, 1);
-      mbar_init(sfull + i, 1);
-      mbar_init(sfree + i, kSoft);
+    }
+    for (int i = 0; i < kKStages; ++i) {
+      mbar_init(kfull + i, 1);
+      mbar_init(kempty + i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(pfull + i, kSoft / 2);
       mbar_init(pvdone + i, 1);
     }
     mbar_init(mmadone, 1);
+    mbar_init(sfull, 1);
+    mbar_init(sfree, kSoft);
     mbar_fence_init();
     *abort_flag = 0;
   }
@@ -482,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     for (int j = 0; j < nt; ++j) {
       const int s = j & 1;
       const bool quant = j < nqt;
-      if (!mbar_wait_or_abort(sfull + s, (j >> 1) & 1, abort_flag)) {
+      if (!mbar_wait_or_abort(sfull, j & 1, abort_flag)) {
         fail();
         ok = false;
         break;
@@ -491,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       float x[64];
       {
         uint32_t ra[32], rb[32];
-        const uint32_t ts = tbase + lane_off + (s ? kColS1 : kColS0) + 64 * hf;
+        const uint32_t ts = tbase + lane_off + kColS + 64 * hf;
         tc_ld32(ts, ra);
         tc_ld32(ts + 32, rb);
         tc_wait_ld();
@@ -502,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         }
       }
       tc_fence_before();
-      mbar_arrive(sfree + s);
+      mbar_arrive(sfree);  // the MMA warp may compute the next tile's S now
 
       // A scale is 0 only when every code it multiplies is 0; keeping it
       // positive changes no score and makes masked (-inf) keys give 0.
@@ -565,20 +574,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           tc_wait_st();
         }
       }
+      {
+        // P_h (BF16 pairs, the value scale folded in) into P buffer j % 2,
+        // whose previous tile's P.V is done: the A operand of P.V.
+        uint32_t pw[32];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 u = make_uint4(pack_bf16x2(x[8 * c] * vf, x[8 * c + 1] * vf),
-                                   pack_bf16x2(x[8 * c + 2] * vf, x[8 * c + 3] * vf),
-                                   pack_bf16x2(x[8 * c + 4] * vf, x[8 * c + 5] * vf),
-                                   pack_bf16x2(x[8 * c + 6] * vf, x[8 * c + 7] * vf));
-        *reinterpret_cast<uint4*>(sm + kOffP + hf * kRegion + swz(rr, c)) = u;
+        for (int w = 0; w < 32; ++w) pw[w] = pack_bf16x2(x[2 * w] * vf, x[2 * w + 1] * vf);
+        tc_st32(tbase + lane_off + kColP + 64 * s + 32 * hf, pw);
+        tc_wait_st();
       }
-      fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(pfull + hf);
     }
     // Merge the two halves.  Each half waits for its own last P.V, leaves
-    // (m, l) in its own P region (free from then on), and the named barrier
+    // (m, l) in its own region of key stage 0 (no copy or MMA touches it any
+    // more: every MMA before that last P.V has finished), and the named barrier
     // makes both halves' accumulators and (m, l) visible to every thread;
     // each thread then writes dims 64hf .. 64hf+63 of its row.
     bool done = ok && nt > 0;
@@ -586,8 +596,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       fail();
       done = false;
     }
-    float* xch_own = reinterpret_cast<float*>(sm + kOffP + hf * kRegion);
-    const float* xch_oth = reinterpret_cast<const float*>(sm + kOffP + (hf ^ 1) * kRegion);
+    float* xch_own = reinterpret_cast<float*>(sm + kOffK + hf * kRegion);
+    const float* xch_oth = reinterpret_cast<const float*>(sm + kOffK + (hf ^ 1) * kRegion);
     if (done) {
       xch_own[rr] = m_used;
       xch_own[kRows + rr] = l_sum;
@@ -627,85 +637,91 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     }
   } else if (warp == kCopyWarp || warp == kCopyWarp + 1) {
     // ---------------- copy warps: keys (8) and values (9), each its own
-    // 2-stage ring, so that key tiles are not held back by value tiles ---
-    if (lane == 0) {
-      const bool is_v = warp != kCopyWarp;
-      uint64_t* full = is_v ? vfull : kfull;
-      uint64_t* empty = is_v ? vempty : kempty;
-      const int qimg = is_v ? kImg16 : kKImg;
-      const uint8_t* qsrc = is_v ? p.vq + bh * p.ntq * (size_t)kImg16 : p.kq + bh * p.ntq * (size_t)kKImg;
-      const uint8_t* fsrc = (is_v ? p.vf : p.kf) + bh * p.ntf * (size_t)kImg16;
-      uint8_t* dst = sm + (is_v ? kOffV : kOffK);
-      int last_j = -1;
-      bool ok = true;
-      for (int j = 0; j < nt; ++j) {
-        const int s = j & 1;
-        if (j >= 2 && !mbar_wait_or_abort(empty + s, ((j >> 1) & 1) ^ 1, abort_flag)) {
+    // ring, so that key tiles are not held back by value tiles.  A tile
+    // image goes as four quarter copies from lanes 0-3: the bulk copies one
+    // thread issues complete one after another, so four issuing lanes keep
+    // four in flight. ----------------------------------------------------
+    const bool is_v = warp != kCopyWarp;
+    uint64_t* full = is_v ? vfull : kfull;
+    uint64_t* empty = is_v ? vempty : kempty;
+    const int qimg = is_v ? kImg16 : kKImg;
+    const uint8_t* qsrc = is_v ? p.vq + bh * p.ntq * (size_t)kImg16 : p.kq + bh * p.ntq * (size_t)kKImg;
+    const uint8_t* fsrc = (is_v ? p.vf : p.kf) + bh * p.ntf * (size_t)kImg16;
+    uint8_t* dst = sm + (is_v ? kOffV : kOffK);
+    const int nst = is_v ? kVStages : kKStages;  // ring stages
+    int last_j = -1;
+    bool ok = true;
+    for (int j = 0; j < nt; ++j) {
+      const int s = j % nst;
+      if (j >= nst) {
+        bool got = true;
+        if (lane == 0) got = mbar_wait_or_abort(empty + s, ((j / nst) & 1) ^ 1, abort_flag);
+        if (!__shfl_sync(0xffffffffu, got, 0)) {
           ok = false;
           break;
         }
-        const bool quant = j < nqt;
-        const uint32_t bytes = quant ? qimg : kImg16;
-        mbar_arrive_expect_tx(full + s, bytes);
-        bulk_g2s(dst + s * kImg16, quant ? qsrc + (size_t)j * qimg : fsrc + (size_t)(j - nqt) * kImg16, bytes,
-                 full + s);
-        last_j = j;
       }
-      if (!ok) {
-        *abort_flag = 1;
-        hyq_set_err(p.err, HYQ_DEVERR_TIMEOUT);
-        // let the copies in flight (the last two tiles') land before the
-        // CTA's shared memory goes away
-        for (int j = max(0, last_j - 1); j <= last_j; ++j) mbar_wait(full + (j & 1), (j >> 1) & 1);
-      }
+      const bool quant = j < nqt;
+      const uint32_t bytes = quant ? qimg : kImg16, part = bytes / 4;
+      const uint8_t* src = quant ? qsrc + (size_t)j * qimg : fsrc + (size_t)(j - nqt) * kImg16;
+      if (lane == 0) mbar_arrive_expect_tx(full + s, bytes);
+      __syncwarp();
+      if (lane < 4) bulk_g2s(dst + s * kImg16 + lane * part, src + lane * part, part, full + s);
+      last_j = j;
+    }
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      hyq_set_err(p.err, HYQ_DEVERR_TIMEOUT);
+      // let the copies in flight (the last stages' tiles) land before the
+      // CTA's shared memory goes away
+      for (int j = max(0, last_j - nst + 1); j <= last_j; ++j) mbar_wait(full + j % nst, (j / nst) & 1);
     }
   } else {
     // ---------------- MMA warp -----------------------------------------
     if (lane == 0) {
-      const uint32_t aQ = smem_u32(sm + kOffQ), aQc = smem_u32(sm + kOffQc), aP = smem_u32(sm + kOffP);
+      const uint32_t aQ = smem_u32(sm + kOffQ), aQc = smem_u32(sm + kOffQc);
       bool ok = mbar_wait_or_abort(qready, 0, abort_flag);
       tc_fence_after();
       for (int j = 0; ok && j <= nt; ++j) {
         if (j < nt) {
-          const int s = j & 1;
-          ok = mbar_wait_or_abort(kfull + s, (j >> 1) & 1, abort_flag);
-          if (ok && j >= 2) ok = mbar_wait_or_abort(sfree + s, ((j >> 1) & 1) ^ 1, abort_flag);
+          const int s = j & 1, sk = j % kKStages;
+          ok = mbar_wait_or_abort(kfull + sk, (j / kKStages) & 1, abort_flag);
+          // the softmax has read S of the previous tile
+          if (ok && j >= 1) ok = mbar_wait_or_abort(sfree, (j - 1) & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t aK = smem_u32(sm + kOffK + s * kImg16);
+          const uint32_t aK = smem_u32(sm + kOffK + sk * kImg16);
           if (kFp8 && j < nqt) {
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-              tc_mma_f8(tbase + (s ? kColS1 : kColS0), tc_desc_sw128(aQc + 32 * ks), tc_desc_sw128(aK + 32 * ks), kIdescE4M3, ks > 0);
+              tc_mma_f8(tbase + kColS, tc_desc_sw128(aQc + 32 * ks), tc_desc_sw128(aK + 32 * ks), kIdescE4M3, ks > 0);
           } else {
             const uint32_t aA = j < nqt ? aQc : aQ;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
               const uint32_t off = (ks >> 2) * kRegion + (ks & 3) * 32;
-              tc_mma_f16(tbase + (s ? kColS1 : kColS0), tc_desc_sw128(aA + off), tc_desc_sw128(aK + off), kIdescBF16, ks > 0);
+              tc_mma_f16(tbase + kColS, tc_desc_sw128(aA + off), tc_desc_sw128(aK + off), kIdescBF16, ks > 0);
             }
           }
-          tc_commit(sfull + s);
-          tc_commit(kempty + s);
+          tc_commit(sfull);
+          tc_commit(kempty + sk);
         }
         if (j >= 1) {  // O_h += P_h V_h for tile i = j - 1, one key half at a time
-          const int i = j - 1, s = i & 1;
-          ok = mbar_wait_or_abort(vfull + s, (i >> 1) & 1, abort_flag);
-          const uint32_t aV = smem_u32(sm + kOffV + s * kImg16);
+          const int i = j - 1, s = i & 1, sv = i % kVStages;
+          ok = mbar_wait_or_abort(vfull + sv, (i / kVStages) & 1, abort_flag);
+          const uint32_t aV = smem_u32(sm + kOffV + sv * kImg16);
           for (int hf = 0; ok && hf < 2; ++hf) {
             ok = mbar_wait_or_abort(pfull + hf, i & 1, abort_flag);
             if (!ok) break;
             tc_fence_after();
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-              const uint32_t off = hf * kRegion + ks * 32;
-              tc_mma_f16(tbase + (hf ? kColO1 : kColO0), tc_desc_sw128(aP + off), tc_desc_sw128(aV + off), kIdescBF16,
-                         (i > 0 || ks > 0) ? 1u : 0u);
-            }
+            for (int ks = 0; ks < 4; ++ks)
+              tc_mma_f16_ts(tbase + (hf ? kColO1 : kColO0), tbase + kColP + 64 * s + 32 * hf + 8 * ks,
+                            tc_desc_sw128(aV + hf * kRegion + ks * 32), kIdescBF16, (i > 0 || ks > 0) ? 1u : 0u);
             tc_commit(pvdone + hf);
           }
           if (!ok) break;
-          tc_commit(vempty + s);
+          tc_commit(vempty + sv);
         }
       }
       if (!ok) {

@@ -40,6 +40,16 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a, uint64_t
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T with A read from tensor memory: row m of
+// A in lane m, two consecutive 16-bit K elements per 32-bit column.
+__device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
 // Same with 8-bit floating-point operands (e4m3).
 __device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
                                           uint32_t accumulate) {
