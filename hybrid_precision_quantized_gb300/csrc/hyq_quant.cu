@@ -52,14 +52,24 @@ __device__ __forceinline__ void unpack8(uint4 v, float (&f)[8]) {
 __device__ void build_block(BuildSmem& sm, const __nv_bfloat16* kbase, const __nv_bfloat16* vbase,
                             uint8_t* dst, bool any_keep, int32_t* err) {
   const int tid = threadIdx.x;
-  // Pass 1: load the rows, per-group min / max (4 chunks of 8 per group are
-  // on 4 consecutive lanes).
-  for (int f = tid; f < 2 * kRows * kChunks; f += kThreads) {
+  // Pass 1: load the rows (all of a thread's loads first), per-group min /
+  // max (4 chunks of 8 per group are on 4 consecutive lanes).
+  constexpr int kPer = 2 * kRows * kChunks / kThreads;
+  uint4 vin[kPer];
+#pragma unroll
+  for (int it = 0; it < kPer; ++it) {
+    const int f = tid + it * kThreads;
     const int T = f >> 10, row = (f >> 4) & (kRows - 1), c = f & (kChunks - 1);
     const int32_t p = sm.pos[row];
-    uint4 v = make_uint4(0, 0, 0, 0);
+    vin[it] = make_uint4(0, 0, 0, 0);
     if (p >= 0 && !sm.keep[row])
-      v = *reinterpret_cast<const uint4*>((T ? vbase : kbase) + (size_t)p * HYQ_D + 8 * c);
+      vin[it] = __ldg(reinterpret_cast<const uint4*>((T ? vbase : kbase) + (size_t)p * HYQ_D + 8 * c));
+  }
+#pragma unroll
+  for (int it = 0; it < kPer; ++it) {
+    const int f = tid + it * kThreads;
+    const int T = f >> 10, row = (f >> 4) & (kRows - 1), c = f & (kChunks - 1);
+    const uint4 v = vin[it];
     *reinterpret_cast<uint4*>(&sm.x[T][row][8 * c]) = v;
     float e[8];
     unpack8(v, e);
@@ -196,6 +206,28 @@ __device__ __forceinline__ int32_t stream_pos(int32_t r, const int32_t* idx, int
   return r + lo;
 }
 
+// Warp-cooperative #{i < k : idx[i] - i <= x} for a strictly ascending idx
+// (so idx[i] - i is non-decreasing): 32 probes per round.
+__device__ __forceinline__ int32_t warp_count_f_le(const int32_t* idx, int32_t k, int32_t x, int lane) {
+  int32_t lo = 0, hi = k;  // f(i) <= x for i < lo, f(i) > x for i >= hi
+  while (lo < hi) {
+    const int32_t step = (hi - lo + 31) >> 5;
+    const int32_t i = lo + lane * step;
+    const bool le = i < hi && __ldg(idx + i) - i <= x;
+    const int cnt = __popc(__ballot_sync(0xffffffffu, le));
+    if (cnt == 0) {
+      hi = lo;
+    } else {
+      const int32_t nlo = lo + (cnt - 1) * step + 1;
+      hi = min(hi, lo + cnt * step);
+      lo = nlo;
+    }
+  }
+  return lo;
+}
+
+constexpr int kWinF = 256;  // vertical-line entries a block resolves in shared memory
+
 // grid (blocks of the new stream, HKV, B)
 __global__ void __launch_bounds__(kThreads) rebuild_blocks_kernel(
     const __nv_bfloat16* __restrict__ k_src, const __nv_bfloat16* __restrict__ v_src, int32_t ld,
@@ -206,11 +238,35 @@ __global__ void __launch_bounds__(kThreads) rebuild_blocks_kernel(
   const size_t bh = (size_t)b * HKV + h;
   const int32_t nq = P - k;
   const int32_t* idx_bh = idx ? idx + bh * k : nullptr;
+  // Stream row R sits at position R + #{i : idx[i] - i <= R}.  Warps 0 and 1
+  // find that count at the block's first and last row; the entries in
+  // between go to shared memory, where every row counts its own.
+  __shared__ int32_t s_c[2];
+  __shared__ int32_t s_f[kWinF];
+  const int32_t r0 = bi * kRows, r1 = min(nq, r0 + kRows) - 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (k > 0 && warp < 2) {
+    const int32_t c = warp_count_f_le(idx_bh, k, warp == 0 ? r0 - 1 : r1, lane);
+    if (lane == 0) s_c[warp] = c;
+  }
+  __syncthreads();
+  const int32_t c0 = k > 0 ? s_c[0] : 0, m = k > 0 ? s_c[1] - s_c[0] : 0;
+  if (m <= kWinF)
+    for (int i = threadIdx.x; i < m; i += kThreads) s_f[i] = __ldg(idx_bh + c0 + i) - (c0 + i);
+  __syncthreads();
   if (threadIdx.x < kRows) {
     const int32_t r = bi * kRows + threadIdx.x;
     int32_t p = -1;
     if (r < nq) {
-      p = k > 0 ? stream_pos(r, idx_bh, k) : r;
+      if (k == 0) {
+        p = r;
+      } else if (m <= kWinF) {
+        int32_t c = c0;
+        for (int i = 0; i < m; ++i) c += s_f[i] <= r;
+        p = r + c;
+      } else {
+        p = stream_pos(r, idx_bh, k);  // a run of more than kWinF vertical lines
+      }
       if (p < 0 || p >= P) {  // only possible for an invalid idx list
         hyq_set_err(err, HYQ_DEVERR_INDEX);
         p = min(max(p, 0), P - 1);

@@ -7,6 +7,8 @@
 //          written in ascending order.
 // Three launches: proxy sum, scores (HBM-bound pass over the BF16 keys),
 // radix select + ordered compaction (one CTA per KV head).
+#include <cooperative_groups.h>
+
 #include "hyq_common.cuh"
 
 namespace {
@@ -36,16 +38,39 @@ SelectWs carve(const hyq_config* c, int32_t L, void* ws) {
   return w;
 }
 
-// u[b][kvh][d] = sum over t < n_proxy and the g heads of the group.  grid (HKV, B), 128 threads
-__global__ void proxy_sum_kernel(const __nv_bfloat16* __restrict__ qp, int32_t n_proxy,
-                                 int32_t n_ld, int32_t gq, float* __restrict__ u) {
-  const int h = blockIdx.x, b = blockIdx.y, HKV = gridDim.x, d = threadIdx.x;
-  float acc = 0.f;
-  for (int j = 0; j < gq; ++j) {
-    const __nv_bfloat16* base = qp + (((size_t)b * HKV * gq + (size_t)h * gq + j) * n_ld) * HYQ_D + d;
-    for (int t = 0; t < n_proxy; ++t) acc += __bfloat162float(base[(size_t)t * HYQ_D]);
+// u[b][kvh][d] = sum over t < n_proxy and the g heads of the group.
+// grid (HKV, B), 512 threads: thread (r, c) sums 8 dims (c) over the rows
+// r, r + 32, ... of the g * n_proxy query rows with 16-byte loads; the 32
+// row-group partials are then added in a fixed order (deterministic).
+constexpr int kProxyThreads = 512;
+__global__ void __launch_bounds__(kProxyThreads) proxy_sum_kernel(const __nv_bfloat16* __restrict__ qp,
+                                                                  int32_t n_proxy, int32_t n_ld, int32_t gq,
+                                                                  float* __restrict__ u) {
+  __shared__ float part[32][HYQ_D + 4];
+  const int h = blockIdx.x, b = blockIdx.y, HKV = gridDim.x;
+  const int r0 = threadIdx.x >> 4, c = threadIdx.x & 15;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  const int rows = gq * n_proxy;
+  for (int r = r0; r < rows; r += 32) {
+    const int j = r / n_proxy, t = r - j * n_proxy;
+    const __nv_bfloat16* row = qp + (((size_t)b * HKV * gq + (size_t)h * gq + j) * n_ld + t) * HYQ_D;
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(row) + c);
+    const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(p2[i]);
+      acc[2 * i] += f.x;
+      acc[2 * i + 1] += f.y;
+    }
   }
-  u[((size_t)b * HKV + h) * HYQ_D + d] = acc;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) part[r0][8 * c + i] = acc[i];
+  __syncthreads();
+  if (threadIdx.x < HYQ_D) {
+    float s = 0.f;
+    for (int r = 0; r < 32; ++r) s += part[r][threadIdx.x];
+    u[((size_t)b * HKV + h) * HYQ_D + threadIdx.x] = s;
+  }
 }
 
 __device__ __forceinline__ uint32_t order_key(float s, int32_t* err) {
@@ -93,57 +118,78 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(
   }
 }
 
-// Block-wide exclusive scan of 0/1 flags (1024 threads).  Returns the prefix
-// for this thread; *total gets the block total.
-__device__ __forceinline__ int block_scan_flag(int f, int* warp_sums, int* total) {
+// Block-wide exclusive scan of small counts (1024 threads).  Returns the
+// prefix for this thread; *total gets the block total.
+__device__ __forceinline__ int block_scan_count(int v, int* warp_sums, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  unsigned m = __ballot_sync(0xffffffffu, f);
-  int pre = __popc(m & ((1u << lane) - 1u));
-  if (lane == 0) warp_sums[warp] = __popc(m);
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    int v = warp_sums[lane];
-    int x = v;
+    const int w = warp_sums[lane];
+    int z = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      int y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
+      const int y = __shfl_up_sync(0xffffffffu, z, o);
+      if (lane >= o) z += y;
     }
-    warp_sums[lane] = x - v;  // exclusive
-    if (lane == 31) warp_sums[32] = x;
+    warp_sums[lane] = z - w;
+    if (lane == 31) warp_sums[32] = z;
   }
   __syncthreads();
-  int r = warp_sums[warp] + pre;
+  const int r = warp_sums[warp] + x - v;
   *total = warp_sums[32];
   __syncthreads();
   return r;
 }
 
+// Keys staged in shared memory when they fit (up to 200 KB).
+constexpr int kTopkSmemKeys = 51200;
+
 // Radix select of the k-th largest key, then the ordered compaction of the
-// selected positions.  grid (HKV, B), 1024 threads.
+// selected positions.  grid (HKV, B), 1024 threads.  The keys are read once
+// into shared memory (when they fit); histogram updates are aggregated per
+// warp (the high bytes of similar scores fall into few bins); the
+// compaction takes 4 consecutive positions per thread per round.
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const uint32_t* __restrict__ keys,
                                                             int32_t pmax, int32_t P, int32_t k,
                                                             int32_t* __restrict__ idx_out) {
+  extern __shared__ uint32_t skeys[];
   __shared__ int hist[256];
   __shared__ int warp_sums[33];
   __shared__ uint32_t s_prefix;
   __shared__ int s_remaining;
   const int h = blockIdx.x, b = blockIdx.y, HKV = gridDim.x;
+  const int lane = threadIdx.x & 31;
   const size_t bh = (size_t)b * HKV + h;
-  const uint32_t* kk = keys + bh * pmax;
+  const uint32_t* gk = keys + bh * pmax;
+  const bool staged = P <= kTopkSmemKeys;
+  if (staged) {
+    for (int i = threadIdx.x; i < P; i += kTopkThreads) skeys[i] = gk[i];
+    __syncthreads();
+  }
+  const uint32_t* kk = staged ? skeys : gk;
   uint32_t prefix = 0, mask = 0;
   int remaining = k;  // how many still to take among keys matching the prefix
   for (int shift = 24; shift >= 0; shift -= 8) {
     for (int i = threadIdx.x; i < 256; i += kTopkThreads) hist[i] = 0;
     __syncthreads();
-    for (int j = threadIdx.x; j < P; j += kTopkThreads) {
-      uint32_t key = kk[j];
-      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1);
+    for (int j0 = 0; j0 < P; j0 += kTopkThreads) {  // uniform trip count for the warp vote
+      const int j = j0 + threadIdx.x;
+      const uint32_t key = j < P ? kk[j] : 0u;
+      const bool in = j < P && (key & mask) == prefix;
+      const int bin = in ? (int)((key >> shift) & 255u) : -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, bin);
+      if (in && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
     }
     __syncthreads();
     if (threadIdx.x < 32) {
       // Find the digit D (from the top) where the running count reaches `remaining`.
-      int lane = threadIdx.x;
       int above = 0, digit = -1, rem = remaining;
       for (int base = 255; base >= 0 && digit < 0; base -= 32) {
         int bin = base - lane;
@@ -180,17 +226,178 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const uint32_t* __re
   const uint32_t T = prefix;
   int eq_base = 0, out_base = 0, total;
   int32_t* out = idx_out + bh * k;
-  for (int j0 = 0; j0 < P; j0 += kTopkThreads) {
-    int j = j0 + threadIdx.x;
-    uint32_t key = j < P ? kk[j] : 0u;
-    int eq = (j < P) && key == T;
-    int eq_rank = block_scan_flag(eq, warp_sums, &total);
-    int take = (j < P) && (key > T || (eq && eq_base + eq_rank < remaining));
+  for (int j0 = 0; j0 < P; j0 += 4 * kTopkThreads) {
+    const int jb = j0 + 4 * threadIdx.x;
+    uint32_t kv[4];
+    bool eqf[4];
+    int neq = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int j = jb + e;
+      kv[e] = j < P ? kk[j] : 0u;
+      eqf[e] = j < P && kv[e] == T;
+      neq += eqf[e];
+    }
+    int eqr = eq_base + block_scan_count(neq, warp_sums, &total);
     eq_base += total;
-    int pos = block_scan_flag(take, warp_sums, &total);
-    if (take && out_base + pos < k) out[out_base + pos] = j;
+    bool tk[4];
+    int ntake = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      tk[e] = jb + e < P && (kv[e] > T || (eqf[e] && eqr < remaining));
+      eqr += eqf[e];
+      ntake += tk[e];
+    }
+    int o = out_base + block_scan_count(ntake, warp_sums, &total);
     out_base += total;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (tk[e]) {
+        if (o < k) out[o] = jb + e;
+        ++o;
+      }
   }
+}
+
+// Cluster top-k: kTopkCluster blocks share one (sequence, KV head).  Block r
+// holds positions [r * kTopkCtaThreads * KPT, ...) in registers, KPT
+// consecutive positions per thread.  Each radix pass builds a local
+// histogram; after a cluster barrier every block sums the kTopkCluster
+// histograms over distributed shared memory and finds the same digit.  The
+// selected positions are then written in position order: a key at global
+// order j goes to out[#{greater before j} + min(#{equal before j}, remaining)],
+// both counts from one packed block scan plus the counts of lower-ranked
+// blocks.
+constexpr int kTopkCluster = 8;
+constexpr int kTopkCtaThreads = 512;
+constexpr int kTopkCtaWarps = kTopkCtaThreads / 32;
+
+template <int KPT>
+__global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkCtaThreads)
+    topk_cluster_kernel(const uint32_t* __restrict__ keys, int32_t pmax, int32_t P, int32_t k,
+                        int32_t* __restrict__ idx_out) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cl = cg::this_cluster();
+  __shared__ int hist[4][256];
+  __shared__ int wsum[kTopkCtaWarps];
+  __shared__ int s_cnt[2];  // this block's (greater, equal) counts
+  __shared__ int s_base[2];
+  __shared__ uint32_t s_prefix;
+  __shared__ int s_remaining;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int rank = (int)cl.block_rank();
+  const size_t bh = (size_t)blockIdx.z * gridDim.y + blockIdx.y;
+  const uint32_t* gk = keys + bh * pmax;
+  const int32_t j0 = (rank * kTopkCtaThreads + tid) * KPT;
+  uint32_t kv[KPT];
+#pragma unroll
+  for (int e = 0; e < KPT; ++e) kv[e] = j0 + e < P ? __ldg(gk + j0 + e) : 0u;
+  for (int i = tid; i < 4 * 256; i += kTopkCtaThreads) (&hist[0][0])[i] = 0;
+  __syncthreads();
+  uint32_t prefix = 0, mask = 0;
+  int remaining = k;  // 1 <= remaining <= #keys matching prefix
+#pragma unroll 1
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+#pragma unroll
+    for (int e = 0; e < KPT; ++e) {
+      const bool in = j0 + e < P && (kv[e] & mask) == prefix;
+      if (__any_sync(0xffffffffu, in)) {
+        const int bin = in ? (int)((kv[e] >> shift) & 255u) : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, bin);
+        if (in && lane == __ffs(peers) - 1) atomicAdd(&hist[pass][bin], __popc(peers));
+      }
+    }
+    cl.sync();  // every block's histogram of this pass is complete
+    int tot = 0, x = 0;
+    if (tid < 256) {
+#pragma unroll
+      for (int c = 0; c < kTopkCluster; ++c) tot += cl.map_shared_rank(&hist[pass][0], c)[tid];
+      x = tot;  // suffix sum over this warp's bins >= tid
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_down_sync(0xffffffffu, x, o);
+        if (lane + o < 32) x += y;
+      }
+      if (lane == 0) wsum[warp] = x;
+    }
+    __syncthreads();
+    if (tid < 256) {
+      int S = x;  // #keys matching prefix with digit >= tid
+      for (int w = warp + 1; w < 8; ++w) S += wsum[w];
+      if (S >= remaining && S - tot < remaining) {
+        s_prefix = prefix | ((uint32_t)tid << shift);
+        s_remaining = remaining - (S - tot);
+      }
+    }
+    __syncthreads();
+    prefix = s_prefix;
+    remaining = s_remaining;
+    mask |= 255u << shift;
+  }
+  const uint32_t T = prefix;
+  int ngt = 0, neq = 0;
+#pragma unroll
+  for (int e = 0; e < KPT; ++e) {
+    const bool valid = j0 + e < P;
+    ngt += valid && kv[e] > T;
+    neq += valid && kv[e] == T;
+  }
+  // Packed exclusive scan of (greater << 16 | equal); a block holds at most
+  // kTopkCtaThreads * KPT <= 8192 keys, so neither half overflows.
+  const int v = (ngt << 16) | neq;
+  int xs = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, xs, o);
+    if (lane >= o) xs += y;
+  }
+  __shared__ int wscan[kTopkCtaWarps];
+  if (lane == 31) wscan[warp] = xs;
+  __syncthreads();
+  int excl = xs - v;
+  for (int w = 0; w < warp; ++w) excl += wscan[w];
+  if (tid == 0) {
+    int t = 0;
+    for (int w = 0; w < kTopkCtaWarps; ++w) t += wscan[w];
+    s_cnt[0] = t >> 16;
+    s_cnt[1] = t & 0xffff;
+  }
+  cl.sync();  // every block's counts are published
+  if (warp == 0) {
+    int g = 0, q = 0;
+    if (lane < rank) {
+      const int* rc = cl.map_shared_rank(s_cnt, lane);
+      g = rc[0];
+      q = rc[1];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      g += __shfl_xor_sync(0xffffffffu, g, o);
+      q += __shfl_xor_sync(0xffffffffu, q, o);
+    }
+    if (lane == 0) {
+      s_base[0] = g;
+      s_base[1] = q;
+    }
+  }
+  cl.barrier_arrive();  // this block reads no other block's shared memory after here
+  __syncthreads();
+  int gt_before = s_base[0] + (excl >> 16), eq_before = s_base[1] + (excl & 0xffff);
+  int32_t* out = idx_out + bh * k;
+#pragma unroll
+  for (int e = 0; e < KPT; ++e) {
+    if (j0 + e < P) {
+      if (kv[e] > T) {
+        out[gt_before + min(eq_before, remaining)] = j0 + e;
+        ++gt_before;
+      } else if (kv[e] == T) {
+        if (eq_before < remaining) out[gt_before + eq_before] = j0 + e;
+        ++eq_before;
+      }
+    }
+  }
+  cl.barrier_wait();  // no block leaves while another may still read its counts
 }
 
 }  // namespace
@@ -207,7 +414,7 @@ cudaError_t hyq_launch_select(const hyq_config* c, const void* q_proxy, int32_t 
   SelectWs w = carve(c, L, ws);
   const int32_t P = L - c->window;  // > 0 since k > 0
   const int32_t gq = c->num_q_heads / c->num_kv_heads;
-  proxy_sum_kernel<<<dim3(c->num_kv_heads, c->batch), HYQ_D, 0, s>>>(
+  proxy_sum_kernel<<<dim3(c->num_kv_heads, c->batch), kProxyThreads, 0, s>>>(
       static_cast<const __nv_bfloat16*>(q_proxy), n_proxy, n_proxy_ld, gq, w.u);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -216,6 +423,28 @@ cudaError_t hyq_launch_select(const hyq_config* c, const void* q_proxy, int32_t 
                                             w.keys, P, w.err);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  topk_kernel<<<dim3(c->num_kv_heads, c->batch), kTopkThreads, 0, s>>>(w.keys, P, P, k, idx_out);
+  const int32_t cap = kTopkCluster * kTopkCtaThreads;
+  dim3 gc(kTopkCluster, c->num_kv_heads, c->batch);
+  if (P <= 4 * cap) {
+    topk_cluster_kernel<4><<<gc, kTopkCtaThreads, 0, s>>>(w.keys, P, P, k, idx_out);
+    return cudaGetLastError();
+  }
+  if (P <= 8 * cap) {
+    topk_cluster_kernel<8><<<gc, kTopkCtaThreads, 0, s>>>(w.keys, P, P, k, idx_out);
+    return cudaGetLastError();
+  }
+  if (P <= 16 * cap) {
+    topk_cluster_kernel<16><<<gc, kTopkCtaThreads, 0, s>>>(w.keys, P, P, k, idx_out);
+    return cudaGetLastError();
+  }
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kTopkSmemKeys * (int)sizeof(uint32_t));
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  const size_t tk_smem = P <= kTopkSmemKeys ? (size_t)P * sizeof(uint32_t) : 0;
+  topk_kernel<<<dim3(c->num_kv_heads, c->batch), kTopkThreads, tk_smem, s>>>(w.keys, P, P, k, idx_out);
   return cudaGetLastError();
 }

@@ -100,3 +100,31 @@ def test_select_full_size_llama_32k(hyq):
     assert abs(hit(got) - hit(want)) <= 2.0 / c.sinks.shape[-1]
     assert hit(got) > 0.5
     print("ambiguous keys at the boundary:", amb, "planted keys chosen:", hit(got))
+
+
+@pytest.mark.parametrize("Lc", [40_000, 70_000])
+def test_select_long_prefixes(hyq, Lc):
+    """Prefixes past 32K keys (16 keys a thread in the cluster kernel) and
+    past 64K (the single-block radix select)."""
+    c = decode_case(23, 1, 4, 2, Lc, window=128, n_proxy=16, sink_frac=0.02)
+    got = run_select(c, Lc, 128, 50_000)
+    check(c, got, Lc, 128, 50_000)
+
+
+def test_select_ties_span_cluster_blocks(hyq):
+    """Equal scores spread over several blocks of the cluster: the lowest
+    positions among the ties are taken, after every strictly larger score.
+    Rows scaled by a power of two score exactly that multiple in any
+    precision, so no key is ambiguous and the sets must match exactly."""
+    Lc, W, ppm = 20_000, 128, 500_000
+    c = decode_case(24, 1, 4, 1, Lc, window=W, n_proxy=8)
+    P = prefix_len(Lc, W)
+    c.k[:, :, :P] = c.k[:, :, :1]
+    for p in (9000, 12000, 19000):
+        c.k[:, :, p] = 2 * c.k[:, :, 0]
+    for p in (3, 5000, 15000):
+        c.k[:, :, p] = 0.5 * c.k[:, :, 0]
+    got = run_select(c, Lc, W, ppm)
+    want, _ = select_vertical(c.q_proxy.double().numpy(), c.k.double().numpy(), Lc, W, ppm)
+    assert got.shape[-1] == vl_count(P, ppm) > 8192
+    np.testing.assert_array_equal(got, want)
