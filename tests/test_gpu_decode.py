@@ -22,6 +22,14 @@ pytestmark = pytest.mark.gpu
 
 
 def build_and_decode(c, Lc, W, ppm, capacity=None, len_hint=0, period=64):
+    got, idx_np, st = decode_gpu(c, Lc, W, ppm, capacity, len_hint, period)
+    k_np, v_np = c.k.double().numpy(), c.v.double().numpy()
+    want = hybrid_decode(c.q.double().numpy(), k_np, v_np, Lc, prefix_len(Lc, W), idx_np)
+    return got, want, st
+
+
+def decode_gpu(c, Lc, W, ppm, capacity=None, len_hint=0, period=64):
+    """Layout from the oracle's selection, then one GPU decode call."""
     B, HQ = c.q.shape[:2]
     HKV = c.k.shape[1]
     cfg = make_config(B, HQ, HKV, capacity=capacity or max(Lc, 1), window=W, rho_ppm=ppm, period=period)
@@ -38,8 +46,7 @@ def build_and_decode(c, Lc, W, ppm, capacity=None, len_hint=0, period=64):
     hyq_decode_attention(cfg, c.q.cuda(), layer.c, out, ws, len_hint)
     torch.cuda.synchronize()
     assert hyq_read_device_error(layer.err()) == 0
-    want = hybrid_decode(c.q.double().numpy(), k_np, v_np, Lc, prefix_len(Lc, W), idx_np)
-    return to_np(out), want, (cfg, layer, ws, out)
+    return to_np(out), idx_np, (cfg, layer, ws, out)
 
 
 @pytest.mark.parametrize("seed,B,HQ,HKV,Lc,W,ppm", [
@@ -120,6 +127,30 @@ def test_decode_full_size_llama_32k(hyq):
     cnt = layer.counts()[0].tolist()
     assert cnt[:4] == [32640 - 1632, 1632, 128, 32768]
     assert_attention_close(got, want, what="32K")
+
+
+@pytest.mark.parametrize("ppm,W,sink_frac",
+                         [(r, w, 0.02) for r in (20_000, 50_000, 100_000) for w in (64, 128, 256)]
+                         + [(50_000, 128, 0.01), (50_000, 128, 0.03)])
+def test_decode_qwen32b_shaped_sweep_sampled(hyq, ppm, W, sink_frac):
+    """Qwen3-32B-shaped decode: batch 4, 64/8 heads, 32K context, planted
+    sinks with heavy-tailed (Student-t, 3 degrees of freedom) magnitudes, over
+    the rho x W sweep.  The GPU computes every head; the oracle, which treats
+    each (sequence, KV head) on its own, checks three sampled pairs (24 query
+    heads) in full."""
+    B, HQ, HKV, Lc = 4, 64, 8, 32768
+    g = HQ // HKV
+    c = decode_case(1004, B, HQ, HKV, Lc, window=W, n_proxy=64, sink_frac=sink_frac, heavy_tail=True)
+    got, idx_np, (cfg, layer, _, _) = decode_gpu(c, Lc, W, ppm, capacity=Lc + 64)
+    P = prefix_len(Lc, W)
+    k = idx_np.shape[-1]
+    assert layer.counts()[0].tolist()[:4] == [P - k, k, Lc - P, Lc]
+    q, kk, vv = c.q.double().numpy(), c.k.double().numpy(), c.v.double().numpy()
+    for b, kh in ((0, 0), (1, 5), (3, 7)):
+        hs = slice(kh * g, (kh + 1) * g)
+        want = hybrid_decode(q[b:b + 1, hs], kk[b:b + 1, kh:kh + 1], vv[b:b + 1, kh:kh + 1], Lc, P,
+                             idx_np[b:b + 1, kh:kh + 1])
+        assert_attention_close(got[b:b + 1, hs], want, what=f"rho={ppm} W={W} b={b} kvh={kh}")
 
 
 def test_decode_pipeline_with_reselection(hyq):

@@ -128,3 +128,14 @@ def test_select_ties_span_cluster_blocks(hyq):
     want, _ = select_vertical(c.q_proxy.double().numpy(), c.k.double().numpy(), Lc, W, ppm)
     assert got.shape[-1] == vl_count(P, ppm) > 8192
     np.testing.assert_array_equal(got, want)
+
+
+@pytest.mark.parametrize("ppm", [20_000, 50_000, 100_000])
+@pytest.mark.parametrize("W", [64, 128, 256])
+def test_select_qwen32b_shaped_sweep(hyq, ppm, W):
+    """Qwen3-32B-shaped selection: batch 4, 64/8 heads, 32K context,
+    heavy-tailed planted sinks, every (rho, W) of the sweep, all 32 sets."""
+    Lc = 32768
+    c = decode_case(1004, 4, 64, 8, Lc, window=W, n_proxy=64, sink_frac=0.02, heavy_tail=True)
+    got = run_select(c, Lc, W, ppm)
+    check(c, got, Lc, W, ppm)
