@@ -23,14 +23,69 @@ constexpr int kChunks = HYQ_D / 8;      // 16 chunks of 8 elements per row
 struct BuildSmem {
   __nv_bfloat16 x[2][kRows][HYQ_D];  // K and V rows (zero for padding / kept rows)
   float mn[2][kRows][4], mx[2][kRows][4];
-  float s[2][kRows][4], z[2][kRows][4], r[2][kRows][4];
+  float z[2][kRows][4], r[2][kRows][4];
   int32_t pos[kRows];      // source row of each slot, -1 for none
   uint8_t keep[kRows];     // slot already holds a stream row (append)
   uint8_t nan[2][kRows][4];
+  uint8_t fast[2][kRows][4];  // every code of the group needs no clamp
 };
 
-__device__ __forceinline__ uint32_t code_of(float x, float s, float z, float r) {
-  if (s == 0.f) return 0u;
+// Packed float32 pairs (two lanes of one 64-bit register, low half first).
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_splat(float v) {
+  const uint64_t u = __float_as_uint(v);
+  return (u << 32) | u;
+}
+
+// Rounding by addition: for |t| < 2^22, fl32(t + 1.5 * 2^23) is
+// 1.5 * 2^23 + rint(t) (the sum's ulp is 1, ties to even), so its bit
+// pattern is kMagicBits + rint(t).
+constexpr float kMagic = 12582912.f;
+constexpr uint32_t kMagicBits = 0x4B400000u;
+__host__ __device__ constexpr uint32_t magic_sum8() {
+  uint32_t s = 0;
+  for (int p = 0; p < 8; ++p) s += kMagicBits << (4 * p);
+  return s;
+}
+constexpr uint32_t kMagicSum = magic_sum8();
+
+__device__ __forceinline__ uint32_t lo32(uint64_t v) { return (uint32_t)v; }
+__device__ __forceinline__ uint32_t hi32(uint64_t v) { return (uint32_t)(v >> 32); }
+
+// Bit patterns kMagicBits + code of the two BF16 elements of w (x: low half),
+// for a group whose (x - z) * r all lie in (-0.5, 15.5): there the clamp of
+// the code decision is the identity and the added magic rounds exactly as
+// rint does.  nz2 = (-z, -z), r2 = (r, r).  The magic add is a scalar
+// __fadd_rn, which is never contracted with the product into a fused
+// multiply-add (that would round the unrounded product).
+__device__ __forceinline__ uint2 code_bits2(uint32_t w, uint64_t nz2, uint64_t r2) {
+  const uint64_t x2 = (uint64_t)(w << 16) | ((uint64_t)(w & 0xffff0000u) << 32);
+  const uint64_t t2 = f2_mul(f2_add(x2, nz2), r2);
+  return make_uint2(__float_as_uint(__fadd_rn(__uint_as_float(lo32(t2)), kMagic)),
+                    __float_as_uint(__fadd_rn(__uint_as_float(hi32(t2)), kMagic)));
+}
+
+// Code word from b[p] = kMagicBits + code of nibble p: the shift-add chain
+// sums b[p] << 4p modulo 2^32, which is the word plus sum_p kMagicBits << 4p.
+__device__ __forceinline__ uint32_t pack_nibbles(const uint32_t (&b)[8]) {
+  uint32_t w = b[7];
+#pragma unroll
+  for (int p = 6; p >= 0; --p) w = (w << 4) + b[p];
+  return w - kMagicSum;
+}
+
+// r = 1 / s rounded, and 0 exactly when the step s is 0.
+__device__ __forceinline__ uint32_t code_of(float x, float z, float r) {
+  if (r == 0.f) return 0u;
   float t = rintf(__fmul_rn(__fsub_rn(x, z), r));
   t = fminf(fmaxf(t, 0.f), 15.f);
   return (uint32_t)t;
@@ -71,26 +126,21 @@ __device__ void build_block(BuildSmem& sm, const __nv_bfloat16* kbase, const __n
     const int T = f >> 10, row = (f >> 4) & (kRows - 1), c = f & (kChunks - 1);
     const uint4 v = vin[it];
     *reinterpret_cast<uint4*>(&sm.x[T][row][8 * c]) = v;
-    float e[8];
-    unpack8(v, e);
-    float mn = e[0], mx = e[0];
-    int nan = isnan(e[0]);
-#pragma unroll
-    for (int i = 1; i < 8; ++i) {
-      mn = fminf(mn, e[i]);
-      mx = fmaxf(mx, e[i]);
-      nan |= isnan(e[i]);
-    }
+    // BF16 pairs: min / max are exact in BF16, and the _nan forms carry a
+    // NaN through, so one test at the end finds any NaN of the group.
+    const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+    __nv_bfloat162 mn2 = __hmin2_nan(__hmin2_nan(p2[0], p2[1]), __hmin2_nan(p2[2], p2[3]));
+    __nv_bfloat162 mx2 = __hmax2_nan(__hmax2_nan(p2[0], p2[1]), __hmax2_nan(p2[2], p2[3]));
 #pragma unroll
     for (int o = 1; o < 4; o <<= 1) {
-      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      nan |= __shfl_xor_sync(0xffffffffu, nan, o);
+      mn2 = __hmin2_nan(mn2, __shfl_xor_sync(0xffffffffu, mn2, o));
+      mx2 = __hmax2_nan(mx2, __shfl_xor_sync(0xffffffffu, mx2, o));
     }
     if ((c & 3) == 0) {
-      sm.mn[T][row][c >> 2] = mn;
-      sm.mx[T][row][c >> 2] = mx;
-      sm.nan[T][row][c >> 2] = (uint8_t)nan;
+      const float2 fm = __bfloat1622float2(mn2), fx = __bfloat1622float2(mx2);
+      sm.mn[T][row][c >> 2] = fminf(fm.x, fm.y);
+      sm.mx[T][row][c >> 2] = fmaxf(fx.x, fx.y);
+      sm.nan[T][row][c >> 2] = (uint8_t)(isnan(fm.x) || isnan(fm.y));
     }
   }
   __syncthreads();
@@ -109,9 +159,13 @@ __device__ void build_block(BuildSmem& sm, const __nv_bfloat16* kbase, const __n
       sh = zh = __float2half_rn(0.f);
       s32 = z32 = 0.f;
     }
-    sm.s[T][row][q] = s32;
+    const float r32 = s32 > 0.f ? __frcp_rn(s32) : 0.f;
     sm.z[T][row][q] = z32;
-    sm.r[T][row][q] = s32 > 0.f ? __frcp_rn(s32) : 0.f;
+    sm.r[T][row][q] = r32;
+    // (x - z) * r is monotone in x, so the group's extremes bound every code
+    // argument; a NaN extreme fails the test.
+    const float tl = __fmul_rn(__fsub_rn(mn, z32), r32), th = __fmul_rn(__fsub_rn(mx, z32), r32);
+    sm.fast[T][row][q] = (uint8_t)(tl > -0.5f && th < 15.5f);
     const uint32_t w = (uint32_t)__half_as_ushort(sh) | ((uint32_t)__half_as_ushort(zh) << 16);
     *reinterpret_cast<uint32_t*>(dst + (row >> 4) * HYQ_QTILE_BYTES + 2048 + T * 256 + (row & 15) * 16 + 4 * q) = w;
   }
@@ -122,6 +176,36 @@ __device__ void build_block(BuildSmem& sm, const __nv_bfloat16* kbase, const __n
     const int tile = j >> 7, g = (j >> 4) & 7, cc = j & 15;
     const int q = cc >> 2, t = cc & 3;
     uint8_t* wp = dst + tile * HYQ_QTILE_BYTES + 512 * (cc >> 3) + 16 * (4 * g + t) + 4 * (2 * (q & 1));
+    const int rk0 = 16 * tile + g, rk1 = rk0 + 8;
+    if (!any_keep && sm.fast[0][rk0][q] && sm.fast[0][rk1][q]) {
+      // Row a, element 4 sub + 2 b + c -> nibble a + 2 b + 4 c of word sub.
+      uint2 pb[2][4];
+#pragma unroll
+      for (int a = 0; a < 2; ++a) {
+        const int row = a ? rk1 : rk0;
+        const uint4 xv = *reinterpret_cast<const uint4*>(&sm.x[0][row][8 * cc]);
+        const uint64_t nz2 = f2_splat(-sm.z[0][row][q]), r2 = f2_splat(sm.r[0][row][q]);
+        pb[a][0] = code_bits2(xv.x, nz2, r2);
+        pb[a][1] = code_bits2(xv.y, nz2, r2);
+        pb[a][2] = code_bits2(xv.z, nz2, r2);
+        pb[a][3] = code_bits2(xv.w, nz2, r2);
+      }
+      uint32_t wf[2];
+#pragma unroll
+      for (int sub = 0; sub < 2; ++sub) {
+        uint32_t bb[8];
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+          for (int b = 0; b < 2; ++b) {
+            bb[a + 2 * b] = pb[a][2 * sub + b].x;
+            bb[a + 2 * b + 4] = pb[a][2 * sub + b].y;
+          }
+        wf[sub] = pack_nibbles(bb);
+      }
+      *reinterpret_cast<uint2*>(wp) = make_uint2(wf[0], wf[1]);
+      continue;
+    }
     uint32_t w[2] = {0u, 0u};
     uint2 old = make_uint2(0, 0);
     if (any_keep) old = *reinterpret_cast<const uint2*>(wp);
@@ -136,14 +220,14 @@ __device__ void build_block(BuildSmem& sm, const __nv_bfloat16* kbase, const __n
       }
       float e[8];
       unpack8(*reinterpret_cast<const uint4*>(&sm.x[0][row][8 * cc]), e);
-      const float s = sm.s[0][row][q], z = sm.z[0][row][q], r = sm.r[0][row][q];
+      const float z = sm.z[0][row][q], r = sm.r[0][row][q];
 #pragma unroll
       for (int sub = 0; sub < 2; ++sub)
 #pragma unroll
         for (int b = 0; b < 2; ++b)
 #pragma unroll
           for (int c = 0; c < 2; ++c)
-            w[sub] |= code_of(e[4 * sub + 2 * b + c], s, z, r) << (4 * (a + 2 * b + 4 * c));
+            w[sub] |= code_of(e[4 * sub + 2 * b + c], z, r) << (4 * (a + 2 * b + 4 * c));
     }
     *reinterpret_cast<uint2*>(wp) = make_uint2(w[0], w[1]);
   }
@@ -154,6 +238,41 @@ __device__ void build_block(BuildSmem& sm, const __nv_bfloat16* kbase, const __n
   for (int j = tid; j < 4 * 4 * kChunks; j += kThreads) {
     const int tile = j >> 6, t = (j >> 4) & 3, cc = j & 15;
     const int q = cc >> 2;
+    const int rv = 16 * tile + 2 * t;  // rows rv + 8 b + c
+    if (!any_keep && sm.fast[1][rv][q] && sm.fast[1][rv + 1][q] && sm.fast[1][rv + 8][q] &&
+        sm.fast[1][rv + 9][q]) {
+      // Row (b, c), element 4 gl + 2 ss + a -> nibble a + 2 b + 4 c of word (gl, ss).
+      uint2 pb[4][4];
+#pragma unroll
+      for (int bc = 0; bc < 4; ++bc) {
+        const int row = rv + 8 * (bc & 1) + (bc >> 1);
+        const uint4 xv = *reinterpret_cast<const uint4*>(&sm.x[1][row][8 * cc]);
+        const uint64_t nz2 = f2_splat(-sm.z[1][row][q]), r2 = f2_splat(sm.r[1][row][q]);
+        pb[bc][0] = code_bits2(xv.x, nz2, r2);
+        pb[bc][1] = code_bits2(xv.y, nz2, r2);
+        pb[bc][2] = code_bits2(xv.z, nz2, r2);
+        pb[bc][3] = code_bits2(xv.w, nz2, r2);
+      }
+#pragma unroll
+      for (int gl = 0; gl < 2; ++gl) {
+        uint32_t wf[2];
+#pragma unroll
+        for (int ss = 0; ss < 2; ++ss) {
+          uint32_t bb[8];
+#pragma unroll
+          for (int bc = 0; bc < 4; ++bc) {  // b = bc & 1, c = bc >> 1: nibbles 2 b + 4 c + a
+            const int n0 = 2 * (bc & 1) + 4 * (bc >> 1);
+            bb[n0] = pb[bc][2 * gl + ss].x;
+            bb[n0 + 1] = pb[bc][2 * gl + ss].y;
+          }
+          wf[ss] = pack_nibbles(bb);
+        }
+        const int g = 2 * (cc & 3) + gl;
+        *reinterpret_cast<uint2*>(dst + tile * HYQ_QTILE_BYTES + 1024 + 512 * (cc >> 3) + 16 * (4 * g + t) +
+                                  8 * (q & 1)) = make_uint2(wf[0], wf[1]);
+      }
+      continue;
+    }
     uint8_t* wp[2];
     uint32_t w[2][2] = {{0u, 0u}, {0u, 0u}};
     uint2 old[2] = {make_uint2(0, 0), make_uint2(0, 0)};
@@ -179,14 +298,14 @@ __device__ void build_block(BuildSmem& sm, const __nv_bfloat16* kbase, const __n
         }
         float e[8];
         unpack8(*reinterpret_cast<const uint4*>(&sm.x[1][row][8 * cc]), e);
-        const float s = sm.s[1][row][q], z = sm.z[1][row][q], r = sm.r[1][row][q];
+        const float z = sm.z[1][row][q], r = sm.r[1][row][q];
 #pragma unroll
         for (int gl = 0; gl < 2; ++gl)
 #pragma unroll
           for (int ss = 0; ss < 2; ++ss)
 #pragma unroll
             for (int a = 0; a < 2; ++a)
-              w[gl][ss] |= code_of(e[4 * gl + 2 * ss + a], s, z, r) << (4 * (a + 2 * b + 4 * c));
+              w[gl][ss] |= code_of(e[4 * gl + 2 * ss + a], z, r) << (4 * (a + 2 * b + 4 * c));
       }
 #pragma unroll
     for (int gl = 0; gl < 2; ++gl) *reinterpret_cast<uint2*>(wp[gl]) = make_uint2(w[gl][0], w[gl][1]);

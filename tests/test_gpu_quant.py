@@ -123,3 +123,33 @@ def test_rebuild_flags_unsorted_index_list(hyq):
     hyq_rebuild(cfg, c.k.cuda(), c.v.cuda(), 400, idx, 3, layer.c)
     torch.cuda.synchronize()
     assert hyq_read_device_error(layer.err()) & L.DEVERR_INDEX
+
+
+def test_rebuild_bit_exact_on_edge_groups(hyq):
+    """Rebuild of rows with widely different group ranges, constant groups,
+    unit-grid ties, subnormal-size steps, and two planted groups whose code
+    argument (x - z) / s reaches exactly -0.5 and 15.5 (zero point rounded
+    off an FP16 subnormal), where the clamp of the code decision acts."""
+    B, HQ, HKV, Lc, W = 1, 2, 2, 400, 64
+    P = Lc - W
+    k_rows, v_rows = mixed_rows(8, (B, HKV, Lc, 128)), mixed_rows(9, (B, HKV, Lc, 128))
+    g = torch.Generator().manual_seed(10)
+    for x in (k_rows, v_rows):
+        x[0, :, 10, 0:32] = 1.5 * 2.0 ** -24       # z rounds up by half a step: argument -0.5
+        x[0, :, 10, 1] = 15.5 * 2.0 ** -24
+        x[0, :, 11, 96:128] = 2.5 * 2.0 ** -24     # z rounds down by half a step: argument 15.5
+        x[0, :, 11, 97] = 17.5 * 2.0 ** -24
+        x[0, :, 12:20, 32:64] = (1e-7 * torch.randn(2, 8, 32, generator=g)).to(torch.bfloat16)
+    idx_np = np.stack([np.arange(3, P, 13), np.arange(5, P, 13)])[None].astype(np.int64)
+    k = idx_np.shape[-1]   # 26 of 336: a 10% ratio leaves room for them
+    cfg = make_config(B, HQ, HKV, capacity=Lc + 64, window=W, rho_ppm=100_000)
+    layer = HybridLayer(cfg)
+    layer.reset()
+    idx = torch.from_numpy(idx_np).to(torch.int32).cuda().contiguous()
+    hyq_rebuild(cfg, k_rows.cuda(), v_rows.cuda(), Lc, idx, k, layer.c)
+    torch.cuda.synchronize()
+    assert hyq_read_device_error(layer.err()) == 0
+    for h in range(HKV):
+        qpos = np.setdiff1d(np.arange(P), idx_np[0, h])
+        _check_stream(layer, 0, h, len(qpos), k_rows[0, h, qpos].double().numpy(),
+                      v_rows[0, h, qpos].double().numpy())
