@@ -464,18 +464,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
   if (owner && warp == 2 && !ovl)
     nrow = __ldg(reinterpret_cast<const uint4*>((lane >= 16 ? sa.v_new : sa.k_new) + bh * HYQ_D) + (lane & 15));
   uint8_t* fstage = smem + kRingBytes + warp * kFTileBytes;
+  // A warp's ring and staging barriers are its own: lane 0 initialises them
+  // and the warp issues its first copies at once, behind the query copy
+  // issued at entry, so that the preparation of the query below overlaps
+  // their latency.
   if (lane == 0) {
     for (int i = 0; i < kSlots; ++i) mbar_init(&wb[i], 1);
     if (warp < n_staged) mbar_init(&fbars[warp], 1);
     mbar_fence_init();
   }
-  for (int i = gq * HYQ_D / 8 + tid; i < HYQ_MAX_GQA * HYQ_D / 8; i += kThreads)
-    reinterpret_cast<uint4*>(q_s)[i] = make_uint4(0, 0, 0, 0);  // query rows past g
-  __syncthreads();
-  // Without overlap nothing else is requested until the query has arrived:
-  // a flood of tile copies ahead of it would delay the start of all compute
-  // by the flood's service time.
-  if (!ovl && !mbar_wait(&qbar, 0) && tid == 0) hyq_set_err(lay.err, HYQ_DEVERR_TIMEOUT);
+  __syncwarp();
   if (warp < n_staged) {
     // The first kFStaged BF16 tiles of this block: the rows of a tile are
     // contiguous in the vertical-line buffer and in the tail, so a tile takes
@@ -508,6 +506,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
     bulk_g2s(ring + j * HYQ_QTILE_BYTES, tiles + (size_t)(t0 + my0 + kWarps * j) * HYQ_QTILE_BYTES,
              HYQ_QTILE_BYTES, &wb[j]);
   }
+  for (int i = gq * HYQ_D / 8 + tid; i < HYQ_MAX_GQA * HYQ_D / 8; i += kThreads)
+    reinterpret_cast<uint4*>(q_s)[i] = make_uint4(0, 0, 0, 0);  // query rows past g
+  __syncthreads();
+  if (!ovl && !mbar_wait(&qbar, 0) && tid == 0) hyq_set_err(lay.err, HYQ_DEVERR_TIMEOUT);
   if (ovl) {
     // The layout copies are in flight; now wait for the preceding kernel and
     // fetch what it may have produced.
@@ -529,11 +531,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
       reinterpret_cast<uint4*>(smem + kRingBytes + fw * kFTileBytes + (lane >= 16 ? 16 * kFKStride : 0) +
                                rin * kFKStride)[lane & 15] = nrow;
   }
-  if (tid < 32) {
-    float sacc = 0.f;
-    const __nv_bfloat16* r = q_s + (tid >> 2) * HYQ_D + 32 * (tid & 3);
-    for (int i = 0; i < 32; ++i) sacc += __bfloat162float(r[i]);
-    qsum_s[tid] = sacc;
+  if (tid < 256) {  // 8 threads per (query row, group of 32 elements)
+    const int e = tid >> 3;
+    const uint2 v = *reinterpret_cast<const uint2*>(q_s + (e >> 2) * HYQ_D + 32 * (e & 3) + 4 * (tid & 7));
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+    const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+    float sacc = (a.x + a.y) + (c.x + c.y);
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) sacc += __shfl_xor_sync(0xffffffffu, sacc, o);
+    if ((tid & 7) == 0) qsum_s[e] = sacc;
   }
   __syncthreads();
   // The query in fp16 for the 4-bit path, scaled by 2^e (exact) so that its
