@@ -16,12 +16,15 @@
 //     stored transposed (dims x keys) for the P.V product.
 //  2. prefill_kernel (stage 3): one CTA per (query block of 128 rows, query
 //     head).  Warps 8 and 9 stream key and value tiles (bulk copies, one
-//     2-stage ring each); warp 10 issues tcgen05.mma: S = Q K^T into TMEM (double buffer), then
+//     ring each); warp 10 issues tcgen05.mma: S = Q K^T into TMEM, then
 //     O_h += P_h V_h into TMEM for the two 64-key halves h of each tile;
 //     warps 0-7 (one thread per query row = TMEM lane and key half) read S,
-//     scale, mask, run an online softmax per half and write P as BF16 over
-//     the S columns they have read, where the P.V MMA takes its A operand
-//     from tensor memory; the two halves' (max, sum, O) merge once at the end.  The quantised segment uses e4m3 codes (kind::f8f6f4) or INT8
+//     scale, mask, run an online softmax per half and write P as BF16 into
+//     one of two TMEM buffers, where the P.V MMA takes its A operand; one
+//     barrier signals both halves' P of a tile and one commit their P.V, and
+//     the two halves' (max, sum, O) merge once at the end.  The MMA thread
+//     shares a scheduler with softmax warps, so its loop is kept to a few
+//     instructions.  The quantised segment uses e4m3 codes (kind::f8f6f4) or INT8
 //     codes held exactly as BF16 integers (kind::f16; sm_103a has no integer
 //     tensor-core MMA); the full-precision segment uses BF16.  P.V runs in
 //     BF16 with the value codes (exact in BF16) and the value scale folded
@@ -164,6 +167,34 @@ __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Packed float32 pairs (one 64-bit register, low half first).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  return (static_cast<uint64_t>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ uint64_t f2_splat(float v) { return f2_pack(v, v); }
+__device__ __forceinline__ float f2_lo(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+__device__ __forceinline__ float f2_hi(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 __device__ __forceinline__ float block_max(float v, float* red, int nwarps) {
@@ -348,8 +379,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   uint64_t* kempty = bars + 21; // [kKStages]
   uint64_t* sfull = bars + 5;   // S of the current tile is in TMEM
   uint64_t* sfree = bars + 6;   // every softmax thread has read it
-  uint64_t* pfull = bars + 7;   // [2], one per key half
-  uint64_t* pvdone = bars + 9;  // [2]
+  uint64_t* pfull = bars + 7;   // both key halves' P of a tile written
+  uint64_t* pvdone = bars + 9;  // that tile's P.V done (both halves)
   uint64_t* mmadone = bars + 11;
   uint64_t* vfull = bars + 12;  // [kVStages]
   uint64_t* vempty = bars + 15; // [kVStages]
@@ -380,10 +411,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       mbar_init(kfull + i, 1);
       mbar_init(kempty + i, 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(pfull + i, kSoft / 2);
-      mbar_init(pvdone + i, 1);
-    }
+    mbar_init(pfull, kSoft);
+    mbar_init(pvdone, 1);
     mbar_init(mmadone, 1);
     mbar_init(sfull, 1);
     mbar_init(sfree, kSoft);
@@ -534,28 +563,46 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #pragma unroll
       for (int u = 0; u < 8; ++u) a[u] = x[u];
 #pragma unroll
-      for (int i = 8; i < 64; ++i) a[i & 7] = fmaxf(a[i & 7], x[i]);
-      const float hmax = fmaxf(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])), fmaxf(fmaxf(a[4], a[5]), fmaxf(a[6], a[7])));
+      for (int i = 8; i < 64; i += 2) a[(i >> 1) & 7] = fmax3(a[(i >> 1) & 7], x[i], x[i + 1]);
+      const float hmax = fmax3(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
       const float tmax = hmax == -INFINITY ? -INFINITY : hmax * cs;
       // Lazy maximum: rescale only when the row maximum grew by more than 2^8.
       const bool grow = tmax > m_used + 8.f;
       const float m_new = grow ? tmax : m_used;
       const float fac = grow ? fast_exp2(m_used - m_new) : 1.f;
       const float mb = (m_new == -INFINITY) ? 0.f : m_new;
-      float ps[8];
+      float rs;
+      if (!masked) {
+        // Pairs: scale, shift and sum packed (fewer instructions on the
+        // softmax warps leaves more issue slots to the MMA warp beside them).
+        const uint64_t cs2 = f2_splat(cs), nmb2 = f2_splat(-mb);
+        uint64_t ps2[4] = {0, 0, 0, 0};
 #pragma unroll
-      for (int u = 0; u < 8; ++u) ps[u] = 0.f;
+        for (int w = 0; w < 32; ++w) {
+          uint64_t e2 = f2_fma(f2_pack(x[2 * w], x[2 * w + 1]), cs2, nmb2);
+          e2 = f2_pack(fast_exp2(f2_lo(e2)), fast_exp2(f2_hi(e2)));
+          ps2[w & 3] = f2_add(ps2[w & 3], e2);
+          x[2 * w] = f2_lo(e2);
+          x[2 * w + 1] = f2_hi(e2);
+        }
+        const uint64_t r2 = f2_add(f2_add(ps2[0], ps2[1]), f2_add(ps2[2], ps2[3]));
+        rs = f2_lo(r2) + f2_hi(r2);
+      } else {
+        float ps[8];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        x[i] = fast_exp2(fmaf(x[i], cs, -mb));
-        ps[i & 7] += x[i];
+        for (int u = 0; u < 8; ++u) ps[u] = 0.f;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          x[i] = fast_exp2(fmaf(x[i], cs, -mb));
+          ps[i & 7] += x[i];
+        }
+        rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       }
-      const float rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       l_sum = l_sum * fac + rs;
       m_used = m_new;
 
-      if (j > 0) {  // this half's P.V of the previous tile is done: O stable, P free
-        if (!mbar_wait_or_abort(pvdone + hf, (j - 1) & 1, abort_flag)) {
+      if (j > 0) {  // the previous tile's P.V is done: O stable, P buffer free
+        if (!mbar_wait_or_abort(pvdone, (j - 1) & 1, abort_flag)) {
           fail();
           ok = false;
           break;
@@ -578,21 +625,25 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         // P_h (BF16 pairs, the value scale folded in) into P buffer j % 2,
         // whose previous tile's P.V is done: the A operand of P.V.
         uint32_t pw[32];
+        const uint64_t vf2 = f2_splat(vf);
 #pragma unroll
-        for (int w = 0; w < 32; ++w) pw[w] = pack_bf16x2(x[2 * w] * vf, x[2 * w + 1] * vf);
+        for (int w = 0; w < 32; ++w) {
+          const uint64_t pv = f2_mul(f2_pack(x[2 * w], x[2 * w + 1]), vf2);
+          pw[w] = pack_bf16x2(f2_lo(pv), f2_hi(pv));
+        }
         tc_st32(tbase + lane_off + kColP + 64 * s + 32 * hf, pw);
         tc_wait_st();
       }
       tc_fence_before();
-      mbar_arrive(pfull + hf);
+      mbar_arrive(pfull);
     }
-    // Merge the two halves.  Each half waits for its own last P.V, leaves
+    // Merge the two halves.  Each half waits for the last P.V, leaves
     // (m, l) in its own region of key stage 0 (no copy or MMA touches it any
     // more: every MMA before that last P.V has finished), and the named barrier
     // makes both halves' accumulators and (m, l) visible to every thread;
     // each thread then writes dims 64hf .. 64hf+63 of its row.
     bool done = ok && nt > 0;
-    if (done && !mbar_wait_or_abort(pvdone + hf, (nt - 1) & 1, abort_flag)) {
+    if (done && !mbar_wait_or_abort(pvdone, (nt - 1) & 1, abort_flag)) {
       fail();
       done = false;
     }
@@ -638,9 +689,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   } else if (warp == kCopyWarp || warp == kCopyWarp + 1) {
     // ---------------- copy warps: keys (8) and values (9), each its own
     // ring, so that key tiles are not held back by value tiles.  A tile
-    // image goes as four quarter copies from lanes 0-3: the bulk copies one
-    // thread issues complete one after another, so four issuing lanes keep
-    // four in flight. ----------------------------------------------------
+    // image goes as four quarter copies from the four lanes of its stage:
+    // the bulk copies one thread issues complete one after another, so
+    // separate lanes per stage keep every stage's copies in flight. -------
     const bool is_v = warp != kCopyWarp;
     uint64_t* full = is_v ? vfull : kfull;
     uint64_t* empty = is_v ? vempty : kempty;
@@ -666,7 +717,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       const uint8_t* src = quant ? qsrc + (size_t)j * qimg : fsrc + (size_t)(j - nqt) * kImg16;
       if (lane == 0) mbar_arrive_expect_tx(full + s, bytes);
       __syncwarp();
-      if (lane < 4) bulk_g2s(dst + s * kImg16 + lane * part, src + lane * part, part, full + s);
+      // stage s is always filled by lanes 4s .. 4s+3, so the stages' copies
+      // are in flight together
+      const int qt = lane - 4 * s;
+      if (qt >= 0 && qt < 4) bulk_g2s(dst + s * kImg16 + qt * part, src + qt * part, part, full + s);
       last_j = j;
     }
     if (!ok && lane == 0) {
@@ -682,46 +736,64 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       const uint32_t aQ = smem_u32(sm + kOffQ), aQc = smem_u32(sm + kOffQc);
       bool ok = mbar_wait_or_abort(qready, 0, abort_flag);
       tc_fence_after();
+      // The MMA thread shares its scheduler with two softmax warps, so its
+      // own instructions are few: descriptors are built once and advanced by
+      // adding offsets (the start-address field counts 16-byte units), ring
+      // stages and phases are tracked incrementally.
+      const uint64_t dQc = tc_desc_sw128(aQc), dQ = tc_desc_sw128(aQ);
+      const uint64_t dK0 = tc_desc_sw128(smem_u32(sm + kOffK)), dV0 = tc_desc_sw128(smem_u32(sm + kOffV));
+      constexpr uint64_t kStageStep = kImg16 >> 4, kRegionStep = kRegion >> 4;
+      const uint32_t tS = tbase + kColS;
+      int sk = 0, sv = 0;
+      uint32_t kph = 0, vph = 0;
       for (int j = 0; ok && j <= nt; ++j) {
         if (j < nt) {
-          const int s = j & 1, sk = j % kKStages;
-          ok = mbar_wait_or_abort(kfull + sk, (j / kKStages) & 1, abort_flag);
+          ok = mbar_wait_or_abort(kfull + sk, kph, abort_flag);
           // the softmax has read S of the previous tile
           if (ok && j >= 1) ok = mbar_wait_or_abort(sfree, (j - 1) & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t aK = smem_u32(sm + kOffK + sk * kImg16);
+          const uint64_t dK = dK0 + sk * kStageStep;
           if (kFp8 && j < nqt) {
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              tc_mma_f8(tbase + kColS, tc_desc_sw128(aQc + 32 * ks), tc_desc_sw128(aK + 32 * ks), kIdescE4M3, ks > 0);
+            for (int ks = 0; ks < 4; ++ks) tc_mma_f8(tS, dQc + 2 * ks, dK + 2 * ks, kIdescE4M3, ks > 0);
           } else {
-            const uint32_t aA = j < nqt ? aQc : aQ;
+            const uint64_t dA = j < nqt ? dQc : dQ;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
-              const uint32_t off = (ks >> 2) * kRegion + (ks & 3) * 32;
-              tc_mma_f16(tbase + kColS, tc_desc_sw128(aA + off), tc_desc_sw128(aK + off), kIdescBF16, ks > 0);
+              const uint64_t off = (ks >> 2) * kRegionStep + (ks & 3) * 2;
+              tc_mma_f16(tS, dA + off, dK + off, kIdescBF16, ks > 0);
             }
           }
           tc_commit(sfull);
           tc_commit(kempty + sk);
+          if (++sk == kKStages) {
+            sk = 0;
+            kph ^= 1;
+          }
         }
         if (j >= 1) {  // O_h += P_h V_h for tile i = j - 1, one key half at a time
-          const int i = j - 1, s = i & 1, sv = i % kVStages;
-          ok = mbar_wait_or_abort(vfull + sv, (i / kVStages) & 1, abort_flag);
-          const uint32_t aV = smem_u32(sm + kOffV + sv * kImg16);
-          for (int hf = 0; ok && hf < 2; ++hf) {
-            ok = mbar_wait_or_abort(pfull + hf, i & 1, abort_flag);
-            if (!ok) break;
-            tc_fence_after();
+          const int i = j - 1;
+          const uint32_t tP = tbase + kColP + 64 * (i & 1);
+          ok = mbar_wait_or_abort(vfull + sv, vph, abort_flag);
+          const uint64_t dV = dV0 + sv * kStageStep;
+          if (ok) ok = mbar_wait_or_abort(pfull, i & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const uint32_t tO = tbase + (hf ? kColO1 : kColO0);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-              tc_mma_f16_ts(tbase + (hf ? kColO1 : kColO0), tbase + kColP + 64 * s + 32 * hf + 8 * ks,
-                            tc_desc_sw128(aV + hf * kRegion + ks * 32), kIdescBF16, (i > 0 || ks > 0) ? 1u : 0u);
-            tc_commit(pvdone + hf);
+              tc_mma_f16_ts(tO, tP + 32 * hf + 8 * ks, dV + hf * kRegionStep + 2 * ks, kIdescBF16,
+                            (i > 0 || ks > 0) ? 1u : 0u);
           }
-          if (!ok) break;
+          tc_commit(pvdone);
           tc_commit(vempty + sv);
+          if (++sv == kVStages) {
+            sv = 0;
+            vph ^= 1;
+          }
         }
       }
       if (!ok) {
