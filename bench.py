@@ -50,6 +50,9 @@ def parse():
     p.add_argument("--no-baseline", action="store_true", help="skip the CPU oracle timing")
     p.add_argument("--no-prefill", action="store_true", help="skip the prefill measurement")
     p.add_argument("--no-batched", action="store_true", help="skip the batch-16 decode measurement")
+    p.add_argument("--no-prefetch", dest="prefetch", action="store_false",
+                   help="plain fused decode steps; by default each step warms L2 with the next layer's share "
+                        "once its own reads are done (hyq_decode_step_prefetch)")
     p.add_argument("--overlap", action="store_true",
                    help="launch decode steps with programmatic dependent launch")
     p.add_argument("--case", default="period", choices=["period", "decode-layer", "prefill"],
@@ -486,7 +489,7 @@ def run_ours(args, rank, world, local):
     # overlap the one before it (programmatic dependent launch); measured
     # slower inside CUDA graphs on GB300, hence off unless asked for
     hyq.hyq_set_decode_overlap(args.overlap)
-    run = PeriodRunner(cfg, k_srcs, v_srcs, L0, dev)
+    run = PeriodRunner(cfg, k_srcs, v_srcs, L0, dev, prefetch_next=args.prefetch)
     run.q_tok.copy_(q_tok)
     run.k_tok.copy_(k_tok)
     run.v_tok.copy_(v_tok)
@@ -553,7 +556,7 @@ def run_ours(args, rank, world, local):
                                "rho 5%, K4V4 G32; 32 distinct layers; step = 64-token re-selection period",
                    "context": CTX, "layers": nl, "tokens_per_step": PERIOD,
                    "l2": "no flush: the 32 layers' caches (~1.6 GB) exceed L2 between reuses",
-                   "launch_overlap": args.overlap},
+                   "launch_overlap": args.overlap, "prefetch_next_layer": args.prefetch},
         "gpu_launches": run.launches_per_period * args.steps,
         "decode_kernel_us": dec_us,
         "us_per_token_all_layers": value * nl,

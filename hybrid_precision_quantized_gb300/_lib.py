@@ -38,7 +38,8 @@ SYMBOLS = ("hyq_status_string", "hyq_config_check", "hyq_vl_count", "hyq_layout_
            "hyq_workspace_size", "hyq_layout_reset", "hyq_quantize_append",
            "hyq_select_vertical", "hyq_rebuild", "hyq_decode_append", "hyq_decode_attention",
            "hyq_decode_attention_noalloc", "hyq_read_device_error", "hyq_set_decode_plan",
-           "hyq_prefill_attention", "hyq_decode_step", "hyq_set_decode_overlap")
+           "hyq_prefill_attention", "hyq_decode_step", "hyq_set_decode_overlap",
+           "hyq_decode_step_prefetch")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -98,6 +99,9 @@ def load() -> ctypes.CDLL:
         "hyq_set_decode_overlap": (c_int32, [c_int32]),
         "hyq_decode_step": (c_int32, [P(HyqConfig), c_void_p, c_void_p, c_void_p, P(HyqLayout), c_void_p,
                                       c_void_p, c_int32, c_void_p, c_int32, c_void_p, c_size_t, c_void_p]),
+        "hyq_decode_step_prefetch": (c_int32, [P(HyqConfig), c_void_p, c_void_p, c_void_p, P(HyqLayout),
+                                               P(HyqLayout), c_void_p, c_void_p, c_int32, c_void_p, c_int32,
+                                               c_void_p, c_size_t, c_void_p]),
         "hyq_prefill_attention": (c_int32, [P(HyqConfig), c_int32, c_void_p, c_int32, c_void_p, c_void_p,
                                             c_int32, c_int32, c_void_p, c_int32, c_void_p, c_void_p,
                                             c_void_p, c_size_t, c_void_p]),
@@ -207,6 +211,18 @@ def hyq_decode_step(cfg, q, k_new, v_new, lay: HyqLayout, out, ws, k_src=None, v
     ld = row_ld(k_src) if k_src is not None else 0
     _check("hyq_decode_step", load().hyq_decode_step(
         ctypes.byref(cfg), ptr(q), ptr(k_new), ptr(v_new), ctypes.byref(lay), ptr(k_src), ptr(v_src), ld,
+        ptr(out), len_hint, ptr(ws), ws.numel() * ws.element_size(), stream_ptr(stream)))
+
+
+def hyq_decode_step_prefetch(cfg, q, k_new, v_new, lay: HyqLayout, next_lay, out, ws, k_src=None, v_src=None,
+                             len_hint: int = 0, stream=None):
+    """hyq_decode_step that, once each block has read its share of ``lay``,
+    asks L2 to prefetch the share of ``next_lay`` (the layout of the next
+    decode call, or None for none) that the same block index will read."""
+    ld = row_ld(k_src) if k_src is not None else 0
+    _check("hyq_decode_step_prefetch", load().hyq_decode_step_prefetch(
+        ctypes.byref(cfg), ptr(q), ptr(k_new), ptr(v_new), ctypes.byref(lay),
+        ctypes.byref(next_lay) if next_lay is not None else None, ptr(k_src), ptr(v_src), ld,
         ptr(out), len_hint, ptr(ws), ws.numel() * ws.element_size(), stream_ptr(stream)))
 
 

@@ -198,6 +198,14 @@ extern "C" hyq_status hyq_decode_step(const hyq_config* c, const void* q, const 
                                       const void* v_new, const hyq_layout* l, void* k_src, void* v_src,
                                       int32_t ld, void* out, int32_t len_hint, void* ws, size_t ws_bytes,
                                       hyq_stream_t s) {
+  return hyq_decode_step_prefetch(c, q, k_new, v_new, l, nullptr, k_src, v_src, ld, out, len_hint, ws, ws_bytes,
+                                  s);
+}
+
+extern "C" hyq_status hyq_decode_step_prefetch(const hyq_config* c, const void* q, const void* k_new,
+                                               const void* v_new, const hyq_layout* l, const hyq_layout* next,
+                                               void* k_src, void* v_src, int32_t ld, void* out, int32_t len_hint,
+                                               void* ws, size_t ws_bytes, hyq_stream_t s) {
   hyq_status st = hyq_config_check(c);
   if (st != HYQ_OK) return st;
   if (!layout_ok(l) || !q || !k_new || !v_new || !out || len_hint < 0) return HYQ_ERR_INVALID_ARG;
@@ -206,8 +214,9 @@ extern "C" hyq_status hyq_decode_step(const hyq_config* c, const void* q, const 
   if ((k_src == nullptr) != (v_src == nullptr)) return HYQ_ERR_INVALID_ARG;
   if (k_src && (ld < 1 || !aligned(k_src, 16) || !aligned(v_src, 16))) return HYQ_ERR_INVALID_ARG;
   if (len_hint == 0 || len_hint > c->capacity) len_hint = c->capacity;
+  if (next && !layout_ok(next)) return HYQ_ERR_INVALID_ARG;
   if (!ws || !aligned(ws, kAlign) || ws_bytes < hyq_decode_ws_bytes(c, len_hint)) return HYQ_ERR_WORKSPACE;
-  return from_cuda(hyq_launch_decode(c, q, l, out, len_hint, ws, s, k_new, v_new, k_src, v_src, ld));
+  return from_cuda(hyq_launch_decode(c, q, l, out, len_hint, ws, s, k_new, v_new, k_src, v_src, ld, next));
 }
 
 extern "C" hyq_status hyq_prefill_attention(const hyq_config* c, int32_t dtype, const void* q,

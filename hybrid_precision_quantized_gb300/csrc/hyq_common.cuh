@@ -45,7 +45,8 @@ cudaError_t hyq_launch_decode_append(const hyq_config* c, const void* q, const v
 cudaError_t hyq_launch_decode(const hyq_config* c, const void* q, const hyq_layout* lay,
                               void* out, int32_t len_hint, void* ws, cudaStream_t s,
                               const void* k_new = nullptr, const void* v_new = nullptr,
-                              void* k_src = nullptr, void* v_src = nullptr, int32_t ld = 0);
+                              void* k_src = nullptr, void* v_src = nullptr, int32_t ld = 0,
+                              const hyq_layout* next = nullptr);
 size_t hyq_decode_ws_bytes(const hyq_config* c, int32_t len_hint);
 cudaError_t hyq_launch_prefill(const hyq_config* c, int dtype, const void* q, int64_t ldq, const void* k,
                                const void* v, int64_t ldk, int32_t L, const int32_t* vl, int32_t kvl, void* out,

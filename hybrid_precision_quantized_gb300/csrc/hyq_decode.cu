@@ -111,7 +111,64 @@ struct StepArgs {
   int32_t ld, period;
   int32_t* tickets_b;          // [B] per-sequence ticket of the counter update
   int32_t overlap;             // launched as a programmatic dependent (hyq_set_decode_overlap)
+  // Layout of the next decode call (hyq_decode_step_prefetch), or nullptr:
+  // once a block has read its share of this layer it asks L2 to prefetch the
+  // share of that layout the same block index will read.
+  const uint8_t* nx_qblocks;
+  const int32_t* nx_counts;
+  const __nv_bfloat16 *nx_vl_k, *nx_vl_v, *nx_tail_k, *nx_tail_v;
 };
+
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// The next layout's counts for sequence b, clamped to the capacities so that
+// every prefetched address lies in that layout's buffers.
+struct NextCounts {
+  int32_t nq, nvl, ntail;
+};
+__device__ __forceinline__ NextCounts next_counts(const StepArgs& sa, int b, int nblk_cap, int cap_vl,
+                                                  int cap_tail) {
+  const int32_t* cn = sa.nx_counts + (size_t)b * HYQ_COUNTS;
+  return NextCounts{min(max(cn[HYQ_CNT_NQ], 0), nblk_cap * HYQ_QBLOCK_ROWS), min(max(cn[HYQ_CNT_NVL], 0), cap_vl),
+                    min(max(cn[HYQ_CNT_NTAIL], 0), cap_tail)};
+}
+
+// One warp, once the block has read its share of this layer: prefetch into
+// L2 the next layout's 4-bit tiles [t0, t1) of KV head bh, the share of
+// block `split` under the same partition (contiguous, 16 KB per lane).
+__device__ void prefetch_next_tiles(const StepArgs& sa, const NextCounts& n, size_t bh, int split, int S,
+                                    int nblk_cap, int lane) {
+  const int nt = (n.nq + 15) >> 4;
+  const int t0 = (int)((int64_t)split * nt / S), t1 = (int)((int64_t)(split + 1) * nt / S);
+  const uint8_t* tiles = sa.nx_qblocks + bh * (size_t)nblk_cap * HYQ_QBLOCK_BYTES + (size_t)t0 * HYQ_QTILE_BYTES;
+  const uint32_t bytes = (uint32_t)(t1 - t0) * HYQ_QTILE_BYTES;
+  constexpr uint32_t kChunk = 16384;
+  for (uint32_t off = lane * kChunk; off < bytes; off += 32 * kChunk)
+    prefetch_l2(tiles + off, min(kChunk, bytes - off));
+}
+
+// One warp: prefetch into L2 the next layout's BF16 rows [16 f0, 16 f1)
+// (vertical lines, then tail) of KV head bh, the share of block `split`.
+__device__ void prefetch_next_rows(const StepArgs& sa, const NextCounts& n, size_t bh, int split, int S,
+                                   int cap_vl, int cap_tail, int lane) {
+  const int32_t nvl = n.nvl, ntail = n.ntail;
+  const int nft = (nvl + ntail + 15) >> 4;
+  if (lane < 4) {
+    const int f0 = (int)((int64_t)split * nft / S), f1 = (int)((int64_t)(split + 1) * nft / S);
+    const int r0 = 16 * f0, r1 = min(16 * f1, nvl + ntail);
+    const bool vpart = lane & 1;
+    if (lane < 2 && min(r1, nvl) > r0) {  // vertical-line rows
+      const __nv_bfloat16* base = (vpart ? sa.nx_vl_v : sa.nx_vl_k) + (bh * cap_vl + r0) * HYQ_D;
+      prefetch_l2(base, (uint32_t)(min(r1, nvl) - r0) * HYQ_D * 2);
+    } else if (lane >= 2 && r1 > max(r0, nvl)) {  // tail rows
+      const int a = max(r0, nvl) - nvl;
+      const __nv_bfloat16* base = (vpart ? sa.nx_tail_v : sa.nx_tail_k) + (bh * cap_tail + a) * HYQ_D;
+      prefetch_l2(base, (uint32_t)(r1 - nvl - a) * HYQ_D * 2);
+    }
+  }
+}
 
 // The fused step's counter update: one ticket per (sequence, KV head), taken
 // by the block that finishes that pair; the last of the sequence's KV heads
@@ -642,6 +699,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
       for (int o = 4; o < 32; o <<= 1) st.zacc[j][qq] += __shfl_xor_sync(0xffffffffu, st.zacc[j][qq], o);
   }
   __syncthreads();  // every warp is done with its ring: reuse shared memory
+  if (sa.nx_counts && warp == kWarps - 1) {
+    const NextCounts nxc = next_counts(sa, b, nblk_cap, cap_vl, cap_tail);
+    prefetch_next_tiles(sa, nxc, bh, split, S, nblk_cap, lane);
+    prefetch_next_rows(sa, nxc, bh, split, S, cap_vl, cap_tail, lane);
+  }
   float* red = reinterpret_cast<float*>(smem);                    // [warp][head][128]
   float* blk = red + kWarps * HYQ_MAX_GQA * HYQ_D;                  // [head][2 + 128]
   // Accumulator (m-tile u, ci) of thread (g, t): element 32(u/2) + 4g + 2(u%2)
@@ -950,7 +1012,7 @@ extern "C" hyq_status hyq_set_decode_plan(int32_t merge, int32_t splits) {
 
 cudaError_t hyq_launch_decode(const hyq_config* c, const void* q, const hyq_layout* lay, void* out,
                               int32_t len_hint, void* ws, cudaStream_t s, const void* k_new, const void* v_new,
-                              void* k_src, void* v_src, int32_t ld) {
+                              void* k_src, void* v_src, int32_t ld, const hyq_layout* next) {
   cudaError_t e = set_attrs<kDirect>();
   if (e == cudaSuccess) e = set_attrs<kCluster>();
   if (e == cudaSuccess) e = set_attrs<kGlobal>();
@@ -959,9 +1021,20 @@ cudaError_t hyq_launch_decode(const hyq_config* c, const void* q, const hyq_layo
   if (p.mode == kCluster && !cluster_fits(p.S)) p.mode = kGlobal;  // same S, workspace merge
   size_t bh = (size_t)c->batch * c->num_kv_heads;
   int32_t* tickets = static_cast<int32_t*>(ws);
-  StepArgs sa{static_cast<const __nv_bfloat16*>(k_new), static_cast<const __nv_bfloat16*>(v_new),
-              static_cast<__nv_bfloat16*>(k_src), static_cast<__nv_bfloat16*>(v_src), ld, c->period,
-              reinterpret_cast<int32_t*>(static_cast<char*>(ws) + round_up(bh * 4)), g_overlap};
+  StepArgs sa{static_cast<const __nv_bfloat16*>(k_new),
+              static_cast<const __nv_bfloat16*>(v_new),
+              static_cast<__nv_bfloat16*>(k_src),
+              static_cast<__nv_bfloat16*>(v_src),
+              ld,
+              c->period,
+              reinterpret_cast<int32_t*>(static_cast<char*>(ws) + round_up(bh * 4)),
+              g_overlap,
+              next ? next->qblocks : nullptr,
+              next ? next->counts : nullptr,
+              next ? static_cast<const __nv_bfloat16*>(next->vl_k) : nullptr,
+              next ? static_cast<const __nv_bfloat16*>(next->vl_v) : nullptr,
+              next ? static_cast<const __nv_bfloat16*>(next->tail_k) : nullptr,
+              next ? static_cast<const __nv_bfloat16*>(next->tail_v) : nullptr};
   float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + round_up(bh * 4) + round_up((size_t)c->batch * 4));
   const int gq = c->num_q_heads / c->num_kv_heads;
   cudaLaunchConfig_t cfg = {};

@@ -3,7 +3,9 @@ layers, captured as CUDA graphs so that host overhead does not gate the
 kernels.
 
 For every token t of the period but the last, one graph holds the fused
-decode step (append + attention, hyq_decode_step) of every layer.  At the
+decode step (append + attention, hyq_decode_step) of every layer; with
+``prefetch_next`` each step also warms L2 with the next layer's share
+(hyq_decode_step_prefetch; the layer after the last is the first).  At the
 last token two graphs are captured: the appends of all layers with the
 re-selection and rebuild of every layer, then the decode attention of all
 layers (maintenance sits between the append and the attention).  A reset graph restores the
@@ -27,8 +29,9 @@ class PeriodRunner:
     k_tok / v_tok   : [period, n_layers, B, HKV, 128] bf16
     """
 
-    def __init__(self, cfg, k_srcs, v_srcs, L0: int, device="cuda"):
+    def __init__(self, cfg, k_srcs, v_srcs, L0: int, device="cuda", prefetch_next: bool = False):
         self.cfg = cfg
+        self.prefetch_next = prefetch_next
         self.n_layers = len(k_srcs)
         self.k_srcs, self.v_srcs = k_srcs, v_srcs
         self.L0 = L0
@@ -85,8 +88,14 @@ class PeriodRunner:
 
     def _steps(self, t):
         for li, lay in enumerate(self.layers):
-            L.hyq_decode_step(self.cfg, self.q_tok[t, li], self.k_tok[t, li], self.v_tok[t, li], lay.c,
-                              self.out[t, li], self.ws_dec, self.k_srcs[li], self.v_srcs[li], self.L_end)
+            if self.prefetch_next:
+                nxt = self.layers[(li + 1) % self.n_layers].c
+                L.hyq_decode_step_prefetch(self.cfg, self.q_tok[t, li], self.k_tok[t, li], self.v_tok[t, li],
+                                           lay.c, nxt, self.out[t, li], self.ws_dec, self.k_srcs[li],
+                                           self.v_srcs[li], self.L_end)
+            else:
+                L.hyq_decode_step(self.cfg, self.q_tok[t, li], self.k_tok[t, li], self.v_tok[t, li], lay.c,
+                                  self.out[t, li], self.ws_dec, self.k_srcs[li], self.v_srcs[li], self.L_end)
         return self.n_layers
 
     def _fused(self, t):

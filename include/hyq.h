@@ -305,6 +305,30 @@ hyq_status hyq_decode_step(const hyq_config *cfg, const void *q, const void *k_n
                            hyq_stream_t stream);
 
 /*
+ * hyq_decode_step that also warms L2 for the next decode call on the stream.
+ * The paper has no counterpart: it overlaps the HBM reads of the next layer
+ * with the end of this launch (the block reduction and split merge, when
+ * most SMs and most of the HBM bandwidth are idle).
+ *
+ * Same arguments, result and layout updates as hyq_decode_step, plus
+ *   next  the layout the next decode call will read (typically the next
+ *         layer's), allocated for the same cfg; or NULL (no prefetch, the
+ *         same launch as hyq_decode_step); may equal lay.
+ * Once each block has read its share of lay, it issues L2 prefetches (bulk
+ * prefetch hints, no data is written) for the share of next that the same
+ * block index of a decode call with the same cfg and len_hint reads: its
+ * 4-bit tiles and its vertical-line and tail rows, from next's counters at
+ * the time (clamped to the capacities of cfg, so every address is inside
+ * next's buffers).  Results never depend on next; a stale or concurrently
+ * updated next only makes the hint less useful.  Errors as hyq_decode_step,
+ * and HYQ_ERR_INVALID_ARG when next is non-NULL with a NULL buffer.
+ */
+hyq_status hyq_decode_step_prefetch(const hyq_config *cfg, const void *q, const void *k_new,
+                                    const void *v_new, const hyq_layout *lay, const hyq_layout *next,
+                                    void *k_src, void *v_src, int32_t ld, void *out, int32_t len_hint,
+                                    void *ws, size_t ws_bytes, hyq_stream_t stream);
+
+/*
  * Let hyq_decode_attention and hyq_decode_step launches overlap the kernel
  * launched before them on the same stream (programmatic dependent launch;
  * process-wide, off by default).  With it on, every such launch lets the next

@@ -360,3 +360,51 @@ def test_decode_overlap_across_layers(hyq, fused):
         got, cgot = run(True, graph)
         assert torch.equal(got, ref), f"overlap changed the result (graph={graph})"
         assert all(torch.equal(a, b) for a, b in zip(cgot, cref))
+
+
+@pytest.mark.parametrize("plan", [(0, 0), (1, 0), (3, 7)])
+def test_decode_step_prefetch_changes_nothing(hyq, plan):
+    """hyq_decode_step_prefetch (L2 prefetch of the next call's share) gives the
+    same bits, counters, tail and proxy ring as hyq_decode_step, with the next
+    layout another layer, the same layer, or none."""
+    from hybrid_precision_quantized_gb300 import hyq_decode_step, hyq_decode_step_prefetch, hyq_set_decode_plan
+    L0, W, ppm, steps = 1500, 128, 50_000, 3
+    cap = L0 + steps
+    cases = [decode_case(91 + i, 1, 8, 2, cap, window=W, n_proxy=16, sink_frac=0.02) for i in range(2)]
+    g = gen_for(91, "q-steps")
+    qs = torch.randn(steps, 2, 1, 8, 128, generator=g).to(torch.bfloat16).cuda()
+    kn = [[c.k[:, :, L0 + s].contiguous().cuda() for s in range(steps)] for c in cases]
+    vn = [[c.v[:, :, L0 + s].contiguous().cuda() for s in range(steps)] for c in cases]
+
+    def run(mode):
+        hyq_set_decode_plan(*plan)
+        try:
+            layers, cfg = [], None
+            for c in cases:
+                cfg, (la, _), _ = _two_layers(c, L0, W, ppm, cap)
+                layers.append(la)
+            ws = workspace(cfg, L.OP_DECODE, cap)
+            outs = torch.zeros(steps, 2, 1, 8, 128, dtype=torch.bfloat16, device="cuda")
+            for s in range(steps):
+                for i in range(2):
+                    lay = layers[i].c
+                    if mode == "plain":
+                        hyq_decode_step(cfg, qs[s, i], kn[i][s], vn[i][s], lay, outs[s, i], ws, None, None, cap)
+                    else:
+                        nxt = {"other": layers[1 - i].c, "self": lay, "none": None}[mode]
+                        hyq_decode_step_prefetch(cfg, qs[s, i], kn[i][s], vn[i][s], lay, nxt, outs[s, i], ws,
+                                                 None, None, cap)
+            torch.cuda.synchronize()
+        finally:
+            hyq_set_decode_plan(0, 0)
+        for la in layers:
+            assert hyq_read_device_error(la.err()) == 0
+        return (outs.cpu(), [la.counts().cpu() for la in layers], [la.tail_k().cpu() for la in layers],
+                [la.q_ring().cpu() for la in layers])
+
+    ref = run("plain")
+    for mode in ("other", "self", "none"):
+        got = run(mode)
+        assert torch.equal(got[0], ref[0]), mode
+        for a, b in zip(got[1:], ref[1:]):
+            assert all(torch.equal(x, y) for x, y in zip(a, b)), mode
