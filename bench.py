@@ -50,6 +50,7 @@ def parse():
     p.add_argument("--no-baseline", action="store_true", help="skip the CPU oracle timing")
     p.add_argument("--no-prefill", action="store_true", help="skip the prefill measurement")
     p.add_argument("--no-batched", action="store_true", help="skip the batch-16 decode measurement")
+    p.add_argument("--no-frozen", action="store_true", help="skip the frozen-mode period measurement")
     p.add_argument("--no-prefetch", dest="prefetch", action="store_false",
                    help="plain fused decode steps; by default each step warms L2 with the next layer's share "
                         "once its own reads are done (hyq_decode_step_prefetch)")
@@ -537,6 +538,35 @@ def run_ours(args, rank, world, local):
     h2d = q_h.numel() * 2 + k_h.numel() * 2 + v_h.numel() * 2
     d2h = o_h.numel() * 2
 
+    # frozen mode (Algorithm 4 as written): the same period with the last
+    # token's maintenance done by hyq_age_tail instead of re-selection
+    frozen = None
+    main_launches = run.launches_per_period
+    if not args.no_frozen:
+        del run
+        fr = PeriodRunner(cfg, k_srcs, v_srcs, L0, dev, prefetch_next=args.prefetch, mode="frozen")
+        fr.q_tok.copy_(q_tok)
+        fr.k_tok.copy_(k_tok)
+        fr.v_tok.copy_(v_tok)
+        fr.freeze(q_tail)
+        fr.capture()
+        for _ in range(args.warmup):
+            fr.run_period()
+        torch.cuda.synchronize()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record()
+        for _ in range(args.steps):
+            fr.run_period()
+        f1.record()
+        torch.cuda.synchronize()
+        fms = reduce_timing(f0.elapsed_time(f1), world, dev)
+        frozen = {"maintenance": "hyq_age_tail: tail rows older than the window quantised onto the 4-bit stream; "
+                                 "vertical lines fixed at freeze",
+                  "value": job_value(fms, args.steps, PERIOD * nl, world), "unit": "us/token/layer",
+                  "ms_per_step": fms / args.steps, "launches_per_period": fr.launches_per_period,
+                  "device_error_word": max(hyq.hyq_read_device_error(l.err()) for l in fr.layers)}
+        del fr
+
     if rank != 0:
         return
     n_dec = args.steps * PERIOD * nl
@@ -557,7 +587,7 @@ def run_ours(args, rank, world, local):
                    "context": CTX, "layers": nl, "tokens_per_step": PERIOD,
                    "l2": "no flush: the 32 layers' caches (~1.6 GB) exceed L2 between reuses",
                    "launch_overlap": args.overlap, "prefetch_next_layer": args.prefetch},
-        "gpu_launches": run.launches_per_period * args.steps,
+        "gpu_launches": main_launches * args.steps,
         "decode_kernel_us": dec_us,
         "us_per_token_all_layers": value * nl,
         "device_error_word": err,
@@ -570,6 +600,7 @@ def run_ours(args, rank, world, local):
         "clocks": clk.summary(),
         "cpu_baseline": base,
         "batched": batched,
+        "frozen": frozen,
         "prefill": ({"workload": "llama3.1-8b-shaped causal prefill, B1, 32/8 heads, d128, 32K, W128, rho 5% "
                                  "(hyq_prefill_attention: pack + main kernel)",
                      "flops": "4 d HQ L(L+1)/2", "l2": "256 MB flush before every timed call",

@@ -6,7 +6,8 @@ streams.  Build the library with ``__graft_entry__.build()``.
 """
 from . import _lib
 from ._lib import (HyqConfig, HyqError, HyqLayout, load, lib_path, hyq_config_check,
-                   hyq_decode_append, hyq_decode_attention, hyq_decode_step, hyq_decode_step_prefetch,
+                   hyq_age_tail, hyq_decode_append, hyq_decode_attention, hyq_decode_step,
+                   hyq_decode_step_prefetch,
                    hyq_decode_attention_noalloc, hyq_layout_reset, hyq_layout_sizes, hyq_prefill_attention,
                    hyq_quantize_append, hyq_read_device_error, hyq_rebuild, hyq_select_vertical,
                    hyq_set_decode_plan, hyq_set_decode_overlap,

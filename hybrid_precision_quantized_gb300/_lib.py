@@ -39,7 +39,7 @@ SYMBOLS = ("hyq_status_string", "hyq_config_check", "hyq_vl_count", "hyq_layout_
            "hyq_select_vertical", "hyq_rebuild", "hyq_decode_append", "hyq_decode_attention",
            "hyq_decode_attention_noalloc", "hyq_read_device_error", "hyq_set_decode_plan",
            "hyq_prefill_attention", "hyq_decode_step", "hyq_set_decode_overlap",
-           "hyq_decode_step_prefetch")
+           "hyq_decode_step_prefetch", "hyq_age_tail")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -96,6 +96,7 @@ def load() -> ctypes.CDLL:
                                                    c_void_p]),
         "hyq_read_device_error": (c_int32, [c_void_p, P(c_int32), c_void_p]),
         "hyq_set_decode_plan": (c_int32, [c_int32, c_int32]),
+        "hyq_age_tail": (c_int32, [P(HyqConfig), P(HyqLayout), c_void_p]),
         "hyq_set_decode_overlap": (c_int32, [c_int32]),
         "hyq_decode_step": (c_int32, [P(HyqConfig), c_void_p, c_void_p, c_void_p, P(HyqLayout), c_void_p,
                                       c_void_p, c_int32, c_void_p, c_int32, c_void_p, c_size_t, c_void_p]),
@@ -212,6 +213,12 @@ def hyq_decode_step(cfg, q, k_new, v_new, lay: HyqLayout, out, ws, k_src=None, v
     _check("hyq_decode_step", load().hyq_decode_step(
         ctypes.byref(cfg), ptr(q), ptr(k_new), ptr(v_new), ctypes.byref(lay), ptr(k_src), ptr(v_src), ld,
         ptr(out), len_hint, ptr(ws), ws.numel() * ws.element_size(), stream_ptr(stream)))
+
+
+def hyq_age_tail(cfg, lay: HyqLayout, stream=None):
+    """Frozen-mode maintenance: the tail rows older than the window go to the
+    4-bit stream (quantised as by hyq_quantize_append), the last W stay."""
+    _check("hyq_age_tail", load().hyq_age_tail(ctypes.byref(cfg), ctypes.byref(lay), stream_ptr(stream)))
 
 
 def hyq_decode_step_prefetch(cfg, q, k_new, v_new, lay: HyqLayout, next_lay, out, ws, k_src=None, v_src=None,

@@ -131,6 +131,13 @@ extern "C" hyq_status hyq_quantize_append(const hyq_config* c, const void* k_row
   return from_cuda(hyq_launch_quantize_append(c, k_rows, v_rows, n_rows, l, s));
 }
 
+extern "C" hyq_status hyq_age_tail(const hyq_config* c, const hyq_layout* l, hyq_stream_t s) {
+  hyq_status st = hyq_config_check(c);
+  if (st != HYQ_OK) return st;
+  if (!layout_ok(l)) return HYQ_ERR_INVALID_ARG;
+  return from_cuda(hyq_launch_age_tail(c, l, s));
+}
+
 extern "C" hyq_status hyq_select_vertical(const hyq_config* c, const void* q_proxy,
                                           int32_t n_proxy, int32_t n_proxy_ld, const void* k_src,
                                           int32_t ld, int32_t L, int32_t* idx_out, int32_t* k_out,

@@ -29,6 +29,7 @@ inline int32_t hyq_vl_stride(const hyq_config* c) { return hyq_cap_vl(c) > 0 ? h
 inline int32_t hyq_nblk(const hyq_config* c) { return (c->capacity + HYQ_QBLOCK_ROWS - 1) / HYQ_QBLOCK_ROWS; }
 
 // Kernel launchers (return the launch's cudaError_t).
+cudaError_t hyq_launch_age_tail(const hyq_config* c, const hyq_layout* lay, cudaStream_t s);
 cudaError_t hyq_launch_quantize_append(const hyq_config* c, const void* k, const void* v,
                                        int32_t n_rows, const hyq_layout* lay, cudaStream_t s);
 cudaError_t hyq_launch_rebuild(const hyq_config* c, const void* k_src, const void* v_src,

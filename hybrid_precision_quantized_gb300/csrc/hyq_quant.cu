@@ -442,6 +442,22 @@ __global__ void __launch_bounds__(kThreads) rebuild_gather_kernel(
   }
 }
 
+// Block blockIdx.x of appending rows [0, end - nq0) of kbase / vbase (row r
+// at kbase + r * 128) to the 4-bit stream of (b, h) after its nq0 rows.
+__device__ void append_body(BuildSmem& sm, const __nv_bfloat16* kbase, const __nv_bfloat16* vbase, int32_t nq0,
+                            int32_t end, size_t bh, const hyq_layout& lay, int32_t nblk_cap) {
+  const int32_t bi = nq0 / kRows + blockIdx.x;
+  if (max(bi * kRows, nq0) >= min((bi + 1) * kRows, end)) return;  // uniform across the block
+  if (threadIdx.x < kRows) {
+    const int32_t row = bi * kRows + threadIdx.x;
+    sm.keep[threadIdx.x] = row < nq0;
+    sm.pos[threadIdx.x] = (row >= nq0 && row < end) ? row - nq0 : -1;
+  }
+  __syncthreads();
+  build_block(sm, kbase, vbase, lay.qblocks + (bh * nblk_cap + bi) * (size_t)HYQ_QBLOCK_BYTES, bi * kRows < nq0,
+              lay.err);
+}
+
 // Append n rows per (b, h) after the current NQ rows.  grid (blocks touched, HKV, B)
 __global__ void __launch_bounds__(kThreads) append_blocks_kernel(
     const __nv_bfloat16* __restrict__ k_rows, const __nv_bfloat16* __restrict__ v_rows, int32_t n,
@@ -458,16 +474,80 @@ __global__ void __launch_bounds__(kThreads) append_blocks_kernel(
   const int32_t end = min(nq0 + n, cap_rows);
   if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0 && nq0 + n > cap_rows)
     hyq_set_err(lay.err, HYQ_DEVERR_COUNT);
-  const int32_t bi = nq0 / kRows + blockIdx.x;
-  if (max(bi * kRows, nq0) >= min((bi + 1) * kRows, end)) return;  // uniform across the block
-  if (threadIdx.x < kRows) {
-    const int32_t row = bi * kRows + threadIdx.x;
-    sm.keep[threadIdx.x] = row < nq0;
-    sm.pos[threadIdx.x] = (row >= nq0 && row < end) ? row - nq0 : -1;
+  append_body(sm, k_rows + bh * n * HYQ_D, v_rows + bh * n * HYQ_D, nq0, end, bh, lay, nblk_cap);
+}
+
+// Rows the tail of sequence b gives up in hyq_age_tail: max(0, NTAIL - W),
+// or 0 (and the layout left unchanged) when the counters are out of range or
+// the stream has no room for them.
+__device__ __forceinline__ int32_t age_rows(const hyq_layout& lay, int b, int32_t window, int32_t cap_rows,
+                                            int32_t cap_tail) {
+  const int32_t* cnt = lay.counts + (size_t)b * HYQ_COUNTS;
+  const int32_t nq = cnt[HYQ_CNT_NQ], ntail = cnt[HYQ_CNT_NTAIL];
+  if (nq < 0 || nq > cap_rows || ntail < 0 || ntail > cap_tail) return 0;
+  const int32_t m = max(0, ntail - window);
+  return nq + m <= cap_rows ? m : 0;
+}
+
+// hyq_age_tail, step 1: the oldest m tail rows of (b, h) onto the 4-bit
+// stream.  grid (blocks touched, HKV, B)
+__global__ void __launch_bounds__(kThreads) age_blocks_kernel(hyq_layout lay, int32_t nblk_cap, int32_t window,
+                                                              int32_t cap_tail) {
+  __shared__ __align__(16) BuildSmem sm;
+  const int h = blockIdx.y, b = blockIdx.z, HKV = gridDim.y;
+  const size_t bh = (size_t)b * HKV + h;
+  const int32_t m = age_rows(lay, b, window, nblk_cap * kRows, cap_tail);
+  if (m == 0) return;
+  const int32_t nq0 = lay.counts[(size_t)b * HYQ_COUNTS + HYQ_CNT_NQ];
+  append_body(sm, static_cast<const __nv_bfloat16*>(lay.tail_k) + bh * cap_tail * HYQ_D,
+              static_cast<const __nv_bfloat16*>(lay.tail_v) + bh * cap_tail * HYQ_D, nq0, nq0 + m, bh, lay,
+              nblk_cap);
+}
+
+// hyq_age_tail, step 2: tail rows [m, NTAIL) of (b, h) move to [0, NTAIL - m).
+// The destination lies below the source, so chunks taken in ascending order,
+// each read whole before any of it is written, never overwrite a row still
+// to be read.  grid (HKV, B)
+__global__ void __launch_bounds__(kThreads) age_shift_kernel(hyq_layout lay, int32_t nblk_cap, int32_t window,
+                                                             int32_t cap_tail) {
+  const int h = blockIdx.x, b = blockIdx.y, HKV = gridDim.x;
+  const size_t bh = (size_t)b * HKV + h;
+  const int32_t m = age_rows(lay, b, window, nblk_cap * kRows, cap_tail);
+  if (m == 0) return;
+  const int32_t keep = lay.counts[(size_t)b * HYQ_COUNTS + HYQ_CNT_NTAIL] - m;
+  uint4* tk = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(lay.tail_k) + bh * cap_tail * HYQ_D);
+  uint4* tv = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(lay.tail_v) + bh * cap_tail * HYQ_D);
+  constexpr int kChunkRows = kThreads / kChunks;  // 16 uint4 per row
+  for (int r0 = 0; r0 < keep; r0 += kChunkRows) {
+    const int r = r0 + threadIdx.x / kChunks, c = threadIdx.x % kChunks;
+    uint4 a = make_uint4(0, 0, 0, 0), bv = a;
+    if (r < keep) {
+      a = tk[(size_t)(m + r) * kChunks + c];
+      bv = tv[(size_t)(m + r) * kChunks + c];
+    }
+    __syncthreads();
+    if (r < keep) {
+      tk[(size_t)r * kChunks + c] = a;
+      tv[(size_t)r * kChunks + c] = bv;
+    }
+    __syncthreads();
   }
-  __syncthreads();
-  build_block(sm, k_rows + bh * n * HYQ_D, v_rows + bh * n * HYQ_D,
-              lay.qblocks + (bh * nblk_cap + bi) * (size_t)HYQ_QBLOCK_BYTES, bi * kRows < nq0, lay.err);
+}
+
+// hyq_age_tail, step 3: NQ += m, NTAIL -= m (LEN unchanged).  grid (B)
+__global__ void age_counts_kernel(hyq_layout lay, int32_t nblk_cap, int32_t window, int32_t cap_tail) {
+  const int b = blockIdx.x;
+  int32_t* cnt = lay.counts + (size_t)b * HYQ_COUNTS;
+  const int32_t nq = cnt[HYQ_CNT_NQ], ntail = cnt[HYQ_CNT_NTAIL];
+  const int32_t m = age_rows(lay, b, window, nblk_cap * kRows, cap_tail);
+  if (m == 0) {
+    const bool bad = nq < 0 || nq > nblk_cap * kRows || ntail < 0 || ntail > cap_tail ||
+                     (ntail > window && nq + (ntail - window) > nblk_cap * kRows);
+    if (bad) hyq_set_err(lay.err, HYQ_DEVERR_COUNT);
+    return;
+  }
+  cnt[HYQ_CNT_NQ] = nq + m;
+  cnt[HYQ_CNT_NTAIL] = ntail - m;
 }
 
 __global__ void append_counts_kernel(hyq_layout lay, int32_t n, int32_t cap_rows) {
@@ -481,6 +561,22 @@ __global__ void append_counts_kernel(hyq_layout lay, int32_t n, int32_t cap_rows
 }
 
 }  // namespace
+
+cudaError_t hyq_launch_age_tail(const hyq_config* c, const hyq_layout* lay, cudaStream_t s) {
+  const int32_t nblk = hyq_nblk(c), ct = hyq_cap_tail(c);
+  // at most cap_tail - W = period rows leave: that many 64-row blocks plus one
+  const int32_t most = ct - c->window;
+  if (most <= 0) return cudaSuccess;
+  dim3 grid((most + HYQ_QBLOCK_ROWS - 1) / HYQ_QBLOCK_ROWS + 1, c->num_kv_heads, c->batch);
+  age_blocks_kernel<<<grid, kThreads, 0, s>>>(*lay, nblk, c->window, ct);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  age_shift_kernel<<<dim3(c->num_kv_heads, c->batch), kThreads, 0, s>>>(*lay, nblk, c->window, ct);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  age_counts_kernel<<<c->batch, 1, 0, s>>>(*lay, nblk, c->window, ct);
+  return cudaGetLastError();
+}
 
 cudaError_t hyq_launch_quantize_append(const hyq_config* c, const void* k, const void* v,
                                        int32_t n_rows, const hyq_layout* lay, cudaStream_t s) {

@@ -5,7 +5,11 @@ kernels.
 For every token t of the period but the last, one graph holds the fused
 decode step (append + attention, hyq_decode_step) of every layer; with
 ``prefetch_next`` each step also warms L2 with the next layer's share
-(hyq_decode_step_prefetch; the layer after the last is the first).  At the
+(hyq_decode_step_prefetch; the layer after the last is the first).  In
+``mode="frozen"`` (Algorithm 4 as written) the last token's maintenance is
+hyq_age_tail (the tail rows older than the window go to the 4-bit stream,
+the vertical-line set chosen at freeze stays) instead of re-selection and
+rebuild; the reset then also restores the tail rows the aging shifted.  At the
 last token two graphs are captured: the appends of all layers with the
 re-selection and rebuild of every layer, then the decode attention of all
 layers (maintenance sits between the append and the attention).  A reset graph restores the
@@ -29,9 +33,14 @@ class PeriodRunner:
     k_tok / v_tok   : [period, n_layers, B, HKV, 128] bf16
     """
 
-    def __init__(self, cfg, k_srcs, v_srcs, L0: int, device="cuda", prefetch_next: bool = False):
+    def __init__(self, cfg, k_srcs, v_srcs, L0: int, device="cuda", prefetch_next: bool = False,
+                 mode: str = "reselect"):
+        if mode not in ("reselect", "frozen"):
+            raise ValueError(f"mode must be 'reselect' or 'frozen', not {mode!r}")
         self.cfg = cfg
         self.prefetch_next = prefetch_next
+        self.frozen = mode == "frozen"
+        self.tail0 = None
         self.n_layers = len(k_srcs)
         self.k_srcs, self.v_srcs = k_srcs, v_srcs
         self.L0 = L0
@@ -61,11 +70,16 @@ class PeriodRunner:
             L.hyq_rebuild(self.cfg, self.k_srcs[li], self.v_srcs[li], self.L0, self.idx[li], k, lay.c)
         torch.cuda.synchronize()
         self.counts0 = torch.stack([lay.counts().clone() for lay in self.layers])
+        if self.frozen:
+            self.tail0 = [(lay.tail_k().clone(), lay.tail_v().clone()) for lay in self.layers]
 
     # --- the per-token work, as eager calls (captured below) ---------------
     def _reset(self):
         for li, lay in enumerate(self.layers):
             lay.counts().copy_(self.counts0[li])
+            if self.tail0 is not None:
+                lay.tail_k().copy_(self.tail0[li][0])
+                lay.tail_v().copy_(self.tail0[li][1])
 
     def _appends(self, t):
         n = 0
@@ -73,7 +87,10 @@ class PeriodRunner:
             L.hyq_decode_append(self.cfg, self.q_tok[t, li], self.k_tok[t, li], self.v_tok[t, li], lay.c,
                                 self.k_srcs[li], self.v_srcs[li])
             n += 1
-            if t == self.cfg.period - 1:
+            if t == self.cfg.period - 1 and self.frozen:
+                L.hyq_age_tail(self.cfg, lay.c)
+                n += 3
+            elif t == self.cfg.period - 1:
                 ring = lay.q_ring()
                 k = L.hyq_select_vertical(self.cfg, ring, ring.shape[2], self.k_srcs[li], self.L_end,
                                           self.idx[li], self.ws_sel)

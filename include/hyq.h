@@ -186,6 +186,21 @@ hyq_status hyq_quantize_append(const hyq_config *cfg, const void *k_rows, const 
                                int32_t n_rows, const hyq_layout *lay, hyq_stream_t stream);
 
 /*
+ * Frozen-mode maintenance (Algorithm 4 as written, Appendix A.4: the
+ * vertical-line set is fixed at freeze and only positions that leave the
+ * window are quantised).  For every sequence b, the oldest
+ * m = max(0, NTAIL - W) tail rows (positions [L - NTAIL, L - W)) are
+ * quantised exactly as hyq_quantize_append does and appended to the 4-bit
+ * stream after its NQ rows, and the last W tail rows move to the front of the
+ * tail: NQ += m, NTAIL -= m, LEN, the vertical-line rows and the proxy ring
+ * unchanged.  The partition afterwards is that of hyq_rebuild at LEN with the
+ * same index list.  A sequence whose counters are out of range or whose
+ * stream has no room for the m rows is left unchanged and sets
+ * HYQ_DEVERR_COUNT.  Three launches, no workspace.
+ */
+hyq_status hyq_age_tail(const hyq_config *cfg, const hyq_layout *lay, hyq_stream_t stream);
+
+/*
  * Vertical-line token identification, Eq. 4-5 and Algorithm 1 (Appendix A.1).
  *   q_proxy  device bf16 [B][HQ][n_proxy_ld][128]; the first n_proxy query
  *            rows of each head are used (order does not matter)

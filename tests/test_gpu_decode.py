@@ -408,3 +408,86 @@ def test_decode_step_prefetch_changes_nothing(hyq, plan):
         assert torch.equal(got[0], ref[0]), mode
         for a, b in zip(got[1:], ref[1:]):
             assert all(torch.equal(x, y) for x, y in zip(a, b)), mode
+
+
+def test_frozen_mode_age_tail(hyq):
+    """Frozen mode (Algorithm 4 as written): the vertical-line set chosen at
+    freeze stays; every 64 tokens hyq_age_tail moves the tail rows older than
+    the window into the 4-bit stream.  After each aging the counters, the tail
+    rows and every stream row (codes, scales, zeros: bit-exact with the
+    oracle quantiser) equal the partition at the new length with the frozen
+    index set, and the attention matches the oracle over that partition."""
+    from hybrid_precision_quantized_gb300 import hyq_age_tail, hyq_decode_step
+    from tests.test_gpu_quant import _check_stream
+    B, HQ, HKV, W, ppm, T = 2, 8, 2, 128, 50_000, 64
+    L0, periods = 900, 2
+    cap = L0 + periods * T
+    c = decode_case(95, B, HQ, HKV, cap, window=W, n_proxy=16, sink_frac=0.02)
+    cfg, (lay, _), idx_np = _two_layers(c, L0, W, ppm, cap)
+    k = idx_np.shape[-1]
+    ks = torch.zeros(B, HKV, cap, 128, dtype=torch.bfloat16, device="cuda")
+    vs = torch.zeros_like(ks)
+    ks[:, :, :L0] = c.k[:, :, :L0].cuda()
+    vs[:, :, :L0] = c.v[:, :, :L0].cuda()
+    ws = workspace(cfg, L.OP_DECODE, cap)
+    g = gen_for(95, "q-steps")
+    k_np, v_np = c.k.double().numpy(), c.v.double().numpy()
+    out = torch.empty(B, HQ, 128, dtype=torch.bfloat16, device="cuda")
+    Lc = L0
+    for _ in range(periods):
+        for _ in range(T):
+            q = torch.randn(B, HQ, 128, generator=g).to(torch.bfloat16)
+            hyq_decode_step(cfg, q.cuda(), c.k[:, :, Lc].contiguous().cuda(), c.v[:, :, Lc].contiguous().cuda(),
+                            lay.c, out, ws, ks, vs, cap)
+            Lc += 1
+        torch.cuda.synchronize()
+        assert layer_counts(lay)[:3] == [L0 - W - k + (Lc - L0 - T), k, W + T]
+        # the last step's attention over the 4-bit stream of the last aging
+        P_before = Lc - 1 - (W + T - 1)
+        want = hybrid_decode(q.double().numpy(), k_np, v_np, Lc, P_before, idx_np)
+        assert_attention_close(to_np(out), want, what=f"before aging, L={Lc}")
+        hyq_age_tail(cfg, lay.c)
+        torch.cuda.synchronize()
+        assert hyq_read_device_error(lay.err()) == 0
+        P = Lc - W
+        assert layer_counts(lay)[:4] == [P - k, k, W, Lc]
+        for b in range(B):
+            for h in range(HKV):
+                qpos = np.setdiff1d(np.arange(P), idx_np[b, h])
+                _check_stream(lay, b, h, len(qpos), c.k[b, h, qpos].double().numpy(),
+                              c.v[b, h, qpos].double().numpy())
+                assert torch.equal(lay.tail_k()[b, h, :W].cpu(), c.k[b, h, P:Lc])
+                assert torch.equal(lay.tail_v()[b, h, :W].cpu(), c.v[b, h, P:Lc])
+        q = torch.randn(B, HQ, 128, generator=g).to(torch.bfloat16)
+        hyq_decode_attention(cfg, q.cuda(), lay.c, out, ws, cap)
+        torch.cuda.synchronize()
+        want = hybrid_decode(q.double().numpy(), k_np, v_np, Lc, P, idx_np)
+        assert_attention_close(to_np(out), want, what=f"after aging, L={Lc}")
+
+
+def test_age_tail_without_room_is_flagged(hyq):
+    """A stream without room for the aged rows leaves the layout unchanged and
+    sets HYQ_DEVERR_COUNT."""
+    from hybrid_precision_quantized_gb300 import hyq_age_tail, hyq_decode_step
+    B, HQ, HKV, W, ppm, L0 = 1, 4, 1, 64, 0, 600
+    cap = L0 + 64
+    c = decode_case(96, B, HQ, HKV, cap, window=W, n_proxy=8)
+    cfg, (lay, _), _ = _two_layers(c, L0, W, ppm, cap)
+    ws = workspace(cfg, L.OP_DECODE, cap)
+    out = torch.empty(B, HQ, 128, dtype=torch.bfloat16, device="cuda")
+    for t in range(64):
+        hyq_decode_step(cfg, c.q.cuda(), c.k[:, :, L0 + t].contiguous().cuda(),
+                        c.v[:, :, L0 + t].contiguous().cuda(), lay.c, out, ws, None, None, cap)
+    torch.cuda.synchronize()
+    assert layer_counts(lay)[:3] == [L0 - W, 0, W + 64]
+    stream_rows = -(-cap // 64) * 64           # the 4-bit stream's capacity in rows
+    lay.counts()[0, L.CNT_NQ] = stream_rows - 10   # as if the stream were nearly full
+    before = layer_counts(lay)
+    hyq_age_tail(cfg, lay.c)
+    torch.cuda.synchronize()
+    assert hyq_read_device_error(lay.err()) & L.DEVERR_COUNT
+    assert layer_counts(lay) == before
+
+
+def layer_counts(lay):
+    return lay.counts()[0].tolist()
