@@ -491,3 +491,39 @@ def test_age_tail_without_room_is_flagged(hyq):
 
 def layer_counts(lay):
     return lay.counts()[0].tolist()
+
+
+def test_decode_qwen8b_shaped_batch16_32k_sampled(hyq):
+    """Qwen3-8B-shaped batched decode at full size: batch 16, 32/8 heads, 32K
+    context, W 128, rho 5%, the launch configuration the benchmark times
+    (automatic plan).  Each sequence is its own seeded case; the oracle picks
+    each sequence's vertical lines, the GPU decodes all 16 x 32 heads, and
+    three sampled (sequence, KV head) pairs are checked in full."""
+    B, HQ, HKV, Lc, W, ppm = 16, 32, 8, 32768, 128, 50_000
+    g = HQ // HKV
+    P = prefix_len(Lc, W)
+    cases = [decode_case(1300 + b, 1, HQ, HKV, Lc, window=W, n_proxy=64, sink_frac=0.02, outlier_channels=3)
+             for b in range(B)]
+    idx_np = np.concatenate([select_vertical(c.q_proxy.double().numpy(), c.k.double().numpy(), Lc, W, ppm)[0]
+                             for c in cases])
+    cfg = make_config(B, HQ, HKV, capacity=Lc, window=W, rho_ppm=ppm)
+    layer = HybridLayer(cfg)
+    layer.reset()
+    kd = torch.cat([c.k for c in cases]).cuda()
+    vd = torch.cat([c.v for c in cases]).cuda()
+    idx = torch.from_numpy(idx_np).to(torch.int32).cuda().contiguous()
+    hyq_rebuild(cfg, kd, vd, Lc, idx, idx_np.shape[-1], layer.c)
+    del kd, vd
+    q = torch.cat([c.q for c in cases])
+    out = torch.empty(B, HQ, 128, dtype=torch.bfloat16, device="cuda")
+    ws = workspace(cfg, L.OP_DECODE, Lc)
+    hyq_decode_attention(cfg, q.cuda(), layer.c, out, ws, Lc)
+    torch.cuda.synchronize()
+    assert hyq_read_device_error(layer.err()) == 0
+    got = to_np(out)
+    for b, kh in ((0, 0), (7, 3), (15, 7)):
+        c = cases[b]
+        hs = slice(kh * g, (kh + 1) * g)
+        want = hybrid_decode(c.q.double().numpy()[:, hs], c.k.double().numpy()[:, kh:kh + 1],
+                             c.v.double().numpy()[:, kh:kh + 1], Lc, P, idx_np[b:b + 1, kh:kh + 1])
+        assert_attention_close(got[b:b + 1, hs], want, what=f"b={b} kvh={kh}")
