@@ -50,6 +50,8 @@ def parse():
     p.add_argument("--no-baseline", action="store_true", help="skip the CPU oracle timing")
     p.add_argument("--no-prefill", action="store_true", help="skip the prefill measurement")
     p.add_argument("--no-batched", action="store_true", help="skip the batch-16 decode measurement")
+    p.add_argument("--decode-plan", type=int, nargs=2, default=(0, 0), metavar=("MERGE", "SPLITS"),
+                   help="tuning: hyq_set_decode_plan(MERGE, SPLITS) for the period (0 0 = automatic)")
     p.add_argument("--no-frozen", action="store_true", help="skip the frozen-mode period measurement")
     p.add_argument("--no-prefetch", dest="prefetch", action="store_false",
                    help="plain fused decode steps; by default each step warms L2 with the next layer's share "
@@ -66,9 +68,10 @@ def parse():
 
 
 def run_decode_layer_case(args, local):
-    """One Llama-shaped 32K layer: freeze at 32K - 64 positions, then 6 fused
-    decode steps (hyq_decode_step, the call the benchmark times); prints the
-    mean launch time.  Used as a small, self-contained ncu target."""
+    """Two Llama-shaped 32K layers: freeze each at 32K - 64 positions, then 6
+    fused decode steps alternating between them, each warming L2 with the
+    other layer (hyq_decode_step_prefetch, the call the benchmark times);
+    prints the mean launch time.  Used as a small, self-contained ncu target."""
     import torch
     import hybrid_precision_quantized_gb300 as hyq
     from hybrid_precision_quantized_gb300 import _lib as L
@@ -77,23 +80,29 @@ def run_decode_layer_case(args, local):
     dev = torch.device("cuda", local)
     hyq.load()
     cfg = hyq.make_config(B, HQ, HKV, capacity=CTX, window=WINDOW, period=PERIOD, rho_ppm=RHO_PPM)
-    k_srcs, v_srcs, q_tail, q_tok, k_tok, v_tok = make_inputs(dev, 1)
-    layer = hyq.HybridLayer(cfg, dev)
-    layer.reset()
-    idx = torch.zeros(B, HKV, hyq.hyq_vl_count(cfg, L0 - WINDOW), dtype=torch.int32, device=dev)
-    k = hyq.hyq_select_vertical(cfg, q_tail[0], 64, k_srcs[0], L0, idx, hyq.workspace(cfg, L.OP_SELECT, CTX, dev))
-    hyq.hyq_rebuild(cfg, k_srcs[0], v_srcs[0], L0, idx, k, layer.c)
+    k_srcs, v_srcs, q_tail, q_tok, k_tok, v_tok = make_inputs(dev, 2)
+    layers = []
+    for li in range(2):
+        layer = hyq.HybridLayer(cfg, dev)
+        layer.reset()
+        idx = torch.zeros(B, HKV, hyq.hyq_vl_count(cfg, L0 - WINDOW), dtype=torch.int32, device=dev)
+        k = hyq.hyq_select_vertical(cfg, q_tail[li], 64, k_srcs[li], L0, idx,
+                                    hyq.workspace(cfg, L.OP_SELECT, CTX, dev))
+        hyq.hyq_rebuild(cfg, k_srcs[li], v_srcs[li], L0, idx, k, layer.c)
+        layers.append(layer)
     ws = hyq.workspace(cfg, L.OP_DECODE, CTX, dev)
     out = torch.empty(B, HQ, D, dtype=torch.bfloat16, device=dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for i in range(6):
         if i == 2:
             e0.record()
-        hyq.hyq_decode_step(cfg, q_tok[i, 0], k_tok[i, 0], v_tok[i, 0], layer.c, out, ws, k_srcs[0], v_srcs[0], CTX)
+        li = i % 2
+        hyq.hyq_decode_step_prefetch(cfg, q_tok[i // 2, li], k_tok[i // 2, li], v_tok[i // 2, li], layers[li].c,
+                                     layers[1 - li].c, out, ws, k_srcs[li], v_srcs[li], CTX)
     e1.record()
     torch.cuda.synchronize()
     print(json.dumps({"case": "decode-layer", "us_per_launch_l2_warm": e0.elapsed_time(e1) * 1e3 / 4,
-                      "device_error_word": hyq.hyq_read_device_error(layer.err())}))
+                      "device_error_word": max(hyq.hyq_read_device_error(la.err()) for la in layers)}))
 
 
 def measured_tensor_peaks():
@@ -490,6 +499,7 @@ def run_ours(args, rank, world, local):
     # overlap the one before it (programmatic dependent launch); measured
     # slower inside CUDA graphs on GB300, hence off unless asked for
     hyq.hyq_set_decode_overlap(args.overlap)
+    hyq.hyq_set_decode_plan(*args.decode_plan)
     run = PeriodRunner(cfg, k_srcs, v_srcs, L0, dev, prefetch_next=args.prefetch)
     run.q_tok.copy_(q_tok)
     run.k_tok.copy_(k_tok)
@@ -586,7 +596,8 @@ def run_ours(args, rank, world, local):
                                "rho 5%, K4V4 G32; 32 distinct layers; step = 64-token re-selection period",
                    "context": CTX, "layers": nl, "tokens_per_step": PERIOD,
                    "l2": "no flush: the 32 layers' caches (~1.6 GB) exceed L2 between reuses",
-                   "launch_overlap": args.overlap, "prefetch_next_layer": args.prefetch},
+                   "launch_overlap": args.overlap, "prefetch_next_layer": args.prefetch,
+                   "decode_plan": "automatic" if tuple(args.decode_plan) == (0, 0) else list(args.decode_plan)},
         "gpu_launches": main_launches * args.steps,
         "decode_kernel_us": dec_us,
         "us_per_token_all_layers": value * nl,
