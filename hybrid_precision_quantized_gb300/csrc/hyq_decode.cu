@@ -119,6 +119,14 @@ struct StepArgs {
   const __nv_bfloat16 *nx_vl_k, *nx_vl_v, *nx_tail_k, *nx_tail_v;
 };
 
+// floor(i * n / S) for 0 <= i <= S: 32-bit unsigned arithmetic when the
+// product fits (the usual case: a few thousand tiles, S <= 1024), else 64-bit.
+__device__ __forceinline__ int share_bound(int i, int n, int S) {
+  const uint32_t a = (uint32_t)i, nn = (uint32_t)n, s = (uint32_t)S;
+  if ((uint64_t)s * nn <= 0xFFFFFFFFull) return (int)(a * nn / s);
+  return (int)((uint64_t)a * nn / s);
+}
+
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(bytes) : "memory");
 }
@@ -141,7 +149,7 @@ __device__ __forceinline__ NextCounts next_counts(const StepArgs& sa, int b, int
 __device__ void prefetch_next_tiles(const StepArgs& sa, const NextCounts& n, size_t bh, int split, int S,
                                     int nblk_cap, int lane) {
   const int nt = (n.nq + 15) >> 4;
-  const int t0 = (int)((int64_t)split * nt / S), t1 = (int)((int64_t)(split + 1) * nt / S);
+  const int t0 = share_bound(split, nt, S), t1 = share_bound(split + 1, nt, S);
   const uint8_t* tiles = sa.nx_qblocks + bh * (size_t)nblk_cap * HYQ_QBLOCK_BYTES + (size_t)t0 * HYQ_QTILE_BYTES;
   const uint32_t bytes = (uint32_t)(t1 - t0) * HYQ_QTILE_BYTES;
   constexpr uint32_t kChunk = 16384;
@@ -156,7 +164,7 @@ __device__ void prefetch_next_rows(const StepArgs& sa, const NextCounts& n, size
   const int32_t nvl = n.nvl, ntail = n.ntail;
   const int nft = (nvl + ntail + 15) >> 4;
   if (lane < 4) {
-    const int f0 = (int)((int64_t)split * nft / S), f1 = (int)((int64_t)(split + 1) * nft / S);
+    const int f0 = share_bound(split, nft, S), f1 = share_bound(split + 1, nft, S);
     const int r0 = 16 * f0, r1 = min(16 * f1, nvl + ntail);
     const bool vpart = lane & 1;
     if (lane < 2 && min(r1, nvl) > r0) {  // vertical-line rows
@@ -468,15 +476,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
   // kernel but the immediately preceding one has finished whenever a launch
   // starts.
   const bool ovl = sa.overlap != 0;
-  // The query rows of the KV group go first in this SM's copy queue.
+  // The query rows of the KV group: plain 16-byte loads issued first (a
+  // load returns well before a bulk copy would), stored to shared memory
+  // just before the block barrier below.  With overlap the query may only be
+  // read after griddepcontrol.wait and comes by bulk copy there.
   if (tid == 0) {
     mbar_init(&qbar, 1);
     mbar_fence_init();
-    if (!ovl) {
-      mbar_arrive_expect_tx(&qbar, gq * HYQ_D * 2);
-      bulk_g2s(q_s, q + ((size_t)b * HQ + (size_t)h * gq) * HYQ_D, gq * HYQ_D * 2, &qbar);
-    }
   }
+  const int nq16 = gq * HYQ_D / 8;
+  uint4 qv = make_uint4(0, 0, 0, 0);
+  if (!ovl && tid < nq16)
+    qv = __ldg(reinterpret_cast<const uint4*>(q + ((size_t)b * HQ + (size_t)h * gq) * HYQ_D) + tid);
   const int32_t* cnt = lay.counts + (size_t)b * HYQ_COUNTS;
   int32_t nq = cnt[HYQ_CNT_NQ], nvl = cnt[HYQ_CNT_NVL], ntail = cnt[HYQ_CNT_NTAIL];
   if (nq < 0 || nq > nblk_cap * HYQ_QBLOCK_ROWS || nvl < 0 || nvl > cap_vl || ntail < 0 || ntail > cap_tail) {
@@ -498,8 +509,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
   }
   // This block's share of the 4-bit tiles and of the BF16 tiles.
   const int nt = (nq + 15) >> 4, nf = nvl + ntail + (app ? 1 : 0), nft = (nf + 15) >> 4;
-  const int t0 = (int)((int64_t)split * nt / S), t1 = (int)((int64_t)(split + 1) * nt / S);
-  const int f0 = (int)((int64_t)split * nft / S), f1 = (int)((int64_t)(split + 1) * nft / S);
+  const int t0 = share_bound(split, nt, S), t1 = share_bound(split + 1, nt, S);
+  const int f0 = share_bound(split, nft, S), f1 = share_bound(split + 1, nft, S);
   // 4-bit tiles go round-robin over the warps, starting after the warps that
   // also take a BF16 tile.
   const int ntc = t1 - t0, rot = (f1 - f0) % kWarps;
@@ -565,8 +576,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
   }
   for (int i = gq * HYQ_D / 8 + tid; i < HYQ_MAX_GQA * HYQ_D / 8; i += kThreads)
     reinterpret_cast<uint4*>(q_s)[i] = make_uint4(0, 0, 0, 0);  // query rows past g
+  if (!ovl && tid < nq16) reinterpret_cast<uint4*>(q_s)[tid] = qv;
   __syncthreads();
-  if (!ovl && !mbar_wait(&qbar, 0) && tid == 0) hyq_set_err(lay.err, HYQ_DEVERR_TIMEOUT);
   if (ovl) {
     // The layout copies are in flight; now wait for the preceding kernel and
     // fetch what it may have produced.
