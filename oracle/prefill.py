@@ -95,10 +95,12 @@ def hybrid_prefill(q, k, v, vl_idx, window: int, dtype: str = "int8",
     g = HQ // HKV
     alpha = 1.0 / math.sqrt(d)
     P = max(0, L - window)
-    out = np.zeros_like(q)
-    mag = np.zeros_like(q)
+    out = np.zeros(q.shape)  # zero pages are mapped on first write
+    mag = np.zeros(q.shape)
     for b in range(B):
         for kh in range(HKV):
+            if heads is not None and not any(h in heads for h in range(kh * g, (kh + 1) * g)):
+                continue  # no requested query head reads this KV head
             vl = (np.zeros(0, np.int64) if vl_idx is None
                   else np.asarray(vl_idx[b, kh], np.int64))
             qpos = np.setdiff1d(np.arange(P), vl)
