@@ -16,15 +16,16 @@
 //     stored transposed (dims x keys) for the P.V product.
 //  2. prefill_kernel (stage 3): one CTA per (query block of 128 rows, query
 //     head).  Warps 8 and 9 stream key and value tiles (bulk copies, one
-//     ring each); warp 10 issues tcgen05.mma: S = Q K^T into TMEM, then
+//     ring each); warp 10 issues tcgen05.mma S = Q K^T into TMEM and warp 11
 //     O_h += P_h V_h into TMEM for the two 64-key halves h of each tile;
 //     warps 0-7 (one thread per query row = TMEM lane and key half) read S,
 //     scale, mask, run an online softmax per half and write P as BF16 into
 //     one of two TMEM buffers, where the P.V MMA takes its A operand; one
 //     barrier signals both halves' P of a tile and one commit their P.V, and
-//     the two halves' (max, sum, O) merge once at the end.  The MMA thread
-//     shares a scheduler with softmax warps, so its loop is kept to a few
-//     instructions.  The quantised segment uses e4m3 codes (kind::f8f6f4) or INT8
+//     the two halves' (max, sum, O) merge once at the end.  The MMA threads
+//     share schedulers with softmax warps, so their loops are kept to a few
+//     instructions, and the two products are issued from two threads so
+//     that neither's waits hold back the other.  The quantised segment uses e4m3 codes (kind::f8f6f4) or INT8
 //     codes held exactly as BF16 integers (kind::f16; sm_103a has no integer
 //     tensor-core MMA); the full-precision segment uses BF16.  P.V runs in
 //     BF16 with the value codes (exact in BF16) and the value scale folded
@@ -48,8 +49,10 @@ constexpr int kRegion = 16384;       // 128 rows x 128 bytes, swizzled
 constexpr int kImg16 = 2 * kRegion;  // 128 x 128 16-bit operand image
 constexpr int kImg8 = kRegion;       // 128 x 128 8-bit operand image
 constexpr int kSoft = 256;           // softmax threads (warps 0-7)
-constexpr int kCopyWarp = 8, kMmaWarp = 10;  // copy warps 8 (keys) and 9 (values)
-constexpr int kThreads = 352;
+constexpr int kCopyWarp = 8;  // copy warps 8 (keys) and 9 (values)
+constexpr int kMmaWarp = 10;  // issues S = Q K^T (and allocates TMEM)
+constexpr int kPvWarp = 11;   // issues O += P V
+constexpr int kThreads = 384;
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns: S (one 128-key tile, FP32), P (two tiles in flight, BF16
 // pairs: 64 columns per tile, 32 per key half), one O accumulator per key half.
@@ -413,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     }
     mbar_init(pfull, kSoft);
     mbar_init(pvdone, 1);
-    mbar_init(mmadone, 1);
+    mbar_init(mmadone, 2);  // one commit from each MMA-issuing thread
     mbar_init(sfull, 1);
     mbar_init(sfree, kSoft);
     mbar_fence_init();
@@ -730,13 +733,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       // CTA's shared memory goes away
       for (int j = max(0, last_j - nst + 1); j <= last_j; ++j) mbar_wait(full + j % nst, (j / nst) & 1);
     }
-  } else {
-    // ---------------- MMA warp -----------------------------------------
+  } else if (warp == kMmaWarp || warp == kPvWarp) {
+    // ---------------- MMA warps ----------------------------------------
     if (lane == 0) {
       const uint32_t aQ = smem_u32(sm + kOffQ), aQc = smem_u32(sm + kOffQc);
       bool ok = mbar_wait_or_abort(qready, 0, abort_flag);
       tc_fence_after();
-      // The MMA thread shares its scheduler with two softmax warps, so its
+      // Each MMA thread shares its scheduler with two softmax warps, so its
       // own instructions are few: descriptors are built once and advanced by
       // adding offsets (the start-address field counts 16-byte units), ring
       // stages and phases are tracked incrementally.
@@ -746,8 +749,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       const uint32_t tS = tbase + kColS;
       int sk = 0, sv = 0;
       uint32_t kph = 0, vph = 0;
-      for (int j = 0; ok && j <= nt; ++j) {
-        if (j < nt) {
+      // Two issuing threads: warp 10 the S = Q K^T products, warp 11 the
+      // O += P V products.  A commit tracks the MMAs of the thread that
+      // issues it, and the two streams write disjoint TMEM (S; O, reading P
+      // from its own buffers), so each waits only on its own inputs.
+      if (warp == kMmaWarp) {
+        for (int j = 0; ok && j < nt; ++j) {
           ok = mbar_wait_or_abort(kfull + sk, kph, abort_flag);
           // the softmax has read S of the previous tile
           if (ok && j >= 1) ok = mbar_wait_or_abort(sfree, (j - 1) & 1, abort_flag);
@@ -772,8 +779,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             kph ^= 1;
           }
         }
-        if (j >= 1) {  // O_h += P_h V_h for tile i = j - 1, one key half at a time
-          const int i = j - 1;
+      } else {
+        for (int i = 0; ok && i < nt; ++i) {  // O_h += P_h V_h for the two key halves h
           const uint32_t tP = tbase + kColP + 64 * (i & 1);
           ok = mbar_wait_or_abort(vfull + sv, vph, abort_flag);
           const uint64_t dV = dV0 + sv * kStageStep;
@@ -800,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         *abort_flag = 1;
         hyq_set_err(p.err, HYQ_DEVERR_TIMEOUT);
       }
-      tc_commit(mmadone);  // every MMA issued above has finished once this arrives
+      tc_commit(mmadone);  // every MMA this thread issued has finished once both arrive
       mbar_wait(mmadone, 0);
     }
   }
