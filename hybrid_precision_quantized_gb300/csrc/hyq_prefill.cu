@@ -574,10 +574,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       const float m_new = grow ? tmax : m_used;
       const float fac = grow ? fast_exp2(m_used - m_new) : 1.f;
       const float mb = (m_new == -INFINITY) ? 0.f : m_new;
+      // P_h as BF16 pairs with the value scale folded in (the A operand of
+      // P.V), built with the exponentials; stored once the P buffer is free.
       float rs;
+      uint32_t pw[32];
+      const uint64_t vf2 = f2_splat(vf);
       if (!masked) {
-        // Pairs: scale, shift and sum packed (fewer instructions on the
-        // softmax warps leaves more issue slots to the MMA warp beside them).
+        // Pairs: scale, shift, sum and scale by vf packed.
         const uint64_t cs2 = f2_splat(cs), nmb2 = f2_splat(-mb);
         uint64_t ps2[4] = {0, 0, 0, 0};
 #pragma unroll
@@ -585,8 +588,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           uint64_t e2 = f2_fma(f2_pack(x[2 * w], x[2 * w + 1]), cs2, nmb2);
           e2 = f2_pack(fast_exp2(f2_lo(e2)), fast_exp2(f2_hi(e2)));
           ps2[w & 3] = f2_add(ps2[w & 3], e2);
-          x[2 * w] = f2_lo(e2);
-          x[2 * w + 1] = f2_hi(e2);
+          const uint64_t pv = f2_mul(e2, vf2);
+          pw[w] = pack_bf16x2(f2_lo(pv), f2_hi(pv));
         }
         const uint64_t r2 = f2_add(f2_add(ps2[0], ps2[1]), f2_add(ps2[2], ps2[3]));
         rs = f2_lo(r2) + f2_hi(r2);
@@ -600,6 +603,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           ps[i & 7] += x[i];
         }
         rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+#pragma unroll
+        for (int w = 0; w < 32; ++w) {
+          const uint64_t pv = f2_mul(f2_pack(x[2 * w], x[2 * w + 1]), vf2);
+          pw[w] = pack_bf16x2(f2_lo(pv), f2_hi(pv));
+        }
       }
       l_sum = l_sum * fac + rs;
       m_used = m_new;
@@ -624,19 +632,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           tc_wait_st();
         }
       }
-      {
-        // P_h (BF16 pairs, the value scale folded in) into P buffer j % 2,
-        // whose previous tile's P.V is done: the A operand of P.V.
-        uint32_t pw[32];
-        const uint64_t vf2 = f2_splat(vf);
-#pragma unroll
-        for (int w = 0; w < 32; ++w) {
-          const uint64_t pv = f2_mul(f2_pack(x[2 * w], x[2 * w + 1]), vf2);
-          pw[w] = pack_bf16x2(f2_lo(pv), f2_hi(pv));
-        }
-        tc_st32(tbase + lane_off + kColP + 64 * s + 32 * hf, pw);
-        tc_wait_st();
-      }
+      // P buffer j % 2: its previous tile's P.V is done
+      tc_st32(tbase + lane_off + kColP + 64 * s + 32 * hf, pw);
+      tc_wait_st();
       tc_fence_before();
       mbar_arrive(pfull);
     }
