@@ -213,6 +213,14 @@ struct State {
 // logits of tokens (g, g+8); returns the probabilities p[2r + j].  The
 // accumulators are rescaled only when some head's running max moved (the
 // factor is exactly 1 otherwise).
+// 2^x on the special-function unit, one instruction (relative error about
+// 2^-22; 2^-inf = 0, results below 2^-126 flush to 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void softmax_update(const float (&lg)[4], State& st, float (&p)[4]) {
   float corr[2];
   bool moved = false;
@@ -225,9 +233,9 @@ __device__ __forceinline__ void softmax_update(const float (&lg)[4], State& st, 
     const float mn = fmaxf(st.m[j], tm);
     const float ms = (mn == -INFINITY) ? 0.f : mn;
     moved |= mn != st.m[j];
-    corr[j] = exp2f(st.m[j] - ms);
-    p[j] = exp2f(lg[j] - ms);
-    p[2 + j] = exp2f(lg[2 + j] - ms);
+    corr[j] = ex2(st.m[j] - ms);
+    p[j] = ex2(lg[j] - ms);
+    p[2 + j] = ex2(lg[2 + j] - ms);
     st.l[j] = fmaf(st.l[j], corr[j], p[j] + p[2 + j]);
     st.m[j] = mn;
   }
@@ -740,7 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     const float Ms = (M == -INFINITY) ? 0.f : M;
-    const float wt = lane < kWarps ? exp2f(mw - Ms) : 0.f;
+    const float wt = lane < kWarps ? ex2(mw - Ms) : 0.f;
     if (lane < kWarps) wts[lane][hd] = wt;
     float Lsum = lane < kWarps ? red_l[lane][hd] * wt : 0.f;
 #pragma unroll
@@ -809,7 +817,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
       const float Ms = (M == -INFINITY) ? 0.f : M;
       float Lsum = 0.f;
       for (int r = 0; r < S; ++r) {
-        const float wt = exp2f(rm[r * HYQ_MAX_GQA + tid] - Ms);
+        const float wt = ex2(rm[r * HYQ_MAX_GQA + tid] - Ms);
         rm[r * HYQ_MAX_GQA + tid] = wt;
         Lsum = fmaf(rl[r * HYQ_MAX_GQA + tid], wt, Lsum);
       }
@@ -875,7 +883,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
     const float Ms = (M == -INFINITY) ? 0.f : M;
     float Lsum = 0.f;
     for (int s2 = lane; s2 < S; s2 += 32) {
-      const float wt = exp2f(sm_m[s2 * HYQ_MAX_GQA + hd] - Ms);
+      const float wt = ex2(sm_m[s2 * HYQ_MAX_GQA + hd] - Ms);
       Lsum = fmaf(sm_w[s2 * HYQ_MAX_GQA + hd], wt, Lsum);
       sm_w[s2 * HYQ_MAX_GQA + hd] = wt;
     }
