@@ -85,6 +85,106 @@ def select_vertical(q_proxy, k_src, L: int, window: int, rho_ppm: int):
     return topk_ascending(S, k), S
 
 
+# --- Eq. 4: the softmax-mass score (an alternative to Algorithm 1's) -------
+#
+# Eq. 4 defines the vertical-line score as the accumulated column mass
+# S(j) = sum_{t in T} a_{t,j}, with a_{t,j} the attention probability of
+# query t on key j.  Readings: T is the proxy buffer (the last <= 64 queries)
+# and, for GQA, every query head of the KV group (as for Algorithm 1's
+# score); a_{t,j} is the softmax over the L current keys of alpha q_t . k_j
+# (alpha = 1/sqrt(d)), the keys present when the selection runs; Eq. 5 then
+# takes the top-k of S over the non-window prefix [0, P).
+
+def mass_scores(q_proxy, k_src, L: int, window: int, alpha=None) -> np.ndarray:
+    """Eq. 4: ``S(j) = sum_t sum_h softmax_j(alpha q_{t,h} . k_j)`` for j in
+    [0, P), the softmax over all L keys.  q_proxy [B, HQ, T, d], k_src
+    [B, HKV, >=L, d] -> S [B, HKV, P] float64."""
+    q = np.asarray(q_proxy, dtype=np.float64)
+    k = np.asarray(k_src, dtype=np.float64)
+    B, HQ, T, d = q.shape
+    HKV = k.shape[1]
+    g = HQ // HKV
+    a = 1.0 / np.sqrt(d) if alpha is None else alpha
+    P = prefix_len(L, window)
+    S = np.zeros((B, HKV, P))
+    if P == 0:
+        return S
+    for b in range(B):
+        for kh in range(HKV):
+            Q = q[b, kh * g:(kh + 1) * g].reshape(g * T, d)      # every (head, proxy) row
+            z = a * (Q @ k[b, kh, :L].T)                          # rows x L logits
+            e = np.exp(z - z.max(axis=1, keepdims=True))
+            A = e / e.sum(axis=1, keepdims=True)                  # softmax over the L keys
+            S[b, kh] = A[:, :P].sum(axis=0)                        # column mass on the prefix
+    return S
+
+
+def select_vertical_mass(q_proxy, k_src, L: int, window: int, rho_ppm: int):
+    """Eq. 4-5 with the softmax-mass score.  Returns (idx [B, HKV, k]
+    ascending, S [B, HKV, P])."""
+    P = prefix_len(L, window)
+    k = vl_count(P, rho_ppm)
+    S = mass_scores(q_proxy, k_src, L, window)
+    return topk_ascending(S, k), S
+
+
+def mass_error_bound(q_proxy, k_src, L: int, window: int, chunks: int = 1024,
+                     ex2_rel: float = 2.0 ** -21) -> np.ndarray:
+    """A rigorous bound on |S32(j) - S(j)| for a float32 evaluation that
+    computes, per row r and key j, z32 = q_r . k_j with exact products of the
+    BF16 inputs accumulated in float32 (any order), t = fl(z32 * c) with
+    c = fl(alpha log2 e), the row maximum m and the row sum l of
+    ex2(t - m) (partial sums over at most ``chunks`` key ranges merged once
+    with ex2 rescaling), a = ex2(t - m) / l, and S(j) = sum_r a (float32, any
+    order); ex2 has relative error at most ``ex2_rel`` and flushes results
+    below 2^-126 to zero.
+
+    With u = 2^-23 (one float32 ulp, covering truncating accumulators):
+      dt_rj = c (1 + 2u) gamma_d sum_i |q_ri k_ji| + 2u c |z_rj|     (error of t)
+      dm_r  = max_j dt_rj                                               (of m)
+      eta_rj = dt_rj + dm_r + u |t_rj - m_r|                 (of t - m, log2 units)
+    the computed numerator is 2^(t-m) 2^(+-eta) (1 +- ex2_rel), the row sum
+    l within the a-weighted mean of those factors times (1 +- gamma_(L +
+    chunks) (1 + ex2_rel)), the quotient within 2u; the column sum adds
+    gamma_R sum_r a.  Elements whose numerator can flush (t - m - eta <
+    -126) count with their whole weight.  Returned per (b, kvh, j < P).
+    """
+    q = np.asarray(q_proxy, dtype=np.float64)
+    k = np.asarray(k_src, dtype=np.float64)
+    B, HQ, T, d = q.shape
+    HKV = k.shape[1]
+    g = HQ // HKV
+    R = g * T
+    u = 2.0 ** -23
+    alpha = 1.0 / np.sqrt(d)
+    c = alpha / np.log(2.0)
+    P = prefix_len(L, window)
+    bound = np.zeros((B, HKV, P))
+    if P == 0:
+        return bound
+    gl = _gamma(L + chunks) * (1 + ex2_rel) + ex2_rel
+    for b in range(B):
+        for kh in range(HKV):
+            Q = q[b, kh * g:(kh + 1) * g].reshape(R, d)
+            K = k[b, kh, :L]
+            z = Q @ K.T
+            t = c * z
+            m = t.max(axis=1, keepdims=True)
+            A = np.exp2(t - m)
+            A /= A.sum(axis=1, keepdims=True)
+            dt = c * (1 + 2 * u) * _gamma(d) * (np.abs(Q) @ np.abs(K).T) + 2 * u * c * np.abs(z)
+            eta = dt + dt.max(axis=1, keepdims=True) + u * np.abs(t - m)
+            up = np.exp2(eta) * (1 + ex2_rel)
+            lo = np.exp2(-eta) * (1 - ex2_rel)
+            den_hi = (A * up).sum(axis=1, keepdims=True) * (1 + gl)
+            den_lo = (A * lo).sum(axis=1, keepdims=True) * (1 - gl)
+            rel = np.maximum(up * (1 + 2 * u) / den_lo - 1.0, 1.0 - lo * (1 - 2 * u) / den_hi)
+            rel = np.where(t - m - eta < -126.0, 1.0, rel)
+            err = (A * rel)[:, :P].sum(axis=0) + _gamma(R) * (A * (1 + rel))[:, :P].sum(axis=0)
+            bound[b, kh] = err
+    return bound
+
+
 # --- float32 error bounds used to judge a float32 implementation -----------
 
 def _gamma(n: int, unit: float = 2.0 ** -23) -> float:

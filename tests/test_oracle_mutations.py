@@ -49,6 +49,14 @@ MUTATIONS = [
      "ties to the higher index"),
     ("select", "return max(0, int(L) - int(window))", "return max(0, int(L) - int(window) - 1)",
      "prefix length off by one"),
+    ("select", "z = a * (Q @ k[b, kh, :L].T)", "z = a * (Q @ k[b, kh, :P].T)",
+     "mass softmax over the prefix only"),
+    ("select", "z = a * (Q @ k[b, kh, :L].T)", "z = (Q @ k[b, kh, :L].T)", "mass logits without alpha"),
+    ("select", "A = e / e.sum(axis=1, keepdims=True)                  # softmax over the L keys",
+     "A = e / e.sum(axis=0, keepdims=True)                  # softmax over the L keys",
+     "mass normalised over the rows"),
+    ("select", "Q = q[b, kh * g:(kh + 1) * g].reshape(g * T, d)", "Q = q[b, kh::HKV].reshape(g * T, d)",
+     "mass GQA grouping strided"),
     ("attention", "a = 1.0 / math.sqrt(d) if alpha is None else alpha",
      "a = 1.0 / d if alpha is None else alpha", "alpha = 1/d"),
     ("attention", "K[:, :, :P, :] = np.where(keep[..., None], K[:, :, :P, :], Kq)",

@@ -1,5 +1,8 @@
 """Pins for the oracle's vertical-line token identification (Eq. 4-5, Algorithm 1)."""
+import math
+
 import numpy as np
+import torch
 import pytest
 
 from gen import decode_case
@@ -130,3 +133,98 @@ def test_error_bound_covers_float32_evaluation():
     S = scores(proxy_sum(c.q_proxy.double().numpy(), 8), c.k.double().numpy(), P)
     bnd = score_error_bound(c.q_proxy.double().numpy(), c.k.double().numpy(), P)
     assert np.all(np.abs(S32 - S) <= bnd)
+
+
+# --- Eq. 4: the softmax-mass score ------------------------------------------
+
+def _mass_brute(q, k, L, W):
+    """Pure-Python Eq. 4 on a tiny case: per (b, kvh), per proxy row of every
+    query head of the group, a softmax over the L keys, summed per key."""
+    B, HQ, T, d = q.shape
+    HKV = k.shape[1]
+    g = HQ // HKV
+    P = max(0, L - W)
+    out = np.zeros((B, HKV, P))
+    for b in range(B):
+        for kh in range(HKV):
+            for h in range(kh * g, (kh + 1) * g):
+                for t in range(T):
+                    z = [sum(q[b, h, t, i] * k[b, kh, j, i] for i in range(d)) / math.sqrt(d) for j in range(L)]
+                    m = max(z)
+                    e = [math.exp(x - m) for x in z]
+                    tot = sum(e)
+                    for j in range(P):
+                        out[b, kh, j] += e[j] / tot
+    return out
+
+
+def test_mass_scores_brute_force_gqa():
+    from oracle.select import mass_scores
+    rng = np.random.default_rng(41)
+    q = rng.standard_normal((2, 4, 3, 8))
+    k = rng.standard_normal((2, 2, 11, 8)) * 2
+    np.testing.assert_allclose(mass_scores(q, k, 11, 4), _mass_brute(q, k, 11, 4), rtol=1e-12, atol=1e-14)
+
+
+def test_mass_scores_sum_to_rows_without_window():
+    """Each row's probabilities sum to one, so with W = 0 the column masses
+    of a KV head sum to the number of (proxy, query head) rows."""
+    from oracle.select import mass_scores
+    rng = np.random.default_rng(42)
+    q = rng.standard_normal((1, 6, 5, 16)) * 3
+    k = rng.standard_normal((1, 2, 40, 16))
+    S = mass_scores(q, k, 40, 0)
+    np.testing.assert_allclose(S.sum(axis=-1), 3 * 5, rtol=1e-12)
+    assert np.all(S > 0)
+
+
+def test_mass_scores_shift_invariant():
+    """Adding one vector to every key shifts each row's logits by a constant:
+    the softmax, hence the score, is unchanged."""
+    from oracle.select import mass_scores
+    rng = np.random.default_rng(43)
+    q = rng.standard_normal((1, 2, 4, 16))
+    k = rng.standard_normal((1, 1, 30, 16))
+    shifted = k + rng.standard_normal(16)[None, None, None, :] * 5
+    np.testing.assert_allclose(mass_scores(q, shifted, 30, 6), mass_scores(q, k, 30, 6), rtol=1e-10)
+
+
+def test_mass_planted_key_takes_the_mass():
+    from oracle.select import mass_scores, select_vertical_mass
+    rng = np.random.default_rng(44)
+    u = rng.standard_normal(32)
+    u /= np.linalg.norm(u)
+    q = 0.3 * rng.standard_normal((1, 2, 8, 32)) + 3 * u     # every proxy row leans along u
+    k = rng.standard_normal((1, 1, 50, 32)) * 0.1
+    k[0, 0, 17] = 40 * u
+    S = mass_scores(q, k, 50, 10)
+    assert S[0, 0, 17] > 0.99 * 16
+    idx, _ = select_vertical_mass(q, k, 50, 10, 50_000)
+    assert 17 in idx[0, 0]
+
+
+def test_mass_error_bound_covers_a_float32_evaluation():
+    """A float32 evaluation in the bound's own recipe (float32 dot products
+    of BF16-valued inputs, a scaled logit, row maximum and sum of exp2, the
+    quotient and a float32 column sum) stays inside the bound."""
+    from oracle.select import mass_error_bound, mass_scores
+    rng = np.random.default_rng(45)
+    to_bf16 = lambda x: torch.from_numpy(x).to(torch.bfloat16).double().numpy()
+    q = to_bf16(rng.standard_normal((1, 4, 16, 128)))
+    k = to_bf16(rng.standard_normal((1, 2, 700, 128)))
+    L, W = 700, 128
+    S = mass_scores(q, k, L, W)
+    bnd = mass_error_bound(q, k, L, W)
+    c = np.float32(1.0 / np.sqrt(128) / np.log(2.0))
+    P = L - W
+    for kh in range(2):
+        Q = q[0, 2 * kh:2 * kh + 2].reshape(32, 128).astype(np.float32)
+        K = k[0, kh, :L].astype(np.float32)
+        t = (Q @ K.T).astype(np.float32) * c
+        m = t.max(axis=1, keepdims=True)
+        p = np.exp2(t - m).astype(np.float32)
+        a = (p / p.sum(axis=1, keepdims=True, dtype=np.float32)).astype(np.float32)
+        S32 = a[:, :P].sum(axis=0, dtype=np.float32)
+        err = np.abs(S32.astype(np.float64) - S[0, kh])
+        assert np.all(err <= bnd[0, kh]), float((err - bnd[0, kh]).max())
+        assert bnd[0, kh].max() < 1e-3 * S[0, kh].max()   # tight enough to decide most keys
