@@ -30,7 +30,7 @@ QBLOCK_BYTES = 10240
 COUNTS = 8
 CNT_NQ, CNT_NVL, CNT_NTAIL, CNT_LEN, CNT_RING_N, CNT_RING_POS = range(6)
 LAYOUT_FIELDS = ("qblocks", "vl_k", "vl_v", "vl_idx", "tail_k", "tail_v", "q_ring", "counts", "err")
-OP_SELECT, OP_DECODE, OP_PREFILL = 1, 2, 3
+OP_SELECT, OP_DECODE, OP_PREFILL, OP_SELECT_MASS = 1, 2, 3, 4
 PREFILL_INT8, PREFILL_FP8 = 1, 2
 
 # Every symbol include/hyq.h declares.
@@ -39,7 +39,7 @@ SYMBOLS = ("hyq_status_string", "hyq_config_check", "hyq_vl_count", "hyq_layout_
            "hyq_select_vertical", "hyq_rebuild", "hyq_decode_append", "hyq_decode_attention",
            "hyq_decode_attention_noalloc", "hyq_read_device_error", "hyq_set_decode_plan",
            "hyq_prefill_attention", "hyq_decode_step", "hyq_set_decode_overlap",
-           "hyq_decode_step_prefetch", "hyq_age_tail")
+           "hyq_decode_step_prefetch", "hyq_age_tail", "hyq_select_vertical_mass")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -86,6 +86,8 @@ def load() -> ctypes.CDLL:
         "hyq_quantize_append": (c_int32, [P(HyqConfig), c_void_p, c_void_p, c_int32, P(HyqLayout), c_void_p]),
         "hyq_select_vertical": (c_int32, [P(HyqConfig), c_void_p, c_int32, c_int32, c_void_p, c_int32,
                                           c_int32, c_void_p, P(c_int32), c_void_p, c_size_t, c_void_p]),
+        "hyq_select_vertical_mass": (c_int32, [P(HyqConfig), c_void_p, c_int32, c_int32, c_void_p, c_int32,
+                                               c_int32, c_void_p, P(c_int32), c_void_p, c_size_t, c_void_p]),
         "hyq_rebuild": (c_int32, [P(HyqConfig), c_void_p, c_void_p, c_int32, c_int32, c_void_p, c_int32,
                                   P(HyqLayout), c_void_p]),
         "hyq_decode_append": (c_int32, [P(HyqConfig), c_void_p, c_void_p, c_void_p, P(HyqLayout),
@@ -178,6 +180,16 @@ def hyq_select_vertical(cfg, q_proxy, n_proxy: int, k_src, L: int, idx_out, ws, 
     k_src [B, HKV, ld, 128]; idx_out int32 [B, HKV, k] contiguous."""
     k_out = c_int32(0)
     _check("hyq_select_vertical", load().hyq_select_vertical(
+        ctypes.byref(cfg), ptr(q_proxy), n_proxy, row_ld(q_proxy), ptr(k_src), row_ld(k_src), L,
+        ptr(idx_out), ctypes.byref(k_out), ptr(ws), ws.numel() * ws.element_size(), stream_ptr(stream)))
+    return k_out.value
+
+
+def hyq_select_vertical_mass(cfg, q_proxy, n_proxy: int, k_src, L: int, idx_out, ws, stream=None) -> int:
+    """As hyq_select_vertical with the softmax-mass score of Eq. 4; the
+    workspace is workspace(cfg, OP_SELECT_MASS, L)."""
+    k_out = c_int32(0)
+    _check("hyq_select_vertical_mass", load().hyq_select_vertical_mass(
         ctypes.byref(cfg), ptr(q_proxy), n_proxy, row_ld(q_proxy), ptr(k_src), row_ld(k_src), L,
         ptr(idx_out), ctypes.byref(k_out), ptr(ws), ws.numel() * ws.element_size(), stream_ptr(stream)))
     return k_out.value

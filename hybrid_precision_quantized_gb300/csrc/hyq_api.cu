@@ -104,6 +104,7 @@ extern "C" size_t hyq_workspace_size(const hyq_config* c, int op, int32_t len_hi
   if (len_hint == 0 || len_hint > c->capacity) len_hint = c->capacity;
   switch (op) {
     case HYQ_OP_SELECT: return hyq_select_ws_bytes(c, len_hint);
+    case HYQ_OP_SELECT_MASS: return hyq_select_mass_ws_bytes(c, len_hint);
     case HYQ_OP_DECODE: return hyq_decode_ws_bytes(c, len_hint);
     case HYQ_OP_PREFILL: return hyq_prefill_ws_bytes_hint(c, len_hint);
     default: return 0;
@@ -156,6 +157,26 @@ extern "C" hyq_status hyq_select_vertical(const hyq_config* c, const void* q_pro
   if (n_proxy < 1) return HYQ_ERR_INVALID_ARG;
   if (!ws || !aligned(ws, kAlign) || ws_bytes < hyq_select_ws_bytes(c, L)) return HYQ_ERR_WORKSPACE;
   return from_cuda(hyq_launch_select(c, q_proxy, n_proxy, n_proxy_ld, k_src, ld, L, idx_out, k, ws, s));
+}
+
+extern "C" hyq_status hyq_select_vertical_mass(const hyq_config* c, const void* q_proxy, int32_t n_proxy,
+                                               int32_t n_proxy_ld, const void* k_src, int32_t ld, int32_t L,
+                                               int32_t* idx_out, int32_t* k_out, void* ws, size_t ws_bytes,
+                                               hyq_stream_t s) {
+  hyq_status st = hyq_config_check(c);
+  if (st != HYQ_OK) return st;
+  if (!k_out) return HYQ_ERR_INVALID_ARG;
+  if (L < 0 || L > c->capacity) return HYQ_ERR_CAPACITY;
+  if (ld < L || ld < 1 || n_proxy < 0 || n_proxy_ld < n_proxy || n_proxy > c->period) return HYQ_ERR_INVALID_ARG;
+  int32_t P = L - c->window > 0 ? L - c->window : 0;
+  int32_t k = hyq_vl_count(c, P);
+  *k_out = k;
+  if (k == 0) return HYQ_OK;
+  if (!q_proxy || !k_src || !idx_out || !aligned(k_src, 16) || !aligned(q_proxy, 16))
+    return HYQ_ERR_INVALID_ARG;
+  if (n_proxy < 1) return HYQ_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, kAlign) || ws_bytes < hyq_select_mass_ws_bytes(c, L)) return HYQ_ERR_WORKSPACE;
+  return from_cuda(hyq_launch_select_mass(c, q_proxy, n_proxy, n_proxy_ld, k_src, ld, L, idx_out, k, ws, s));
 }
 
 extern "C" hyq_status hyq_rebuild(const hyq_config* c, const void* k_src, const void* v_src,

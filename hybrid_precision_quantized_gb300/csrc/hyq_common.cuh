@@ -39,6 +39,10 @@ cudaError_t hyq_launch_select(const hyq_config* c, const void* q_proxy, int32_t 
                               int32_t n_proxy_ld, const void* k_src, int32_t ld, int32_t L,
                               int32_t* idx_out, int32_t k, void* ws, cudaStream_t s);
 size_t hyq_select_ws_bytes(const hyq_config* c, int32_t L);
+size_t hyq_select_mass_ws_bytes(const hyq_config* c, int32_t L);
+cudaError_t hyq_launch_select_mass(const hyq_config* c, const void* q_proxy, int32_t n_proxy,
+                                   int32_t n_proxy_ld, const void* k_src, int32_t ld, int32_t L,
+                                   int32_t* idx_out, int32_t k, void* ws, cudaStream_t s);
 cudaError_t hyq_launch_decode_append(const hyq_config* c, const void* q, const void* k_new,
                                      const void* v_new, const hyq_layout* lay, void* k_src,
                                      void* v_src, int32_t ld, cudaStream_t s);

@@ -9,6 +9,9 @@
 // radix select + ordered compaction (one CTA per KV head).
 #include <cooperative_groups.h>
 
+#include <algorithm>
+#include <cmath>
+
 #include "hyq_common.cuh"
 
 namespace {
@@ -400,6 +403,272 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkCtaT
   cl.barrier_wait();  // no block leaves while another may still read its counts
 }
 
+// ---------------------------------------------------------------------------
+// Eq. 4: the softmax-mass score S(j) = sum_r softmax_j(alpha q_r . k_j) over
+// the rows r = (query head i of the group, proxy t), r = i * n_proxy + t,
+// the softmax taken over the L current keys and S kept for j < P.
+// Pass 1 (mass_stats_kernel): per key split (at most 32), each row's running maximum m
+// and sum l of 2^(t - m), t = fl(z c), z = q_r . k_j (exact BF16 products,
+// float32 accumulation on the tensor cores), c = alpha log2 e.  Merge
+// (mass_merge_kernel): m = max over splits, l = sum_s l_s 2^(m_s - m), and
+// 1/l.  Pass 2 (mass_colsum_kernel): per 64-key tile of [0, P), the column
+// sums of 2^(t - m) (1/l) over a group of at most 256 rows.  Final
+// (mass_keys_kernel): the row groups' sums in a fixed order, as the
+// order-preserving keys of the top-k kernels.
+constexpr int kMassThreads = 256;     // 8 warps, each two 16-row blocks of a row group
+constexpr int kMassGroupRows = 256;
+constexpr int kMassKeys = 64;         // keys per tile (8 MMA n-blocks)
+constexpr int kMassStride = 136;      // bf16 per staged row: 272 bytes, conflict-free fragment loads
+constexpr int kMassSplits = 32;       // most key splits of pass 1 per (sequence, KV head, row group)
+
+__device__ __forceinline__ float mass_ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Stage the query rows [rg * 256, +256) of the group into shared memory
+// (stride kMassStride); rows past R are zero.
+__device__ void mass_stage_q(__nv_bfloat16* qs, const __nv_bfloat16* qp, int b, int h, int HKV, int gq,
+                             int n_proxy, int n_ld, int R, int rg) {
+  for (int i = threadIdx.x; i < kMassGroupRows * 16; i += kMassThreads) {
+    const int lr = i >> 4, c = i & 15, r = rg * kMassGroupRows + lr;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (r < R) {
+      const int hi = r / n_proxy, t = r - hi * n_proxy;
+      v = __ldg(reinterpret_cast<const uint4*>(qp + (((size_t)b * HKV * gq + (size_t)h * gq + hi) * n_ld + t) * HYQ_D) + c);
+    }
+    *reinterpret_cast<uint4*>(qs + lr * kMassStride + 8 * c) = v;
+  }
+}
+
+// Stage key rows [j0, j0 + 64) of (b, h), zero past `end`.
+__device__ void mass_stage_k(__nv_bfloat16* ks, const __nv_bfloat16* kb, int j0, int end) {
+  for (int i = threadIdx.x; i < kMassKeys * 16; i += kMassThreads) {
+    const int r = i >> 4, c = i & 15;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (j0 + r < end) v = __ldg(reinterpret_cast<const uint4*>(kb + (size_t)(j0 + r) * HYQ_D) + c);
+    *reinterpret_cast<uint4*>(ks + r * kMassStride + 8 * c) = v;
+  }
+}
+
+// A fragments (m16n8k16, row-major 16 x 128) of the 16-row block rb.
+__device__ __forceinline__ void mass_load_a(const __nv_bfloat16* qs, int rb, int lane, uint32_t (&a)[8][4]) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    const uint32_t* r0 = reinterpret_cast<const uint32_t*>(qs + (16 * rb + g) * kMassStride + 16 * ks + 2 * t);
+    const uint32_t* r8 = reinterpret_cast<const uint32_t*>(qs + (16 * rb + g + 8) * kMassStride + 16 * ks + 2 * t);
+    a[ks][0] = r0[0];
+    a[ks][1] = r8[0];
+    a[ks][2] = r0[4];
+    a[ks][3] = r8[4];
+  }
+}
+
+// z = Q K^T for the warp's two row blocks and the staged 64-key tile:
+// C[blk][nb][i] is row 16 rb + g + 8 (i >> 1), key 8 nb + 2 t + (i & 1).
+__device__ __forceinline__ void mass_tile(const __nv_bfloat16* ksm, int lane, const uint32_t (&a0)[8][4],
+                                          const uint32_t (&a1)[8][4], float (&C)[2][8][4]) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int blk = 0; blk < 2; ++blk)
+#pragma unroll
+    for (int nb = 0; nb < 8; ++nb) C[blk][nb][0] = C[blk][nb][1] = C[blk][nb][2] = C[blk][nb][3] = 0.f;
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks)
+#pragma unroll
+    for (int nb = 0; nb < 8; ++nb) {
+      const uint32_t* kr = reinterpret_cast<const uint32_t*>(ksm + (8 * nb + g) * kMassStride + 16 * ks + 2 * t);
+      const uint32_t b0 = kr[0], b1 = kr[4];
+      mma_bf16(C[0][nb], a0[ks], b0, b1);
+      mma_bf16(C[1][nb], a1[ks], b0, b1);
+    }
+}
+
+// Pass 1.  grid (splits <= kMassSplits, HKV * n_groups, B); dynamic smem: the row
+// group's queries and one key tile.  part[((bh * n_groups + rg) *
+// kMassSplits + split) * 256 + row] = (m, l) of the split's keys.
+__global__ void __launch_bounds__(kMassThreads) mass_stats_kernel(
+    const __nv_bfloat16* __restrict__ qp, int32_t n_proxy, int32_t n_ld, int32_t gq,
+    const __nv_bfloat16* __restrict__ k_src, int32_t ld, int32_t L, float c, int32_t R, int32_t n_groups,
+    float2* __restrict__ part) {
+  extern __shared__ __align__(16) unsigned char mass_smem[];
+  __nv_bfloat16* qs = reinterpret_cast<__nv_bfloat16*>(mass_smem);
+  __nv_bfloat16* ksm = qs + kMassGroupRows * kMassStride;
+  const int split = blockIdx.x, HKV = gridDim.y / n_groups, h = blockIdx.y / n_groups, rg = blockIdx.y % n_groups;
+  const int b = blockIdx.z;
+  const size_t bh = (size_t)b * HKV + h;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t = lane & 3;
+  mass_stage_q(qs, qp, b, h, HKV, gq, n_proxy, n_ld, R, rg);
+  __syncthreads();
+  uint32_t a0[8][4], a1[8][4];
+  mass_load_a(qs, 2 * warp, lane, a0);
+  mass_load_a(qs, 2 * warp + 1, lane, a1);
+  // rows (blk, half): 16 (2 warp + blk) + g + 8 half
+  float m[2][2], l[2][2];
+#pragma unroll
+  for (int blk = 0; blk < 2; ++blk) m[blk][0] = m[blk][1] = -INFINITY, l[blk][0] = l[blk][1] = 0.f;
+  const int ns = gridDim.x;
+  const int j0 = (int)((int64_t)split * L / ns), j1 = (int)((int64_t)(split + 1) * L / ns);
+  const __nv_bfloat16* kb = k_src + bh * ld * HYQ_D;
+  for (int kt = j0; kt < j1; kt += kMassKeys) {
+    __syncthreads();  // the previous tile is consumed
+    mass_stage_k(ksm, kb, kt, j1);
+    __syncthreads();
+    float C[2][8][4];
+    mass_tile(ksm, lane, a0, a1, C);
+    const int nvalid = min(kMassKeys, j1 - kt);
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        float v[16];
+        float tm = -INFINITY;
+#pragma unroll
+        for (int nb = 0; nb < 8; ++nb)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int key = 8 * nb + 2 * t + e;
+            const float x = key < nvalid ? C[blk][nb][2 * hf + e] * c : -INFINITY;
+            v[2 * nb + e] = x;
+            tm = fmaxf(tm, x);
+          }
+        tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 1));
+        tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 2));
+        const float mn = fmaxf(m[blk][hf], tm);
+        float sum = 0.f;
+        if (mn != -INFINITY) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) sum += mass_ex2(v[i] - mn);
+        }
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        if (mn != -INFINITY) {
+          l[blk][hf] = l[blk][hf] * mass_ex2(m[blk][hf] - mn) + sum;
+          m[blk][hf] = mn;
+        }
+      }
+  }
+  if (t == 0) {
+    float2* out = part + ((bh * n_groups + rg) * kMassSplits + split) * kMassGroupRows;
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) out[16 * (2 * warp + blk) + (lane >> 2) + 8 * hf] = make_float2(m[blk][hf], l[blk][hf]);
+  }
+}
+
+// Merge.  grid (HKV * n_groups, B), 256 threads (one row each):
+// stats = (m, 1/l) over all splits; padding rows (past R) get weight 0.
+__global__ void __launch_bounds__(kMassGroupRows) mass_merge_kernel(const float2* __restrict__ part,
+                                                                    float2* __restrict__ stats, int32_t R,
+                                                                    int32_t n_groups, int32_t ns) {
+  const size_t bg = (size_t)blockIdx.y * gridDim.x + blockIdx.x;  // (bh, rg) flattened
+  const int r = threadIdx.x;
+  if ((int)(blockIdx.x % n_groups) * kMassGroupRows + r >= R) {
+    stats[bg * kMassGroupRows + r] = make_float2(0.f, 0.f);
+    return;
+  }
+  const float2* p = part + bg * kMassSplits * kMassGroupRows + r;
+  float m = -INFINITY;
+  for (int s = 0; s < ns; ++s) m = fmaxf(m, p[s * kMassGroupRows].x);
+  float l = 0.f;
+  if (m != -INFINITY) {
+    for (int s = 0; s < ns; ++s) {
+      const float2 v = p[s * kMassGroupRows];
+      if (v.x != -INFINITY) l += v.y * mass_ex2(v.x - m);
+    }
+  }
+  stats[bg * kMassGroupRows + r] = make_float2(m == -INFINITY ? 0.f : m, l > 0.f ? __frcp_rn(l) : 0.f);
+}
+
+// Pass 2.  grid (blocks, HKV * n_groups, B), block x taking the 64-key tiles
+// x, x + blocks, ... of [0, P): the row group's column sums of 2^(t - m) / l,
+// in a fixed order.
+// colsum[((bh * n_groups + rg) * pmax + j].
+__global__ void __launch_bounds__(kMassThreads) mass_colsum_kernel(
+    const __nv_bfloat16* __restrict__ qp, int32_t n_proxy, int32_t n_ld, int32_t gq,
+    const __nv_bfloat16* __restrict__ k_src, int32_t ld, int32_t P, float c, int32_t R, int32_t n_groups,
+    const float2* __restrict__ stats, float* __restrict__ colsum, int32_t pmax) {
+  extern __shared__ __align__(16) unsigned char mass_smem[];
+  __nv_bfloat16* qs = reinterpret_cast<__nv_bfloat16*>(mass_smem);
+  __nv_bfloat16* ksm = qs + kMassGroupRows * kMassStride;
+  float* red = reinterpret_cast<float*>(ksm + kMassKeys * kMassStride);  // [8 warps][64 keys]
+  const int HKV = gridDim.y / n_groups, h = blockIdx.y / n_groups, rg = blockIdx.y % n_groups;
+  const int b = blockIdx.z;
+  const size_t bh = (size_t)b * HKV + h, bg = bh * n_groups + rg;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  mass_stage_q(qs, qp, b, h, HKV, gq, n_proxy, n_ld, R, rg);
+  __syncthreads();
+  uint32_t a0[8][4], a1[8][4];
+  mass_load_a(qs, 2 * warp, lane, a0);
+  mass_load_a(qs, 2 * warp + 1, lane, a1);
+  float2 st[2][2];  // this thread's rows: (m, 1/l)
+#pragma unroll
+  for (int blk = 0; blk < 2; ++blk)
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) st[blk][hf] = stats[bg * kMassGroupRows + 16 * (2 * warp + blk) + g + 8 * hf];
+  for (int kt = blockIdx.x * kMassKeys; kt < P; kt += gridDim.x * kMassKeys) {
+  __syncthreads();  // the previous tile's key rows and sums are consumed
+  mass_stage_k(ksm, k_src + bh * ld * HYQ_D, kt, P);
+  __syncthreads();
+  float C[2][8][4];
+  mass_tile(ksm, lane, a0, a1, C);
+  float cs[8][2];
+#pragma unroll
+  for (int nb = 0; nb < 8; ++nb) cs[nb][0] = cs[nb][1] = 0.f;
+#pragma unroll
+  for (int blk = 0; blk < 2; ++blk)
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf)  // rows past R have 1/l = 0
+#pragma unroll
+      for (int nb = 0; nb < 8; ++nb)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+          cs[nb][e] += mass_ex2(C[blk][nb][2 * hf + e] * c - st[blk][hf].x) * st[blk][hf].y;
+#pragma unroll
+  for (int nb = 0; nb < 8; ++nb)
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) cs[nb][e] += __shfl_xor_sync(0xffffffffu, cs[nb][e], o);
+  if (g == 0) {
+#pragma unroll
+    for (int nb = 0; nb < 8; ++nb)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) red[warp * kMassKeys + 8 * nb + 2 * t + e] = cs[nb][e];
+  }
+  __syncthreads();
+  if (threadIdx.x < kMassKeys && kt + (int)threadIdx.x < P) {
+    float S = 0.f;
+#pragma unroll
+    for (int w = 0; w < kMassThreads / 32; ++w) S += red[w * kMassKeys + threadIdx.x];
+    colsum[bg * pmax + kt + threadIdx.x] = S;
+  }
+  }
+}
+
+// Final.  grid (ceil(P / 256), HKV, B): S(j) = sum over row groups (fixed
+// order) -> order-preserving key.
+__global__ void mass_keys_kernel(const float* __restrict__ colsum, int32_t n_groups, int32_t P, int32_t pmax,
+                                 uint32_t* __restrict__ keys, int32_t* err) {
+  const size_t bh = (size_t)blockIdx.z * gridDim.y + blockIdx.y;
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= P) return;
+  float S = 0.f;
+  for (int rg = 0; rg < n_groups; ++rg) S += colsum[(bh * n_groups + rg) * pmax + j];
+  keys[bh * pmax + j] = order_key(S, err);
+}
+
 }  // namespace
 
 size_t hyq_select_ws_bytes(const hyq_config* c, int32_t L) {
@@ -408,21 +677,35 @@ size_t hyq_select_ws_bytes(const hyq_config* c, int32_t L) {
   return 256 + round_up(bh * HYQ_D * 4) + round_up(bh * (size_t)(P > 0 ? P : 1) * 4);
 }
 
-cudaError_t hyq_launch_select(const hyq_config* c, const void* q_proxy, int32_t n_proxy,
-                              int32_t n_proxy_ld, const void* k_src, int32_t ld, int32_t L,
-                              int32_t* idx_out, int32_t k, void* ws, cudaStream_t s) {
-  SelectWs w = carve(c, L, ws);
-  const int32_t P = L - c->window;  // > 0 since k > 0
-  const int32_t gq = c->num_q_heads / c->num_kv_heads;
-  proxy_sum_kernel<<<dim3(c->num_kv_heads, c->batch), kProxyThreads, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(q_proxy), n_proxy, n_proxy_ld, gq, w.u);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  dim3 g2((P + kScoreRowsPerCta - 1) / kScoreRowsPerCta, c->num_kv_heads, c->batch);
-  score_kernel<<<g2, kScoreThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(k_src), ld, P, w.u,
-                                            w.keys, P, w.err);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+namespace {
+
+// Row groups of the mass score for n_proxy proxy rows per query head.
+int32_t mass_groups(const hyq_config* c, int32_t n_proxy) {
+  const int32_t R = c->num_q_heads / c->num_kv_heads * n_proxy;
+  return (R + kMassGroupRows - 1) / kMassGroupRows;
+}
+
+struct MassWs {
+  float2* part;    // [bh][groups][kMassSplits][256]
+  float2* stats;   // [bh][groups][256]
+  float* colsum;   // [bh][groups][P]
+};
+
+MassWs carve_mass(const hyq_config* c, int32_t L, void* ws) {
+  const size_t bh = (size_t)c->batch * c->num_kv_heads;
+  const size_t ng = (size_t)mass_groups(c, c->period);
+  char* p = static_cast<char*>(ws) + hyq_select_ws_bytes(c, L);
+  MassWs w;
+  w.part = reinterpret_cast<float2*>(p);
+  p += round_up(bh * ng * kMassSplits * kMassGroupRows * sizeof(float2));
+  w.stats = reinterpret_cast<float2*>(p);
+  p += round_up(bh * ng * kMassGroupRows * sizeof(float2));
+  w.colsum = reinterpret_cast<float*>(p);
+  return w;
+}
+
+cudaError_t launch_topk(const hyq_config* c, const SelectWs& w, int32_t P, int32_t k, int32_t* idx_out,
+                        cudaStream_t s) {
   const int32_t cap = kTopkCluster * kTopkCtaThreads;
   dim3 gc(kTopkCluster, c->num_kv_heads, c->batch);
   if (P <= 4 * cap) {
@@ -447,4 +730,82 @@ cudaError_t hyq_launch_select(const hyq_config* c, const void* q_proxy, int32_t 
   const size_t tk_smem = P <= kTopkSmemKeys ? (size_t)P * sizeof(uint32_t) : 0;
   topk_kernel<<<dim3(c->num_kv_heads, c->batch), kTopkThreads, tk_smem, s>>>(w.keys, P, P, k, idx_out);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t hyq_select_mass_ws_bytes(const hyq_config* c, int32_t L) {
+  const size_t bh = (size_t)c->batch * c->num_kv_heads;
+  const size_t ng = (size_t)mass_groups(c, c->period);
+  int32_t P = L - c->window > 0 ? L - c->window : 0;
+  return hyq_select_ws_bytes(c, L) + round_up(bh * ng * kMassSplits * kMassGroupRows * sizeof(float2)) +
+         round_up(bh * ng * kMassGroupRows * sizeof(float2)) + round_up(bh * ng * (size_t)(P > 0 ? P : 1) * 4);
+}
+
+cudaError_t hyq_launch_select(const hyq_config* c, const void* q_proxy, int32_t n_proxy,
+                              int32_t n_proxy_ld, const void* k_src, int32_t ld, int32_t L,
+                              int32_t* idx_out, int32_t k, void* ws, cudaStream_t s) {
+  SelectWs w = carve(c, L, ws);
+  const int32_t P = L - c->window;  // > 0 since k > 0
+  const int32_t gq = c->num_q_heads / c->num_kv_heads;
+  proxy_sum_kernel<<<dim3(c->num_kv_heads, c->batch), kProxyThreads, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(q_proxy), n_proxy, n_proxy_ld, gq, w.u);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  dim3 g2((P + kScoreRowsPerCta - 1) / kScoreRowsPerCta, c->num_kv_heads, c->batch);
+  score_kernel<<<g2, kScoreThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(k_src), ld, P, w.u,
+                                            w.keys, P, w.err);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_topk(c, w, P, k, idx_out, s);
+}
+
+cudaError_t hyq_launch_select_mass(const hyq_config* c, const void* q_proxy, int32_t n_proxy,
+                                   int32_t n_proxy_ld, const void* k_src, int32_t ld, int32_t L,
+                                   int32_t* idx_out, int32_t k, void* ws, cudaStream_t s) {
+  SelectWs w = carve(c, L, ws);
+  MassWs mw = carve_mass(c, L, ws);
+  const int32_t P = L - c->window;  // > 0 since k > 0
+  const int32_t gq = c->num_q_heads / c->num_kv_heads, R = gq * n_proxy, ng = mass_groups(c, n_proxy);
+  const float cs = (float)(1.0 / std::sqrt((double)HYQ_D) / std::log(2.0));  // fl(alpha log2 e)
+  const int smem_stats = (kMassGroupRows + kMassKeys) * kMassStride * 2;
+  const int smem_col = smem_stats + (kMassThreads / 32) * kMassKeys * 4;
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(mass_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_stats);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(mass_colsum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_col);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  static int n_sm = 0;
+  if (n_sm == 0) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+  }
+  // one block per SM for pass 1 (one fits an SM) and two per SM for pass 2
+  const int units = c->num_kv_heads * ng * c->batch;
+  const int ns = std::min(kMassSplits, std::max(1, (n_sm + units - 1) / units));
+  const int ntiles = (P + kMassKeys - 1) / kMassKeys;
+  const int ncol = std::min(ntiles, std::max(1, (2 * n_sm + units - 1) / units));
+  const __nv_bfloat16* qp = static_cast<const __nv_bfloat16*>(q_proxy);
+  const __nv_bfloat16* kk = static_cast<const __nv_bfloat16*>(k_src);
+  mass_stats_kernel<<<dim3(ns, c->num_kv_heads * ng, c->batch), kMassThreads, smem_stats, s>>>(
+      qp, n_proxy, n_proxy_ld, gq, kk, ld, L, cs, R, ng, mw.part);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  mass_merge_kernel<<<dim3(c->num_kv_heads * ng, c->batch), kMassGroupRows, 0, s>>>(mw.part, mw.stats, R, ng,
+                                                                                    ns);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  mass_colsum_kernel<<<dim3(ncol, c->num_kv_heads * ng, c->batch), kMassThreads, smem_col, s>>>(qp, n_proxy, n_proxy_ld, gq, kk, ld, P, cs, R, ng, mw.stats, mw.colsum, P);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  mass_keys_kernel<<<dim3((P + 255) / 256, c->num_kv_heads, c->batch), 256, 0, s>>>(mw.colsum, ng, P, P, w.keys,
+                                                                                   w.err);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_topk(c, w, P, k, idx_out, s);
 }

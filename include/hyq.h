@@ -140,6 +140,7 @@ typedef struct {
 #define HYQ_OP_SELECT 1
 #define HYQ_OP_DECODE 2
 #define HYQ_OP_PREFILL 3
+#define HYQ_OP_SELECT_MASS 4
 
 #define HYQ_PREFILL_INT8 1
 #define HYQ_PREFILL_FP8 2
@@ -216,6 +217,26 @@ hyq_status hyq_select_vertical(const hyq_config *cfg, const void *q_proxy, int32
                                int32_t n_proxy_ld, const void *k_src, int32_t ld, int32_t L,
                                int32_t *idx_out, int32_t *k_out, void *ws, size_t ws_bytes,
                                hyq_stream_t stream);
+
+/*
+ * Vertical-line identification with the score of Eq. 4 (§4.1): the
+ * accumulated column mass of the attention probabilities instead of
+ * Algorithm 1's summed logits.  Same arguments and output as
+ * hyq_select_vertical, and n_proxy <= cfg->period.  Per KV head, with the
+ * rows r = (query head i of the group, proxy t) and alpha = 1/sqrt(d):
+ *   a_rj = softmax over the L keys j < L of alpha q_r . k_j
+ *   S(j) = sum_r a_rj for j < P = max(0, L - W)
+ * then the k positions with the largest S, ties to the lower position.
+ * Evaluated in float32 from exact BF16 products on the tensor cores: per
+ * row the maximum m and the sum l of 2^(t - m), t = (q_r . k_j) fl(alpha
+ * log2 e), over at most 32 key ranges merged once, then S(j) = sum_r 2^(t - m) / l;
+ * a NaN score sets HYQ_DEVERR_SCORE in the workspace's error word.
+ * Workspace: hyq_workspace_size(cfg, HYQ_OP_SELECT_MASS, L).  Five launches.
+ */
+hyq_status hyq_select_vertical_mass(const hyq_config *cfg, const void *q_proxy, int32_t n_proxy,
+                                    int32_t n_proxy_ld, const void *k_src, int32_t ld, int32_t L,
+                                    int32_t *idx_out, int32_t *k_out, void *ws, size_t ws_bytes,
+                                    hyq_stream_t stream);
 
 /*
  * Build a layer's hybrid cache for context length L (Algorithm 4, with the

@@ -139,3 +139,80 @@ def test_select_qwen32b_shaped_sweep(hyq, ppm, W):
     c = decode_case(1004, 4, 64, 8, Lc, window=W, n_proxy=64, sink_frac=0.02, heavy_tail=True)
     got = run_select(c, Lc, W, ppm)
     check(c, got, Lc, W, ppm)
+
+
+# --- Eq. 4: the softmax-mass score ------------------------------------------
+
+def run_select_mass(c, Lc, W, ppm, n_proxy=None, capacity=None):
+    from hybrid_precision_quantized_gb300 import hyq_select_vertical_mass
+    B, HQ = c.q.shape[:2]
+    HKV = c.k.shape[1]
+    cfg = make_config(B, HQ, HKV, capacity=capacity or Lc, window=W, rho_ppm=ppm)
+    ws = workspace(cfg, L.OP_SELECT_MASS, Lc)
+    k = vl_count(prefix_len(Lc, W), ppm)
+    idx = torch.full((B, HKV, max(k, 1)), -1, dtype=torch.int32, device="cuda")
+    qp = c.q_proxy.cuda()
+    n = qp.shape[2] if n_proxy is None else n_proxy
+    kk = hyq_select_vertical_mass(cfg, qp, n, c.k.cuda(), Lc, idx, ws)
+    torch.cuda.synchronize()
+    assert kk == k
+    assert hyq_read_device_error(ws[:4].view(torch.int32)) == 0
+    return idx[..., :k].cpu().numpy()
+
+
+def check_mass(c, got, Lc, W, ppm, n_proxy=None, require_exact=True):
+    from oracle.select import mass_error_bound, select_vertical_mass
+    qp = c.q_proxy.double().numpy()
+    if n_proxy is not None:
+        qp = qp[:, :, :n_proxy]
+    k_np = c.k.double().numpy()
+    want, S = select_vertical_mass(qp, k_np, Lc, W, ppm)
+    # per row at most L / 64 tile rescales plus 16 split merges, each counted
+    # generously as a few float32 roundings
+    bnd = mass_error_bound(qp, k_np, Lc, W, chunks=8 * (Lc // 64 + 32))
+    k = vl_count(prefix_len(Lc, W), ppm)
+    amb = 0
+    for b in range(got.shape[0]):
+        for h in range(got.shape[1]):
+            res = check_selection(S[b, h], bnd[b, h], k, got[b, h])
+            assert res["ok"], res["reason"]
+            amb += res["ambiguous"]
+            if res["ambiguous"] == 0 and require_exact:
+                assert np.array_equal(got[b, h], want[b, h])
+    return amb
+
+
+@pytest.mark.parametrize("seed,B,HQ,HKV,Lc,W,ppm", [
+    (1000, 1, 4, 4, 1024, 128, 50_000),      # tiny decode workload
+    (1001, 1, 32, 8, 1024, 128, 50_000),
+    (1001, 1, 32, 8, 4096, 128, 50_000),
+    (1003, 2, 64, 8, 2048, 64, 20_000),      # g = 8: 512 rows, two row groups; two sequences
+    (7, 1, 8, 2, 1000, 128, 1_000_000),      # k = P
+    (9, 1, 6, 2, 700, 0, 50_000),            # no window: the prefix is the whole context
+])
+def test_select_mass_parity(hyq, seed, B, HQ, HKV, Lc, W, ppm):
+    c = decode_case(seed, B, HQ, HKV, Lc, window=W, n_proxy=64, sink_frac=0.02, outlier_channels=3)
+    got = run_select_mass(c, Lc, W, ppm)
+    check_mass(c, got, Lc, W, ppm)
+
+
+def test_select_mass_uses_only_the_first_n_proxies(hyq):
+    c = decode_case(25, 1, 8, 2, 1500, window=128, n_proxy=64, sink_frac=0.02)
+    got = run_select_mass(c, 1500, 128, 50_000, n_proxy=17)
+    check_mass(c, got, 1500, 128, 50_000, n_proxy=17)
+
+
+def test_select_mass_ties_go_to_lower_position(hyq):
+    c = decode_case(26, 1, 4, 1, 600, window=128, n_proxy=8)
+    c.k[:, :, :472] = c.k[:, :, :1]
+    got = run_select_mass(c, 600, 128, 50_000)
+    assert got[0, 0].tolist() == list(range(vl_count(472, 50_000)))
+
+
+def test_select_mass_full_size_llama_32k(hyq):
+    """32K context, 32/8 heads: 256 rows of 64 proxies per KV head."""
+    c = decode_case(1001, 1, 32, 8, 32768, window=128, n_proxy=64, sink_frac=0.02, outlier_channels=3)
+    got = run_select_mass(c, 32768, 128, 50_000)
+    assert got.shape == (1, 8, 1632)
+    amb = check_mass(c, got, 32768, 128, 50_000)
+    print("ambiguous keys at the boundary:", amb)
