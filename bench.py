@@ -52,6 +52,7 @@ def parse():
     p.add_argument("--no-batched", action="store_true", help="skip the batch-16 decode measurement")
     p.add_argument("--decode-plan", type=int, nargs=2, default=(0, 0), metavar=("MERGE", "SPLITS"),
                    help="tuning: hyq_set_decode_plan(MERGE, SPLITS) for the period (0 0 = automatic)")
+    p.add_argument("--no-mass", action="store_true", help="skip the Eq. 4 mass-score period measurement")
     p.add_argument("--no-frozen", action="store_true", help="skip the frozen-mode period measurement")
     p.add_argument("--no-prefetch", dest="prefetch", action="store_false",
                    help="plain fused decode steps; by default each step warms L2 with the next layer's share "
@@ -548,13 +549,11 @@ def run_ours(args, rank, world, local):
     h2d = q_h.numel() * 2 + k_h.numel() * 2 + v_h.numel() * 2
     d2h = o_h.numel() * 2
 
-    # frozen mode (Algorithm 4 as written): the same period with the last
-    # token's maintenance done by hyq_age_tail instead of re-selection
-    frozen = None
-    main_launches = run.launches_per_period
-    if not args.no_frozen:
-        del run
-        fr = PeriodRunner(cfg, k_srcs, v_srcs, L0, dev, prefetch_next=args.prefetch, mode="frozen")
+    # variants of the maintenance: frozen mode (Algorithm 4 as written: the
+    # last token's maintenance is hyq_age_tail instead of re-selection) and
+    # re-selection by the softmax-mass score of Eq. 4
+    def variant_period(**kw):
+        fr = PeriodRunner(cfg, k_srcs, v_srcs, L0, dev, prefetch_next=args.prefetch, **kw)
         fr.q_tok.copy_(q_tok)
         fr.k_tok.copy_(k_tok)
         fr.v_tok.copy_(v_tok)
@@ -570,12 +569,22 @@ def run_ours(args, rank, world, local):
         f1.record()
         torch.cuda.synchronize()
         fms = reduce_timing(f0.elapsed_time(f1), world, dev)
-        frozen = {"maintenance": "hyq_age_tail: tail rows older than the window quantised onto the 4-bit stream; "
-                                 "vertical lines fixed at freeze",
-                  "value": job_value(fms, args.steps, PERIOD * nl, world), "unit": "us/token/layer",
-                  "ms_per_step": fms / args.steps, "launches_per_period": fr.launches_per_period,
-                  "device_error_word": max(hyq.hyq_read_device_error(l.err()) for l in fr.layers)}
+        res = {"value": job_value(fms, args.steps, PERIOD * nl, world), "unit": "us/token/layer",
+               "ms_per_step": fms / args.steps, "launches_per_period": fr.launches_per_period,
+               "device_error_word": max(hyq.hyq_read_device_error(l.err()) for l in fr.layers)}
         del fr
+        return res
+
+    frozen = mass = None
+    main_launches = run.launches_per_period
+    if not (args.no_frozen and args.no_mass):
+        del run
+    if not args.no_frozen:
+        frozen = {"maintenance": "hyq_age_tail: tail rows older than the window quantised onto the 4-bit stream; "
+                                 "vertical lines fixed at freeze", **variant_period(mode="frozen")}
+    if not args.no_mass:
+        mass = {"maintenance": "re-selection by the softmax-mass score of Eq. 4 (hyq_select_vertical_mass), "
+                               "then rebuild", **variant_period(score="mass")}
 
     if rank != 0:
         return
@@ -612,6 +621,7 @@ def run_ours(args, rank, world, local):
         "cpu_baseline": base,
         "batched": batched,
         "frozen": frozen,
+        "mass_selection": mass,
         "prefill": ({"workload": "llama3.1-8b-shaped causal prefill, B1, 32/8 heads, d128, 32K, W128, rho 5% "
                                  "(hyq_prefill_attention: pack + main kernel)",
                      "flops": "4 d HQ L(L+1)/2", "l2": "256 MB flush before every timed call",

@@ -9,7 +9,9 @@ decode step (append + attention, hyq_decode_step) of every layer; with
 ``mode="frozen"`` (Algorithm 4 as written) the last token's maintenance is
 hyq_age_tail (the tail rows older than the window go to the 4-bit stream,
 the vertical-line set chosen at freeze stays) instead of re-selection and
-rebuild; the reset then also restores the tail rows the aging shifted.  At the
+rebuild; the reset then also restores the tail rows the aging shifted.
+With ``score="mass"`` re-selection uses the softmax-mass score of Eq. 4
+(hyq_select_vertical_mass) instead of Algorithm 1's summed logits.  At the
 last token two graphs are captured: the appends of all layers with the
 re-selection and rebuild of every layer, then the decode attention of all
 layers (maintenance sits between the append and the attention).  A reset graph restores the
@@ -34,9 +36,12 @@ class PeriodRunner:
     """
 
     def __init__(self, cfg, k_srcs, v_srcs, L0: int, device="cuda", prefetch_next: bool = False,
-                 mode: str = "reselect"):
+                 mode: str = "reselect", score: str = "logits"):
         if mode not in ("reselect", "frozen"):
             raise ValueError(f"mode must be 'reselect' or 'frozen', not {mode!r}")
+        if score not in ("logits", "mass"):
+            raise ValueError(f"score must be 'logits' or 'mass', not {score!r}")
+        self.select = L.hyq_select_vertical_mass if score == "mass" else L.hyq_select_vertical
         self.cfg = cfg
         self.prefetch_next = prefetch_next
         self.frozen = mode == "frozen"
@@ -46,7 +51,7 @@ class PeriodRunner:
         self.L0 = L0
         self.L_end = L0 + cfg.period
         self.layers = [HybridLayer(cfg, device) for _ in k_srcs]
-        self.ws_sel = workspace(cfg, L.OP_SELECT, self.L_end, device)
+        self.ws_sel = workspace(cfg, L.OP_SELECT_MASS if score == "mass" else L.OP_SELECT, self.L_end, device)
         self.ws_dec = workspace(cfg, L.OP_DECODE, self.L_end, device)
         kmax = max(1, L.hyq_vl_count(cfg, max(0, cfg.capacity - cfg.window)))
         self.idx = [torch.zeros(cfg.batch, cfg.num_kv_heads, kmax, dtype=torch.int32, device=device)
@@ -65,8 +70,8 @@ class PeriodRunner:
         vertical-line set from ``q_tail`` [n_layers, B, HQ, T, 128]."""
         for li, lay in enumerate(self.layers):
             lay.reset()
-            k = L.hyq_select_vertical(self.cfg, q_tail[li], q_tail.shape[3], self.k_srcs[li], self.L0,
-                                      self.idx[li], self.ws_sel)
+            k = self.select(self.cfg, q_tail[li], q_tail.shape[3], self.k_srcs[li], self.L0, self.idx[li],
+                            self.ws_sel)
             L.hyq_rebuild(self.cfg, self.k_srcs[li], self.v_srcs[li], self.L0, self.idx[li], k, lay.c)
         torch.cuda.synchronize()
         self.counts0 = torch.stack([lay.counts().clone() for lay in self.layers])
@@ -92,10 +97,11 @@ class PeriodRunner:
                 n += 3
             elif t == self.cfg.period - 1:
                 ring = lay.q_ring()
-                k = L.hyq_select_vertical(self.cfg, ring, ring.shape[2], self.k_srcs[li], self.L_end,
-                                          self.idx[li], self.ws_sel)
+                k = self.select(self.cfg, ring, ring.shape[2], self.k_srcs[li], self.L_end, self.idx[li],
+                                self.ws_sel)
                 L.hyq_rebuild(self.cfg, self.k_srcs[li], self.v_srcs[li], self.L_end, self.idx[li], k, lay.c)
-                n += (3 if k > 0 else 0) + (2 if self.L_end - self.cfg.window - k > 0 else 1)
+                n += ((5 if self.select is L.hyq_select_vertical_mass else 3) if k > 0 else 0) + \
+                    (2 if self.L_end - self.cfg.window - k > 0 else 1)
         return n
 
     def _decodes(self, t):
