@@ -189,6 +189,9 @@ def check_mass(c, got, Lc, W, ppm, n_proxy=None, require_exact=True):
     (1003, 2, 64, 8, 2048, 64, 20_000),      # g = 8: 512 rows, two row groups; two sequences
     (7, 1, 8, 2, 1000, 128, 1_000_000),      # k = P
     (9, 1, 6, 2, 700, 0, 50_000),            # no window: the prefix is the whole context
+    (10, 1, 8, 2, 129, 128, 50_000),         # P = 1: most key splits are empty
+    (11, 1, 8, 4, 100, 64, 50_000),          # P = 36 < one 64-key tile
+    (12, 2, 32, 8, 8192, 128, 50_000),       # two sequences at 8K
 ])
 def test_select_mass_parity(hyq, seed, B, HQ, HKV, Lc, W, ppm):
     c = decode_case(seed, B, HQ, HKV, Lc, window=W, n_proxy=64, sink_frac=0.02, outlier_channels=3)
