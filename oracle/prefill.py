@@ -28,6 +28,13 @@ Readings (the paper leaves these open):
   INT8 codes are ``clamp(rint(t), -127, 127)`` (ties to even), FP8 codes the
   e4m3 value nearest to ``t`` (ties to even, saturating at +-448); a block
   of zeros gets ``s = 0`` and zero codes;
+* ``band=True`` takes the window per query instead (a diagonal band): query
+  ``i`` sees the keys ``(i - W, i]`` in BF16, the vertical lines at or
+  before ``i - W`` in BF16 and the other keys at or before ``i - W`` from
+  the quantised prefix; vertical lines, the quantised-prefix list, its
+  tiles and its scales are those of the fixed window (for every row
+  ``i - W <= L - 1 - W < P``, so no quantised key outside ``[0, P)`` is
+  ever needed).  The two readings agree on the last row and whenever W = 0;
 * the softmax probabilities are *not* quantised here.  A kernel that feeds a
   low-precision P to the PV product differs from this oracle by the P
   rounding step only; that difference is covered by the test tolerance
@@ -74,7 +81,7 @@ def quantize_symmetric(x, axis, dtype: str):
 
 def hybrid_prefill(q, k, v, vl_idx, window: int, dtype: str = "int8",
                    key_tile: int = KEY_TILE, query_block: int = QUERY_BLOCK,
-                   query_blocks=None, heads=None, return_abs: bool = False):
+                   query_blocks=None, heads=None, return_abs: bool = False, band: bool = False):
     """Eq. 7 with Algorithm 2's quantisation, causal, float64.
 
     q [B, HQ, L, d]; k, v [B, HKV, L, d]; vl_idx [B, HKV, k] (positions in
@@ -86,6 +93,7 @@ def hybrid_prefill(q, k, v, vl_idx, window: int, dtype: str = "int8",
     sum_j p_j`` (the same softmax weights applied to the magnitudes of the
     effective values): ``2^-8 a`` bounds what rounding the probabilities to
     BF16 (unit roundoff 2^-8) before the P.V product can change in ``o``.
+    ``band`` selects the per-query window (module docstring).
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -111,7 +119,9 @@ def hybrid_prefill(q, k, v, vl_idx, window: int, dtype: str = "int8",
                 j = qpos[t0:t0 + key_tile]
                 kq[t0:t0 + len(j)] = quantize_symmetric(k[b, kh, j], None, dtype)[0]
                 vq[t0:t0 + len(j)] = quantize_symmetric(v[b, kh, j], None, dtype)[0]
-            fp = np.concatenate([vl, np.arange(P, L)])
+            # Full-precision list: the vertical lines, then (fixed window) the
+            # last W positions; a band's keys are taken per query block below.
+            fp = vl if band else np.concatenate([vl, np.arange(P, L)])
             pos = np.concatenate([qpos, fp])
             Kall = np.concatenate([kq, k[b, kh, fp]])
             Vall = np.concatenate([vq, v[b, kh, fp]])
@@ -129,12 +139,24 @@ def hybrid_prefill(q, k, v, vl_idx, window: int, dtype: str = "int8",
                     # full-precision segments the BF16 queries (Algorithm 2).
                     lg = np.concatenate([alpha * qhat @ Kall[:nq].T,
                                          alpha * qb @ Kall[nq:].T], axis=1)
-                    lg = np.where(pos[None, :] <= rows[:, None], lg, -np.inf)
+                    Vx = Vall
+                    if band:
+                        # quantised prefix and vertical lines: j <= i - W;
+                        # the band (i - W, i] in BF16 from the source rows
+                        lim = rows - window
+                        lg = np.where(pos[None, :] <= lim[:, None], lg, -np.inf)
+                        bpos = np.arange(max(0, r0 - window + 1), rows[-1] + 1)
+                        inb = (bpos[None, :] > lim[:, None]) & (bpos[None, :] <= rows[:, None])
+                        lgb = np.where(inb, alpha * qb @ k[b, kh, bpos].T, -np.inf)
+                        lg = np.concatenate([lg, lgb], axis=1)
+                        Vx = np.concatenate([Vall, v[b, kh, bpos]])
+                    else:
+                        lg = np.where(pos[None, :] <= rows[:, None], lg, -np.inf)
                     m = lg.max(axis=1, keepdims=True)
                     e = np.exp(lg - m)
-                    out[b, h, rows] = (e @ Vall) / e.sum(axis=1, keepdims=True)
+                    out[b, h, rows] = (e @ Vx) / e.sum(axis=1, keepdims=True)
                     if return_abs:
-                        mag[b, h, rows] = (e @ np.abs(Vall)) / e.sum(axis=1, keepdims=True)
+                        mag[b, h, rows] = (e @ np.abs(Vx)) / e.sum(axis=1, keepdims=True)
     return (out, mag) if return_abs else out
 
 

@@ -77,6 +77,12 @@ MUTATIONS = [
      "vq[t0:t0 + len(j)] = quantize_symmetric(v[b, kh, j], 0, dtype)[0]", "V scales per channel"),
     ("prefill", "s = (amax / np.float32(C_B[dtype])).astype(np.float32)",
      "s = (amax / np.float32(C_B[dtype] + 1)).astype(np.float32)", "c_B off by one"),
+    ("prefill", "inb = (bpos[None, :] > lim[:, None])", "inb = (bpos[None, :] >= lim[:, None])",
+     "band includes i - W"),
+    ("prefill", "lg = np.where(pos[None, :] <= lim[:, None], lg, -np.inf)",
+     "lg = np.where(pos[None, :] <= rows[:, None], lg, -np.inf)", "band: quantised keys up to i"),
+    ("prefill", "& (bpos[None, :] <= rows[:, None])", "& (bpos[None, :] < rows[:, None])",
+     "band leaves out the query's own key"),
     ("accounting", "return d // 2 + ((d // group) * 4 if with_meta else 0)",
      "return d // 2 + ((d // group) * 2 if with_meta else 0)", "metadata bytes halved"),
 ]

@@ -181,3 +181,93 @@ def test_abs_weighted_values(dtype):
     np.testing.assert_allclose(a, hybrid_prefill(q, k, np.abs(v), idx, window=32, dtype=dtype),
                                rtol=1e-13, atol=1e-15)
     assert np.all(a >= np.abs(o) - 1e-15)
+
+
+# --- the per-query band (``band=True``): query i sees (i - W, i] in BF16 ---
+
+def _vl(P, n, seed, early=16):
+    """[1, 2, n] ascending vertical-line positions in [0, P); the first KV
+    head's set has four positions below ``early`` (inside the first window)."""
+    rng = np.random.default_rng(seed)
+    e = rng.choice(min(early, P), size=4, replace=False)
+    rest = rng.choice(np.setdiff1d(np.arange(P), e), size=n - 4, replace=False)
+    return np.stack([np.sort(np.concatenate([e, rest])), np.sort(rng.choice(P, size=n, replace=False))])[None]
+
+
+def _exactly_quantisable(seed, L, d, dtype):
+    """Q [1,4,L,d], K, V [1,2,L,d] whose every tile quantises without error:
+    each value is a code (an integer in [-127, 127], or an e4m3 value) times
+    2^-7 (INT8) or 2^-9 (FP8), and every row holds the largest code, so every
+    tile's scale is exactly that power of two and x / s is the code itself."""
+    rng = np.random.default_rng(seed)
+    if dtype == "int8":
+        codes, top, unit = np.arange(-127, 128, dtype=np.float64), 127.0, 2.0 ** -7
+    else:
+        codes, top, unit = np.array(sorted(_e4m3_values().values())), 448.0, 2.0 ** -9
+
+    def mat(h):
+        c = rng.choice(codes, size=(1, h, L, d))
+        c[..., 0] = top
+        return c * unit
+    return mat(4), mat(2), mat(2)
+
+
+@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+@pytest.mark.parametrize("band", [False, True])
+def test_exactly_quantisable_inputs_give_exact_attention(dtype, band):
+    """With quantisation error-free, either window reading is exact causal
+    attention at every row: no key is counted twice or left out by the
+    segment masks (quantised prefix, vertical lines, window or band)."""
+    L, W = 300, 48
+    q, k, v = _exactly_quantisable(50, L, 64, dtype)
+    idx = _vl(L - W, 12, 51)
+    o = hybrid_prefill(q, k, v, idx, W, dtype, band=band)
+    np.testing.assert_allclose(o, causal_attention(q, k, v), rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+def test_band_rows_inside_window_are_full_precision(dtype):
+    """Rows i < W have every key j <= i inside their band: exact attention,
+    unlike the fixed window, which quantises them; later rows quantise the
+    keys W or more positions back."""
+    L, W = 300, 64
+    q, k, v = _np(prefill_case(52, 1, 4, 2, L, d=64, window=W, sink_frac=0.03))
+    idx = _vl(L - W, 12, 53)
+    ex = causal_attention(q, k, v)
+    band = hybrid_prefill(q, k, v, idx, W, dtype, band=True)
+    fixed = hybrid_prefill(q, k, v, idx, W, dtype)
+    np.testing.assert_allclose(band[:, :, :W], ex[:, :, :W], rtol=1e-12, atol=1e-13)
+    assert np.abs(fixed[:, :, 1:W] - ex[:, :, 1:W]).max() > 1e-6
+    assert np.abs(band[:, :, W + 8:] - ex[:, :, W + 8:]).max() > 1e-6
+
+
+@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+def test_band_agrees_with_fixed_window_on_last_row_and_without_window(dtype):
+    """The last row's band (P - 1, L - 1] is the fixed window [P, L); with
+    W = 0 both readings quantise every key but the vertical lines."""
+    L, W = 300, 64
+    q, k, v = _np(prefill_case(54, 1, 4, 2, L, d=64, window=W, sink_frac=0.03))
+    idx = _vl(L - W, 12, 55)
+    band = hybrid_prefill(q, k, v, idx, W, dtype, band=True)
+    fixed = hybrid_prefill(q, k, v, idx, W, dtype)
+    np.testing.assert_allclose(band[:, :, L - 1], fixed[:, :, L - 1], rtol=1e-12, atol=1e-13)
+    assert np.abs(band[:, :, W:L - 1] - fixed[:, :, W:L - 1]).max() > 1e-6
+    q0, k0, v0 = _np(prefill_case(56, 1, 4, 2, L, d=64, window=0, sink_frac=0.03))
+    idx0 = _vl(L, 12, 57)
+    np.testing.assert_allclose(hybrid_prefill(q0, k0, v0, idx0, 0, dtype, band=True),
+                               hybrid_prefill(q0, k0, v0, idx0, 0, dtype), rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+def test_band_window_covering_sequence_is_exact(dtype):
+    q, k, v = _np(prefill_case(58, 1, 4, 2, 150, d=64))
+    o = hybrid_prefill(q, k, v, None, window=150, dtype=dtype, band=True)
+    np.testing.assert_allclose(o, _sdpa_causal(q, k, v), rtol=1e-12, atol=1e-13)
+
+
+def test_band_restricted_blocks_equal_full_computation():
+    q, k, v = _np(prefill_case(59, 1, 4, 2, 300, d=64, window=32))
+    idx = _vl(268, 10, 60)
+    full = hybrid_prefill(q, k, v, idx, window=32, dtype="int8", band=True)
+    part = hybrid_prefill(q, k, v, idx, window=32, dtype="int8", query_blocks=[1], heads=[3], band=True)
+    np.testing.assert_array_equal(part[0, 3, 128:256], full[0, 3, 128:256])
