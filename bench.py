@@ -138,10 +138,12 @@ def prefill_inputs(dev, Lc, seed=1005):
     return q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16)
 
 
-def prefill_measure(dev, lengths, reps=5, warmup=3):
+def prefill_measure(dev, lengths, reps=5, warmup=3, windows=("fixed", "band")):
     """Time hyq_prefill_attention (pack + main kernel) per length and dtype with
-    CUDA events, L2 flushed (a 256 MB write) before every timed call.  The
-    vertical-line set comes from hyq_select_vertical on the last 64 queries."""
+    CUDA events, L2 flushed (a 256 MB write) before every timed call; with
+    window "band" hyq_prefill_attention_band (each query's window is its own
+    last W keys).  The vertical-line set comes from hyq_select_vertical on the
+    last 64 queries."""
     import torch
     import hybrid_precision_quantized_gb300 as hyq
     from hybrid_precision_quantized_gb300 import _lib as L
@@ -155,32 +157,34 @@ def prefill_measure(dev, lengths, reps=5, warmup=3):
         idx = torch.zeros(B, HKV, kmax, dtype=torch.int32, device=dev)
         kvl = hyq.hyq_select_vertical(cfg, q[:, :, Lc - 64:], 64, k, Lc, idx,
                                       hyq.workspace(cfg, L.OP_SELECT, Lc, dev))
-        ws = hyq.workspace(cfg, L.OP_PREFILL, Lc, dev)
         out = torch.empty(B, HQ, Lc, D, dtype=torch.bfloat16, device=dev)
         err = torch.zeros(1, dtype=torch.int32, device=dev)
         flops = 4.0 * D * HQ * Lc * (Lc + 1) / 2
-        for name, dt in (("fp8", L.PREFILL_FP8), ("int8", L.PREFILL_INT8)):
+        for win, (name, dt) in [(w, x) for w in windows for x in (("fp8", L.PREFILL_FP8), ("int8", L.PREFILL_INT8))]:
+            fn = hyq.hyq_prefill_attention_band if win == "band" else hyq.hyq_prefill_attention
+            ws = hyq.workspace(cfg, L.OP_PREFILL_BAND if win == "band" else L.OP_PREFILL, Lc, dev)
             for _ in range(warmup):
-                hyq.hyq_prefill_attention(cfg, dt, q, k, v, Lc, idx, kvl, out, ws, err)
+                fn(cfg, dt, q, k, v, Lc, idx, kvl, out, ws, err)
             times = []
             for _ in range(reps):
                 flush.fill_(1)
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record()
-                hyq.hyq_prefill_attention(cfg, dt, q, k, v, Lc, idx, kvl, out, ws, err)
+                fn(cfg, dt, q, k, v, Lc, idx, kvl, out, ws, err)
                 e1.record()
                 torch.cuda.synchronize()
                 times.append(e0.elapsed_time(e1))
+            del ws
             ms = statistics.median(times)
             tf = flops / (ms * 1e-3) / 1e12
             peak = peaks["fp8"] if name == "fp8" else peaks["bf16"]
-            res.append({"seq_len": Lc, "dtype": name, "ms": ms, "tflops": tf,
+            res.append({"seq_len": Lc, "dtype": name, "window": win, "ms": ms, "tflops": tf,
                         "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
                                      "frac": tf / peak,
                                      "peak_source": (peaks["source"] + (" x 2 (nominal fp8/bf16)" if name == "fp8"
                                                                         else " (INT8 codes run on the bf16 pipe)"))},
                         "device_error_word": hyq.hyq_read_device_error(err)})
-        del q, k, v, out, ws
+        del q, k, v, out
     return res
 
 
@@ -623,7 +627,8 @@ def run_ours(args, rank, world, local):
         "frozen": frozen,
         "mass_selection": mass,
         "prefill": ({"workload": "llama3.1-8b-shaped causal prefill, B1, 32/8 heads, d128, 32K, W128, rho 5% "
-                                 "(hyq_prefill_attention: pack + main kernel)",
+                                 "(pack + main kernel; window fixed: hyq_prefill_attention, band: "
+                                 "hyq_prefill_attention_band)",
                      "flops": "4 d HQ L(L+1)/2", "l2": "256 MB flush before every timed call",
                      "results": prefill} if prefill is not None else None),
     }

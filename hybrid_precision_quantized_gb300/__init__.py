@@ -9,6 +9,7 @@ from ._lib import (HyqConfig, HyqError, HyqLayout, load, lib_path, hyq_config_ch
                    hyq_age_tail, hyq_decode_append, hyq_decode_attention, hyq_decode_step,
                    hyq_decode_step_prefetch,
                    hyq_decode_attention_noalloc, hyq_layout_reset, hyq_layout_sizes, hyq_prefill_attention,
+                   hyq_prefill_attention_band,
                    hyq_quantize_append, hyq_read_device_error, hyq_rebuild, hyq_select_vertical,
                    hyq_select_vertical_mass, hyq_set_decode_plan, hyq_set_decode_overlap,
                    hyq_status_string, hyq_vl_count, hyq_workspace_size)

@@ -30,7 +30,7 @@ QBLOCK_BYTES = 10240
 COUNTS = 8
 CNT_NQ, CNT_NVL, CNT_NTAIL, CNT_LEN, CNT_RING_N, CNT_RING_POS = range(6)
 LAYOUT_FIELDS = ("qblocks", "vl_k", "vl_v", "vl_idx", "tail_k", "tail_v", "q_ring", "counts", "err")
-OP_SELECT, OP_DECODE, OP_PREFILL, OP_SELECT_MASS = 1, 2, 3, 4
+OP_SELECT, OP_DECODE, OP_PREFILL, OP_SELECT_MASS, OP_PREFILL_BAND = 1, 2, 3, 4, 5
 PREFILL_INT8, PREFILL_FP8 = 1, 2
 
 # Every symbol include/hyq.h declares.
@@ -39,7 +39,8 @@ SYMBOLS = ("hyq_status_string", "hyq_config_check", "hyq_vl_count", "hyq_layout_
            "hyq_select_vertical", "hyq_rebuild", "hyq_decode_append", "hyq_decode_attention",
            "hyq_decode_attention_noalloc", "hyq_read_device_error", "hyq_set_decode_plan",
            "hyq_prefill_attention", "hyq_decode_step", "hyq_set_decode_overlap",
-           "hyq_decode_step_prefetch", "hyq_age_tail", "hyq_select_vertical_mass")
+           "hyq_decode_step_prefetch", "hyq_age_tail", "hyq_select_vertical_mass",
+           "hyq_prefill_attention_band")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -108,6 +109,9 @@ def load() -> ctypes.CDLL:
         "hyq_prefill_attention": (c_int32, [P(HyqConfig), c_int32, c_void_p, c_int32, c_void_p, c_void_p,
                                             c_int32, c_int32, c_void_p, c_int32, c_void_p, c_void_p,
                                             c_void_p, c_size_t, c_void_p]),
+        "hyq_prefill_attention_band": (c_int32, [P(HyqConfig), c_int32, c_void_p, c_int32, c_void_p, c_void_p,
+                                                 c_int32, c_int32, c_void_p, c_int32, c_void_p, c_void_p,
+                                                 c_void_p, c_size_t, c_void_p]),
     }
     for name in SYMBOLS:
         fn = getattr(lib, name)
@@ -258,10 +262,21 @@ def hyq_prefill_attention(cfg, dtype: int, q, k, v, L: int, vl_idx, kvl: int, ou
     """q [B, HQ, ldq, 128]; k, v [B, HKV, ldk, 128] (bf16 views with dense
     rows); vl_idx int32 [B, HKV, kvl] contiguous (or None when kvl = 0);
     out bf16 [B, HQ, L, 128] contiguous; err int32 [1] device or None."""
+    _prefill("hyq_prefill_attention", cfg, dtype, q, k, v, L, vl_idx, kvl, out, ws, err, stream)
+
+
+def hyq_prefill_attention_band(cfg, dtype: int, q, k, v, L: int, vl_idx, kvl: int, out, ws, err=None,
+                               stream=None):
+    """As hyq_prefill_attention with the window taken per query: row i sees
+    (i - W, i] in BF16; workspace is workspace(cfg, OP_PREFILL_BAND, L)."""
+    _prefill("hyq_prefill_attention_band", cfg, dtype, q, k, v, L, vl_idx, kvl, out, ws, err, stream)
+
+
+def _prefill(name, cfg, dtype, q, k, v, L, vl_idx, kvl, out, ws, err, stream):
     ldk = row_ld(k)
     if row_ld(v) != ldk:
         raise ValueError("k and v must share the leading dimension")
-    _check("hyq_prefill_attention", load().hyq_prefill_attention(
+    _check(name, getattr(load(), name)(
         ctypes.byref(cfg), dtype, ptr(q), row_ld(q), ptr(k), ptr(v), ldk, L,
         ptr(vl_idx) if kvl > 0 else None, kvl, ptr(out), ptr(err), ptr(ws),
         ws.numel() * ws.element_size(), stream_ptr(stream)))

@@ -106,7 +106,8 @@ extern "C" size_t hyq_workspace_size(const hyq_config* c, int op, int32_t len_hi
     case HYQ_OP_SELECT: return hyq_select_ws_bytes(c, len_hint);
     case HYQ_OP_SELECT_MASS: return hyq_select_mass_ws_bytes(c, len_hint);
     case HYQ_OP_DECODE: return hyq_decode_ws_bytes(c, len_hint);
-    case HYQ_OP_PREFILL: return hyq_prefill_ws_bytes_hint(c, len_hint);
+    case HYQ_OP_PREFILL: return hyq_prefill_ws_bytes_hint(c, len_hint, false);
+    case HYQ_OP_PREFILL_BAND: return hyq_prefill_ws_bytes_hint(c, len_hint, true);
     default: return 0;
   }
 }
@@ -247,10 +248,9 @@ extern "C" hyq_status hyq_decode_step_prefetch(const hyq_config* c, const void* 
   return from_cuda(hyq_launch_decode(c, q, l, out, len_hint, ws, s, k_new, v_new, k_src, v_src, ld, next));
 }
 
-extern "C" hyq_status hyq_prefill_attention(const hyq_config* c, int32_t dtype, const void* q,
-                                            int32_t ldq, const void* k, const void* v, int32_t ldk,
-                                            int32_t L, const int32_t* vl_idx, int32_t kvl, void* out,
-                                            int32_t* err, void* ws, size_t ws_bytes, hyq_stream_t s) {
+static hyq_status prefill_call(const hyq_config* c, int32_t dtype, const void* q, int32_t ldq, const void* k,
+                               const void* v, int32_t ldk, int32_t L, const int32_t* vl_idx, int32_t kvl,
+                               void* out, int32_t* err, void* ws, size_t ws_bytes, hyq_stream_t s, bool band) {
   hyq_status st = hyq_config_check(c);
   if (st != HYQ_OK) return st;
   if (dtype != HYQ_PREFILL_INT8 && dtype != HYQ_PREFILL_FP8) return HYQ_ERR_INVALID_ARG;
@@ -262,9 +262,23 @@ extern "C" hyq_status hyq_prefill_attention(const hyq_config* c, int32_t dtype, 
   if (!q || !k || !v || !out) return HYQ_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16)) return HYQ_ERR_INVALID_ARG;
   if ((L + 127) / 128 > 65535) return HYQ_ERR_UNSUPPORTED;
-  if (!ws || !aligned(ws, kAlign) || ws_bytes < hyq_prefill_ws_bytes(c, dtype, L, kvl))
+  if (!ws || !aligned(ws, kAlign) || ws_bytes < hyq_prefill_ws_bytes(c, dtype, L, kvl, band))
     return HYQ_ERR_WORKSPACE;
-  return from_cuda(hyq_launch_prefill(c, dtype, q, ldq, k, v, ldk, L, vl_idx, kvl, out, ws, err, s));
+  return from_cuda(hyq_launch_prefill(c, dtype, q, ldq, k, v, ldk, L, vl_idx, kvl, out, ws, err, s, band));
+}
+
+extern "C" hyq_status hyq_prefill_attention(const hyq_config* c, int32_t dtype, const void* q,
+                                            int32_t ldq, const void* k, const void* v, int32_t ldk,
+                                            int32_t L, const int32_t* vl_idx, int32_t kvl, void* out,
+                                            int32_t* err, void* ws, size_t ws_bytes, hyq_stream_t s) {
+  return prefill_call(c, dtype, q, ldq, k, v, ldk, L, vl_idx, kvl, out, err, ws, ws_bytes, s, false);
+}
+
+extern "C" hyq_status hyq_prefill_attention_band(const hyq_config* c, int32_t dtype, const void* q,
+                                                 int32_t ldq, const void* k, const void* v, int32_t ldk,
+                                                 int32_t L, const int32_t* vl_idx, int32_t kvl, void* out,
+                                                 int32_t* err, void* ws, size_t ws_bytes, hyq_stream_t s) {
+  return prefill_call(c, dtype, q, ldq, k, v, ldk, L, vl_idx, kvl, out, err, ws, ws_bytes, s, true);
 }
 
 extern "C" hyq_status hyq_read_device_error(const int32_t* err_dev, int32_t* err_host,

@@ -55,9 +55,9 @@ cudaError_t hyq_launch_decode(const hyq_config* c, const void* q, const hyq_layo
 size_t hyq_decode_ws_bytes(const hyq_config* c, int32_t len_hint);
 cudaError_t hyq_launch_prefill(const hyq_config* c, int dtype, const void* q, int64_t ldq, const void* k,
                                const void* v, int64_t ldk, int32_t L, const int32_t* vl, int32_t kvl, void* out,
-                               void* ws, int32_t* err, cudaStream_t s);
-size_t hyq_prefill_ws_bytes(const hyq_config* c, int dtype, int32_t L, int32_t kvl);
-size_t hyq_prefill_ws_bytes_hint(const hyq_config* c, int32_t L);
+                               void* ws, int32_t* err, cudaStream_t s, bool band);
+size_t hyq_prefill_ws_bytes(const hyq_config* c, int dtype, int32_t L, int32_t kvl, bool band);
+size_t hyq_prefill_ws_bytes_hint(const hyq_config* c, int32_t L, bool band);
 
 // ---------------------------------------------------------------------------
 // Device helpers

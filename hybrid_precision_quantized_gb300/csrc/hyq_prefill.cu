@@ -87,12 +87,14 @@ struct PackParams {
   uint8_t* vq;  // [B][HKV][ntq] value code images (BF16, transposed)
   uint8_t* kf;  // [B][HKV][ntf] BF16 key images
   uint8_t* vf;  // [B][HKV][ntf] BF16 value images (transposed)
+  uint8_t* kb;  // [B][HKV][ntb] per-query band: BF16 key images of positions 128t .. 128t+127
+  uint8_t* vb;  // [B][HKV][ntb] the same for values (transposed)
   int32_t* kpos;
   int32_t* fpos;
   float* sk;
   float* sv;
   int32_t* err;
-  int32_t L, P, HKV, nq, nfp, ntq, ntf;
+  int32_t L, P, HKV, nq, nfp, ntq, ntf, ntb;
 };
 
 struct MainParams {
@@ -102,13 +104,15 @@ struct MainParams {
   const uint8_t* vq;
   const uint8_t* kf;
   const uint8_t* vf;
+  const uint8_t* kb;    // per-query band images (band mode)
+  const uint8_t* vb;
   const int32_t* kpos;  // [B][HKV][ntq*128], ascending, padding INT32_MAX
   const int32_t* fpos;  // [B][HKV][ntf*128]
   const float* sk;      // [B][HKV][ntq*2]
   const float* sv;
   int32_t* err;
   int64_t ldq;
-  int32_t L, HQ, HKV, ntq, ntf;
+  int32_t L, HQ, HKV, ntq, ntf, ntb, W;
   float alpha_log2e;
 };
 
@@ -212,8 +216,10 @@ __device__ __forceinline__ float block_max(float v, float* red, int nwarps) {
 }
 
 // ---------------------------------------------------------------------------
-// Stage 1-2: key lists, scales, code images.  Grid (2 ntq + 2 ntf, HKV, B);
-// each block handles one 64-key scale tile of one list.
+// Stage 1-2: key lists, scales, code images.  Grid (2 ntq + 2 ntf + 2 ntb,
+// HKV, B); each block handles one 64-key scale tile of one list: the
+// quantised prefix, the full-precision list, or (per-query band, ntb > 0)
+// the BF16 images of all positions in order.
 // ---------------------------------------------------------------------------
 template <bool kFp8>
 __global__ void __launch_bounds__(256) pack_kernel(const __grid_constant__ PackParams p) {
@@ -223,9 +229,11 @@ __global__ void __launch_bounds__(256) pack_kernel(const __grid_constant__ PackP
   const int tid = threadIdx.x;
   const int kh = blockIdx.y, b = blockIdx.z;
   const size_t bh = (size_t)b * p.HKV + kh;
-  const bool quant = blockIdx.x < 2 * p.ntq;
-  const int t64 = quant ? blockIdx.x : blockIdx.x - 2 * p.ntq;
-  const int n = quant ? p.nq : p.nfp;
+  const int nq2 = 2 * p.ntq, nf2 = 2 * p.ntf;
+  const int seg = blockIdx.x < nq2 ? 0 : (blockIdx.x < nq2 + nf2 ? 1 : 2);  // quantised, full, band
+  const bool quant = seg == 0;
+  const int t64 = blockIdx.x - (seg == 0 ? 0 : (seg == 1 ? nq2 : nq2 + nf2));
+  const int n = seg == 0 ? p.nq : (seg == 1 ? p.nfp : p.L);
   const int32_t* vl = p.vl + bh * p.kvl;
 
   if (tid < kScaleTile) {
@@ -242,6 +250,8 @@ __global__ void __launch_bounds__(256) pack_kernel(const __grid_constant__ PackP
           else lo = mid + 1;
         }
         pos = lo;
+      } else if (seg == 2) {
+        pos = i;
       } else {
         if (i < p.kvl) {
           pos = __ldg(vl + i);
@@ -255,8 +265,8 @@ __global__ void __launch_bounds__(256) pack_kernel(const __grid_constant__ PackP
       }
     }
     spos[tid] = pos;
-    if (quant) p.kpos[bh * p.ntq * kKeys + i] = pos;
-    else p.fpos[bh * p.ntf * kKeys + i] = pos;
+    if (seg == 0) p.kpos[bh * p.ntq * kKeys + i] = pos;
+    else if (seg == 1) p.fpos[bh * p.ntf * kKeys + i] = pos;
   }
   __syncthreads();
 
@@ -320,8 +330,9 @@ __global__ void __launch_bounds__(256) pack_kernel(const __grid_constant__ PackP
       *reinterpret_cast<uint4*>(img + swz(key, 2 * qq + h)) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   } else {
-    uint8_t* img = quant ? p.kq + (bh * p.ntq + tile) * (size_t)kImg16
-                         : p.kf + (bh * p.ntf + tile) * (size_t)kImg16;
+    uint8_t* img = quant      ? p.kq + (bh * p.ntq + tile) * (size_t)kImg16
+                   : seg == 1 ? p.kf + (bh * p.ntf + tile) * (size_t)kImg16
+                              : p.kb + (bh * p.ntb + tile) * (size_t)kImg16;
     // dims 32qq .. 32qq+31 = bytes 64qq .. 64qq+63: region qq/2, chunks 4(qq&1)..+3
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
@@ -354,8 +365,9 @@ __global__ void __launch_bounds__(256) pack_kernel(const __grid_constant__ PackP
     vs[r][32 * qq + e] = y;
   }
   __syncthreads();
-  uint8_t* vimg = quant ? p.vq + (bh * p.ntq + tile) * (size_t)kImg16
-                        : p.vf + (bh * p.ntf + tile) * (size_t)kImg16;
+  uint8_t* vimg = quant      ? p.vq + (bh * p.ntq + tile) * (size_t)kImg16
+                  : seg == 1 ? p.vf + (bh * p.ntf + tile) * (size_t)kImg16
+                             : p.vb + (bh * p.ntb + tile) * (size_t)kImg16;
   vimg += (t64 & 1) * kRegion;
 #pragma unroll
   for (int it = 0; it < 4; ++it) {
@@ -369,9 +381,13 @@ __global__ void __launch_bounds__(256) pack_kernel(const __grid_constant__ PackP
 }
 
 // ---------------------------------------------------------------------------
-// Stage 3: segmented online softmax on tcgen05.
+// Stage 3: segmented online softmax on tcgen05.  Tiles in order: the
+// quantised prefix, the full-precision list, and with kBand the band tiles
+// (positions 128 tb0 .. 128 (tb0 + nbt) - 1).  Fixed window: every segment
+// masks keys after the row (j <= i).  Per-query band: the quantised prefix
+// and the vertical lines mask j <= i - W, the band tiles i - W < j <= i.
 // ---------------------------------------------------------------------------
-template <bool kFp8>
+template <bool kFp8, bool kBand>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ MainParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -389,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   uint64_t* vempty = bars + 15; // [kVStages]
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kOffMisc + 4);
-  int* ntiles = reinterpret_cast<int*>(sm + kOffMisc + 8);     // [4]
+  int* ntiles = reinterpret_cast<int*>(sm + kOffMisc + 8);     // [6]
   float* red = reinterpret_cast<float*>(sm + kOffMisc + 32);   // [8]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -423,16 +439,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     *abort_flag = 0;
   }
   if (warp == kCopyWarp) {
-    const int cq1 = warp_count_le(kpos, p.ntq * kKeys, rlast, lane);
-    const int cf1 = warp_count_le(fpos, p.ntf * kKeys, rlast, lane);
-    const int cq0 = warp_count_le(kpos, p.ntq * kKeys, r0, lane);
-    const int cf0 = warp_count_le(fpos, p.ntf * kKeys, r0, lane);
+    // last key position any row of the block may see in the listed segments
+    const int32_t hi = kBand ? rlast - p.W : rlast, lo = kBand ? r0 - p.W : r0;
+    const int cq1 = warp_count_le(kpos, p.ntq * kKeys, hi, lane);
+    const int cf1 = warp_count_le(fpos, p.ntf * kKeys, hi, lane);
+    const int cq0 = warp_count_le(kpos, p.ntq * kKeys, lo, lane);
+    const int cf0 = warp_count_le(fpos, p.ntf * kKeys, lo, lane);
     if (lane == 0) {
       ntiles[0] = (cq1 + kKeys - 1) / kKeys;
       ntiles[1] = (cf1 + kKeys - 1) / kKeys;
-      // tiles before these hold only keys <= r0 (no mask needed for any row)
+      // tiles before these hold only keys every row of the block sees
       ntiles[2] = cq0 / kKeys;
       ntiles[3] = cf0 / kKeys;
+      // band tiles: positions r0 - W + 1 .. rlast
+      const int tb0 = max(0, r0 - p.W + 1) / kKeys;
+      ntiles[4] = tb0;
+      ntiles[5] = (kBand && p.W > 0) ? rlast / kKeys - tb0 + 1 : 0;
     }
   }
   if (warp == kMmaWarp) tc_alloc(tslot, kTmemCols);
@@ -440,8 +462,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tslot;
-  const int nqt = ntiles[0], nt = ntiles[0] + ntiles[1];
-  const int mask_q = ntiles[2], mask_f = ntiles[3];
+  const int nqt = ntiles[0], nlt = ntiles[0] + ntiles[1], nt = nlt + ntiles[5];
+  const int mask_q = ntiles[2], mask_f = ntiles[3], tb0 = ntiles[4];
 
   if (tid < kSoft) {
     // ---------------- softmax / epilogue warps --------------------------
@@ -550,16 +572,28 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       const float cs = quant ? fmaxf(qfac * sc.x, 1.17549435e-38f) : p.alpha_log2e;
       const float vf = quant ? sc.y : 1.f;
       if (j + 1 < nqt) sc = make_float2(__ldg(skp + 2 * j + 2), __ldg(svp + 2 * j + 2));
-      const bool masked = quant ? j >= mask_q : j - nqt >= mask_f;  // some key after some row
+      // some key of the tile is hidden from some row of the block
+      const bool masked = quant ? j >= mask_q : (j < nlt ? j - nqt >= mask_f : true);
       if (masked) {
-        const int4* pp = reinterpret_cast<const int4*>((quant ? kpos + j * kKeys : fpos + (j - nqt) * kKeys) + 64 * hf);
+        const int lim = kBand ? row - p.W : row;  // last visible position of a listed segment
+        if (!kBand || j < nlt) {
+          const int4* pp =
+              reinterpret_cast<const int4*>((quant ? kpos + j * kKeys : fpos + (j - nqt) * kKeys) + 64 * hf);
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const int4 q4 = __ldg(pp + c);
-          if (q4.x > row) x[4 * c] = -INFINITY;
-          if (q4.y > row) x[4 * c + 1] = -INFINITY;
-          if (q4.z > row) x[4 * c + 2] = -INFINITY;
-          if (q4.w > row) x[4 * c + 3] = -INFINITY;
+          for (int c = 0; c < 16; ++c) {
+            const int4 q4 = __ldg(pp + c);
+            if (q4.x > lim) x[4 * c] = -INFINITY;
+            if (q4.y > lim) x[4 * c + 1] = -INFINITY;
+            if (q4.z > lim) x[4 * c + 2] = -INFINITY;
+            if (q4.w > lim) x[4 * c + 3] = -INFINITY;
+          }
+        } else {
+          // band tile: key i of this half is position base + i, visible
+          // when lim < base + i <= row
+          const int base = kKeys * (tb0 + j - nlt) + 64 * hf, ilo = lim - base, ihi = row - base;
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            if (i <= ilo || i > ihi) x[i] = -INFINITY;
         }
       }
       float a[8];
@@ -699,6 +733,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const int qimg = is_v ? kImg16 : kKImg;
     const uint8_t* qsrc = is_v ? p.vq + bh * p.ntq * (size_t)kImg16 : p.kq + bh * p.ntq * (size_t)kKImg;
     const uint8_t* fsrc = (is_v ? p.vf : p.kf) + bh * p.ntf * (size_t)kImg16;
+    const uint8_t* bsrc = (is_v ? p.vb : p.kb) + bh * p.ntb * (size_t)kImg16;
     uint8_t* dst = sm + (is_v ? kOffV : kOffK);
     const int nst = is_v ? kVStages : kKStages;  // ring stages
     int last_j = -1;
@@ -715,7 +750,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       }
       const bool quant = j < nqt;
       const uint32_t bytes = quant ? qimg : kImg16, part = bytes / 4;
-      const uint8_t* src = quant ? qsrc + (size_t)j * qimg : fsrc + (size_t)(j - nqt) * kImg16;
+      const uint8_t* src = quant     ? qsrc + (size_t)j * qimg
+                           : j < nlt ? fsrc + (size_t)(j - nqt) * kImg16
+                                     : bsrc + (size_t)(tb0 + j - nlt) * kImg16;
       if (lane == 0) mbar_arrive_expect_tx(full + s, bytes);
       __syncwarp();
       // stage s is always filled by lanes 4s .. 4s+3, so the stages' copies
@@ -821,10 +858,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 size_t align_up(size_t x) { return (x + 1023) & ~static_cast<size_t>(1023); }
 
 struct WsLayout {
-  size_t kq, vq, kf, vf, kpos, fpos, sk, sv, total;
+  size_t kq, vq, kf, vf, kb, vb, kpos, fpos, sk, sv, total;
 };
 
-WsLayout ws_layout(const hyq_config* c, bool fp8, int32_t ntq, int32_t ntf) {
+WsLayout ws_layout(const hyq_config* c, bool fp8, int32_t ntq, int32_t ntf, int32_t ntb) {
   const size_t bh = (size_t)c->batch * c->num_kv_heads;
   WsLayout w{};
   size_t off = 0;
@@ -836,6 +873,10 @@ WsLayout ws_layout(const hyq_config* c, bool fp8, int32_t ntq, int32_t ntf) {
   off = align_up(off + bh * ntf * (size_t)kImg16);
   w.vf = off;
   off = align_up(off + bh * ntf * (size_t)kImg16);
+  w.kb = off;
+  off = align_up(off + bh * ntb * (size_t)kImg16);
+  w.vb = off;
+  off = align_up(off + bh * ntb * (size_t)kImg16);
   w.kpos = off;
   off = align_up(off + bh * ntq * (size_t)kKeys * 4);
   w.fpos = off;
@@ -848,40 +889,48 @@ WsLayout ws_layout(const hyq_config* c, bool fp8, int32_t ntq, int32_t ntf) {
   return w;
 }
 
-template <bool kFp8>
-cudaError_t set_attrs() {
+template <bool kFp8, bool kBand>
+cudaError_t launch_main(const MainParams& mp, dim3 grid, cudaStream_t s) {
   static bool done = false;
-  if (done) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e == cudaSuccess) done = true;
-  return e;
+  if (!done) {
+    cudaError_t e =
+        cudaFuncSetAttribute(prefill_kernel<kFp8, kBand>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    done = true;
+  }
+  prefill_kernel<kFp8, kBand><<<grid, kThreads, kSmemBytes, s>>>(mp);
+  return cudaGetLastError();
 }
+
+int32_t tiles_of(int32_t n) { return (n + kKeys - 1) / kKeys; }
 
 }  // namespace
 
-size_t hyq_prefill_ws_bytes(const hyq_config* c, int dtype, int32_t L, int32_t kvl) {
+// Full-precision list: the vertical lines, plus the last W positions for the
+// fixed window; the band mode adds BF16 images of all L positions instead.
+size_t hyq_prefill_ws_bytes(const hyq_config* c, int dtype, int32_t L, int32_t kvl, bool band) {
   const int32_t P = L - c->window > 0 ? L - c->window : 0;
-  const int32_t nq = P - kvl, nfp = kvl + (L - P);
-  return ws_layout(c, dtype == HYQ_PREFILL_FP8, (nq + kKeys - 1) / kKeys, (nfp + kKeys - 1) / kKeys).total;
+  const int32_t nq = P - kvl, nfp = band ? kvl : kvl + (L - P);
+  return ws_layout(c, dtype == HYQ_PREFILL_FP8, tiles_of(nq), tiles_of(nfp), band ? tiles_of(L) : 0).total;
 }
 
-size_t hyq_prefill_ws_bytes_hint(const hyq_config* c, int32_t L) {
+size_t hyq_prefill_ws_bytes_hint(const hyq_config* c, int32_t L, bool band) {
   // Worst case over the calls with context length <= L: every prefix position
   // quantised (kvl = 0) for the code images, the configured vertical-line
-  // count plus the window for the BF16 images; 16-bit key codes.
+  // count (plus the window) for the BF16 images; 16-bit key codes.
   const int32_t P = L - c->window > 0 ? L - c->window : 0;
-  const int32_t nfp = hyq_vl_count(c, P) + (L - P);
-  return ws_layout(c, false, (P + kKeys - 1) / kKeys, (nfp + kKeys - 1) / kKeys).total;
+  const int32_t nfp = hyq_vl_count(c, P) + (band ? 0 : L - P);
+  return ws_layout(c, false, tiles_of(P), tiles_of(nfp), band ? tiles_of(L) : 0).total;
 }
 
 cudaError_t hyq_launch_prefill(const hyq_config* c, int dtype, const void* q, int64_t ldq, const void* k,
                                const void* v, int64_t ldk, int32_t L, const int32_t* vl, int32_t kvl, void* out,
-                               void* ws, int32_t* err, cudaStream_t s) {
+                               void* ws, int32_t* err, cudaStream_t s, bool band) {
   const bool fp8 = dtype == HYQ_PREFILL_FP8;
   const int32_t P = L - c->window > 0 ? L - c->window : 0;
-  const int32_t nq = P - kvl, nfp = kvl + (L - P);
-  const int32_t ntq = (nq + kKeys - 1) / kKeys, ntf = (nfp + kKeys - 1) / kKeys;
-  const WsLayout w = ws_layout(c, fp8, ntq, ntf);
+  const int32_t nq = P - kvl, nfp = band ? kvl : kvl + (L - P);
+  const int32_t ntq = tiles_of(nq), ntf = tiles_of(nfp), ntb = band ? tiles_of(L) : 0;
+  const WsLayout w = ws_layout(c, fp8, ntq, ntf, ntb);
   uint8_t* base = static_cast<uint8_t*>(ws);
 
   PackParams pp{};
@@ -894,6 +943,8 @@ cudaError_t hyq_launch_prefill(const hyq_config* c, int dtype, const void* q, in
   pp.vq = base + w.vq;
   pp.kf = base + w.kf;
   pp.vf = base + w.vf;
+  pp.kb = base + w.kb;
+  pp.vb = base + w.vb;
   pp.kpos = reinterpret_cast<int32_t*>(base + w.kpos);
   pp.fpos = reinterpret_cast<int32_t*>(base + w.fpos);
   pp.sk = reinterpret_cast<float*>(base + w.sk);
@@ -906,7 +957,8 @@ cudaError_t hyq_launch_prefill(const hyq_config* c, int dtype, const void* q, in
   pp.nfp = nfp;
   pp.ntq = ntq;
   pp.ntf = ntf;
-  dim3 g1(2 * ntq + 2 * ntf, c->num_kv_heads, c->batch);
+  pp.ntb = ntb;
+  dim3 g1(2 * ntq + 2 * ntf + 2 * ntb, c->num_kv_heads, c->batch);
   if (fp8) pack_kernel<true><<<g1, 256, 0, s>>>(pp);
   else pack_kernel<false><<<g1, 256, 0, s>>>(pp);
   cudaError_t e = cudaGetLastError();
@@ -919,6 +971,8 @@ cudaError_t hyq_launch_prefill(const hyq_config* c, int dtype, const void* q, in
   mp.vq = pp.vq;
   mp.kf = pp.kf;
   mp.vf = pp.vf;
+  mp.kb = pp.kb;
+  mp.vb = pp.vb;
   mp.kpos = pp.kpos;
   mp.fpos = pp.fpos;
   mp.sk = pp.sk;
@@ -930,14 +984,10 @@ cudaError_t hyq_launch_prefill(const hyq_config* c, int dtype, const void* q, in
   mp.HKV = c->num_kv_heads;
   mp.ntq = ntq;
   mp.ntf = ntf;
+  mp.ntb = ntb;
+  mp.W = c->window;
   mp.alpha_log2e = kLog2e / sqrtf(static_cast<float>(HYQ_D));
   dim3 g2(c->num_q_heads, (L + kRows - 1) / kRows, c->batch);
-  if (fp8) {
-    if ((e = set_attrs<true>()) != cudaSuccess) return e;
-    prefill_kernel<true><<<g2, kThreads, kSmemBytes, s>>>(mp);
-  } else {
-    if ((e = set_attrs<false>()) != cudaSuccess) return e;
-    prefill_kernel<false><<<g2, kThreads, kSmemBytes, s>>>(mp);
-  }
-  return cudaGetLastError();
+  if (fp8) return band ? launch_main<true, true>(mp, g2, s) : launch_main<true, false>(mp, g2, s);
+  return band ? launch_main<false, true>(mp, g2, s) : launch_main<false, false>(mp, g2, s);
 }

@@ -141,6 +141,7 @@ typedef struct {
 #define HYQ_OP_DECODE 2
 #define HYQ_OP_PREFILL 3
 #define HYQ_OP_SELECT_MASS 4
+#define HYQ_OP_PREFILL_BAND 5
 
 #define HYQ_PREFILL_INT8 1
 #define HYQ_PREFILL_FP8 2
@@ -322,6 +323,29 @@ hyq_status hyq_prefill_attention(const hyq_config *cfg, int32_t dtype, const voi
                                  const void *k, const void *v, int32_t ldk, int32_t L,
                                  const int32_t *vl_idx, int32_t kvl, void *out, int32_t *err,
                                  void *ws, size_t ws_bytes, hyq_stream_t stream);
+
+/*
+ * Hybrid-precision prefill attention with the window taken per query (a
+ * diagonal band) instead of as the last W positions: the reading of
+ * Algorithm 2's window (Appendix A.2) in which every query keeps its own most
+ * recent keys in full precision.  Query row i sees
+ *   - the keys (i - W, i] as BF16 rows (its band),
+ *   - the vertical lines at or before i - W as BF16 rows,
+ *   - every other key at or before i - W from the quantised prefix,
+ * where vl_idx, the quantised-prefix positions ([0, P) minus vl_idx), their
+ * tiles, scales and codes, and the query scales are exactly those of
+ * hyq_prefill_attention (for every row i - W <= P - 1, so no other key is
+ * needed in quantised form).  The last row, and every row when W = 0, equal
+ * hyq_prefill_attention's.  Arguments, layouts, error reporting and
+ * asynchrony as hyq_prefill_attention.
+ * Workspace: hyq_workspace_size(cfg, HYQ_OP_PREFILL_BAND, L) covers every
+ * call with context length <= L and kvl <= hyq_vl_count(cfg, P); it holds
+ * BF16 images of all L key and value rows in addition to the code images.
+ */
+hyq_status hyq_prefill_attention_band(const hyq_config *cfg, int32_t dtype, const void *q,
+                                      int32_t ldq, const void *k, const void *v, int32_t ldk,
+                                      int32_t L, const int32_t *vl_idx, int32_t kvl, void *out,
+                                      int32_t *err, void *ws, size_t ws_bytes, hyq_stream_t stream);
 
 /*
  * One decode step in one launch: hyq_decode_append followed by

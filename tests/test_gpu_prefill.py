@@ -14,7 +14,8 @@ import torch
 
 from gen import prefill_case
 from hybrid_precision_quantized_gb300 import _lib as L
-from hybrid_precision_quantized_gb300 import hyq_prefill_attention, hyq_read_device_error, make_config, workspace
+from hybrid_precision_quantized_gb300 import (hyq_prefill_attention, hyq_prefill_attention_band,
+                                              hyq_read_device_error, make_config, workspace)
 from oracle.prefill import hybrid_prefill
 from oracle.select import select_vertical
 from tests.gpu_util import assert_prefill_close, to_np
@@ -31,16 +32,17 @@ def vl_for(c, Lc, W, ppm):
     return idx
 
 
-def run_gpu(c, Lc, W, ppm, dtype, idx, ws_len=None):
+def run_gpu(c, Lc, W, ppm, dtype, idx, ws_len=None, band=False):
     B, HQ = c.q.shape[:2]
     HKV = c.k.shape[1]
     cfg = make_config(B, HQ, HKV, capacity=max(Lc, ws_len or 0, 1), window=W, rho_ppm=ppm)
     kvl = idx.shape[-1]
     vl = torch.from_numpy(np.ascontiguousarray(idx)).to(torch.int32).cuda() if kvl else None
-    ws = workspace(cfg, L.OP_PREFILL, ws_len or Lc)
+    ws = workspace(cfg, L.OP_PREFILL_BAND if band else L.OP_PREFILL, ws_len or Lc)
     out = torch.full((B, HQ, Lc, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    hyq_prefill_attention(cfg, DT[dtype], c.q.cuda(), c.k.cuda(), c.v.cuda(), Lc, vl, kvl, out, ws, err)
+    fn = hyq_prefill_attention_band if band else hyq_prefill_attention
+    fn(cfg, DT[dtype], c.q.cuda(), c.k.cuda(), c.v.cuda(), Lc, vl, kvl, out, ws, err)
     torch.cuda.synchronize()
     assert hyq_read_device_error(err) == 0
     return to_np(out)
@@ -138,3 +140,68 @@ def test_prefill_llama_shaped_32k_sampled(hyq, dtype):
             rows = slice(128 * blk, 128 * blk + 128)
             assert_prefill_close(got[:, hq, rows], want[:, hq, rows], a[:, hq, rows],
                                  what=f"{dtype} head {hq} block {blk}")
+
+
+# --- per-query band window (hyq_prefill_attention_band) --------------------
+
+def oracle_band(c, idx, W, dtype, **kw):
+    return hybrid_prefill(c.q.double().numpy(), c.k.double().numpy(), c.v.double().numpy(),
+                          idx if idx.shape[-1] else None, W, dtype, return_abs=True, band=True, **kw)
+
+
+@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+@pytest.mark.parametrize("seed,B,HQ,HKV,Lc,W,ppm", [
+    (41, 1, 4, 2, 300, 64, 50_000),     # a few tiles, ragged tails
+    (42, 1, 8, 2, 1000, 128, 50_000),   # the band spans two key tiles per query block
+    (43, 2, 4, 4, 515, 100, 20_000),    # W not a multiple of the tile, two sequences
+    (44, 1, 16, 2, 777, 200, 50_000),   # W > one tile: up to three band tiles
+    (45, 1, 6, 2, 1100, 1, 100_000),    # W = 1: the band is the query's own key
+])
+def test_prefill_band_parity(hyq, dtype, seed, B, HQ, HKV, Lc, W, ppm):
+    c = prefill_case(seed, B, HQ, HKV, Lc, window=W, sink_frac=0.02)
+    idx = vl_for(c, Lc, W, ppm)
+    got = run_gpu(c, Lc, W, ppm, dtype, idx, band=True)
+    want, a = oracle_band(c, idx, W, dtype)
+    assert_prefill_close(got, want, a, what=f"band {dtype} L={Lc} W={W}")
+
+
+@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+@pytest.mark.parametrize("Lc,W,ppm,what", [
+    (1, 128, 50_000, "single position"),
+    (100, 128, 50_000, "sequence inside the window: all BF16"),
+    (129, 128, 50_000, "P = 1"),
+    (600, 0, 0, "W = 0: no band, all quantised"),
+    (600, 64, 1_000_000, "rho = 100%: no quantised keys"),
+    (257, 128, 50_000, "two query blocks, one row in the second"),
+])
+def test_prefill_band_edge_cases(hyq, dtype, Lc, W, ppm, what):
+    c = prefill_case(46, 1, 4, 2, Lc, window=W, sink_frac=0.03)
+    idx = vl_for(c, Lc, W, ppm) if W < Lc else np.zeros((1, 2, 0), np.int64)
+    got = run_gpu(c, Lc, W, ppm, dtype, idx, band=True)
+    want, a = oracle_band(c, idx, W, dtype)
+    assert_prefill_close(got, want, a, what=what)
+
+
+def test_prefill_band_last_row_matches_fixed_window(hyq):
+    """Both GPU entry points give the same last row (its band is the fixed
+    window) up to the summation order of the two kernels' tiles."""
+    c = prefill_case(47, 1, 8, 2, 900, window=128)
+    idx = vl_for(c, 900, 128, 50_000)
+    band = run_gpu(c, 900, 128, 50_000, "fp8", idx, band=True)
+    fixed = run_gpu(c, 900, 128, 50_000, "fp8", idx)
+    np.testing.assert_allclose(band[:, :, -1], fixed[:, :, -1], rtol=1e-2, atol=2e-3)
+
+
+@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+def test_prefill_band_llama_shaped_8k_sampled(hyq, dtype):
+    """Llama-3.1-8B-shaped heads at 8K with the per-query band: every head of
+    four query blocks (first, second, a middle one, last) against the oracle."""
+    Lc, W, ppm = 8192, 128, 50_000
+    c = prefill_case(1007, 1, 32, 8, Lc, window=W, sink_frac=0.02)
+    idx = vl_for(c, Lc, W, ppm)
+    got = run_gpu(c, Lc, W, ppm, dtype, idx, band=True)
+    blocks = [0, 1, 40, Lc // 128 - 1]
+    want, a = oracle_band(c, idx, W, dtype, query_blocks=blocks)
+    for blk in blocks:
+        rows = slice(128 * blk, 128 * blk + 128)
+        assert_prefill_close(got[:, :, rows], want[:, :, rows], a[:, :, rows], what=f"band {dtype} block {blk}")
