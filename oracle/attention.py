@@ -45,11 +45,13 @@ def textbook_attention(q, K, V, alpha: float) -> np.ndarray:
     return (e @ V) / e.sum(axis=-1, keepdims=True)
 
 
-def effective_cache(k_src, v_src, L: int, P: int, idx, bits: int = 4):
+def effective_cache(k_src, v_src, L: int, P: int, idx, bits: int = 4, bits_v: int | None = None):
     """Effective (K~, V~) of Eq. 8 for every (b, kvh): float64 [B, HKV, L, d].
 
     Positions in [0, P) not in ``idx[b, kvh]`` are replaced by
-    DeQuant(Quant(.)); ``idx`` (vertical-line positions) and [P, L) stay as
+    DeQuant(Quant(.)) with B_K = ``bits`` for keys and B_V = ``bits_v``
+    (default: ``bits``) for values (Algorithm 4 quantises K and V with their
+    own bit-widths); ``idx`` (vertical-line positions) and [P, L) stay as
     given.  ``idx`` may be None (no vertical-line set).
     """
     K = np.array(np.asarray(k_src, dtype=np.float64)[:, :, :L, :])
@@ -64,21 +66,22 @@ def effective_cache(k_src, v_src, L: int, P: int, idx, bits: int = 4):
             for h in range(HKV):
                 keep[b, h, idx[b, h]] = True
     Kq = fake_quant(K[:, :, :P, :], bits)
-    Vq = fake_quant(V[:, :, :P, :], bits)
+    Vq = fake_quant(V[:, :, :P, :], bits if bits_v is None else bits_v)
     K[:, :, :P, :] = np.where(keep[..., None], K[:, :, :P, :], Kq)
     V[:, :, :P, :] = np.where(keep[..., None], V[:, :, :P, :], Vq)
     return K, V
 
 
 def hybrid_decode(q, k_src, v_src, L: int, P: int, idx, bits: int = 4,
-                  alpha: float | None = None) -> np.ndarray:
-    """Hybrid decode output o [B, HQ, d] in float64 (plain definition)."""
+                  alpha: float | None = None, bits_v: int | None = None) -> np.ndarray:
+    """Hybrid decode output o [B, HQ, d] in float64 (plain definition);
+    ``bits`` / ``bits_v`` are B_K / B_V (``bits_v`` defaults to ``bits``)."""
     q = np.asarray(q, dtype=np.float64)
     B, HQ, d = q.shape
     HKV = np.asarray(k_src).shape[1]
     g = HQ // HKV
     a = 1.0 / math.sqrt(d) if alpha is None else alpha
-    K, V = effective_cache(k_src, v_src, L, P, idx, bits)
+    K, V = effective_cache(k_src, v_src, L, P, idx, bits, bits_v)
     out = np.zeros((B, HQ, d))
     for b in range(B):
         for kh in range(HKV):
@@ -115,7 +118,7 @@ def reduce_softmax(states):
 
 
 def decode_alg3(q, k_src, v_src, L: int, P: int, idx, splits: int = 4,
-                tile: int = 64, bits: int = 4) -> np.ndarray:
+                tile: int = 64, bits: int = 4, bits_v: int | None = None) -> np.ndarray:
     """Algorithm 3: quantised prefix in ``splits`` chunks (each its own
     FlashOS from (-inf, 0, 0)), ReduceSoftmax, then the vertical-line and the
     full-precision tail segments tile by tile; o = acc / l."""
@@ -124,7 +127,7 @@ def decode_alg3(q, k_src, v_src, L: int, P: int, idx, splits: int = 4,
     HKV = np.asarray(k_src).shape[1]
     g = HQ // HKV
     alpha = 1.0 / math.sqrt(d)
-    K, V = effective_cache(k_src, v_src, L, P, idx, bits)
+    K, V = effective_cache(k_src, v_src, L, P, idx, bits, bits_v)
     out = np.zeros((B, HQ, d))
     for b in range(B):
         for kh in range(HKV):

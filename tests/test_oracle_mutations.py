@@ -67,6 +67,8 @@ MUTATIONS = [
      "for seg in (vl, np.arange(max(P, 0) + 1, L)):", "tail segment off by one"),
     ("attention", "logits = alpha * (q @ K.T)", "logits = alpha * (q @ K.T) * 1.0001",
      "perturbed logit scale"),
+    ("attention", "Vq = fake_quant(V[:, :, :P, :], bits if bits_v is None else bits_v)",
+     "Vq = fake_quant(V[:, :, :P, :], bits)", "values quantised at the key width"),
     ("prefill", "lg = np.where(pos[None, :] <= rows[:, None], lg, -np.inf)",
      "lg = np.where(pos[None, :] < rows[:, None] + 2, lg, -np.inf)", "causal mask off by one"),
     ("prefill", "alpha * qb @ Kall[nq:].T], axis=1)", "alpha * qhat @ Kall[nq:].T], axis=1)",
