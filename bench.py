@@ -49,6 +49,8 @@ def parse():
     p.add_argument("--layers", type=int, default=N_LAYERS)
     p.add_argument("--no-baseline", action="store_true", help="skip the CPU oracle timing")
     p.add_argument("--no-prefill", action="store_true", help="skip the prefill measurement")
+    p.add_argument("--no-widths", action="store_true",
+                   help="skip the code-width variants (K8V8, K4V8) of the decode period")
     p.add_argument("--no-batched", action="store_true", help="skip the batch-16 decode measurement")
     p.add_argument("--decode-plan", type=int, nargs=2, default=(0, 0), metavar=("MERGE", "SPLITS"),
                    help="tuning: hyq_set_decode_plan(MERGE, SPLITS) for the period (0 0 = automatic)")
@@ -291,24 +293,31 @@ def job_value(ms_total, steps, units_per_rank, world):
     return ms_total / steps * 1e3 / (units_per_rank * world)
 
 
-def algorithmic_bytes(n_q, n_vl, n_tail):
-    """Bytes one decode-attention call must move (B=1 layer): 160 per 4-bit
-    row (K+V codes, FP16 scale+zero), 512 per BF16 row (K+V), q and out."""
-    return B * (HKV * (n_q * 160 + (n_vl + n_tail) * 512) + 2 * HQ * D * 2)
+def q_row_bytes(bits_k=4, bits_v=4):
+    """Bytes of one quantised position (K and V): d B / 8 code bytes plus four
+    FP16 (scale, zero) pairs per tensor; 160 for K4V4, 288 for K8V8."""
+    return D * (bits_k + bits_v) // 8 + 2 * (D // 32) * 4
 
 
-def period_bytes_per_decode():
+def algorithmic_bytes(n_q, n_vl, n_tail, q_row=160):
+    """Bytes one decode-attention call must move (B=1 layer): q_row per
+    quantised row (K+V codes, FP16 scale+zero; 160 at 4 bits), 512 per BF16
+    row (K+V), q and out."""
+    return B * (HKV * (n_q * q_row + (n_vl + n_tail) * 512) + 2 * HQ * D * 2)
+
+
+def period_bytes_per_decode(q_row=160):
     """Mean algorithmic bytes of the 64 decode calls of one period."""
     P0 = L0 - WINDOW
     k0 = -(-P0 * RHO_PPM // 1_000_000)
     tot = 0
     for t in range(PERIOD):
         if t < PERIOD - 1:
-            tot += algorithmic_bytes(P0 - k0, k0, WINDOW + t + 1)
+            tot += algorithmic_bytes(P0 - k0, k0, WINDOW + t + 1, q_row)
         else:
             P = CTX - WINDOW
             k = -(-P * RHO_PPM // 1_000_000)
-            tot += algorithmic_bytes(P - k, k, WINDOW)
+            tot += algorithmic_bytes(P - k, k, WINDOW, q_row)
     return tot / PERIOD
 
 
@@ -556,8 +565,10 @@ def run_ours(args, rank, world, local):
     # variants of the maintenance: frozen mode (Algorithm 4 as written: the
     # last token's maintenance is hyq_age_tail instead of re-selection) and
     # re-selection by the softmax-mass score of Eq. 4
-    def variant_period(**kw):
-        fr = PeriodRunner(cfg, k_srcs, v_srcs, L0, dev, prefetch_next=args.prefetch, **kw)
+    def variant_period(bits=(4, 4), **kw):
+        cfg_v = cfg if bits == (4, 4) else hyq.make_config(B, HQ, HKV, capacity=CTX, window=WINDOW, period=PERIOD,
+                                                            rho_ppm=RHO_PPM, bits_k=bits[0], bits_v=bits[1])
+        fr = PeriodRunner(cfg_v, k_srcs, v_srcs, L0, dev, prefetch_next=args.prefetch, **kw)
         fr.q_tok.copy_(q_tok)
         fr.k_tok.copy_(k_tok)
         fr.v_tok.copy_(v_tok)
@@ -567,21 +578,27 @@ def run_ours(args, rank, world, local):
             fr.run_period()
         torch.cuda.synchronize()
         f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        fev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(PERIOD)] for _ in range(args.steps)]
         f0.record()
-        for _ in range(args.steps):
-            fr.run_period()
+        for st in range(args.steps):
+            fr.run_period(fev[st])
         f1.record()
         torch.cuda.synchronize()
         fms = reduce_timing(f0.elapsed_time(f1), world, dev)
+        fdec_us = sum(a.elapsed_time(b) for row in fev for a, b in row) * 1e3 / (args.steps * PERIOD * nl)
+        fbytes = period_bytes_per_decode(q_row_bytes(*bits))
         res = {"value": job_value(fms, args.steps, PERIOD * nl, world), "unit": "us/token/layer",
                "ms_per_step": fms / args.steps, "launches_per_period": fr.launches_per_period,
+               "decode_us_per_token_layer": fdec_us,
+               "decode_gbs": fbytes / (fdec_us * 1e-6) / 1e9, "algorithmic_bytes_per_launch": fbytes,
                "device_error_word": max(hyq.hyq_read_device_error(l.err()) for l in fr.layers)}
         del fr
         return res
 
-    frozen = mass = None
+    frozen = mass = widths = None
     main_launches = run.launches_per_period
-    if not (args.no_frozen and args.no_mass):
+    if not (args.no_frozen and args.no_mass and args.no_widths):
         del run
     if not args.no_frozen:
         frozen = {"maintenance": "hyq_age_tail: tail rows older than the window quantised onto the 4-bit stream; "
@@ -589,6 +606,9 @@ def run_ours(args, rank, world, local):
     if not args.no_mass:
         mass = {"maintenance": "re-selection by the softmax-mass score of Eq. 4 (hyq_select_vertical_mass), "
                                "then rebuild", **variant_period(score="mass")}
+    if not args.no_widths:
+        widths = {f"K{bk}V{bv}": {"q_row_bytes": q_row_bytes(bk, bv), **variant_period(bits=(bk, bv))}
+                  for bk, bv in ((8, 8), (4, 8))}
 
     if rank != 0:
         return
@@ -626,6 +646,7 @@ def run_ours(args, rank, world, local):
         "batched": batched,
         "frozen": frozen,
         "mass_selection": mass,
+        "widths": widths,
         "prefill": ({"workload": "llama3.1-8b-shaped causal prefill, B1, 32/8 heads, d128, 32K, W128, rho 5% "
                                  "(pack + main kernel; window fixed: hyq_prefill_attention, band: "
                                  "hyq_prefill_attention_band)",

@@ -26,7 +26,16 @@ DEVERR_SCORE = 0x8
 DEVERR_TIMEOUT = 0x10
 
 QBLOCK_ROWS = 64
-QBLOCK_BYTES = 10240
+QBLOCK_BYTES = 10240          # B_K = B_V = 4
+
+
+def qtile_bytes(bits_k: int = 4, bits_v: int = 4) -> int:
+    """Bytes of one 16-row quantised tile (include/hyq.h)."""
+    return 256 * ((bits_k or 4) + (bits_v or 4)) + 512
+
+
+def qblock_bytes(bits_k: int = 4, bits_v: int = 4) -> int:
+    return 4 * qtile_bytes(bits_k, bits_v)
 COUNTS = 8
 CNT_NQ, CNT_NVL, CNT_NTAIL, CNT_LEN, CNT_RING_N, CNT_RING_POS = range(6)
 LAYOUT_FIELDS = ("qblocks", "vl_k", "vl_v", "vl_idx", "tail_k", "tail_v", "q_ring", "counts", "err")
@@ -47,7 +56,8 @@ NOALLOC_SCRATCH_BYTES = 4 << 20
 class HyqConfig(ctypes.Structure):
     _fields_ = [("batch", c_int32), ("num_q_heads", c_int32), ("num_kv_heads", c_int32),
                 ("head_dim", c_int32), ("group", c_int32), ("window", c_int32),
-                ("period", c_int32), ("rho_ppm", c_int32), ("capacity", c_int32)]
+                ("period", c_int32), ("rho_ppm", c_int32), ("capacity", c_int32),
+                ("bits_k", c_int32), ("bits_v", c_int32)]
 
 
 class HyqLayout(ctypes.Structure):

@@ -13,10 +13,10 @@ from ._lib import HyqConfig, HyqLayout
 
 
 def make_config(batch, num_q_heads, num_kv_heads, capacity, window=128, period=64,
-                rho_ppm=50_000, head_dim=128, group=32) -> HyqConfig:
+                rho_ppm=50_000, head_dim=128, group=32, bits_k=4, bits_v=4) -> HyqConfig:
     return HyqConfig(batch=batch, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
                      head_dim=head_dim, group=group, window=window, period=period,
-                     rho_ppm=rho_ppm, capacity=capacity)
+                     rho_ppm=rho_ppm, capacity=capacity, bits_k=bits_k, bits_v=bits_v)
 
 
 class HybridLayer:
@@ -40,8 +40,9 @@ class HybridLayer:
     def qblocks(self) -> torch.Tensor:
         c = self.cfg
         nblk = -(-c.capacity // L.QBLOCK_ROWS)
-        n = c.batch * c.num_kv_heads * nblk * L.QBLOCK_BYTES
-        return self.buf["qblocks"][:n].view(c.batch, c.num_kv_heads, nblk, L.QBLOCK_BYTES)
+        bb = L.qblock_bytes(c.bits_k, c.bits_v)
+        n = c.batch * c.num_kv_heads * nblk * bb
+        return self.buf["qblocks"][:n].view(c.batch, c.num_kv_heads, nblk, bb)
 
     def cap_vl(self) -> int:
         c = self.cfg
@@ -89,9 +90,28 @@ def workspace(cfg: HyqConfig, op: int, len_hint: int = 0, device="cuda") -> torc
     return torch.zeros(n, dtype=torch.uint8, device=device)
 
 
-# --- 4-bit stream reader/writer (documented format of include/hyq.h) -------
+# --- quantised stream reader/writer (documented format of include/hyq.h) ---
 
-TILE_BYTES = 2560
+TILE_BYTES = 2560   # B_K = B_V = 4
+
+
+def _tile_maps8():
+    """(row, element) of every byte of a 2048-byte 8-bit code region, for the K
+    and the V orders, indexed by byte offset."""
+    krow = np.zeros(2048, np.int64)
+    kel = np.zeros(2048, np.int64)
+    vrow = np.zeros(2048, np.int64)
+    vel = np.zeros(2048, np.int64)
+    for u in range(16):
+        for lane in range(32):
+            g, t = lane // 4, lane % 4
+            base = 512 * (u // 4) + 16 * lane + 4 * (u % 4)
+            for j in range(4):
+                krow[base + j] = g + 8 * (u % 2)
+                kel[base + j] = 16 * (u // 2) + 4 * t + (0, 2, 1, 3)[j]
+                vrow[base + j] = 2 * t + (0, 8, 1, 9)[j]
+                vel[base + j] = 32 * (u // 4) + 4 * g + 2 * ((u // 2) % 2) + u % 2
+    return krow, kel, vrow, vel
 
 
 def _tile_maps():
@@ -115,65 +135,81 @@ def _tile_maps():
     return krow, kel, vrow, vel
 
 
-_MAPS = None
+_MAPS = {}
 
 
-def _maps():
-    global _MAPS
-    if _MAPS is None:
-        _MAPS = _tile_maps()
-    return _MAPS
+def _maps(bits=4):
+    if bits not in _MAPS:
+        _MAPS[bits] = _tile_maps() if bits == 4 else _tile_maps8()
+    return _MAPS[bits]
 
 
-def unpack_qblocks(blocks: np.ndarray, n_rows: int):
-    """Decode the first ``n_rows`` rows of a 4-bit stream.
+def _regions(bits_k, bits_v):
+    """(offset, bits, 0 = K | 1 = V) of the two code regions, and the K / V
+    metadata offsets, of a tile."""
+    ck, cv = 256 * bits_k, 256 * bits_v
+    return ((0, bits_k, 0), (ck, bits_v, 1)), ck + cv, ck + cv + 256
 
-    blocks : uint8 [nblk, 10240] or [ntiles * 2560] (one (batch, KV head) stream)
+
+def unpack_qblocks(blocks: np.ndarray, n_rows: int, bits_k: int = 4, bits_v: int = 4):
+    """Decode the first ``n_rows`` rows of a quantised stream.
+
+    blocks : uint8 [nblk, qblock_bytes] or [ntiles * qtile_bytes] (one
+    (batch, KV head) stream of B_K-bit keys and B_V-bit values)
     Returns k_codes, v_codes uint8 [n_rows, 128]; k_scale, k_zero, v_scale,
     v_zero float16 [n_rows, 4].
     """
-    krow, kel, vrow, vel = _maps()
-    tiles = np.asarray(blocks, dtype=np.uint8).reshape(-1, TILE_BYTES)
+    regions, mk, mv = _regions(bits_k, bits_v)
+    tiles = np.asarray(blocks, dtype=np.uint8).reshape(-1, L.qtile_bytes(bits_k, bits_v))
     nt = tiles.shape[0]
-    kc = np.zeros((nt * 16, 128), np.uint8)
-    vc = np.zeros((nt * 16, 128), np.uint8)
-    for ti in range(nt):
-        for off, codes, rmap, emap in ((0, kc, krow, kel), (1024, vc, vrow, vel)):
-            raw = tiles[ti, off:off + 1024]
-            nib = np.stack([raw & 15, raw >> 4], axis=1).reshape(-1)
-            codes[ti * 16 + rmap, emap] = nib
-    meta_k = tiles[:, 2048:2304].copy().view(np.float16).reshape(nt * 16, 4, 2)
-    meta_v = tiles[:, 2304:2560].copy().view(np.float16).reshape(nt * 16, 4, 2)
+    out = [np.zeros((nt * 16, 128), np.uint8), np.zeros((nt * 16, 128), np.uint8)]
+    for off, bits, kv in regions:
+        maps = _maps(bits)
+        rmap, emap = maps[2 * kv], maps[2 * kv + 1]
+        size = 256 * bits      # code bytes of 16 rows
+        for ti in range(nt):
+            raw = tiles[ti, off:off + size]
+            vals = np.stack([raw & 15, raw >> 4], axis=1).reshape(-1) if bits == 4 else raw
+            out[kv][ti * 16 + rmap, emap] = vals
+    meta_k = tiles[:, mk:mk + 256].copy().view(np.float16).reshape(nt * 16, 4, 2)
+    meta_v = tiles[:, mv:mv + 256].copy().view(np.float16).reshape(nt * 16, 4, 2)
     n = n_rows
+    kc, vc = out
     return (kc[:n], vc[:n], meta_k[:n, :, 0], meta_k[:n, :, 1], meta_v[:n, :, 0], meta_v[:n, :, 1])
 
 
-def pack_qblocks(k_codes, v_codes, k_scale, k_zero, v_scale, v_zero) -> np.ndarray:
+def pack_qblocks(k_codes, v_codes, k_scale, k_zero, v_scale, v_zero, bits_k: int = 4,
+                 bits_v: int = 4) -> np.ndarray:
     """Inverse of ``unpack_qblocks``: rows padded with zeros to whole 64-row
-    blocks; returns uint8 [nblk, 10240]."""
-    krow, kel, vrow, vel = _maps()
+    blocks; returns uint8 [nblk, qblock_bytes(bits_k, bits_v)]."""
+    regions, mk, mv = _regions(bits_k, bits_v)
     n = k_codes.shape[0]
     nblk = -(-n // 64)
     nt = 4 * nblk
-    tiles = np.zeros((nt, TILE_BYTES), np.uint8)
+    tiles = np.zeros((nt, L.qtile_bytes(bits_k, bits_v)), np.uint8)
 
     def pad(a, shape, dtype):
         z = np.zeros(shape, dtype)
         z[: a.shape[0]] = a
         return z
 
-    kc = pad(np.asarray(k_codes), (nt * 16, 128), np.uint8)
-    vc = pad(np.asarray(v_codes), (nt * 16, 128), np.uint8)
-    for ti in range(nt):
-        for off, codes, rmap, emap in ((0, kc, krow, kel), (1024, vc, vrow, vel)):
-            nib = codes[ti * 16 + rmap, emap].reshape(1024, 2)
-            tiles[ti, off:off + 1024] = nib[:, 0] | (nib[:, 1] << 4)
-    for off, sc, zr in ((2048, k_scale, k_zero), (2304, v_scale, v_zero)):
+    codes = [pad(np.asarray(k_codes), (nt * 16, 128), np.uint8), pad(np.asarray(v_codes), (nt * 16, 128), np.uint8)]
+    for off, bits, kv in regions:
+        maps = _maps(bits)
+        rmap, emap = maps[2 * kv], maps[2 * kv + 1]
+        size = 256 * bits      # code bytes of 16 rows
+        for ti in range(nt):
+            vals = codes[kv][ti * 16 + rmap, emap]
+            if bits == 4:
+                nib = vals.reshape(size, 2)
+                vals = nib[:, 0] | (nib[:, 1] << 4)
+            tiles[ti, off:off + size] = vals
+    for off, sc, zr in ((mk, k_scale, k_zero), (mv, v_scale, v_zero)):
         m = np.zeros((nt * 16, 4, 2), np.float16)
         m[:n, :, 0] = sc
         m[:n, :, 1] = zr
         tiles[:, off:off + 256] = m.view(np.uint8).reshape(nt, 256)
-    return tiles.reshape(nblk, 10240)
+    return tiles.reshape(nblk, 4 * L.qtile_bytes(bits_k, bits_v))
 
 
 class HybridDecoder:

@@ -63,6 +63,8 @@ extern "C" hyq_status hyq_config_check(const hyq_config* c) {
   if (c->rho_ppm < 0 || c->rho_ppm > 1000000) return HYQ_ERR_INVALID_ARG;
   if (c->capacity < 1 || c->capacity > (1 << 30)) return HYQ_ERR_INVALID_ARG;
   if (c->batch > 65535 || c->num_kv_heads > 65535) return HYQ_ERR_INVALID_ARG;
+  if ((c->bits_k != 0 && c->bits_k != 4 && c->bits_k != 8) || (c->bits_v != 0 && c->bits_v != 4 && c->bits_v != 8))
+    return HYQ_ERR_UNSUPPORTED;
   return HYQ_OK;
 }
 
@@ -87,7 +89,7 @@ extern "C" hyq_status hyq_layout_sizes(const hyq_config* c, size_t* out) {
   size_t bh = (size_t)c->batch * c->num_kv_heads;
   size_t cap_vl = hyq_vl_stride(c);
   size_t cap_tail = hyq_cap_tail(c);
-  out[0] = round_up(bh * hyq_nblk(c) * HYQ_QBLOCK_BYTES);
+  out[0] = round_up(bh * hyq_nblk(c) * hyq_qblock_bytes(c));
   out[1] = round_up(bh * cap_vl * HYQ_D * 2);
   out[2] = out[1];
   out[3] = round_up(bh * cap_vl * 4);

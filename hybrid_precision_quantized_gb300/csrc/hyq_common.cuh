@@ -27,6 +27,23 @@ inline int32_t hyq_cap_tail(const hyq_config* c) { return c->window + c->period;
 // Row stride of the vertical-line buffers (at least one row is allocated).
 inline int32_t hyq_vl_stride(const hyq_config* c) { return hyq_cap_vl(c) > 0 ? hyq_cap_vl(c) : 1; }
 inline int32_t hyq_nblk(const hyq_config* c) { return (c->capacity + HYQ_QBLOCK_ROWS - 1) / HYQ_QBLOCK_ROWS; }
+// Code widths B_K / B_V (a zero field means 4) and the stream's block size.
+inline int hyq_bits_k(const hyq_config* c) { return c->bits_k == 0 ? 4 : c->bits_k; }
+inline int hyq_bits_v(const hyq_config* c) { return c->bits_v == 0 ? 4 : c->bits_v; }
+inline size_t hyq_qblock_bytes(const hyq_config* c) {
+  return HYQ_QBLOCK_BYTES_BITS((size_t)hyq_bits_k(c), (size_t)hyq_bits_v(c));
+}
+
+// Byte layout of one 16-row quantised tile with B_K-bit keys and B_V-bit values.
+template <int BK, int BV>
+struct QFmt {
+  static_assert((BK == 4 || BK == 8) && (BV == 4 || BV == 8), "code widths are 4 or 8 bits");
+  static constexpr int kVCode = 256 * BK;        // K codes at 0, V codes here
+  static constexpr int kKMeta = 256 * (BK + BV);  // K (scale, zero) pairs
+  static constexpr int kVMeta = kKMeta + 256;     // V (scale, zero) pairs
+  static constexpr int kTile = HYQ_QTILE_BYTES_BITS(BK, BV);
+  static constexpr int kBlock = 4 * kTile;
+};
 
 // Kernel launchers (return the launch's cudaError_t).
 cudaError_t hyq_launch_age_tail(const hyq_config* c, const hyq_layout* lay, cudaStream_t s);

@@ -37,14 +37,24 @@ namespace {
 
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
-constexpr int kSlots = 3;                                     // 4-bit tiles in flight per warp
-constexpr int kRingBytes = kWarps * kSlots * HYQ_QTILE_BYTES; // 120 KiB of rings
+constexpr int kMaxSlots = 3;
 // BF16 tiles staged in shared memory by a few contiguous bulk copies (K rows,
 // then V rows, 256 bytes each): a handful of copies instead of one per row.
 constexpr int kFKStride = 256, kFVStride = 256;
 constexpr int kFTileBytes = 16 * kFKStride + 16 * kFVStride;  // 8192
 constexpr int kFStaged = 7;                                     // staged BF16 tiles per block
-constexpr int kSmemBytes = kRingBytes + kFStaged * kFTileBytes;
+
+// Shared-memory plan for B_K-bit keys and B_V-bit values: each warp streams
+// its quantised tiles through a ring of kSlots tiles (3 of 2560 bytes for
+// 4-bit codes: 120 KiB of rings; 2 of the larger 8-bit tiles), followed by
+// the staged BF16 tiles.
+template <int BK, int BV>
+struct Dec : QFmt<BK, BV> {
+  static constexpr int kSlots = (BK == 4 && BV == 4) ? 3 : 2;
+  static constexpr int kRingBytes = kWarps * kSlots * QFmt<BK, BV>::kTile;
+  static constexpr int kSmemBytes = kRingBytes + kFStaged * kFTileBytes;
+  static_assert(kSlots <= kMaxSlots, "ring barriers");
+};
 constexpr int kPart = 2 + HYQ_D;                              // m, l, acc[128] per head
 constexpr int kMaxSplits = 1024;
 // log2(e) / sqrt(128): logits are kept in the base-2 domain.
@@ -144,14 +154,15 @@ __device__ __forceinline__ NextCounts next_counts(const StepArgs& sa, int b, int
 }
 
 // One warp, once the block has read its share of this layer: prefetch into
-// L2 the next layout's 4-bit tiles [t0, t1) of KV head bh, the share of
+// L2 the next layout's quantised tiles [t0, t1) of KV head bh, the share of
 // block `split` under the same partition (contiguous, 16 KB per lane).
+template <int kTileBytes>
 __device__ void prefetch_next_tiles(const StepArgs& sa, const NextCounts& n, size_t bh, int split, int S,
                                     int nblk_cap, int lane) {
   const int nt = (n.nq + 15) >> 4;
   const int t0 = share_bound(split, nt, S), t1 = share_bound(split + 1, nt, S);
-  const uint8_t* tiles = sa.nx_qblocks + bh * (size_t)nblk_cap * HYQ_QBLOCK_BYTES + (size_t)t0 * HYQ_QTILE_BYTES;
-  const uint32_t bytes = (uint32_t)(t1 - t0) * HYQ_QTILE_BYTES;
+  const uint8_t* tiles = sa.nx_qblocks + bh * (size_t)nblk_cap * (4 * kTileBytes) + (size_t)t0 * kTileBytes;
+  const uint32_t bytes = (uint32_t)(t1 - t0) * kTileBytes;
   constexpr uint32_t kChunk = 16384;
   for (uint32_t off = lane * kChunk; off < bytes; off += 32 * kChunk)
     prefetch_l2(tiles + off, min(kChunk, bytes - off));
@@ -259,28 +270,59 @@ struct QConst {
   float qs[2][4]; // per-group query sums of heads 2t, 2t+1, times log2(e)/sqrt(d)
 };
 
-// One 16-row 4-bit tile (2560 bytes at `tb`), `vr` valid rows.  The codes
-// enter the fp16 MMAs as subnormals: the low nibble of a byte as c * 2^-24,
-// the high nibble, masked in place, as 16 c * 2^-24.  In both code orders the
-// high nibbles are exactly fragment rows g+8 (K: tokens g+8; V: output rows
-// g+8), so the factor 16 is a per-row constant: folded into ksc[1] for K and
-// into the epilogue for V.  bq holds the query as fp16, scaled by 2^e.
+// The two codes of bytes 1 and 3 of w as the low bytes of two 16-bit halves.
+__device__ __forceinline__ uint32_t odd_bytes(uint32_t w) { return __byte_perm(w, 0u, 0x4341); }
+
+// `n` 32-bit words of a code region: word u of this lane at
+// 512 (u / 4) + 16 lane + 4 (u % 4).
+template <int n>
+__device__ __forceinline__ void load_words(const uint8_t* region, int lane, uint32_t (&w)[n]) {
+#pragma unroll
+  for (int i = 0; i < n / 4; ++i) {
+    const uint4 v = *reinterpret_cast<const uint4*>(region + 512 * i + 16 * lane);
+    w[4 * i] = v.x;
+    w[4 * i + 1] = v.y;
+    w[4 * i + 2] = v.z;
+    w[4 * i + 3] = v.w;
+  }
+}
+
+// One 16-row quantised tile at `tb` (byte layout QFmt<BK, BV>), `vr` valid
+// rows.  The codes enter the fp16 MMAs as subnormals c * 2^-24.  4-bit: the
+// low nibble of a byte as c * 2^-24, the high nibble, masked in place, as
+// 16 c * 2^-24; in both code orders the high nibbles are exactly fragment
+// rows g+8 (K: tokens g+8; V: output rows g+8), so the factor 16 is a
+// per-row constant: folded into ksc[1] for K and into the epilogue for V.
+// 8-bit: bytes 0 and 2 of a word by one AND, bytes 1 and 3 by one byte
+// permute, each a fragment register of two codes.  bq holds the query as
+// fp16, scaled by 2^e.
+template <int BK, int BV>
 __device__ __forceinline__ void q_tile(const uint8_t* tb, int lane, int vr, const uint32_t (&bq)[8][2],
                                        const QConst& qc, State& st) {
+  using F = QFmt<BK, BV>;
   const int g = lane >> 2;
-  const uint4 kw0 = *reinterpret_cast<const uint4*>(tb + lane * 16);
-  const uint4 kw1 = *reinterpret_cast<const uint4*>(tb + 512 + lane * 16);
-  const uint32_t kw[8] = {kw0.x, kw0.y, kw0.z, kw0.w, kw1.x, kw1.y, kw1.z, kw1.w};
   float C[4][4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) C[q][0] = C[q][1] = C[q][2] = C[q][3] = 0.f;
+  if (BK == 4) {
+    uint32_t kw[8];
+    load_words<8>(tb, lane, kw);
 #pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    const uint32_t w = kw[ks], w8 = w >> 8;
-    mma_f16(C[ks >> 1], w & 0x000F000Fu, w & 0x00F000F0u, w8 & 0x000F000Fu, w8 & 0x00F000F0u, bq[ks][0],
-            bq[ks][1]);
+    for (int ks = 0; ks < 8; ++ks) {
+      const uint32_t w = kw[ks], w8 = w >> 8;
+      mma_f16(C[ks >> 1], w & 0x000F000Fu, w & 0x00F000F0u, w8 & 0x000F000Fu, w8 & 0x00F000F0u, bq[ks][0],
+              bq[ks][1]);
+    }
+  } else {
+    uint32_t kw[16];  // k-step ks: word 2ks (token g), 2ks + 1 (token g + 8)
+    load_words<16>(tb, lane, kw);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const uint32_t w0 = kw[2 * ks], w1 = kw[2 * ks + 1];
+      mma_f16(C[ks >> 1], w0 & 0x00FF00FFu, w1 & 0x00FF00FFu, odd_bytes(w0), odd_bytes(w1), bq[ks][0], bq[ks][1]);
+    }
   }
-  const uint8_t* km = tb + 2048;
+  const uint8_t* km = tb + F::kKMeta;
   float lg[4];
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
@@ -301,10 +343,9 @@ __device__ __forceinline__ void q_tile(const uint8_t* tb, int lane, int vr, cons
   }
   float p[4];
   softmax_update(lg, st, p);
-  const uint4 vw0 = *reinterpret_cast<const uint4*>(tb + 1024 + lane * 16);
-  const uint4 vw1 = *reinterpret_cast<const uint4*>(tb + 1024 + 512 + lane * 16);
-  const uint32_t vw[8] = {vw0.x, vw0.y, vw0.z, vw0.w, vw1.x, vw1.y, vw1.z, vw1.w};
-  const uint8_t* vm = tb + 2304;
+  uint32_t vw[BV == 4 ? 8 : 16];
+  load_words<BV == 4 ? 8 : 16>(tb + F::kVCode, lane, vw);
+  const uint8_t* vm = tb + F::kVMeta;
   const uint4 mv0 = *reinterpret_cast<const uint4*>(vm + g * 16);
   const uint4 mv1 = *reinterpret_cast<const uint4*>(vm + (g + 8) * 16);
   const uint32_t m0[4] = {mv0.x, mv0.y, mv0.z, mv0.w};
@@ -323,15 +364,23 @@ __device__ __forceinline__ void q_tile(const uint8_t* tb, int lane, int vr, cons
     st.zacc[0][q] = fmaf(p[0], z0, fmaf(p[2], z1, st.zacc[0][q]));
     st.zacc[1][q] = fmaf(p[1], z0, fmaf(p[3], z1, st.zacc[1][q]));
 #pragma unroll
-    for (int mm = 0; mm < 2; ++mm) {
-      const uint32_t x = vw[2 * q + mm], x8 = x >> 8;  // m-tile 2q + mm lies in group q
-      mma_f16(st.acc[2 * q + mm], x & 0x000F000Fu, x & 0x00F000F0u, x8 & 0x000F000Fu, x8 & 0x00F000F0u, b0, b1);
+    for (int mm = 0; mm < 2; ++mm) {  // m-tile 2q + mm lies in group q
+      if (BV == 4) {
+        const uint32_t x = vw[2 * q + mm], x8 = x >> 8;
+        mma_f16(st.acc[2 * q + mm], x & 0x000F000Fu, x & 0x00F000F0u, x8 & 0x000F000Fu, x8 & 0x00F000F0u, b0, b1);
+      } else {  // m-tile mt: words 2mt (fragment rows g) and 2mt + 1 (rows g + 8)
+        const uint32_t y0 = vw[2 * (2 * q + mm)], y1 = vw[2 * (2 * q + mm) + 1];
+        mma_f16(st.acc[2 * q + mm], y0 & 0x00FF00FFu, y1 & 0x00FF00FFu, odd_bytes(y0), odd_bytes(y1), b0, b1);
+      }
     }
   }
 }
 
-// 16 x a bf16 pair (exact: a power of two).
-__device__ __forceinline__ uint32_t times16_bf16x2(uint32_t x) {
+// 16 x a bf16 pair (exact: a power of two); the identity for 8-bit values,
+// whose accumulator rows carry no factor.
+template <int BV>
+__device__ __forceinline__ uint32_t row_factor_bf16x2(uint32_t x) {
+  if (BV == 8) return x;
   __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&x);
   v = __hmul2(v, __floats2bfloat162_rn(16.f, 16.f));
   return *reinterpret_cast<uint32_t*>(&v);
@@ -343,7 +392,9 @@ __device__ __forceinline__ uint32_t u4c(const uint4& v, int i) {
 
 // One 16-row tile of BF16 rows (rows row0.. of the vertical-line rows followed
 // by the tail), `vr` valid rows, loaded directly into fragment registers; row
-// `rnew` (a fused step's new row) is read from knew/vnew.
+// `rnew` (a fused step's new row) is read from knew/vnew.  BV: the value code
+// width of the quantised tiles, whose accumulator convention the tile follows.
+template <int BV>
 __device__ __forceinline__ void f_tile(const __nv_bfloat16* vlk, const __nv_bfloat16* vlv,
                                        const __nv_bfloat16* tk, const __nv_bfloat16* tv, int nvl,
                                        int rnew, const __nv_bfloat16* knew, const __nv_bfloat16* vnew,
@@ -399,8 +450,8 @@ __device__ __forceinline__ void f_tile(const __nv_bfloat16* vlk, const __nv_bflo
     const uint32_t w0 = s2 ? va[0][G].y : va[0][G].x, w1 = s2 ? va[1][G].y : va[1][G].x;
     const uint32_t w2 = s2 ? va[2][G].y : va[2][G].x, w3 = s2 ? va[3][G].y : va[3][G].x;
     // rows g+8 carry the same factor 16 as the 4-bit high-nibble rows
-    mma_bf16(st.acc[u], __byte_perm(w0, w1, 0x5410), times16_bf16x2(__byte_perm(w0, w1, 0x7632)),
-             __byte_perm(w2, w3, 0x5410), times16_bf16x2(__byte_perm(w2, w3, 0x7632)), b0, b1);
+    mma_bf16(st.acc[u], __byte_perm(w0, w1, 0x5410), row_factor_bf16x2<BV>(__byte_perm(w0, w1, 0x7632)),
+             __byte_perm(w2, w3, 0x5410), row_factor_bf16x2<BV>(__byte_perm(w2, w3, 0x7632)), b0, b1);
   }
 }
 
@@ -408,6 +459,7 @@ __device__ __forceinline__ void f_tile(const __nv_bfloat16* vlk, const __nv_bflo
 // at kFVStride); rows at or past `vr` are masked (their contents are undefined).
 // The unpadded rows cost 2-way (K) and 4-way (V) bank conflicts on these few
 // loads, against 32 single-row copies per tile otherwise.
+template <int BV>
 __device__ __forceinline__ void f_tile_smem(const uint8_t* Ks, const uint8_t* Vs, int vr, int lane,
                                             const __nv_bfloat16* q_s, State& st) {
   const int g = lane >> 2, t = lane & 3;
@@ -453,12 +505,12 @@ __device__ __forceinline__ void f_tile_smem(const uint8_t* Ks, const uint8_t* Vs
     const uint32_t w0 = s2 ? va[0][G].y : va[0][G].x, w1 = s2 ? va[1][G].y : va[1][G].x;
     const uint32_t w2 = s2 ? va[2][G].y : va[2][G].x, w3 = s2 ? va[3][G].y : va[3][G].x;
     // rows g+8 carry the same factor 16 as the 4-bit high-nibble rows
-    mma_bf16(st.acc[u], __byte_perm(w0, w1, 0x5410), times16_bf16x2(__byte_perm(w0, w1, 0x7632)),
-             __byte_perm(w2, w3, 0x5410), times16_bf16x2(__byte_perm(w2, w3, 0x7632)), b0, b1);
+    mma_bf16(st.acc[u], __byte_perm(w0, w1, 0x5410), row_factor_bf16x2<BV>(__byte_perm(w0, w1, 0x7632)),
+             __byte_perm(w2, w3, 0x5410), row_factor_bf16x2<BV>(__byte_perm(w2, w3, 0x7632)), b0, b1);
   }
 }
 
-template <int kMode>
+template <int kMode, int BK, int BV>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
     const __nv_bfloat16* __restrict__ q, hyq_layout lay, __nv_bfloat16* __restrict__ out,
     int32_t* __restrict__ tickets, float* __restrict__ part, int HQ, int gq, int nblk_cap,
@@ -466,13 +518,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(16) __nv_bfloat16 q_s[HYQ_MAX_GQA * HYQ_D];
   __shared__ float qsum_s[HYQ_MAX_GQA * 4];
-  __shared__ __align__(8) uint64_t bars[kWarps * kSlots];
+  __shared__ __align__(8) uint64_t bars[kWarps * kMaxSlots];
   __shared__ __align__(8) uint64_t fbars[kFStaged];
   __shared__ __align__(8) uint64_t qbar;
   __shared__ float red_m[kWarps][HYQ_MAX_GQA], red_l[kWarps][HYQ_MAX_GQA], wts[kWarps][HYQ_MAX_GQA];
   __shared__ float sM[HYQ_MAX_GQA], sL[HYQ_MAX_GQA];
   __shared__ int s_flag;
 
+  using D = Dec<BK, BV>;
+  constexpr int kSlots = D::kSlots, kTile = D::kTile;
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z, HKV = gridDim.y;
   const size_t bh = (size_t)b * HKV + h;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
@@ -524,8 +578,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
   const int ntc = t1 - t0, rot = (f1 - f0) % kWarps;
   const int my0 = (warp - rot + kWarps) % kWarps;
   const int nj = ntc > my0 ? (ntc - my0 + kWarps - 1) / kWarps : 0;
-  const uint8_t* tiles = lay.qblocks + bh * (size_t)nblk_cap * HYQ_QBLOCK_BYTES;
-  uint8_t* ring = smem + warp * kSlots * HYQ_QTILE_BYTES;
+  const uint8_t* tiles = lay.qblocks + bh * (size_t)nblk_cap * D::kBlock;
+  uint8_t* ring = smem + warp * kSlots * kTile;
   uint64_t* wb = bars + warp * kSlots;
   const __nv_bfloat16* vlk = static_cast<const __nv_bfloat16*>(lay.vl_k) + bh * cap_vl * HYQ_D;
   const __nv_bfloat16* vlv = static_cast<const __nv_bfloat16*>(lay.vl_v) + bh * cap_vl * HYQ_D;
@@ -539,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
   uint4 nrow = make_uint4(0, 0, 0, 0);
   if (owner && warp == 2 && !ovl)
     nrow = __ldg(reinterpret_cast<const uint4*>((lane >= 16 ? sa.v_new : sa.k_new) + bh * HYQ_D) + (lane & 15));
-  uint8_t* fstage = smem + kRingBytes + warp * kFTileBytes;
+  uint8_t* fstage = smem + D::kRingBytes + warp * kFTileBytes;
   // A warp's ring and staging barriers are its own: lane 0 initialises them
   // and the warp issues its first copies at once, behind the query copy
   // issued at entry, so that the preparation of the query below overlaps
@@ -578,9 +632,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
   // warp's slots in flight at once.
   if (lane < kSlots && lane < nj) {
     const int j = lane;
-    mbar_arrive_expect_tx(&wb[j], HYQ_QTILE_BYTES);
-    bulk_g2s(ring + j * HYQ_QTILE_BYTES, tiles + (size_t)(t0 + my0 + kWarps * j) * HYQ_QTILE_BYTES,
-             HYQ_QTILE_BYTES, &wb[j]);
+    mbar_arrive_expect_tx(&wb[j], kTile);
+    bulk_g2s(ring + j * kTile, tiles + (size_t)(t0 + my0 + kWarps * j) * kTile, kTile, &wb[j]);
   }
   for (int i = gq * HYQ_D / 8 + tid; i < HYQ_MAX_GQA * HYQ_D / 8; i += kThreads)
     reinterpret_cast<uint4*>(q_s)[i] = make_uint4(0, 0, 0, 0);  // query rows past g
@@ -604,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
     // barrier before the main loop orders this for the warp that reads it
     const int fw = ((nvl + ntail) >> 4) - f0, rin = (nvl + ntail) & 15;
     if (fw < n_staged)
-      reinterpret_cast<uint4*>(smem + kRingBytes + fw * kFTileBytes + (lane >= 16 ? 16 * kFKStride : 0) +
+      reinterpret_cast<uint4*>(smem + D::kRingBytes + fw * kFTileBytes + (lane >= 16 ? 16 * kFKStride : 0) +
                                rin * kFKStride)[lane & 15] = nrow;
   }
   if (tid < 256) {  // 8 threads per (query row, group of 32 elements)
@@ -636,12 +689,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
   if (amax > 0.f && isfinite(amax)) (void)frexpf(amax, &ex);
   const int qe = 14 - ex;
   const float qscale = ldexpf(1.f, qe);
-  // B fragments of q in the permuted k order: kstep ks covers elements
-  // 8(t + 4(ks/2)) + 4(ks%2) + {0,1} and + {2,3}.
+  // B fragments of q in the permuted k order of the key codes: kstep ks
+  // covers elements e + {0,1} and e + {2,3}, e = 8(t + 4(ks/2)) + 4(ks%2)
+  // for 4-bit keys, e = 16 ks + 4t for 8-bit keys.
   uint32_t bq[8][2];
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
-    const int e = 8 * (t + 4 * (ks >> 1)) + 4 * (ks & 1);
+    const int e = BK == 4 ? 8 * (t + 4 * (ks >> 1)) + 4 * (ks & 1) : 16 * ks + 4 * t;
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(q_s + g * HYQ_D + e + 2 * hh));
@@ -650,7 +704,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
   }
   QConst qc;
   qc.ksc[0] = ldexpf(kScale, 24 - qe);
-  qc.ksc[1] = ldexpf(kScale, 20 - qe);
+  qc.ksc[1] = ldexpf(kScale, (BK == 4 ? 20 : 24) - qe);  // 4-bit tokens g+8 carry 16 c
 #pragma unroll
   for (int j = 0; j < 2; ++j)
 #pragma unroll
@@ -679,13 +733,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
       break;
     }
     const int tile = t0 + my0 + kWarps * j;
-    q_tile(ring + slot * HYQ_QTILE_BYTES, lane, min(16, nq - 16 * tile), bq, qc, st);
+    q_tile<BK, BV>(ring + slot * kTile, lane, min(16, nq - 16 * tile), bq, qc, st);
     __syncwarp();
     if (lane == slot && j + kSlots < nj) {
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-      mbar_arrive_expect_tx(&wb[slot], HYQ_QTILE_BYTES);
-      bulk_g2s(ring + slot * HYQ_QTILE_BYTES, tiles + (size_t)(tile + kWarps * kSlots) * HYQ_QTILE_BYTES,
-               HYQ_QTILE_BYTES, &wb[slot]);
+      mbar_arrive_expect_tx(&wb[slot], kTile);
+      bulk_g2s(ring + slot * kTile, tiles + (size_t)(tile + kWarps * kSlots) * kTile, kTile, &wb[slot]);
     }
   }
 
@@ -700,11 +753,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
       }
       __syncwarp();
     } else {
-      f_tile_smem(fstage, fstage + 16 * kFKStride, min(16, nf - 16 * (f0 + warp)), lane, q_s, st);
+      f_tile_smem<BV>(fstage, fstage + 16 * kFKStride, min(16, nf - 16 * (f0 + warp)), lane, q_s, st);
     }
   }
   for (int fi = f0 + kFStaged + warp; fi < f1; fi += kWarps)  // tiles past the staged ones
-    f_tile(vlk, vlv, tk, tv, nvl, app ? nvl + ntail : -1, sa.k_new + bh * HYQ_D, sa.v_new + bh * HYQ_D, 16 * fi,
+    f_tile<BV>(vlk, vlv, tk, tv, nvl, app ? nvl + ntail : -1, sa.k_new + bh * HYQ_D, sa.v_new + bh * HYQ_D, 16 * fi,
            min(16, nf - 16 * fi), lane, q_s, st);
 
   // ---- warp partials -> block partial (m, l, acc) in shared memory ---------
@@ -720,20 +773,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
   __syncthreads();  // every warp is done with its ring: reuse shared memory
   if (sa.nx_counts && warp == kWarps - 1) {
     const NextCounts nxc = next_counts(sa, b, nblk_cap, cap_vl, cap_tail);
-    prefetch_next_tiles(sa, nxc, bh, split, S, nblk_cap, lane);
+    prefetch_next_tiles<kTile>(sa, nxc, bh, split, S, nblk_cap, lane);
     prefetch_next_rows(sa, nxc, bh, split, S, cap_vl, cap_tail, lane);
   }
   float* red = reinterpret_cast<float*>(smem);                    // [warp][head][128]
   float* blk = red + kWarps * HYQ_MAX_GQA * HYQ_D;                  // [head][2 + 128]
-  // Accumulator (m-tile u, ci) of thread (g, t): element 32(u/2) + 4g + 2(u%2)
-  // + (ci >> 1), head 2t + (ci & 1).
+  // Accumulator (m-tile u, ci) of thread (g, t): element 32(u/2) + 4g +
+  // 2(u%2) + (ci >> 1), head 2t + (ci & 1); with 4-bit values the rows
+  // ci >= 2 carry 16 c.
 #pragma unroll
   for (int u = 0; u < 8; ++u)
 #pragma unroll
     for (int ci = 0; ci < 4; ++ci) {
       const int d = 32 * (u >> 1) + 4 * g + 2 * (u & 1) + (ci >> 1), hd = 2 * t + (ci & 1);
-      red[(warp * HYQ_MAX_GQA + hd) * HYQ_D + d] =
-          fmaf(st.acc[u][ci], ci < 2 ? HYQ_F16_SUB_SCALE : HYQ_F16_SUB_SCALE / 16.f, st.zacc[ci & 1][u >> 1]);
+      const float f = (BV == 4 && ci >= 2) ? HYQ_F16_SUB_SCALE / 16.f : HYQ_F16_SUB_SCALE;
+      red[(warp * HYQ_MAX_GQA + hd) * HYQ_D + d] = fmaf(st.acc[u][ci], f, st.zacc[ci & 1][u >> 1]);
     }
   if (g == 0)
     for (int j = 0; j < 2; ++j) {
@@ -980,13 +1034,14 @@ size_t hyq_decode_ws_bytes(const hyq_config* c, int32_t len_hint) {
   return round_up(bh * 4) + round_up((size_t)c->batch * 4) + round_up(bh * (size_t)p.S * HYQ_MAX_GQA * kPart * 4);
 }
 
-template <int kMode>
+template <int kMode, int BK, int BV>
 cudaError_t set_attrs() {
   static bool done = false;
   if (done) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<kMode, BK, BV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Dec<BK, BV>::kSmemBytes);
   if (e == cudaSuccess && kMode == kCluster)
-    e = cudaFuncSetAttribute(decode_kernel<kMode>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = cudaFuncSetAttribute(decode_kernel<kMode, BK, BV>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e == cudaSuccess) done = true;
   return e;
 }
@@ -999,7 +1054,7 @@ bool cluster_fits(int S) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(S, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = Dec<4, 4>::kSmemBytes;
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeClusterDimension;
   attr.val.clusterDim.x = S;
@@ -1008,7 +1063,7 @@ bool cluster_fits(int S) {
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   int n = 0;
-  bool ok = cudaOccupancyMaxActiveClusters(&n, decode_kernel<kCluster>, &cfg) == cudaSuccess && n >= 1;
+  bool ok = cudaOccupancyMaxActiveClusters(&n, decode_kernel<kCluster, 4, 4>, &cfg) == cudaSuccess && n >= 1;
   cudaGetLastError();
   cached[S] = ok ? 1 : 2;
   return ok;
@@ -1032,12 +1087,16 @@ extern "C" hyq_status hyq_set_decode_plan(int32_t merge, int32_t splits) {
 cudaError_t hyq_launch_decode(const hyq_config* c, const void* q, const hyq_layout* lay, void* out,
                               int32_t len_hint, void* ws, cudaStream_t s, const void* k_new, const void* v_new,
                               void* k_src, void* v_src, int32_t ld, const hyq_layout* next) {
-  cudaError_t e = set_attrs<kDirect>();
-  if (e == cudaSuccess) e = set_attrs<kCluster>();
-  if (e == cudaSuccess) e = set_attrs<kGlobal>();
-  if (e != cudaSuccess) return e;
+  const int bk = hyq_bits_k(c), bv = hyq_bits_v(c);
+  const bool w44 = bk == 4 && bv == 4;
+  if (w44) {
+    cudaError_t e = set_attrs<kCluster, 4, 4>();
+    if (e != cudaSuccess) return e;
+  }
   DecodePlan p = decode_plan(c, len_hint);
-  if (p.mode == kCluster && !cluster_fits(p.S)) p.mode = kGlobal;  // same S, workspace merge
+  // Cluster merge: 4-bit codes only, and only when the clusters fit; else the
+  // workspace merge with the same S.
+  if (p.mode == kCluster && (!w44 || !cluster_fits(p.S))) p.mode = kGlobal;
   size_t bh = (size_t)c->batch * c->num_kv_heads;
   int32_t* tickets = static_cast<int32_t*>(ws);
   StepArgs sa{static_cast<const __nv_bfloat16*>(k_new),
@@ -1059,7 +1118,6 @@ cudaError_t hyq_launch_decode(const hyq_config* c, const void* q, const hyq_layo
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.S, c->num_kv_heads, c->batch);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
   cudaLaunchAttribute attrs[2];
   attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1073,16 +1131,28 @@ cudaError_t hyq_launch_decode(const hyq_config* c, const void* q, const hyq_layo
   const __nv_bfloat16* qq = static_cast<const __nv_bfloat16*>(q);
   __nv_bfloat16* oo = static_cast<__nv_bfloat16*>(out);
   const int nblk = hyq_nblk(c), cvl = hyq_vl_stride(c), ct = hyq_cap_tail(c);
-  if (p.mode == kCluster) {
+  // Launch one instantiation with its shared-memory plan.
+  auto go = [&](auto kern, int smem_bytes, cudaError_t attr_err) {
+    if (attr_err != cudaSuccess) return attr_err;
+    cfg.dynamicSmemBytes = smem_bytes;
+    return cudaLaunchKernelEx(&cfg, kern, qq, *lay, oo, tickets, part, c->num_q_heads, gq, nblk, cvl, ct, p.S, sa);
+  };
+  if (p.mode == kCluster) {  // 4-bit codes only (above)
     cfg.numAttrs += 1;
-    return cudaLaunchKernelEx(&cfg, decode_kernel<kCluster>, qq, *lay, oo, tickets, part, c->num_q_heads, gq,
-                              nblk, cvl, ct, p.S, sa);
+    return go(decode_kernel<kCluster, 4, 4>, Dec<4, 4>::kSmemBytes, cudaSuccess);
   }
-  if (p.mode == kDirect)
-    return cudaLaunchKernelEx(&cfg, decode_kernel<kDirect>, qq, *lay, oo, tickets, part, c->num_q_heads, gq,
-                              nblk, cvl, ct, p.S, sa);
-  return cudaLaunchKernelEx(&cfg, decode_kernel<kGlobal>, qq, *lay, oo, tickets, part, c->num_q_heads, gq,
-                            nblk, cvl, ct, p.S, sa);
+  const bool direct = p.mode == kDirect;
+  if (w44)
+    return direct ? go(decode_kernel<kDirect, 4, 4>, Dec<4, 4>::kSmemBytes, set_attrs<kDirect, 4, 4>())
+                  : go(decode_kernel<kGlobal, 4, 4>, Dec<4, 4>::kSmemBytes, set_attrs<kGlobal, 4, 4>());
+  if (bk == 8 && bv == 8)
+    return direct ? go(decode_kernel<kDirect, 8, 8>, Dec<8, 8>::kSmemBytes, set_attrs<kDirect, 8, 8>())
+                  : go(decode_kernel<kGlobal, 8, 8>, Dec<8, 8>::kSmemBytes, set_attrs<kGlobal, 8, 8>());
+  if (bk == 4)
+    return direct ? go(decode_kernel<kDirect, 4, 8>, Dec<4, 8>::kSmemBytes, set_attrs<kDirect, 4, 8>())
+                  : go(decode_kernel<kGlobal, 4, 8>, Dec<4, 8>::kSmemBytes, set_attrs<kGlobal, 4, 8>());
+  return direct ? go(decode_kernel<kDirect, 8, 4>, Dec<8, 4>::kSmemBytes, set_attrs<kDirect, 8, 4>())
+                : go(decode_kernel<kGlobal, 8, 4>, Dec<8, 4>::kSmemBytes, set_attrs<kGlobal, 8, 4>());
 }
 
 cudaError_t hyq_launch_decode_append(const hyq_config* c, const void* q, const void* k_new,

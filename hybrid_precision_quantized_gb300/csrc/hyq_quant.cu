@@ -1,7 +1,8 @@
-// 4-bit group quantiser and hybrid-cache construction.
+// Low-bit group quantiser and hybrid-cache construction.
 //
 // Quant_B(.; G) of Algorithm 4 ("HyQuant: Hybrid-Precision Quantization for
-// LLM Attention", Appendix A.4) with B = 4 and G = 32 along head_dim, and the
+// LLM Attention", Appendix A.4) with B = B_K for keys and B_V for values (4 or
+// 8 bits) and G = 32 along head_dim, and the
 // Freeze re-organisation of the cache into a 4-bit stream, vertical-line rows
 // and a BF16 tail (§4.3 Eq. 8).
 //
@@ -10,6 +11,8 @@
 // the FP16 step and zero point, and each thread then assembles whole 32-bit
 // code words in the tensor-core fragment order documented in hyq.h and
 // stores them directly (no atomics, no float64).
+#include <type_traits>
+
 #include "hyq_common.cuh"
 
 namespace {
@@ -83,11 +86,11 @@ __device__ __forceinline__ uint32_t pack_nibbles(const uint32_t (&b)[8]) {
   return w - kMagicSum;
 }
 
-// r = 1 / s rounded, and 0 exactly when the step s is 0.
-__device__ __forceinline__ uint32_t code_of(float x, float z, float r) {
+// r = 1 / s rounded, and 0 exactly when the step s is 0; qmax = 2^B - 1.
+__device__ __forceinline__ uint32_t code_of(float x, float z, float r, float qmax = 15.f) {
   if (r == 0.f) return 0u;
   float t = rintf(__fmul_rn(__fsub_rn(x, z), r));
-  t = fminf(fmaxf(t, 0.f), 15.f);
+  t = fminf(fmaxf(t, 0.f), qmax);
   return (uint32_t)t;
 }
 
@@ -101,11 +104,42 @@ __device__ __forceinline__ void unpack8(uint4 v, float (&f)[8]) {
   }
 }
 
-// Build one 64-row block of the 4-bit stream at `dst` (10240 bytes, global).
-// sm.pos / sm.keep must be set.  Rows with keep = 1 keep their existing
-// codes and metadata; rows with pos < 0 become zero padding.
+// Pass 3 of an 8-bit code region (tensor T: 0 = K, 1 = V): one 32-bit word
+// (four codes of the byte order in hyq.h) per job; rows with keep = 1 keep
+// their bytes.
+template <int T, int kTileBytes, int kOff>
+__device__ void pack_codes8(const BuildSmem& sm, uint8_t* dst, bool any_keep) {
+  for (int j = threadIdx.x; j < 4 * 32 * 16; j += kThreads) {
+    const int tile = j >> 9, lane = (j >> 4) & 31, u = j & 15;
+    const int g = lane >> 2, t = lane & 3;
+    uint8_t* wp = dst + tile * kTileBytes + kOff + 512 * (u >> 2) + 16 * lane + 4 * (u & 3);
+    const uint32_t old = any_keep ? *reinterpret_cast<const uint32_t*>(wp) : 0u;
+    uint32_t w = 0;
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      // K: row g + 8(u%2), element 16(u/2) + 4t + (0, 2, 1, 3)[jj];
+      // V: row 2t + (0, 8, 1, 9)[jj], element 32(u/4) + 4g + 2((u/2)%2) + u%2
+      const int row = T == 0 ? 16 * tile + g + 8 * (u & 1) : 16 * tile + 2 * t + 8 * (jj & 1) + (jj >> 1);
+      const int e = T == 0 ? 16 * (u >> 1) + 4 * t + 2 * (jj & 1) + (jj >> 1)
+                           : 32 * (u >> 2) + 4 * g + 2 * ((u >> 1) & 1) + (u & 1);
+      const int q = e >> 5;
+      const uint32_t c = sm.keep[row] ? (old >> (8 * jj)) & 0xFFu
+                                      : code_of(__bfloat162float(sm.x[T][row][e]), sm.z[T][row][q], sm.r[T][row][q],
+                                                255.f);
+      w |= c << (8 * jj);
+    }
+    *reinterpret_cast<uint32_t*>(wp) = w;
+  }
+}
+
+// Build one 64-row block of the quantised stream at `dst` (global), keys with
+// BK-bit and values with BV-bit codes.  sm.pos / sm.keep must be set.  Rows
+// with keep = 1 keep their existing codes and metadata; rows with pos < 0
+// become zero padding.
+template <int BK, int BV>
 __device__ void build_block(BuildSmem& sm, const __nv_bfloat16* kbase, const __nv_bfloat16* vbase,
                             uint8_t* dst, bool any_keep, int32_t* err) {
+  using F = QFmt<BK, BV>;
   const int tid = threadIdx.x;
   // Pass 1: load the rows (all of a thread's loads first), per-group min /
   // max (4 chunks of 8 per group are on 4 consecutive lanes).
@@ -144,14 +178,16 @@ __device__ void build_block(BuildSmem& sm, const __nv_bfloat16* kbase, const __n
     }
   }
   __syncthreads();
-  // Pass 2: one thread per group: step s = smallest FP16 with 15 s >= mx - mn
+  // Pass 2: one thread per group: step s = smallest FP16 with qmax s >= mx - mn
   // (the subtraction, the division and the FP16 conversion all round up,
-  // which gives exactly that value); zero z = FP16(mn) to nearest.
+  // which gives exactly that value: qmax h is exact in FP32 for every FP16 h);
+  // zero z = FP16(mn) to nearest.
   for (int i = tid; i < 2 * kRows * 4; i += kThreads) {
     const int T = i >> 8, row = (i >> 2) & (kRows - 1), q = i & 3;
     if (sm.keep[row]) continue;
+    const float qmax = (T == 0 ? BK : BV) == 8 ? 255.f : 15.f;
     const float mn = sm.mn[T][row][q], mx = sm.mx[T][row][q];
-    __half sh = __float2half_ru(__fdiv_ru(__fsub_ru(mx, mn), 15.f));
+    __half sh = __float2half_ru(__fdiv_ru(__fsub_ru(mx, mn), qmax));
     __half zh = __float2half_rn(mn);
     float s32 = __half2float(sh), z32 = __half2float(zh);
     if (sm.nan[T][row][q] || isinf(s32) || isinf(z32)) {
@@ -165,17 +201,19 @@ __device__ void build_block(BuildSmem& sm, const __nv_bfloat16* kbase, const __n
     // (x - z) * r is monotone in x, so the group's extremes bound every code
     // argument; a NaN extreme fails the test.
     const float tl = __fmul_rn(__fsub_rn(mn, z32), r32), th = __fmul_rn(__fsub_rn(mx, z32), r32);
-    sm.fast[T][row][q] = (uint8_t)(tl > -0.5f && th < 15.5f);
+    sm.fast[T][row][q] = (uint8_t)(tl > -0.5f && th < qmax + 0.5f);
     const uint32_t w = (uint32_t)__half_as_ushort(sh) | ((uint32_t)__half_as_ushort(zh) << 16);
-    *reinterpret_cast<uint32_t*>(dst + (row >> 4) * HYQ_QTILE_BYTES + 2048 + T * 256 + (row & 15) * 16 + 4 * q) = w;
+    *reinterpret_cast<uint32_t*>(dst + (row >> 4) * F::kTile + F::kKMeta + T * 256 + (row & 15) * 16 + 4 * q) = w;
   }
   __syncthreads();
-  // Pass 3a: K code words.  Job (tile, g, chunk cc): rows g and g+8 of the
-  // tile, elements 8cc..8cc+7 -> the two words u = 2(cc/4) + {0,1} of lane 4g + cc%4.
-  for (int j = tid; j < 4 * 8 * kChunks; j += kThreads) {
+  if (BK == 8) pack_codes8<0, F::kTile, 0>(sm, dst, any_keep);
+  if (BV == 8) pack_codes8<1, F::kTile, F::kVCode>(sm, dst, any_keep);
+  // Pass 3a: 4-bit K code words.  Job (tile, g, chunk cc): rows g and g+8 of
+  // the tile, elements 8cc..8cc+7 -> the two words u = 2(cc/4) + {0,1} of lane 4g + cc%4.
+  for (int j = tid; j < (BK == 4 ? 4 * 8 * kChunks : 0); j += kThreads) {
     const int tile = j >> 7, g = (j >> 4) & 7, cc = j & 15;
     const int q = cc >> 2, t = cc & 3;
-    uint8_t* wp = dst + tile * HYQ_QTILE_BYTES + 512 * (cc >> 3) + 16 * (4 * g + t) + 4 * (2 * (q & 1));
+    uint8_t* wp = dst + tile * F::kTile + 512 * (cc >> 3) + 16 * (4 * g + t) + 4 * (2 * (q & 1));
     const int rk0 = 16 * tile + g, rk1 = rk0 + 8;
     if (!any_keep && sm.fast[0][rk0][q] && sm.fast[0][rk1][q]) {
       // Row a, element 4 sub + 2 b + c -> nibble a + 2 b + 4 c of word sub.
@@ -231,11 +269,11 @@ __device__ void build_block(BuildSmem& sm, const __nv_bfloat16* kbase, const __n
     }
     *reinterpret_cast<uint2*>(wp) = make_uint2(w[0], w[1]);
   }
-  // Pass 3b: V code words.  Job (tile, t, chunk cc): rows 2t + 8b + c,
+  // Pass 3b: 4-bit V code words.  Job (tile, t, chunk cc): rows 2t + 8b + c,
   // elements 8cc..8cc+7 = 32q + 4g + 2s + a with q = cc/4 and g = 2(cc%4) + gl
   // -> the words (lane 4g + t, u = 2q + s) for gl, s in {0, 1}; the two s
   // words of one lane are adjacent.
-  for (int j = tid; j < 4 * 4 * kChunks; j += kThreads) {
+  for (int j = tid; j < (BV == 4 ? 4 * 4 * kChunks : 0); j += kThreads) {
     const int tile = j >> 6, t = (j >> 4) & 3, cc = j & 15;
     const int q = cc >> 2;
     const int rv = 16 * tile + 2 * t;  // rows rv + 8 b + c
@@ -268,7 +306,7 @@ __device__ void build_block(BuildSmem& sm, const __nv_bfloat16* kbase, const __n
           wf[ss] = pack_nibbles(bb);
         }
         const int g = 2 * (cc & 3) + gl;
-        *reinterpret_cast<uint2*>(dst + tile * HYQ_QTILE_BYTES + 1024 + 512 * (cc >> 3) + 16 * (4 * g + t) +
+        *reinterpret_cast<uint2*>(dst + tile * F::kTile + F::kVCode + 512 * (cc >> 3) + 16 * (4 * g + t) +
                                   8 * (q & 1)) = make_uint2(wf[0], wf[1]);
       }
       continue;
@@ -279,7 +317,7 @@ __device__ void build_block(BuildSmem& sm, const __nv_bfloat16* kbase, const __n
 #pragma unroll
     for (int gl = 0; gl < 2; ++gl) {
       const int g = 2 * (cc & 3) + gl;
-      wp[gl] = dst + tile * HYQ_QTILE_BYTES + 1024 + 512 * (cc >> 3) + 16 * (4 * g + t) + 8 * (q & 1);
+      wp[gl] = dst + tile * F::kTile + F::kVCode + 512 * (cc >> 3) + 16 * (4 * g + t) + 8 * (q & 1);
       if (any_keep) old[gl] = *reinterpret_cast<const uint2*>(wp[gl]);
     }
 #pragma unroll
@@ -348,6 +386,7 @@ __device__ __forceinline__ int32_t warp_count_f_le(const int32_t* idx, int32_t k
 constexpr int kWinF = 256;  // vertical-line entries a block resolves in shared memory
 
 // grid (blocks of the new stream, HKV, B)
+template <int BK, int BV>
 __global__ void __launch_bounds__(kThreads) rebuild_blocks_kernel(
     const __nv_bfloat16* __restrict__ k_src, const __nv_bfloat16* __restrict__ v_src, int32_t ld,
     int32_t P, const int32_t* __restrict__ idx, int32_t k, uint8_t* __restrict__ qblocks,
@@ -395,8 +434,8 @@ __global__ void __launch_bounds__(kThreads) rebuild_blocks_kernel(
     sm.keep[threadIdx.x] = 0;
   }
   __syncthreads();
-  build_block(sm, k_src + bh * ld * HYQ_D, v_src + bh * ld * HYQ_D,
-              qblocks + (bh * nblk_cap + bi) * (size_t)HYQ_QBLOCK_BYTES, false, err);
+  build_block<BK, BV>(sm, k_src + bh * ld * HYQ_D, v_src + bh * ld * HYQ_D,
+                      qblocks + (bh * nblk_cap + bi) * (size_t)QFmt<BK, BV>::kBlock, false, err);
 }
 
 // Vertical-line gather, BF16 tail copy and counters.  One warp per row:
@@ -443,7 +482,8 @@ __global__ void __launch_bounds__(kThreads) rebuild_gather_kernel(
 }
 
 // Block blockIdx.x of appending rows [0, end - nq0) of kbase / vbase (row r
-// at kbase + r * 128) to the 4-bit stream of (b, h) after its nq0 rows.
+// at kbase + r * 128) to the quantised stream of (b, h) after its nq0 rows.
+template <int BK, int BV>
 __device__ void append_body(BuildSmem& sm, const __nv_bfloat16* kbase, const __nv_bfloat16* vbase, int32_t nq0,
                             int32_t end, size_t bh, const hyq_layout& lay, int32_t nblk_cap) {
   const int32_t bi = nq0 / kRows + blockIdx.x;
@@ -454,11 +494,12 @@ __device__ void append_body(BuildSmem& sm, const __nv_bfloat16* kbase, const __n
     sm.pos[threadIdx.x] = (row >= nq0 && row < end) ? row - nq0 : -1;
   }
   __syncthreads();
-  build_block(sm, kbase, vbase, lay.qblocks + (bh * nblk_cap + bi) * (size_t)HYQ_QBLOCK_BYTES, bi * kRows < nq0,
-              lay.err);
+  build_block<BK, BV>(sm, kbase, vbase, lay.qblocks + (bh * nblk_cap + bi) * (size_t)QFmt<BK, BV>::kBlock,
+                      bi * kRows < nq0, lay.err);
 }
 
 // Append n rows per (b, h) after the current NQ rows.  grid (blocks touched, HKV, B)
+template <int BK, int BV>
 __global__ void __launch_bounds__(kThreads) append_blocks_kernel(
     const __nv_bfloat16* __restrict__ k_rows, const __nv_bfloat16* __restrict__ v_rows, int32_t n,
     hyq_layout lay, int32_t nblk_cap) {
@@ -474,7 +515,7 @@ __global__ void __launch_bounds__(kThreads) append_blocks_kernel(
   const int32_t end = min(nq0 + n, cap_rows);
   if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0 && nq0 + n > cap_rows)
     hyq_set_err(lay.err, HYQ_DEVERR_COUNT);
-  append_body(sm, k_rows + bh * n * HYQ_D, v_rows + bh * n * HYQ_D, nq0, end, bh, lay, nblk_cap);
+  append_body<BK, BV>(sm, k_rows + bh * n * HYQ_D, v_rows + bh * n * HYQ_D, nq0, end, bh, lay, nblk_cap);
 }
 
 // Rows the tail of sequence b gives up in hyq_age_tail: max(0, NTAIL - W),
@@ -491,6 +532,7 @@ __device__ __forceinline__ int32_t age_rows(const hyq_layout& lay, int b, int32_
 
 // hyq_age_tail, step 1: the oldest m tail rows of (b, h) onto the 4-bit
 // stream.  grid (blocks touched, HKV, B)
+template <int BK, int BV>
 __global__ void __launch_bounds__(kThreads) age_blocks_kernel(hyq_layout lay, int32_t nblk_cap, int32_t window,
                                                               int32_t cap_tail) {
   __shared__ __align__(16) BuildSmem sm;
@@ -499,7 +541,7 @@ __global__ void __launch_bounds__(kThreads) age_blocks_kernel(hyq_layout lay, in
   const int32_t m = age_rows(lay, b, window, nblk_cap * kRows, cap_tail);
   if (m == 0) return;
   const int32_t nq0 = lay.counts[(size_t)b * HYQ_COUNTS + HYQ_CNT_NQ];
-  append_body(sm, static_cast<const __nv_bfloat16*>(lay.tail_k) + bh * cap_tail * HYQ_D,
+  append_body<BK, BV>(sm, static_cast<const __nv_bfloat16*>(lay.tail_k) + bh * cap_tail * HYQ_D,
               static_cast<const __nv_bfloat16*>(lay.tail_v) + bh * cap_tail * HYQ_D, nq0, nq0 + m, bh, lay,
               nblk_cap);
 }
@@ -560,6 +602,17 @@ __global__ void append_counts_kernel(hyq_layout lay, int32_t n, int32_t cap_rows
   cnt[HYQ_CNT_LEN] += add;
 }
 
+// Calls f(std::integral_constant<int, BK>, std::integral_constant<int, BV>)
+// for the config's code widths.
+template <class Fn>
+auto with_widths(const hyq_config* c, Fn f) {
+  const int bk = hyq_bits_k(c), bv = hyq_bits_v(c);
+  using I4 = std::integral_constant<int, 4>;
+  using I8 = std::integral_constant<int, 8>;
+  if (bk == 8) return bv == 8 ? f(I8{}, I8{}) : f(I8{}, I4{});
+  return bv == 8 ? f(I4{}, I8{}) : f(I4{}, I4{});
+}
+
 }  // namespace
 
 cudaError_t hyq_launch_age_tail(const hyq_config* c, const hyq_layout* lay, cudaStream_t s) {
@@ -568,7 +621,10 @@ cudaError_t hyq_launch_age_tail(const hyq_config* c, const hyq_layout* lay, cuda
   const int32_t most = ct - c->window;
   if (most <= 0) return cudaSuccess;
   dim3 grid((most + HYQ_QBLOCK_ROWS - 1) / HYQ_QBLOCK_ROWS + 1, c->num_kv_heads, c->batch);
-  age_blocks_kernel<<<grid, kThreads, 0, s>>>(*lay, nblk, c->window, ct);
+  with_widths(c, [&](auto bk, auto bv) {
+    age_blocks_kernel<bk.value, bv.value><<<grid, kThreads, 0, s>>>(*lay, nblk, c->window, ct);
+    return 0;
+  });
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   age_shift_kernel<<<dim3(c->num_kv_heads, c->batch), kThreads, 0, s>>>(*lay, nblk, c->window, ct);
@@ -582,9 +638,11 @@ cudaError_t hyq_launch_quantize_append(const hyq_config* c, const void* k, const
                                        int32_t n_rows, const hyq_layout* lay, cudaStream_t s) {
   int32_t nblk = hyq_nblk(c);
   dim3 grid((n_rows + HYQ_QBLOCK_ROWS - 1) / HYQ_QBLOCK_ROWS + 1, c->num_kv_heads, c->batch);
-  append_blocks_kernel<<<grid, kThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(k),
-                                                 static_cast<const __nv_bfloat16*>(v), n_rows,
-                                                 *lay, nblk);
+  with_widths(c, [&](auto bk, auto bv) {
+    append_blocks_kernel<bk.value, bv.value><<<grid, kThreads, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), n_rows, *lay, nblk);
+    return 0;
+  });
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   append_counts_kernel<<<c->batch, 1, 0, s>>>(*lay, n_rows, nblk * HYQ_QBLOCK_ROWS);
@@ -601,7 +659,11 @@ cudaError_t hyq_launch_rebuild(const hyq_config* c, const void* k_src, const voi
   const __nv_bfloat16* vv = static_cast<const __nv_bfloat16*>(v_src);
   if (nq > 0) {
     dim3 grid((nq + HYQ_QBLOCK_ROWS - 1) / HYQ_QBLOCK_ROWS, c->num_kv_heads, c->batch);
-    rebuild_blocks_kernel<<<grid, kThreads, 0, s>>>(kk, vv, ld, P, idx, k, lay->qblocks, nblk, lay->err);
+    with_widths(c, [&](auto bk, auto bv) {
+      rebuild_blocks_kernel<bk.value, bv.value><<<grid, kThreads, 0, s>>>(kk, vv, ld, P, idx, k, lay->qblocks, nblk,
+                                                                          lay->err);
+      return 0;
+    });
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

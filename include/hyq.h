@@ -66,37 +66,50 @@ typedef struct {
   int32_t period;       /* re-selection period and proxy-query count (64)      */
   int32_t rho_ppm;      /* vertical-line ratio rho in parts per million (5% = 50000) */
   int32_t capacity;     /* largest context length L the layout must hold        */
+  int32_t bits_k;       /* B_K, key code width: 4 or 8 (0 means 4)              */
+  int32_t bits_v;       /* B_V, value code width: 4 or 8 (0 means 4)            */
 } hyq_config;
 
 /*
- * 4-bit stream format.  The 4-bit stream of one (batch, KV head) is an array
- * of 16-row tiles of HYQ_QTILE_BYTES each, tile i holding stream rows
- * 16i..16i+15; four consecutive tiles form a block of HYQ_QBLOCK_ROWS rows,
- * the unit the stream is allocated in.  A tile is
+ * Quantised stream format.  The quantised ("4-bit") stream of one (batch, KV
+ * head) is an array of 16-row tiles of HYQ_QTILE_BYTES_BITS(B_K, B_V) bytes
+ * each, tile i holding stream rows 16i..16i+15; four consecutive tiles form a
+ * block of HYQ_QBLOCK_ROWS rows, the unit the stream is allocated in.  With
+ * CK = 256 B_K and CV = 256 B_V (the code bytes of 16 rows) a tile is
  *
- *   [0,    1024)  K codes
- *   [1024, 2048)  V codes
- *   [2048, 2304)  K metadata: 16 rows x 4 groups x (scale, zero) FP16 pairs
- *   [2304, 2560)  V metadata: same
+ *   [0,            CK)           K codes
+ *   [CK,           CK+CV)        V codes
+ *   [CK+CV,        CK+CV+256)    K metadata: 16 rows x 4 groups x (scale, zero) FP16 pairs
+ *   [CK+CV+256,    CK+CV+512)    V metadata: same
+ *
+ * (B_K = B_V = 4: 1024 + 1024 + 256 + 256 = HYQ_QTILE_BYTES.)
  *
  * Metadata entry (row r, group q) lives at byte 16*r + 4*q of its region:
  * scale s then zero z.  The dequantised value of element e (group q = e/32)
- * is c * s + z with c the 4-bit code.
+ * is c * s + z with c the B_K- (K) or B_V-bit (V) code.
  *
- * Inside a 1024-byte code region the 16 x 128 codes are ordered for the
+ * Inside a 4-bit (1024-byte) code region the 16 x 128 codes are ordered for the
  * register fragments of 16x16 tensor-core tiles: byte offset
  *   512*(u/4) + 16*lane + 4*(u%4)          (u = 0..7, lane = 0..31)
  * holds a 32-bit word whose nibble n (bits 4n..4n+3, n = 0..7) is the code
  * of, with g = lane/4, t = lane%4, a = n&1, b = (n>>1)&1, c = n>>2,
  *   K: row g + 8a,          element 8*(t + 4*(u/2)) + 4*(u%2) + 2b + c
  *   V: row 2t + 8b + c,     element 32*(u/2) + 4g + 2*(u%2) + a
+ * An 8-bit code region (2048 bytes) holds one code per byte: byte offset
+ *   512*(u/4) + 16*lane + 4*(u%4) + j      (u = 0..15, lane = 0..31, j = 0..3)
+ * is the code of
+ *   K: row g + 8*(u%2),          element 16*(u/2) + 4t + (0, 2, 1, 3)[j]
+ *   V: row 2t + (0, 8, 1, 9)[j],  element 32*(u/4) + 4g + 2*((u/2)%2) + u%2
+ * (the V output elements of m-tile u/2 are those of the 4-bit order).
  * Rows past the stream length inside the last block have zero codes and
  * zero metadata.
  */
 #define HYQ_QBLOCK_ROWS 64
-#define HYQ_QBLOCK_BYTES 10240
 #define HYQ_QTILE_ROWS 16
-#define HYQ_QTILE_BYTES 2560
+#define HYQ_QTILE_BYTES_BITS(bk, bv) (256 * ((bk) + (bv)) + 512)
+#define HYQ_QBLOCK_BYTES_BITS(bk, bv) (4 * HYQ_QTILE_BYTES_BITS(bk, bv))
+#define HYQ_QBLOCK_BYTES 10240 /* B_K = B_V = 4 */
+#define HYQ_QTILE_BYTES 2560   /* B_K = B_V = 4 */
 
 /*
  * Device buffers of one layer's hybrid cache (§4.3 Eq. 8, Algorithm 4's four
@@ -104,7 +117,7 @@ typedef struct {
  * Sizes in bytes come from hyq_layout_sizes(); all pointers are device
  * pointers, 256-byte aligned.
  *
- *   qblocks  [B][HKV][nblk][HYQ_QBLOCK_BYTES]  4-bit stream, positions of the
+ *   qblocks  [B][HKV][nblk][HYQ_QBLOCK_BYTES_BITS(B_K, B_V)]  quantised stream, positions of the
  *            non-window prefix that are not vertical-line, ascending
  *   vl_k/v   bf16 [B][HKV][cap_vl][128]  vertical-line rows, ascending position
  *   vl_idx   int32 [B][HKV][cap_vl]      their positions

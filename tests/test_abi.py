@@ -163,3 +163,58 @@ def test_block_format_fragment_order_examples():
     # V: element 32*(3//2) + 4*1 + 2*(3%2) + a = 38 + a
     assert [(vrow[base + n], vel[base + n]) for n in range(8)] == [
         (2, 38), (2, 39), (10, 38), (10, 39), (3, 38), (3, 39), (11, 38), (11, 39)]
+
+
+@pytest.mark.parametrize("bk,bv", [(8, 8), (4, 8), (8, 4)])
+def test_block_format_round_trip_wide_codes(bk, bv):
+    rng = np.random.default_rng(bk * 10 + bv)
+    n = 150
+    kc = rng.integers(0, 1 << bk, (n, 128), dtype=np.uint8)
+    vc = rng.integers(0, 1 << bv, (n, 128), dtype=np.uint8)
+    ks, kz, vs, vz = (rng.standard_normal((n, 4)).astype(np.float16) for _ in range(4))
+    blocks = hyq.pack_qblocks(kc, vc, ks, kz, vs, vz, bits_k=bk, bits_v=bv)
+    assert blocks.shape == (3, L.qblock_bytes(bk, bv)) == (3, 4 * (256 * (bk + bv) + 512))
+    out = hyq.unpack_qblocks(blocks, n, bits_k=bk, bits_v=bv)
+    for a, b in zip(out, (kc, vc, ks, kz, vs, vz)):
+        assert np.array_equal(a, b)
+
+
+def test_eight_bit_order_follows_the_fragment_rule():
+    """Every (row, element) of a 16 x 128 tile appears once in each 8-bit
+    order; in a K word the AND half (bytes 0, 2) and the permuted half (bytes
+    1, 3) are consecutive element pairs of one row, four consecutive elements
+    in all; a V word holds one element of tokens 2t, 2t+8, 2t+1, 2t+9."""
+    from hybrid_precision_quantized_gb300.cache import _tile_maps8
+    krow, kel, vrow, vel = _tile_maps8()
+    assert len(set(zip(krow.tolist(), kel.tolist()))) == 2048
+    assert len(set(zip(vrow.tolist(), vel.tolist()))) == 2048
+    for base in range(0, 2048, 4):
+        w = slice(base, base + 4)
+        assert len(set(krow[w].tolist())) == 1
+        assert (kel[base + 2], kel[base + 1], kel[base + 3]) == (kel[base] + 1, kel[base] + 2, kel[base] + 3)
+        assert kel[base] % 4 == 0
+        assert len(set(vel[w].tolist())) == 1
+        t = vrow[base] // 2
+        assert tuple(vrow[w].tolist()) == (2 * t, 2 * t + 8, 2 * t + 1, 2 * t + 9)
+    # a lane's 16 words: K keys g and g + 8, 16-element k-steps in order
+    lane = 9   # g = 2, t = 1
+    ku = [(krow[512 * (u // 4) + 16 * lane + 4 * (u % 4)], kel[512 * (u // 4) + 16 * lane + 4 * (u % 4)])
+          for u in range(16)]
+    assert ku == [(2 + 8 * (u % 2), 16 * (u // 2) + 4) for u in range(16)]
+
+
+def test_code_widths_are_validated(lib):
+    ok = hyq.make_config(1, 4, 2, 256, bits_k=8, bits_v=4)
+    assert L.hyq_config_check(ok) == 0
+    assert L.hyq_config_check(hyq.make_config(1, 4, 2, 256, bits_k=0, bits_v=0)) == 0   # 0 means 4
+    for bk, bv in [(5, 4), (4, 2), (16, 8), (-4, 4)]:
+        assert L.hyq_config_check(hyq.make_config(1, 4, 2, 256, bits_k=bk, bits_v=bv)) != 0
+
+
+def test_stream_size_follows_the_code_widths(lib):
+    sizes = {(bk, bv): L.hyq_layout_sizes(hyq.make_config(2, 8, 2, 1000, bits_k=bk, bits_v=bv))
+             for bk in (4, 8) for bv in (4, 8)}
+    nblk = -(-1000 // 64)
+    for (bk, bv), s in sizes.items():
+        assert s[0] == -(-(2 * 2 * nblk * L.qblock_bytes(bk, bv)) // 256) * 256
+        assert s[1:] == sizes[(4, 4)][1:]       # BF16 buffers do not depend on the widths

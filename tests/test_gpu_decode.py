@@ -21,18 +21,21 @@ from tests.gpu_util import assert_attention_close, to_np
 pytestmark = pytest.mark.gpu
 
 
-def build_and_decode(c, Lc, W, ppm, capacity=None, len_hint=0, period=64):
-    got, idx_np, st = decode_gpu(c, Lc, W, ppm, capacity, len_hint, period)
+def build_and_decode(c, Lc, W, ppm, capacity=None, len_hint=0, period=64, bits=(4, 4)):
+    got, idx_np, st = decode_gpu(c, Lc, W, ppm, capacity, len_hint, period, bits)
     k_np, v_np = c.k.double().numpy(), c.v.double().numpy()
-    want = hybrid_decode(c.q.double().numpy(), k_np, v_np, Lc, prefix_len(Lc, W), idx_np)
+    want = hybrid_decode(c.q.double().numpy(), k_np, v_np, Lc, prefix_len(Lc, W), idx_np, bits=bits[0],
+                         bits_v=bits[1])
     return got, want, st
 
 
-def decode_gpu(c, Lc, W, ppm, capacity=None, len_hint=0, period=64):
-    """Layout from the oracle's selection, then one GPU decode call."""
+def decode_gpu(c, Lc, W, ppm, capacity=None, len_hint=0, period=64, bits=(4, 4)):
+    """Layout from the oracle's selection (B_K, B_V = ``bits``), then one GPU
+    decode call."""
     B, HQ = c.q.shape[:2]
     HKV = c.k.shape[1]
-    cfg = make_config(B, HQ, HKV, capacity=capacity or max(Lc, 1), window=W, rho_ppm=ppm, period=period)
+    cfg = make_config(B, HQ, HKV, capacity=capacity or max(Lc, 1), window=W, rho_ppm=ppm, period=period,
+                      bits_k=bits[0], bits_v=bits[1])
     layer = HybridLayer(cfg)
     layer.reset()
     qp = c.q_proxy.double().numpy()

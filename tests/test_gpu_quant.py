@@ -17,16 +17,17 @@ pytestmark = pytest.mark.gpu
 
 
 def _check_stream(layer, b, h, n_rows, k_rows, v_rows):
+    bk, bv = layer.cfg.bits_k or 4, layer.cfg.bits_v or 4
     blocks = layer.qblocks()[b, h].cpu().numpy()
-    kc, vc, ks, kz, vs, vz = unpack_qblocks(blocks, n_rows)
-    for got_c, got_s, got_z, rows in ((kc, ks, kz, k_rows), (vc, vs, vz, v_rows)):
-        c, s, z = quantize(rows)
+    kc, vc, ks, kz, vs, vz = unpack_qblocks(blocks, n_rows, bk, bv)
+    for got_c, got_s, got_z, rows, bits in ((kc, ks, kz, k_rows, bk), (vc, vs, vz, v_rows, bv)):
+        c, s, z = quantize(rows, bits)
         assert np.array_equal(got_c, c), f"codes differ at {np.argwhere(got_c != c)[:5].tolist()}"
         assert np.array_equal(got_s.view(np.uint16), s.view(np.uint16)), "scales differ"
         assert np.array_equal(got_z.view(np.uint16), z.view(np.uint16)), "zeros differ"
     # rows past the stream end inside the last block are zero
     if n_rows % 64:
-        kc_all, vc_all, ks_all, *_ = unpack_qblocks(blocks, blocks.shape[0] * 64)
+        kc_all, vc_all, ks_all, *_ = unpack_qblocks(blocks, blocks.shape[0] * 64, bk, bv)
         assert not kc_all[n_rows:(n_rows + 63) // 64 * 64].any()
 
 
