@@ -190,16 +190,19 @@ def prefill_measure(dev, lengths, reps=5, warmup=3, windows=("fixed", "band")):
     return res
 
 
-def batched_measure(dev, batch=16, n_layers=4, reps=5, warmup=3, seed=1003):
+def batched_measure(dev, batch=16, n_layers=4, reps=5, warmup=3, seed=1003, hq=HQ, model_layers=36,
+                    heavy_tail=False, workload=None):
     """Decode attention at batch 16 (Qwen3-8B-shaped heads: 32 query / 8 KV,
     d 128, 32K context, W 128, rho 5%): per-call time over n_layers distinct
     layers (~3 GB of hybrid caches, far beyond L2), CUDA events.  Each layer
     is built from device-generated BF16 (2% planted vertical lines) that is
-    freed once the layer's hybrid cache is built."""
+    freed once the layer's hybrid cache is built.  ``heavy_tail`` scales each
+    planted key's direction by 4 |t|, t ~ Student-t(3) (the Qwen3-32B-shaped
+    workload's sinks)."""
     import torch
     import hybrid_precision_quantized_gb300 as hyq
     from hybrid_precision_quantized_gb300 import _lib as L
-    Bb = batch
+    Bb, HQ = batch, hq
     cfg = hyq.make_config(Bb, HQ, HKV, capacity=CTX, window=WINDOW, period=PERIOD, rho_ppm=RHO_PPM)
     g = torch.Generator(device=dev)
     g.manual_seed(seed)
@@ -214,7 +217,12 @@ def batched_measure(dev, batch=16, n_layers=4, reps=5, warmup=3, seed=1003):
         pos = torch.randint(0, P, (Bb, HKV, ns), generator=g, device=dev)
         bi = torch.arange(Bb, device=dev)[:, None, None].expand_as(pos)
         hi = torch.arange(HKV, device=dev)[None, :, None].expand_as(pos)
-        k[bi, hi, pos] += (4.0 * u[:, :, None, :]).to(torch.bfloat16).expand(Bb, HKV, ns, D)
+        mag = torch.full((Bb, HKV, ns, 1), 4.0, device=dev)
+        if heavy_tail:   # t = N / sqrt(chi2_3 / 3)
+            t = torch.randn(Bb, HKV, ns, 1, generator=g, device=dev)
+            chi = torch.randn(Bb, HKV, ns, 3, generator=g, device=dev).pow(2).sum(-1, keepdim=True) / 3.0
+            mag = 4.0 * (t / chi.sqrt()).abs()
+        k[bi, hi, pos] += (mag * u[:, :, None, :]).to(torch.bfloat16)
         v = torch.randn(Bb, HKV, CTX, D, generator=g, device=dev, dtype=torch.bfloat16)
         qt = (torch.randn(Bb, HQ, 64, D, generator=g, device=dev)
               + 2.0 * u.repeat_interleave(HQ // HKV, 1)[:, :, None]).to(torch.bfloat16)
@@ -245,8 +253,9 @@ def batched_measure(dev, batch=16, n_layers=4, reps=5, warmup=3, seed=1003):
     peak, kind = measured_peaks()
     gbs = nbytes / (us * 1e-6) / 1e9
     err = max(hyq.hyq_read_device_error(l.err()) for l in layers)
-    return {"workload": "qwen3-8b-shaped batched decode attention, B16, 32/8 heads, d128, 32K ctx, W128, rho 5%, "
-                        "K4V4 G32; 4 distinct layers", "us_per_call": us, "us_per_token_36_layers": us * 36 / Bb,
+    return {"workload": workload or ("qwen3-8b-shaped batched decode attention, B16, 32/8 heads, d128, 32K ctx, "
+                                     "W128, rho 5%, K4V4 G32; 4 distinct layers"),
+            "us_per_call": us, f"us_per_token_{model_layers}_layers": us * model_layers / Bb,
             "algorithmic_bytes_per_call": nbytes,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                          "peak_source": f"{kind} hbm_gbs"},
@@ -620,6 +629,10 @@ def run_ours(args, rank, world, local):
     base = None if args.no_baseline else cpu_baseline()
     prefill = None if args.no_prefill else prefill_measure(dev, [CTX], reps=5)
     batched = None if args.no_batched else batched_measure(dev)
+    batched32 = None if args.no_batched else batched_measure(
+        dev, batch=4, hq=64, n_layers=6, seed=1004, model_layers=64, heavy_tail=True,
+        workload="qwen3-32b-shaped decode attention, B4, 64/8 heads, d128, 32K ctx, W128, rho 5%, K4V4 G32, "
+                 "2% planted sinks with 4|t| magnitudes (Student-t, nu 3); 6 distinct layers")
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": False,
@@ -644,6 +657,7 @@ def run_ours(args, rank, world, local):
         "clocks": clk.summary(),
         "cpu_baseline": base,
         "batched": batched,
+        "batched_qwen32b": batched32,
         "frozen": frozen,
         "mass_selection": mass,
         "widths": widths,
