@@ -450,14 +450,25 @@ __device__ void mass_stage_q(__nv_bfloat16* qs, const __nv_bfloat16* qp, int b, 
   }
 }
 
-// Stage key rows [j0, j0 + 64) of (b, h), zero past `end`.
-__device__ void mass_stage_k(__nv_bfloat16* ks, const __nv_bfloat16* kb, int j0, int end) {
+// Start the asynchronous copy of key rows [j0, j0 + 64) of (b, h) into a
+// staging buffer (rows past `end` are zero-filled) and commit it as one
+// group of this thread's copies.
+__device__ void mass_stage_k_async(__nv_bfloat16* ks, const __nv_bfloat16* kb, int j0, int end) {
   for (int i = threadIdx.x; i < kMassKeys * 16; i += kMassThreads) {
     const int r = i >> 4, c = i & 15;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (j0 + r < end) v = __ldg(reinterpret_cast<const uint4*>(kb + (size_t)(j0 + r) * HYQ_D) + c);
-    *reinterpret_cast<uint4*>(ks + r * kMassStride + 8 * c) = v;
+    const bool in = j0 + r < end;
+    const __nv_bfloat16* src = kb + (size_t)(in ? j0 + r : 0) * HYQ_D + 8 * c;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(ks + r * kMassStride + 8 * c)),
+                 "l"(src), "r"(in ? 16 : 0)
+                 : "memory");
   }
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+
+// Wait until at most `n` of this thread's most recent copy groups are pending.
+template <int n>
+__device__ __forceinline__ void mass_wait_async() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(n) : "memory");
 }
 
 // A fragments (m16n8k16, row-major 16 x 128) of the 16-row block rb.
@@ -495,7 +506,7 @@ __device__ __forceinline__ void mass_tile(const __nv_bfloat16* ksm, int lane, co
 }
 
 // Pass 1.  grid (splits <= kMassSplits, HKV * n_groups, B); dynamic smem: the row
-// group's queries and one key tile.  part[((bh * n_groups + rg) *
+// group's queries and two key tiles (one landing while the other is used).  part[((bh * n_groups + rg) *
 // kMassSplits + split) * 256 + row] = (m, l) of the split's keys.
 __global__ void __launch_bounds__(kMassThreads) mass_stats_kernel(
     const __nv_bfloat16* __restrict__ qp, int32_t n_proxy, int32_t n_ld, int32_t gq,
@@ -520,12 +531,19 @@ __global__ void __launch_bounds__(kMassThreads) mass_stats_kernel(
   const int ns = gridDim.x;
   const int j0 = (int)((int64_t)split * L / ns), j1 = (int)((int64_t)(split + 1) * L / ns);
   const __nv_bfloat16* kb = k_src + bh * ld * HYQ_D;
-  for (int kt = j0; kt < j1; kt += kMassKeys) {
-    __syncthreads();  // the previous tile is consumed
-    mass_stage_k(ksm, kb, kt, j1);
-    __syncthreads();
+  // two staging buffers: tile i + 1 is in flight while tile i is consumed
+  if (j0 < j1) mass_stage_k_async(ksm, kb, j0, j1);
+  for (int kt = j0, it = 0; kt < j1; kt += kMassKeys, ++it) {
+    __nv_bfloat16* kcur = ksm + (it & 1) * kMassKeys * kMassStride;
+    if (kt + kMassKeys < j1) {
+      mass_stage_k_async(ksm + ((it + 1) & 1) * kMassKeys * kMassStride, kb, kt + kMassKeys, j1);
+      mass_wait_async<1>();
+    } else {
+      mass_wait_async<0>();
+    }
+    __syncthreads();  // tile `it` has landed for every thread
     float C[2][8][4];
-    mass_tile(ksm, lane, a0, a1, C);
+    mass_tile(kcur, lane, a0, a1, C);
     const int nvalid = min(kMassKeys, j1 - kt);
 #pragma unroll
     for (int blk = 0; blk < 2; ++blk)
@@ -557,6 +575,7 @@ __global__ void __launch_bounds__(kMassThreads) mass_stats_kernel(
           m[blk][hf] = mn;
         }
       }
+    __syncthreads();  // every warp is done with buffer `it & 1` before it is refilled
   }
   if (t == 0) {
     float2* out = part + ((bh * n_groups + rg) * kMassSplits + split) * kMassGroupRows;
@@ -602,7 +621,7 @@ __global__ void __launch_bounds__(kMassThreads) mass_colsum_kernel(
   extern __shared__ __align__(16) unsigned char mass_smem[];
   __nv_bfloat16* qs = reinterpret_cast<__nv_bfloat16*>(mass_smem);
   __nv_bfloat16* ksm = qs + kMassGroupRows * kMassStride;
-  float* red = reinterpret_cast<float*>(ksm + kMassKeys * kMassStride);  // [8 warps][64 keys]
+  float* red = reinterpret_cast<float*>(ksm + 2 * kMassKeys * kMassStride);  // [8 warps][64 keys]
   const int HKV = gridDim.y / n_groups, h = blockIdx.y / n_groups, rg = blockIdx.y % n_groups;
   const int b = blockIdx.z;
   const size_t bh = (size_t)b * HKV + h, bg = bh * n_groups + rg;
@@ -617,12 +636,20 @@ __global__ void __launch_bounds__(kMassThreads) mass_colsum_kernel(
   for (int blk = 0; blk < 2; ++blk)
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) st[blk][hf] = stats[bg * kMassGroupRows + 16 * (2 * warp + blk) + g + 8 * hf];
-  for (int kt = blockIdx.x * kMassKeys; kt < P; kt += gridDim.x * kMassKeys) {
-  __syncthreads();  // the previous tile's key rows and sums are consumed
-  mass_stage_k(ksm, k_src + bh * ld * HYQ_D, kt, P);
-  __syncthreads();
+  const __nv_bfloat16* kb = k_src + bh * ld * HYQ_D;
+  const int step = gridDim.x * kMassKeys;
+  if ((int)blockIdx.x * kMassKeys < P) mass_stage_k_async(ksm, kb, blockIdx.x * kMassKeys, P);
+  for (int kt = blockIdx.x * kMassKeys, it = 0; kt < P; kt += step, ++it) {
+  __nv_bfloat16* kcur = ksm + (it & 1) * kMassKeys * kMassStride;
+  if (kt + step < P) {
+    mass_stage_k_async(ksm + ((it + 1) & 1) * kMassKeys * kMassStride, kb, kt + step, P);
+    mass_wait_async<1>();
+  } else {
+    mass_wait_async<0>();
+  }
+  __syncthreads();  // tile `it` has landed for every thread; the sums of the previous one are read
   float C[2][8][4];
-  mass_tile(ksm, lane, a0, a1, C);
+  mass_tile(kcur, lane, a0, a1, C);
   float cs[8][2];
 #pragma unroll
   for (int nb = 0; nb < 8; ++nb) cs[nb][0] = cs[nb][1] = 0.f;
@@ -654,6 +681,7 @@ __global__ void __launch_bounds__(kMassThreads) mass_colsum_kernel(
     for (int w = 0; w < kMassThreads / 32; ++w) S += red[w * kMassKeys + threadIdx.x];
     colsum[bg * pmax + kt + threadIdx.x] = S;
   }
+  __syncthreads();  // buffer `it & 1` and the sums are consumed before they are reused
   }
 }
 
@@ -768,7 +796,7 @@ cudaError_t hyq_launch_select_mass(const hyq_config* c, const void* q_proxy, int
   const int32_t P = L - c->window;  // > 0 since k > 0
   const int32_t gq = c->num_q_heads / c->num_kv_heads, R = gq * n_proxy, ng = mass_groups(c, n_proxy);
   const float cs = (float)(1.0 / std::sqrt((double)HYQ_D) / std::log(2.0));  // fl(alpha log2 e)
-  const int smem_stats = (kMassGroupRows + kMassKeys) * kMassStride * 2;
+  const int smem_stats = (kMassGroupRows + 2 * kMassKeys) * kMassStride * 2;  // queries + two key buffers
   const int smem_col = smem_stats + (kMassThreads / 32) * kMassKeys * 4;
   static bool attr_done = false;
   if (!attr_done) {
