@@ -763,6 +763,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
            min(16, nf - 16 * fi), lane, q_s, st);
 
   // ---- warp partials -> block partial (m, l, acc) in shared memory ---------
+  if (sa.nx_counts && warp == kWarps - 1) {  // as soon as this warp's own reads are done
+    const NextCounts nxc = next_counts(sa, b, nblk_cap, cap_vl, cap_tail);
+    prefetch_next_tiles<kTile>(sa, nxc, bh, split, S, nblk_cap, lane);
+    prefetch_next_rows(sa, nxc, bh, split, S, cap_vl, cap_tail, lane);
+  }
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
 #pragma unroll
@@ -773,11 +778,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
       for (int o = 4; o < 32; o <<= 1) st.zacc[j][qq] += __shfl_xor_sync(0xffffffffu, st.zacc[j][qq], o);
   }
   __syncthreads();  // every warp is done with its ring: reuse shared memory
-  if (sa.nx_counts && warp == kWarps - 1) {
-    const NextCounts nxc = next_counts(sa, b, nblk_cap, cap_vl, cap_tail);
-    prefetch_next_tiles<kTile>(sa, nxc, bh, split, S, nblk_cap, lane);
-    prefetch_next_rows(sa, nxc, bh, split, S, cap_vl, cap_tail, lane);
-  }
   float* red = reinterpret_cast<float*>(smem);                    // [warp][head][128]
   float* blk = red + kWarps * HYQ_MAX_GQA * HYQ_D;                  // [head][2 + 128]
   // Accumulator (m-tile u, ci) of thread (g, t): element 32(u/2) + 4g +

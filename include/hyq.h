@@ -387,7 +387,7 @@ hyq_status hyq_decode_step(const hyq_config *cfg, const void *q, const void *k_n
  *   next  the layout the next decode call will read (typically the next
  *         layer's), allocated for the same cfg; or NULL (no prefetch, the
  *         same launch as hyq_decode_step); may equal lay.
- * Once each block has read its share of lay, it issues L2 prefetches (bulk
+ * Once one warp of each block has read its tiles of lay, it issues L2 prefetches (bulk
  * prefetch hints, no data is written) for the share of next that the same
  * block index of a decode call with the same cfg and len_hint reads: its
  * 4-bit tiles and its vertical-line and tail rows, from next's counters at
