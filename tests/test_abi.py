@@ -218,3 +218,31 @@ def test_stream_size_follows_the_code_widths(lib):
     for (bk, bv), s in sizes.items():
         assert s[0] == -(-(2 * 2 * nblk * L.qblock_bytes(bk, bv)) // 256) * 256
         assert s[1:] == sizes[(4, 4)][1:]       # BF16 buffers do not depend on the widths
+
+
+def test_prefill_band_workspace_holds_the_position_images(lib):
+    """The band workspace adds BF16 key and value images of all L positions
+    (2 x ceil(L / 128) images of 32 KiB per KV head) and drops the window
+    from the full-precision list (at most two images at W = 128)."""
+    c = cfg()
+    for Lc in (1000, 8192):
+        fixed = hyq.hyq_workspace_size(c, L.OP_PREFILL, Lc)
+        band = hyq.hyq_workspace_size(c, L.OP_PREFILL_BAND, Lc)
+        bh, img, ntb = c.batch * c.num_kv_heads, 32768, -(-Lc // 128)
+        assert 2 * bh * img * (ntb - 2) <= band - fixed <= 2 * bh * img * ntb + 4096
+
+
+def test_decode_plan_override_is_validated_and_sizes_the_workspace(lib):
+    c = cfg()
+    try:
+        for merge, splits in [(5, 0), (-1, 0), (2, 1), (2, 17), (3, 0), (3, 1025)]:
+            with pytest.raises(hyq.HyqError):
+                hyq.hyq_set_decode_plan(merge, splits)
+        hyq.hyq_set_decode_plan(3, 2)
+        small = hyq.hyq_workspace_size(c, L.OP_DECODE, 32768)
+        hyq.hyq_set_decode_plan(3, 7)
+        large = hyq.hyq_workspace_size(c, L.OP_DECODE, 32768)
+        bh = c.batch * c.num_kv_heads
+        assert large - small >= bh * 5 * 8 * 130 * 4      # five more partial slots per (sequence, KV head)
+    finally:
+        hyq.hyq_set_decode_plan(0, 0)
