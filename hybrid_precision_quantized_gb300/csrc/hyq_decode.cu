@@ -124,8 +124,8 @@ struct StepArgs {
   int32_t* tickets_b;          // [B] per-sequence ticket of the counter update
   int32_t overlap;             // launched as a programmatic dependent (hyq_set_decode_overlap)
   // Layout of the next decode call (hyq_decode_step_prefetch), or nullptr:
-  // once a block has read its share of this layer it asks L2 to prefetch the
-  // share of that layout the same block index will read.
+  // once the block's last warp has read its tiles of this layer, that warp
+  // asks L2 to prefetch the share of that layout the same block index will read.
   const uint8_t* nx_qblocks;
   const int32_t* nx_counts;
   const __nv_bfloat16 *nx_vl_k, *nx_vl_v, *nx_tail_k, *nx_tail_v;
