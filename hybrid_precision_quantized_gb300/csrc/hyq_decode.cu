@@ -157,7 +157,7 @@ __device__ __forceinline__ NextCounts next_counts(const StepArgs& sa, int b, int
 
 // One warp, once the block has read its share of this layer: prefetch into
 // L2 the next layout's quantised tiles [t0, t1) of KV head bh, the share of
-// block `split` under the same partition (contiguous, 16 KB per lane).
+// block `split` under the same partition (contiguous, 64 KB per lane).
 template <int kTileBytes>
 __device__ void prefetch_next_tiles(const StepArgs& sa, const NextCounts& n, size_t bh, int split, int S,
                                     int nblk_cap, int lane) {
@@ -165,7 +165,7 @@ __device__ void prefetch_next_tiles(const StepArgs& sa, const NextCounts& n, siz
   const int t0 = share_bound(split, nt, S), t1 = share_bound(split + 1, nt, S);
   const uint8_t* tiles = sa.nx_qblocks + bh * (size_t)nblk_cap * (4 * kTileBytes) + (size_t)t0 * kTileBytes;
   const uint32_t bytes = (uint32_t)(t1 - t0) * kTileBytes;
-  constexpr uint32_t kChunk = 16384;
+  constexpr uint32_t kChunk = 65536;
   for (uint32_t off = lane * kChunk; off < bytes; off += 32 * kChunk)
     prefetch_l2(tiles + off, min(kChunk, bytes - off));
 }
