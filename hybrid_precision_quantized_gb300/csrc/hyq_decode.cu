@@ -155,7 +155,7 @@ __device__ __forceinline__ NextCounts next_counts(const StepArgs& sa, int b, int
                     min(max(cn[HYQ_CNT_NTAIL], 0), cap_tail)};
 }
 
-// One warp, once the block has read its share of this layer: prefetch into
+// One warp, once it has read its own tiles of this layer: prefetch into
 // L2 the next layout's quantised tiles [t0, t1) of KV head bh, the share of
 // block `split` under the same partition (contiguous, 64 KB per lane).
 template <int kTileBytes>
