@@ -185,7 +185,7 @@ def mass_error_bound(q_proxy, k_src, L: int, window: int, chunks: int = 1024,
     return bound
 
 
-# --- float32 error bounds used to judge a float32 implementation -----------
+# --- float32 error bounds used to check a float32 implementation -----------
 
 def _gamma(n: int, unit: float = 2.0 ** -23) -> float:
     # unit = 2^-23 (one float32 ulp, not half) so that the bound also covers
