@@ -234,7 +234,29 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// kLazy: first test (one warp vote) whether any logit of the tile exceeds its
+// head's running maximum; if none does, the maximum stays, the correction is
+// 1 and no cross-lane maximum is needed (the full path would give the same
+// bits).  It pays off on long per-warp runs of tiles (one block per
+// sequence and KV head), not on short ones, where early tiles move the
+// maximum.
+template <bool kLazy>
 __device__ __forceinline__ void softmax_update(const float (&lg)[4], State& st, float (&p)[4]) {
+  if (kLazy) {
+    bool above = false;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) above |= fmaxf(lg[j], lg[2 + j]) > st.m[j];
+    if (!__any_sync(0xffffffffu, above)) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float ms = st.m[j] == -INFINITY ? 0.f : st.m[j];
+        p[j] = ex2(lg[j] - ms);
+        p[2 + j] = ex2(lg[2 + j] - ms);
+        st.l[j] += p[j] + p[2 + j];
+      }
+      return;
+    }
+  }
   float corr[2];
   bool moved = false;
 #pragma unroll
@@ -298,7 +320,7 @@ __device__ __forceinline__ void load_words(const uint8_t* region, int lane, uint
 // 8-bit: bytes 0 and 2 of a word by one AND, bytes 1 and 3 by one byte
 // permute, each a fragment register of two codes.  bq holds the query as
 // fp16, scaled by 2^e.
-template <int BK, int BV>
+template <int BK, int BV, bool kLazy>
 __device__ __forceinline__ void q_tile(const uint8_t* tb, int lane, int vr, const uint32_t (&bq)[8][2],
                                        const QConst& qc, State& st) {
   using F = QFmt<BK, BV>;
@@ -344,7 +366,7 @@ __device__ __forceinline__ void q_tile(const uint8_t* tb, int lane, int vr, cons
     lg[2 * r + 1] = valid ? fmaf(a1, qc.ksc[r], b1) : -INFINITY;
   }
   float p[4];
-  softmax_update(lg, st, p);
+  softmax_update<kLazy>(lg, st, p);
   uint32_t vw[BV == 4 ? 8 : 16];
   load_words<BV == 4 ? 8 : 16>(tb + F::kVCode, lane, vw);
   const uint8_t* vm = tb + F::kVMeta;
@@ -396,7 +418,7 @@ __device__ __forceinline__ uint32_t u4c(const uint4& v, int i) {
 // by the tail), `vr` valid rows, loaded directly into fragment registers; row
 // `rnew` (a fused step's new row) is read from knew/vnew.  BV: the value code
 // width of the quantised tiles, whose accumulator convention the tile follows.
-template <int BV>
+template <int BV, bool kLazy>
 __device__ __forceinline__ void f_tile(const __nv_bfloat16* vlk, const __nv_bfloat16* vlv,
                                        const __nv_bfloat16* tk, const __nv_bfloat16* tv, int nvl,
                                        int rnew, const __nv_bfloat16* knew, const __nv_bfloat16* vnew,
@@ -431,7 +453,7 @@ __device__ __forceinline__ void f_tile(const __nv_bfloat16* vlk, const __nv_bflo
   lg[2] = g + 8 < vr ? S[2] * kScale : -INFINITY;
   lg[3] = g + 8 < vr ? S[3] * kScale : -INFINITY;
   float p[4];
-  softmax_update(lg, st, p);
+  softmax_update<kLazy>(lg, st, p);
   // P^T (tokens x heads), scaled by 2^-24 like the 4-bit accumulators.
   const uint32_t b0 = movmatrix_trans(pack_bf16x2(p[0] * kSubScale, p[1] * kSubScale));
   const uint32_t b1 = movmatrix_trans(pack_bf16x2(p[2] * kSubScale, p[3] * kSubScale));
@@ -461,7 +483,7 @@ __device__ __forceinline__ void f_tile(const __nv_bfloat16* vlk, const __nv_bflo
 // at kFVStride); rows at or past `vr` are masked (their contents are undefined).
 // The unpadded rows cost 2-way (K) and 4-way (V) bank conflicts on these few
 // loads, against 32 single-row copies per tile otherwise.
-template <int BV>
+template <int BV, bool kLazy>
 __device__ __forceinline__ void f_tile_smem(const uint8_t* Ks, const uint8_t* Vs, int vr, int lane,
                                             const __nv_bfloat16* q_s, State& st) {
   const int g = lane >> 2, t = lane & 3;
@@ -489,7 +511,7 @@ __device__ __forceinline__ void f_tile_smem(const uint8_t* Ks, const uint8_t* Vs
   lg[2] = g + 8 < vr ? S[2] * kScale : -INFINITY;
   lg[3] = g + 8 < vr ? S[3] * kScale : -INFINITY;
   float p[4];
-  softmax_update(lg, st, p);
+  softmax_update<kLazy>(lg, st, p);
   const uint32_t b0 = movmatrix_trans(pack_bf16x2(p[0] * kSubScale, p[1] * kSubScale));
   const uint32_t b1 = movmatrix_trans(pack_bf16x2(p[2] * kSubScale, p[3] * kSubScale));
   uint2 va[4][4];
@@ -735,7 +757,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
       break;
     }
     const int tile = t0 + my0 + kWarps * j;
-    q_tile<BK, BV>(ring + slot * kTile, lane, min(16, nq - 16 * tile), bq, qc, st);
+    q_tile<BK, BV, kMode == kDirect>(ring + slot * kTile, lane, min(16, nq - 16 * tile), bq, qc, st);
     __syncwarp();
     if (lane == slot && j + kSlots < nj) {
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
@@ -755,11 +777,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
       }
       __syncwarp();
     } else {
-      f_tile_smem<BV>(fstage, fstage + 16 * kFKStride, min(16, nf - 16 * (f0 + warp)), lane, q_s, st);
+      f_tile_smem<BV, kMode == kDirect>(fstage, fstage + 16 * kFKStride, min(16, nf - 16 * (f0 + warp)), lane, q_s,
+                                        st);
     }
   }
   for (int fi = f0 + kFStaged + warp; fi < f1; fi += kWarps)  // tiles past the staged ones
-    f_tile<BV>(vlk, vlv, tk, tv, nvl, app ? nvl + ntail : -1, sa.k_new + bh * HYQ_D, sa.v_new + bh * HYQ_D, 16 * fi,
+    f_tile<BV, kMode == kDirect>(vlk, vlv, tk, tv, nvl, app ? nvl + ntail : -1, sa.k_new + bh * HYQ_D, sa.v_new + bh * HYQ_D, 16 * fi,
            min(16, nf - 16 * fi), lane, q_s, st);
 
   // ---- warp partials -> block partial (m, l, acc) in shared memory ---------
