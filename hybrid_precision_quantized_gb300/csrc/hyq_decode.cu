@@ -628,6 +628,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
     mbar_fence_init();
   }
   __syncwarp();
+  // Ring slot i is always filled by lane i: the bulk copies one thread issues
+  // complete one after another, so one issuing lane per slot keeps all of a
+  // warp's slots in flight at once.
+  if (lane < kSlots && lane < nj) {
+    const int j = lane;
+    mbar_arrive_expect_tx(&wb[j], kTile);
+    bulk_g2s(ring + j * kTile, tiles + (size_t)(t0 + my0 + kWarps * j) * kTile, kTile, &wb[j]);
+  }
   if (warp < n_staged) {
     // The first kFStaged BF16 tiles of this block: the rows of a tile are
     // contiguous in the vertical-line buffer and in the tail, so a tile takes
@@ -650,14 +658,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
       bulk_g2s(fstage + na * kFKStride, tk + (size_t)tr * HYQ_D, ntr * HYQ_D * 2, &fbars[warp]);
       bulk_g2s(fstage + 16 * kFKStride + na * kFVStride, tv + (size_t)tr * HYQ_D, ntr * HYQ_D * 2, &fbars[warp]);
     }
-  }
-  // Ring slot i is always filled by lane i: the bulk copies one thread issues
-  // complete one after another, so one issuing lane per slot keeps all of a
-  // warp's slots in flight at once.
-  if (lane < kSlots && lane < nj) {
-    const int j = lane;
-    mbar_arrive_expect_tx(&wb[j], kTile);
-    bulk_g2s(ring + j * kTile, tiles + (size_t)(t0 + my0 + kWarps * j) * kTile, kTile, &wb[j]);
   }
   for (int i = gq * HYQ_D / 8 + tid; i < HYQ_MAX_GQA * HYQ_D / 8; i += kThreads)
     reinterpret_cast<uint4*>(q_s)[i] = make_uint4(0, 0, 0, 0);  // query rows past g
