@@ -5,9 +5,11 @@
  * The method is the one of "HyQuant: Hybrid-Precision Quantization for LLM
  * Attention": per layer and KV head, the key/value positions are split into a
  * small set of vertical-line positions and a recent window, kept in BF16, and
- * the remaining majority, stored as asymmetric 4-bit codes (§4.1 Eq. 1-3,
- * §4.3 Eq. 8).  Decode attention dequantises the 4-bit rows inside one
- * online-softmax pass (§4.3 Eq. 9, Appendix A.3 Algorithm 3).
+ * the remaining majority, stored as asymmetric low-bit codes (§4.1 Eq. 1-3,
+ * §4.3 Eq. 8): 4-bit keys and values by default, 8-bit keys and/or values
+ * when hyq_config.bits_k / bits_v ask for them.  Decode attention
+ * dequantises the quantised rows inside one online-softmax pass (§4.3 Eq. 9,
+ * Appendix A.3 Algorithm 3).
  *
  * Conventions for every entry point
  * ---------------------------------
@@ -186,12 +188,13 @@ hyq_status hyq_layout_reset(const hyq_config *cfg, const hyq_layout *lay, hyq_st
 /*
  * Quant_B(.; G) of Algorithm 4 (Appendix A.4) and the low-bit cache of §4.3
  * Eq. 8: quantise n_rows new rows per (batch, KV head) of K and V and append
- * them to the 4-bit stream after its current NQ rows.
+ * them to the quantised stream after its current NQ rows.
  *   k_rows, v_rows  device bf16 [B][HKV][n_rows][128]
- * Per group of 32 elements along head_dim, with mn/mx the group min/max:
- *   s = FP16 value of (mx - mn) / 15 (float64 quotient) rounded toward +inf,
+ * Per group of 32 elements along head_dim, with mn/mx the group min/max and
+ * qmax = 2^B - 1 (B = bits_k for K, bits_v for V: 15 or 255):
+ *   s = FP16 value of (mx - mn) / qmax (exact quotient) rounded toward +inf,
  *   z = FP16 value of mn rounded to nearest even,
- *   c = clamp(rint((x - z) * r), 0, 15) in float32 with r = 1/s rounded to
+ *   c = clamp(rint((x - z) * r), 0, qmax) in float32 with r = 1/s rounded to
  *       nearest (c = 0 when s = 0).
  * A group with a non-finite s or z gets zero codes, s = z = 0 and sets
  * HYQ_DEVERR_QUANT_RANGE.  Rows that would pass the capacity are dropped and
@@ -287,8 +290,9 @@ hyq_status hyq_decode_append(const hyq_config *cfg, const void *q, const void *k
  * A.3): for every query head h (KV head h / g)
  *   out_h = sum_j exp(a q_h.k~_j - M) v~_j / sum_j exp(a q_h.k~_j - M),
  * a = 1/sqrt(128), over the LEN positions of the layout, with k~, v~ the
- * dequantised 4-bit rows (c*s + z) and the BF16 vertical-line and tail rows.
- * The 4-bit stream is split along the sequence across thread blocks, the g
+ * dequantised rows of the quantised stream (c*s + z, B_K- and B_V-bit codes)
+ * and the BF16 vertical-line and tail rows.
+ * The quantised stream is split along the sequence across thread blocks, the g
  * query heads of a KV head are processed together, and the split partials
  * are merged by log-sum-exp rescaling in the same launch.
  *   q    device bf16 [B][HQ][128]
