@@ -613,8 +613,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       float rs;
       uint32_t pw[32];
       const uint64_t vf2 = f2_splat(vf);
-      if (!masked) {
-        // Pairs: scale, shift, sum and scale by vf packed.
+      {
+        // Pairs: scale, shift, sum and scale by vf packed (masked keys are
+        // -inf here and give 0).
         const uint64_t cs2 = f2_splat(cs), nmb2 = f2_splat(-mb);
         uint64_t ps2[4] = {0, 0, 0, 0};
 #pragma unroll
@@ -627,21 +628,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         }
         const uint64_t r2 = f2_add(f2_add(ps2[0], ps2[1]), f2_add(ps2[2], ps2[3]));
         rs = f2_lo(r2) + f2_hi(r2);
-      } else {
-        float ps[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) ps[u] = 0.f;
-#pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          x[i] = fast_exp2(fmaf(x[i], cs, -mb));
-          ps[i & 7] += x[i];
-        }
-        rs = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-#pragma unroll
-        for (int w = 0; w < 32; ++w) {
-          const uint64_t pv = f2_mul(f2_pack(x[2 * w], x[2 * w + 1]), vf2);
-          pw[w] = pack_bf16x2(f2_lo(pv), f2_hi(pv));
-        }
       }
       l_sum = l_sum * fac + rs;
       m_used = m_new;
