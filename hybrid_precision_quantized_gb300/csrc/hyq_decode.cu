@@ -6,8 +6,9 @@
 //   the 4-bit stream of a (batch, KV head) is split along the sequence into
 //   S chunks (Algorithm 3, segment 1), and so are its BF16 rows (vertical-
 //   line rows, then the tail).  Inside a block every warp works alone on
-//   16-row tiles: BF16 tiles first, then 4-bit tiles streamed through its own
-//   ring of bulk copies (TMA, no block-wide barrier in the main loop).  Each
+//   16-row tiles: its 4-bit tiles streamed through its own ring of bulk
+//   copies (TMA, no block-wide barrier in the main loop), then its BF16
+//   tiles.  Each
 //   warp keeps one online-softmax state (m, l, acc) for the g query heads of
 //   the KV group, packed into one tensor-core tile (Algorithm 3, "pack g GQA
 //   heads").  The block merges its warps; the S block partials are merged by
@@ -25,7 +26,9 @@
 // per-group query sums are applied in fp32.  BF16 tiles are staged by bulk
 // copies (or loaded straight into fragment registers); the head_dim order of
 // the K products and of the V outputs is permuted (identically in both paths,
-// see hyq.h) so that those loads are 16- and 8-byte vectors.
+// see hyq.h) so that those loads are 16- and 8-byte vectors.  The code
+// widths are template parameters: 4- or 8-bit keys (BK) and values (BV), in
+// the tile layouts of hyq.h.
 #include <cooperative_groups.h>
 #include <math.h>
 
