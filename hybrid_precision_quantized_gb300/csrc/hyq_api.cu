@@ -1,6 +1,7 @@
 // Host side of the libhyq C ABI: argument validation, buffer sizing and
 // dispatch to the kernels.  Every check runs before any launch, so an invalid
 // call leaves all buffers untouched.
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 
@@ -28,14 +29,19 @@ bool layout_ok(const hyq_layout* l) {
 
 }  // namespace
 
+// Streaming-multiprocessor count of the current device, cached per device
+// (atomics: any host thread may call this for any device).
 int hyq_num_sms() {
-  static int cached = 0;
-  if (cached > 0) return cached;
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-    n = 148;
-  cached = n;
+  static std::atomic<int> cached[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) dev = -1;
+  if (dev >= 0 && dev < kMaxDevices) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  int n = 0;
+  if (dev < 0 || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  if (dev >= 0 && dev < kMaxDevices) cached[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 

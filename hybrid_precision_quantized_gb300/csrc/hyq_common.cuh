@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/hyq.h"
 
 #define HYQ_D 128
@@ -16,12 +18,31 @@
 #define HYQ_KMETA_OFF 8192
 #define HYQ_VMETA_OFF 9216
 #define HYQ_VCODE_OFF 4096
-#define HYQ_DEVERR_TIMEOUT 0x10  // internal: a bounded wait gave up
 
 // ---------------------------------------------------------------------------
 // Launch plumbing shared by the translation units (defined in hyq_api.cu).
 // ---------------------------------------------------------------------------
+// Devices the per-device host caches cover (device ordinals 0 .. kMaxDevices-1).
+constexpr int kMaxDevices = 64;
 int hyq_num_sms();
+// Ordinal of the current device, or -1 when it cannot be read or lies past kMaxDevices.
+inline int hyq_device() {
+  int d = 0;
+  return cudaGetDevice(&d) == cudaSuccess && d >= 0 && d < kMaxDevices ? d : -1;
+}
+// Runs f() (an idempotent setup returning cudaError_t, e.g. a kernel attribute)
+// until it has succeeded once with the current device; `done` holds one bit
+// per device.  Two threads making the first call at once may both run f.
+template <class F>
+cudaError_t hyq_once_per_device(std::atomic<uint64_t>& done, F f) {
+  const int d = hyq_device();
+  if (d < 0) return f();
+  const uint64_t bit = 1ull << d;
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  const cudaError_t e = f();
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 int32_t hyq_cap_vl(const hyq_config* c);
 inline int32_t hyq_cap_tail(const hyq_config* c) { return c->window + c->period; }
 // Row stride of the vertical-line buffers (at least one row is allocated).

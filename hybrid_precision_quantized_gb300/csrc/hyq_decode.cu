@@ -82,9 +82,11 @@ struct DecodePlan {
 // About one block per SM over all (batch, KV head) pairs, and not more
 // blocks than there are 16-row tiles to share; one block per pair when even
 // two would not fit in one wave.
-int g_plan_merge = 0;   // hyq_set_decode_plan override (0 = automatic)
-int g_overlap = 0;      // hyq_set_decode_overlap
-int g_plan_splits = 0;
+// Process-wide settings, written by the two setters from any host thread: the
+// plan override packs (merge << 16) | splits into one word so that a launch
+// never sees the merge mode of one call with the split count of another.
+std::atomic<int32_t> g_plan{0};     // hyq_set_decode_plan override (merge 0 = automatic)
+std::atomic<int32_t> g_overlap{0};  // hyq_set_decode_overlap
 
 DecodePlan decode_plan(const hyq_config* c, int32_t len) {
   const int bh = c->batch * c->num_kv_heads;
@@ -93,9 +95,10 @@ DecodePlan decode_plan(const hyq_config* c, int32_t len) {
   int64_t tiles = (int64_t)(P + 15) / 16 + (hyq_vl_count(c, P) + hyq_cap_tail(c) + 15) / 16;
   int cap = (int)(tiles / 32 > 0 ? tiles / 32 : 1);
   DecodePlan p;
-  if (g_plan_merge != 0) {
-    p.mode = g_plan_merge - 1;
-    p.S = p.mode == kDirect ? 1 : g_plan_splits;
+  const int32_t plan = g_plan.load(std::memory_order_relaxed);
+  if (plan >> 16 != 0) {
+    p.mode = (plan >> 16) - 1;
+    p.S = p.mode == kDirect ? 1 : plan & 0xFFFF;
     return p;
   }
   if (2 * bh > sms || cap < 2) {  // even two blocks per pair would not fit in one wave
@@ -1064,21 +1067,26 @@ size_t hyq_decode_ws_bytes(const hyq_config* c, int32_t len_hint) {
 
 template <int kMode, int BK, int BV>
 cudaError_t set_attrs() {
-  static bool done = false;
-  if (done) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<kMode, BK, BV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Dec<BK, BV>::kSmemBytes);
-  if (e == cudaSuccess && kMode == kCluster)
-    e = cudaFuncSetAttribute(decode_kernel<kMode, BK, BV>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  if (e == cudaSuccess) done = true;
-  return e;
+  static std::atomic<uint64_t> done{0};
+  return hyq_once_per_device(done, [] {
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<kMode, BK, BV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Dec<BK, BV>::kSmemBytes);
+    if (e == cudaSuccess && kMode == kCluster)
+      e = cudaFuncSetAttribute(decode_kernel<kMode, BK, BV>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    return e;
+  });
 }
 
-// Can one cluster of S decode blocks be resident on this device?
+// Can one cluster of S decode blocks be resident on the current device?
+// Cached per device (0 unknown, 1 yes, 2 no).
 bool cluster_fits(int S) {
-  static int cached[17] = {0};  // 0 unknown, 1 yes, 2 no
+  static std::atomic<uint8_t> cached[kMaxDevices][17];
   if (S < 2 || S > 16) return false;
-  if (cached[S]) return cached[S] == 1;
+  const int dev = hyq_device();
+  if (dev >= 0) {
+    const uint8_t c = cached[dev][S].load(std::memory_order_relaxed);
+    if (c) return c == 1;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(S, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -1093,13 +1101,13 @@ bool cluster_fits(int S) {
   int n = 0;
   bool ok = cudaOccupancyMaxActiveClusters(&n, decode_kernel<kCluster, 4, 4>, &cfg) == cudaSuccess && n >= 1;
   cudaGetLastError();
-  cached[S] = ok ? 1 : 2;
+  if (dev >= 0) cached[dev][S].store(ok ? 1 : 2, std::memory_order_relaxed);
   return ok;
 }
 
 extern "C" hyq_status hyq_set_decode_overlap(int32_t enable) {
   if (enable != 0 && enable != 1) return HYQ_ERR_INVALID_ARG;
-  g_overlap = enable;
+  g_overlap.store(enable, std::memory_order_relaxed);
   return HYQ_OK;
 }
 
@@ -1107,8 +1115,7 @@ extern "C" hyq_status hyq_set_decode_plan(int32_t merge, int32_t splits) {
   if (merge < 0 || merge > 3) return HYQ_ERR_INVALID_ARG;
   if (merge == 2 && (splits < 2 || splits > 16)) return HYQ_ERR_INVALID_ARG;
   if (merge == 3 && (splits < 1 || splits > kMaxSplits)) return HYQ_ERR_INVALID_ARG;
-  g_plan_merge = merge;
-  g_plan_splits = splits;
+  g_plan.store((merge << 16) | (merge == 0 ? 0 : splits), std::memory_order_relaxed);
   return HYQ_OK;
 }
 
@@ -1127,6 +1134,7 @@ cudaError_t hyq_launch_decode(const hyq_config* c, const void* q, const hyq_layo
   if (p.mode == kCluster && (!w44 || !cluster_fits(p.S))) p.mode = kGlobal;
   size_t bh = (size_t)c->batch * c->num_kv_heads;
   int32_t* tickets = static_cast<int32_t*>(ws);
+  const int32_t overlap = g_overlap.load(std::memory_order_relaxed);
   StepArgs sa{static_cast<const __nv_bfloat16*>(k_new),
               static_cast<const __nv_bfloat16*>(v_new),
               static_cast<__nv_bfloat16*>(k_src),
@@ -1134,7 +1142,7 @@ cudaError_t hyq_launch_decode(const hyq_config* c, const void* q, const hyq_layo
               ld,
               c->period,
               reinterpret_cast<int32_t*>(static_cast<char*>(ws) + round_up(bh * 4)),
-              g_overlap,
+              overlap,
               next ? next->qblocks : nullptr,
               next ? next->counts : nullptr,
               next ? static_cast<const __nv_bfloat16*>(next->vl_k) : nullptr,
@@ -1154,8 +1162,8 @@ cudaError_t hyq_launch_decode(const hyq_config* c, const void* q, const hyq_layo
   attrs[1].val.clusterDim.x = p.S;
   attrs[1].val.clusterDim.y = 1;
   attrs[1].val.clusterDim.z = 1;
-  cfg.attrs = g_overlap ? attrs : attrs + 1;
-  cfg.numAttrs = g_overlap ? 1 : 0;
+  cfg.attrs = overlap ? attrs : attrs + 1;
+  cfg.numAttrs = overlap ? 1 : 0;
   const __nv_bfloat16* qq = static_cast<const __nv_bfloat16*>(q);
   __nv_bfloat16* oo = static_cast<__nv_bfloat16*>(out);
   const int nblk = hyq_nblk(c), cvl = hyq_vl_stride(c), ct = hyq_cap_tail(c);
@@ -1204,7 +1212,6 @@ cudaError_t hyq_launch_decode_append(const hyq_config* c, const void* q, const v
 static __device__ __align__(256) unsigned char g_hyq_noalloc_scratch[HYQ_NOALLOC_SCRATCH_BYTES];
 
 namespace {
-constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mutex;
 void* g_noalloc_addr[kMaxDevices] = {};
 

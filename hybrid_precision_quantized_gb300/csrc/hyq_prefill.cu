@@ -877,13 +877,11 @@ WsLayout ws_layout(const hyq_config* c, bool fp8, int32_t ntq, int32_t ntf, int3
 
 template <bool kFp8, bool kBand>
 cudaError_t launch_main(const MainParams& mp, dim3 grid, cudaStream_t s) {
-  static bool done = false;
-  if (!done) {
-    cudaError_t e =
-        cudaFuncSetAttribute(prefill_kernel<kFp8, kBand>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    done = true;
-  }
+  static std::atomic<uint64_t> done{0};
+  const cudaError_t e = hyq_once_per_device(done, [] {
+    return cudaFuncSetAttribute(prefill_kernel<kFp8, kBand>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  });
+  if (e != cudaSuccess) return e;
   prefill_kernel<kFp8, kBand><<<grid, kThreads, kSmemBytes, s>>>(mp);
   return cudaGetLastError();
 }

@@ -748,13 +748,12 @@ cudaError_t launch_topk(const hyq_config* c, const SelectWs& w, int32_t P, int32
     topk_cluster_kernel<16><<<gc, kTopkCtaThreads, 0, s>>>(w.keys, P, P, k, idx_out);
     return cudaGetLastError();
   }
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kTopkSmemKeys * (int)sizeof(uint32_t));
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  const cudaError_t ea = hyq_once_per_device(attr_done, [] {
+    return cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kTopkSmemKeys * (int)sizeof(uint32_t));
+  });
+  if (ea != cudaSuccess) return ea;
   const size_t tk_smem = P <= kTopkSmemKeys ? (size_t)P * sizeof(uint32_t) : 0;
   topk_kernel<<<dim3(c->num_kv_heads, c->batch), kTopkThreads, tk_smem, s>>>(w.keys, P, P, k, idx_out);
   return cudaGetLastError();
@@ -798,21 +797,15 @@ cudaError_t hyq_launch_select_mass(const hyq_config* c, const void* q_proxy, int
   const float cs = (float)(1.0 / std::sqrt((double)HYQ_D) / std::log(2.0));  // fl(alpha log2 e)
   const int smem_stats = (kMassGroupRows + 2 * kMassKeys) * kMassStride * 2;  // queries + two key buffers
   const int smem_col = smem_stats + (kMassThreads / 32) * kMassKeys * 4;
-  static bool attr_done = false;
-  if (!attr_done) {
+  static std::atomic<uint64_t> attr_done{0};
+  const cudaError_t ea = hyq_once_per_device(attr_done, [&] {
     cudaError_t e = cudaFuncSetAttribute(mass_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_stats);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(mass_colsum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_col);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
-  static int n_sm = 0;
-  if (n_sm == 0) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-  }
+    return e;
+  });
+  if (ea != cudaSuccess) return ea;
+  const int n_sm = hyq_num_sms();
   // one block per SM for pass 1 (one fits an SM) and two per SM for pass 2
   const int units = c->num_kv_heads * ng * c->batch;
   const int ns = std::min(kMassSplits, std::max(1, (n_sm + units - 1) / units));

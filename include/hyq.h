@@ -56,6 +56,9 @@ typedef enum {
 #define HYQ_DEVERR_COUNT 0x2       /* a device-side count exceeded the layout capacity */
 #define HYQ_DEVERR_INDEX 0x4       /* an index list was not strictly ascending in range */
 #define HYQ_DEVERR_SCORE 0x8       /* a selection score was NaN */
+#define HYQ_DEVERR_TIMEOUT 0x10    /* a bounded wait inside a kernel gave up (a bulk copy or a
+                                      tensor-core commit did not complete); the kernel stopped
+                                      issuing work, drained what it had in flight and returned */
 
 /* Shape and method parameters of one attention layer. */
 typedef struct {
@@ -451,8 +454,11 @@ hyq_status hyq_set_decode_plan(int32_t merge, int32_t splits);
  *    len_hint), exceeds HYQ_NOALLOC_SCRATCH_BYTES is rejected with
  *    HYQ_ERR_WORKSPACE before anything is launched.
  *  - Every call on a device shares the one array and each call re-zeroes the
- *    part that must start at zero; two calls that overlap on the GPU (other
- *    streams, other threads) race on it and give wrong results.
+ *    part that must start at zero (a memset on `stream` before the kernel);
+ *    two calls that overlap on the GPU (other streams, other threads) race on
+ *    it and give wrong results.
+ *  - Because of that memset, hyq_set_decode_overlap has no effect on this
+ *    entry point: its kernel is never launched as a programmatic dependent.
  */
 #define HYQ_NOALLOC_SCRATCH_BYTES (4u << 20)
 hyq_status hyq_decode_attention_noalloc(const hyq_config *cfg, const void *q, const hyq_layout *lay,

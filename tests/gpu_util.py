@@ -1,4 +1,7 @@
 """Shared helpers for the GPU parity tests."""
+import os
+import time
+
 import numpy as np
 import torch
 
@@ -59,3 +62,19 @@ def assert_prefill_close(got, want, a, what=""):
     assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} outside tolerance; "
                            f"max abs err {err.max():.3e}, worst excess {(err - bound).max():.3e}")
     return float(err.max())
+
+
+def sample_pairs(B, HKV, n, tag):
+    """n distinct (sequence, KV head) pairs for a sampled full-size parity
+    check, always including the first and the last pair.  The others come
+    from a seed that changes from run to run (so that, over runs, every pair
+    gets checked); set HYQ_SAMPLE_SEED to replay one.  The seed is printed
+    and returned, so a failure message can name it."""
+    seed = int(os.environ.get("HYQ_SAMPLE_SEED", time.time_ns() % (1 << 31)))
+    rng = np.random.default_rng([seed, sum(map(ord, tag))])
+    pairs = [(0, 0), (B - 1, HKV - 1)]
+    rest = [(b, h) for b in range(B) for h in range(HKV) if (b, h) not in pairs]
+    for i in rng.choice(len(rest), size=min(max(n - 2, 0), len(rest)), replace=False):
+        pairs.append(rest[int(i)])
+    print(f"{tag}: HYQ_SAMPLE_SEED={seed} pairs={pairs}")
+    return pairs, seed

@@ -16,7 +16,7 @@ from hybrid_precision_quantized_gb300 import (HybridDecoder, HybridLayer, hyq_de
 from hybrid_precision_quantized_gb300 import _lib as L
 from oracle.attention import hybrid_decode
 from oracle.select import check_selection, prefix_len, score_error_bound, select_vertical
-from tests.gpu_util import assert_attention_close, to_np
+from tests.gpu_util import assert_attention_close, sample_pairs, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -139,8 +139,8 @@ def test_decode_qwen32b_shaped_sweep_sampled(hyq, ppm, W, sink_frac):
     """Qwen3-32B-shaped decode: batch 4, 64/8 heads, 32K context, planted
     sinks with heavy-tailed (Student-t, 3 degrees of freedom) magnitudes, over
     the rho x W sweep.  The GPU computes every head; the oracle, which treats
-    each (sequence, KV head) on its own, checks three sampled pairs (24 query
-    heads) in full."""
+    each (sequence, KV head) on its own, checks three pairs (24 query heads)
+    in full: the first, the last and one drawn from a logged seed."""
     B, HQ, HKV, Lc = 4, 64, 8, 32768
     g = HQ // HKV
     c = decode_case(1004, B, HQ, HKV, Lc, window=W, n_proxy=64, sink_frac=sink_frac, heavy_tail=True)
@@ -149,11 +149,12 @@ def test_decode_qwen32b_shaped_sweep_sampled(hyq, ppm, W, sink_frac):
     k = idx_np.shape[-1]
     assert layer.counts()[0].tolist()[:4] == [P - k, k, Lc - P, Lc]
     q, kk, vv = c.q.double().numpy(), c.k.double().numpy(), c.v.double().numpy()
-    for b, kh in ((0, 0), (1, 5), (3, 7)):
+    pairs, seed = sample_pairs(B, HKV, 3, f"qwen32b rho={ppm} W={W} sinks={sink_frac}")
+    for b, kh in pairs:
         hs = slice(kh * g, (kh + 1) * g)
         want = hybrid_decode(q[b:b + 1, hs], kk[b:b + 1, kh:kh + 1], vv[b:b + 1, kh:kh + 1], Lc, P,
                              idx_np[b:b + 1, kh:kh + 1])
-        assert_attention_close(got[b:b + 1, hs], want, what=f"rho={ppm} W={W} b={b} kvh={kh}")
+        assert_attention_close(got[b:b + 1, hs], want, what=f"rho={ppm} W={W} b={b} kvh={kh} seed={seed}")
 
 
 def test_decode_pipeline_with_reselection(hyq):
@@ -501,7 +502,8 @@ def test_decode_qwen8b_shaped_batch16_32k_sampled(hyq):
     context, W 128, rho 5%, the launch configuration the benchmark times
     (automatic plan).  Each sequence is its own seeded case; the oracle picks
     each sequence's vertical lines, the GPU decodes all 16 x 32 heads, and
-    three sampled (sequence, KV head) pairs are checked in full."""
+    three (sequence, KV head) pairs are checked in full: the first, the last
+    and one drawn from a logged seed."""
     B, HQ, HKV, Lc, W, ppm = 16, 32, 8, 32768, 128, 50_000
     g = HQ // HKV
     P = prefix_len(Lc, W)
@@ -524,9 +526,10 @@ def test_decode_qwen8b_shaped_batch16_32k_sampled(hyq):
     torch.cuda.synchronize()
     assert hyq_read_device_error(layer.err()) == 0
     got = to_np(out)
-    for b, kh in ((0, 0), (7, 3), (15, 7)):
+    pairs, seed = sample_pairs(B, HKV, 3, "qwen8b batch16")
+    for b, kh in pairs:
         c = cases[b]
         hs = slice(kh * g, (kh + 1) * g)
         want = hybrid_decode(c.q.double().numpy()[:, hs], c.k.double().numpy()[:, kh:kh + 1],
                              c.v.double().numpy()[:, kh:kh + 1], Lc, P, idx_np[b:b + 1, kh:kh + 1])
-        assert_attention_close(got[b:b + 1, hs], want, what=f"b={b} kvh={kh}")
+        assert_attention_close(got[b:b + 1, hs], want, what=f"b={b} kvh={kh} seed={seed}")

@@ -205,3 +205,22 @@ def test_prefill_band_llama_shaped_8k_sampled(hyq, dtype):
     for blk in blocks:
         rows = slice(128 * blk, 128 * blk + 128)
         assert_prefill_close(got[:, :, rows], want[:, :, rows], a[:, :, rows], what=f"band {dtype} block {blk}")
+
+
+@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+def test_prefill_band_llama_shaped_32k_sampled(hyq, dtype):
+    """The benchmark's band workload (Llama-3.1-8B-shaped heads, causal 32K,
+    W 128, rho 5%, the window read per query): the GPU computes every head
+    and query block; the oracle checks three query blocks (first, middle,
+    last) of two heads (the first and the last KV group)."""
+    Lc, W, ppm = 32768, 128, 50_000
+    c = prefill_case(1006, 1, 32, 8, Lc, window=W, sink_frac=0.02)
+    idx = vl_for(c, Lc, W, ppm)
+    got = run_gpu(c, Lc, W, ppm, dtype, idx, band=True)
+    blocks, heads = [0, 128, Lc // 128 - 1], [0, 31]
+    want, a = oracle_band(c, idx, W, dtype, query_blocks=blocks, heads=heads)
+    for hq in heads:
+        for blk in blocks:
+            rows = slice(128 * blk, 128 * blk + 128)
+            assert_prefill_close(got[:, hq, rows], want[:, hq, rows], a[:, hq, rows],
+                                 what=f"band {dtype} head {hq} block {blk}")
