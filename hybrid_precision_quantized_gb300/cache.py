@@ -151,6 +151,21 @@ def _regions(bits_k, bits_v):
     return ((0, bits_k, 0), (ck, bits_v, 1)), ck + cv, ck + cv + 256
 
 
+def _meta_offsets(kv):
+    """Byte offsets [16 rows, 4 groups] of the FP16 scale and zero of every
+    (row, group) inside a tile's 256-byte metadata region: K (kv = 0) row r
+    at 16 r, its four scales then its four zeros; V (kv = 1) rows paired
+    (2i, 2i + 1): the scale pair of group q at 16 i + 4 q, the zero pair 128
+    bytes further."""
+    r = np.arange(16)[:, None]
+    q = np.arange(4)[None, :]
+    if kv == 0:
+        so = 16 * r + 2 * q
+        return so, so + 8
+    so = 16 * (r // 2) + 4 * q + 2 * (r % 2)
+    return so, so + 128
+
+
 def unpack_qblocks(blocks: np.ndarray, n_rows: int, bits_k: int = 4, bits_v: int = 4):
     """Decode the first ``n_rows`` rows of a quantised stream.
 
@@ -171,11 +186,14 @@ def unpack_qblocks(blocks: np.ndarray, n_rows: int, bits_k: int = 4, bits_v: int
             raw = tiles[ti, off:off + size]
             vals = np.stack([raw & 15, raw >> 4], axis=1).reshape(-1) if bits == 4 else raw
             out[kv][ti * 16 + rmap, emap] = vals
-    meta_k = tiles[:, mk:mk + 256].copy().view(np.float16).reshape(nt * 16, 4, 2)
-    meta_v = tiles[:, mv:mv + 256].copy().view(np.float16).reshape(nt * 16, 4, 2)
+    meta = []
+    for off, kv in ((mk, 0), (mv, 1)):
+        so, zo = _meta_offsets(kv)
+        m = tiles[:, off:off + 256].copy().view(np.float16)        # [nt, 128] halves
+        meta.append((m[:, so // 2].reshape(nt * 16, 4), m[:, zo // 2].reshape(nt * 16, 4)))
     n = n_rows
     kc, vc = out
-    return (kc[:n], vc[:n], meta_k[:n, :, 0], meta_k[:n, :, 1], meta_v[:n, :, 0], meta_v[:n, :, 1])
+    return (kc[:n], vc[:n], meta[0][0][:n], meta[0][1][:n], meta[1][0][:n], meta[1][1][:n])
 
 
 def pack_qblocks(k_codes, v_codes, k_scale, k_zero, v_scale, v_zero, bits_k: int = 4,
@@ -204,11 +222,12 @@ def pack_qblocks(k_codes, v_codes, k_scale, k_zero, v_scale, v_zero, bits_k: int
                 nib = vals.reshape(size, 2)
                 vals = nib[:, 0] | (nib[:, 1] << 4)
             tiles[ti, off:off + size] = vals
-    for off, sc, zr in ((mk, k_scale, k_zero), (mv, v_scale, v_zero)):
-        m = np.zeros((nt * 16, 4, 2), np.float16)
-        m[:n, :, 0] = sc
-        m[:n, :, 1] = zr
-        tiles[:, off:off + 256] = m.view(np.uint8).reshape(nt, 256)
+    for off, kv, sc, zr in ((mk, 0, k_scale, k_zero), (mv, 1, v_scale, v_zero)):
+        so, zo = _meta_offsets(kv)
+        m = np.zeros((nt, 128), np.float16)
+        m[:, so // 2] = pad(np.asarray(sc, np.float16), (nt * 16, 4), np.float16).reshape(nt, 16, 4)
+        m[:, zo // 2] = pad(np.asarray(zr, np.float16), (nt * 16, 4), np.float16).reshape(nt, 16, 4)
+        tiles[:, off:off + 256] = m.view(np.uint8)
     return tiles.reshape(nblk, 4 * L.qtile_bytes(bits_k, bits_v))
 
 

@@ -149,20 +149,23 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(bytes) : "memory");
 }
 
-// The next layout's counts for sequence b, clamped to the capacities so that
-// every prefetched address lies in that layout's buffers.
+// The next layout's counts for sequence b, loaded at kernel entry and used
+// once they have arrived; clamped to the capacities so that every prefetched
+// address lies in that layout's buffers.
 struct NextCounts {
   int32_t nq, nvl, ntail;
 };
-__device__ __forceinline__ NextCounts next_counts(const StepArgs& sa, int b, int nblk_cap, int cap_vl,
-                                                  int cap_tail) {
+__device__ __forceinline__ NextCounts load_next_counts(const StepArgs& sa, int b) {
   const int32_t* cn = sa.nx_counts + (size_t)b * HYQ_COUNTS;
-  return NextCounts{min(max(cn[HYQ_CNT_NQ], 0), nblk_cap * HYQ_QBLOCK_ROWS), min(max(cn[HYQ_CNT_NVL], 0), cap_vl),
-                    min(max(cn[HYQ_CNT_NTAIL], 0), cap_tail)};
+  return NextCounts{cn[HYQ_CNT_NQ], cn[HYQ_CNT_NVL], cn[HYQ_CNT_NTAIL]};
+}
+__device__ __forceinline__ NextCounts clamp_next_counts(const NextCounts& n, int nblk_cap, int cap_vl,
+                                                        int cap_tail) {
+  return NextCounts{min(max(n.nq, 0), nblk_cap * HYQ_QBLOCK_ROWS), min(max(n.nvl, 0), cap_vl),
+                    min(max(n.ntail, 0), cap_tail)};
 }
 
-// One warp, once it has read its own tiles of this layer: prefetch into
-// L2 the next layout's quantised tiles [t0, t1) of KV head bh, the share of
+// One warp: prefetch into L2 the next layout's quantised tiles [t0, t1) of KV head bh, the share of
 // block `split` under the same partition (contiguous, 64 KB per lane).
 template <int kTileBytes>
 __device__ void prefetch_next_tiles(const StepArgs& sa, const NextCounts& n, size_t bh, int split, int S,
@@ -222,16 +225,18 @@ __device__ __forceinline__ void step_ticket_finish(int old, const StepArgs& sa, 
   sa.tickets_b[b] = 0;
 }
 
+// Online-softmax state of one warp for the two heads (2t, 2t+1) a thread owns.
+// Logits live in a scaled base-2 domain, lambda' = 2^sigma log2(e) q.k / sqrt(d)
+// with one sigma per query head (QConst), chosen so that the per-group query
+// sums fit the fp16 operand of the zero-point product; p = 2^((lambda' - m) 2^-sigma).
 struct State {
-  float m[2], l[2];
-  float acc[8][4];   // PV accumulators in units of 2^-24
-  float zacc[2][4];  // sum_j p_j z_jq per head (2t, 2t+1) and group q
+  float m[2];       // running maximum (scaled domain)
+  float nm[2];      // -m 2^-sigma (0 while m = -inf)
+  float l[2];       // running sum of this thread's probabilities
+  float acc[8][4];  // PV accumulators in units of 2^-24
+  float zd[4];      // sum_j p_j z_jq: rows g < 4 = group g, columns heads 2t, 2t+1
 };
 
-// Online-softmax update of the two heads (2t, 2t+1) this thread owns with the
-// logits of tokens (g, g+8); returns the probabilities p[2r + j].  The
-// accumulators are rescaled only when some head's running max moved (the
-// factor is exactly 1 otherwise).
 // 2^x on the special-function unit, one instruction (relative error about
 // 2^-22; 2^-inf = 0, results below 2^-126 flush to 0).
 __device__ __forceinline__ float ex2(float x) {
@@ -240,14 +245,18 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Online-softmax update of the two heads (2t, 2t+1) this thread owns with the
+// logits of tokens (g, g+8); returns the probabilities p[2r + j].  The
+// accumulators are rescaled only when some head's running max moved (the
+// factor is exactly 1 otherwise).
 // kLazy: first test (one warp vote) whether any logit of the tile exceeds its
 // head's running maximum; if none does, the maximum stays, the correction is
 // 1 and no cross-lane maximum is needed (the full path would give the same
 // bits).  It pays off on long per-warp runs of tiles (one block per
-// sequence and KV head), not on short ones, where early tiles move the
-// maximum.
+// sequence and KV head), not on short ones, where early tiles move the maximum.
 template <bool kLazy>
-__device__ __forceinline__ void softmax_update(const float (&lg)[4], State& st, float (&p)[4]) {
+__device__ __forceinline__ void softmax_update(const float (&lg)[4], State& st, float (&p)[4],
+                                               const float (&inv)[2]) {
   if (kLazy) {
     bool above = false;
 #pragma unroll
@@ -255,9 +264,8 @@ __device__ __forceinline__ void softmax_update(const float (&lg)[4], State& st, 
     if (!__any_sync(0xffffffffu, above)) {
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        const float ms = st.m[j] == -INFINITY ? 0.f : st.m[j];
-        p[j] = ex2(lg[j] - ms);
-        p[2 + j] = ex2(lg[2 + j] - ms);
+        p[j] = ex2(fmaf(lg[j], inv[j], st.nm[j]));
+        p[2 + j] = ex2(fmaf(lg[2 + j], inv[j], st.nm[j]));
         st.l[j] += p[j] + p[2 + j];
       }
       return;
@@ -272,13 +280,14 @@ __device__ __forceinline__ void softmax_update(const float (&lg)[4], State& st, 
     tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 8));
     tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 16));
     const float mn = fmaxf(st.m[j], tm);
-    const float ms = (mn == -INFINITY) ? 0.f : mn;
+    const float nm = (mn == -INFINITY) ? 0.f : -mn * inv[j];
     moved |= mn != st.m[j];
-    corr[j] = ex2(st.m[j] - ms);
-    p[j] = ex2(lg[j] - ms);
-    p[2 + j] = ex2(lg[2 + j] - ms);
+    corr[j] = ex2(fmaf(st.m[j], inv[j], nm));
+    p[j] = ex2(fmaf(lg[j], inv[j], nm));
+    p[2 + j] = ex2(fmaf(lg[2 + j], inv[j], nm));
     st.l[j] = fmaf(st.l[j], corr[j], p[j] + p[2 + j]);
     st.m[j] = mn;
+    st.nm[j] = nm;
   }
   if (__any_sync(0xffffffffu, moved)) {
 #pragma unroll
@@ -288,20 +297,40 @@ __device__ __forceinline__ void softmax_update(const float (&lg)[4], State& st, 
         st.acc[mt][j] *= corr[j];
         st.acc[mt][2 + j] *= corr[j];
       }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) st.zacc[j][q] *= corr[j];
+      st.zd[j] *= corr[j];
     }
   }
 }
 
-// Per-block constants of the 4-bit path.
+// Binary exponent e of a finite x > 0 with x = f 2^e, f in [0.5, 1)
+// (subnormals included), 2^k for k in [-126, 127], and the clamp to that range.
+__device__ __forceinline__ int exp_of(float x) {
+  const int b = __float_as_int(x) >> 23;
+  return b != 0 ? b - 126 : (__float_as_int(x * 16777216.f) >> 23) - 150;
+}
+__device__ __forceinline__ int clamp_exp(int k) { return min(max(k, -126), 127); }
+__device__ __forceinline__ float pow2i(int k) { return __int_as_float((clamp_exp(k) + 127) << 23); }
+__device__ __forceinline__ bool pos_finite(float x) { return x > 0.f && x <= 3.402823466e38f; }
+
+// Per-block constants of the quantised path.
 struct QConst {
-  float ksc[2];   // logit factor of the code products for tokens g (x1) and g+8 (x16 codes)
-  float qs[2][4]; // per-group query sums of heads 2t, 2t+1, times log2(e)/sqrt(d)
+  float ksc[2][2];  // scaled-domain factor of the code products [token g (x1) | g+8 (x16 codes)][head 2t + j]
+  float inv[2];     // 2^-sigma of heads 2t, 2t+1
+  float kss[2];     // scaled-domain factor of the BF16 products 2^sigma log2(e) / sqrt(d), heads 2t, 2t+1
+  // B fragment of the zero-point product for head g: the scaled query sums
+  // 2^sigma log2(e)/sqrt(d) sum(q over group) of groups 2(t&1), 2(t&1)+1 as
+  // an fp16 pair, their high parts for t < 2 and the remainders for t >= 2
+  // (hi + lo carries 22 bits).
+  uint32_t bz;
 };
 
 // The two codes of bytes 1 and 3 of w as the low bytes of two 16-bit halves.
 __device__ __forceinline__ uint32_t odd_bytes(uint32_t w) { return __byte_perm(w, 0u, 0x4341); }
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
 
 // `n` 32-bit words of a code region: word u of this lane at
 // 512 (u / 4) + 16 lane + 4 (u % 4).
@@ -317,6 +346,10 @@ __device__ __forceinline__ void load_words(const uint8_t* region, int lane, uint
   }
 }
 
+__device__ __forceinline__ uint32_t u4c(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
 // One 16-row quantised tile at `tb` (byte layout QFmt<BK, BV>), `vr` valid
 // rows.  The codes enter the fp16 MMAs as subnormals c * 2^-24.  4-bit: the
 // low nibble of a byte as c * 2^-24, the high nibble, masked in place, as
@@ -326,11 +359,15 @@ __device__ __forceinline__ void load_words(const uint8_t* region, int lane, uint
 // 8-bit: bytes 0 and 2 of a word by one AND, bytes 1 and 3 by one byte
 // permute, each a fragment register of two codes.  bq holds the query as
 // fp16, scaled by 2^e.
+//   logit = sum_q s_q (q.c)_q  (per-group code products scaled in fp32)
+//         + sum_q z_q (sum q)_q (one MMA: the zero pairs against qc.bz)
+//   out  += sum_j (p_j s_jq) c_jd  (P^T scaled by the V scale pairs in fp16)
+//         + sum_j p_j z_jq          (one MMA: the V zero pairs against P^T)
 template <int BK, int BV, bool kLazy>
 __device__ __forceinline__ void q_tile(const uint8_t* tb, int lane, int vr, const uint32_t (&bq)[8][2],
                                        const QConst& qc, State& st) {
   using F = QFmt<BK, BV>;
-  const int g = lane >> 2;
+  const int g = lane >> 2, t = lane & 3;
   float C[4][4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) C[q][0] = C[q][1] = C[q][2] = C[q][3] = 0.f;
@@ -352,47 +389,48 @@ __device__ __forceinline__ void q_tile(const uint8_t* tb, int lane, int vr, cons
       mma_f16(C[ks >> 1], w0 & 0x00FF00FFu, w1 & 0x00FF00FFu, odd_bytes(w0), odd_bytes(w1), bq[ks][0], bq[ks][1]);
     }
   }
-  const uint8_t* km = tb + F::kKMeta;
+  // K metadata of tokens g and g+8: four scales, then four zeros.
+  const uint4 ma = *reinterpret_cast<const uint4*>(tb + F::kKMeta + 16 * g);
+  const uint4 mb = *reinterpret_cast<const uint4*>(tb + F::kKMeta + 16 * (g + 8));
+  const float2 a01 = half2_to_float2(ma.x), a23 = half2_to_float2(ma.y);
+  const float2 b01 = half2_to_float2(mb.x), b23 = half2_to_float2(mb.y);
   float lg[4];
 #pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const uint4 mk = *reinterpret_cast<const uint4*>(km + (g + 8 * r) * 16);
-    const uint32_t mw[4] = {mk.x, mk.y, mk.z, mk.w};
-    float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float2 sz = half2_to_float2(mw[q]);
-      a0 = fmaf(sz.x, C[q][2 * r], a0);
-      a1 = fmaf(sz.x, C[q][2 * r + 1], a1);
-      b0 = fmaf(sz.y, qc.qs[0][q], b0);
-      b1 = fmaf(sz.y, qc.qs[1][q], b1);
-    }
-    const bool valid = g + 8 * r < vr;
-    lg[2 * r] = valid ? fmaf(a0, qc.ksc[r], b0) : -INFINITY;
-    lg[2 * r + 1] = valid ? fmaf(a1, qc.ksc[r], b1) : -INFINITY;
+  for (int c = 0; c < 2; ++c) {
+    lg[c] = qc.ksc[0][c] * fmaf(a01.x, C[0][c], fmaf(a01.y, C[1][c], fmaf(a23.x, C[2][c], a23.y * C[3][c])));
+    lg[2 + c] = qc.ksc[1][c] *
+                fmaf(b01.x, C[0][2 + c], fmaf(b01.y, C[1][2 + c], fmaf(b23.x, C[2][2 + c], b23.y * C[3][2 + c])));
+  }
+  // + sum_q z_q (scaled query sum)_q: the A fragment's k slots 2t, 2t+1 are
+  // groups 2(t&1), 2(t&1)+1 (high parts of the sums for t < 2, remainders
+  // for t >= 2), so a lane passes the zero pair of those groups.
+  mma_f16(lg, (t & 1) ? ma.w : ma.z, (t & 1) ? mb.w : mb.z, 0u, 0u, qc.bz, 0u);
+  if (vr < 16) {
+    if (g >= vr) lg[0] = lg[1] = -INFINITY;
+    if (g + 8 >= vr) lg[2] = lg[3] = -INFINITY;
   }
   float p[4];
-  softmax_update<kLazy>(lg, st, p);
+  softmax_update<kLazy>(lg, st, p, qc.inv);
+  // P^T fragments in fp16: tokens (2t, 2t+1) and (2t+8, 2t+9) of head g.
+  const uint32_t pt0 = movmatrix_trans(pack_f16x2(p[0], p[1]));
+  const uint32_t pt1 = movmatrix_trans(pack_f16x2(p[2], p[3]));
+  const uint8_t* vm = tb + F::kVMeta;
+  // V scale pairs of tokens (2t, 2t+1) and (2t+8, 2t+9), groups 0..3.
+  const uint4 sv0 = *reinterpret_cast<const uint4*>(vm + 16 * t);
+  const uint4 sv1 = *reinterpret_cast<const uint4*>(vm + 16 * (t + 4));
+  // sum_j p_j z_jq on the tensor core: A rows = groups (g < 4), k = tokens.
+  uint32_t z0 = 0u, z1 = 0u;
+  if (g < 4) {
+    z0 = *reinterpret_cast<const uint32_t*>(vm + 128 + 16 * t + 4 * g);
+    z1 = *reinterpret_cast<const uint32_t*>(vm + 128 + 16 * (t + 4) + 4 * g);
+  }
+  mma_f16(st.zd, z0, 0u, z1, 0u, pt0, pt1);
   uint32_t vw[BV == 4 ? 8 : 16];
   load_words<BV == 4 ? 8 : 16>(tb + F::kVCode, lane, vw);
-  const uint8_t* vm = tb + F::kVMeta;
-  const uint4 mv0 = *reinterpret_cast<const uint4*>(vm + g * 16);
-  const uint4 mv1 = *reinterpret_cast<const uint4*>(vm + (g + 8) * 16);
-  const uint32_t m0[4] = {mv0.x, mv0.y, mv0.z, mv0.w};
-  const uint32_t m1[4] = {mv1.x, mv1.y, mv1.z, mv1.w};
-  const __half2 p0 = __floats2half2_rn(p[0], p[1]), p1 = __floats2half2_rn(p[2], p[3]);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    // B operand (tokens x heads) of group q: p * s in packed fp16, transposed into place.
-    const uint32_t s0 = __byte_perm(m0[q], 0, 0x1010), s1 = __byte_perm(m1[q], 0, 0x1010);
-    const __half2 x0 = __hmul2(p0, *reinterpret_cast<const __half2*>(&s0));
-    const __half2 x1 = __hmul2(p1, *reinterpret_cast<const __half2*>(&s1));
-    const uint32_t b0 = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&x0));
-    const uint32_t b1 = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&x1));
-    const float z0 = __high2float(*reinterpret_cast<const __half2*>(&m0[q]));
-    const float z1 = __high2float(*reinterpret_cast<const __half2*>(&m1[q]));
-    st.zacc[0][q] = fmaf(p[0], z0, fmaf(p[2], z1, st.zacc[0][q]));
-    st.zacc[1][q] = fmaf(p[1], z0, fmaf(p[3], z1, st.zacc[1][q]));
+    // B operand (tokens x heads) of group q: p * s in packed fp16.
+    const uint32_t b0 = hmul2_u32(pt0, u4c(sv0, q)), b1 = hmul2_u32(pt1, u4c(sv1, q));
 #pragma unroll
     for (int mm = 0; mm < 2; ++mm) {  // m-tile 2q + mm lies in group q
       if (BV == 4) {
@@ -416,9 +454,6 @@ __device__ __forceinline__ uint32_t row_factor_bf16x2(uint32_t x) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__device__ __forceinline__ uint32_t u4c(const uint4& v, int i) {
-  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
-}
 
 // One 16-row tile of BF16 rows (rows row0.. of the vertical-line rows followed
 // by the tail), `vr` valid rows, loaded directly into fragment registers; row
@@ -428,7 +463,8 @@ template <int BV, bool kLazy>
 __device__ __forceinline__ void f_tile(const __nv_bfloat16* vlk, const __nv_bfloat16* vlv,
                                        const __nv_bfloat16* tk, const __nv_bfloat16* tv, int nvl,
                                        int rnew, const __nv_bfloat16* knew, const __nv_bfloat16* vnew,
-                                       int row0, int vr, int lane, const __nv_bfloat16* q_s, State& st) {
+                                       int row0, int vr, int lane, const __nv_bfloat16* q_s, const QConst& qc,
+                                       State& st) {
   const int g = lane >> 2, t = lane & 3;
 
   float S[4] = {0.f, 0.f, 0.f, 0.f};
@@ -454,12 +490,12 @@ __device__ __forceinline__ void f_tile(const __nv_bfloat16* vlk, const __nv_bflo
     }
   }
   float lg[4];
-  lg[0] = g < vr ? S[0] * kScale : -INFINITY;
-  lg[1] = g < vr ? S[1] * kScale : -INFINITY;
-  lg[2] = g + 8 < vr ? S[2] * kScale : -INFINITY;
-  lg[3] = g + 8 < vr ? S[3] * kScale : -INFINITY;
+  lg[0] = g < vr ? S[0] * qc.kss[0] : -INFINITY;
+  lg[1] = g < vr ? S[1] * qc.kss[1] : -INFINITY;
+  lg[2] = g + 8 < vr ? S[2] * qc.kss[0] : -INFINITY;
+  lg[3] = g + 8 < vr ? S[3] * qc.kss[1] : -INFINITY;
   float p[4];
-  softmax_update<kLazy>(lg, st, p);
+  softmax_update<kLazy>(lg, st, p, qc.inv);
   // P^T (tokens x heads), scaled by 2^-24 like the 4-bit accumulators.
   const uint32_t b0 = movmatrix_trans(pack_bf16x2(p[0] * kSubScale, p[1] * kSubScale));
   const uint32_t b1 = movmatrix_trans(pack_bf16x2(p[2] * kSubScale, p[3] * kSubScale));
@@ -491,7 +527,7 @@ __device__ __forceinline__ void f_tile(const __nv_bfloat16* vlk, const __nv_bflo
 // loads, against 32 single-row copies per tile otherwise.
 template <int BV, bool kLazy>
 __device__ __forceinline__ void f_tile_smem(const uint8_t* Ks, const uint8_t* Vs, int vr, int lane,
-                                            const __nv_bfloat16* q_s, State& st) {
+                                            const __nv_bfloat16* q_s, const QConst& qc, State& st) {
   const int g = lane >> 2, t = lane & 3;
 
   float S[4] = {0.f, 0.f, 0.f, 0.f};
@@ -512,12 +548,12 @@ __device__ __forceinline__ void f_tile_smem(const uint8_t* Ks, const uint8_t* Vs
     }
   }
   float lg[4];
-  lg[0] = g < vr ? S[0] * kScale : -INFINITY;
-  lg[1] = g < vr ? S[1] * kScale : -INFINITY;
-  lg[2] = g + 8 < vr ? S[2] * kScale : -INFINITY;
-  lg[3] = g + 8 < vr ? S[3] * kScale : -INFINITY;
+  lg[0] = g < vr ? S[0] * qc.kss[0] : -INFINITY;
+  lg[1] = g < vr ? S[1] * qc.kss[1] : -INFINITY;
+  lg[2] = g + 8 < vr ? S[2] * qc.kss[0] : -INFINITY;
+  lg[3] = g + 8 < vr ? S[3] * qc.kss[1] : -INFINITY;
   float p[4];
-  softmax_update<kLazy>(lg, st, p);
+  softmax_update<kLazy>(lg, st, p, qc.inv);
   const uint32_t b0 = movmatrix_trans(pack_bf16x2(p[0] * kSubScale, p[1] * kSubScale));
   const uint32_t b1 = movmatrix_trans(pack_bf16x2(p[2] * kSubScale, p[3] * kSubScale));
   uint2 va[4][4];
@@ -547,12 +583,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
     int cap_vl, int cap_tail, int S, const StepArgs sa) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(16) __nv_bfloat16 q_s[HYQ_MAX_GQA * HYQ_D];
-  __shared__ float qsum_s[HYQ_MAX_GQA * 4];
+  __shared__ __align__(16) uint32_t bq_s[HYQ_MAX_GQA][4][16];  // per query row and lane t: the B fragments
+  __shared__ float rowc_s[HYQ_MAX_GQA][4];                       // per query row: ksc (x1, x16), 2^-sigma, kss
+  __shared__ uint32_t bz_s[HYQ_MAX_GQA][4];                      // per query row and lane t: zero-point B fragment
   __shared__ __align__(8) uint64_t bars[kWarps * kMaxSlots];
   __shared__ __align__(8) uint64_t fbars[kFStaged];
   __shared__ __align__(8) uint64_t qbar;
-  __shared__ float red_m[kWarps][HYQ_MAX_GQA], red_l[kWarps][HYQ_MAX_GQA], wts[kWarps][HYQ_MAX_GQA];
-  __shared__ float sM[HYQ_MAX_GQA], sL[HYQ_MAX_GQA];
+  __shared__ float red_m[kWarps][HYQ_MAX_GQA], red_l[kWarps][HYQ_MAX_GQA];
+  __shared__ float sL[HYQ_MAX_GQA];
   __shared__ int s_flag;
 
   using D = Dec<BK, BV>;
@@ -582,6 +620,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
     qv = __ldg(reinterpret_cast<const uint4*>(q + ((size_t)b * HQ + (size_t)h * gq) * HYQ_D) + tid);
   const int32_t* cnt = lay.counts + (size_t)b * HYQ_COUNTS;
   int32_t nq = cnt[HYQ_CNT_NQ], nvl = cnt[HYQ_CNT_NVL], ntail = cnt[HYQ_CNT_NTAIL];
+  const bool next_cnt_loaded = sa.nx_counts != nullptr;
+  NextCounts nxraw{0, 0, 0};
+  if (next_cnt_loaded && warp == kWarps - 1) nxraw = load_next_counts(sa, b);
   if (nq < 0 || nq > nblk_cap * HYQ_QBLOCK_ROWS || nvl < 0 || nvl > cap_vl || ntail < 0 || ntail > cap_tail) {
     if (tid == 0 && split == 0) hyq_set_err(lay.err, HYQ_DEVERR_COUNT);
     nq = min(max(nq, 0), nblk_cap * HYQ_QBLOCK_ROWS);
@@ -690,63 +731,98 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
       reinterpret_cast<uint4*>(smem + D::kRingBytes + fw * kFTileBytes + (lane >= 16 ? 16 * kFKStride : 0) +
                                rin * kFKStride)[lane & 15] = nrow;
   }
-  if (tid < 256) {  // 8 threads per (query row, group of 32 elements)
-    const int e = tid >> 3;
-    const uint2 v = *reinterpret_cast<const uint2*>(q_s + (e >> 2) * HYQ_D + 32 * (e & 3) + 4 * (tid & 7));
-    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
-    const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
-    float sacc = (a.x + a.y) + (c.x + c.y);
+  // One warp per query row (rows past g stay zero): the row's fp16 B
+  // fragments, scaled by an exact power of two 2^qe so that max |q| lies in
+  // [2^13, 2^14), stored in the order lane (g, t) reads them; and the row's
+  // constants: sigma (its largest scaled group sum 2^sigma log2(e)/sqrt(d)
+  // |sum q| below 2^13, and sigma <= 23 - exponent(max |q|), which bounds the
+  // scaled logits), the code-product factors and the zero-point fragments.
+  if (warp < HYQ_MAX_GQA) {
+    const int r = warp;
+    float x[4] = {0.f, 0.f, 0.f, 0.f};
+    if (r < gq) {
+      const uint2 v = *reinterpret_cast<const uint2*>(q_s + r * HYQ_D + 4 * lane);
+      const float2 x01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+      const float2 x23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+      x[0] = x01.x, x[1] = x01.y, x[2] = x23.x, x[3] = x23.y;
+    }
+    float gs = (x[0] + x[1]) + (x[2] + x[3]);  // group lane / 8
 #pragma unroll
-    for (int o = 1; o < 8; o <<= 1) sacc += __shfl_xor_sync(0xffffffffu, sacc, o);
-    if ((tid & 7) == 0) qsum_s[e] = sacc;
-  }
-  __syncthreads();
-  // The query in fp16 for the 4-bit path, scaled by 2^e (exact) so that its
-  // largest element is below 2^14; e = 14 - (binary exponent of max |q|).
-  float amax = 0.f;
-  for (int i = lane; i < gq * HYQ_D / 8; i += 32) {
-    const uint4 v = reinterpret_cast<const uint4*>(q_s)[i];
-    const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+    for (int o = 1; o < 8; o <<= 1) gs += __shfl_xor_sync(0xffffffffu, gs, o);
+    float am = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+    float gm = fabsf(gs * kScale);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float2 f = __bfloat1622float2(p2[k]);
-      amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+    for (int o = 1; o < 32; o <<= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+#pragma unroll
+    for (int o = 8; o < 32; o <<= 1) gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, o));
+    const int qe = pos_finite(am) ? clamp_exp(14 - exp_of(am)) : 14;
+    const float gmb = fmaxf(gm, am * 0.0009765625f);  // 2^-10 max |q|
+    const int sg = pos_finite(gmb) ? clamp_exp(13 - exp_of(gmb)) : 13;
+    const float qscale = pow2i(qe);
+#pragma unroll
+    for (int hp = 0; hp < 2; ++hp) {
+      const int e = 4 * lane + 2 * hp;  // pair (e, e + 1) -> lane t, k-step ks, half hh
+      const int hh = (e >> 1) & 1;
+      const int tt = BK == 4 ? (e >> 3) & 3 : (e >> 2) & 3;
+      const int ks = BK == 4 ? 2 * (e >> 5) + ((e >> 2) & 1) : e >> 4;
+      bq_s[r][tt][2 * ks + hh] = pack_f16x2(x[2 * hp] * qscale, x[2 * hp + 1] * qscale);
+    }
+    const float kss = kScale * pow2i(sg);
+    const float s0 = __shfl_sync(0xffffffffu, gs, 0) * kss, s1 = __shfl_sync(0xffffffffu, gs, 8) * kss;
+    const float s2 = __shfl_sync(0xffffffffu, gs, 16) * kss, s3 = __shfl_sync(0xffffffffu, gs, 24) * kss;
+    if (lane < 4) {  // lane = t of the reading thread
+      const float y0 = (lane & 1) ? s2 : s0, y1 = (lane & 1) ? s3 : s1;
+      const float h0 = __half2float(__float2half_rn(y0)), h1 = __half2float(__float2half_rn(y1));
+      bz_s[r][lane] = lane < 2 ? pack_f16x2(h0, h1) : pack_f16x2(y0 - h0, y1 - h1);
+    }
+    if (lane == 0) {
+      const float k0 = kScale * pow2i(clamp_exp(24 - qe)) * pow2i(sg);
+      rowc_s[r][0] = k0;
+      rowc_s[r][1] = BK == 4 ? k0 * 0.0625f : k0;  // 4-bit tokens g+8 carry 16 c
+      rowc_s[r][2] = pow2i(-sg);
+      rowc_s[r][3] = kss;
     }
   }
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  int ex = 0;
-  if (amax > 0.f && isfinite(amax)) (void)frexpf(amax, &ex);
-  const int qe = 14 - ex;
-  const float qscale = ldexpf(1.f, qe);
+  __syncthreads();
   // B fragments of q in the permuted k order of the key codes: kstep ks
   // covers elements e + {0,1} and e + {2,3}, e = 8(t + 4(ks/2)) + 4(ks%2)
   // for 4-bit keys, e = 16 ks + 4t for 8-bit keys.
   uint32_t bq[8][2];
 #pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    const int e = BK == 4 ? 8 * (t + 4 * (ks >> 1)) + 4 * (ks & 1) : 16 * ks + 4 * t;
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(q_s + g * HYQ_D + e + 2 * hh));
-      bq[ks][hh] = pack_f16x2(f.x * qscale, f.y * qscale);
-    }
+  for (int i = 0; i < 4; ++i) {
+    const uint4 v = *reinterpret_cast<const uint4*>(&bq_s[g][t][4 * i]);
+    bq[2 * i][0] = v.x, bq[2 * i][1] = v.y, bq[2 * i + 1][0] = v.z, bq[2 * i + 1][1] = v.w;
   }
   QConst qc;
-  qc.ksc[0] = ldexpf(kScale, 24 - qe);
-  qc.ksc[1] = ldexpf(kScale, (BK == 4 ? 20 : 24) - qe);  // 4-bit tokens g+8 carry 16 c
 #pragma unroll
-  for (int j = 0; j < 2; ++j)
-#pragma unroll
-    for (int qq = 0; qq < 4; ++qq) qc.qs[j][qq] = qsum_s[(2 * t + j) * 4 + qq] * kScale;
+  for (int j = 0; j < 2; ++j) {
+    qc.ksc[0][j] = rowc_s[2 * t + j][0];
+    qc.ksc[1][j] = rowc_s[2 * t + j][1];
+    qc.inv[j] = rowc_s[2 * t + j][2];
+    qc.kss[j] = rowc_s[2 * t + j][3];
+  }
+  qc.bz = bz_s[g][t];
 
   State st;
   st.m[0] = st.m[1] = -INFINITY;
+  st.nm[0] = st.nm[1] = 0.f;
   st.l[0] = st.l[1] = 0.f;
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) st.acc[mt][0] = st.acc[mt][1] = st.acc[mt][2] = st.acc[mt][3] = 0.f;
-#pragma unroll
-  for (int j = 0; j < 2; ++j) st.zacc[j][0] = st.zacc[j][1] = st.zacc[j][2] = st.zacc[j][3] = 0.f;
+  st.zd[0] = st.zd[1] = st.zd[2] = st.zd[3] = 0.f;
+
+  // Next-layer L2 prefetch (hyq_decode_step_prefetch): issued by the last
+  // warp once its own tiles are read (the next layout's counters, loaded at
+  // entry, have long arrived), so that it keeps HBM busy through this
+  // launch's reductions and merge.  Issued at the warp's first tile instead,
+  // it slowed the call (18.96 against 15.95 us at the 32K layer): the
+  // prefetch then competes with this layer's own reads.
+  const bool pf_warp = next_cnt_loaded && warp == kWarps - 1;
+  auto issue_prefetch = [&]() {
+    const NextCounts nxc = clamp_next_counts(nxraw, nblk_cap, cap_vl, cap_tail);
+    prefetch_next_tiles<kTile>(sa, nxc, bh, split, S, nblk_cap, lane);
+    prefetch_next_rows(sa, nxc, bh, split, S, cap_vl, cap_tail, lane);
+  };
 
   // ---- 4-bit tiles through the warp's ring ---------------------------------
   for (int j = 0; j < nj; ++j) {
@@ -784,31 +860,30 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
       __syncwarp();
     } else {
       f_tile_smem<BV, kMode == kDirect>(fstage, fstage + 16 * kFKStride, min(16, nf - 16 * (f0 + warp)), lane, q_s,
-                                        st);
+                                        qc, st);
     }
   }
   for (int fi = f0 + kFStaged + warp; fi < f1; fi += kWarps)  // tiles past the staged ones
-    f_tile<BV, kMode == kDirect>(vlk, vlv, tk, tv, nvl, app ? nvl + ntail : -1, sa.k_new + bh * HYQ_D, sa.v_new + bh * HYQ_D, 16 * fi,
-           min(16, nf - 16 * fi), lane, q_s, st);
+    f_tile<BV, kMode == kDirect>(vlk, vlv, tk, tv, nvl, app ? nvl + ntail : -1, sa.k_new + bh * HYQ_D,
+                                 sa.v_new + bh * HYQ_D, 16 * fi, min(16, nf - 16 * fi), lane, q_s, qc, st);
 
-  // ---- warp partials -> block partial (m, l, acc) in shared memory ---------
-  if (sa.nx_counts && warp == kWarps - 1) {  // as soon as this warp's own reads are done
-    const NextCounts nxc = next_counts(sa, b, nblk_cap, cap_vl, cap_tail);
-    prefetch_next_tiles<kTile>(sa, nxc, bh, split, S, nblk_cap, lane);
-    prefetch_next_rows(sa, nxc, bh, split, S, cap_vl, cap_tail, lane);
-  }
+  if (pf_warp) issue_prefetch();
+  // ---- warp partial -> this warp's own ring (every copy into it has been
+  // consumed): acc[head][128] with the zero-point terms, (m, l) per head -----
 #pragma unroll
-  for (int j = 0; j < 2; ++j) {
+  for (int j = 0; j < 2; ++j)
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) st.l[j] += __shfl_xor_sync(0xffffffffu, st.l[j], o);
+  // sum_j p_j z_jq of heads 2t, 2t+1 sits in lane (q, t): gather all four groups.
+  float zt[4][2];
 #pragma unroll
-    for (int qq = 0; qq < 4; ++qq)
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1) st.zacc[j][qq] += __shfl_xor_sync(0xffffffffu, st.zacc[j][qq], o);
+  for (int q = 0; q < 4; ++q) {
+    zt[q][0] = __shfl_sync(0xffffffffu, st.zd[0], 4 * q + t);
+    zt[q][1] = __shfl_sync(0xffffffffu, st.zd[1], 4 * q + t);
   }
-  __syncthreads();  // every warp is done with its ring: reuse shared memory
-  float* red = reinterpret_cast<float*>(smem);                    // [warp][head][128]
-  float* blk = red + kWarps * HYQ_MAX_GQA * HYQ_D;                  // [head][2 + 128]
+  // [8 heads][128] = 4 KB <= the ring; element d of head hd at hd*128 + (d ^ (hd/2)),
+  // so that the 32 lanes' stores of one accumulator fall in 32 banks.
+  float* wpart = reinterpret_cast<float*>(ring);
   // Accumulator (m-tile u, ci) of thread (g, t): element 32(u/2) + 4g +
   // 2(u%2) + (ci >> 1), head 2t + (ci & 1); with 4-bit values the rows
   // ci >= 2 carry 16 c.
@@ -818,50 +893,44 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
     for (int ci = 0; ci < 4; ++ci) {
       const int d = 32 * (u >> 1) + 4 * g + 2 * (u & 1) + (ci >> 1), hd = 2 * t + (ci & 1);
       const float f = (BV == 4 && ci >= 2) ? HYQ_F16_SUB_SCALE / 16.f : HYQ_F16_SUB_SCALE;
-      red[(warp * HYQ_MAX_GQA + hd) * HYQ_D + d] = fmaf(st.acc[u][ci], f, st.zacc[ci & 1][u >> 1]);
+      wpart[hd * HYQ_D + (d ^ t)] = fmaf(st.acc[u][ci], f, zt[u >> 1][ci & 1]);
     }
   if (g == 0)
+#pragma unroll
     for (int j = 0; j < 2; ++j) {
-      red_m[warp][2 * t + j] = st.m[j];
+      red_m[warp][2 * t + j] = st.m[j] == -INFINITY ? -INFINITY : st.m[j] * qc.inv[j];  // back to log2 units
       red_l[warp][2 * t + j] = st.l[j];
     }
   __syncthreads();
-  if (warp < gq) {  // warp = head, lane = warp of the block
-    const int hd = warp;
+  // ---- block partial: thread i takes elements i, i + 512 (a warp shares one
+  // head); the warps' weights 2^(m_w - M) come from lanes 0..15 by shuffle --
+  float* blk = reinterpret_cast<float*>(smem + D::kRingBytes);  // [head][2 + 128] (staged area, consumed)
+  float* pp = part + (bh * S + split) * (size_t)(HYQ_MAX_GQA * kPart);
+  for (int i = tid; i < gq * HYQ_D; i += kThreads) {
+    const int hd = i >> 7, d = i & (HYQ_D - 1);
     const float mw = lane < kWarps ? red_m[lane][hd] : -INFINITY;
     float M = mw;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     const float Ms = (M == -INFINITY) ? 0.f : M;
     const float wt = lane < kWarps ? ex2(mw - Ms) : 0.f;
-    if (lane < kWarps) wts[lane][hd] = wt;
     float Lsum = lane < kWarps ? red_l[lane][hd] * wt : 0.f;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, o);
-    if (lane == 0) {
-      blk[hd * kPart + 0] = M;
-      blk[hd * kPart + 1] = Lsum;
-    }
-  }
-  __syncthreads();
-  // kGlobal writes the block partial straight to its workspace slot.
-  float* pp = part + (bh * S + split) * (size_t)(HYQ_MAX_GQA * kPart);
-  if (kMode == kGlobal && tid < gq) {
-    pp[tid * kPart + 0] = blk[tid * kPart + 0];
-    pp[tid * kPart + 1] = blk[tid * kPart + 1];
-  }
-  for (int i = tid; i < gq * HYQ_D; i += kThreads) {
-    const int hd = i >> 7, d = i & (HYQ_D - 1);
     float a = 0.f;
-#pragma unroll 4
-    for (int w = 0; w < kWarps; ++w) a = fmaf(red[(w * HYQ_MAX_GQA + hd) * HYQ_D + d], wts[w][hd], a);
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w)
+      a = fmaf(__shfl_sync(0xffffffffu, wt, w),
+               reinterpret_cast<const float*>(smem + w * kSlots * kTile)[hd * HYQ_D + (d ^ (hd >> 1))], a);
     if (kMode == kDirect) {
-      const float Lh = blk[hd * kPart + 1];
-      out[((size_t)b * HQ + (size_t)h * gq + hd) * HYQ_D + d] = __float2bfloat16_rn(Lh > 0.f ? a / Lh : 0.f);
-    } else if (kMode == kCluster) {
-      blk[hd * kPart + 2 + d] = a;
+      out[((size_t)b * HQ + (size_t)h * gq + hd) * HYQ_D + d] = __float2bfloat16_rn(Lsum > 0.f ? a / Lsum : 0.f);
     } else {
-      pp[hd * kPart + 2 + d] = a;
+      float* dst = kMode == kCluster ? blk : pp;
+      dst[hd * kPart + 2 + d] = a;
+      if (d == 0) {
+        dst[hd * kPart + 0] = M;
+        dst[hd * kPart + 1] = Lsum;
+      }
     }
   }
   if (owner) {
@@ -887,8 +956,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
     // ---- ReduceSoftmax across the cluster through distributed shared memory
     cg::cluster_group cluster = cg::this_cluster();
     cluster.sync();  // every block's partial is in its shared memory
-    float* rm = red;                         // [S][8] remote m, then weights
-    float* rl = red + 16 * HYQ_MAX_GQA;      // [S][8] remote l
+    float* rm = reinterpret_cast<float*>(smem);  // [S][8] remote m, then weights (rings are free now)
+    float* rl = rm + 16 * HYQ_MAX_GQA;          // [S][8] remote l
     for (int i = tid; i < S * gq; i += kThreads) {
       const int r = i / gq, hd = i % gq;
       const float* rb = cluster.map_shared_rank(blk, r);
@@ -941,64 +1010,40 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
   if (!s_flag) return;
   const int tk_old = ticket_thread ? step_ticket_issue(sa, b) : 0;  // overlaps the merge
   const float* pb = part + bh * S * (size_t)(HYQ_MAX_GQA * kPart);
-  float* sm_m = red;                             // [S][8]
-  float* sm_w = red + kMaxSplits * HYQ_MAX_GQA;  // [S][8]
-  for (int i = tid; i < S * gq; i += kThreads) {
-    const int s2 = i / gq, hd = i % gq;
-    sm_m[s2 * HYQ_MAX_GQA + hd] = __ldcg(pb + (size_t)s2 * HYQ_MAX_GQA * kPart + hd * kPart);
-    sm_w[s2 * HYQ_MAX_GQA + hd] = __ldcg(pb + (size_t)s2 * HYQ_MAX_GQA * kPart + hd * kPart + 1);
-  }
-  // This thread's first output element: its partial accumulators are loaded
-  // now, in the same round trip as the (m, l) above.
-  float v0[32];
-  {
-    const int i = tid, hd = i >> 7, d = i & (HYQ_D - 1);
-    const float* e = pb + hd * kPart + 2 + d;
-#pragma unroll
-    for (int k = 0; k < 32; ++k)
-      v0[k] = (i < gq * HYQ_D && k < S) ? __ldcg(e + (size_t)k * HYQ_MAX_GQA * kPart) : 0.f;
-  }
-  __syncthreads();
-  if (warp < gq) {  // warp = head, lanes over the splits
-    const int hd = warp;
-    float M = -INFINITY;
-    for (int s2 = lane; s2 < S; s2 += 32) M = fmaxf(M, sm_m[s2 * HYQ_MAX_GQA + hd]);
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    const float Ms = (M == -INFINITY) ? 0.f : M;
-    float Lsum = 0.f;
-    for (int s2 = lane; s2 < S; s2 += 32) {
-      const float wt = ex2(sm_m[s2 * HYQ_MAX_GQA + hd] - Ms);
-      Lsum = fmaf(sm_w[s2 * HYQ_MAX_GQA + hd], wt, Lsum);
-      sm_w[s2 * HYQ_MAX_GQA + hd] = wt;
-    }
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, o);
-    if (lane == 0) {
-      sM[hd] = Ms;
-      sL[hd] = Lsum;
-    }
-  }
-  __syncthreads();
+  constexpr size_t kSplitStride = HYQ_MAX_GQA * kPart;
+  // Thread i merges element i (and i + 512) of head i >> 7 (one head per
+  // warp): lanes load the splits' (m, l) of that head, 32 splits at a time,
+  // every thread its element of those splits, all in one round trip; the
+  // weights reach the other lanes by shuffle.
   for (int i = tid; i < gq * HYQ_D; i += kThreads) {
     const int hd = i >> 7, d = i & (HYQ_D - 1);
     const float* e = pb + hd * kPart + 2 + d;
-    float a = 0.f;
-    for (int s0 = 0; s0 < S; s0 += 32) {  // all loads of a chunk in flight at once
+    float M = -INFINITY;
+    if (S > 32)  // a first pass for the maximum over all splits
+      for (int s0 = 0; s0 < S; s0 += 32)
+        M = fmaxf(M, s0 + lane < S ? __ldcg(pb + (size_t)(s0 + lane) * kSplitStride + hd * kPart) : -INFINITY);
+    float a = 0.f, Lsum = 0.f;
+    for (int s0 = 0; s0 < S; s0 += 32) {
+      const int sl = s0 + lane;
+      const float mw = sl < S ? __ldcg(pb + (size_t)sl * kSplitStride + hd * kPart) : -INFINITY;
+      const float lw = sl < S ? __ldcg(pb + (size_t)sl * kSplitStride + hd * kPart + 1) : 0.f;
       float v[32];
-      if (i == tid && s0 == 0) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) v[k] = v0[k];
-      } else {
+      for (int k = 0; k < 32; ++k) v[k] = s0 + k < S ? __ldcg(e + (size_t)(s0 + k) * kSplitStride) : 0.f;
+      float Mc = fmaxf(M, mw);
 #pragma unroll
-        for (int k = 0; k < 32; ++k) v[k] = s0 + k < S ? __ldcg(e + (size_t)(s0 + k) * HYQ_MAX_GQA * kPart) : 0.f;
-      }
+      for (int o = 1; o < 32; o <<= 1) Mc = fmaxf(Mc, __shfl_xor_sync(0xffffffffu, Mc, o));
+      M = Mc;  // S <= 32: the maximum of this (only) chunk; S > 32: the first pass's
+      const float Ms = (M == -INFINITY) ? 0.f : M;
+      const float wt = sl < S ? ex2(mw - Ms) : 0.f;
+      float lsum = lw * wt;
 #pragma unroll
-      for (int k = 0; k < 32; ++k)
-        if (s0 + k < S) a = fmaf(v[k], sm_w[(s0 + k) * HYQ_MAX_GQA + hd], a);
+      for (int o = 1; o < 32; o <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+      Lsum += lsum;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) a = fmaf(__shfl_sync(0xffffffffu, wt, k), v[k], a);
     }
-    const float Lh = sL[hd];
-    out[((size_t)b * HQ + (size_t)h * gq + hd) * HYQ_D + d] = __float2bfloat16_rn(Lh > 0.f ? a / Lh : 0.f);
+    out[((size_t)b * HQ + (size_t)h * gq + hd) * HYQ_D + d] = __float2bfloat16_rn(Lsum > 0.f ? a / Lsum : 0.f);
   }
   if (tid == 0) tickets[bh] = 0;
   if (ticket_thread) step_ticket_finish(tk_old, sa, lay, b, HKV, app, ntail, len, rpos, rn);

@@ -202,8 +202,14 @@ __device__ void build_block(BuildSmem& sm, const __nv_bfloat16* kbase, const __n
     // argument; a NaN extreme fails the test.
     const float tl = __fmul_rn(__fsub_rn(mn, z32), r32), th = __fmul_rn(__fsub_rn(mx, z32), r32);
     sm.fast[T][row][q] = (uint8_t)(tl > -0.5f && th < qmax + 0.5f);
-    const uint32_t w = (uint32_t)__half_as_ushort(sh) | ((uint32_t)__half_as_ushort(zh) << 16);
-    *reinterpret_cast<uint32_t*>(dst + (row >> 4) * F::kTile + F::kKMeta + T * 256 + (row & 15) * 16 + 4 * q) = w;
+    // Metadata order of hyq.h: K rows hold four scales then four zeros; V
+    // rows pair up (2i, 2i + 1), scales in the first half, zeros in the second.
+    uint8_t* mb = dst + (row >> 4) * F::kTile + F::kKMeta + T * 256;
+    const int r = row & 15;
+    const int so = T == 0 ? 16 * r + 2 * q : 16 * (r >> 1) + 4 * q + 2 * (r & 1);
+    const int zo = T == 0 ? so + 8 : so + 128;
+    *reinterpret_cast<uint16_t*>(mb + so) = __half_as_ushort(sh);
+    *reinterpret_cast<uint16_t*>(mb + zo) = __half_as_ushort(zh);
   }
   __syncthreads();
   if (BK == 8) pack_codes8<0, F::kTile, 0>(sm, dst, any_keep);
