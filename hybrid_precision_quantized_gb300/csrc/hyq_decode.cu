@@ -88,9 +88,12 @@ struct DecodePlan {
 std::atomic<int32_t> g_plan{0};     // hyq_set_decode_plan override (merge 0 = automatic)
 std::atomic<int32_t> g_overlap{0};  // hyq_set_decode_overlap
 
-DecodePlan decode_plan(const hyq_config* c, int32_t len) {
+// overlap: launched as a programmatic dependent, when one SM per merging
+// block of the preceding call (assumed of the same shape) is left free, so
+// that every block of this call can start while those blocks finish.
+DecodePlan decode_plan(const hyq_config* c, int32_t len, bool overlap) {
   const int bh = c->batch * c->num_kv_heads;
-  const int sms = hyq_num_sms();
+  const int sms = hyq_num_sms() - (overlap && 3 * bh <= hyq_num_sms() ? bh : 0);
   int32_t P = len - c->window > 0 ? len - c->window : 0;
   int64_t tiles = (int64_t)(P + 15) / 16 + (hyq_vl_count(c, P) + hyq_cap_tail(c) + 15) / 16;
   int cap = (int)(tiles / 32 > 0 ? tiles / 32 : 1);
@@ -583,7 +586,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
     int cap_vl, int cap_tail, int S, const StepArgs sa) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(16) __nv_bfloat16 q_s[HYQ_MAX_GQA * HYQ_D];
-  __shared__ __align__(16) uint32_t bq_s[HYQ_MAX_GQA][4][16];  // per query row and lane t: the B fragments
+  // B fragments of the query, [k-step pair][row g][lane t][4]: a lane's four
+  // 16-byte loads are consecutive across the warp (no bank conflicts).
+  __shared__ __align__(16) uint32_t bq_s[4][HYQ_MAX_GQA][4][4];
   __shared__ float rowc_s[HYQ_MAX_GQA][4];                       // per query row: ksc (x1, x16), 2^-sigma, kss
   __shared__ uint32_t bz_s[HYQ_MAX_GQA][4];                      // per query row and lane t: zero-point B fragment
   __shared__ __align__(8) uint64_t bars[kWarps * kMaxSlots];
@@ -615,6 +620,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
     mbar_fence_init();
   }
   const int nq16 = gq * HYQ_D / 8;
+  if (ovl && tid == 0) {
+    // Warm L2 (and the address translation) for the query rows, which may
+    // only be read after griddepcontrol.wait; a prefetch returns no data, so
+    // it is correct whatever the preceding kernel still writes there.
+    prefetch_l2(q + ((size_t)b * HQ + (size_t)h * gq) * HYQ_D, gq * HYQ_D * 2);
+    if (sa.k_new) {
+      prefetch_l2(sa.k_new + bh * HYQ_D, HYQ_D * 2);
+      prefetch_l2(sa.v_new + bh * HYQ_D, HYQ_D * 2);
+    }
+  }
   uint4 qv = make_uint4(0, 0, 0, 0);
   if (!ovl && tid < nq16)
     qv = __ldg(reinterpret_cast<const uint4*>(q + ((size_t)b * HQ + (size_t)h * gq) * HYQ_D) + tid);
@@ -765,7 +780,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
       const int hh = (e >> 1) & 1;
       const int tt = BK == 4 ? (e >> 3) & 3 : (e >> 2) & 3;
       const int ks = BK == 4 ? 2 * (e >> 5) + ((e >> 2) & 1) : e >> 4;
-      bq_s[r][tt][2 * ks + hh] = pack_f16x2(x[2 * hp] * qscale, x[2 * hp + 1] * qscale);
+      bq_s[ks >> 1][r][tt][2 * (ks & 1) + hh] = pack_f16x2(x[2 * hp] * qscale, x[2 * hp + 1] * qscale);
     }
     const float kss = kScale * pow2i(sg);
     const float s0 = __shfl_sync(0xffffffffu, gs, 0) * kss, s1 = __shfl_sync(0xffffffffu, gs, 8) * kss;
@@ -790,7 +805,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
   uint32_t bq[8][2];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const uint4 v = *reinterpret_cast<const uint4*>(&bq_s[g][t][4 * i]);
+    const uint4 v = *reinterpret_cast<const uint4*>(&bq_s[i][g][t][0]);
     bq[2 * i][0] = v.x, bq[2 * i][1] = v.y, bq[2 * i + 1][0] = v.z, bq[2 * i + 1][1] = v.w;
   }
   QConst qc;
@@ -1105,7 +1120,7 @@ __global__ void decode_append_kernel(const __nv_bfloat16* __restrict__ q, const 
 size_t hyq_decode_ws_bytes(const hyq_config* c, int32_t len_hint) {
   // Enough for the global merge at the plan's split count (the fallback when
   // a cluster cannot be resident); the cluster and direct merges use none.
-  const DecodePlan p = decode_plan(c, len_hint);
+  const DecodePlan p = decode_plan(c, len_hint, false);  // the larger of the two plans
   size_t bh = (size_t)c->batch * c->num_kv_heads;
   return round_up(bh * 4) + round_up((size_t)c->batch * 4) + round_up(bh * (size_t)p.S * HYQ_MAX_GQA * kPart * 4);
 }
@@ -1173,13 +1188,13 @@ cudaError_t hyq_launch_decode(const hyq_config* c, const void* q, const hyq_layo
     cudaError_t e = set_attrs<kCluster, 4, 4>();
     if (e != cudaSuccess) return e;
   }
-  DecodePlan p = decode_plan(c, len_hint);
+  const int32_t overlap = g_overlap.load(std::memory_order_relaxed);
+  DecodePlan p = decode_plan(c, len_hint, overlap != 0);
   // Cluster merge: 4-bit codes only, and only when the clusters fit; else the
   // workspace merge with the same S.
   if (p.mode == kCluster && (!w44 || !cluster_fits(p.S))) p.mode = kGlobal;
   size_t bh = (size_t)c->batch * c->num_kv_heads;
   int32_t* tickets = static_cast<int32_t*>(ws);
-  const int32_t overlap = g_overlap.load(std::memory_order_relaxed);
   StepArgs sa{static_cast<const __nv_bfloat16*>(k_new),
               static_cast<const __nv_bfloat16*>(v_new),
               static_cast<__nv_bfloat16*>(k_src),

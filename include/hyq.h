@@ -84,14 +84,19 @@ typedef struct {
  *
  *   [0,            CK)           K codes
  *   [CK,           CK+CV)        V codes
- *   [CK+CV,        CK+CV+256)    K metadata: 16 rows x 4 groups x (scale, zero) FP16 pairs
- *   [CK+CV+256,    CK+CV+512)    V metadata: same
+ *   [CK+CV,        CK+CV+256)    K metadata: 16 rows x 4 groups x FP16 scale and zero
+ *   [CK+CV+256,    CK+CV+512)    V metadata: same values, another order
  *
  * (B_K = B_V = 4: 1024 + 1024 + 256 + 256 = HYQ_QTILE_BYTES.)
  *
- * Metadata entry (row r, group q) lives at byte 16*r + 4*q of its region:
- * scale s then zero z.  The dequantised value of element e (group q = e/32)
- * is c * s + z with c the B_K- (K) or B_V-bit (V) code.
+ * Metadata order (byte offsets inside the 256-byte region, r = row 0..15,
+ * q = group 0..3, each entry one FP16):
+ *   K: scale of (r, q) at 16*r + 2*q, zero at 16*r + 8 + 2*q
+ *      (a row's four scales, then its four zeros);
+ *   V: scale of (r, q) at 16*(r/2) + 4*q + 2*(r%2), zero 128 bytes further
+ *      (rows paired (2i, 2i+1): one FP16 pair per pair of rows and group).
+ * The dequantised value of element e (group q = e/32) is c * s + z with c
+ * the B_K- (K) or B_V-bit (V) code.
  *
  * Inside a 4-bit (1024-byte) code region the 16 x 128 codes are ordered for the
  * register fragments of 16x16 tensor-core tiles: byte offset
