@@ -125,17 +125,49 @@ __device__ __forceinline__ float bf16_at(const uint4& u, int e) {
   return __uint_as_float((e & 1) ? (w & 0xFFFF0000u) : (w << 16));
 }
 
-// INT8 code of t (rint, ties to even, clamped to +-127).
-__device__ __forceinline__ float code_i8(float t) { return fminf(fmaxf(rintf(t), -127.f), 127.f); }
+// Codes of the exact quotient x / s (x a BF16 value, s > 0 the FP32 scale, or
+// s = 0 for an all-zero tile).  t = fl32(x / s) is correctly rounded and
+// monotone in x / s, so rounding t to the code grid gives the code of x / s
+// except when t itself is a midpoint of that grid; then the sign of
+// x - t * s, exact in float64 (t has at most 9 significant bits, s 24),
+// decides, and an exact tie keeps the even code.
+__device__ __forceinline__ float quotient(float x, float s) { return s > 0.f ? __fdiv_rn(x, s) : 0.f; }
 
-// e4m3 code of t (nearest, ties to even, saturating) as its float value.
-__device__ __forceinline__ float code_f8(float t) {
-  __nv_fp8_e4m3 c(t);  // round to nearest even, saturate to finite
-  return static_cast<float>(c);
+__device__ __noinline__ float past_midpoint(float x, float s, float t, float below, float above, float even) {
+  const double d = (double)x - (double)t * (double)s;
+  return d > 0.0 ? above : d < 0.0 ? below : even;
 }
 
-__device__ __forceinline__ uint8_t code_f8_bits(float t) {
-  return __nv_cvt_float_to_fp8(t, __NV_SATFINITE, __NV_E4M3);
+// INT8: the nearest integer to x / s, ties to even, clamped to +-127.
+__device__ __forceinline__ float code_i8(float x, float s) {
+  const float t = quotient(x, s);
+  float c = rintf(t);
+  const float f = floorf(t);
+  if (t - f == 0.5f && fabsf(t) < 128.f) c = past_midpoint(x, s, t, f, f + 1.f, c);
+  return fminf(fmaxf(c, -127.f), 127.f);
+}
+
+// e4m3: the value nearest to x / s, ties to even, saturating at +-448.  Its
+// midpoints are the odd multiples of 2^-10 below 2^-6 and, above, the values
+// whose FP32 fraction ends in binary 1 followed by 19 zeros; h is half the
+// e4m3 spacing there.
+__device__ __forceinline__ float code_f8(float x, float s) {
+  const float t = quotient(x, s);
+  const float c = static_cast<float>(__nv_fp8_e4m3(t));  // nearest even, saturating
+  const float a = fabsf(t);
+  if (a >= 448.f) return c;
+  float h = 0.f;
+  if (a < 0.015625f) {
+    const float u = a * 1024.f;  // exact
+    if (u == floorf(u) && fmodf(u, 2.f) == 1.f) h = 0.0009765625f;
+  } else if ((__float_as_uint(a) & 0x000FFFFFu) == 0x00080000u) {
+    h = __uint_as_float(__float_as_uint(a) & 0xFF800000u) * 0.0625f;  // 2^(E-4)
+  }
+  return h > 0.f ? past_midpoint(x, s, t, t - h, t + h, c) : c;
+}
+
+__device__ __forceinline__ uint8_t code_f8_bits(float x, float s) {
+  return __nv_cvt_float_to_fp8(code_f8(x, s), __NV_SATFINITE, __NV_E4M3);  // exact: an e4m3 value
 }
 
 // Number of entries <= x in the ascending array a[0..n).
@@ -322,8 +354,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const __grid_constant__ PackP
         for (int e = 0; e < 4; ++e) {
           const int el = 16 * h + 4 * u + e;
           const float x = bf16_at(kr[el >> 3], el & 7);
-          const float t = sk > 0.f ? __fdiv_rn(x, sk) : 0.f;
-          acc |= static_cast<uint32_t>(code_f8_bits(t)) << (8 * e);
+          acc |= static_cast<uint32_t>(code_f8_bits(x, sk)) << (8 * e);
         }
         w[u] = acc;
       }
@@ -342,9 +373,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const __grid_constant__ PackP
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float x0 = bf16_at(kr[c], 2 * e), x1 = bf16_at(kr[c], 2 * e + 1);
-          const float t0 = sk > 0.f ? __fdiv_rn(x0, sk) : 0.f;
-          const float t1 = sk > 0.f ? __fdiv_rn(x1, sk) : 0.f;
-          w[e] = pack_bf16x2(code_i8(t0), code_i8(t1));
+          w[e] = pack_bf16x2(code_i8(x0, sk), code_i8(x1, sk));
         }
         u = make_uint4(w[0], w[1], w[2], w[3]);
       }
@@ -358,10 +387,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const __grid_constant__ PackP
   for (int e = 0; e < 32; ++e) {
     const float x = bf16_at(vr[e >> 3], e & 7);
     float y = x;
-    if (quant) {
-      const float t = sv > 0.f ? __fdiv_rn(x, sv) : 0.f;
-      y = kFp8 ? code_f8(t) : code_i8(t);
-    }
+    if (quant) y = kFp8 ? code_f8(x, sv) : code_i8(x, sv);
     vs[r][32 * qq + e] = y;
   }
   __syncthreads();
@@ -509,8 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           for (int e = 0; e < 4; ++e) {
             const int el = 16 * c16 + 4 * u + e;
             const float x = bf16_at(qv[el >> 3], el & 7);
-            const float t = sq > 0.f ? __fdiv_rn(x, sq) : 0.f;
-            acc |= static_cast<uint32_t>(code_f8_bits(t)) << (8 * e);
+            acc |= static_cast<uint32_t>(code_f8_bits(x, sq)) << (8 * e);
           }
           w[u] = acc;
         }
@@ -523,9 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float x0 = bf16_at(qv[c], 2 * e), x1 = bf16_at(qv[c], 2 * e + 1);
-          const float t0 = sq > 0.f ? __fdiv_rn(x0, sq) : 0.f;
-          const float t1 = sq > 0.f ? __fdiv_rn(x1, sq) : 0.f;
-          w[e] = pack_bf16x2(code_i8(t0), code_i8(t1));
+          w[e] = pack_bf16x2(code_i8(x0, sq), code_i8(x1, sq));
         }
         *reinterpret_cast<uint4*>(sm + kOffQc + hf * kRegion + swz(rr, c)) = make_uint4(w[0], w[1], w[2], w[3]);
       }

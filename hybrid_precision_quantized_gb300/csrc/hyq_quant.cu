@@ -26,7 +26,7 @@ constexpr int kChunks = HYQ_D / 8;      // 16 chunks of 8 elements per row
 struct BuildSmem {
   __nv_bfloat16 x[2][kRows][HYQ_D];  // K and V rows (zero for padding / kept rows)
   float mn[2][kRows][4], mx[2][kRows][4];
-  float z[2][kRows][4], r[2][kRows][4];
+  float z[2][kRows][4], r[2][kRows][4], s[2][kRows][4];
   int32_t pos[kRows];      // source row of each slot, -1 for none
   uint8_t keep[kRows];     // slot already holds a stream row (append)
   uint8_t nan[2][kRows][4];
@@ -64,17 +64,40 @@ constexpr uint32_t kMagicSum = magic_sum8();
 __device__ __forceinline__ uint32_t lo32(uint64_t v) { return (uint32_t)v; }
 __device__ __forceinline__ uint32_t hi32(uint64_t v) { return (uint32_t)(v >> 32); }
 
+// The code is the grid point z + c s nearest to x, ties to the even c.  It is
+// found from t = fl32(fl32(x - z) * r), r = RN(1/s), whose relative error is
+// at most about 3 * 2^-24 (|t| < 2^8 where it matters: under 5e-5), so
+// rint(t) is the exact answer unless t lies within kNearTie of a half
+// integer; those elements are decided exactly (exact_code).
+constexpr float kNearTie = 0.5f - 0.000244140625f;  // 1/2 - 2^-12
+
+// Exact decision near the midpoint k + 1/2, k = floor(t): in float64 the
+// midpoint z + (k + 1/2) s is exact (s and z are FP16 values: a multiple of
+// 2^-25 below 2^25 in magnitude) and the sign of x minus it is exact.
+__device__ __noinline__ float exact_code(float x, float z, float s, float t) {
+  const float k = floorf(t);
+  const double d = (double)x - ((double)z + ((double)k + 0.5) * (double)s);
+  if (d > 0.0) return k + 1.f;
+  if (d < 0.0) return k;
+  return fmodf(k, 2.f) == 0.f ? k : k + 1.f;  // a tie: the even one
+}
+
 // Bit patterns kMagicBits + code of the two BF16 elements of w (x: low half),
 // for a group whose (x - z) * r all lie in (-0.5, 15.5): there the clamp of
 // the code decision is the identity and the added magic rounds exactly as
 // rint does.  nz2 = (-z, -z), r2 = (r, r).  The magic add is a scalar
 // __fadd_rn, which is never contracted with the product into a fused
-// multiply-add (that would round the unrounded product).
-__device__ __forceinline__ uint2 code_bits2(uint32_t w, uint64_t nz2, uint64_t r2) {
+// multiply-add (that would round the unrounded product).  `near` is set when
+// either element lies within kNearTie of a midpoint (the caller then takes
+// the exact path for the whole word).
+__device__ __forceinline__ uint2 code_bits2(uint32_t w, uint64_t nz2, uint64_t r2, bool& near) {
   const uint64_t x2 = (uint64_t)(w << 16) | ((uint64_t)(w & 0xffff0000u) << 32);
   const uint64_t t2 = f2_mul(f2_add(x2, nz2), r2);
-  return make_uint2(__float_as_uint(__fadd_rn(__uint_as_float(lo32(t2)), kMagic)),
-                    __float_as_uint(__fadd_rn(__uint_as_float(hi32(t2)), kMagic)));
+  const float t0 = __uint_as_float(lo32(t2)), t1 = __uint_as_float(hi32(t2));
+  const float b0 = __fadd_rn(t0, kMagic), b1 = __fadd_rn(t1, kMagic);
+  near |= fabsf(__fsub_rn(t0, __fsub_rn(b0, kMagic))) > kNearTie ||
+          fabsf(__fsub_rn(t1, __fsub_rn(b1, kMagic))) > kNearTie;
+  return make_uint2(__float_as_uint(b0), __float_as_uint(b1));
 }
 
 // Code word from b[p] = kMagicBits + code of nibble p: the shift-add chain
@@ -87,11 +110,13 @@ __device__ __forceinline__ uint32_t pack_nibbles(const uint32_t (&b)[8]) {
 }
 
 // r = 1 / s rounded, and 0 exactly when the step s is 0; qmax = 2^B - 1.
-__device__ __forceinline__ uint32_t code_of(float x, float z, float r, float qmax = 15.f) {
+__device__ __forceinline__ uint32_t code_of(float x, float z, float r, float s, float qmax = 15.f) {
   if (r == 0.f) return 0u;
-  float t = rintf(__fmul_rn(__fsub_rn(x, z), r));
-  t = fminf(fmaxf(t, 0.f), qmax);
-  return (uint32_t)t;
+  const float t = __fmul_rn(__fsub_rn(x, z), r);
+  float c = rintf(t);
+  if (fabsf(__fsub_rn(t, c)) > kNearTie) c = exact_code(x, z, s, t);
+  c = fminf(fmaxf(c, 0.f), qmax);
+  return (uint32_t)c;
 }
 
 __device__ __forceinline__ void unpack8(uint4 v, float (&f)[8]) {
@@ -125,7 +150,7 @@ __device__ void pack_codes8(const BuildSmem& sm, uint8_t* dst, bool any_keep) {
       const int q = e >> 5;
       const uint32_t c = sm.keep[row] ? (old >> (8 * jj)) & 0xFFu
                                       : code_of(__bfloat162float(sm.x[T][row][e]), sm.z[T][row][q], sm.r[T][row][q],
-                                                255.f);
+                                                sm.s[T][row][q], 255.f);
       w |= c << (8 * jj);
     }
     *reinterpret_cast<uint32_t*>(wp) = w;
@@ -198,6 +223,7 @@ __device__ void build_block(BuildSmem& sm, const __nv_bfloat16* kbase, const __n
     const float r32 = s32 > 0.f ? __frcp_rn(s32) : 0.f;
     sm.z[T][row][q] = z32;
     sm.r[T][row][q] = r32;
+    sm.s[T][row][q] = s32;
     // (x - z) * r is monotone in x, so the group's extremes bound every code
     // argument; a NaN extreme fails the test.
     const float tl = __fmul_rn(__fsub_rn(mn, z32), r32), th = __fmul_rn(__fsub_rn(mx, z32), r32);
@@ -224,15 +250,16 @@ __device__ void build_block(BuildSmem& sm, const __nv_bfloat16* kbase, const __n
     if (!any_keep && sm.fast[0][rk0][q] && sm.fast[0][rk1][q]) {
       // Row a, element 4 sub + 2 b + c -> nibble a + 2 b + 4 c of word sub.
       uint2 pb[2][4];
+      bool near = false;
 #pragma unroll
       for (int a = 0; a < 2; ++a) {
         const int row = a ? rk1 : rk0;
         const uint4 xv = *reinterpret_cast<const uint4*>(&sm.x[0][row][8 * cc]);
         const uint64_t nz2 = f2_splat(-sm.z[0][row][q]), r2 = f2_splat(sm.r[0][row][q]);
-        pb[a][0] = code_bits2(xv.x, nz2, r2);
-        pb[a][1] = code_bits2(xv.y, nz2, r2);
-        pb[a][2] = code_bits2(xv.z, nz2, r2);
-        pb[a][3] = code_bits2(xv.w, nz2, r2);
+        pb[a][0] = code_bits2(xv.x, nz2, r2, near);
+        pb[a][1] = code_bits2(xv.y, nz2, r2, near);
+        pb[a][2] = code_bits2(xv.z, nz2, r2, near);
+        pb[a][3] = code_bits2(xv.w, nz2, r2, near);
       }
       uint32_t wf[2];
 #pragma unroll
@@ -247,8 +274,10 @@ __device__ void build_block(BuildSmem& sm, const __nv_bfloat16* kbase, const __n
           }
         wf[sub] = pack_nibbles(bb);
       }
-      *reinterpret_cast<uint2*>(wp) = make_uint2(wf[0], wf[1]);
-      continue;
+      if (!near) {
+        *reinterpret_cast<uint2*>(wp) = make_uint2(wf[0], wf[1]);
+        continue;
+      }
     }
     uint32_t w[2] = {0u, 0u};
     uint2 old = make_uint2(0, 0);
@@ -264,14 +293,14 @@ __device__ void build_block(BuildSmem& sm, const __nv_bfloat16* kbase, const __n
       }
       float e[8];
       unpack8(*reinterpret_cast<const uint4*>(&sm.x[0][row][8 * cc]), e);
-      const float z = sm.z[0][row][q], r = sm.r[0][row][q];
+      const float z = sm.z[0][row][q], r = sm.r[0][row][q], sc = sm.s[0][row][q];
 #pragma unroll
       for (int sub = 0; sub < 2; ++sub)
 #pragma unroll
         for (int b = 0; b < 2; ++b)
 #pragma unroll
           for (int c = 0; c < 2; ++c)
-            w[sub] |= code_of(e[4 * sub + 2 * b + c], z, r) << (4 * (a + 2 * b + 4 * c));
+            w[sub] |= code_of(e[4 * sub + 2 * b + c], z, r, sc) << (4 * (a + 2 * b + 4 * c));
     }
     *reinterpret_cast<uint2*>(wp) = make_uint2(w[0], w[1]);
   }
@@ -287,15 +316,16 @@ __device__ void build_block(BuildSmem& sm, const __nv_bfloat16* kbase, const __n
         sm.fast[1][rv + 9][q]) {
       // Row (b, c), element 4 gl + 2 ss + a -> nibble a + 2 b + 4 c of word (gl, ss).
       uint2 pb[4][4];
+      bool near = false;
 #pragma unroll
       for (int bc = 0; bc < 4; ++bc) {
         const int row = rv + 8 * (bc & 1) + (bc >> 1);
         const uint4 xv = *reinterpret_cast<const uint4*>(&sm.x[1][row][8 * cc]);
         const uint64_t nz2 = f2_splat(-sm.z[1][row][q]), r2 = f2_splat(sm.r[1][row][q]);
-        pb[bc][0] = code_bits2(xv.x, nz2, r2);
-        pb[bc][1] = code_bits2(xv.y, nz2, r2);
-        pb[bc][2] = code_bits2(xv.z, nz2, r2);
-        pb[bc][3] = code_bits2(xv.w, nz2, r2);
+        pb[bc][0] = code_bits2(xv.x, nz2, r2, near);
+        pb[bc][1] = code_bits2(xv.y, nz2, r2, near);
+        pb[bc][2] = code_bits2(xv.z, nz2, r2, near);
+        pb[bc][3] = code_bits2(xv.w, nz2, r2, near);
       }
 #pragma unroll
       for (int gl = 0; gl < 2; ++gl) {
@@ -312,10 +342,11 @@ __device__ void build_block(BuildSmem& sm, const __nv_bfloat16* kbase, const __n
           wf[ss] = pack_nibbles(bb);
         }
         const int g = 2 * (cc & 3) + gl;
-        *reinterpret_cast<uint2*>(dst + tile * F::kTile + F::kVCode + 512 * (cc >> 3) + 16 * (4 * g + t) +
-                                  8 * (q & 1)) = make_uint2(wf[0], wf[1]);
+        if (!near)
+          *reinterpret_cast<uint2*>(dst + tile * F::kTile + F::kVCode + 512 * (cc >> 3) + 16 * (4 * g + t) +
+                                    8 * (q & 1)) = make_uint2(wf[0], wf[1]);
       }
-      continue;
+      if (!near) continue;
     }
     uint8_t* wp[2];
     uint32_t w[2][2] = {{0u, 0u}, {0u, 0u}};
@@ -342,14 +373,14 @@ __device__ void build_block(BuildSmem& sm, const __nv_bfloat16* kbase, const __n
         }
         float e[8];
         unpack8(*reinterpret_cast<const uint4*>(&sm.x[1][row][8 * cc]), e);
-        const float z = sm.z[1][row][q], r = sm.r[1][row][q];
+        const float z = sm.z[1][row][q], r = sm.r[1][row][q], sc = sm.s[1][row][q];
 #pragma unroll
         for (int gl = 0; gl < 2; ++gl)
 #pragma unroll
           for (int ss = 0; ss < 2; ++ss)
 #pragma unroll
             for (int a = 0; a < 2; ++a)
-              w[gl][ss] |= code_of(e[4 * gl + 2 * ss + a], z, r) << (4 * (a + 2 * b + 4 * c));
+              w[gl][ss] |= code_of(e[4 * gl + 2 * ss + a], z, r, sc) << (4 * (a + 2 * b + 4 * c));
       }
 #pragma unroll
     for (int gl = 0; gl < 2; ++gl) *reinterpret_cast<uint2*>(wp[gl]) = make_uint2(w[gl][0], w[gl][1]);

@@ -23,11 +23,12 @@ Readings (the paper leaves these open):
   ``s_T = max|K_T| / c_B`` for K; Eq. 7 quantises V_Q as well and names no
   other rule, so V takes the same one); Q uses one scale per block of 128
   query rows of one head (``s^Q``, Algorithm 2 line 13);
-* scales and codes are decided in float32, the kernel's precision (the
-  paper fixes none): ``s = fl32(max|x| / c_B)`` and ``t = fl32(x / s)``;
-  INT8 codes are ``clamp(rint(t), -127, 127)`` (ties to even), FP8 codes the
-  e4m3 value nearest to ``t`` (ties to even, saturating at +-448); a block
-  of zeros gets ``s = 0`` and zero codes;
+* the stored scale is a float32 number, ``s = RN_fp32(max|x| / c_B)`` (the
+  paper fixes no precision; one rounding of the exact quotient); the code of
+  x is the grid value nearest to the exact quotient ``x / s``, ties to the
+  even code: INT8 the integers -127..127, FP8 the e4m3 values (bias 7,
+  three fraction bits, subnormals below 2^-6, largest 448; values beyond it
+  take +-448).  A block of zeros gets ``s = 0`` and zero codes;
 * ``band=True`` takes the window per query instead (a diagonal band): query
   ``i`` sees the keys ``(i - W, i]`` in BF16, the vertical lines at or
   before ``i - W`` in BF16 and the other keys at or before ``i - W`` from
@@ -52,18 +53,49 @@ KEY_TILE = 64
 QUERY_BLOCK = 128
 
 
-def _codes(x: np.ndarray, s, dtype: str) -> np.ndarray:
-    """Low-bit codes of ``fl32(x / s)`` (float32 in, float64 code values out)."""
-    x = np.asarray(x, dtype=np.float32)
-    s = np.asarray(s, dtype=np.float32)
+def e4m3_values() -> np.ndarray:
+    """The non-negative finite e4m3 values, ascending, built from the format:
+    exponent bias 7, three fraction bits, subnormals m 2^-9 (exponent field
+    0), normals (1 + m/8) 2^(e-7); exponent field 15 with fraction 7 is NaN
+    and there are no infinities, so the largest value is 448.  The index of
+    a value is its 7-bit code, so an even index is an even code."""
+    vals = [m * 2.0 ** -9 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7)
+            for e in range(16) for m in range(8) if not (e == 15 and m == 7)]
+    return np.array(vals, dtype=np.float64)
+
+
+_GRIDS = {"int8": np.arange(128, dtype=np.float64), "fp8": e4m3_values()}
+
+
+def nearest_grid_index(a, s, grid) -> np.ndarray:
+    """Index into the ascending non-negative ``grid`` of the value nearest to
+    the exact quotient a / s (a >= 0, s > 0), ties to the even index, values
+    past the top taking the top.  A float64 quotient gives a candidate; it
+    is moved across the midpoints (grid[i] + grid[i+1]) / 2, whose products
+    with s are exact in float64 (at most 9 + 24 significant bits), by the
+    exact sign of a minus that product."""
+    mids = (grid[:-1] + grid[1:]) / 2
+    n = len(mids)
     with np.errstate(divide="ignore", invalid="ignore"):
-        t = np.where(s > 0, x / np.where(s > 0, s, np.float32(1.0)), np.float32(0.0)).astype(np.float32)
-    if dtype == "int8":
-        return np.clip(np.rint(t), -127, 127).astype(np.float64)
-    if dtype == "fp8":
-        t = np.clip(t, np.float32(-448.0), np.float32(448.0))
-        return torch.from_numpy(t).to(torch.float8_e4m3fn).to(torch.float64).numpy()
-    raise ValueError(dtype)
+        i = np.searchsorted(mids, a / s)
+    for _ in range(2):
+        d = a - mids[np.minimum(i, n - 1)] * s
+        i = np.where((i < n) & ((d > 0) | ((d == 0) & (i % 2 == 1))), i + 1, i)
+        d = a - mids[np.maximum(i - 1, 0)] * s
+        i = np.where((i > 0) & ((d < 0) | ((d == 0) & (i % 2 == 1))), i - 1, i)
+    return i
+
+
+def _codes(x: np.ndarray, s, dtype: str) -> np.ndarray:
+    """Low-bit codes (as float64 code values) of the exact quotients x / s."""
+    if dtype not in _GRIDS:
+        raise ValueError(dtype)
+    x = np.asarray(x, dtype=np.float64)
+    s = np.broadcast_to(np.asarray(s, dtype=np.float64), x.shape)
+    live = s > 0
+    grid = _GRIDS[dtype]
+    i = nearest_grid_index(np.abs(x), np.where(live, s, 1.0), grid)
+    return np.where(live, np.sign(x) * grid[i], 0.0)
 
 
 def quantize_symmetric(x, axis, dtype: str):
@@ -74,7 +106,7 @@ def quantize_symmetric(x, axis, dtype: str):
     x = np.asarray(x, dtype=np.float64)
     amax = np.abs(x).max(axis=axis, keepdims=True).astype(np.float32)
     s = (amax / np.float32(C_B[dtype])).astype(np.float32)
-    c = _codes(x.astype(np.float32), s, dtype)
+    c = _codes(x, s, dtype)
     s64 = s.astype(np.float64)
     return c * s64, c, s64
 

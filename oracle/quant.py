@@ -12,9 +12,12 @@ form nor the rounding; the readings adopted here are:
   in exact arithmetic: the step of the 2^bits-level grid rounded *up* to
   float16, so that the top code still reaches the group maximum;
 * ``z = RN_fp16(min)``;
-* the code decision is taken in float32 (the kernel's precision):
-  ``r = fl32(1 / s)``, ``c = clamp(rint(fl32(fl32(x - z) * r)), 0, qmax)``
-  with round-half-to-even; a group with ``s == 0`` gets all-zero codes;
+* the code of x is the grid point z + c * s nearest to x, c in [0, qmax],
+  with ties going to the even code (round-half-to-even of (x - z) / s,
+  then clamped); a group with ``s == 0`` gets all-zero codes.  The decision
+  is exact: each midpoint z + (c +- 1/2) s is a multiple of 2^-25 below
+  2^25 in magnitude (s and z are float16), so it is exact in float64, and
+  the sign of x - midpoint is exact in IEEE arithmetic;
 * a group whose scale or zero is not a finite float16 (|x| beyond the
   float16 range, or NaN input) is an error.
 
@@ -77,6 +80,29 @@ def min_step_fp16(mx, mn, qmax: int) -> np.ndarray:
     return res.astype(np.float16)
 
 
+def nearest_codes(x, z, s, qmax: int) -> np.ndarray:
+    """Index c in [0, qmax] of the grid point z + c*s nearest to x, ties to
+    the even index; 0 where s == 0.  x, z, s: float64 arrays (BF16 values,
+    float16 zero and step) of one broadcast shape.
+
+    A float64 quotient gives a candidate at most one index off; it is then
+    moved across the midpoints z + (c +- 1/2) s, each exact in float64, by
+    the exact sign of x minus that midpoint."""
+    x, z, s = np.broadcast_arrays(np.asarray(x, np.float64), np.asarray(z, np.float64),
+                                  np.asarray(s, np.float64))
+    live = s > 0
+    with np.errstate(divide="ignore", invalid="ignore"):
+        c = np.where(live, np.clip(np.rint((x - z) / np.where(live, s, 1.0)), 0, qmax), 0.0)
+    for _ in range(2):
+        up = live & (c < qmax)
+        d = x - (z + (c + 0.5) * s)            # exact sign: x against the midpoint above c
+        c = np.where(up & ((d > 0) | ((d == 0) & (c % 2 == 1))), c + 1, c)
+        dn = live & (c > 0)
+        d = x - (z + (c - 0.5) * s)            # against the midpoint below c
+        c = np.where(dn & ((d < 0) | ((d == 0) & (c % 2 == 1))), c - 1, c)
+    return c
+
+
 def quantize(x, bits: int = 4, group: int = GROUP):
     """Quantise rows of ``x`` (values exactly representable in BF16).
 
@@ -105,15 +131,7 @@ def quantize(x, bits: int = 4, group: int = GROUP):
         zero = mn.astype(np.float16)
     if not (np.isfinite(scale).all() and np.isfinite(zero).all()):
         raise QuantRangeError("group range exceeds the float16 metadata range")
-    # Code decision in float32, one IEEE operation at a time.
-    s32 = scale.astype(np.float32)[..., None]
-    z32 = zero.astype(np.float32)[..., None]
-    x32 = xg.astype(np.float32)
-    with np.errstate(divide="ignore", invalid="ignore"):
-        r32 = np.float32(1.0) / s32
-        t = (x32 - z32) * r32
-        c = np.clip(np.rint(t), 0, qmax)
-    c = np.where(s32 == 0, 0, c)
+    c = nearest_codes(xg, zero.astype(np.float64)[..., None], scale.astype(np.float64)[..., None], qmax)
     codes = c.astype(np.uint8).reshape(x.shape)
     return codes, scale, zero
 

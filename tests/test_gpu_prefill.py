@@ -224,3 +224,38 @@ def test_prefill_band_llama_shaped_32k_sampled(hyq, dtype):
             rows = slice(128 * blk, 128 * blk + 128)
             assert_prefill_close(got[:, hq, rows], want[:, hq, rows], a[:, hq, rows],
                                  what=f"band {dtype} head {hq} block {blk}")
+
+
+@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+def test_prefill_codes_of_exact_quotients(hyq, dtype):
+    """Values whose float32 quotient x / s lands exactly on a midpoint of the
+    code grid while the exact quotient does not (found exhaustively, largest
+    quotients first), one per 64-key tile: key 64t carries such a value and
+    is the only key query row 64t + 1 attends to (one-hot query and key on
+    dimension t, logit ~22), so that row's output is the dequantised value
+    row, and a code decided by rounding twice falls outside the tolerance."""
+    from types import SimpleNamespace
+    from tests.gpu_util import double_rounding_cases
+    cases = double_rounding_cases(dtype, want=12)
+    T = len(cases)
+    Lc = 64 * T + 2
+    rng = np.random.default_rng(31)
+    q = np.zeros((1, 1, Lc, 128))
+    k = np.zeros((1, 1, Lc, 128))
+    v = np.zeros((1, 1, Lc, 128))
+    for t, (A, x) in enumerate(cases):
+        A, x = A * 32, x * 32
+        rows = slice(64 * t, 64 * t + 64)
+        v[0, 0, rows] = rng.uniform(-A / 4, A / 4, (64, 128))
+        v[0, 0, 64 * t + 5, 7] = A                        # the tile maximum
+        v[0, 0, 64 * t, 3 + t] = x                        # the planted value
+        k[0, 0, 64 * t, t] = 16.0
+        q[0, 0, 64 * t + 1, t] = 16.0
+    c = SimpleNamespace(q=torch.from_numpy(q).to(torch.bfloat16), k=torch.from_numpy(k).to(torch.bfloat16),
+                        v=torch.from_numpy(v).to(torch.bfloat16))
+    idx = np.zeros((1, 1, 0), np.int64)
+    got = run_gpu(c, Lc, 0, 0, dtype, idx)
+    want, a = hybrid_prefill(c.q.double().numpy(), c.k.double().numpy(), c.v.double().numpy(), None, 0, dtype,
+                             return_abs=True)
+    rows = [64 * t + 1 for t in range(T)]
+    assert_prefill_close(got[:, :, rows], want[:, :, rows], a[:, :, rows], what=f"{dtype} planted quotients")

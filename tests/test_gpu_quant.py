@@ -154,3 +154,35 @@ def test_rebuild_bit_exact_on_edge_groups(hyq):
         qpos = np.setdiff1d(np.arange(P), idx_np[0, h])
         _check_stream(layer, 0, h, len(qpos), k_rows[0, h, qpos].double().numpy(),
                       v_rows[0, h, qpos].double().numpy())
+
+
+@pytest.mark.parametrize("bits", [(4, 4), (8, 8), (4, 8)])
+def test_codes_at_planted_midpoints_bit_exact(hyq, bits):
+    """Groups on grids whose step has an inexact float32 reciprocal, with
+    elements at exact midpoints (the even code) and one BF16 step either side
+    (the nearer code): appended in two calls (the second starts inside a
+    block, so both the word-at-a-time and the per-element code paths run)
+    and rebuilt, every code, scale and zero equal to the oracle's."""
+    from tests.gpu_util import tie_rows
+    B, HQ, HKV, n1, n2 = 1, 2, 2, 70, 50
+    cfg = make_config(B, HQ, HKV, capacity=256, window=0, bits_k=bits[0], bits_v=bits[1])
+    layer = HybridLayer(cfg)
+    layer.reset()
+    k = tie_rows(21, (B, HKV, n1 + n2, 128), bits[0])
+    v = tie_rows(22, (B, HKV, n1 + n2, 128), bits[1])
+    hyq_quantize_append(cfg, k[:, :, :n1].contiguous().cuda(), v[:, :, :n1].contiguous().cuda(), n1, layer.c)
+    hyq_quantize_append(cfg, k[:, :, n1:].contiguous().cuda(), v[:, :, n1:].contiguous().cuda(), n2, layer.c)
+    torch.cuda.synchronize()
+    assert hyq_read_device_error(layer.err()) == 0
+    for h in range(HKV):
+        _check_stream(layer, 0, h, n1 + n2, k[0, h].double().numpy(), v[0, h].double().numpy())
+    # the same rows through the rebuild (W = 0, no vertical lines)
+    cfg2 = make_config(B, HQ, HKV, capacity=256, window=0, rho_ppm=0, bits_k=bits[0], bits_v=bits[1])
+    layer2 = HybridLayer(cfg2)
+    layer2.reset()
+    idx = torch.zeros(B, HKV, 1, dtype=torch.int32, device="cuda")
+    hyq_rebuild(cfg2, k.cuda(), v.cuda(), n1 + n2, idx, 0, layer2.c)
+    torch.cuda.synchronize()
+    assert hyq_read_device_error(layer2.err()) == 0
+    for h in range(HKV):
+        _check_stream(layer2, 0, h, n1 + n2, k[0, h].double().numpy(), v[0, h].double().numpy())

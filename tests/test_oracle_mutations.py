@@ -35,10 +35,10 @@ MUTATIONS = [
     ("quant", "zero = mn.astype(np.float16)", "zero = mx.astype(np.float16)", "zero point = max"),
     ("quant", "scale = min_step_fp16(mx, mn, qmax)",
      "scale = ((mx - mn) / float(qmax)).astype(np.float16)", "scale rounded to nearest"),
-    ("quant", "c = np.clip(np.rint(t), 0, qmax)", "c = np.clip(np.floor(t + 0.5), 0, qmax)",
-     "ties away from zero"),
-    ("quant", "c = np.clip(np.rint(t), 0, qmax)", "c = np.clip(np.floor(t), 0, qmax)",
-     "truncating codes"),
+    ("quant", "c = np.where(dn & ((d < 0) | ((d == 0) & (c % 2 == 1))), c - 1, c)",
+     "c = np.where(dn & (d <= 0), c - 1, c)", "ties always to the lower code"),
+    ("quant", "d = x - (z + (c - 0.5) * s)            # against the midpoint below c",
+     "d = x - (z + c * s)", "truncated codes"),
     ("quant", "return (cg * s + z).reshape(codes.shape)", "return (cg * s - z).reshape(codes.shape)",
      "dequantise sign"),
     ("select", "k = -((-P * int(rho_ppm)) // 1_000_000)", "k = (P * int(rho_ppm)) // 1_000_000",
@@ -73,8 +73,10 @@ MUTATIONS = [
      "lg = np.where(pos[None, :] < rows[:, None] + 2, lg, -np.inf)", "causal mask off by one"),
     ("prefill", "alpha * qb @ Kall[nq:].T], axis=1)", "alpha * qhat @ Kall[nq:].T], axis=1)",
      "BF16 branch uses quantised queries"),
-    ("prefill", "return np.clip(np.rint(t), -127, 127)", "return np.clip(np.trunc(t), -127, 127)",
-     "INT8 codes truncated"),
+    ("prefill", "d = a - mids[np.maximum(i - 1, 0)] * s",
+     "d = a - grid[np.maximum(i, 0)] * s", "codes truncated toward zero"),
+    ("prefill", "i = np.where((i > 0) & ((d < 0) | ((d == 0) & (i % 2 == 1))), i - 1, i)",
+     "i = np.where((i > 0) & (d <= 0), i - 1, i)", "ties toward zero"),
     ("prefill", "vq[t0:t0 + len(j)] = quantize_symmetric(v[b, kh, j], None, dtype)[0]",
      "vq[t0:t0 + len(j)] = quantize_symmetric(v[b, kh, j], 0, dtype)[0]", "V scales per channel"),
     ("prefill", "s = (amax / np.float32(C_B[dtype])).astype(np.float32)",

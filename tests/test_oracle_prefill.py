@@ -59,8 +59,8 @@ def test_fp8_codes_are_e4m3_values_with_max_at_448():
     x = rng.standard_normal((64, 128)) * 3
     xh, c, s = quantize_symmetric(x, 0, "fp8")          # per-channel scales
     assert np.abs(c).max(axis=0).min() == 448.0
-    back = torch.from_numpy(c).to(torch.float8_e4m3fn).double().numpy()
-    assert np.array_equal(back, c)                      # representable exactly
+    table = set(_e4m3_values().values())
+    assert all(v in table for v in np.unique(c))        # every code is an e4m3 value
     rel = np.abs(xh - x) / np.maximum(np.abs(x), 1e-3)
     assert np.median(rel) < 2 ** -4                     # 3-bit mantissa
 
@@ -109,36 +109,72 @@ def _e4m3_values():
     return vals
 
 
-def test_fp8_codes_are_nearest_e4m3_ties_to_even():
-    vals = _e4m3_values()
-    pos = sorted((v, b) for b, v in vals.items() if v >= 0 and not (v == 0 and b & 0x80))
-    grid = np.array([v for v, _ in pos])
-    mant_even = np.array([(b & 1) == 0 for _, b in pos])
-    rng = np.random.default_rng(11)
-    t = np.concatenate([rng.uniform(0, 448, 4000), rng.uniform(0, 0.05, 2000),
-                        (grid[:-1] + grid[1:]) / 2])          # exact midpoints: ties
-    t = t.astype(np.float32).astype(np.float64)
-    x = np.concatenate([t, -t, [448.0]])
-    _, c, s = quantize_symmetric(x.reshape(1, -1), None, "fp8")
-    tt = (x.astype(np.float32) / np.float32(s.item())).astype(np.float64)
-    a = np.abs(tt)
-    i = np.clip(np.searchsorted(grid, a), 1, len(grid) - 1)
-    lo, hi = grid[i - 1], grid[i]
-    pick_hi = (a - lo > hi - a) | ((a - lo == hi - a) & mant_even[i])
-    want = np.where(pick_hi, hi, lo) * np.sign(tt)
-    np.testing.assert_array_equal(c.ravel(), want)
+def test_oracle_e4m3_table_matches_the_bit_patterns():
+    """The oracle's e4m3 value list (built from the format) equals the
+    non-negative finite values of the 256 bit patterns, decoded here by
+    hand and by torch's float8_e4m3fn type."""
+    from oracle.prefill import e4m3_values
+    by_hand = sorted({v for v in _e4m3_values().values() if v >= 0})
+    assert list(e4m3_values()) == by_hand and len(by_hand) == 127 and by_hand[-1] == 448.0
+    u8 = torch.arange(256, dtype=torch.uint8)
+    dec = u8.view(torch.float8_e4m3fn).double().numpy()
+    for bits, v in _e4m3_values().items():
+        assert dec[bits] == v
 
 
-def test_int8_scale_and_codes_in_float32():
+def _exact_nearest(x, s, grid_pos, even_of):
+    """Brute force over the signed grid with exact rationals: the grid value
+    nearest to x / s, ties to the candidate whose ``even_of`` is true."""
+    from fractions import Fraction
+    q = Fraction(float(x)) / Fraction(float(s))
+    cands = sorted({Fraction(g) for g in grid_pos} | {-Fraction(g) for g in grid_pos})
+    best = min(abs(q - c) for c in cands)
+    near = [c for c in cands if abs(q - c) == best]
+    if len(near) == 1:
+        return float(near[0])
+    return float([c for c in near if even_of(abs(float(c)))][0])
+
+
+def _tie_inputs(grid, s, rng, n_rand):
+    """Values x with x / s at exact midpoints of the grid, one float64 step
+    either side of them, and random ones."""
+    mids = (grid[:-1] + grid[1:]) / 2
+    pick = mids[rng.choice(len(mids), 40, replace=False)]
+    xs = np.concatenate([pick * s, np.nextafter(pick * s, np.inf), np.nextafter(pick * s, -np.inf),
+                         rng.uniform(0, grid[-1] * s, n_rand)])
+    return np.concatenate([xs, -xs])
+
+
+@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+@pytest.mark.parametrize("s_mant", [1.0, 3.0, 1.0 + 2.0 ** -23])
+def test_codes_are_nearest_to_the_exact_quotient(dtype, s_mant):
+    """Codes against exact rational brute force: planted exact midpoints go
+    to the even code, their float64 neighbours to the nearer code."""
+    from oracle.prefill import C_B, _codes, e4m3_values
+    grid = e4m3_values() if dtype == "fp8" else np.arange(128.0)
+    s = float(np.float32(s_mant * 2.0 ** -7))
+    rng = np.random.default_rng(13)
+    x = _tie_inputs(grid, s, rng, 100)
+    got = _codes(x, np.float64(s), dtype)
+    idx = {float(v): i for i, v in enumerate(grid)}
+    want = [_exact_nearest(xi, s, grid, lambda a: idx[a] % 2 == 0) for xi in x]
+    np.testing.assert_array_equal(got, np.array(want))
+    # beyond the top of the grid: saturate
+    assert _codes(np.array([grid[-1] * s * 1.5]), np.float64(s), dtype)[0] == grid[-1]
+    assert C_B[dtype] == grid[-1]
+
+
+def test_int8_scale_is_one_float32_rounding():
     rng = np.random.default_rng(12)
     x = rng.standard_normal((64, 128)).astype(np.float32).astype(np.float64)
     _, c, s = quantize_symmetric(x, None, "int8")
-    s32 = np.float32(np.abs(x).max()) / np.float32(127.0)
-    assert s.item() == float(np.float32(s32))
-    t = (x.astype(np.float32) / np.float32(s32)).astype(np.float64)
-    assert np.all(np.abs(t - c) <= 0.5)
-    half = np.abs(np.abs(t - c) - 0.5) == 0
-    assert np.all(c[half] % 2 == 0)
+    from fractions import Fraction
+    q = Fraction(float(np.abs(x).max())) / 127                 # the exact quotient
+    f = np.float32(s.item())
+    assert float(f) == s.item()                                 # a float32 number ...
+    for nb in (np.nextafter(f, np.float32(np.inf)), np.nextafter(f, np.float32(-np.inf))):
+        assert abs(Fraction(float(f)) - q) <= abs(Fraction(float(nb)) - q)   # ... nearest to it
+    assert np.abs(c).max() == 127.0
 
 
 def test_value_tiles_share_one_scale():
@@ -271,3 +307,24 @@ def test_band_restricted_blocks_equal_full_computation():
     full = hybrid_prefill(q, k, v, idx, window=32, dtype="int8", band=True)
     part = hybrid_prefill(q, k, v, idx, window=32, dtype="int8", query_blocks=[1], heads=[3], band=True)
     np.testing.assert_array_equal(part[0, 3, 128:256], full[0, 3, 128:256])
+
+
+@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+def test_double_rounding_cases_change_the_code_visibly(dtype):
+    """The prefill tie workload: each planted value's exact code differs from
+    the code of its rounded float32 quotient, by more than the parity
+    tolerance once multiplied out at the test's scale (so a kernel that
+    rounds twice fails the GPU test)."""
+    from oracle.prefill import C_B, _codes, e4m3_values, nearest_grid_index
+    from tests.gpu_util import double_rounding_cases
+    grid = np.arange(128.0) if dtype == "int8" else e4m3_values()
+    cases = double_rounding_cases(dtype)
+    assert len(cases) >= 8
+    for A, x in cases:
+        A, x = A * 32, x * 32                           # the GPU test's scale: A in [32, 64)
+        s = float(np.float32(np.float32(A) / np.float32(C_B[dtype])))
+        exact = _codes(np.array([x]), np.float64(s), dtype)[0] * s
+        t32 = float(np.float32(np.float32(x) / np.float32(s)))
+        twice = grid[nearest_grid_index(np.array([t32]), 1.0, grid)[0]] * s
+        tol = 2e-3 + 1e-2 * abs(exact) + 2.0 ** -8 * abs(exact)
+        assert abs(exact - twice) > tol, (A, x, exact, twice)

@@ -29,21 +29,69 @@ def test_round_up_fp16_is_smallest_half_not_below():
     assert np.all(below < x)
 
 
+def _brute_force_codes(x, s, z, qmax):
+    """For every element, the index of the exactly nearest grid point z + c*s
+    (rational arithmetic over all qmax + 1 candidates), ties to the even
+    index; 0 for a zero step."""
+    from fractions import Fraction
+    out = np.zeros(x.shape, np.int64)
+    for idx in np.ndindex(x.shape):
+        sf, zf, xf = Fraction(float(s[idx])), Fraction(float(z[idx])), Fraction(float(x[idx]))
+        if sf == 0:
+            continue
+        dist = [abs(xf - (zf + c * sf)) for c in range(qmax + 1)]
+        best = min(dist)
+        cands = [c for c in range(qmax + 1) if dist[c] == best]
+        out[idx] = cands[0] if len(cands) == 1 else [c for c in cands if c % 2 == 0][0]
+    return out
+
+
 @pytest.mark.parametrize("bits", [4, 8])
 def test_codes_are_nearest_grid_points_brute_force(bits):
-    x = bf16_rows(1, 64)
+    x = bf16_rows(1, 16)
     c, s, z = quantize(x, bits)
     qmax = (1 << bits) - 1
-    xs = x.reshape(64, 4, 32)
-    sd = s.astype(np.float64)[..., None]
-    zd = z.astype(np.float64)[..., None]
-    grid = np.arange(qmax + 1)[None, None, None, :] * sd[..., None] + zd[..., None]
-    err = np.abs(xs[..., None] - grid)                       # every candidate code
-    best = err.min(axis=-1)
-    chosen = np.take_along_axis(err, c.reshape(64, 4, 32)[..., None].astype(np.int64), -1)[..., 0]
-    # the decision is taken in float32: allow a 1e-5 relative slack near ties
-    assert np.all(chosen <= best + 1e-5 * sd + 1e-12)
+    xs = x.reshape(16, 4, 32)
+    want = _brute_force_codes(xs, np.broadcast_to(s[..., None], xs.shape), np.broadcast_to(z[..., None], xs.shape),
+                              qmax)
+    assert np.array_equal(c.reshape(16, 4, 32).astype(np.int64), want)
     assert c.max() <= qmax and c.dtype == np.uint8
+
+
+def _tie_rows(bits):
+    """Rows whose elements sit exactly on a midpoint z + (c + 1/2) s, one BF16
+    step either side of it, and far from it: per group the minimum 0 and the
+    maximum qmax * 2^-k fix s = 2^-k and z = 0, and the remaining elements
+    are chosen on that grid."""
+    qmax = (1 << bits) - 1
+    rows = []
+    for k in (0, 3, 6):
+        step = 2.0 ** -k
+        for base in range(0, qmax, max(1, qmax // 7)):
+            mid = (base + 0.5) * step
+            vals = [0.0, qmax * step, mid, float(np.nextafter(np.float32(mid), np.float32(np.inf))),
+                    float(np.nextafter(np.float32(mid), np.float32(-np.inf))), base * step, (base + 1) * step]
+            g = (vals * 5)[:32]
+            rows.append(g)
+    n = len(rows) // 4 * 4
+    x = np.array(rows[:n], np.float64).reshape(-1, 128)
+    return torch.from_numpy(x).to(torch.bfloat16).double().numpy()
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_codes_at_exact_midpoints_go_to_even(bits):
+    """Planted ties and near-ties: exact midpoints take the even code; BF16
+    neighbours of a midpoint take the nearer code (brute force, exact)."""
+    x = _tie_rows(bits)
+    qmax = (1 << bits) - 1
+    c, s, z = quantize(x, bits)
+    xs = x.reshape(x.shape[0], 4, 32)
+    want = _brute_force_codes(xs, np.broadcast_to(s[..., None], xs.shape), np.broadcast_to(z[..., None], xs.shape),
+                              qmax)
+    assert np.array_equal(c.reshape(xs.shape).astype(np.int64), want)
+    # some elements really are ties (the test plants them)
+    u = (xs - z.astype(np.float64)[..., None]) / s.astype(np.float64)[..., None]  # exact: s is a power of two
+    assert np.count_nonzero(u - np.floor(u) == 0.5) > 10
 
 
 def test_error_bound_half_step_over_contiguous_groups():
@@ -169,3 +217,25 @@ def test_large_but_representable_group_is_fine():
     row[0, 5] = 70000.0          # step 4667 and zero 0 are finite float16
     c, s, z = quantize(row)
     assert c[0, 5] == 15 and np.all(c[0, :5] == 0)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_tie_rows_plant_exact_midpoints_and_neighbours(bits):
+    """The GPU tie workload really contains exact midpoints (decided to the
+    even code) and near-midpoints, and its codes agree with exact rational
+    brute force."""
+    from tests.gpu_util import tie_rows
+    x = tie_rows(7, (6, 128), bits).double().numpy()
+    qmax = (1 << bits) - 1
+    c, s, z = quantize(x, bits)
+    xs = x.reshape(6, 4, 32)
+    sd, zd = s.astype(np.float64)[..., None], z.astype(np.float64)[..., None]
+    u = (xs - zd) / sd
+    assert np.count_nonzero(u - np.floor(u) == 0.5) >= 20
+    want = _brute_force_codes(xs, np.broadcast_to(sd, xs.shape), np.broadcast_to(zd, xs.shape), qmax)
+    assert np.array_equal(c.reshape(xs.shape).astype(np.int64), want)
+    # the float32 recipe (x - z) * fl32(1/s) really differs from the exact codes somewhere
+    r32 = (np.float32(1.0) / s.astype(np.float32))[..., None]
+    t32 = ((xs.astype(np.float32) - z.astype(np.float32)[..., None]) * r32).astype(np.float32)
+    rec = np.clip(np.rint(t32), 0, qmax)
+    assert np.count_nonzero(rec != want) > 0
