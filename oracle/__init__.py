@@ -8,8 +8,12 @@ module is the seeded input generator ``gen``.
 
 It is a plain, slow, obviously-correct restatement of what the method in
 *HyQuant: Hybrid-Precision Quantization for LLM Attention* computes, in
-float64 unless the method (or the kernel, where floating point decides an
-integer) fixes another precision.  Each function names the passage it follows.
+float64; integer decisions (codes) are taken exactly, by their definition
+(the nearest grid point, ties to even).  Each function names the passage it
+follows.  It exists twice, written independently: the Python modules below
+and ``cpp/hyq_oracle.cpp`` (plain C++17, float64 accumulation, its own
+binary16 / e4m3 arithmetic; ``cpp_oracle`` binds it), and the tests assert
+that the two agree.
 
 Modules
 -------
@@ -19,6 +23,8 @@ attention  hybrid decode attention (Eq. 8-9, Alg. 3) and textbook softmax
 prefill    hybrid prefill operator (Eq. 6-7, Alg. 2)
 metrics    attention-output MSE and attention-mass coverage (Table 1, Fig. 2/6)
 accounting byte counts of the hybrid cache (Table 14, §5.5)
+cpp_oracle ctypes binding of the C++ restatement (quantiser, selection, decode,
+           prefill), built by ``cpp_oracle.build()`` with g++
 
 Pins: every function here is checked by ``tests/test_oracle_*.py`` against
 closed forms, special cases that reduce to a library routine, brute force on
