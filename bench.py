@@ -56,6 +56,9 @@ def parse():
                    help="tuning: hyq_set_decode_plan(MERGE, SPLITS) for the period (0 0 = automatic)")
     p.add_argument("--no-mass", action="store_true", help="skip the Eq. 4 mass-score period measurement")
     p.add_argument("--no-frozen", action="store_true", help="skip the frozen-mode period measurement")
+    p.add_argument("--no-sweep", action="store_true",
+                   help="skip the 1K/4K/16K context periods and the batch-16 period with maintenance")
+    p.add_argument("--no-grid", action="store_true", help="skip the Qwen3-32B-shaped rho x W timing grid")
     p.add_argument("--no-prefetch", dest="prefetch", action="store_false",
                    help="plain fused decode steps; by default each step warms L2 with the next layer's share "
                         "once its own reads are done (hyq_decode_step_prefetch)")
@@ -191,7 +194,7 @@ def prefill_measure(dev, lengths, reps=5, warmup=3, windows=("fixed", "band")):
 
 
 def batched_measure(dev, batch=16, n_layers=4, reps=5, warmup=3, seed=1003, hq=HQ, model_layers=36,
-                    heavy_tail=False, workload=None):
+                    heavy_tail=False, workload=None, rho_ppm=RHO_PPM, window=WINDOW):
     """Decode attention at batch 16 (Qwen3-8B-shaped heads: 32 query / 8 KV,
     d 128, 32K context, W 128, rho 5%): per-call time over n_layers distinct
     layers (~3 GB of hybrid caches, far beyond L2), CUDA events.  Each layer
@@ -203,10 +206,10 @@ def batched_measure(dev, batch=16, n_layers=4, reps=5, warmup=3, seed=1003, hq=H
     import hybrid_precision_quantized_gb300 as hyq
     from hybrid_precision_quantized_gb300 import _lib as L
     Bb, HQ = batch, hq
-    cfg = hyq.make_config(Bb, HQ, HKV, capacity=CTX, window=WINDOW, period=PERIOD, rho_ppm=RHO_PPM)
+    cfg = hyq.make_config(Bb, HQ, HKV, capacity=CTX, window=window, period=PERIOD, rho_ppm=rho_ppm)
     g = torch.Generator(device=dev)
     g.manual_seed(seed)
-    P = CTX - WINDOW
+    P = CTX - window
     k_vl = hyq.hyq_vl_count(cfg, P)
     layers = []
     for _ in range(n_layers):
@@ -249,17 +252,32 @@ def batched_measure(dev, batch=16, n_layers=4, reps=5, warmup=3, seed=1003, hq=H
     e1.record()
     torch.cuda.synchronize()
     us = e0.elapsed_time(e1) * 1e3 / (reps * n_layers)
-    nbytes = Bb * (HKV * ((P - k_vl) * 160 + (k_vl + WINDOW) * 512) + 2 * HQ * D * 2)
+    nbytes = Bb * (HKV * ((P - k_vl) * 160 + (k_vl + window) * 512) + 2 * HQ * D * 2)
     peak, kind = measured_peaks()
     gbs = nbytes / (us * 1e-6) / 1e9
     err = max(hyq.hyq_read_device_error(l.err()) for l in layers)
     return {"workload": workload or ("qwen3-8b-shaped batched decode attention, B16, 32/8 heads, d128, 32K ctx, "
                                      "W128, rho 5%, K4V4 G32; 4 distinct layers"),
+            "rho_ppm": rho_ppm, "window": window,
             "us_per_call": us, f"us_per_token_{model_layers}_layers": us * model_layers / Bb,
             "algorithmic_bytes_per_call": nbytes,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                          "peak_source": f"{kind} hbm_gbs"},
             "device_error_word": err}
+
+
+def qwen32b_grid(dev):
+    """The Qwen3-32B-shaped batch-4 decode attention over the rho x W sweep
+    (rho 2, 5, 10%; W 64, 128, 256), heavy-tailed sink magnitudes, 4
+    distinct layers per point."""
+    out = []
+    for rho in (20_000, 50_000, 100_000):
+        for w in (64, 128, 256):
+            r = batched_measure(dev, batch=4, hq=64, n_layers=4, seed=1004, model_layers=64, heavy_tail=True,
+                                rho_ppm=rho, window=w, workload="qwen3-32b-shaped decode attention, B4, 64/8 heads")
+            out.append({k: r[k] for k in ("rho_ppm", "window", "us_per_call", "us_per_token_64_layers",
+                                          "algorithmic_bytes_per_call", "roofline", "device_error_word")})
+    return out
 
 
 def run_prefill_case(args, local):
@@ -412,38 +430,120 @@ def decode_traffic():
     return None
 
 
-def make_inputs(device, n_layers, seed=1001):
-    """Synthetic per-layer BF16 caches and per-token inputs (Llama-shaped)."""
+def make_inputs(device, n_layers, seed=1001, batch=B, hq=HQ, ctx=CTX):
+    """Synthetic per-layer BF16 caches and per-token inputs (Llama-shaped by
+    default: 3 outlier key channels x8, 2% planted vertical-line keys 4u +
+    noise, queries N(0, 1) + 2u); ``batch``, ``hq`` and ``ctx`` select other
+    shapes of the same recipe.  The period's tokens are the cache rows
+    ctx - 64 .. ctx - 1."""
     import torch
     g = torch.Generator(device=device)
     g.manual_seed(seed)
-    P = CTX - WINDOW
+    l0 = ctx - PERIOD
+    P = ctx - WINDOW
     k_srcs, v_srcs = [], []
-    q_tail = torch.empty(n_layers, B, HQ, 64, D, dtype=torch.bfloat16, device=device)
+    q_tail = torch.empty(n_layers, batch, hq, 64, D, dtype=torch.bfloat16, device=device)
     us = []
     for li in range(n_layers):
-        u = torch.randn(B, HKV, D, generator=g, device=device)
+        u = torch.randn(batch, HKV, D, generator=g, device=device)
         u = u / u.norm(dim=-1, keepdim=True)
         us.append(u)
-        k = torch.randn(B, HKV, CTX, D, generator=g, device=device)
+        k = torch.randn(batch, HKV, ctx, D, generator=g, device=device)
         ch = torch.randperm(D, generator=g, device=device)[:3]
         k[:, :, :, ch] *= 8.0                                   # 3 outlier channels
         ns = int(0.02 * P)                                      # 2% planted vertical lines
-        for h in range(HKV):
-            pos = torch.randperm(P, generator=g, device=device)[:ns]
-            k[0, h, pos] += 4.0 * u[0, h]
+        for bb in range(batch):
+            for h in range(HKV):
+                pos = torch.randperm(P, generator=g, device=device)[:ns]
+                k[bb, h, pos] += 4.0 * u[bb, h]
         k_srcs.append(k.to(torch.bfloat16))
-        v_srcs.append(torch.randn(B, HKV, CTX, D, generator=g, device=device).to(torch.bfloat16))
-        uq = u.repeat_interleave(HQ // HKV, dim=1)
-        q_tail[li] = (torch.randn(B, HQ, 64, D, generator=g, device=device) + 2.0 * uq[:, :, None]).to(torch.bfloat16)
-    q_tok = torch.empty(PERIOD, n_layers, B, HQ, D, dtype=torch.bfloat16, device=device)
+        del k
+        v_srcs.append(torch.randn(batch, HKV, ctx, D, generator=g, device=device).to(torch.bfloat16))
+        uq = u.repeat_interleave(hq // HKV, dim=1)
+        q_tail[li] = (torch.randn(batch, hq, 64, D, generator=g, device=device) + 2.0 * uq[:, :, None]).to(
+            torch.bfloat16)
+    q_tok = torch.empty(PERIOD, n_layers, batch, hq, D, dtype=torch.bfloat16, device=device)
     for li in range(n_layers):
-        uq = us[li].repeat_interleave(HQ // HKV, dim=1)
-        q_tok[:, li] = (torch.randn(PERIOD, B, HQ, D, generator=g, device=device) + 2.0 * uq[None]).to(torch.bfloat16)
-    # the tokens appended during the period are the cache rows L0 .. L0+63
-    k_tok = torch.stack([k[:, :, L0:L0 + PERIOD].permute(2, 0, 1, 3) for k in k_srcs], dim=1).contiguous()
-    v_tok = torch.stack([v[:, :, L0:L0 + PERIOD].permute(2, 0, 1, 3) for v in v_srcs], dim=1).contiguous()
+        uq = us[li].repeat_interleave(hq // HKV, dim=1)
+        q_tok[:, li] = (torch.randn(PERIOD, batch, hq, D, generator=g, device=device) + 2.0 * uq[None]).to(
+            torch.bfloat16)
+    # the tokens appended during the period are the cache rows l0 .. l0+63
+    k_tok = torch.stack([k[:, :, l0:l0 + PERIOD].permute(2, 0, 1, 3) for k in k_srcs], dim=1).contiguous()
+    v_tok = torch.stack([v[:, :, l0:l0 + PERIOD].permute(2, 0, 1, 3) for v in v_srcs], dim=1).contiguous()
     return k_srcs, v_srcs, q_tail, q_tok, k_tok, v_tok
+
+
+def period_bytes(ctx, batch=B, hq=HQ, q_row=160):
+    """Mean algorithmic bytes of the decode calls of one 64-token period
+    at context ``ctx`` (the cache frozen at ctx - 64, re-selected at ctx)."""
+    def call(n_q, n_vl, n_tail):
+        return batch * (HKV * (n_q * q_row + (n_vl + n_tail) * 512) + 2 * hq * D * 2)
+    P0 = ctx - PERIOD - WINDOW
+    k0 = -(-P0 * RHO_PPM // 1_000_000)
+    tot = sum(call(P0 - k0, k0, WINDOW + t + 1) for t in range(PERIOD - 1))
+    P = ctx - WINDOW
+    k = -(-P * RHO_PPM // 1_000_000)
+    return (tot + call(P - k, k, WINDOW)) / PERIOD
+
+
+def period_measure(dev, ctx, n_layers, batch=B, hq=HQ, steps=2, warmup=2, prefetch=True, seed=1011,
+                   model_layers=None):
+    """One configuration's 64-token re-selection period (fused decode steps,
+    then append + re-selection + rebuild + attention at the last token) over
+    ``n_layers`` distinct layers, timed with CUDA events: µs per token per
+    layer, the decode calls' own time and HBM roofline, and the share of the
+    period spent outside the decode calls (the maintenance)."""
+    import torch
+    import hybrid_precision_quantized_gb300 as hyq
+    from hybrid_precision_quantized_gb300.runner import PeriodRunner
+    cfg = hyq.make_config(batch, hq, HKV, capacity=ctx, window=WINDOW, period=PERIOD, rho_ppm=RHO_PPM)
+    k_srcs, v_srcs, q_tail, q_tok, k_tok, v_tok = make_inputs(dev, n_layers, seed, batch, hq, ctx)
+    run = PeriodRunner(cfg, k_srcs, v_srcs, ctx - PERIOD, dev, prefetch_next=prefetch)
+    run.q_tok.copy_(q_tok)
+    run.k_tok.copy_(k_tok)
+    run.v_tok.copy_(v_tok)
+    run.freeze(q_tail)
+    run.capture()
+    for _ in range(warmup):
+        run.run_period()
+    torch.cuda.synchronize()
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(PERIOD)]
+          for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for st in range(steps):
+        run.run_period(ev[st])
+    t1.record()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    dec_us = sum(a.elapsed_time(b) for row in ev for a, b in row) * 1e3 / (steps * PERIOD * n_layers)
+    value = ms * 1e3 / (PERIOD * n_layers)
+    nbytes = period_bytes(ctx, batch, hq)
+    peak, kind = measured_peaks()
+    gbs = nbytes / (dec_us * 1e-6) / 1e9
+    err = max(hyq.hyq_read_device_error(l.err()) for l in run.layers)
+    res = {"context": ctx, "batch": batch, "layers": n_layers, "us_per_token_layer": value,
+           "decode_us_per_call": dec_us, "maintenance_share": 1.0 - dec_us / value,
+           "algorithmic_bytes_per_call": nbytes, "cache_bytes_all_layers": nbytes * n_layers,
+           "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                        "peak_source": f"{kind} hbm_gbs"},
+           "device_error_word": err}
+    if model_layers:
+        res[f"us_per_token_{model_layers}_layers"] = value * model_layers
+        res[f"us_per_sequence_token_{model_layers}_layers"] = value * model_layers / batch
+    del run, k_srcs, v_srcs
+    torch.cuda.empty_cache()
+    return res
+
+
+def context_sweep(dev, contexts=(1024, 4096, 16384)):
+    """The Llama-shaped period at shorter contexts, each over enough distinct
+    layers that one replay's caches exceed ~2x the 129 MB L2 (at least 32)."""
+    out = []
+    for ctx in contexts:
+        nl = int(min(160, max(32, -(-2 * 129e6 // period_bytes(ctx)))))
+        out.append(period_measure(dev, ctx, nl))
+    return out
 
 
 def oracle_timing(threads, budget_s, min_calls=2, warmup=0):
@@ -657,8 +757,14 @@ def run_ours(args, rank, world, local):
     achieved = bytes_per / (dec_us * 1e-6) / 1e9
     peak, peak_kind = measured_peaks()
     base = None if args.no_baseline else cpu_baseline()
-    prefill = None if args.no_prefill else prefill_measure(dev, [CTX], reps=5)
+    prefill = None if args.no_prefill else prefill_measure(dev, [8192, CTX], reps=5)
     batched = None if args.no_batched else batched_measure(dev)
+    sweep = None if args.no_sweep else context_sweep(dev)
+    b16_period = None if args.no_sweep else {
+        "workload": "qwen3-8b-shaped batched decode, B16, 32/8 heads, d128, 32K ctx, W128, rho 5%, K4V4 G32; "
+                    "64-token period with re-selection and rebuild at its last token; 4 distinct layers",
+        **period_measure(dev, CTX, 4, batch=16, hq=HQ, steps=2, warmup=1, seed=1013, model_layers=36)}
+    grid = None if args.no_grid else qwen32b_grid(dev)
     batched32 = None if args.no_batched else batched_measure(
         dev, batch=4, hq=64, n_layers=6, seed=1004, model_layers=64, heavy_tail=True,
         workload="qwen3-32b-shaped decode attention, B4, 64/8 heads, d128, 32K ctx, W128, rho 5%, K4V4 G32, "
@@ -688,10 +794,13 @@ def run_ours(args, rank, world, local):
         "cpu_baseline": base,
         "batched": batched,
         "batched_qwen32b": batched32,
+        "context_sweep": sweep,
+        "batched_period": b16_period,
+        "qwen32b_grid": grid,
         "frozen": frozen,
         "mass_selection": mass,
         "widths": widths,
-        "prefill": ({"workload": "llama3.1-8b-shaped causal prefill, B1, 32/8 heads, d128, 32K, W128, rho 5% "
+        "prefill": ({"workload": "llama3.1-8b-shaped causal prefill, B1, 32/8 heads, d128, 8K and 32K, W128, rho 5% "
                                  "(pack + main kernel; window fixed: hyq_prefill_attention, band: "
                                  "hyq_prefill_attention_band)",
                      "flops": "4 d HQ L(L+1)/2", "l2": "256 MB flush before every timed call",

@@ -835,6 +835,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(
   const bool pf_warp = next_cnt_loaded && warp == kWarps - 1;
   auto issue_prefetch = [&]() {
     const NextCounts nxc = clamp_next_counts(nxraw, nblk_cap, cap_vl, cap_tail);
+    // Only a next layer that fits comfortably in L2 (its estimate from this
+    // sequence's counts below half of the 129 MB) is worth prefetching; a
+    // larger one would only evict lines before they are used.
+    const double next_bytes = (double)gridDim.z * HKV *
+                              ((double)((nxc.nq + 15) >> 4) * kTile + (double)(nxc.nvl + nxc.ntail) * 4 * HYQ_D);
+    if (next_bytes > 64.0 * 1024 * 1024) return;
     prefetch_next_tiles<kTile>(sa, nxc, bh, split, S, nblk_cap, lane);
     prefetch_next_rows(sa, nxc, bh, split, S, cap_vl, cap_tail, lane);
   };

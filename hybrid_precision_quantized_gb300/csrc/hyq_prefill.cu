@@ -128,14 +128,16 @@ __device__ __forceinline__ float bf16_at(const uint4& u, int e) {
 // Codes of the exact quotient x / s (x a BF16 value, s > 0 the FP32 scale, or
 // s = 0 for an all-zero tile).  t = fl32(x / s) is correctly rounded and
 // monotone in x / s, so rounding t to the code grid gives the code of x / s
-// except when t itself is a midpoint of that grid; then the sign of
-// x - t * s, exact in float64 (t has at most 9 significant bits, s 24),
-// decides, and an exact tie keeps the even code.
+// except when t itself is a midpoint of that grid; then the sign of x - t s
+// decides (an exact tie keeps the even code).  One fused multiply-add gives
+// it: t s is formed exactly (t has at most 9 significant bits, s 24) and the
+// difference is rounded once, which keeps its sign (scales below the FP32
+// normal range, tiles whose maximum is under c_B 2^-126, aside).
 __device__ __forceinline__ float quotient(float x, float s) { return s > 0.f ? __fdiv_rn(x, s) : 0.f; }
 
-__device__ __noinline__ float past_midpoint(float x, float s, float t, float below, float above, float even) {
-  const double d = (double)x - (double)t * (double)s;
-  return d > 0.0 ? above : d < 0.0 ? below : even;
+__device__ __forceinline__ float past_midpoint(float x, float s, float t, float below, float above, float even) {
+  const float d = fmaf(-t, s, x);
+  return d > 0.f ? above : d < 0.f ? below : even;
 }
 
 // INT8: the nearest integer to x / s, ties to even, clamped to +-127.
@@ -159,7 +161,7 @@ __device__ __forceinline__ float code_f8(float x, float s) {
   float h = 0.f;
   if (a < 0.015625f) {
     const float u = a * 1024.f;  // exact
-    if (u == floorf(u) && fmodf(u, 2.f) == 1.f) h = 0.0009765625f;
+    if (u == floorf(u) && (__float2int_rz(u) & 1)) h = 0.0009765625f;
   } else if ((__float_as_uint(a) & 0x000FFFFFu) == 0x00080000u) {
     h = __uint_as_float(__float_as_uint(a) & 0xFF800000u) * 0.0625f;  // 2^(E-4)
   }

@@ -74,12 +74,12 @@ constexpr float kNearTie = 0.5f - 0.000244140625f;  // 1/2 - 2^-12
 // Exact decision near the midpoint k + 1/2, k = floor(t): in float64 the
 // midpoint z + (k + 1/2) s is exact (s and z are FP16 values: a multiple of
 // 2^-25 below 2^25 in magnitude) and the sign of x minus it is exact.
-__device__ __noinline__ float exact_code(float x, float z, float s, float t) {
+__device__ __forceinline__ float exact_code(float x, float z, float s, float t) {
   const float k = floorf(t);
   const double d = (double)x - ((double)z + ((double)k + 0.5) * (double)s);
   if (d > 0.0) return k + 1.f;
   if (d < 0.0) return k;
-  return fmodf(k, 2.f) == 0.f ? k : k + 1.f;  // a tie: the even one
+  return (__float2int_rz(k) & 1) ? k + 1.f : k;  // a tie: the even one
 }
 
 // Bit patterns kMagicBits + code of the two BF16 elements of w (x: low half),
