@@ -408,6 +408,10 @@ __device__ __forceinline__ void q_tile(const uint8_t* tb, int lane, int vr, cons
   // groups 2(t&1), 2(t&1)+1 (high parts of the sums for t < 2, remainders
   // for t >= 2), so a lane passes the zero pair of those groups.
   mma_f16(lg, (t & 1) ? ma.w : ma.z, (t & 1) ? mb.w : mb.z, 0u, 0u, qc.bz, 0u);
+  // A vertical-line position (held in BF16 elsewhere) has NaN key steps in
+  // the stream: its logit is NaN, and the row is left out.
+#pragma unroll
+  for (int i = 0; i < 4; ++i) lg[i] = lg[i] != lg[i] ? -INFINITY : lg[i];
   if (vr < 16) {
     if (g >= vr) lg[0] = lg[1] = -INFINITY;
     if (g + 8 >= vr) lg[2] = lg[3] = -INFINITY;

@@ -71,6 +71,13 @@ __device__ __forceinline__ uint32_t hi32(uint64_t v) { return (uint32_t)(v >> 32
 // integer; those elements are decided exactly (exact_code).
 constexpr float kNearTie = 0.5f - 0.000244140625f;  // 1/2 - 2^-12
 
+// Step of a group: the smallest FP16 value s with qmax s >= mx - mn (the
+// subtraction, the division and the FP16 conversion all round up, which gives
+// exactly that value: qmax h is exact in FP32 for every FP16 h).
+__device__ __forceinline__ __half group_step(float mn, float mx, float qmax) {
+  return __float2half_ru(__fdiv_ru(__fsub_ru(mx, mn), qmax));
+}
+
 // Exact decision near the midpoint k + 1/2, k = floor(t): in float64 the
 // midpoint z + (k + 1/2) s is exact (s and z are FP16 values: a multiple of
 // 2^-25 below 2^25 in magnitude) and the sign of x minus it is exact.
@@ -212,7 +219,7 @@ __device__ void build_block(BuildSmem& sm, const __nv_bfloat16* kbase, const __n
     if (sm.keep[row]) continue;
     const float qmax = (T == 0 ? BK : BV) == 8 ? 255.f : 15.f;
     const float mn = sm.mn[T][row][q], mx = sm.mx[T][row][q];
-    __half sh = __float2half_ru(__fdiv_ru(__fsub_ru(mx, mn), qmax));
+    __half sh = group_step(mn, mx, qmax);
     __half zh = __float2half_rn(mn);
     float s32 = __half2float(sh), z32 = __half2float(zh);
     if (sm.nan[T][row][q] || isinf(s32) || isinf(z32)) {
@@ -387,92 +394,133 @@ __device__ void build_block(BuildSmem& sm, const __nv_bfloat16* kbase, const __n
   }
 }
 
-// Source position of stream row r: the r-th position of [0, P) not in idx
-// (idx strictly ascending).  With f(i) = idx[i] - i non-decreasing, the
-// number of idx entries before that position is #{i : f(i) <= r}.
-__device__ __forceinline__ int32_t stream_pos(int32_t r, const int32_t* idx, int32_t k) {
-  int32_t lo = 0, hi = k;
-  while (lo < hi) {
-    int32_t mid = (lo + hi) >> 1;
-    if (idx[mid] - mid <= r) lo = mid + 1;
-    else hi = mid;
-  }
-  return r + lo;
-}
+// The 4-bit stream holds every position that has left the BF16 tail, at
+// row = position; a vertical-line position keeps its codes but its four key
+// steps hold FP16 NaN, which the decode kernel reads as "skip this row".
+// A rebuild therefore quantises only the positions [NQ, P) not in the stream
+// yet, and moves the NaN marks from the old vertical-line set to the new one.
 
-// Warp-cooperative #{i < k : idx[i] - i <= x} for a strictly ascending idx
-// (so idx[i] - i is non-decreasing): 32 probes per round.
-__device__ __forceinline__ int32_t warp_count_f_le(const int32_t* idx, int32_t k, int32_t x, int lane) {
-  int32_t lo = 0, hi = k;  // f(i) <= x for i < lo, f(i) > x for i >= hi
-  while (lo < hi) {
-    const int32_t step = (hi - lo + 31) >> 5;
-    const int32_t i = lo + lane * step;
-    const bool le = i < hi && __ldg(idx + i) - i <= x;
-    const int cnt = __popc(__ballot_sync(0xffffffffu, le));
-    if (cnt == 0) {
-      hi = lo;
-    } else {
-      const int32_t nlo = lo + (cnt - 1) * step + 1;
-      hi = min(hi, lo + cnt * step);
-      lo = nlo;
-    }
-  }
-  return lo;
-}
-
-constexpr int kWinF = 256;  // vertical-line entries a block resolves in shared memory
-
-// grid (blocks of the new stream, HKV, B)
+// Rebuild, step 1: quantise stream rows [NQ, P) from the BF16 source (rows
+// already in the stream are kept: their positions and codes do not change).
+// Block-row loop over the 64-row blocks from NQ / 64.  grid (n, HKV, B)
 template <int BK, int BV>
-__global__ void __launch_bounds__(kThreads) rebuild_blocks_kernel(
-    const __nv_bfloat16* __restrict__ k_src, const __nv_bfloat16* __restrict__ v_src, int32_t ld,
-    int32_t P, const int32_t* __restrict__ idx, int32_t k, uint8_t* __restrict__ qblocks,
-    int32_t nblk_cap, int32_t* err) {
+__global__ void __launch_bounds__(kThreads) rebuild_rows_kernel(
+    const __nv_bfloat16* __restrict__ k_src, const __nv_bfloat16* __restrict__ v_src, int32_t ld, int32_t P,
+    hyq_layout lay, int32_t nblk_cap) {
   __shared__ __align__(16) BuildSmem sm;
-  const int bi = blockIdx.x, h = blockIdx.y, b = blockIdx.z, HKV = gridDim.y;
+  const int h = blockIdx.y, b = blockIdx.z, HKV = gridDim.y;
   const size_t bh = (size_t)b * HKV + h;
-  const int32_t nq = P - k;
-  const int32_t* idx_bh = idx ? idx + bh * k : nullptr;
-  // Stream row R sits at position R + #{i : idx[i] - i <= R}.  Warps 0 and 1
-  // find that count at the block's first and last row; the entries in
-  // between go to shared memory, where every row counts its own.
-  __shared__ int32_t s_c[2];
-  __shared__ int32_t s_f[kWinF];
-  const int32_t r0 = bi * kRows, r1 = min(nq, r0 + kRows) - 1;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (k > 0 && warp < 2) {
-    const int32_t c = warp_count_f_le(idx_bh, k, warp == 0 ? r0 - 1 : r1, lane);
-    if (lane == 0) s_c[warp] = c;
+  const int32_t nq_cnt = lay.counts[(size_t)b * HYQ_COUNTS + HYQ_CNT_NQ];
+  const int32_t nq0 = min(max(nq_cnt, 0), P);
+  const int32_t nblocks = (P + kRows - 1) / kRows - nq0 / kRows;
+  for (int32_t i = blockIdx.x; i < nblocks; i += gridDim.x) {
+    // append_body handles block nq0 / 64 + blockIdx.x; shift the source so
+    // that its row (r - nq0) is position r
+    BuildSmem& s2 = sm;
+    const int32_t bi = nq0 / kRows + i;
+    if (threadIdx.x < kRows) {
+      const int32_t row = bi * kRows + threadIdx.x;
+      s2.keep[threadIdx.x] = row < nq0;
+      s2.pos[threadIdx.x] = (row >= nq0 && row < P) ? row - nq0 : -1;
+    }
+    __syncthreads();
+    build_block<BK, BV>(s2, k_src + (bh * ld + nq0) * HYQ_D, v_src + (bh * ld + nq0) * HYQ_D,
+                        lay.qblocks + (bh * nblk_cap + bi) * (size_t)QFmt<BK, BV>::kBlock, bi * kRows < nq0, lay.err);
+    __syncthreads();
   }
+}
+
+// Rebuild, step 2: NaN key steps for the new vertical-line positions; the
+// true steps (recomputed from the BF16 key row, as step 1 computes them) for
+// positions of the old set that left it and stay in the stream.  grid
+// (kMarkChunks, HKV, B): block c takes the c-th share of the old and of the
+// new list; it reads the old set and counts before step 3 replaces them.
+// The new list is staged in shared memory (dynamic, k ints; a list too long
+// for it is searched in global memory).
+constexpr int kMarkChunks = 8;
+constexpr int kMarkSmemInts = 11776;  // 46 KB: with the static arrays under the 48 KB default
+
+template <int BK, int BV>
+__global__ void __launch_bounds__(kThreads) rebuild_marks_kernel(
+    const __nv_bfloat16* __restrict__ k_src, int32_t ld, int32_t P, const int32_t* __restrict__ idx, int32_t k,
+    hyq_layout lay, int32_t cap_vl, int32_t nblk_cap) {
+  using F = QFmt<BK, BV>;
+  extern __shared__ int32_t s_new[];
+  __shared__ int32_t s_leave[kThreads];
+  __shared__ int s_nleave;
+  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z, HKV = gridDim.y;
+  const size_t bh = (size_t)b * HKV + h;
+  const int32_t* cnt = lay.counts + (size_t)b * HYQ_COUNTS;
+  const int32_t nq_old = min(max(cnt[HYQ_CNT_NQ], 0), P), nvl_old = min(max(cnt[HYQ_CNT_NVL], 0), cap_vl);
+  const int32_t* inew = idx + bh * k;
+  const int32_t* iold = lay.vl_idx + bh * cap_vl;
+  uint8_t* stream = lay.qblocks + bh * (size_t)nblk_cap * F::kBlock;
+  auto kmeta = [&](int32_t pos) {  // the four key steps of stream row pos
+    return reinterpret_cast<__half*>(stream + (pos >> 4) * F::kTile + F::kKMeta + 16 * (pos & 15));
+  };
+  const bool staged = k <= kMarkSmemInts;
+  if (staged)
+    for (int32_t i = threadIdx.x; i < k; i += kThreads) s_new[i] = __ldg(inew + i);
+  if (threadIdx.x == 0) s_nleave = 0;
   __syncthreads();
-  const int32_t c0 = k > 0 ? s_c[0] : 0, m = k > 0 ? s_c[1] - s_c[0] : 0;
-  if (m <= kWinF)
-    for (int i = threadIdx.x; i < m; i += kThreads) s_f[i] = __ldg(idx_bh + c0 + i) - (c0 + i);
-  __syncthreads();
-  if (threadIdx.x < kRows) {
-    const int32_t r = bi * kRows + threadIdx.x;
-    int32_t p = -1;
-    if (r < nq) {
-      if (k == 0) {
-        p = r;
-      } else if (m <= kWinF) {
-        int32_t c = c0;
-        for (int i = 0; i < m; ++i) c += s_f[i] <= r;
-        p = r + c;
-      } else {
-        p = stream_pos(r, idx_bh, k);  // a run of more than kWinF vertical lines
+  const int32_t* list = staged ? s_new : inew;
+  // this block's old entries, one per thread per pass: leaving the set?
+  const int32_t o0 = (int32_t)((int64_t)nvl_old * c / kMarkChunks), o1 = (int32_t)((int64_t)nvl_old * (c + 1) / kMarkChunks);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float qmax = BK == 8 ? 255.f : 15.f;
+  for (int32_t base = o0; base < o1; base += kThreads) {
+    const int32_t i = base + threadIdx.x;
+    if (i < o1) {
+      const int32_t pos = __ldg(iold + i);
+      int32_t lo = 0, hi = k;
+      while (lo < hi) {
+        const int32_t m = (lo + hi) >> 1;
+        if (list[m] < pos) lo = m + 1;
+        else hi = m;
       }
-      if (p < 0 || p >= P) {  // only possible for an invalid idx list
-        hyq_set_err(err, HYQ_DEVERR_INDEX);
-        p = min(max(p, 0), P - 1);
+      if (pos >= 0 && pos < nq_old && !(lo < k && list[lo] == pos)) s_leave[atomicAdd(&s_nleave, 1)] = pos;
+    }
+    __syncthreads();
+    // restore the leaving rows: a warp per row, four rows' loads in flight per warp
+    const int nl = s_nleave;
+    for (int r0 = 4 * warp; r0 < nl; r0 += 4 * kWarps) {
+      uint2 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        v[u] = r0 + u < nl ? __ldg(reinterpret_cast<const uint2*>(k_src + (bh * ld + s_leave[r0 + u]) * HYQ_D) + lane)
+                           : make_uint2(0, 0);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        // lane: elements 4 lane .. 4 lane + 3 of the key row; group lane / 8
+        const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&v[u]);
+        __nv_bfloat162 mn2 = __hmin2_nan(p2[0], p2[1]), mx2 = __hmax2_nan(p2[0], p2[1]);
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+          mn2 = __hmin2_nan(mn2, __shfl_xor_sync(0xffffffffu, mn2, o));
+          mx2 = __hmax2_nan(mx2, __shfl_xor_sync(0xffffffffu, mx2, o));
+        }
+        if ((lane & 7) == 0 && r0 + u < nl) {
+          const float2 fm = __bfloat1622float2(mn2), fx = __bfloat1622float2(mx2);
+          __half sh = group_step(fminf(fm.x, fm.y), fmaxf(fx.x, fx.y), qmax);
+          if (isinf(__half2float(sh)) || isnan(fm.x) || isnan(fm.y)) sh = __float2half_rn(0.f);  // as step 1 stores it
+          kmeta(s_leave[r0 + u])[lane >> 3] = sh;
+        }
       }
     }
-    sm.pos[threadIdx.x] = p;
-    sm.keep[threadIdx.x] = 0;
+    __syncthreads();
+    if (threadIdx.x == 0) s_nleave = 0;
+    __syncthreads();
   }
-  __syncthreads();
-  build_block<BK, BV>(sm, k_src + bh * ld * HYQ_D, v_src + bh * ld * HYQ_D,
-                      qblocks + (bh * nblk_cap + bi) * (size_t)QFmt<BK, BV>::kBlock, false, err);
+  // this block's share of the new set: NaN steps
+  const __half nanh = __ushort_as_half((unsigned short)0x7E00);
+  const int32_t n0 = (int32_t)((int64_t)k * c / kMarkChunks), n1 = (int32_t)((int64_t)k * (c + 1) / kMarkChunks);
+  for (int32_t i = n0 + threadIdx.x; i < n1; i += kThreads) {
+    const int32_t pos = list[i];
+    if (pos >= 0 && pos < P) {
+      __half* m = kmeta(pos);
+      m[0] = m[1] = m[2] = m[3] = nanh;
+    }
+  }
 }
 
 // Vertical-line gather, BF16 tail copy and counters.  One warp per row:
@@ -511,7 +559,7 @@ __global__ void __launch_bounds__(kThreads) rebuild_gather_kernel(
   }
   if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0) {
     int32_t* cnt = lay.counts + (size_t)b * HYQ_COUNTS;
-    cnt[HYQ_CNT_NQ] = P - k;
+    cnt[HYQ_CNT_NQ] = P;
     cnt[HYQ_CNT_NVL] = k;
     cnt[HYQ_CNT_NTAIL] = ntail;
     cnt[HYQ_CNT_LEN] = L;
@@ -690,15 +738,20 @@ cudaError_t hyq_launch_rebuild(const hyq_config* c, const void* k_src, const voi
                                int32_t ld, int32_t L, const int32_t* idx, int32_t k,
                                const hyq_layout* lay, cudaStream_t s) {
   int32_t P = L - c->window > 0 ? L - c->window : 0;
-  int32_t nq = P - k;
   int32_t nblk = hyq_nblk(c);
   const __nv_bfloat16* kk = static_cast<const __nv_bfloat16*>(k_src);
   const __nv_bfloat16* vv = static_cast<const __nv_bfloat16*>(v_src);
-  if (nq > 0) {
-    dim3 grid((nq + HYQ_QBLOCK_ROWS - 1) / HYQ_QBLOCK_ROWS, c->num_kv_heads, c->batch);
+  if (P > 0) {
+    // the rows still to quantise are unknown here (the stream length is on the
+    // device): a few blocks per (b, KV head) loop over them; a first rebuild
+    // of a long context gets more
+    const int32_t blocks = (P + HYQ_QBLOCK_ROWS - 1) / HYQ_QBLOCK_ROWS;
+    dim3 grid(blocks < 8 ? blocks : (blocks / 8 < 8 ? 8 : blocks / 8), c->num_kv_heads, c->batch);
     with_widths(c, [&](auto bk, auto bv) {
-      rebuild_blocks_kernel<bk.value, bv.value><<<grid, kThreads, 0, s>>>(kk, vv, ld, P, idx, k, lay->qblocks, nblk,
-                                                                          lay->err);
+      rebuild_rows_kernel<bk.value, bv.value><<<grid, kThreads, 0, s>>>(kk, vv, ld, P, *lay, nblk);
+      const size_t smem = k <= kMarkSmemInts ? (size_t)k * sizeof(int32_t) : 0;
+      rebuild_marks_kernel<bk.value, bv.value><<<dim3(kMarkChunks, c->num_kv_heads, c->batch), kThreads, smem, s>>>(
+          kk, ld, P, idx, k, *lay, hyq_vl_stride(c), nblk);
       return 0;
     });
     cudaError_t e = cudaGetLastError();

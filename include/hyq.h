@@ -127,8 +127,11 @@ typedef struct {
  * Sizes in bytes come from hyq_layout_sizes(); all pointers are device
  * pointers, 256-byte aligned.
  *
- *   qblocks  [B][HKV][nblk][HYQ_QBLOCK_BYTES_BITS(B_K, B_V)]  quantised stream, positions of the
- *            non-window prefix that are not vertical-line, ascending
+ *   qblocks  [B][HKV][nblk][HYQ_QBLOCK_BYTES_BITS(B_K, B_V)]  quantised stream: row r is
+ *            position r, for every position r < NQ that has left the BF16 tail;
+ *            the rows of vertical-line positions keep their codes but their
+ *            four key steps are FP16 NaN (decode leaves those rows out; their
+ *            values are the BF16 vertical-line rows)
  *   vl_k/v   bf16 [B][HKV][cap_vl][128]  vertical-line rows, ascending position
  *   vl_idx   int32 [B][HKV][cap_vl]      their positions
  *   tail_k/v bf16 [B][HKV][cap_tail][128] positions [P, L) in order
@@ -151,10 +154,10 @@ typedef struct {
 } hyq_layout;
 
 #define HYQ_COUNTS 8
-#define HYQ_CNT_NQ 0       /* rows in the 4-bit stream                     */
+#define HYQ_CNT_NQ 0       /* rows in the 4-bit stream (positions 0..NQ-1) */
 #define HYQ_CNT_NVL 1      /* vertical-line rows                           */
 #define HYQ_CNT_NTAIL 2    /* BF16 tail rows                               */
-#define HYQ_CNT_LEN 3      /* context length L = NQ + NVL + NTAIL          */
+#define HYQ_CNT_LEN 3      /* context length L = NQ + NTAIL                */
 #define HYQ_CNT_RING_N 4   /* valid entries in q_ring (<= period)          */
 #define HYQ_CNT_RING_POS 5 /* next q_ring slot                             */
 
@@ -202,8 +205,8 @@ hyq_status hyq_layout_reset(const hyq_config *cfg, const hyq_layout *lay, hyq_st
  * qmax = 2^B - 1 (B = bits_k for K, bits_v for V: 15 or 255):
  *   s = FP16 value of (mx - mn) / qmax (exact quotient) rounded toward +inf,
  *   z = FP16 value of mn rounded to nearest even,
- *   c = clamp(rint((x - z) * r), 0, qmax) in float32 with r = 1/s rounded to
- *       nearest (c = 0 when s = 0).
+ *   c = the integer in [0, qmax] nearest to (x - z) / s, ties to even (the
+ *       grid point z + c s nearest to x; c = 0 when s = 0), decided exactly.
  * A group with a non-finite s or z gets zero codes, s = z = 0 and sets
  * HYQ_DEVERR_QUANT_RANGE.  Rows that would pass the capacity are dropped and
  * set HYQ_DEVERR_COUNT.  Updates NQ and LEN.
@@ -219,7 +222,7 @@ hyq_status hyq_quantize_append(const hyq_config *cfg, const void *k_rows, const 
  * quantised exactly as hyq_quantize_append does and appended to the 4-bit
  * stream after its NQ rows, and the last W tail rows move to the front of the
  * tail: NQ += m, NTAIL -= m, LEN, the vertical-line rows and the proxy ring
- * unchanged.  The partition afterwards is that of hyq_rebuild at LEN with the
+ * unchanged.  The layout afterwards is that of hyq_rebuild at LEN with the
  * same index list.  A sequence whose counters are out of range or whose
  * stream has no room for the m rows is left unchanged and sets
  * HYQ_DEVERR_COUNT.  Three launches, no workspace.
@@ -265,12 +268,18 @@ hyq_status hyq_select_vertical_mass(const hyq_config *cfg, const void *q_proxy, 
 
 /*
  * Build a layer's hybrid cache for context length L (Algorithm 4, with the
- * vertical-line set re-chosen): the 4-bit stream holds the positions of
- * [0, P) \ idx in ascending order, quantised as in hyq_quantize_append; the
- * vertical-line buffers hold the BF16 rows of idx; the tail holds [P, L).
+ * vertical-line set re-chosen): the 4-bit stream holds the positions [0, P),
+ * row = position, quantised as in hyq_quantize_append, those of idx marked
+ * (NaN key steps); the vertical-line buffers hold the BF16 rows of idx; the
+ * tail holds [P, L).  Rows already in the stream (positions below its NQ)
+ * are kept: only [NQ, P) is quantised, and the marks move from the previous
+ * vertical-line set to idx (a position leaving the set gets its key steps
+ * back from its BF16 row), so a re-selection costs O(64 + k), not O(P).
+ * The stream must therefore hold the same sequence as k_src: reset the
+ * layout (hyq_layout_reset) before building it for another one.
  *   k_src, v_src  device bf16 [B][HKV][ld][128]
  *   idx           device int32 [B][HKV][k], strictly ascending in [0, P)
- * Sets NQ = P - k, NVL = k, NTAIL = L - P, LEN = L.  Leaves q_ring alone.
+ * Sets NQ = P, NVL = k, NTAIL = L - P, LEN = L.  Leaves q_ring alone.
  * An idx list that is not strictly ascending within [0, P) sets
  * HYQ_DEVERR_INDEX (the output is then unspecified but in bounds).
  */

@@ -128,7 +128,7 @@ def test_decode_full_size_llama_32k(hyq):
     c = decode_case(1001, 1, 32, 8, 32768, window=128, n_proxy=64, sink_frac=0.02, outlier_channels=3)
     got, want, (cfg, layer, _, _) = build_and_decode(c, 32768, 128, 50_000, capacity=32768 + 64)
     cnt = layer.counts()[0].tolist()
-    assert cnt[:4] == [32640 - 1632, 1632, 128, 32768]
+    assert cnt[:4] == [32640, 1632, 128, 32768]
     assert_attention_close(got, want, what="32K")
 
 
@@ -147,7 +147,7 @@ def test_decode_qwen32b_shaped_sweep_sampled(hyq, ppm, W, sink_frac):
     got, idx_np, (cfg, layer, _, _) = decode_gpu(c, Lc, W, ppm, capacity=Lc + 64)
     P = prefix_len(Lc, W)
     k = idx_np.shape[-1]
-    assert layer.counts()[0].tolist()[:4] == [P - k, k, Lc - P, Lc]
+    assert layer.counts()[0].tolist()[:4] == [P, k, Lc - P, Lc]
     q, kk, vv = c.q.double().numpy(), c.k.double().numpy(), c.v.double().numpy()
     pairs, seed = sample_pairs(B, HKV, 3, f"qwen32b rho={ppm} W={W} sinks={sink_frac}")
     for b, kh in pairs:
@@ -422,7 +422,7 @@ def test_frozen_mode_age_tail(hyq):
     oracle quantiser) equal the partition at the new length with the frozen
     index set, and the attention matches the oracle over that partition."""
     from hybrid_precision_quantized_gb300 import hyq_age_tail, hyq_decode_step
-    from tests.test_gpu_quant import _check_stream
+    from tests.test_gpu_quant import _check_positional
     B, HQ, HKV, W, ppm, T = 2, 8, 2, 128, 50_000, 64
     L0, periods = 900, 2
     cap = L0 + periods * T
@@ -445,7 +445,7 @@ def test_frozen_mode_age_tail(hyq):
                             lay.c, out, ws, ks, vs, cap)
             Lc += 1
         torch.cuda.synchronize()
-        assert layer_counts(lay)[:3] == [L0 - W - k + (Lc - L0 - T), k, W + T]
+        assert layer_counts(lay)[:3] == [L0 - W + (Lc - L0 - T), k, W + T]
         # the last step's attention over the 4-bit stream of the last aging
         P_before = Lc - 1 - (W + T - 1)
         want = hybrid_decode(q.double().numpy(), k_np, v_np, Lc, P_before, idx_np)
@@ -454,12 +454,11 @@ def test_frozen_mode_age_tail(hyq):
         torch.cuda.synchronize()
         assert hyq_read_device_error(lay.err()) == 0
         P = Lc - W
-        assert layer_counts(lay)[:4] == [P - k, k, W, Lc]
+        assert layer_counts(lay)[:4] == [P, k, W, Lc]
         for b in range(B):
             for h in range(HKV):
-                qpos = np.setdiff1d(np.arange(P), idx_np[b, h])
-                _check_stream(lay, b, h, len(qpos), c.k[b, h, qpos].double().numpy(),
-                              c.v[b, h, qpos].double().numpy())
+                _check_positional(lay, b, h, P, c.k[b, h].double().numpy(), c.v[b, h].double().numpy(),
+                                  idx_np[b, h])
                 assert torch.equal(lay.tail_k()[b, h, :W].cpu(), c.k[b, h, P:Lc])
                 assert torch.equal(lay.tail_v()[b, h, :W].cpu(), c.v[b, h, P:Lc])
         q = torch.randn(B, HQ, 128, generator=g).to(torch.bfloat16)

@@ -31,6 +31,27 @@ def _check_stream(layer, b, h, n_rows, k_rows, v_rows):
         assert not kc_all[n_rows:(n_rows + 63) // 64 * 64].any()
 
 
+def _check_positional(layer, b, h, P, k_rows, v_rows, vl):
+    """The stream of (b, h) holds positions [0, P) at row = position, every
+    code, step and zero equal to the oracle quantiser's on those rows, except
+    that the vertical-line positions ``vl`` carry FP16 NaN as their key steps
+    (decode leaves them out)."""
+    bk, bv = layer.cfg.bits_k or 4, layer.cfg.bits_v or 4
+    blocks = layer.qblocks()[b, h].cpu().numpy()
+    kc, vc, ks, kz, vs, vz = unpack_qblocks(blocks, P, bk, bv)
+    ck, sk, zk = quantize(k_rows[:P], bk)
+    cv, sv, zv = quantize(v_rows[:P], bv)
+    vl = np.asarray(vl, np.int64)
+    assert np.array_equal(kc, ck) and np.array_equal(vc, cv), "codes differ"
+    assert np.array_equal(kz.view(np.uint16), zk.view(np.uint16)) and np.array_equal(vz.view(np.uint16),
+                                                                                      zv.view(np.uint16))
+    assert np.array_equal(vs.view(np.uint16), sv.view(np.uint16)), "value steps differ"
+    marked = np.zeros(P, bool)
+    marked[vl] = True
+    assert np.all(np.isnan(ks[marked].astype(np.float64))), "a vertical-line row is not marked"
+    assert np.array_equal(ks[~marked].view(np.uint16), sk[~marked].view(np.uint16)), "key steps differ"
+
+
 def test_quantize_append_bit_exact_two_appends(hyq):
     B, HQ, HKV = 2, 4, 2
     cfg = make_config(B, HQ, HKV, capacity=512, window=0)
@@ -101,13 +122,12 @@ def test_rebuild_matches_partition(hyq, B, HQ, HKV, Lc, W, ppm):
     torch.cuda.synchronize()
     assert hyq_read_device_error(layer.err()) == 0
     cnt = layer.counts().cpu().numpy()
-    assert cnt[:, :4].tolist() == [[P - k, k, Lc - P, Lc]] * B
+    assert cnt[:, :4].tolist() == [[P, k, Lc - P, Lc]] * B
     for b in range(B):
         for h in range(HKV):
-            qpos = np.setdiff1d(np.arange(P), idx_np[b, h])
-            if len(qpos):
-                _check_stream(layer, b, h, len(qpos), c.k[b, h, qpos].double().numpy(),
-                              c.v[b, h, qpos].double().numpy())
+            if P:
+                _check_positional(layer, b, h, P, c.k[b, h].double().numpy(), c.v[b, h].double().numpy(),
+                                  idx_np[b, h])
             assert torch.equal(layer.vl_k()[b, h, :k].cpu(), c.k[b, h, idx_np[b, h]])
             assert torch.equal(layer.vl_v()[b, h, :k].cpu(), c.v[b, h, idx_np[b, h]])
             assert np.array_equal(layer.vl_idx()[b, h, :k].cpu().numpy(), idx_np[b, h])
@@ -151,9 +171,8 @@ def test_rebuild_bit_exact_on_edge_groups(hyq):
     torch.cuda.synchronize()
     assert hyq_read_device_error(layer.err()) == 0
     for h in range(HKV):
-        qpos = np.setdiff1d(np.arange(P), idx_np[0, h])
-        _check_stream(layer, 0, h, len(qpos), k_rows[0, h, qpos].double().numpy(),
-                      v_rows[0, h, qpos].double().numpy())
+        _check_positional(layer, 0, h, P, k_rows[0, h].double().numpy(), v_rows[0, h].double().numpy(),
+                          idx_np[0, h])
 
 
 @pytest.mark.parametrize("bits", [(4, 4), (8, 8), (4, 8)])
@@ -186,3 +205,42 @@ def test_codes_at_planted_midpoints_bit_exact(hyq, bits):
     assert hyq_read_device_error(layer2.err()) == 0
     for h in range(HKV):
         _check_stream(layer2, 0, h, n1 + n2, k[0, h].double().numpy(), v[0, h].double().numpy())
+
+
+def test_rebuild_incremental_equals_fresh(hyq):
+    """A rebuild over a layout already built for a shorter context (the
+    re-selection every 64 tokens) quantises only the new positions and moves
+    the vertical-line marks; the result is bit-identical to building the new
+    context on a fresh layout, with a different index set (positions leave
+    and join the set)."""
+    B, HQ, HKV, L1, W, ppm = 2, 8, 2, 700, 128, 50_000
+    L2 = L1 + 64
+    c = decode_case(13, B, HQ, HKV, L2, window=W, n_proxy=16, sink_frac=0.03)
+    cfg = make_config(B, HQ, HKV, capacity=L2 + 64, window=W, rho_ppm=ppm)
+    kq, vq = c.k.cuda(), c.v.cuda()
+    idx1, _ = select_vertical(c.q_proxy.double().numpy(), c.k.double().numpy(), L1, W, ppm)
+    q2 = c.q_proxy.double().numpy()[:, :, ::-1] * np.array([1.0, -0.5])[None, None, :, None].repeat(8, 2)
+    idx2, _ = select_vertical(q2, c.k.double().numpy(), L2, W, ppm)
+    assert len(np.setdiff1d(idx1[0, 0], idx2[0, 0])) > 0          # some positions leave the set
+    inc, fresh = HybridLayer(cfg), HybridLayer(cfg)
+    inc.reset()
+    fresh.reset()
+    for lay, steps in ((inc, ((L1, idx1), (L2, idx2))), (fresh, ((L2, idx2),))):
+        for Lc, ix in steps:
+            t = torch.from_numpy(ix).to(torch.int32).cuda().contiguous()
+            hyq_rebuild(cfg, kq, vq, Lc, t, ix.shape[-1], lay.c)
+    torch.cuda.synchronize()
+    assert hyq_read_device_error(inc.err()) == 0 and hyq_read_device_error(fresh.err()) == 0
+    P2 = L2 - W
+    assert torch.equal(inc.counts(), fresh.counts())
+    rows = (P2 + 15) // 16 * 16
+    ib, fb = inc.qblocks().cpu().numpy(), fresh.qblocks().cpu().numpy()
+    for b in range(B):
+        for h in range(HKV):
+            a = ib[b, h].reshape(-1)[:rows // 16 * 2560]
+            f = fb[b, h].reshape(-1)[:rows // 16 * 2560]
+            assert np.array_equal(a, f)
+            _check_positional(inc, b, h, P2, c.k[b, h].double().numpy(), c.v[b, h].double().numpy(), idx2[b, h])
+    k2 = idx2.shape[-1]
+    assert torch.equal(inc.vl_k()[:, :, :k2], fresh.vl_k()[:, :, :k2])
+    assert torch.equal(inc.tail_k()[:, :, :L2 - P2], fresh.tail_k()[:, :, :L2 - P2])

@@ -17,7 +17,7 @@ from oracle.attention import hybrid_decode
 from oracle.select import prefix_len, select_vertical
 from tests.gpu_util import assert_attention_close, mixed_rows, to_np
 from tests.test_gpu_decode import build_and_decode, layer_counts
-from tests.test_gpu_quant import _check_stream
+from tests.test_gpu_quant import _check_positional, _check_stream
 
 pytestmark = pytest.mark.gpu
 
@@ -75,9 +75,8 @@ def test_rebuild_bit_exact_wide_codes(hyq, bk, bv, B, HQ, HKV, Lc, W, ppm):
     assert hyq_read_device_error(layer.err()) == 0
     for b in range(B):
         for h in range(HKV):
-            qpos = np.setdiff1d(np.arange(P), idx_np[b, h])
-            _check_stream(layer, b, h, len(qpos), k_rows[b, h, qpos].double().numpy(),
-                          v_rows[b, h, qpos].double().numpy())
+            _check_positional(layer, b, h, P, k_rows[b, h].double().numpy(), v_rows[b, h].double().numpy(),
+                              idx_np[b, h])
 
 
 @pytest.mark.parametrize("bk,bv", WIDE)
@@ -166,10 +165,9 @@ def test_fused_steps_and_tail_aging_wide_codes(hyq, bk, bv):
     torch.cuda.synchronize()
     assert hyq_read_device_error(lay.err()) == 0
     P = Lc - W
-    assert layer_counts(lay)[:4] == [P - k, k, W, Lc]
+    assert layer_counts(lay)[:4] == [P, k, W, Lc]
     for h in range(HKV):
-        qpos = np.setdiff1d(np.arange(P), idx_np[0, h])
-        _check_stream(lay, 0, h, len(qpos), c.k[0, h, qpos].double().numpy(), c.v[0, h, qpos].double().numpy())
+        _check_positional(lay, 0, h, P, c.k[0, h].double().numpy(), c.v[0, h].double().numpy(), idx_np[0, h])
     q = torch.randn(B, HQ, 128, generator=g).to(torch.bfloat16)
     hyq_decode_attention(cfg, q.cuda(), lay.c, out, ws, cap)
     torch.cuda.synchronize()
