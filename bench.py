@@ -56,6 +56,8 @@ def parse():
                    help="tuning: hyq_set_decode_plan(MERGE, SPLITS) for the period (0 0 = automatic)")
     p.add_argument("--no-mass", action="store_true", help="skip the Eq. 4 mass-score period measurement")
     p.add_argument("--no-frozen", action="store_true", help="skip the frozen-mode period measurement")
+    p.add_argument("--no-per-head", action="store_true",
+                   help="skip the period with Algorithm 1's per-query-head vertical-line sets")
     p.add_argument("--no-sweep", action="store_true",
                    help="skip the 1K/4K/16K context periods and the batch-16 period with maintenance")
     p.add_argument("--no-grid", action="store_true", help="skip the Qwen3-32B-shaped rho x W timing grid")
@@ -333,17 +335,18 @@ def algorithmic_bytes(n_q, n_vl, n_tail, q_row=160):
     return B * (HKV * (n_q * q_row + (n_vl + n_tail) * 512) + 2 * HQ * D * 2)
 
 
-def period_bytes_per_decode(q_row=160):
-    """Mean algorithmic bytes of the 64 decode calls of one period."""
+def period_bytes_per_decode(q_row=160, vl_mult=1):
+    """Mean algorithmic bytes of the 64 decode calls of one period; vl_mult =
+    g for the per-query-head lists (min(P, g k) vertical lines per KV head)."""
     P0 = L0 - WINDOW
-    k0 = -(-P0 * RHO_PPM // 1_000_000)
+    k0 = min(P0, vl_mult * -(-P0 * RHO_PPM // 1_000_000))
     tot = 0
     for t in range(PERIOD):
         if t < PERIOD - 1:
             tot += algorithmic_bytes(P0 - k0, k0, WINDOW + t + 1, q_row)
         else:
             P = CTX - WINDOW
-            k = -(-P * RHO_PPM // 1_000_000)
+            k = min(P, vl_mult * -(-P * RHO_PPM // 1_000_000))
             tot += algorithmic_bytes(P - k, k, WINDOW, q_row)
     return tot / PERIOD
 
@@ -704,9 +707,10 @@ def run_ours(args, rank, world, local):
     # variants of the maintenance: frozen mode (Algorithm 4 as written: the
     # last token's maintenance is hyq_age_tail instead of re-selection) and
     # re-selection by the softmax-mass score of Eq. 4
-    def variant_period(bits=(4, 4), **kw):
-        cfg_v = cfg if bits == (4, 4) else hyq.make_config(B, HQ, HKV, capacity=CTX, window=WINDOW, period=PERIOD,
-                                                            rho_ppm=RHO_PPM, bits_k=bits[0], bits_v=bits[1])
+    def variant_period(bits=(4, 4), vl_mode=0, **kw):
+        cfg_v = cfg if bits == (4, 4) and vl_mode == 0 else hyq.make_config(
+            B, HQ, HKV, capacity=CTX, window=WINDOW, period=PERIOD, rho_ppm=RHO_PPM, bits_k=bits[0],
+            bits_v=bits[1], vl_mode=vl_mode)
         fr = PeriodRunner(cfg_v, k_srcs, v_srcs, L0, dev, prefetch_next=args.prefetch, **kw)
         fr.q_tok.copy_(q_tok)
         fr.k_tok.copy_(k_tok)
@@ -726,7 +730,7 @@ def run_ours(args, rank, world, local):
         torch.cuda.synchronize()
         fms = reduce_timing(f0.elapsed_time(f1), world, dev)
         fdec_us = sum(a.elapsed_time(b) for row in fev for a, b in row) * 1e3 / (args.steps * PERIOD * nl)
-        fbytes = period_bytes_per_decode(q_row_bytes(*bits))
+        fbytes = period_bytes_per_decode(q_row_bytes(*bits), HQ // HKV if vl_mode else 1)
         res = {"value": job_value(fms, args.steps, PERIOD * nl, world), "unit": "us/token/layer",
                "ms_per_step": fms / args.steps, "launches_per_period": fr.launches_per_period,
                "decode_us_per_token_layer": fdec_us,
@@ -735,9 +739,9 @@ def run_ours(args, rank, world, local):
         del fr
         return res
 
-    frozen = mass = widths = None
+    frozen = mass = widths = per_head = None
     main_launches = run.launches_per_period
-    if not (args.no_frozen and args.no_mass and args.no_widths):
+    if not (args.no_frozen and args.no_mass and args.no_widths and args.no_per_head):
         del run
     if not args.no_frozen:
         frozen = {"maintenance": "hyq_age_tail: tail rows older than the window quantised onto the 4-bit stream; "
@@ -748,6 +752,13 @@ def run_ours(args, rank, world, local):
     if not args.no_widths:
         widths = {f"K{bk}V{bv}": {"q_row_bytes": q_row_bytes(bk, bv), **variant_period(bits=(bk, bv))}
                   for bk, bv in ((8, 8), (4, 8))}
+    if not args.no_per_head:
+        per_head = {"maintenance": "re-selection per query head (Algorithm 1 as written, hyq_config.vl_mode = "
+                                   "VL_PER_QUERY_HEAD): per KV head the union of its 4 query heads' sets filled "
+                                   "up to min(P, 4k) by the group score, then rebuild",
+                    "vl_rows_per_kv_head_at_32k": min(CTX - WINDOW, (HQ // HKV) * -(-(CTX - WINDOW) * RHO_PPM
+                                                                                      // 1_000_000)),
+                    **variant_period(vl_mode=1)}
 
     if rank != 0:
         return
@@ -800,6 +811,7 @@ def run_ours(args, rank, world, local):
         "frozen": frozen,
         "mass_selection": mass,
         "widths": widths,
+        "per_query_head_sets": per_head,
         "prefill": ({"workload": "llama3.1-8b-shaped causal prefill, B1, 32/8 heads, d128, 8K and 32K, W128, rho 5% "
                                  "(pack + main kernel; window fixed: hyq_prefill_attention, band: "
                                  "hyq_prefill_attention_band)",

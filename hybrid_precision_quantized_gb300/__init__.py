@@ -11,7 +11,7 @@ from ._lib import (HyqConfig, HyqError, HyqLayout, load, lib_path, hyq_config_ch
                    hyq_decode_attention_noalloc, hyq_layout_reset, hyq_layout_sizes, hyq_prefill_attention,
                    hyq_prefill_attention_band,
                    hyq_quantize_append, hyq_read_device_error, hyq_rebuild, hyq_select_vertical,
-                   hyq_select_vertical_mass, hyq_set_decode_plan, hyq_set_decode_overlap,
+                   hyq_select_vertical_heads, hyq_select_vertical_mass, hyq_set_decode_plan, hyq_set_decode_overlap,
                    hyq_status_string, hyq_vl_count, hyq_workspace_size)
 from .cache import (HybridDecoder, HybridLayer, make_config, pack_qblocks, unpack_qblocks,
                     workspace)

@@ -41,6 +41,7 @@ CNT_NQ, CNT_NVL, CNT_NTAIL, CNT_LEN, CNT_RING_N, CNT_RING_POS = range(6)
 LAYOUT_FIELDS = ("qblocks", "vl_k", "vl_v", "vl_idx", "tail_k", "tail_v", "q_ring", "counts", "err")
 OP_SELECT, OP_DECODE, OP_PREFILL, OP_SELECT_MASS, OP_PREFILL_BAND = 1, 2, 3, 4, 5
 PREFILL_INT8, PREFILL_FP8 = 1, 2
+VL_PER_KV_HEAD, VL_PER_QUERY_HEAD = 0, 1
 
 # Every symbol include/hyq.h declares.
 SYMBOLS = ("hyq_status_string", "hyq_config_check", "hyq_vl_count", "hyq_layout_sizes",
@@ -49,7 +50,7 @@ SYMBOLS = ("hyq_status_string", "hyq_config_check", "hyq_vl_count", "hyq_layout_
            "hyq_decode_attention_noalloc", "hyq_read_device_error", "hyq_set_decode_plan",
            "hyq_prefill_attention", "hyq_decode_step", "hyq_set_decode_overlap",
            "hyq_decode_step_prefetch", "hyq_age_tail", "hyq_select_vertical_mass",
-           "hyq_prefill_attention_band")
+           "hyq_prefill_attention_band", "hyq_select_vertical_heads")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -57,7 +58,7 @@ class HyqConfig(ctypes.Structure):
     _fields_ = [("batch", c_int32), ("num_q_heads", c_int32), ("num_kv_heads", c_int32),
                 ("head_dim", c_int32), ("group", c_int32), ("window", c_int32),
                 ("period", c_int32), ("rho_ppm", c_int32), ("capacity", c_int32),
-                ("bits_k", c_int32), ("bits_v", c_int32)]
+                ("bits_k", c_int32), ("bits_v", c_int32), ("vl_mode", c_int32)]
 
 
 class HyqLayout(ctypes.Structure):
@@ -99,6 +100,9 @@ def load() -> ctypes.CDLL:
                                           c_int32, c_void_p, P(c_int32), c_void_p, c_size_t, c_void_p]),
         "hyq_select_vertical_mass": (c_int32, [P(HyqConfig), c_void_p, c_int32, c_int32, c_void_p, c_int32,
                                                c_int32, c_void_p, P(c_int32), c_void_p, c_size_t, c_void_p]),
+        "hyq_select_vertical_heads": (c_int32, [P(HyqConfig), c_void_p, c_int32, c_int32, c_void_p, c_int32,
+                                                c_int32, c_void_p, c_void_p, P(c_int32), P(c_int32), c_void_p,
+                                                c_size_t, c_void_p]),
         "hyq_rebuild": (c_int32, [P(HyqConfig), c_void_p, c_void_p, c_int32, c_int32, c_void_p, c_int32,
                                   P(HyqLayout), c_void_p]),
         "hyq_decode_append": (c_int32, [P(HyqConfig), c_void_p, c_void_p, c_void_p, P(HyqLayout),
@@ -207,6 +211,19 @@ def hyq_select_vertical_mass(cfg, q_proxy, n_proxy: int, k_src, L: int, idx_out,
         ctypes.byref(cfg), ptr(q_proxy), n_proxy, row_ld(q_proxy), ptr(k_src), row_ld(k_src), L,
         ptr(idx_out), ctypes.byref(k_out), ptr(ws), ws.numel() * ws.element_size(), stream_ptr(stream)))
     return k_out.value
+
+
+def hyq_select_vertical_heads(cfg, q_proxy, n_proxy: int, k_src, L: int, idx_heads, idx_out, ws,
+                              stream=None) -> tuple:
+    """Algorithm 1 per query head (cfg.vl_mode = VL_PER_QUERY_HEAD):
+    idx_heads int32 [B, HQ, k] contiguous or None, idx_out int32 [B, HKV, ku]
+    contiguous.  Returns (k, ku)."""
+    k_out, ku_out = c_int32(0), c_int32(0)
+    _check("hyq_select_vertical_heads", load().hyq_select_vertical_heads(
+        ctypes.byref(cfg), ptr(q_proxy), n_proxy, row_ld(q_proxy), ptr(k_src), row_ld(k_src), L,
+        None if idx_heads is None else ptr(idx_heads), ptr(idx_out), ctypes.byref(k_out), ctypes.byref(ku_out),
+        ptr(ws), ws.numel() * ws.element_size(), stream_ptr(stream)))
+    return k_out.value, ku_out.value
 
 
 def hyq_rebuild(cfg, k_src, v_src, L: int, idx, k: int, lay: HyqLayout, stream=None):

@@ -13,10 +13,10 @@ from ._lib import HyqConfig, HyqLayout
 
 
 def make_config(batch, num_q_heads, num_kv_heads, capacity, window=128, period=64,
-                rho_ppm=50_000, head_dim=128, group=32, bits_k=4, bits_v=4) -> HyqConfig:
+                rho_ppm=50_000, head_dim=128, group=32, bits_k=4, bits_v=4, vl_mode=0) -> HyqConfig:
     return HyqConfig(batch=batch, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
                      head_dim=head_dim, group=group, window=window, period=period,
-                     rho_ppm=rho_ppm, capacity=capacity, bits_k=bits_k, bits_v=bits_v)
+                     rho_ppm=rho_ppm, capacity=capacity, bits_k=bits_k, bits_v=bits_v, vl_mode=vl_mode)
 
 
 class HybridLayer:

@@ -71,16 +71,24 @@ extern "C" hyq_status hyq_config_check(const hyq_config* c) {
   if (c->batch > 65535 || c->num_kv_heads > 65535) return HYQ_ERR_INVALID_ARG;
   if ((c->bits_k != 0 && c->bits_k != 4 && c->bits_k != 8) || (c->bits_v != 0 && c->bits_v != 4 && c->bits_v != 8))
     return HYQ_ERR_UNSUPPORTED;
+  if (c->vl_mode != HYQ_VL_PER_KV_HEAD && c->vl_mode != HYQ_VL_PER_QUERY_HEAD) return HYQ_ERR_INVALID_ARG;
   return HYQ_OK;
 }
 
-extern "C" int32_t hyq_vl_count(const hyq_config* c, int32_t P) {
-  if (!c) return -1;
+int32_t hyq_vl_count_head(const hyq_config* c, int32_t P) {
   if (P <= 0 || c->rho_ppm <= 0) return 0;
   int64_t k = ((int64_t)P * c->rho_ppm + 999999) / 1000000;  // exact ceil(P * rho)
   if (k < 1) k = 1;
   if (k > P) k = P;
   return (int32_t)k;
+}
+
+extern "C" int32_t hyq_vl_count(const hyq_config* c, int32_t P) {
+  if (!c) return -1;
+  const int64_t k = hyq_vl_count_head(c, P);
+  if (c->vl_mode != HYQ_VL_PER_QUERY_HEAD || c->num_kv_heads < 1) return (int32_t)k;
+  const int64_t ku = k * (c->num_q_heads / c->num_kv_heads);
+  return (int32_t)(ku < P ? ku : P);
 }
 
 int32_t hyq_cap_vl(const hyq_config* c) {
@@ -165,7 +173,31 @@ extern "C" hyq_status hyq_select_vertical(const hyq_config* c, const void* q_pro
     return HYQ_ERR_INVALID_ARG;
   if (n_proxy < 1) return HYQ_ERR_INVALID_ARG;
   if (!ws || !aligned(ws, kAlign) || ws_bytes < hyq_select_ws_bytes(c, L)) return HYQ_ERR_WORKSPACE;
+  if (c->vl_mode == HYQ_VL_PER_QUERY_HEAD)
+    return from_cuda(hyq_launch_select_heads(c, q_proxy, n_proxy, n_proxy_ld, k_src, ld, L, nullptr,
+                                             hyq_vl_count_head(c, P), idx_out, k, ws, s));
   return from_cuda(hyq_launch_select(c, q_proxy, n_proxy, n_proxy_ld, k_src, ld, L, idx_out, k, ws, s));
+}
+
+extern "C" hyq_status hyq_select_vertical_heads(const hyq_config* c, const void* q_proxy, int32_t n_proxy,
+                                                int32_t n_proxy_ld, const void* k_src, int32_t ld, int32_t L,
+                                                int32_t* idx_heads_out, int32_t* idx_out, int32_t* k_out,
+                                                int32_t* ku_out, void* ws, size_t ws_bytes, hyq_stream_t s) {
+  hyq_status st = hyq_config_check(c);
+  if (st != HYQ_OK) return st;
+  if (c->vl_mode != HYQ_VL_PER_QUERY_HEAD || !k_out || !ku_out) return HYQ_ERR_INVALID_ARG;
+  if (L < 0 || L > c->capacity) return HYQ_ERR_CAPACITY;
+  if (ld < L || ld < 1 || n_proxy < 0 || n_proxy_ld < n_proxy) return HYQ_ERR_INVALID_ARG;
+  const int32_t P = L - c->window > 0 ? L - c->window : 0;
+  const int32_t k1 = hyq_vl_count_head(c, P), ku = hyq_vl_count(c, P);
+  *k_out = k1;
+  *ku_out = ku;
+  if (k1 == 0) return HYQ_OK;
+  if (!q_proxy || !k_src || !idx_out || !aligned(k_src, 16) || !aligned(q_proxy, 16)) return HYQ_ERR_INVALID_ARG;
+  if (n_proxy < 1) return HYQ_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, kAlign) || ws_bytes < hyq_select_ws_bytes(c, L)) return HYQ_ERR_WORKSPACE;
+  return from_cuda(hyq_launch_select_heads(c, q_proxy, n_proxy, n_proxy_ld, k_src, ld, L, idx_heads_out, k1,
+                                           idx_out, ku, ws, s));
 }
 
 extern "C" hyq_status hyq_select_vertical_mass(const hyq_config* c, const void* q_proxy, int32_t n_proxy,
@@ -176,6 +208,7 @@ extern "C" hyq_status hyq_select_vertical_mass(const hyq_config* c, const void* 
   if (st != HYQ_OK) return st;
   if (!k_out) return HYQ_ERR_INVALID_ARG;
   if (L < 0 || L > c->capacity) return HYQ_ERR_CAPACITY;
+  if (c->vl_mode != HYQ_VL_PER_KV_HEAD) return HYQ_ERR_UNSUPPORTED;
   if (ld < L || ld < 1 || n_proxy < 0 || n_proxy_ld < n_proxy || n_proxy > c->period) return HYQ_ERR_INVALID_ARG;
   int32_t P = L - c->window > 0 ? L - c->window : 0;
   int32_t k = hyq_vl_count(c, P);

@@ -77,6 +77,13 @@ cudaError_t hyq_launch_select(const hyq_config* c, const void* q_proxy, int32_t 
                               int32_t n_proxy_ld, const void* k_src, int32_t ld, int32_t L,
                               int32_t* idx_out, int32_t k, void* ws, cudaStream_t s);
 size_t hyq_select_ws_bytes(const hyq_config* c, int32_t L);
+size_t hyq_select_kv_ws_bytes(const hyq_config* c, int32_t L);
+// Vertical-line count of one query head (Algorithm 1's k) for a prefix of P.
+int32_t hyq_vl_count_head(const hyq_config* c, int32_t P);
+cudaError_t hyq_launch_select_heads(const hyq_config* c, const void* q_proxy, int32_t n_proxy,
+                                    int32_t n_proxy_ld, const void* k_src, int32_t ld, int32_t L,
+                                    int32_t* idx_heads, int32_t k1, int32_t* idx_out, int32_t ku, void* ws,
+                                    cudaStream_t s);
 size_t hyq_select_mass_ws_bytes(const hyq_config* c, int32_t L);
 cudaError_t hyq_launch_select_mass(const hyq_config* c, const void* q_proxy, int32_t n_proxy,
                                    int32_t n_proxy_ld, const void* k_src, int32_t ld, int32_t L,

@@ -7,6 +7,14 @@
 //          written in ascending order.
 // Three launches: proxy sum, scores (HBM-bound pass over the BF16 keys),
 // radix select + ordered compaction (one CTA per KV head).
+//
+// Per query head (hyq_config.vl_mode = 1, Algorithm 1's B x H_Q x k sets):
+// the proxies are summed per query head as well, one pass over the keys
+// scores every query head of the group and the group itself, a top-k per
+// query head gives the heads' sets, their positions are raised to the top
+// key value in the group's scores, and a top-ku of those gives the stored
+// per-KV-head list: the union of the group's sets, filled up to
+// ku = min(P, g k) by the group score.
 #include <cooperative_groups.h>
 
 #include <algorithm>
@@ -118,6 +126,72 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(
 #pragma unroll
     for (int o = 1; o < 16; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     if (valid && sub == 0) keys[bh * pmax + r] = order_key(s, err);
+  }
+}
+
+// Scores of the g query heads of a KV head and of the group, one half-warp
+// per key row as in score_kernel (the same operation order, so the group
+// keys equal score_kernel's).  grid (ceil(P/64), HKV, B).
+template <int G>
+__global__ void __launch_bounds__(kScoreThreads) score_heads_kernel(
+    const __nv_bfloat16* __restrict__ k_src, int32_t ld, int32_t P, const float* __restrict__ u_heads,
+    const float* __restrict__ u_group, uint32_t* __restrict__ keys_heads, uint32_t* __restrict__ keys_group,
+    int32_t* err) {
+  const int h = blockIdx.y, b = blockIdx.z, HKV = gridDim.y;
+  const size_t bh = (size_t)b * HKV + h;
+  const int lane = threadIdx.x & 31, half = lane >> 4, sub = lane & 15;
+  const int warp = threadIdx.x >> 5;
+  float uu[G + 1][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+#pragma unroll
+    for (int r = 0; r < G; ++r) uu[r][i] = u_heads[(bh * G + r) * HYQ_D + 8 * sub + i];
+    uu[G][i] = u_group[bh * HYQ_D + 8 * sub + i];
+  }
+  const __nv_bfloat16* kb = k_src + bh * ld * HYQ_D;
+  const int end = min(P, (int)(blockIdx.x + 1) * kScoreRowsPerCta);
+  for (int r0 = blockIdx.x * kScoreRowsPerCta + 2 * warp; r0 < end; r0 += 2 * (kScoreThreads / 32)) {
+    const int r = r0 + half;
+    const bool valid = r < end;
+    float s[G + 1];
+#pragma unroll
+    for (int q = 0; q <= G; ++q) s[q] = 0.f;
+    if (valid) {
+      uint4 raw = *reinterpret_cast<const uint4*>(kb + (size_t)r * HYQ_D + 8 * sub);
+      const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float2 f = __bfloat1622float2(pr[i]);
+#pragma unroll
+        for (int q = 0; q <= G; ++q) {
+          s[q] = fmaf(uu[q][2 * i], f.x, s[q]);
+          s[q] = fmaf(uu[q][2 * i + 1], f.y, s[q]);
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q <= G; ++q)
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) s[q] += __shfl_xor_sync(0xffffffffu, s[q], o);
+    if (valid && sub == 0) {
+#pragma unroll
+      for (int q = 0; q < G; ++q) keys_heads[(bh * G + q) * P + r] = order_key(s[q], err);
+      keys_group[bh * P + r] = order_key(s[G], err);
+    }
+  }
+}
+
+// Raise the group keys of every position in a query head's set above any
+// score key, so that a top-ku of the group keys takes the union first.
+// grid (HQ, B).
+__global__ void mark_union_kernel(const int32_t* __restrict__ idx_heads, int32_t k1, int32_t g, int32_t P,
+                                  uint32_t* __restrict__ keys_group) {
+  const int h = blockIdx.x, b = blockIdx.y, HQ = gridDim.x;
+  const int32_t* ih = idx_heads + ((size_t)b * HQ + h) * k1;
+  uint32_t* kg = keys_group + ((size_t)b * (HQ / g) + h / g) * P;
+  for (int i = threadIdx.x; i < k1; i += blockDim.x) {
+    const int32_t j = ih[i];
+    if (j >= 0 && j < P) kg[j] = 0xFFFFFFFFu;  // above order_key(+inf)
   }
 }
 
@@ -699,10 +773,20 @@ __global__ void mass_keys_kernel(const float* __restrict__ colsum, int32_t n_gro
 
 }  // namespace
 
-size_t hyq_select_ws_bytes(const hyq_config* c, int32_t L) {
+size_t hyq_select_kv_ws_bytes(const hyq_config* c, int32_t L) {
   size_t bh = (size_t)c->batch * c->num_kv_heads;
   int32_t P = L - c->window > 0 ? L - c->window : 0;
   return 256 + round_up(bh * HYQ_D * 4) + round_up(bh * (size_t)(P > 0 ? P : 1) * 4);
+}
+
+size_t hyq_select_ws_bytes(const hyq_config* c, int32_t L) {
+  const size_t kv = hyq_select_kv_ws_bytes(c, L);
+  if (c->vl_mode != HYQ_VL_PER_QUERY_HEAD) return kv;
+  const size_t bq = (size_t)c->batch * c->num_q_heads;
+  const int32_t P = L - c->window > 0 ? L - c->window : 0;
+  const size_t k1 = (size_t)hyq_vl_count_head(c, P);
+  return kv + round_up(bq * HYQ_D * 4) + round_up(bq * (size_t)(P > 0 ? P : 1) * 4) +
+         round_up(bq * (k1 > 0 ? k1 : 1) * 4);
 }
 
 namespace {
@@ -732,20 +816,21 @@ MassWs carve_mass(const hyq_config* c, int32_t L, void* ws) {
   return w;
 }
 
-cudaError_t launch_topk(const hyq_config* c, const SelectWs& w, int32_t P, int32_t k, int32_t* idx_out,
-                        cudaStream_t s) {
+// Top-k of `heads` rows of P keys per sequence ([B][heads][P]).
+cudaError_t launch_topk_rows(const hyq_config* c, const uint32_t* keys, int32_t heads, int32_t P, int32_t k,
+                             int32_t* idx_out, cudaStream_t s) {
   const int32_t cap = kTopkCluster * kTopkCtaThreads;
-  dim3 gc(kTopkCluster, c->num_kv_heads, c->batch);
+  dim3 gc(kTopkCluster, heads, c->batch);
   if (P <= 4 * cap) {
-    topk_cluster_kernel<4><<<gc, kTopkCtaThreads, 0, s>>>(w.keys, P, P, k, idx_out);
+    topk_cluster_kernel<4><<<gc, kTopkCtaThreads, 0, s>>>(keys, P, P, k, idx_out);
     return cudaGetLastError();
   }
   if (P <= 8 * cap) {
-    topk_cluster_kernel<8><<<gc, kTopkCtaThreads, 0, s>>>(w.keys, P, P, k, idx_out);
+    topk_cluster_kernel<8><<<gc, kTopkCtaThreads, 0, s>>>(keys, P, P, k, idx_out);
     return cudaGetLastError();
   }
   if (P <= 16 * cap) {
-    topk_cluster_kernel<16><<<gc, kTopkCtaThreads, 0, s>>>(w.keys, P, P, k, idx_out);
+    topk_cluster_kernel<16><<<gc, kTopkCtaThreads, 0, s>>>(keys, P, P, k, idx_out);
     return cudaGetLastError();
   }
   static std::atomic<uint64_t> attr_done{0};
@@ -755,8 +840,35 @@ cudaError_t launch_topk(const hyq_config* c, const SelectWs& w, int32_t P, int32
   });
   if (ea != cudaSuccess) return ea;
   const size_t tk_smem = P <= kTopkSmemKeys ? (size_t)P * sizeof(uint32_t) : 0;
-  topk_kernel<<<dim3(c->num_kv_heads, c->batch), kTopkThreads, tk_smem, s>>>(w.keys, P, P, k, idx_out);
+  topk_kernel<<<dim3(heads, c->batch), kTopkThreads, tk_smem, s>>>(keys, P, P, k, idx_out);
   return cudaGetLastError();
+}
+
+cudaError_t launch_topk(const hyq_config* c, const SelectWs& w, int32_t P, int32_t k, int32_t* idx_out,
+                        cudaStream_t s) {
+  return launch_topk_rows(c, w.keys, c->num_kv_heads, P, k, idx_out, s);
+}
+
+// Per-query-head workspace, after the per-KV-head one: u per query head,
+// keys per query head, the heads' index lists.
+struct HeadsWs {
+  float* u;
+  uint32_t* keys;
+  int32_t* idx;
+};
+
+HeadsWs carve_heads(const hyq_config* c, int32_t L, void* ws) {
+  const size_t bq = (size_t)c->batch * c->num_q_heads;
+  const int32_t P = L - c->window > 0 ? L - c->window : 0;
+  char* p = static_cast<char*>(ws) + hyq_select_kv_ws_bytes(c, L);
+  HeadsWs w;
+  w.u = reinterpret_cast<float*>(p);
+  p += round_up(bq * HYQ_D * 4);
+  w.keys = reinterpret_cast<uint32_t*>(p);
+  p += round_up(bq * (size_t)(P > 0 ? P : 1) * 4);
+  w.idx = reinterpret_cast<int32_t*>(p);
+  (void)P;
+  return w;
 }
 
 }  // namespace
@@ -829,4 +941,49 @@ cudaError_t hyq_launch_select_mass(const hyq_config* c, const void* q_proxy, int
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_topk(c, w, P, k, idx_out, s);
+}
+
+cudaError_t hyq_launch_select_heads(const hyq_config* c, const void* q_proxy, int32_t n_proxy,
+                                    int32_t n_proxy_ld, const void* k_src, int32_t ld, int32_t L,
+                                    int32_t* idx_heads, int32_t k1, int32_t* idx_out, int32_t ku, void* ws,
+                                    cudaStream_t s) {
+  SelectWs w = carve(c, L, ws);
+  HeadsWs hw = carve_heads(c, L, ws);
+  if (!idx_heads) idx_heads = hw.idx;
+  const int32_t P = L - c->window;  // > 0 since k1 > 0
+  const int32_t g = c->num_q_heads / c->num_kv_heads;
+  const __nv_bfloat16* qp = static_cast<const __nv_bfloat16*>(q_proxy);
+  proxy_sum_kernel<<<dim3(c->num_q_heads, c->batch), kProxyThreads, 0, s>>>(qp, n_proxy, n_proxy_ld, 1, hw.u);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  proxy_sum_kernel<<<dim3(c->num_kv_heads, c->batch), kProxyThreads, 0, s>>>(qp, n_proxy, n_proxy_ld, g, w.u);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  dim3 g2((P + kScoreRowsPerCta - 1) / kScoreRowsPerCta, c->num_kv_heads, c->batch);
+  const __nv_bfloat16* kk = static_cast<const __nv_bfloat16*>(k_src);
+  switch (g) {
+#define HYQ_SCORE_HEADS(G)                                                                                    \
+  case G:                                                                                                    \
+    score_heads_kernel<G><<<g2, kScoreThreads, 0, s>>>(kk, ld, P, hw.u, w.u, hw.keys, w.keys, w.err); \
+    break;
+    HYQ_SCORE_HEADS(1)
+    HYQ_SCORE_HEADS(2)
+    HYQ_SCORE_HEADS(3)
+    HYQ_SCORE_HEADS(4)
+    HYQ_SCORE_HEADS(5)
+    HYQ_SCORE_HEADS(6)
+    HYQ_SCORE_HEADS(7)
+    HYQ_SCORE_HEADS(8)
+#undef HYQ_SCORE_HEADS
+    default:
+      return cudaErrorInvalidValue;
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = launch_topk_rows(c, hw.keys, c->num_q_heads, P, k1, idx_heads, s);
+  if (e != cudaSuccess) return e;
+  mark_union_kernel<<<dim3(c->num_q_heads, c->batch), 256, 0, s>>>(idx_heads, k1, g, P, w.keys);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_topk_rows(c, w.keys, c->num_kv_heads, P, ku, idx_out, s);
 }

@@ -100,7 +100,9 @@ class PeriodRunner:
                 k = self.select(self.cfg, ring, ring.shape[2], self.k_srcs[li], self.L_end, self.idx[li],
                                 self.ws_sel)
                 L.hyq_rebuild(self.cfg, self.k_srcs[li], self.v_srcs[li], self.L_end, self.idx[li], k, lay.c)
-                n += ((5 if self.select is L.hyq_select_vertical_mass else 3) if k > 0 else 0) + \
+                n_sel = 5 if self.select is L.hyq_select_vertical_mass else (
+                    6 if self.cfg.vl_mode == L.VL_PER_QUERY_HEAD else 3)
+                n += (n_sel if k > 0 else 0) + \
                     (2 if self.L_end - self.cfg.window - k > 0 else 1)
         return n
 

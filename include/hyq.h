@@ -73,7 +73,29 @@ typedef struct {
   int32_t capacity;     /* largest context length L the layout must hold        */
   int32_t bits_k;       /* B_K, key code width: 4 or 8 (0 means 4)              */
   int32_t bits_v;       /* B_V, value code width: 4 or 8 (0 means 4)            */
+  int32_t vl_mode;      /* HYQ_VL_PER_KV_HEAD (0) or HYQ_VL_PER_QUERY_HEAD       */
 } hyq_config;
+
+/*
+ * Vertical-line granularity (hyq_config.vl_mode).  The cache holds one
+ * vertical-line list per (sequence, KV head) in both modes: a position is
+ * kept in BF16, or in the quantised stream, for the whole KV head.
+ *   HYQ_VL_PER_KV_HEAD     one set per KV head, scored with the proxies of
+ *                          all g query heads of the group summed; k =
+ *                          min(P, max(1, ceil(P rho))) positions.
+ *   HYQ_VL_PER_QUERY_HEAD  Algorithm 1's output as written, one set of k
+ *                          positions per query head (B x H_Q x k), each
+ *                          scored with that head's own proxies; the list
+ *                          stored per KV head is the union of its g query
+ *                          heads' sets, filled up to min(P, g k) positions
+ *                          with the largest group scores (the per-KV-head
+ *                          score) among the others, ties to the lower
+ *                          position, so that every query head's own set is
+ *                          held in BF16 and the list length is the same for
+ *                          every head.  hyq_vl_count gives that length.
+ */
+#define HYQ_VL_PER_KV_HEAD 0
+#define HYQ_VL_PER_QUERY_HEAD 1
 
 /*
  * Quantised stream format.  The quantised ("4-bit") stream of one (batch, KV
@@ -178,8 +200,9 @@ const char *hyq_status_string(hyq_status s);
 /* Validate a config; HYQ_OK when every entry point accepts it. */
 hyq_status hyq_config_check(const hyq_config *cfg);
 
-/* Vertical-line count for a prefix of P positions (Algorithm 1):
- * k = min(P, max(1, ceil(P * rho))), and 0 when P <= 0 or rho = 0.
+/* Length of the per-KV-head vertical-line list for a prefix of P positions:
+ * k = min(P, max(1, ceil(P * rho))) (Algorithm 1), and 0 when P <= 0 or
+ * rho = 0; with vl_mode = HYQ_VL_PER_QUERY_HEAD, min(P, g k).
  * Returns -1 for a null config. */
 int32_t hyq_vl_count(const hyq_config *cfg, int32_t P);
 
@@ -247,6 +270,28 @@ hyq_status hyq_select_vertical(const hyq_config *cfg, const void *q_proxy, int32
                                hyq_stream_t stream);
 
 /*
+ * Algorithm 1 per query head (Appendix A.1, output B x H_Q x k), for a config
+ * with vl_mode = HYQ_VL_PER_QUERY_HEAD (any other config: HYQ_ERR_INVALID_ARG).
+ *   q_proxy, n_proxy, k_src, ld, L  as for hyq_select_vertical
+ *   idx_heads_out  device int32 [B][HQ][k] or NULL: each query head's set,
+ *                  strictly ascending
+ *   idx_out        device int32 [B][HKV][ku]: the stored list, strictly
+ *                  ascending (the union of the group's sets filled up to ku
+ *                  by the group score, see HYQ_VL_PER_QUERY_HEAD)
+ *   k_out, ku_out  host int32: k = min(P, max(1, ceil(P rho))) and
+ *                  ku = hyq_vl_count(cfg, P) = min(P, g k)
+ * Query head h scores S_h(j) = u_h . k_j (u_h the sum of its n_proxy proxy
+ * queries, k_j the key of h's KV head) and keeps its k largest, ties to the
+ * lower position; the group score is hyq_select_vertical's.  Both in
+ * float32.  hyq_select_vertical on such a config computes the same idx_out.
+ * Workspace: hyq_workspace_size(cfg, HYQ_OP_SELECT, L).  Six launches.
+ */
+hyq_status hyq_select_vertical_heads(const hyq_config *cfg, const void *q_proxy, int32_t n_proxy,
+                                     int32_t n_proxy_ld, const void *k_src, int32_t ld, int32_t L,
+                                     int32_t *idx_heads_out, int32_t *idx_out, int32_t *k_out,
+                                     int32_t *ku_out, void *ws, size_t ws_bytes, hyq_stream_t stream);
+
+/*
  * Vertical-line identification with the score of Eq. 4 (§4.1): the
  * accumulated column mass of the attention probabilities instead of
  * Algorithm 1's summed logits.  Same arguments and output as
@@ -259,6 +304,8 @@ hyq_status hyq_select_vertical(const hyq_config *cfg, const void *q_proxy, int32
  * row the maximum m and the sum l of 2^(t - m), t = (q_r . k_j) fl(alpha
  * log2 e), over at most 32 key ranges merged once, then S(j) = sum_r 2^(t - m) / l;
  * a NaN score sets HYQ_DEVERR_SCORE in the workspace's error word.
+ * Per KV head only: a config with vl_mode = HYQ_VL_PER_QUERY_HEAD returns
+ * HYQ_ERR_UNSUPPORTED.
  * Workspace: hyq_workspace_size(cfg, HYQ_OP_SELECT_MASS, L).  Five launches.
  */
 hyq_status hyq_select_vertical_mass(const hyq_config *cfg, const void *q_proxy, int32_t n_proxy,

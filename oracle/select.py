@@ -85,6 +85,75 @@ def select_vertical(q_proxy, k_src, L: int, window: int, rho_ppm: int):
     return topk_ascending(S, k), S
 
 
+# --- Algorithm 1 per query head, kept per KV head ---------------------------
+#
+# Algorithm 1's output is one set per query head (B x H_Q x k): query head h
+# scores the prefix with its own proxy sum against the keys of its KV head.
+# The cache keeps a position in BF16 for a whole KV head (Algorithm 4 gathers
+# the rows from the H_KV-head K), so the list stored per KV head is the union
+# of the g query heads' sets.  Reading: to keep one list length per layer the
+# union is filled up to min(P, g k) positions with the highest group scores
+# (the per-KV-head score above) among the positions not yet in it, ties to the
+# lower position; every query head's own set is then held in BF16.
+
+def vl_count_heads(P: int, rho_ppm: int, g: int) -> int:
+    """Length of the per-KV-head list in the per-query-head reading: min(P, g k)."""
+    return min(max(0, P), g * vl_count(P, rho_ppm))
+
+
+def head_scores(q_proxy, k_src, P: int) -> np.ndarray:
+    """``S_h(j) = (sum_t q_{h,t}) . k_j`` per query head h, with k_j the key
+    of h's KV head.  q_proxy [B, HQ, T, d], k_src [B, HKV, >=P, d] ->
+    [B, HQ, P] float64."""
+    q = np.asarray(q_proxy, dtype=np.float64)
+    k = np.asarray(k_src, dtype=np.float64)[:, :, :P, :]
+    B, HQ, T, d = q.shape
+    HKV = k.shape[1]
+    g = HQ // HKV
+    u = q.sum(axis=2).reshape(B, HKV, g, d)                 # query head kh g + r of KV head kh
+    return np.einsum("bhrd,bhpd->bhrp", u, k).reshape(B, HQ, P)
+
+
+def union_fill(sets, S_group, ku: int) -> np.ndarray:
+    """The ascending union of `sets` (rows of positions), completed to ku
+    positions by the largest S_group among the others, ties to the lower
+    position."""
+    U = sorted({int(j) for row in sets for j in np.asarray(row).ravel()})
+    P = len(S_group)
+    chosen = np.zeros(P, dtype=bool)
+    chosen[U] = True
+    rest = np.flatnonzero(~chosen)
+    need = ku - len(U)
+    if need > 0:
+        order = np.lexsort((rest, -np.asarray(S_group, dtype=np.float64)[rest]))
+        chosen[rest[order[:need]]] = True
+    return np.flatnonzero(chosen).astype(np.int64)
+
+
+def select_vertical_heads(q_proxy, k_src, L: int, window: int, rho_ppm: int):
+    """Algorithm 1 per query head.  Returns (idx_heads [B, HQ, k] ascending,
+    idx_kv [B, HKV, ku] ascending, union sizes [B, HKV], S_heads [B, HQ, P],
+    S_group [B, HKV, P])."""
+    q = np.asarray(q_proxy, dtype=np.float64)
+    B, HQ = q.shape[:2]
+    HKV = np.asarray(k_src).shape[1]
+    g = HQ // HKV
+    P = prefix_len(L, window)
+    k = vl_count(P, rho_ppm)
+    ku = vl_count_heads(P, rho_ppm, g)
+    S_heads = head_scores(q, k_src, P)
+    idx_heads = topk_ascending(S_heads, k)
+    S_group = scores(proxy_sum(q, HKV), k_src, P)
+    idx_kv = np.zeros((B, HKV, ku), dtype=np.int64)
+    usize = np.zeros((B, HKV), dtype=np.int64)
+    for b in range(B):
+        for kh in range(HKV):
+            own = idx_heads[b, kh * g:(kh + 1) * g]
+            usize[b, kh] = len(set(own.ravel().tolist()))
+            idx_kv[b, kh] = union_fill(own, S_group[b, kh], ku)
+    return idx_heads, idx_kv, usize, S_heads, S_group
+
+
 # --- Eq. 4: the softmax-mass score (an alternative to Algorithm 1's) -------
 #
 # Eq. 4 defines the vertical-line score as the accumulated column mass

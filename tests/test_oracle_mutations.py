@@ -22,7 +22,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 PINS = {
     "quant": ["tests/test_oracle_quant.py"],
-    "select": ["tests/test_oracle_select.py"],
+    "select": ["tests/test_oracle_select.py", "tests/test_oracle_select_heads.py"],
     "attention": ["tests/test_oracle_attention.py"],
     "prefill": ["tests/test_oracle_prefill.py"],
     "accounting": ["tests/test_oracle_accounting.py"],
@@ -55,6 +55,12 @@ MUTATIONS = [
     ("select", "A = e / e.sum(axis=1, keepdims=True)                  # softmax over the L keys",
      "A = e / e.sum(axis=0, keepdims=True)                  # softmax over the L keys",
      "mass normalised over the rows"),
+    ("select", "u = q.sum(axis=2).reshape(B, HKV, g, d)", "u = q.sum(axis=2).reshape(B, g, HKV, d).swapaxes(1, 2)",
+     "query head to KV head strided"),
+    ("select", "order = np.lexsort((rest, -np.asarray(S_group, dtype=np.float64)[rest]))",
+     "order = np.lexsort((rest, np.asarray(S_group, dtype=np.float64)[rest]))", "fill by the lowest group score"),
+    ("select", "u = q.sum(axis=2).reshape(B, HKV, g, d)", "u = q[:, :, -1].reshape(B, HKV, g, d)",
+     "head score from one proxy"),
     ("select", "Q = q[b, kh * g:(kh + 1) * g].reshape(g * T, d)", "Q = q[b, kh::HKV].reshape(g * T, d)",
      "mass GQA grouping strided"),
     ("attention", "a = 1.0 / math.sqrt(d) if alpha is None else alpha",
