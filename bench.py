@@ -167,7 +167,8 @@ def prefill_measure(dev, lengths, reps=5, warmup=3, windows=("fixed", "band")):
         out = torch.empty(B, HQ, Lc, D, dtype=torch.bfloat16, device=dev)
         err = torch.zeros(1, dtype=torch.int32, device=dev)
         flops = 4.0 * D * HQ * Lc * (Lc + 1) / 2
-        for win, (name, dt) in [(w, x) for w in windows for x in (("fp8", L.PREFILL_FP8), ("int8", L.PREFILL_INT8))]:
+        for win, (name, dt) in [(w, x) for w in windows for x in (("fp8", L.PREFILL_FP8), ("int8", L.PREFILL_INT8),
+                                                                   ("fp4", L.PREFILL_FP4))]:
             fn = hyq.hyq_prefill_attention_band if win == "band" else hyq.hyq_prefill_attention
             ws = hyq.workspace(cfg, L.OP_PREFILL_BAND if win == "band" else L.OP_PREFILL, Lc, dev)
             for _ in range(warmup):
@@ -184,12 +185,14 @@ def prefill_measure(dev, lengths, reps=5, warmup=3, windows=("fixed", "band")):
             del ws
             ms = statistics.median(times)
             tf = flops / (ms * 1e-3) / 1e12
-            peak = peaks["fp8"] if name == "fp8" else peaks["bf16"]
+            peak = peaks["bf16"] if name == "int8" else peaks["fp8"]
             res.append({"seq_len": Lc, "dtype": name, "window": win, "ms": ms, "tflops": tf,
                         "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
                                      "frac": tf / peak,
-                                     "peak_source": (peaks["source"] + (" x 2 (nominal fp8/bf16)" if name == "fp8"
-                                                                        else " (INT8 codes run on the bf16 pipe)"))},
+                                     "peak_source": peaks["source"] + {
+                                         "fp8": " x 2 (nominal fp8/bf16)",
+                                         "fp4": " x 2 (e2m1 codes on kind::f8f6f4, the fp8 instruction kind)",
+                                         "int8": " (INT8 codes run on the bf16 pipe)"}[name]},
                         "device_error_word": hyq.hyq_read_device_error(err)})
         del q, k, v, out
     return res

@@ -40,7 +40,7 @@ COUNTS = 8
 CNT_NQ, CNT_NVL, CNT_NTAIL, CNT_LEN, CNT_RING_N, CNT_RING_POS = range(6)
 LAYOUT_FIELDS = ("qblocks", "vl_k", "vl_v", "vl_idx", "tail_k", "tail_v", "q_ring", "counts", "err")
 OP_SELECT, OP_DECODE, OP_PREFILL, OP_SELECT_MASS, OP_PREFILL_BAND = 1, 2, 3, 4, 5
-PREFILL_INT8, PREFILL_FP8 = 1, 2
+PREFILL_INT8, PREFILL_FP8, PREFILL_FP4 = 1, 2, 3
 VL_PER_KV_HEAD, VL_PER_QUERY_HEAD = 0, 1
 
 # Every symbol include/hyq.h declares.

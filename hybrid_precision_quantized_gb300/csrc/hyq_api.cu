@@ -294,7 +294,7 @@ static hyq_status prefill_call(const hyq_config* c, int32_t dtype, const void* q
                                void* out, int32_t* err, void* ws, size_t ws_bytes, hyq_stream_t s, bool band) {
   hyq_status st = hyq_config_check(c);
   if (st != HYQ_OK) return st;
-  if (dtype != HYQ_PREFILL_INT8 && dtype != HYQ_PREFILL_FP8) return HYQ_ERR_INVALID_ARG;
+  if (dtype != HYQ_PREFILL_INT8 && dtype != HYQ_PREFILL_FP8 && dtype != HYQ_PREFILL_FP4) return HYQ_ERR_INVALID_ARG;
   if (L < 0 || L > c->capacity) return HYQ_ERR_CAPACITY;
   if (L == 0) return HYQ_OK;
   if (ldq < L || ldk < L) return HYQ_ERR_INVALID_ARG;

@@ -25,9 +25,13 @@
 //     the two halves' (max, sum, O) merge once at the end.  The MMA threads
 //     share schedulers with softmax warps, so their loops are kept to a few
 //     instructions, and the two products are issued from two threads so
-//     that neither's waits hold back the other.  The quantised segment uses e4m3 codes (kind::f8f6f4) or INT8
-//     codes held exactly as BF16 integers (kind::f16; sm_103a has no integer
-//     tensor-core MMA); the full-precision segment uses BF16.  P.V runs in
+//     that neither's waits hold back the other.  The quantised segment uses e4m3 codes or e2m1 (FP4)
+//     codes (kind::f8f6f4; an e2m1 operand row keeps 16 elements in each
+//     16-byte chunk, packed in its first 8 bytes with element 2i in the low
+//     nibble of byte i, the other 8 bytes unread, so that an MMA takes 32
+//     elements from 32 bytes as with e4m3) or INT8 codes held exactly as
+//     BF16 integers (kind::f16; sm_103a has no integer tensor-core MMA); the
+//     full-precision segment uses BF16.  P.V runs in
 //     BF16 with the value codes (exact in BF16) and the value scale folded
 //     into P.
 //
@@ -76,6 +80,13 @@ constexpr int kSmemBytes = kSmemUsed + 1024;  // room to align the base
 
 constexpr uint32_t kIdescBF16 = tc_idesc(kTcBF16, kTcBF16, kRows, kKeys);
 constexpr uint32_t kIdescE4M3 = tc_idesc(kTcE4M3, kTcE4M3, kRows, kKeys);
+constexpr uint32_t kTcE2M1 = 5;  // kind::f8f6f4 operand format e2m1
+constexpr uint32_t kIdescE2M1 = tc_idesc(kTcE2M1, kTcE2M1, kRows, kKeys);
+
+// Code types of the quantised segment (the HYQ_PREFILL_* values).
+constexpr int kDtInt8 = HYQ_PREFILL_INT8, kDtFp8 = HYQ_PREFILL_FP8, kDtFp4 = HYQ_PREFILL_FP4;
+// c_B: the largest code magnitude.
+__host__ __device__ constexpr float code_max(int dt) { return dt == kDtFp8 ? 448.f : dt == kDtFp4 ? 6.f : 127.f; }
 
 struct PackParams {
   const __nv_bfloat16* k;  // [B][HKV][ldk][128]
@@ -172,6 +183,53 @@ __device__ __forceinline__ uint8_t code_f8_bits(float x, float s) {
   return __nv_cvt_float_to_fp8(code_f8(x, s), __NV_SATFINITE, __NV_E4M3);  // exact: an e4m3 value
 }
 
+// e2m1 (FP4): the value nearest to x / s among 0, 0.5, 1, 1.5, 2, 3, 4, 6
+// and their negatives, ties to the even code (the value with a zero fraction
+// bit), saturating at +-6.  Its midpoints are the odd multiples of 1/4 below
+// 2, then 2.5, 3.5 and 5; h is half the spacing there.
+__device__ __forceinline__ float e2m1_nearest(float a) {  // a >= 0
+  return a <= 0.25f ? 0.f : a < 0.75f ? 0.5f : a <= 1.25f ? 1.f : a < 1.75f ? 1.5f
+       : a <= 2.5f  ? 2.f : a < 3.5f  ? 3.f  : a <= 5.f   ? 4.f : 6.f;
+}
+
+__device__ __forceinline__ float code_f4(float x, float s) {
+  const float t = quotient(x, s);
+  const float a = fabsf(t);
+  const float c = copysignf(e2m1_nearest(a), t);
+  float h = 0.f;
+  if (a < 2.f) {
+    const float u = a * 4.f;  // exact
+    if (u == floorf(u) && (__float2int_rz(u) & 1)) h = 0.25f;
+  } else if (a == 2.5f || a == 3.5f) {
+    h = 0.5f;
+  } else if (a == 5.f) {
+    h = 1.f;
+  }
+  return h > 0.f ? past_midpoint(x, s, t, t - h, t + h, c) : c;
+}
+
+// The 4-bit pattern of an e2m1 value c: sign, two exponent bits, one
+// fraction bit (zero as +0).
+__device__ __forceinline__ uint32_t e2m1_bits(float c) {
+  const float a = fabsf(c);
+  const uint32_t m = a < 2.f ? static_cast<uint32_t>(a * 2.f)          // 0, 0.5, 1, 1.5 -> 0..3
+                             : a == 2.f ? 4u : a == 3.f ? 5u : a == 4.f ? 6u : 7u;
+  return (c < 0.f ? 8u : 0u) | m;
+}
+
+// Sixteen consecutive elements x[0..15] (BF16 in two uint4) as the 16-byte
+// operand chunk of e2m1 codes: 8 bytes, element 2i in the low nibble of
+// byte i, then 8 bytes the tensor core does not read (zeros).
+__device__ __forceinline__ uint4 pack_f4x16(const uint4& lo, const uint4& hi, float s) {
+  uint32_t w[2] = {0u, 0u};
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    const float x = bf16_at(e < 8 ? lo : hi, e & 7);
+    w[e >> 3] |= e2m1_bits(code_f4(x, s)) << (4 * (e & 7));
+  }
+  return make_uint4(w[0], w[1], 0u, 0u);
+}
+
 // Number of entries <= x in the ascending array a[0..n).
 __device__ __forceinline__ int count_le(const int32_t* a, int n, int32_t x) {
   int lo = 0, hi = n;
@@ -218,13 +276,13 @@ __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
 }
 __device__ __forceinline__ uint64_t f2_splat(float v) { return f2_pack(v, v); }
 __device__ __forceinline__ float f2_lo(uint64_t v) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  float lo;
+  asm("{\n .reg .b32 t;\n mov.b64 {%0, t}, %1;\n}" : "=f"(lo) : "l"(v));
   return lo;
 }
 __device__ __forceinline__ float f2_hi(uint64_t v) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  float hi;
+  asm("{\n .reg .b32 t;\n mov.b64 {t, %0}, %1;\n}" : "=f"(hi) : "l"(v));
   return hi;
 }
 __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
@@ -265,7 +323,7 @@ __device__ __forceinline__ float block_max(float v, float* red, int nwarps) {
 // quantised prefix, the full-precision list, or (per-query band, ntb > 0)
 // the BF16 images of all positions in order.
 // ---------------------------------------------------------------------------
-template <bool kFp8>
+template <int kDt>
 __global__ void __launch_bounds__(256) pack_kernel(const __grid_constant__ PackParams p) {
   __shared__ float vs[kScaleTile][HYQ_D + 1];
   __shared__ int32_t spos[kScaleTile];
@@ -342,7 +400,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const __grid_constant__ PackP
       ak = fmaxf(ak, fabsf(bf16_at(kr[e >> 3], e & 7)));
       av = fmaxf(av, fabsf(bf16_at(vr[e >> 3], e & 7)));
     }
-    const float cb = kFp8 ? 448.f : 127.f;
+    const float cb = code_max(kDt);
     ak = block_max(ak, red, 8);
     av = block_max(av, red, 8);
     sk = __fdiv_rn(ak, cb);
@@ -354,7 +412,12 @@ __global__ void __launch_bounds__(256) pack_kernel(const __grid_constant__ PackP
   }
 
   // Key image.
-  if (quant && kFp8) {
+  if (quant && kDt == kDtFp4) {
+    // dims 32qq .. 32qq+31: chunks 2qq and 2qq+1 of the row
+    uint8_t* img = p.kq + (bh * p.ntq + tile) * (size_t)kImg8;
+    *reinterpret_cast<uint4*>(img + swz(key, 2 * qq)) = pack_f4x16(kr[0], kr[1], sk);
+    *reinterpret_cast<uint4*>(img + swz(key, 2 * qq + 1)) = pack_f4x16(kr[2], kr[3], sk);
+  } else if (quant && kDt == kDtFp8) {
     uint8_t* img = p.kq + (bh * p.ntq + tile) * (size_t)kImg8;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {  // two 16-byte chunks of 16 codes
@@ -399,7 +462,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const __grid_constant__ PackP
   for (int e = 0; e < 32; ++e) {
     const float x = bf16_at(vr[e >> 3], e & 7);
     float y = x;
-    if (quant) y = kFp8 ? code_f8(x, sv) : code_i8(x, sv);
+    if (quant) y = kDt == kDtFp8 ? code_f8(x, sv) : kDt == kDtFp4 ? code_f4(x, sv) : code_i8(x, sv);
     vs[r][32 * qq + e] = y;
   }
   __syncthreads();
@@ -425,7 +488,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const __grid_constant__ PackP
 // masks keys after the row (j <= i).  Per-query band: the quantised prefix
 // and the vertical lines mask j <= i - W, the band tiles i - W < j <= i.
 // ---------------------------------------------------------------------------
-template <bool kFp8, bool kBand>
+template <int kDt, bool kBand>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ MainParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -456,7 +519,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   const size_t bh = (size_t)b * p.HKV + kh;
   const int32_t* kpos = p.kpos + bh * p.ntq * kKeys;
   const int32_t* fpos = p.fpos + bh * p.ntf * kKeys;
-  constexpr int kKImg = kFp8 ? kImg8 : kImg16;
+  constexpr bool kF8F6F4 = kDt != kDtInt8;  // quantised S on kind::f8f6f4
+  constexpr int kKImg = kF8F6F4 ? kImg8 : kImg16;
 
   if (tid == 0) {
     mbar_init(qready, kSoft);
@@ -535,8 +599,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     amax = red[0];
 #pragma unroll
     for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[w]);
-    const float sq = __fdiv_rn(amax, kFp8 ? 448.f : 127.f);
-    if (kFp8) {
+    const float sq = __fdiv_rn(amax, code_max(kDt));
+    if (kDt == kDtFp4) {
+      // dims 64hf .. 64hf+63: chunks 4hf .. 4hf+3
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<uint4*>(sm + kOffQc + swz(rr, 4 * hf + c)) = pack_f4x16(qv[2 * c], qv[2 * c + 1], sq);
+    } else if (kDt == kDtFp8) {
 #pragma unroll
       for (int c16 = 0; c16 < 4; ++c16) {  // 16 codes per chunk: chunks 4hf .. 4hf+3
         uint32_t w[4];
@@ -817,9 +886,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           if (!ok) break;
           tc_fence_after();
           const uint64_t dK = dK0 + sk * kStageStep;
-          if (kFp8 && j < nqt) {
+          if (kDt == kDtFp8 && j < nqt) {
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) tc_mma_f8(tS, dQc + 2 * ks, dK + 2 * ks, kIdescE4M3, ks > 0);
+          } else if (kDt == kDtFp4 && j < nqt) {  // 32 elements (two 16-byte chunks) per MMA
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) tc_mma_f8(tS, dQc + 2 * ks, dK + 2 * ks, kIdescE2M1, ks > 0);
           } else {
             const uint64_t dA = j < nqt ? dQc : dQ;
 #pragma unroll
@@ -882,12 +954,12 @@ struct WsLayout {
   size_t kq, vq, kf, vf, kb, vb, kpos, fpos, sk, sv, total;
 };
 
-WsLayout ws_layout(const hyq_config* c, bool fp8, int32_t ntq, int32_t ntf, int32_t ntb) {
+WsLayout ws_layout(const hyq_config* c, bool k8, int32_t ntq, int32_t ntf, int32_t ntb) {
   const size_t bh = (size_t)c->batch * c->num_kv_heads;
   WsLayout w{};
   size_t off = 0;
   w.kq = off;
-  off = align_up(off + bh * ntq * (size_t)(fp8 ? kImg8 : kImg16));
+  off = align_up(off + bh * ntq * (size_t)(k8 ? kImg8 : kImg16));
   w.vq = off;
   off = align_up(off + bh * ntq * (size_t)kImg16);
   w.kf = off;
@@ -910,14 +982,14 @@ WsLayout ws_layout(const hyq_config* c, bool fp8, int32_t ntq, int32_t ntf, int3
   return w;
 }
 
-template <bool kFp8, bool kBand>
+template <int kDt, bool kBand>
 cudaError_t launch_main(const MainParams& mp, dim3 grid, cudaStream_t s) {
   static std::atomic<uint64_t> done{0};
   const cudaError_t e = hyq_once_per_device(done, [] {
-    return cudaFuncSetAttribute(prefill_kernel<kFp8, kBand>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    return cudaFuncSetAttribute(prefill_kernel<kDt, kBand>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   });
   if (e != cudaSuccess) return e;
-  prefill_kernel<kFp8, kBand><<<grid, kThreads, kSmemBytes, s>>>(mp);
+  prefill_kernel<kDt, kBand><<<grid, kThreads, kSmemBytes, s>>>(mp);
   return cudaGetLastError();
 }
 
@@ -930,7 +1002,7 @@ int32_t tiles_of(int32_t n) { return (n + kKeys - 1) / kKeys; }
 size_t hyq_prefill_ws_bytes(const hyq_config* c, int dtype, int32_t L, int32_t kvl, bool band) {
   const int32_t P = L - c->window > 0 ? L - c->window : 0;
   const int32_t nq = P - kvl, nfp = band ? kvl : kvl + (L - P);
-  return ws_layout(c, dtype == HYQ_PREFILL_FP8, tiles_of(nq), tiles_of(nfp), band ? tiles_of(L) : 0).total;
+  return ws_layout(c, dtype != HYQ_PREFILL_INT8, tiles_of(nq), tiles_of(nfp), band ? tiles_of(L) : 0).total;
 }
 
 size_t hyq_prefill_ws_bytes_hint(const hyq_config* c, int32_t L, bool band) {
@@ -945,11 +1017,11 @@ size_t hyq_prefill_ws_bytes_hint(const hyq_config* c, int32_t L, bool band) {
 cudaError_t hyq_launch_prefill(const hyq_config* c, int dtype, const void* q, int64_t ldq, const void* k,
                                const void* v, int64_t ldk, int32_t L, const int32_t* vl, int32_t kvl, void* out,
                                void* ws, int32_t* err, cudaStream_t s, bool band) {
-  const bool fp8 = dtype == HYQ_PREFILL_FP8;
+  const bool k8 = dtype != HYQ_PREFILL_INT8;  // 8-bit key images (e4m3, or packed e2m1)
   const int32_t P = L - c->window > 0 ? L - c->window : 0;
   const int32_t nq = P - kvl, nfp = band ? kvl : kvl + (L - P);
   const int32_t ntq = tiles_of(nq), ntf = tiles_of(nfp), ntb = band ? tiles_of(L) : 0;
-  const WsLayout w = ws_layout(c, fp8, ntq, ntf, ntb);
+  const WsLayout w = ws_layout(c, k8, ntq, ntf, ntb);
   uint8_t* base = static_cast<uint8_t*>(ws);
 
   PackParams pp{};
@@ -978,8 +1050,9 @@ cudaError_t hyq_launch_prefill(const hyq_config* c, int dtype, const void* q, in
   pp.ntf = ntf;
   pp.ntb = ntb;
   dim3 g1(2 * ntq + 2 * ntf + 2 * ntb, c->num_kv_heads, c->batch);
-  if (fp8) pack_kernel<true><<<g1, 256, 0, s>>>(pp);
-  else pack_kernel<false><<<g1, 256, 0, s>>>(pp);
+  if (dtype == HYQ_PREFILL_FP8) pack_kernel<kDtFp8><<<g1, 256, 0, s>>>(pp);
+  else if (dtype == HYQ_PREFILL_FP4) pack_kernel<kDtFp4><<<g1, 256, 0, s>>>(pp);
+  else pack_kernel<kDtInt8><<<g1, 256, 0, s>>>(pp);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
@@ -1007,6 +1080,9 @@ cudaError_t hyq_launch_prefill(const hyq_config* c, int dtype, const void* q, in
   mp.W = c->window;
   mp.alpha_log2e = kLog2e / sqrtf(static_cast<float>(HYQ_D));
   dim3 g2(c->num_q_heads, (L + kRows - 1) / kRows, c->batch);
-  if (fp8) return band ? launch_main<true, true>(mp, g2, s) : launch_main<true, false>(mp, g2, s);
-  return band ? launch_main<false, true>(mp, g2, s) : launch_main<false, false>(mp, g2, s);
+  if (dtype == HYQ_PREFILL_FP8)
+    return band ? launch_main<kDtFp8, true>(mp, g2, s) : launch_main<kDtFp8, false>(mp, g2, s);
+  if (dtype == HYQ_PREFILL_FP4)
+    return band ? launch_main<kDtFp4, true>(mp, g2, s) : launch_main<kDtFp4, false>(mp, g2, s);
+  return band ? launch_main<kDtInt8, true>(mp, g2, s) : launch_main<kDtInt8, false>(mp, g2, s);
 }

@@ -193,6 +193,7 @@ typedef struct {
 
 #define HYQ_PREFILL_INT8 1
 #define HYQ_PREFILL_FP8 2
+#define HYQ_PREFILL_FP4 3
 
 /* Human-readable name of a status. */
 const char *hyq_status_string(hyq_status s);
@@ -380,13 +381,15 @@ hyq_status hyq_decode_attention(const hyq_config *cfg, const void *q, const hyq_
  *   x_j = a q^_i . k^_j and v_j = v^_j, with
  *   - the quantised-prefix positions taken in ascending order and cut into
  *     tiles of 64 (the last one may be shorter); per tile one scale for K
- *     and one for V: s = fl32(max|x| / c) over the tile, c = 127 (INT8) or
- *     448 (FP8 e4m3);
+ *     and one for V: s = fl32(max|x| / c) over the tile, c = 127 (INT8),
+ *     448 (FP8 e4m3) or 6 (FP4 e2m1);
  *   - one scale for Q per block of 128 consecutive rows of one head
  *     (rows 128m .. 128m+127, those < L);
- *   - codes of t = fl32(x / s): INT8 rint (ties to even) clamped to +-127,
- *     FP8 the nearest e4m3 value (ties to even, saturating); x^ = code * s.
- *   dtype  HYQ_PREFILL_INT8 or HYQ_PREFILL_FP8
+ *   - the code of x is the grid value nearest to the exact quotient x / s,
+ *     ties to the even code: INT8 the integers -127..127, FP8 the e4m3
+ *     values (saturating at +-448), FP4 the e2m1 values 0, 0.5, 1, 1.5, 2,
+ *     3, 4, 6 and their negatives (saturating at +-6); x^ = code * s.
+ *   dtype  HYQ_PREFILL_INT8, HYQ_PREFILL_FP8 or HYQ_PREFILL_FP4
  *   q      device bf16 [B][HQ][ldq][128]; rows 0..L-1 are used
  *   k, v   device bf16 [B][HKV][ldk][128]
  *   vl_idx device int32 [B][HKV][kvl], strictly ascending in [0, P)

@@ -28,7 +28,11 @@ Readings (the paper leaves these open):
   x is the grid value nearest to the exact quotient ``x / s``, ties to the
   even code: INT8 the integers -127..127, FP8 the e4m3 values (bias 7,
   three fraction bits, subnormals below 2^-6, largest 448; values beyond it
-  take +-448).  A block of zeros gets ``s = 0`` and zero codes;
+  take +-448), FP4 the e2m1 values 0, 0.5, 1, 1.5, 2, 3, 4, 6 and their
+  negatives (c_B = 6: the paper names INT4/FP4 backends for the low-bit
+  segment without further detail, and the same per-tile symmetric rule with
+  the format's largest value is the plain reading).  A block of zeros gets
+  ``s = 0`` and zero codes;
 * ``band=True`` takes the window per query instead (a diagonal band): query
   ``i`` sees the keys ``(i - W, i]`` in BF16, the vertical lines at or
   before ``i - W`` in BF16 and the other keys at or before ``i - W`` from
@@ -48,7 +52,7 @@ import math
 import numpy as np
 import torch
 
-C_B = {"int8": 127.0, "fp8": 448.0}
+C_B = {"int8": 127.0, "fp8": 448.0, "fp4": 6.0}
 KEY_TILE = 64
 QUERY_BLOCK = 128
 
@@ -64,7 +68,16 @@ def e4m3_values() -> np.ndarray:
     return np.array(vals, dtype=np.float64)
 
 
-_GRIDS = {"int8": np.arange(128, dtype=np.float64), "fp8": e4m3_values()}
+def e2m1_values() -> np.ndarray:
+    """The non-negative e2m1 (FP4) values, ascending, from the format:
+    exponent bias 1, one fraction bit, subnormal m 2^-1 (exponent field 0),
+    normals (1 + m/2) 2^(e-1); no infinities or NaN, so the largest is 6.
+    The index of a value is its 3-bit code (even index = even code)."""
+    vals = [m * 0.5 if e == 0 else (1 + m / 2) * 2.0 ** (e - 1) for e in range(4) for m in range(2)]
+    return np.array(vals, dtype=np.float64)
+
+
+_GRIDS = {"int8": np.arange(128, dtype=np.float64), "fp8": e4m3_values(), "fp4": e2m1_values()}
 
 
 def nearest_grid_index(a, s, grid) -> np.ndarray:

@@ -123,13 +123,14 @@ def tie_rows(seed, shape, bits=4):
 def double_rounding_cases(dtype, want=16):
     """Tile maxima A and values x (BF16, 0 < x <= A) for which rounding the
     float32 quotient fl32(x / s) to the code grid, s = RN_fp32(A / c) (c = 127
-    for INT8, 448 for FP8), gives another code than rounding the exact
-    quotient x / s.  Exhaustive over the 128 BF16 mantissas of A in [1, 2)
+    for INT8, 448 for FP8, 6 for FP4), gives another code than rounding the
+    exact quotient x / s.  Exhaustive over the 128 BF16 mantissas of A in [1, 2)
     and every positive BF16 x <= A (scaling A and x by a power of two scales s
     exactly and changes nothing); returned largest quotient first, at most
     ``want`` pairs (A, x)."""
-    from oracle.prefill import e4m3_values, nearest_grid_index
-    c, grid = (127.0, np.arange(128.0)) if dtype == "int8" else (448.0, e4m3_values())
+    from oracle.prefill import e2m1_values, e4m3_values, nearest_grid_index
+    c, grid = {"int8": (127.0, np.arange(128.0)), "fp8": (448.0, e4m3_values()),
+               "fp4": (6.0, e2m1_values())}[dtype]
     u = torch.arange(1, 0x4000, dtype=torch.int32).to(torch.int16).view(torch.bfloat16).double().numpy()
     u = u[np.isfinite(u) & (u > 0)]
     cases = []

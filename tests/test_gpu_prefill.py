@@ -1,5 +1,5 @@
 """GPU parity of the hybrid prefill operator (Eq. 6-7, Algorithm 2) against
-the oracle's float64 restatement, INT8 and FP8 main paths.
+the oracle's float64 restatement, INT8, FP8 and FP4 (e2m1) main paths.
 
 The vertical-line set fed to the GPU is the oracle's own selection from the
 last min(64, L) queries, so the attention comparison does not depend on
@@ -22,7 +22,7 @@ from tests.gpu_util import assert_prefill_close, to_np
 
 pytestmark = pytest.mark.gpu
 
-DT = {"int8": L.PREFILL_INT8, "fp8": L.PREFILL_FP8}
+DT = {"int8": L.PREFILL_INT8, "fp8": L.PREFILL_FP8, "fp4": L.PREFILL_FP4}
 
 
 def vl_for(c, Lc, W, ppm):
@@ -48,7 +48,7 @@ def run_gpu(c, Lc, W, ppm, dtype, idx, ws_len=None, band=False):
     return to_np(out)
 
 
-@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+@pytest.mark.parametrize("dtype", ["int8", "fp8", "fp4"])
 @pytest.mark.parametrize("seed,B,HQ,HKV,Lc,W,ppm", [
     (1, 1, 4, 2, 300, 64, 50_000),      # a few tiles, ragged tails in both lists
     (2, 1, 8, 2, 1000, 128, 50_000),
@@ -65,7 +65,7 @@ def test_prefill_parity(hyq, dtype, seed, B, HQ, HKV, Lc, W, ppm):
     assert_prefill_close(got, want, a, what=f"{dtype} L={Lc}")
 
 
-@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+@pytest.mark.parametrize("dtype", ["int8", "fp8", "fp4"])
 @pytest.mark.parametrize("Lc,W,ppm,what", [
     (1, 128, 50_000, "single position"),
     (100, 128, 50_000, "sequence inside the window: all BF16"),
@@ -106,7 +106,7 @@ def test_prefill_bad_vertical_lines_flagged(hyq):
     assert hyq_read_device_error(err) & L.DEVERR_INDEX
 
 
-@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+@pytest.mark.parametrize("dtype", ["int8", "fp8", "fp4"])
 def test_prefill_llama_shaped_8k_sampled(hyq, dtype):
     """Llama-3.1-8B-shaped heads at 8K: every head of four query blocks (first,
     two middle, last) against the oracle."""
@@ -122,7 +122,7 @@ def test_prefill_llama_shaped_8k_sampled(hyq, dtype):
         assert_prefill_close(got[:, :, rows], want[:, :, rows], a[:, :, rows], what=f"{dtype} block {blk}")
 
 
-@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+@pytest.mark.parametrize("dtype", ["int8", "fp8", "fp4"])
 def test_prefill_llama_shaped_32k_sampled(hyq, dtype):
     """The benchmark's prefill workload (Llama-3.1-8B-shaped heads, causal 32K,
     W 128, rho 5%): the GPU computes every head and query block; the oracle
@@ -149,7 +149,7 @@ def oracle_band(c, idx, W, dtype, **kw):
                           idx if idx.shape[-1] else None, W, dtype, return_abs=True, band=True, **kw)
 
 
-@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+@pytest.mark.parametrize("dtype", ["int8", "fp8", "fp4"])
 @pytest.mark.parametrize("seed,B,HQ,HKV,Lc,W,ppm", [
     (41, 1, 4, 2, 300, 64, 50_000),     # a few tiles, ragged tails
     (42, 1, 8, 2, 1000, 128, 50_000),   # the band spans two key tiles per query block
@@ -165,7 +165,7 @@ def test_prefill_band_parity(hyq, dtype, seed, B, HQ, HKV, Lc, W, ppm):
     assert_prefill_close(got, want, a, what=f"band {dtype} L={Lc} W={W}")
 
 
-@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+@pytest.mark.parametrize("dtype", ["int8", "fp8", "fp4"])
 @pytest.mark.parametrize("Lc,W,ppm,what", [
     (1, 128, 50_000, "single position"),
     (100, 128, 50_000, "sequence inside the window: all BF16"),
@@ -192,7 +192,7 @@ def test_prefill_band_last_row_matches_fixed_window(hyq):
     np.testing.assert_allclose(band[:, :, -1], fixed[:, :, -1], rtol=1e-2, atol=2e-3)
 
 
-@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+@pytest.mark.parametrize("dtype", ["int8", "fp8", "fp4"])
 def test_prefill_band_llama_shaped_8k_sampled(hyq, dtype):
     """Llama-3.1-8B-shaped heads at 8K with the per-query band: every head of
     four query blocks (first, second, a middle one, last) against the oracle."""
@@ -207,7 +207,7 @@ def test_prefill_band_llama_shaped_8k_sampled(hyq, dtype):
         assert_prefill_close(got[:, :, rows], want[:, :, rows], a[:, :, rows], what=f"band {dtype} block {blk}")
 
 
-@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+@pytest.mark.parametrize("dtype", ["int8", "fp8", "fp4"])
 def test_prefill_band_llama_shaped_32k_sampled(hyq, dtype):
     """The benchmark's band workload (Llama-3.1-8B-shaped heads, causal 32K,
     W 128, rho 5%, the window read per query): the GPU computes every head
@@ -226,7 +226,7 @@ def test_prefill_band_llama_shaped_32k_sampled(hyq, dtype):
                                  what=f"band {dtype} head {hq} block {blk}")
 
 
-@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+@pytest.mark.parametrize("dtype", ["int8", "fp8", "fp4"])
 def test_prefill_codes_of_exact_quotients(hyq, dtype):
     """Values whose float32 quotient x / s lands exactly on a midpoint of the
     code grid while the exact quotient does not (found exhaustively, largest

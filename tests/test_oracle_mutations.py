@@ -75,6 +75,8 @@ MUTATIONS = [
      "perturbed logit scale"),
     ("attention", "Vq = fake_quant(V[:, :, :P, :], bits if bits_v is None else bits_v)",
      "Vq = fake_quant(V[:, :, :P, :], bits)", "values quantised at the key width"),
+    ("prefill", '"fp4": 6.0}', '"fp4": 4.0}', "FP4 c_B"),
+    ("prefill", "vals = [m * 0.5 if e == 0 else", "vals = [m * 0.25 if e == 0 else", "e2m1 subnormal step"),
     ("prefill", "lg = np.where(pos[None, :] <= rows[:, None], lg, -np.inf)",
      "lg = np.where(pos[None, :] < rows[:, None] + 2, lg, -np.inf)", "causal mask off by one"),
     ("prefill", "alpha * qb @ Kall[nq:].T], axis=1)", "alpha * qhat @ Kall[nq:].T], axis=1)",

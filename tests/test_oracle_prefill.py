@@ -25,14 +25,14 @@ def test_causal_reference_matches_torch():
     np.testing.assert_allclose(causal_attention(q, k, v), _sdpa_causal(q, k, v), rtol=1e-12, atol=1e-13)
 
 
-@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+@pytest.mark.parametrize("dtype", ["int8", "fp8", "fp4"])
 def test_window_covering_sequence_is_exact(dtype):
     q, k, v = _np(prefill_case(1, 1, 4, 2, 150, d=64))
     o = hybrid_prefill(q, k, v, None, window=150, dtype=dtype)
     np.testing.assert_allclose(o, _sdpa_causal(q, k, v), rtol=1e-12, atol=1e-13)
 
 
-@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+@pytest.mark.parametrize("dtype", ["int8", "fp8", "fp4"])
 def test_full_ratio_is_exact(dtype):
     c = prefill_case(2, 1, 4, 2, 300, d=64, window=32)
     q, k, v = _np(c)
@@ -65,7 +65,7 @@ def test_fp8_codes_are_e4m3_values_with_max_at_448():
     assert np.median(rel) < 2 ** -4                     # 3-bit mantissa
 
 
-@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+@pytest.mark.parametrize("dtype", ["int8", "fp8", "fp4"])
 def test_hybrid_beats_uniform_low_bit(dtype):
     c = prefill_case(5, 1, 4, 2, 512, d=128, window=64, sink_frac=0.02, sink_gain=20.0, q_gain=4.0)
     q, k, v = _np(c)
@@ -139,19 +139,19 @@ def _tie_inputs(grid, s, rng, n_rand):
     """Values x with x / s at exact midpoints of the grid, one float64 step
     either side of them, and random ones."""
     mids = (grid[:-1] + grid[1:]) / 2
-    pick = mids[rng.choice(len(mids), 40, replace=False)]
+    pick = mids[rng.choice(len(mids), min(40, len(mids)), replace=False)]
     xs = np.concatenate([pick * s, np.nextafter(pick * s, np.inf), np.nextafter(pick * s, -np.inf),
                          rng.uniform(0, grid[-1] * s, n_rand)])
     return np.concatenate([xs, -xs])
 
 
-@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+@pytest.mark.parametrize("dtype", ["int8", "fp8", "fp4"])
 @pytest.mark.parametrize("s_mant", [1.0, 3.0, 1.0 + 2.0 ** -23])
 def test_codes_are_nearest_to_the_exact_quotient(dtype, s_mant):
     """Codes against exact rational brute force: planted exact midpoints go
     to the even code, their float64 neighbours to the nearer code."""
-    from oracle.prefill import C_B, _codes, e4m3_values
-    grid = e4m3_values() if dtype == "fp8" else np.arange(128.0)
+    from oracle.prefill import C_B, _codes, e2m1_values, e4m3_values
+    grid = {"fp8": e4m3_values(), "fp4": e2m1_values()}.get(dtype, np.arange(128.0))
     s = float(np.float32(s_mant * 2.0 ** -7))
     rng = np.random.default_rng(13)
     x = _tie_inputs(grid, s, rng, 100)
@@ -205,7 +205,7 @@ def test_restricted_blocks_equal_full_computation():
     assert np.all(part[0, 0] == 0) and np.all(part[0, 1, 128:256] == 0)
 
 
-@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+@pytest.mark.parametrize("dtype", ["int8", "fp8", "fp4"])
 def test_abs_weighted_values(dtype):
     """``a`` is the operator applied to |V| (symmetric quantisation commutes
     with |.|), and bounds |o| by the triangle inequality."""
@@ -232,12 +232,16 @@ def _vl(P, n, seed, early=16):
 
 def _exactly_quantisable(seed, L, d, dtype):
     """Q [1,4,L,d], K, V [1,2,L,d] whose every tile quantises without error:
-    each value is a code (an integer in [-127, 127], or an e4m3 value) times
-    2^-7 (INT8) or 2^-9 (FP8), and every row holds the largest code, so every
+    each value is a code (an integer in [-127, 127], an e4m3 or an e2m1
+    value) times 2^-7 (INT8), 2^-9 (FP8) or 2^-2 (FP4), and every row holds
+    the largest code, so every
     tile's scale is exactly that power of two and x / s is the code itself."""
     rng = np.random.default_rng(seed)
     if dtype == "int8":
         codes, top, unit = np.arange(-127, 128, dtype=np.float64), 127.0, 2.0 ** -7
+    elif dtype == "fp4":
+        e = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+        codes, top, unit = np.array(sorted(set(e) | {-x for x in e})), 6.0, 2.0 ** -2
     else:
         codes, top, unit = np.array(sorted(_e4m3_values().values())), 448.0, 2.0 ** -9
 
@@ -248,7 +252,7 @@ def _exactly_quantisable(seed, L, d, dtype):
     return mat(4), mat(2), mat(2)
 
 
-@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+@pytest.mark.parametrize("dtype", ["int8", "fp8", "fp4"])
 @pytest.mark.parametrize("band", [False, True])
 def test_exactly_quantisable_inputs_give_exact_attention(dtype, band):
     """With quantisation error-free, either window reading is exact causal
@@ -261,7 +265,7 @@ def test_exactly_quantisable_inputs_give_exact_attention(dtype, band):
     np.testing.assert_allclose(o, causal_attention(q, k, v), rtol=1e-12, atol=1e-13)
 
 
-@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+@pytest.mark.parametrize("dtype", ["int8", "fp8", "fp4"])
 def test_band_rows_inside_window_are_full_precision(dtype):
     """Rows i < W have every key j <= i inside their band: exact attention,
     unlike the fixed window, which quantises them; later rows quantise the
@@ -277,7 +281,7 @@ def test_band_rows_inside_window_are_full_precision(dtype):
     assert np.abs(band[:, :, W + 8:] - ex[:, :, W + 8:]).max() > 1e-6
 
 
-@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+@pytest.mark.parametrize("dtype", ["int8", "fp8", "fp4"])
 def test_band_agrees_with_fixed_window_on_last_row_and_without_window(dtype):
     """The last row's band (P - 1, L - 1] is the fixed window [P, L); with
     W = 0 both readings quantise every key but the vertical lines."""
@@ -294,7 +298,7 @@ def test_band_agrees_with_fixed_window_on_last_row_and_without_window(dtype):
                                hybrid_prefill(q0, k0, v0, idx0, 0, dtype), rtol=1e-12, atol=1e-13)
 
 
-@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+@pytest.mark.parametrize("dtype", ["int8", "fp8", "fp4"])
 def test_band_window_covering_sequence_is_exact(dtype):
     q, k, v = _np(prefill_case(58, 1, 4, 2, 150, d=64))
     o = hybrid_prefill(q, k, v, None, window=150, dtype=dtype, band=True)
@@ -309,15 +313,15 @@ def test_band_restricted_blocks_equal_full_computation():
     np.testing.assert_array_equal(part[0, 3, 128:256], full[0, 3, 128:256])
 
 
-@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+@pytest.mark.parametrize("dtype", ["int8", "fp8", "fp4"])
 def test_double_rounding_cases_change_the_code_visibly(dtype):
     """The prefill tie workload: each planted value's exact code differs from
     the code of its rounded float32 quotient, by more than the parity
     tolerance once multiplied out at the test's scale (so a kernel that
     rounds twice fails the GPU test)."""
-    from oracle.prefill import C_B, _codes, e4m3_values, nearest_grid_index
+    from oracle.prefill import C_B, _codes, e2m1_values, e4m3_values, nearest_grid_index
     from tests.gpu_util import double_rounding_cases
-    grid = np.arange(128.0) if dtype == "int8" else e4m3_values()
+    grid = {"int8": np.arange(128.0), "fp8": e4m3_values(), "fp4": e2m1_values()}[dtype]
     cases = double_rounding_cases(dtype)
     assert len(cases) >= 8
     for A, x in cases:
@@ -328,3 +332,26 @@ def test_double_rounding_cases_change_the_code_visibly(dtype):
         twice = grid[nearest_grid_index(np.array([t32]), 1.0, grid)[0]] * s
         tol = 2e-3 + 1e-2 * abs(exact) + 2.0 ** -8 * abs(exact)
         assert abs(exact - twice) > tol, (A, x, exact, twice)
+
+
+def test_oracle_e2m1_table_is_the_two_bit_significand_grid():
+    """e2m1 has one fraction bit and a subnormal step of 1/2 at the bottom of
+    a two-bit exponent: its values are the multiples n/2 (0 <= n <= 12) whose
+    integer n has at most two significant bits."""
+    from oracle.prefill import C_B, e2m1_values
+    want = [n / 2 for n in range(13) if n == 0 or (n >> (n.bit_length() - 2 if n.bit_length() > 1 else 0))
+            << (n.bit_length() - 2 if n.bit_length() > 1 else 0) == n]
+    assert e2m1_values().tolist() == want == [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    assert C_B["fp4"] == 6.0
+
+
+def test_fp4_codes_are_e2m1_values_with_max_at_6():
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((64, 128)) * 3
+    xh, c, s = quantize_symmetric(x, 0, "fp4")          # per-channel scales
+    assert np.abs(c).max(axis=0).min() == 6.0
+    assert set(np.unique(np.abs(c)).tolist()) <= {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0}
+    # the nearest grid value: within half the local spacing (0.5 below 2, 1 to 4, 2 to 6)
+    t = np.abs(x) / s
+    half = np.where(t < 2, 0.25, np.where(t < 4, 0.5, 1.0))
+    assert np.all(np.abs(np.abs(c) - np.minimum(t, 6.0)) <= half + 1e-12)
