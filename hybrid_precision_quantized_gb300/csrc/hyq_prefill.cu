@@ -185,37 +185,33 @@ __device__ __forceinline__ uint8_t code_f8_bits(float x, float s) {
 
 // e2m1 (FP4): the value nearest to x / s among 0, 0.5, 1, 1.5, 2, 3, 4, 6
 // and their negatives, ties to the even code (the value with a zero fraction
-// bit), saturating at +-6.  Its midpoints are the odd multiples of 1/4 below
-// 2, then 2.5, 3.5 and 5; h is half the spacing there.
-__device__ __forceinline__ float e2m1_nearest(float a) {  // a >= 0
-  return a <= 0.25f ? 0.f : a < 0.75f ? 0.5f : a <= 1.25f ? 1.f : a < 1.75f ? 1.5f
-       : a <= 2.5f  ? 2.f : a < 3.5f  ? 3.f  : a <= 5.f   ? 4.f : 6.f;
-}
-
-__device__ __forceinline__ float code_f4(float x, float s) {
-  const float t = quotient(x, s);
-  const float a = fabsf(t);
-  const float c = copysignf(e2m1_nearest(a), t);
-  float h = 0.f;
-  if (a < 2.f) {
-    const float u = a * 4.f;  // exact
-    if (u == floorf(u) && (__float2int_rz(u) & 1)) h = 0.25f;
-  } else if (a == 2.5f || a == 3.5f) {
-    h = 0.5f;
-  } else if (a == 5.f) {
-    h = 1.f;
+// bit), saturating at +-6.  The magnitude code is the number of midpoints
+// m_k = 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5 that |x| / s passes: |x| - m_k s
+// is formed by one fused multiply-add from the exact product m_k s (m_k has
+// at most three significant bits), so its sign is exact, and at a tie
+// (zero) the code moves past m_k only toward an even code (odd k).  No
+// quotient is rounded on the way.  s = 0 (an all-zero tile) gives 0.
+__device__ __forceinline__ uint32_t e2m1_code(float x, float s) {
+  const float a = fabsf(x);
+  constexpr float kMid[7] = {0.25f, 0.75f, 1.25f, 1.75f, 2.5f, 3.5f, 5.f};
+  uint32_t m = 0;
+#pragma unroll
+  for (int k = 0; k < 7; ++k) {
+    const float d = fmaf(-kMid[k], s, a);
+    m += (d > 0.f || (d == 0.f && (k & 1))) ? 1u : 0u;
   }
-  return h > 0.f ? past_midpoint(x, s, t, t - h, t + h, c) : c;
+  if (!(s > 0.f)) m = 0;
+  return (x < 0.f && m != 0 ? 8u : 0u) | m;
 }
 
-// The 4-bit pattern of an e2m1 value c: sign, two exponent bits, one
-// fraction bit (zero as +0).
-__device__ __forceinline__ uint32_t e2m1_bits(float c) {
-  const float a = fabsf(c);
-  const uint32_t m = a < 2.f ? static_cast<uint32_t>(a * 2.f)          // 0, 0.5, 1, 1.5 -> 0..3
-                             : a == 2.f ? 4u : a == 3.f ? 5u : a == 4.f ? 6u : 7u;
-  return (c < 0.f ? 8u : 0u) | m;
+// The e2m1 value of a 4-bit pattern (sign, two exponent bits, one fraction bit).
+__device__ __forceinline__ float e2m1_value(uint32_t c) {
+  const uint32_t m = c & 7u;
+  const float v = m < 4u ? 0.5f * static_cast<float>(m) : static_cast<float>(1u << ((m >> 1) - 1u)) * (m & 1u ? 1.5f : 1.f);
+  return c & 8u ? -v : v;
 }
+
+__device__ __forceinline__ float code_f4(float x, float s) { return e2m1_value(e2m1_code(x, s)); }
 
 // Sixteen consecutive elements x[0..15] (BF16 in two uint4) as the 16-byte
 // operand chunk of e2m1 codes: 8 bytes, element 2i in the low nibble of
@@ -223,10 +219,7 @@ __device__ __forceinline__ uint32_t e2m1_bits(float c) {
 __device__ __forceinline__ uint4 pack_f4x16(const uint4& lo, const uint4& hi, float s) {
   uint32_t w[2] = {0u, 0u};
 #pragma unroll
-  for (int e = 0; e < 16; ++e) {
-    const float x = bf16_at(e < 8 ? lo : hi, e & 7);
-    w[e >> 3] |= e2m1_bits(code_f4(x, s)) << (4 * (e & 7));
-  }
+  for (int e = 0; e < 16; ++e) w[e >> 3] |= e2m1_code(bf16_at(e < 8 ? lo : hi, e & 7), s) << (4 * (e & 7));
   return make_uint4(w[0], w[1], 0u, 0u);
 }
 

@@ -103,7 +103,7 @@ class PeriodRunner:
                 n_sel = 5 if self.select is L.hyq_select_vertical_mass else (
                     6 if self.cfg.vl_mode == L.VL_PER_QUERY_HEAD else 3)
                 n += (n_sel if k > 0 else 0) + \
-                    (2 if self.L_end - self.cfg.window - k > 0 else 1)
+                    (3 if self.L_end - self.cfg.window > 0 else 1)  # rows, marks, gather
         return n
 
     def _decodes(self, t):
