@@ -183,6 +183,20 @@ __device__ __forceinline__ uint8_t code_f8_bits(float x, float s) {
   return __nv_cvt_float_to_fp8(code_f8(x, s), __NV_SATFINITE, __NV_E4M3);  // exact: an e4m3 value
 }
 
+// INT8 fast path with r = RN(1/s): t = fl32(x r) lies within 2^-23 |x / s|
+// of the exact quotient, under 2^-16 for |t| < 2^8, so rounding t gives the
+// code of x / s unless its fractional part is within 2^-15 of 1/2; those
+// elements take the exact path above.  (The same gate for e4m3, around the
+// fraction pattern of its midpoints, measured no faster and is not used.)
+__device__ __forceinline__ float recip(float s) { return s > 0.f ? __frcp_rn(s) : 0.f; }
+
+__device__ __forceinline__ float code_i8_fast(float x, float s, float r) {
+  const float t = x * r;
+  if (s > 0.f && fabsf(t - floorf(t) - 0.5f) > 3.0517578125e-05f) return fminf(fmaxf(rintf(t), -127.f), 127.f);
+  return code_i8(x, s);
+}
+
+
 // e2m1 (FP4): the value nearest to x / s among 0, 0.5, 1, 1.5, 2, 3, 4, 6
 // and their negatives, ties to the even code (the value with a zero fraction
 // bit), saturating at +-6.  The magnitude code is the number of midpoints
@@ -385,7 +399,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const __grid_constant__ PackP
 
   const int key = (t64 & 1) * kScaleTile + r;  // row of the 128-key MMA tile
   const int tile = t64 >> 1;
-  float sk = 1.f, sv = 1.f;
+  float sk = 1.f, sv = 1.f, rk = 1.f, rv = 1.f;
   if (quant) {
     float ak = 0.f, av = 0.f;
 #pragma unroll
@@ -398,6 +412,8 @@ __global__ void __launch_bounds__(256) pack_kernel(const __grid_constant__ PackP
     av = block_max(av, red, 8);
     sk = __fdiv_rn(ak, cb);
     sv = __fdiv_rn(av, cb);
+    rk = recip(sk);
+    rv = recip(sv);
     if (tid == 0) {
       p.sk[bh * p.ntq * 2 + t64] = sk;
       p.sv[bh * p.ntq * 2 + t64] = sv;
@@ -441,7 +457,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const __grid_constant__ PackP
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float x0 = bf16_at(kr[c], 2 * e), x1 = bf16_at(kr[c], 2 * e + 1);
-          w[e] = pack_bf16x2(code_i8(x0, sk), code_i8(x1, sk));
+          w[e] = pack_bf16x2(code_i8_fast(x0, sk, rk), code_i8_fast(x1, sk, rk));
         }
         u = make_uint4(w[0], w[1], w[2], w[3]);
       }
@@ -455,7 +471,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const __grid_constant__ PackP
   for (int e = 0; e < 32; ++e) {
     const float x = bf16_at(vr[e >> 3], e & 7);
     float y = x;
-    if (quant) y = kDt == kDtFp8 ? code_f8(x, sv) : kDt == kDtFp4 ? code_f4(x, sv) : code_i8(x, sv);
+    if (quant) y = kDt == kDtFp8 ? code_f8(x, sv) : kDt == kDtFp4 ? code_f4(x, sv) : code_i8_fast(x, sv, rv);
     vs[r][32 * qq + e] = y;
   }
   __syncthreads();
@@ -592,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     amax = red[0];
 #pragma unroll
     for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[w]);
-    const float sq = __fdiv_rn(amax, code_max(kDt));
+    const float sq = __fdiv_rn(amax, code_max(kDt)), rq = recip(sq);
     if (kDt == kDtFp4) {
       // dims 64hf .. 64hf+63: chunks 4hf .. 4hf+3
 #pragma unroll
@@ -622,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float x0 = bf16_at(qv[c], 2 * e), x1 = bf16_at(qv[c], 2 * e + 1);
-          w[e] = pack_bf16x2(code_i8(x0, sq), code_i8(x1, sq));
+          w[e] = pack_bf16x2(code_i8_fast(x0, sq, rq), code_i8_fast(x1, sq, rq));
         }
         *reinterpret_cast<uint4*>(sm + kOffQc + hf * kRegion + swz(rr, c)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
