@@ -6,8 +6,11 @@
 // tests and the benchmark's CPU-baseline legs load this library.
 //
 //   quantiser        Appendix A.4 Algorithm 4 (Quant_B), Eq. 9 (DeQuant)
-//   selection        Appendix A.1 Algorithm 1 (summed proxy logits), and the
-//                    softmax-mass score of §4.1 Eq. 4 with Eq. 5's top-k
+//   selection        Appendix A.1 Algorithm 1 (summed proxy logits), per KV
+//                    head and per query head (its B x H_Q x k output, kept
+//                    per KV head as the union filled by the group score),
+//                    and the softmax-mass score of §4.1 Eq. 4 with Eq. 5's
+//                    top-k
 //   decode           §4.3 Eq. 8-9: softmax attention over the effective cache
 //   prefill          §4.2 Eq. 6-7, Appendix A.2 Algorithm 2
 //
@@ -15,9 +18,11 @@
 // oracle): groups of 32 along head_dim; x ~ c s + z with s the smallest
 // binary16 step covering the group's range and z = RN_binary16(min); codes
 // are the nearest grid point, ties to even; one vertical-line set per KV
-// head with ties to the lower position; prefill scales s = RN_binary32(max|x|
-// / c_B) per 64-key tile and per 128-row query block, codes the grid value
-// nearest to the exact quotient x / s.
+// head with ties to the lower position (per query head: the union of a
+// group's sets filled up to min(P, g k) by the group score); prefill scales
+// s = RN_binary32(max|x| / c_B) per 64-key tile and per 128-row query block,
+// codes the grid value nearest to the exact quotient x / s (INT8, e4m3 or
+// e2m1 with c_B = 127, 448, 6).
 //
 // Build: g++ -O2 -std=c++17 -ffp-contract=off -shared -fPIC (no fused
 // multiply-add may change a rounding; every operation is one IEEE double
@@ -84,6 +89,16 @@ std::vector<double> e4m3_values() {
       if (e == 15 && m == 7) continue;
       v.push_back(e == 0 ? std::ldexp((double)m, -9) : std::ldexp(1.0 + m / 8.0, e - 7));
     }
+  return v;
+}
+
+// e2m1 (FP4): 1 sign bit, 2 exponent bits (bias 1), 1 fraction bit; exponent
+// field 0 holds the subnormal m 2^-1; no infinities or NaN, so the largest
+// value is 6.  The non-negative values in ascending order (index = code).
+std::vector<double> e2m1_values() {
+  std::vector<double> v;
+  for (int e = 0; e < 4; ++e)
+    for (int m = 0; m < 2; ++m) v.push_back(e == 0 ? m * 0.5 : (1.0 + m / 2.0) * std::ldexp(1.0, e - 1));
   return v;
 }
 
@@ -262,6 +277,9 @@ struct SymQuant {
     if (dtype == 2) {
       grid = e4m3_values();
       cb = 448.f;
+    } else if (dtype == 3) {
+      grid = e2m1_values();
+      cb = 6.f;
     } else {
       for (int i = 0; i < 128; ++i) grid.push_back(i);
       cb = 127.f;
@@ -303,6 +321,12 @@ int64_t hyqo_vl_count(int64_t P, int64_t rho_ppm) { return vl_count(P, rho_ppm);
 // The e4m3 value of a 7-bit magnitude code (0 .. 126).
 double hyqo_e4m3_value(int code) {
   static const std::vector<double> v = e4m3_values();
+  return (code >= 0 && code < (int)v.size()) ? v[code] : NAN;
+}
+
+// The e2m1 value of a 3-bit magnitude code (0 .. 7).
+double hyqo_e2m1_value(int code) {
+  static const std::vector<double> v = e2m1_values();
   return (code >= 0 && code < (int)v.size()) ? v[code] : NAN;
 }
 
@@ -356,6 +380,63 @@ int64_t hyqo_select(const double* qp, const double* k, int B, int HQ, int HKV, i
     if (scores_out) std::copy(S.begin(), S.end(), scores_out + bh * P);
   });
   return kk;
+}
+
+// Algorithm 1 per query head: S_h(j) = u_h . k_j with u_h the sum of query
+// head h's T proxies and k_j the key of its KV head; each head keeps its k
+// largest (ties to the lower position).  Per KV head the stored list is the
+// union of its g heads' sets, filled up to ku = min(P, g k) positions with
+// the largest group scores (Algorithm 1's per-KV-head S) among the others,
+// ties to the lower position.  idx_heads [B][HQ][k], idx_kv [B][HKV][ku]
+// (both ascending), union_size [B][HKV].  Returns ku.
+int64_t hyqo_select_heads(const double* qp, const double* k, int B, int HQ, int HKV, int T, int64_t ldk, int d,
+                          int64_t L, int64_t W, int64_t rho_ppm, int64_t* idx_heads, int64_t* idx_kv,
+                          int64_t* union_size, int threads) {
+  const int64_t P = std::max<int64_t>(0, L - W), kk = vl_count(P, rho_ppm);
+  const int g = HQ / HKV;
+  const int64_t ku = std::min<int64_t>(P, g * kk);
+  parallel_for((int64_t)B * HKV, threads, [&](int64_t bh) {
+    const int64_t b = bh / HKV, kh = bh % HKV;
+    const double* K = k + (b * HKV + kh) * ldk * d;
+    std::vector<double> Sg(P, 0.0), Sh(P);
+    std::vector<char> in_union(std::max<int64_t>(P, 1), 0);
+    std::vector<double> ug(d, 0.0);
+    for (int h = 0; h < g; ++h) {
+      std::vector<double> u(d, 0.0);
+      for (int t = 0; t < T; ++t) {
+        const double* qr = qp + (((b * HQ) + kh * g + h) * (int64_t)T + t) * d;
+        for (int i = 0; i < d; ++i) u[i] += qr[i];
+      }
+      for (int i = 0; i < d; ++i) ug[i] += u[i];
+      for (int64_t j = 0; j < P; ++j) {
+        double acc = 0.0;
+        for (int i = 0; i < d; ++i) acc += u[i] * K[j * d + i];
+        Sh[j] = acc;
+      }
+      int64_t* own = idx_heads + ((b * HQ) + kh * g + h) * kk;
+      topk_ascending(Sh, kk, own);
+      for (int64_t i = 0; i < kk; ++i) in_union[own[i]] = 1;
+    }
+    // the group score, with the proxies of all g heads summed first (as Algorithm 1 per KV head)
+    for (int64_t j = 0; j < P; ++j) {
+      double acc = 0.0;
+      for (int i = 0; i < d; ++i) acc += ug[i] * K[j * d + i];
+      Sg[j] = acc;
+    }
+    int64_t nu = 0;
+    for (int64_t j = 0; j < P; ++j) nu += in_union[j];
+    union_size[bh] = nu;
+    // fill: the positions outside the union by (group score descending, position ascending)
+    std::vector<int64_t> rest;
+    for (int64_t j = 0; j < P; ++j)
+      if (!in_union[j]) rest.push_back(j);
+    std::stable_sort(rest.begin(), rest.end(), [&](int64_t a, int64_t c) { return Sg[a] > Sg[c]; });
+    for (int64_t i = 0; i < ku - nu && i < (int64_t)rest.size(); ++i) in_union[rest[i]] = 1;
+    int64_t o = 0;
+    for (int64_t j = 0; j < P; ++j)
+      if (in_union[j]) idx_kv[bh * ku + o++] = j;
+  });
+  return ku;
 }
 
 // Hybrid decode attention (Eq. 8-9): for every query head h (KV head h / g)
@@ -416,7 +497,7 @@ int hyqo_decode(const double* q, const double* k, const double* v, int B, int HQ
 // The quantised prefix [0, P) minus idx, in ascending order, is cut into
 // tiles of 64 keys, each with one scale for K and one for V; queries use
 // one scale per 128-row block of one head; dtype 1 = INT8 (codes -127..127),
-// 2 = FP8 e4m3.  Quantised keys meet the quantised query, the others
+// 2 = FP8 e4m3, 3 = FP4 e2m1.  Quantised keys meet the quantised query, the others
 // (vertical lines and, for band = 0, [P, L); for band = 1 the keys (i - W, i]
 // of row i) the BF16 query; every key at or before the row (band = 1: the
 // quantised prefix and vertical lines only at or before i - W).

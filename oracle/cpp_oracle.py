@@ -46,10 +46,16 @@ def load():
         lib.hyqo_vl_count.argtypes = [ctypes.c_int64, ctypes.c_int64]
         lib.hyqo_e4m3_value.restype = ctypes.c_double
         lib.hyqo_e4m3_value.argtypes = [ctypes.c_int]
+        lib.hyqo_e2m1_value.restype = ctypes.c_double
+        lib.hyqo_e2m1_value.argtypes = [ctypes.c_int]
         lib.hyqo_select.restype = ctypes.c_int64
         lib.hyqo_select.argtypes = [_c_double_p, _c_double_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_int64, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                     ctypes.c_int, _c_i64_p, _c_double_p, ctypes.c_int]
+        lib.hyqo_select_heads.restype = ctypes.c_int64
+        lib.hyqo_select_heads.argtypes = [_c_double_p, _c_double_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                                          ctypes.c_int64, _c_i64_p, _c_i64_p, _c_i64_p, ctypes.c_int]
         lib.hyqo_decode.restype = ctypes.c_int
         lib.hyqo_decode.argtypes = [_c_double_p, _c_double_p, _c_double_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_int64, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, _c_i64_p,
@@ -93,6 +99,10 @@ def e4m3_value(code: int) -> float:
     return float(load().hyqo_e4m3_value(code))
 
 
+def e2m1_values() -> list:
+    return [float(load().hyqo_e2m1_value(c)) for c in range(8)]
+
+
 def select_vertical(q_proxy, k_src, L: int, window: int, rho_ppm: int, mass: bool = False, threads: int = 1):
     """(idx int64 [B, HKV, k] ascending, S float64 [B, HKV, P])."""
     q = _f64(q_proxy)
@@ -106,6 +116,23 @@ def select_vertical(q_proxy, k_src, L: int, window: int, rho_ppm: int, mass: boo
     load().hyqo_select(_p(q, _c_double_p), _p(k, _c_double_p), B, HQ, HKV, T, ldk, d, L, window, rho_ppm,
                        int(mass), _p(idx, _c_i64_p), _p(S, _c_double_p), threads)
     return idx, S
+
+
+def select_vertical_heads(q_proxy, k_src, L: int, window: int, rho_ppm: int, threads: int = 1):
+    """(idx_heads int64 [B, HQ, k], idx_kv int64 [B, HKV, ku], union sizes [B, HKV])."""
+    q = _f64(q_proxy)
+    k = _f64(k_src)
+    B, HQ, T, d = q.shape
+    HKV, ldk = k.shape[1], k.shape[2]
+    P = max(0, L - window)
+    kk = vl_count(P, rho_ppm)
+    ku = min(P, (HQ // HKV) * kk)
+    ih = np.zeros((B, HQ, kk), np.int64)
+    ik = np.zeros((B, HKV, ku), np.int64)
+    us = np.zeros((B, HKV), np.int64)
+    load().hyqo_select_heads(_p(q, _c_double_p), _p(k, _c_double_p), B, HQ, HKV, T, ldk, d, L, window, rho_ppm,
+                             _p(ih, _c_i64_p), _p(ik, _c_i64_p), _p(us, _c_i64_p), threads)
+    return ih, ik, us
 
 
 def hybrid_decode(q, k_src, v_src, L: int, P: int, idx, bits: int = 4, bits_v=None, threads: int = 0):
@@ -139,6 +166,6 @@ def hybrid_prefill(q, k, v, vl_idx, window: int, dtype: str = "int8", query_bloc
     out = np.zeros(q.shape)
     mag = np.zeros(q.shape)
     load().hyqo_prefill(_p(q, _c_double_p), _p(k, _c_double_p), _p(v, _c_double_p), B, HQ, HKV, L, d, window,
-                        _p(ix, _c_i64_p), ix.shape[-1], {"int8": 1, "fp8": 2}[dtype], int(band), _p(bm, _c_u8_p),
+                        _p(ix, _c_i64_p), ix.shape[-1], {"int8": 1, "fp8": 2, "fp4": 3}[dtype], int(band), _p(bm, _c_u8_p),
                         _p(hm, _c_u8_p), _p(out, _c_double_p), _p(mag, _c_double_p), threads)
     return out, mag

@@ -78,7 +78,7 @@ def test_decode_identical(bits, seed, B, HQ, HKV, Lc, W, ppm):
 
 
 @pytest.mark.parametrize("band", [False, True])
-@pytest.mark.parametrize("dtype", ["int8", "fp8"])
+@pytest.mark.parametrize("dtype", ["int8", "fp8", "fp4"])
 @pytest.mark.parametrize("seed,HQ,HKV,Lc,W,ppm", [(41, 4, 2, 300, 64, 50_000), (44, 8, 2, 777, 200, 50_000),
                                                    (46, 4, 2, 257, 0, 0)])
 def test_prefill_identical(band, dtype, seed, HQ, HKV, Lc, W, ppm):
@@ -101,3 +101,20 @@ def test_prefill_sampled_blocks_and_heads():
     got, _ = C.hybrid_prefill(q, k, v, idx, 64, "fp8", query_blocks=[0, 4], heads=[1, 6])
     np.testing.assert_allclose(got, want, rtol=1e-11, atol=1e-12)
     assert not got[:, [0, 2, 3, 4, 5, 7]].any() and not got[:, :, 128:512].any()
+
+
+@pytest.mark.parametrize("seed,B,HQ,HKV,Lc,W,ppm", [(1000, 1, 8, 2, 1024, 128, 50_000),
+                                                   (1001, 2, 8, 8, 700, 64, 100_000),
+                                                   (1002, 1, 6, 2, 500, 32, 20_000)])
+def test_select_heads_identical(seed, B, HQ, HKV, Lc, W, ppm):
+    from oracle.select import select_vertical_heads
+    c = decode_case(seed, B, HQ, HKV, Lc, window=W, n_proxy=16, n_sinks=6)
+    qp, k = _np(c.q_proxy), _np(c.k)
+    ih, ik, us, _, _ = select_vertical_heads(qp, k, Lc, W, ppm)
+    ih2, ik2, us2 = C.select_vertical_heads(qp, k, Lc, W, ppm, threads=2)
+    assert np.array_equal(ih, ih2) and np.array_equal(ik, ik2) and np.array_equal(us, us2)
+
+
+def test_e2m1_table_identical():
+    from oracle.prefill import e2m1_values
+    assert C.e2m1_values() == list(e2m1_values())
