@@ -96,7 +96,10 @@ DecodePlan decode_plan(const hyq_config* c, int32_t len, bool overlap) {
   const int sms = hyq_num_sms() - (overlap && 3 * bh <= hyq_num_sms() ? bh : 0);
   int32_t P = len - c->window > 0 ? len - c->window : 0;
   int64_t tiles = (int64_t)(P + 15) / 16 + (hyq_vl_count(c, P) + hyq_cap_tail(c) + 15) / 16;
-  int cap = (int)(tiles / 32 > 0 ? tiles / 32 : 1);
+  // At least ~12 tiles per block: at short contexts fewer, fuller blocks beat
+  // one block per SM (Llama-shaped, B1: 1K best at 6 splits, 2K at 12, 4K and
+  // longer at the one-wave maximum).
+  int cap = (int)(tiles / 12 > 0 ? tiles / 12 : 1);
   DecodePlan p;
   const int32_t plan = g_plan.load(std::memory_order_relaxed);
   if (plan >> 16 != 0) {
