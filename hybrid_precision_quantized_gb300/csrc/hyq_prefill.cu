@@ -709,24 +709,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             if (i <= ilo || i > ihi) x[i] = -INFINITY;
         }
       }
-      float a[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) a[u] = x[u];
-#pragma unroll
-      for (int i = 8; i < 64; i += 2) a[(i >> 1) & 7] = fmax3(a[(i >> 1) & 7], x[i], x[i + 1]);
-      const float hmax = fmax3(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
-      const float tmax = hmax == -INFINITY ? -INFINITY : hmax * cs;
-      // Lazy maximum: rescale only when the row maximum grew by more than 2^8.
-      const bool grow = tmax > m_used + 8.f;
-      const float m_new = grow ? tmax : m_used;
-      const float fac = grow ? fast_exp2(m_used - m_new) : 1.f;
-      const float mb = (m_new == -INFINITY) ? 0.f : m_new;
       // P_h as BF16 pairs with the value scale folded in (the A operand of
       // P.V), built with the exponentials; stored once the P buffer is free.
       float rs;
       uint32_t pw[32];
       const uint64_t vf2 = f2_splat(vf);
-      {
+      auto exps = [&](float mb) {
         // Pairs: scale, shift, sum and scale by vf packed (masked keys are
         // -inf here and give 0).
         const uint64_t cs2 = f2_splat(cs), nmb2 = f2_splat(-mb);
@@ -741,9 +729,35 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         }
         const uint64_t r2 = f2_add(f2_add(ps2[0], ps2[1]), f2_add(ps2[2], ps2[3]));
         rs = f2_lo(r2) + f2_hi(r2);
+      };
+      // Lazy maximum.  Once a row has a running maximum, the tile's terms
+      // are formed against it without a row maximum: their sum bounds each
+      // of them, so a sum up to 2^16 means no term exceeds 2^16 and nothing
+      // needs rescaling (all of them are far inside the FP32 and BF16
+      // range).  A warp with a row whose sum is larger (or not finite), or
+      // with a row that has no maximum yet, takes the row maximum and
+      // rescales the rows where it grew by more than 2^8.
+      float fac = 1.f;
+      bool full = __any_sync(0xffffffffu, m_used == -INFINITY);
+      if (!full) {
+        exps(m_used);
+        full = __any_sync(0xffffffffu, !(rs <= 65536.f));
+      }
+      if (full) {
+        float a[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) a[u] = x[u];
+#pragma unroll
+        for (int i = 8; i < 64; i += 2) a[(i >> 1) & 7] = fmax3(a[(i >> 1) & 7], x[i], x[i + 1]);
+        const float hmax = fmax3(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
+        const float tmax = hmax == -INFINITY ? -INFINITY : hmax * cs;
+        const bool grow = tmax > m_used + 8.f;
+        const float m_new = grow ? tmax : m_used;
+        fac = grow ? fast_exp2(m_used - m_new) : 1.f;
+        m_used = m_new;
+        exps(m_new == -INFINITY ? 0.f : m_new);
       }
       l_sum = l_sum * fac + rs;
-      m_used = m_new;
 
       if (j > 0) {  // the previous tile's P.V is done: O stable, P buffer free
         if (!mbar_wait_or_abort(pvdone, (j - 1) & 1, abort_flag)) {

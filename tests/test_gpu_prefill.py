@@ -259,3 +259,30 @@ def test_prefill_codes_of_exact_quotients(hyq, dtype):
                              return_abs=True)
     rows = [64 * t + 1 for t in range(T)]
     assert_prefill_close(got[:, :, rows], want[:, :, rows], a[:, :, rows], what=f"{dtype} planted quotients")
+
+
+@pytest.mark.parametrize("band", [False, True])
+@pytest.mark.parametrize("dtype", ["int8", "fp8", "fp4"])
+def test_prefill_late_score_jumps(hyq, dtype, band):
+    """Keys planted late in the row whose logits rise far above the row's
+    earlier maximum: at positions 430 and 700 (quantised segment, kept out of
+    the vertical-line list) and 940 (inside the BF16 window).  Over the rows
+    that see them the rise spreads from below 0 to ~17, ~26 and ~45 (log2
+    units; medians ~8, ~14 and ~25), so many rows' running maximum trails the
+    tile maximum by 2^8 to 2^16 (terms formed against the stale maximum) and
+    many by more (the maximum has to move); the result is the same softmax
+    either way."""
+    Lc, W, ppm = 1000, 128, 50_000
+    c = prefill_case(41, 1, 4, 2, Lc, window=W, sink_frac=0.02)
+    idx = vl_for(c, Lc, W, ppm)
+    k = c.k.double().clone()
+    for h in range(2):
+        u = c.u[0, h].double()
+        for pos, gain in ((430, 47.0), (700, 102.0), (940, 200.0)):
+            assert pos not in set(idx[0, h].tolist())
+            k[0, h, pos] = gain * u
+    c.k = k.to(torch.bfloat16)
+    got = run_gpu(c, Lc, W, ppm, dtype, idx, band=band)
+    want, a = hybrid_prefill(c.q.double().numpy(), c.k.double().numpy(), c.v.double().numpy(), idx, W, dtype,
+                             return_abs=True, band=band)
+    assert_prefill_close(got, want, a, what=f"{dtype} late jumps band={band}")
