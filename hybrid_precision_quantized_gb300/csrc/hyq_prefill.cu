@@ -275,6 +275,12 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+__device__ __forceinline__ float fast_log2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Packed float32 pairs (one 64-bit register, low half first).
 __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
   uint64_t d;
@@ -300,11 +306,6 @@ __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
 __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   uint64_t d;
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -683,7 +684,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       // A scale is 0 only when every code it multiplies is 0; keeping it
       // positive changes no score and makes masked (-inf) keys give 0.
       const float cs = quant ? fmaxf(qfac * sc.x, 1.17549435e-38f) : p.alpha_log2e;
-      const float vf = quant ? sc.y : 1.f;
+      // log2 of the value scale, added to the exponent (2^(t + log2 vf) =
+      // vf 2^t); a scale below 2^-60 only multiplies codes whose values are
+      // below 2^-51, so raising it to 2^-60 changes no output.
+      const float lvf = quant ? fast_log2(fmaxf(sc.y, 8.67361738e-19f)) : 0.f;
       if (j + 1 < nqt) sc = make_float2(__ldg(skp + 2 * j + 2), __ldg(svp + 2 * j + 2));
       // some key of the tile is hidden from some row of the block
       const bool masked = quant ? j >= mask_q : (j < nlt ? j - nqt >= mask_f : true);
@@ -713,22 +717,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       // P.V), built with the exponentials; stored once the P buffer is free.
       float rs;
       uint32_t pw[32];
-      const uint64_t vf2 = f2_splat(vf);
       auto exps = [&](float mb) {
-        // Pairs: scale, shift, sum and scale by vf packed (masked keys are
-        // -inf here and give 0).
-        const uint64_t cs2 = f2_splat(cs), nmb2 = f2_splat(-mb);
+        // Pairs: scale and shift (by m - log2 vf, so that 2^t comes out
+        // multiplied by vf), sum, pack (masked keys are -inf here and give 0);
+        // the sum is taken back to the unscaled terms once per tile.
+        const uint64_t cs2 = f2_splat(cs), nmb2 = f2_splat(lvf - mb);
         uint64_t ps2[4] = {0, 0, 0, 0};
 #pragma unroll
         for (int w = 0; w < 32; ++w) {
           uint64_t e2 = f2_fma(f2_pack(x[2 * w], x[2 * w + 1]), cs2, nmb2);
           e2 = f2_pack(fast_exp2(f2_lo(e2)), fast_exp2(f2_hi(e2)));
           ps2[w & 3] = f2_add(ps2[w & 3], e2);
-          const uint64_t pv = f2_mul(e2, vf2);
-          pw[w] = pack_bf16x2(f2_lo(pv), f2_hi(pv));
+          pw[w] = pack_bf16x2(f2_lo(e2), f2_hi(e2));
         }
         const uint64_t r2 = f2_add(f2_add(ps2[0], ps2[1]), f2_add(ps2[2], ps2[3]));
-        rs = f2_lo(r2) + f2_hi(r2);
+        rs = (f2_lo(r2) + f2_hi(r2)) * fast_exp2(-lvf);
       };
       // Lazy maximum.  Once a row has a running maximum, the tile's terms
       // are formed against it without a row maximum: their sum bounds each
