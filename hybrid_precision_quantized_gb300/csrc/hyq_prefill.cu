@@ -42,6 +42,7 @@
 #include <cmath>
 #include <cstdint>
 
+#include "hyq_f2.cuh"
 #include "hyq_tc.cuh"
 
 namespace {
@@ -279,39 +280,6 @@ __device__ __forceinline__ float fast_log2(float x) {
   float y;
   asm("lg2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
   return y;
-}
-
-// Packed float32 pairs (one 64-bit register, low half first).
-__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
-  uint64_t d;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
-  return d;
-}
-__device__ __forceinline__ uint64_t f2_splat(float v) { return f2_pack(v, v); }
-__device__ __forceinline__ float f2_lo(uint64_t v) {
-  float lo;
-  asm("{\n .reg .b32 t;\n mov.b64 {%0, t}, %1;\n}" : "=f"(lo) : "l"(v));
-  return lo;
-}
-__device__ __forceinline__ float f2_hi(uint64_t v) {
-  float hi;
-  asm("{\n .reg .b32 t;\n mov.b64 {t, %0}, %1;\n}" : "=f"(hi) : "l"(v));
-  return hi;
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
 }
 
 __device__ __forceinline__ float block_max(float v, float* red, int nwarps) {

@@ -14,6 +14,7 @@
 #include <type_traits>
 
 #include "hyq_common.cuh"
+#include "hyq_f2.cuh"
 
 namespace {
 
@@ -32,22 +33,6 @@ struct BuildSmem {
   uint8_t nan[2][kRows][4];
   uint8_t fast[2][kRows][4];  // every code of the group needs no clamp
 };
-
-// Packed float32 pairs (two lanes of one 64-bit register, low half first).
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ uint64_t f2_splat(float v) {
-  const uint64_t u = __float_as_uint(v);
-  return (u << 32) | u;
-}
 
 // Rounding by addition: for |t| < 2^22, fl32(t + 1.5 * 2^23) is
 // 1.5 * 2^23 + rint(t) (the sum's ulp is 1, ties to even), so its bit

@@ -20,7 +20,12 @@
 #include <algorithm>
 #include <cmath>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "hyq_common.cuh"
+#include "hyq_f2.cuh"
+#include "hyq_tc.cuh"
 
 namespace {
 
@@ -483,17 +488,44 @@ __global__ void __cluster_dims__(kTopkCluster, 1, 1) __launch_bounds__(kTopkCtaT
 // the softmax taken over the L current keys and S kept for j < P.
 // Pass 1 (mass_stats_kernel): per key split (at most 32), each row's running maximum m
 // and sum l of 2^(t - m), t = fl(z c), z = q_r . k_j (exact BF16 products,
-// float32 accumulation on the tensor cores), c = alpha log2 e.  Merge
-// (mass_merge_kernel): m = max over splits, l = sum_s l_s 2^(m_s - m), and
-// 1/l.  Pass 2 (mass_colsum_kernel): per 64-key tile of [0, P), the column
-// sums of 2^(t - m) (1/l) over a group of at most 256 rows.  Final
-// (mass_keys_kernel): the row groups' sums in a fixed order, as the
-// order-preserving keys of the top-k kernels.
-constexpr int kMassThreads = 256;     // 8 warps, each two 16-row blocks of a row group
-constexpr int kMassGroupRows = 256;
-constexpr int kMassKeys = 64;         // keys per tile (8 MMA n-blocks)
-constexpr int kMassStride = 136;      // bf16 per staged row: 272 bytes, conflict-free fragment loads
+// float32 accumulation: tcgen05 MMAs into tensor memory), c = alpha log2 e.
+// Pass 2 (mass_colsum_kernel): the splits' partials merged per row (m = max
+// over splits, l = sum_s l_s 2^(m_s - m), 1/l), then per 128-key tile of
+// [0, P) the column sums of 2^(t - m) (1/l) over a group of at most 256
+// rows; with one row group they are written as the order-preserving keys of
+// the top-k kernels, else (mass_keys_kernel) the row groups' sums are added
+// in a fixed order first.  Both passes stream the keys
+// by TMA (128-byte swizzled tiles of the caller's BF16 cache) through a
+// three-stage ring; one thread issues the MMAs into two TMEM buffers, so a
+// tile's products run while the consumers read the previous one.
+constexpr int kMassGroupRows = 256;   // rows of one row group (two M = 128 halves)
 constexpr int kMassSplits = 32;       // most key splits of pass 1 per (sequence, KV head, row group)
+constexpr int kMassTileKeys = 128;    // keys per tile (MMA N in pass 1, M in pass 2)
+constexpr int kMassCons = 256;        // consumer threads (warps 0-7)
+constexpr int kMassTmaWarp = 8, kMassMmaWarp = 9;
+constexpr int kMassThreads = 320;
+constexpr int kMassStages = 4;        // key-tile ring
+constexpr uint32_t kMassTmemCols = 512;
+// Shared memory from a 1024-byte aligned base.  Operand images are K-major
+// (dims contiguous) in the 128-byte-swizzled layout, one region per 64
+// dims: the row group's queries [dim half][256 rows][128 B], each key stage
+// [dim half][128 keys][128 B].
+constexpr int kMOffQ = 0;
+constexpr int kMQHalf = kMassGroupRows * 128;          // 32 KB
+constexpr int kMKHalf = kMassTileKeys * 128;           // 16 KB
+constexpr int kMOffK = kMOffQ + 2 * kMQHalf;
+constexpr int kMOffSt = kMOffK + kMassStages * 2 * kMKHalf;  // pass 2: (-m, 1/l) of row pairs, float4 [128]
+constexpr int kMOffX = kMOffSt + 128 * 16;                   // pass 2: column-sum exchange, float [2][128]
+constexpr int kMOffBar = kMOffX + 2 * 128 * 4;
+constexpr int kMOffMisc = kMOffBar + 16 * 8;
+constexpr int kMassSmem = kMOffMisc + 64 + 1024;        // + room to align the base
+
+// Shared-memory load by address (a warp reading one address is one broadcast).
+__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];\n" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+  return v;
+}
 
 __device__ __forceinline__ float mass_ex2(float x) {
   float y;
@@ -501,261 +533,397 @@ __device__ __forceinline__ float mass_ex2(float x) {
   return y;
 }
 
-__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+struct MassParams {
+  const __nv_bfloat16* qp;  // [B][HQ][n_ld][128]
+  int32_t n_proxy, n_ld, gq, R, n_groups;
+  int32_t L;      // pass 1: keys [0, L); pass 2: column sums of [0, L) (= P)
+  int32_t ld;     // rows per (sequence, KV head) in the key source
+  float c;        // fl(alpha log2 e)
+  int32_t q_tma;         // the row group's query rows are contiguous: loaded by TMA
+  float2* part;          // pass 1 output, pass 2 input
+  int32_t ns;            // pass 1 splits
+  float* colsum;         // pass 2 output with more than one row group
+  uint32_t* keys;        // pass 2 output with one row group: the top-k keys
+  int32_t pmax;
+  int32_t* err;
+};
+
+// 2D tiled load of a box of 64 dims x rows (128-byte swizzle) from a BF16
+// source viewed as [rows][128 dims]; completion counted on `bar`.
+__device__ __forceinline__ void tma_load_k(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};\n"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
 }
 
-// Stage the query rows [rg * 256, +256) of the group into shared memory
-// (stride kMassStride); rows past R are zero.
-__device__ void mass_stage_q(__nv_bfloat16* qs, const __nv_bfloat16* qp, int b, int h, int HKV, int gq,
-                             int n_proxy, int n_ld, int R, int rg) {
-  for (int i = threadIdx.x; i < kMassGroupRows * 16; i += kMassThreads) {
-    const int lr = i >> 4, c = i & 15, r = rg * kMassGroupRows + lr;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < R) {
-      const int hi = r / n_proxy, t = r - hi * n_proxy;
-      v = __ldg(reinterpret_cast<const uint4*>(qp + (((size_t)b * HKV * gq + (size_t)h * gq + hi) * n_ld + t) * HYQ_D) + c);
+// The row group's queries -> the swizzled K-major image (rows past R zero),
+// by every thread of the block, made visible to the tensor core.
+__device__ void mass_stage_q_tc(uint8_t* sm, const MassParams& p, int b, int h, int HKV, int rg) {
+  // all of a thread's loads are issued before its first store
+  constexpr int kPer = (kMassGroupRows * 16 + kMassThreads - 1) / kMassThreads;
+  uint4 v[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int i = threadIdx.x + u * kMassThreads, lr = i >> 4, c = i & 15, r = rg * kMassGroupRows + lr;
+    v[u] = make_uint4(0, 0, 0, 0);
+    if (i < kMassGroupRows * 16 && r < p.R) {
+      const int hi = r / p.n_proxy, t = r - hi * p.n_proxy;
+      v[u] = __ldg(reinterpret_cast<const uint4*>(
+                       p.qp + (((size_t)b * HKV * p.gq + (size_t)h * p.gq + hi) * p.n_ld + t) * HYQ_D) +
+                   c);
     }
-    *reinterpret_cast<uint4*>(qs + lr * kMassStride + 8 * c) = v;
+  }
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int i = threadIdx.x + u * kMassThreads, lr = i >> 4, c = i & 15;
+    if (i < kMassGroupRows * 16)
+      *reinterpret_cast<uint4*>(sm + kMOffQ + (c >> 3) * kMQHalf + lr * 128 + (((c & 7) ^ (lr & 7)) << 4)) = v[u];
+  }
+  fence_proxy_async_smem();
+}
+
+// Key tiles of one block: `n` tiles, tile i at key row `row0 + i * stride * 128`
+// (rows of the flattened [B][HKV][ld] key source).  The loader thread of the
+// TMA warp fills the ring, the MMA thread issues one tile's products into
+// TMEM buffer i % 2 and releases the stage, the consumers read the buffer and
+// release it.  kCols: TMEM columns per tile (pass 1: 2 x 128, pass 2: 256).
+struct MassBars {
+  uint64_t *kfull, *kempty, *dfull, *dfree, *mmadone, *qfull;
+};
+
+__device__ __forceinline__ MassBars mass_bars(uint8_t* sm) {
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kMOffBar);
+  return MassBars{bars, bars + kMassStages, bars + 2 * kMassStages, bars + 2 * kMassStages + 2,
+                  bars + 2 * kMassStages + 4, bars + 2 * kMassStages + 5};
+}
+
+__device__ void mass_init_bars(const MassBars& mb) {
+  for (int i = 0; i < kMassStages; ++i) {
+    mbar_init(mb.kfull + i, 1);
+    mbar_init(mb.kempty + i, 1);
+  }
+  for (int i = 0; i < 2; ++i) {
+    mbar_init(mb.dfull + i, 1);
+    mbar_init(mb.dfree + i, kMassCons);
+  }
+  mbar_init(mb.mmadone, 1);
+  mbar_init(mb.qfull, 1);
+  mbar_fence_init();
+}
+
+// TMA warp, lane 0, at entry: the row group's 256 query rows (two 32 KB
+// boxes) when they are contiguous in the proxy buffer.
+__device__ void mass_load_q(uint8_t* sm, const MassBars& mb, const CUtensorMap* qmap, const MassParams& p, int b, int h,
+                            int HKV, int rg) {
+  const int y = (int)(((int64_t)b * HKV * p.gq + (int64_t)h * p.gq) * p.n_ld) + rg * kMassGroupRows;
+  mbar_arrive_expect_tx(mb.qfull, 2 * kMQHalf);
+  tma_load_k(sm + kMOffQ, qmap, 0, y, mb.qfull);
+  tma_load_k(sm + kMOffQ + kMQHalf, qmap, 64, y, mb.qfull);
+}
+
+// TMA warp, lane 0: tiles [i0, i1) (the first kMassStages need no free
+// stage and are issued at kernel entry, before the queries are staged).
+__device__ void mass_loader(uint8_t* sm, const MassBars& mb, const CUtensorMap* map, int i0, int i1, int64_t row0,
+                            int64_t stride, volatile int* abort_flag, int32_t* err) {
+  int last = i0 - 1;
+  bool ok = true;
+  for (int i = i0; i < i1; ++i) {
+    const int s = i % kMassStages;
+    if (i >= kMassStages && !mbar_wait_or_abort(mb.kempty + s, ((i / kMassStages) & 1) ^ 1, abort_flag)) {
+      ok = false;
+      break;
+    }
+    uint8_t* dst = sm + kMOffK + s * 2 * kMKHalf;
+    const int y = (int)(row0 + (int64_t)i * stride * kMassTileKeys);
+    mbar_arrive_expect_tx(mb.kfull + s, 2 * kMKHalf);
+    tma_load_k(dst, map, 0, y, mb.kfull + s);
+    tma_load_k(dst + kMKHalf, map, 64, y, mb.kfull + s);
+    last = i;
+  }
+  if (!ok) {
+    *abort_flag = 1;
+    hyq_set_err(err, HYQ_DEVERR_TIMEOUT);
+    // the copies in flight land before the block's shared memory goes away
+    for (int i = max(0, last - kMassStages + 1); i <= last; ++i)
+      (void)mbar_wait(mb.kfull + i % kMassStages, (i / kMassStages) & 1);
   }
 }
 
-// Start the asynchronous copy of key rows [j0, j0 + 64) of (b, h) into a
-// staging buffer (rows past `end` are zero-filled) and commit it as one
-// group of this thread's copies.
-__device__ void mass_stage_k_async(__nv_bfloat16* ks, const __nv_bfloat16* kb, int j0, int end) {
-  for (int i = threadIdx.x; i < kMassKeys * 16; i += kMassThreads) {
-    const int r = i >> 4, c = i & 15;
-    const bool in = j0 + r < end;
-    const __nv_bfloat16* src = kb + (size_t)(in ? j0 + r : 0) * HYQ_D + 8 * c;
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(ks + r * kMassStride + 8 * c)),
-                 "l"(src), "r"(in ? 16 : 0)
-                 : "memory");
-  }
-  asm volatile("cp.async.commit_group;\n" ::: "memory");
-}
-
-// Wait until at most `n` of this thread's most recent copy groups are pending.
-template <int n>
-__device__ __forceinline__ void mass_wait_async() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(n) : "memory");
-}
-
-// A fragments (m16n8k16, row-major 16 x 128) of the 16-row block rb.
-__device__ __forceinline__ void mass_load_a(const __nv_bfloat16* qs, int rb, int lane, uint32_t (&a)[8][4]) {
-  const int g = lane >> 2, t = lane & 3;
+// MMA warp, lane 0.  kPass2: D[key][row] = K Q^T (M = 128 keys, N = 256
+// rows); else D_h[row][key] = Q_h K^T for the row halves h (M = 128, N = 128).
+template <bool kPass2>
+__device__ void mass_mma(uint8_t* sm, const MassBars& mb, uint32_t tbase, int n, bool q_tma, volatile int* abort_flag,
+                         int32_t* err) {
+  constexpr uint32_t kIdesc = tc_idesc(kTcBF16, kTcBF16, 128, kPass2 ? 256 : 128);
+  const uint64_t dQ = tc_desc_sw128(smem_u32(sm + kMOffQ)), dK0 = tc_desc_sw128(smem_u32(sm + kMOffK));
+  bool ok = !(q_tma && n > 0) || mbar_wait_or_abort(mb.qfull, 0, abort_flag);
+  for (int i = 0; ok && i < n; ++i) {
+    const int s = i % kMassStages, bf = i & 1;
+    ok = mbar_wait_or_abort(mb.kfull + s, (i / kMassStages) & 1, abort_flag);
+    if (ok && i >= 2) ok = mbar_wait_or_abort(mb.dfree + bf, ((i >> 1) & 1) ^ 1, abort_flag);
+    if (!ok) break;
+    tc_fence_after();
+    const uint64_t dK = dK0 + (uint64_t)(s * 2 * kMKHalf >> 4);
+    const uint32_t tD = tbase + bf * 256;
 #pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    const uint32_t* r0 = reinterpret_cast<const uint32_t*>(qs + (16 * rb + g) * kMassStride + 16 * ks + 2 * t);
-    const uint32_t* r8 = reinterpret_cast<const uint32_t*>(qs + (16 * rb + g + 8) * kMassStride + 16 * ks + 2 * t);
-    a[ks][0] = r0[0];
-    a[ks][1] = r8[0];
-    a[ks][2] = r0[4];
-    a[ks][3] = r8[4];
-  }
-}
-
-// z = Q K^T for the warp's two row blocks and the staged 64-key tile:
-// C[blk][nb][i] is row 16 rb + g + 8 (i >> 1), key 8 nb + 2 t + (i & 1).
-__device__ __forceinline__ void mass_tile(const __nv_bfloat16* ksm, int lane, const uint32_t (&a0)[8][4],
-                                          const uint32_t (&a1)[8][4], float (&C)[2][8][4]) {
-  const int g = lane >> 2, t = lane & 3;
-#pragma unroll
-  for (int blk = 0; blk < 2; ++blk)
-#pragma unroll
-    for (int nb = 0; nb < 8; ++nb) C[blk][nb][0] = C[blk][nb][1] = C[blk][nb][2] = C[blk][nb][3] = 0.f;
-#pragma unroll
-  for (int ks = 0; ks < 8; ++ks)
-#pragma unroll
-    for (int nb = 0; nb < 8; ++nb) {
-      const uint32_t* kr = reinterpret_cast<const uint32_t*>(ksm + (8 * nb + g) * kMassStride + 16 * ks + 2 * t);
-      const uint32_t b0 = kr[0], b1 = kr[4];
-      mma_bf16(C[0][nb], a0[ks], b0, b1);
-      mma_bf16(C[1][nb], a1[ks], b0, b1);
-    }
-}
-
-// Pass 1.  grid (splits <= kMassSplits, HKV * n_groups, B); dynamic smem: the row
-// group's queries and two key tiles (one landing while the other is used).  part[((bh * n_groups + rg) *
-// kMassSplits + split) * 256 + row] = (m, l) of the split's keys.
-__global__ void __launch_bounds__(kMassThreads) mass_stats_kernel(
-    const __nv_bfloat16* __restrict__ qp, int32_t n_proxy, int32_t n_ld, int32_t gq,
-    const __nv_bfloat16* __restrict__ k_src, int32_t ld, int32_t L, float c, int32_t R, int32_t n_groups,
-    float2* __restrict__ part) {
-  extern __shared__ __align__(16) unsigned char mass_smem[];
-  __nv_bfloat16* qs = reinterpret_cast<__nv_bfloat16*>(mass_smem);
-  __nv_bfloat16* ksm = qs + kMassGroupRows * kMassStride;
-  const int split = blockIdx.x, HKV = gridDim.y / n_groups, h = blockIdx.y / n_groups, rg = blockIdx.y % n_groups;
-  const int b = blockIdx.z;
-  const size_t bh = (size_t)b * HKV + h;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t = lane & 3;
-  mass_stage_q(qs, qp, b, h, HKV, gq, n_proxy, n_ld, R, rg);
-  __syncthreads();
-  uint32_t a0[8][4], a1[8][4];
-  mass_load_a(qs, 2 * warp, lane, a0);
-  mass_load_a(qs, 2 * warp + 1, lane, a1);
-  // rows (blk, half): 16 (2 warp + blk) + g + 8 half
-  float m[2][2], l[2][2];
-#pragma unroll
-  for (int blk = 0; blk < 2; ++blk) m[blk][0] = m[blk][1] = -INFINITY, l[blk][0] = l[blk][1] = 0.f;
-  const int ns = gridDim.x;
-  const int j0 = (int)((int64_t)split * L / ns), j1 = (int)((int64_t)(split + 1) * L / ns);
-  const __nv_bfloat16* kb = k_src + bh * ld * HYQ_D;
-  // two staging buffers: tile i + 1 is in flight while tile i is consumed
-  if (j0 < j1) mass_stage_k_async(ksm, kb, j0, j1);
-  for (int kt = j0, it = 0; kt < j1; kt += kMassKeys, ++it) {
-    __nv_bfloat16* kcur = ksm + (it & 1) * kMassKeys * kMassStride;
-    if (kt + kMassKeys < j1) {
-      mass_stage_k_async(ksm + ((it + 1) & 1) * kMassKeys * kMassStride, kb, kt + kMassKeys, j1);
-      mass_wait_async<1>();
-    } else {
-      mass_wait_async<0>();
-    }
-    __syncthreads();  // tile `it` has landed for every thread
-    float C[2][8][4];
-    mass_tile(kcur, lane, a0, a1, C);
-    const int nvalid = min(kMassKeys, j1 - kt);
-#pragma unroll
-    for (int blk = 0; blk < 2; ++blk)
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        float v[16];
-        float tm = -INFINITY;
-#pragma unroll
-        for (int nb = 0; nb < 8; ++nb)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int key = 8 * nb + 2 * t + e;
-            const float x = key < nvalid ? C[blk][nb][2 * hf + e] * c : -INFINITY;
-            v[2 * nb + e] = x;
-            tm = fmaxf(tm, x);
-          }
-        tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 1));
-        tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 2));
-        const float mn = fmaxf(m[blk][hf], tm);
-        float sum = 0.f;
-        if (mn != -INFINITY) {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) sum += mass_ex2(v[i] - mn);
-        }
-        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-        if (mn != -INFINITY) {
-          l[blk][hf] = l[blk][hf] * mass_ex2(m[blk][hf] - mn) + sum;
-          m[blk][hf] = mn;
-        }
+    for (int ks = 0; ks < 8; ++ks) {
+      // 16 dims = 32 bytes per step; dims 64.. in the second region
+      const uint64_t kq = (uint64_t)((ks >> 2) * kMQHalf >> 4) + (ks & 3) * 2;
+      const uint64_t kk = (uint64_t)((ks >> 2) * kMKHalf >> 4) + (ks & 3) * 2;
+      if (kPass2) {
+        tc_mma_f16(tD, dK + kk, dQ + kq, kIdesc, ks > 0);
+      } else {
+        tc_mma_f16(tD, dQ + kq, dK + kk, kIdesc, ks > 0);
+        tc_mma_f16(tD + 128, dQ + kq + (kMKHalf >> 4), dK + kk, kIdesc, ks > 0);  // rows 128..255
       }
-    __syncthreads();  // every warp is done with buffer `it & 1` before it is refilled
-  }
-  if (t == 0) {
-    float2* out = part + ((bh * n_groups + rg) * kMassSplits + split) * kMassGroupRows;
-#pragma unroll
-    for (int blk = 0; blk < 2; ++blk)
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) out[16 * (2 * warp + blk) + (lane >> 2) + 8 * hf] = make_float2(m[blk][hf], l[blk][hf]);
-  }
-}
-
-// Merge.  grid (HKV * n_groups, B), 256 threads (one row each):
-// stats = (m, 1/l) over all splits; padding rows (past R) get weight 0.
-__global__ void __launch_bounds__(kMassGroupRows) mass_merge_kernel(const float2* __restrict__ part,
-                                                                    float2* __restrict__ stats, int32_t R,
-                                                                    int32_t n_groups, int32_t ns) {
-  const size_t bg = (size_t)blockIdx.y * gridDim.x + blockIdx.x;  // (bh, rg) flattened
-  const int r = threadIdx.x;
-  if ((int)(blockIdx.x % n_groups) * kMassGroupRows + r >= R) {
-    stats[bg * kMassGroupRows + r] = make_float2(0.f, 0.f);
-    return;
-  }
-  const float2* p = part + bg * kMassSplits * kMassGroupRows + r;
-  float m = -INFINITY;
-  for (int s = 0; s < ns; ++s) m = fmaxf(m, p[s * kMassGroupRows].x);
-  float l = 0.f;
-  if (m != -INFINITY) {
-    for (int s = 0; s < ns; ++s) {
-      const float2 v = p[s * kMassGroupRows];
-      if (v.x != -INFINITY) l += v.y * mass_ex2(v.x - m);
     }
+    tc_commit(mb.dfull + bf);
+    tc_commit(mb.kempty + s);
   }
-  stats[bg * kMassGroupRows + r] = make_float2(m == -INFINITY ? 0.f : m, l > 0.f ? __frcp_rn(l) : 0.f);
+  if (!ok) {
+    *abort_flag = 1;
+    hyq_set_err(err, HYQ_DEVERR_TIMEOUT);
+  }
+  tc_commit(mb.mmadone);  // every MMA issued has finished once this arrives
+  (void)mbar_wait(mb.mmadone, 0);
 }
 
-// Pass 2.  grid (blocks, HKV * n_groups, B), block x taking the 64-key tiles
-// x, x + blocks, ... of [0, P): the row group's column sums of 2^(t - m) / l,
-// in a fixed order.
-// colsum[((bh * n_groups + rg) * pmax + j].
-__global__ void __launch_bounds__(kMassThreads) mass_colsum_kernel(
-    const __nv_bfloat16* __restrict__ qp, int32_t n_proxy, int32_t n_ld, int32_t gq,
-    const __nv_bfloat16* __restrict__ k_src, int32_t ld, int32_t P, float c, int32_t R, int32_t n_groups,
-    const float2* __restrict__ stats, float* __restrict__ colsum, int32_t pmax) {
-  extern __shared__ __align__(16) unsigned char mass_smem[];
-  __nv_bfloat16* qs = reinterpret_cast<__nv_bfloat16*>(mass_smem);
-  __nv_bfloat16* ksm = qs + kMassGroupRows * kMassStride;
-  float* red = reinterpret_cast<float*>(ksm + 2 * kMassKeys * kMassStride);  // [8 warps][64 keys]
-  const int HKV = gridDim.y / n_groups, h = blockIdx.y / n_groups, rg = blockIdx.y % n_groups;
+// Consumer: the 128 FP32 columns [col, col + 128) of this thread's TMEM lane.
+__device__ __forceinline__ void mass_ld128(uint32_t taddr, float (&x)[128]) {
+  uint32_t r[4][32];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) tc_ld32(taddr + 32 * c, r[c]);
+  tc_wait_ld();
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+#pragma unroll
+    for (int i = 0; i < 32; ++i) x[32 * c + i] = __uint_as_float(r[c][i]);
+}
+
+// Pass 1.  grid (splits <= kMassSplits, HKV * n_groups, B), 320 threads.
+// Split s takes the 128-key tiles [s nt / S, (s + 1) nt / S) of [0, L);
+// consumer thread = row (TMEM lane) of one row half: per tile the maximum
+// of t = fl(z c) and the running (m, l), l the sum of ex2(fl(z c - m)).
+// part[((bh * n_groups + rg) * kMassSplits + split) * 256 + row] = (m, l).
+__global__ void __launch_bounds__(kMassThreads, 1)
+    mass_stats_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
+                      const __grid_constant__ MassParams p) {
+  extern __shared__ uint8_t mass_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(mass_raw) + 1023) & ~(uintptr_t)1023);
+  const MassBars mb = mass_bars(sm);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + kMOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kMOffMisc + 4);
+  const int split = blockIdx.x, ns = gridDim.x, HKV = gridDim.y / p.n_groups;
+  const int h = blockIdx.y / p.n_groups, rg = blockIdx.y % p.n_groups, b = blockIdx.z;
+  const size_t bh = (size_t)b * HKV + h;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nt = (p.L + kMassTileKeys - 1) / kMassTileKeys;
+  const int t0 = (int)((int64_t)split * nt / ns), t1 = (int)((int64_t)(split + 1) * nt / ns);
+  const int n = t1 - t0;
+  const int64_t krow0 = (int64_t)bh * p.ld + (int64_t)t0 * kMassTileKeys;
+  const int nprime = min(n, kMassStages);
+  if (threadIdx.x == kMassTmaWarp * 32) {
+    mass_init_bars(mb);
+    *abort_flag = 0;
+    if (p.q_tma && n > 0) mass_load_q(sm, mb, &qmap, p, b, h, HKV, rg);
+    mass_loader(sm, mb, &kmap, 0, nprime, krow0, 1, abort_flag, p.err);
+  }
+  if (!p.q_tma) mass_stage_q_tc(sm, p, b, h, HKV, rg);
+  if (warp == kMassMmaWarp) tc_alloc(tslot, kMassTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+
+  if (warp < 8) {
+    const int half = warp >> 2, row = 128 * half + 32 * (warp & 3) + lane;
+    const uint32_t tl = tbase + ((uint32_t)(32 * (warp & 3)) << 16) + 128 * half;
+    const uint64_t c2 = f2_splat(p.c);
+    float m = -INFINITY, l = 0.f;
+    for (int i = 0; i < n; ++i) {
+      const int bf = i & 1;
+      if (!mbar_wait_or_abort(mb.dfull + bf, (i >> 1) & 1, abort_flag)) {
+        *abort_flag = 1;
+        hyq_set_err(p.err, HYQ_DEVERR_TIMEOUT);
+        break;
+      }
+      tc_fence_after();
+      float x[128];
+      mass_ld128(tl + bf * 256, x);
+      tc_fence_before();
+      mbar_arrive(mb.dfree + bf);
+      const int nvalid = p.L - (t0 + i) * kMassTileKeys;  // keys of the tile inside [0, L)
+      // keys past L are -inf
+      if (nvalid < kMassTileKeys) {
+#pragma unroll
+        for (int k = 0; k < 128; ++k) x[k] = k < nvalid ? x[k] : -INFINITY;
+      }
+      // the tile maximum of t = fl(z c) is fl(max z * c) (c > 0, rounding
+      // is monotone)
+      float a[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) a[u] = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 64; ++k) a[k & 7] = fmax3(a[k & 7], x[2 * k], x[2 * k + 1]);
+      const float zm = fmax3(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
+      const float tm = zm == -INFINITY ? -INFINITY : zm * p.c;
+      const float mn = fmaxf(m, tm);
+      if (mn != -INFINITY) {
+        // ex2 of fl(z c - m): one rounding where fl(fl(z c) - m) has two
+        const uint64_t nm2 = f2_splat(-mn);
+        uint64_t s2[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int k = 0; k < 64; ++k) {
+          const uint64_t d2 = f2_fma(f2_pack(x[2 * k], x[2 * k + 1]), c2, nm2);
+          s2[k & 3] = f2_add(s2[k & 3], f2_pack(mass_ex2(f2_lo(d2)), mass_ex2(f2_hi(d2))));
+        }
+        const uint64_t r2 = f2_add(f2_add(s2[0], s2[1]), f2_add(s2[2], s2[3]));
+        l = l * mass_ex2(m - mn) + (f2_lo(r2) + f2_hi(r2));
+        m = mn;
+      }
+    }
+    p.part[((bh * p.n_groups + rg) * kMassSplits + split) * kMassGroupRows + row] = make_float2(m, l);
+  } else if (warp == kMassTmaWarp) {
+    if (lane == 0) {
+      mass_loader(sm, mb, &kmap, nprime, n, krow0, 1, abort_flag, p.err);
+      if (p.q_tma && n > 0) (void)mbar_wait(mb.qfull, 0);  // the query copy has landed (also after a failure)
+    }
+  } else if (lane == 0) {
+    mass_mma<false>(sm, mb, tbase, n, p.q_tma != 0, abort_flag, p.err);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMassMmaWarp) {
+    tc_fence_after();
+    tc_dealloc(tbase, kMassTmemCols);
+  }
+}
+
+// Pass 2.  grid (blocks, HKV * n_groups, B), 320 threads; block x takes the
+// 128-key tiles x, x + blocks, ... of [0, P).  D = K Q^T puts a key in each
+// TMEM lane and the group's 256 rows in the columns; consumer warp w takes
+// the keys of lane quarter w % 4 and the rows 128 (w / 4) .. + 127: the sum
+// over its rows of fma(ex2(fl(z c - m_r)), 1 / l_r); the two row halves are
+// added in a fixed order.  colsum[(bh * n_groups + rg) * pmax + j].
+__global__ void __launch_bounds__(kMassThreads, 1)
+    mass_colsum_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
+                       const __grid_constant__ MassParams p) {
+  extern __shared__ uint8_t mass_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(mass_raw) + 1023) & ~(uintptr_t)1023);
+  const MassBars mb = mass_bars(sm);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + kMOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kMOffMisc + 4);
+  float4* st4 = reinterpret_cast<float4*>(sm + kMOffSt);  // rows (2i, 2i+1): (-m, -m, 1/l, 1/l)
+  float* xch = reinterpret_cast<float*>(sm + kMOffX);     // [2][128]
+  const int HKV = gridDim.y / p.n_groups, h = blockIdx.y / p.n_groups, rg = blockIdx.y % p.n_groups;
   const int b = blockIdx.z;
-  const size_t bh = (size_t)b * HKV + h, bg = bh * n_groups + rg;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  mass_stage_q(qs, qp, b, h, HKV, gq, n_proxy, n_ld, R, rg);
+  const size_t bh = (size_t)b * HKV + h, bg = bh * p.n_groups + rg;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nt = (p.L + kMassTileKeys - 1) / kMassTileKeys;
+  const int n = (int)blockIdx.x < nt ? (nt - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  const int64_t krow0 = (int64_t)bh * p.ld + (int64_t)blockIdx.x * kMassTileKeys;
+  const int nprime = min(n, kMassStages);
+  if (threadIdx.x == kMassTmaWarp * 32) {
+    mass_init_bars(mb);
+    *abort_flag = 0;
+    if (p.q_tma && n > 0) mass_load_q(sm, mb, &qmap, p, b, h, HKV, rg);
+    mass_loader(sm, mb, &kmap, 0, nprime, krow0, gridDim.x, abort_flag, p.err);
+  }
+  if (!p.q_tma) mass_stage_q_tc(sm, p, b, h, HKV, rg);
+  if (warp == kMassMmaWarp) tc_alloc(tslot, kMassTmemCols);
+  tc_fence_before();
   __syncthreads();
-  uint32_t a0[8][4], a1[8][4];
-  mass_load_a(qs, 2 * warp, lane, a0);
-  mass_load_a(qs, 2 * warp + 1, lane, a1);
-  float2 st[2][2];  // this thread's rows: (m, 1/l)
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+
+  if (warp < 8) {
+    {
+      // Row r's split partials merged: m the largest, l the sum over splits
+      // (in split order) of l_s 2^(m_s - m), and 1/l; rows past R weigh 0.
+      const int r = threadIdx.x;
+      float mr = 0.f, il = 0.f;
+      if (rg * kMassGroupRows + r < p.R) {
+        const float2* pr = p.part + bg * kMassSplits * kMassGroupRows + r;
+        float2 v[kMassSplits];
 #pragma unroll
-  for (int blk = 0; blk < 2; ++blk)
+        for (int q = 0; q < kMassSplits; ++q) v[q] = q < p.ns ? pr[q * kMassGroupRows] : make_float2(-INFINITY, 0.f);
+        float mx = -INFINITY;
 #pragma unroll
-    for (int hf = 0; hf < 2; ++hf) st[blk][hf] = stats[bg * kMassGroupRows + 16 * (2 * warp + blk) + g + 8 * hf];
-  const __nv_bfloat16* kb = k_src + bh * ld * HYQ_D;
-  const int step = gridDim.x * kMassKeys;
-  if ((int)blockIdx.x * kMassKeys < P) mass_stage_k_async(ksm, kb, blockIdx.x * kMassKeys, P);
-  for (int kt = blockIdx.x * kMassKeys, it = 0; kt < P; kt += step, ++it) {
-  __nv_bfloat16* kcur = ksm + (it & 1) * kMassKeys * kMassStride;
-  if (kt + step < P) {
-    mass_stage_k_async(ksm + ((it + 1) & 1) * kMassKeys * kMassStride, kb, kt + step, P);
-    mass_wait_async<1>();
-  } else {
-    mass_wait_async<0>();
+        for (int q = 0; q < kMassSplits; ++q) mx = fmaxf(mx, v[q].x);
+        float l = 0.f;
+        if (mx != -INFINITY) {
+#pragma unroll
+          for (int q = 0; q < kMassSplits; ++q)
+            if (v[q].x != -INFINITY) l += v[q].y * mass_ex2(v[q].x - mx);
+        }
+        mr = mx == -INFINITY ? 0.f : mx;
+        il = l > 0.f ? __frcp_rn(l) : 0.f;
+      }
+      float* sf = reinterpret_cast<float*>(st4);
+      sf[(r >> 1) * 4 + (r & 1)] = -mr;
+      sf[(r >> 1) * 4 + 2 + (r & 1)] = il;
+    }
+    asm volatile("bar.sync 1, 256;\n" ::: "memory");  // the rows' constants are in shared memory
+    const int half = warp >> 2, key = 32 * (warp & 3) + lane;
+    const uint32_t tl = tbase + ((uint32_t)(32 * (warp & 3)) << 16) + 128 * half;
+    const uint32_t sth = smem_u32(st4 + 64 * half);
+    const uint64_t c2 = f2_splat(p.c);
+    // Every consumer runs all n iterations (the named barrier below is
+    // passed once per tile by all 256); after a failed wait a thread skips
+    // the work of the remaining tiles.
+    bool ok = true;
+    for (int i = 0; i < n; ++i) {
+      const int bf = i & 1;
+      const int j0 = ((int)blockIdx.x + i * (int)gridDim.x) * kMassTileKeys;
+      if (ok && !mbar_wait_or_abort(mb.dfull + bf, (i >> 1) & 1, abort_flag)) {
+        *abort_flag = 1;
+        hyq_set_err(p.err, HYQ_DEVERR_TIMEOUT);
+        ok = false;
+      }
+      float cs = 0.f;
+      if (ok) {
+        tc_fence_after();
+        float x[128];
+        mass_ld128(tl + bf * 256, x);
+        tc_fence_before();
+        mbar_arrive(mb.dfree + bf);
+        uint64_t acc2[2] = {0, 0};
+#pragma unroll
+        for (int k = 0; k < 64; ++k) {  // rows 128 half + 2k, + 2k + 1
+          const float4 s = lds_f4(sth + 16 * k);
+          const uint64_t t2 = f2_fma(f2_pack(x[2 * k], x[2 * k + 1]), c2, f2_pack(s.x, s.y));  // fl(z c - m)
+          const uint64_t e2 = f2_pack(mass_ex2(f2_lo(t2)), mass_ex2(f2_hi(t2)));
+          acc2[k & 1] = f2_fma(e2, f2_pack(s.z, s.w), acc2[k & 1]);
+        }
+        const uint64_t r2 = f2_add(acc2[0], acc2[1]);
+        cs = f2_lo(r2) + f2_hi(r2);
+      }
+      float* xb = xch + bf * 128;
+      if (half) xb[key] = cs;
+      asm volatile("bar.sync 1, 256;\n" ::: "memory");
+      if (ok && !half && j0 + key < p.L) {
+        const float S = cs + xb[key];
+        if (p.keys)
+          p.keys[bh * p.pmax + j0 + key] = order_key(S, p.err);
+        else
+          p.colsum[bg * p.pmax + j0 + key] = S;
+      }
+    }
+  } else if (warp == kMassTmaWarp) {
+    if (lane == 0) {
+      mass_loader(sm, mb, &kmap, nprime, n, krow0, gridDim.x, abort_flag, p.err);
+      if (p.q_tma && n > 0) (void)mbar_wait(mb.qfull, 0);  // the query copy has landed (also after a failure)
+    }
+  } else if (lane == 0) {
+    mass_mma<true>(sm, mb, tbase, n, p.q_tma != 0, abort_flag, p.err);
   }
-  __syncthreads();  // tile `it` has landed for every thread; the sums of the previous one are read
-  float C[2][8][4];
-  mass_tile(kcur, lane, a0, a1, C);
-  float cs[8][2];
-#pragma unroll
-  for (int nb = 0; nb < 8; ++nb) cs[nb][0] = cs[nb][1] = 0.f;
-#pragma unroll
-  for (int blk = 0; blk < 2; ++blk)
-#pragma unroll
-    for (int hf = 0; hf < 2; ++hf)  // rows past R have 1/l = 0
-#pragma unroll
-      for (int nb = 0; nb < 8; ++nb)
-#pragma unroll
-        for (int e = 0; e < 2; ++e)
-          cs[nb][e] += mass_ex2(C[blk][nb][2 * hf + e] * c - st[blk][hf].x) * st[blk][hf].y;
-#pragma unroll
-  for (int nb = 0; nb < 8; ++nb)
-#pragma unroll
-    for (int e = 0; e < 2; ++e)
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1) cs[nb][e] += __shfl_xor_sync(0xffffffffu, cs[nb][e], o);
-  if (g == 0) {
-#pragma unroll
-    for (int nb = 0; nb < 8; ++nb)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) red[warp * kMassKeys + 8 * nb + 2 * t + e] = cs[nb][e];
-  }
+  tc_fence_before();
   __syncthreads();
-  if (threadIdx.x < kMassKeys && kt + (int)threadIdx.x < P) {
-    float S = 0.f;
-#pragma unroll
-    for (int w = 0; w < kMassThreads / 32; ++w) S += red[w * kMassKeys + threadIdx.x];
-    colsum[bg * pmax + kt + threadIdx.x] = S;
-  }
-  __syncthreads();  // buffer `it & 1` and the sums are consumed before they are reused
+  if (warp == kMassMmaWarp) {
+    tc_fence_after();
+    tc_dealloc(tbase, kMassTmemCols);
   }
 }
 
@@ -799,8 +967,7 @@ int32_t mass_groups(const hyq_config* c, int32_t n_proxy) {
 
 struct MassWs {
   float2* part;    // [bh][groups][kMassSplits][256]
-  float2* stats;   // [bh][groups][256]
-  float* colsum;   // [bh][groups][P]
+  float* colsum;   // [bh][groups][P] (more than one row group)
 };
 
 MassWs carve_mass(const hyq_config* c, int32_t L, void* ws) {
@@ -810,8 +977,6 @@ MassWs carve_mass(const hyq_config* c, int32_t L, void* ws) {
   MassWs w;
   w.part = reinterpret_cast<float2*>(p);
   p += round_up(bh * ng * kMassSplits * kMassGroupRows * sizeof(float2));
-  w.stats = reinterpret_cast<float2*>(p);
-  p += round_up(bh * ng * kMassGroupRows * sizeof(float2));
   w.colsum = reinterpret_cast<float*>(p);
   return w;
 }
@@ -878,7 +1043,7 @@ size_t hyq_select_mass_ws_bytes(const hyq_config* c, int32_t L) {
   const size_t ng = (size_t)mass_groups(c, c->period);
   int32_t P = L - c->window > 0 ? L - c->window : 0;
   return hyq_select_ws_bytes(c, L) + round_up(bh * ng * kMassSplits * kMassGroupRows * sizeof(float2)) +
-         round_up(bh * ng * kMassGroupRows * sizeof(float2)) + round_up(bh * ng * (size_t)(P > 0 ? P : 1) * 4);
+         round_up(bh * ng * (size_t)(P > 0 ? P : 1) * 4);
 }
 
 cudaError_t hyq_launch_select(const hyq_config* c, const void* q_proxy, int32_t n_proxy,
@@ -899,6 +1064,40 @@ cudaError_t hyq_launch_select(const hyq_config* c, const void* q_proxy, int32_t 
   return launch_topk(c, w, P, k, idx_out, s);
 }
 
+namespace {
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encode() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+// A BF16 source [rows][128] as a TMA map whose box is 64 dims x box_rows rows
+// with the 128-byte swizzle of the tensor-core operands; rows past the end
+// read as zero.
+cudaError_t make_row_map(CUtensorMap* map, const void* src, uint64_t rows, uint32_t box_rows) {
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encode();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {HYQ_D, rows};
+  const cuuint64_t strides[1] = {HYQ_D * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(src), dims, strides, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
 cudaError_t hyq_launch_select_mass(const hyq_config* c, const void* q_proxy, int32_t n_proxy,
                                    int32_t n_proxy_ld, const void* k_src, int32_t ld, int32_t L,
                                    int32_t* idx_out, int32_t k, void* ws, cudaStream_t s) {
@@ -907,39 +1106,58 @@ cudaError_t hyq_launch_select_mass(const hyq_config* c, const void* q_proxy, int
   const int32_t P = L - c->window;  // > 0 since k > 0
   const int32_t gq = c->num_q_heads / c->num_kv_heads, R = gq * n_proxy, ng = mass_groups(c, n_proxy);
   const float cs = (float)(1.0 / std::sqrt((double)HYQ_D) / std::log(2.0));  // fl(alpha log2 e)
-  const int smem_stats = (kMassGroupRows + 2 * kMassKeys) * kMassStride * 2;  // queries + two key buffers
-  const int smem_col = smem_stats + (kMassThreads / 32) * kMassKeys * 4;
   static std::atomic<uint64_t> attr_done{0};
   const cudaError_t ea = hyq_once_per_device(attr_done, [&] {
-    cudaError_t e = cudaFuncSetAttribute(mass_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_stats);
+    cudaError_t e = cudaFuncSetAttribute(mass_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMassSmem);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(mass_colsum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_col);
+      e = cudaFuncSetAttribute(mass_colsum_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMassSmem);
     return e;
   });
   if (ea != cudaSuccess) return ea;
+  CUtensorMap kmap, qmap;
+  cudaError_t e = make_row_map(&kmap, k_src, (uint64_t)c->batch * c->num_kv_heads * (uint64_t)ld, kMassTileKeys);
+  if (e == cudaSuccess)
+    e = make_row_map(&qmap, q_proxy, (uint64_t)c->batch * c->num_q_heads * (uint64_t)n_proxy_ld, kMassGroupRows);
+  if (e != cudaSuccess) return e;
+  // one block per SM (a block holds all 512 TMEM columns): the key tiles of a
+  // (sequence, KV head, row group) are shared by floor(SMs / units) blocks
   const int n_sm = hyq_num_sms();
-  // one block per SM for pass 1 (one fits an SM) and two per SM for pass 2
   const int units = c->num_kv_heads * ng * c->batch;
-  const int ns = std::min(kMassSplits, std::max(1, (n_sm + units - 1) / units));
-  const int ntiles = (P + kMassKeys - 1) / kMassKeys;
-  const int ncol = std::min(ntiles, std::max(1, (2 * n_sm + units - 1) / units));
-  const __nv_bfloat16* qp = static_cast<const __nv_bfloat16*>(q_proxy);
-  const __nv_bfloat16* kk = static_cast<const __nv_bfloat16*>(k_src);
-  mass_stats_kernel<<<dim3(ns, c->num_kv_heads * ng, c->batch), kMassThreads, smem_stats, s>>>(
-      qp, n_proxy, n_proxy_ld, gq, kk, ld, L, cs, R, ng, mw.part);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  mass_merge_kernel<<<dim3(c->num_kv_heads * ng, c->batch), kMassGroupRows, 0, s>>>(mw.part, mw.stats, R, ng,
-                                                                                    ns);
+  const int per = std::max(1, n_sm / units);
+  const int nt1 = (L + kMassTileKeys - 1) / kMassTileKeys, ntp = (P + kMassTileKeys - 1) / kMassTileKeys;
+  const int ns = std::max(1, std::min({kMassSplits, per, nt1}));
+  const int ncol = std::max(1, std::min(per, ntp));
+  MassParams mp{};
+  mp.qp = static_cast<const __nv_bfloat16*>(q_proxy);
+  mp.n_proxy = n_proxy;
+  mp.n_ld = n_proxy_ld;
+  mp.gq = gq;
+  mp.R = R;
+  mp.n_groups = ng;
+  mp.L = L;
+  mp.ld = ld;
+  mp.c = cs;
+  // every row group is 256 rows contiguous in the proxy buffer: TMA
+  mp.q_tma = (n_proxy == n_proxy_ld && R % kMassGroupRows == 0) ? 1 : 0;
+  mp.part = mw.part;
+  mp.ns = ns;
+  mp.colsum = mw.colsum;
+  mp.keys = ng == 1 ? w.keys : nullptr;  // one row group: pass 2 writes the keys itself
+  mp.pmax = P;
+  mp.err = w.err;
+  mass_stats_kernel<<<dim3(ns, c->num_kv_heads * ng, c->batch), kMassThreads, kMassSmem, s>>>(kmap, qmap, mp);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  mass_colsum_kernel<<<dim3(ncol, c->num_kv_heads * ng, c->batch), kMassThreads, smem_col, s>>>(qp, n_proxy, n_proxy_ld, gq, kk, ld, P, cs, R, ng, mw.stats, mw.colsum, P);
+  mp.L = P;
+  mass_colsum_kernel<<<dim3(ncol, c->num_kv_heads * ng, c->batch), kMassThreads, kMassSmem, s>>>(kmap, qmap, mp);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  mass_keys_kernel<<<dim3((P + 255) / 256, c->num_kv_heads, c->batch), 256, 0, s>>>(mw.colsum, ng, P, P, w.keys,
-                                                                                   w.err);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if (ng > 1) {
+    mass_keys_kernel<<<dim3((P + 255) / 256, c->num_kv_heads, c->batch), 256, 0, s>>>(mw.colsum, ng, P, P, w.keys,
+                                                                                     w.err);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   return launch_topk(c, w, P, k, idx_out, s);
 }
 

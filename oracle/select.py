@@ -206,7 +206,9 @@ def mass_error_bound(q_proxy, k_src, L: int, window: int, chunks: int = 1024,
     ex2(t - m) (partial sums over at most ``chunks`` key ranges merged once
     with ex2 rescaling), a = ex2(t - m) / l, and S(j) = sum_r a (float32, any
     order); ex2 has relative error at most ``ex2_rel`` and flushes results
-    below 2^-126 to zero.
+    below 2^-126 to zero.  An evaluation that forms the argument as
+    fl(z32 * c - m) with one fused rounding, or a with one fused multiply-add
+    into the column sum, rounds less and stays inside the same bound.
 
     With u = 2^-23 (one float32 ulp, covering truncating accumulators):
       dt_rj = c (1 + 2u) gamma_d sum_i |q_ri k_ji| + 2u c |z_rj|     (error of t)
