@@ -100,8 +100,13 @@ class PeriodRunner:
                 k = self.select(self.cfg, ring, ring.shape[2], self.k_srcs[li], self.L_end, self.idx[li],
                                 self.ws_sel)
                 L.hyq_rebuild(self.cfg, self.k_srcs[li], self.v_srcs[li], self.L_end, self.idx[li], k, lay.c)
-                n_sel = 5 if self.select is L.hyq_select_vertical_mass else (
-                    6 if self.cfg.vl_mode == L.VL_PER_QUERY_HEAD else 3)
+                if self.select is L.hyq_select_vertical_mass:
+                    # two passes and the top-k, plus a group-sum kernel when
+                    # the proxy rows of a KV group exceed one 256-row group
+                    rows = self.cfg.num_q_heads // self.cfg.num_kv_heads * ring.shape[2]
+                    n_sel = 3 if rows <= 256 else 4
+                else:
+                    n_sel = 6 if self.cfg.vl_mode == L.VL_PER_QUERY_HEAD else 3
                 n += (n_sel if k > 0 else 0) + \
                     (3 if self.L_end - self.cfg.window > 0 else 1)  # rows, marks, gather
         return n

@@ -302,12 +302,15 @@ hyq_status hyq_select_vertical_heads(const hyq_config *cfg, const void *q_proxy,
  *   S(j) = sum_r a_rj for j < P = max(0, L - W)
  * then the k positions with the largest S, ties to the lower position.
  * Evaluated in float32 from exact BF16 products on the tensor cores: per
- * row the maximum m and the sum l of 2^(t - m), t = (q_r . k_j) fl(alpha
- * log2 e), over at most 32 key ranges merged once, then S(j) = sum_r 2^(t - m) / l;
- * a NaN score sets HYQ_DEVERR_SCORE in the workspace's error word.
+ * row the maximum m of t = (q_r . k_j) fl(alpha log2 e) and the sum l of
+ * 2^(t - m), over at most 32 key ranges merged once, then
+ * S(j) = sum_r 2^(t - m) / l; a NaN score sets HYQ_DEVERR_SCORE in the
+ * workspace's error word.  k_src and q_proxy must be 16-byte aligned (they
+ * are read through TMA tensor maps).
  * Per KV head only: a config with vl_mode = HYQ_VL_PER_QUERY_HEAD returns
  * HYQ_ERR_UNSUPPORTED.
- * Workspace: hyq_workspace_size(cfg, HYQ_OP_SELECT_MASS, L).  Five launches.
+ * Workspace: hyq_workspace_size(cfg, HYQ_OP_SELECT_MASS, L).  Three launches
+ * when a KV group's proxy rows (g n_proxy) fit one group of 256, four beyond.
  */
 hyq_status hyq_select_vertical_mass(const hyq_config *cfg, const void *q_proxy, int32_t n_proxy,
                                     int32_t n_proxy_ld, const void *k_src, int32_t ld, int32_t L,
