@@ -20,9 +20,11 @@
 //     O_h += P_h V_h into TMEM for the two 64-key halves h of each tile;
 //     warps 0-7 (one thread per query row = TMEM lane and key half) read S,
 //     scale, mask, run an online softmax per half and write P as BF16 into
-//     one of two TMEM buffers, where the P.V MMA takes its A operand; one
-//     barrier signals both halves' P of a tile and one commit their P.V, and
-//     the two halves' (max, sum, O) merge once at the end.  The MMA threads
+//     one of two TMEM buffers, where the P.V MMA takes its A operand; a
+//     barrier per P buffer signals both halves' P of a tile and a commit per
+//     buffer their P.V (so the softmax waits for the P.V two tiles back, the
+//     last reader of the buffer, unless it rescales O), and the two halves'
+//     (max, sum, O) merge once at the end.  The MMA threads
 //     share schedulers with softmax warps, so their loops are kept to a few
 //     instructions, and the two products are issued from two threads so
 //     that neither's waits hold back the other.  The quantised segment uses e4m3 codes or e2m1 (FP4)
@@ -477,8 +479,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   uint64_t* kempty = bars + 21; // [kKStages]
   uint64_t* sfull = bars + 5;   // S of the current tile is in TMEM
   uint64_t* sfree = bars + 6;   // every softmax thread has read it
-  uint64_t* pfull = bars + 7;   // both key halves' P of a tile written
-  uint64_t* pvdone = bars + 9;  // that tile's P.V done (both halves)
+  uint64_t* pfull = bars + 7;   // [2]: both key halves' P of tile i written, on pfull[i % 2]
+  uint64_t* pvdone = bars + 9;  // [2]: tile i's P.V done (both halves) on pvdone[i % 2]
   uint64_t* mmadone = bars + 11;
   uint64_t* vfull = bars + 12;  // [kVStages]
   uint64_t* vempty = bars + 15; // [kVStages]
@@ -511,7 +513,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       mbar_init(kempty + i, 1);
     }
     mbar_init(pfull, kSoft);
+    mbar_init(pfull + 1, kSoft);
     mbar_init(pvdone, 1);
+    mbar_init(pvdone + 1, 1);
     mbar_init(mmadone, 2);  // one commit from each MMA-issuing thread
     mbar_init(sfull, 1);
     mbar_init(sfree, kSoft);
@@ -730,14 +734,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       }
       l_sum = l_sum * fac + rs;
 
-      if (j > 0) {  // the previous tile's P.V is done: O stable, P buffer free
-        if (!mbar_wait_or_abort(pvdone, (j - 1) & 1, abort_flag)) {
+      // A rescale of O needs every earlier P.V finished (the previous
+      // tile's); otherwise only the P.V that last read this tile's P buffer
+      // (two tiles back) has to be.
+      const bool resc = j > 0 && __any_sync(0xffffffffu, fac != 1.f);
+      if (resc || j > 1) {
+        const int jw = resc ? j - 1 : j - 2;
+        if (!mbar_wait_or_abort(pvdone + (jw & 1), (jw >> 1) & 1, abort_flag)) {
           fail();
           ok = false;
           break;
         }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, fac != 1.f)) {
+        if (resc) {
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             uint32_t o[32];
@@ -750,11 +759,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           tc_wait_st();
         }
       }
-      // P buffer j % 2: its previous tile's P.V is done
+      // P buffer j % 2: the P.V that last read it is done
       tc_st32(tbase + lane_off + kColP + 64 * s + 32 * hf, pw);
       tc_wait_st();
       tc_fence_before();
-      mbar_arrive(pfull);
+      mbar_arrive(pfull + s);
     }
     // Merge the two halves.  Each half waits for the last P.V, leaves
     // (m, l) in its own region of key stage 0 (no copy or MMA touches it any
@@ -762,7 +771,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     // makes both halves' accumulators and (m, l) visible to every thread;
     // each thread then writes dims 64hf .. 64hf+63 of its row.
     bool done = ok && nt > 0;
-    if (done && !mbar_wait_or_abort(pvdone, (nt - 1) & 1, abort_flag)) {
+    if (done && !mbar_wait_or_abort(pvdone + ((nt - 1) & 1), ((nt - 1) >> 1) & 1, abort_flag)) {
       fail();
       done = false;
     }
@@ -906,7 +915,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           const uint32_t tP = tbase + kColP + 64 * (i & 1);
           ok = mbar_wait_or_abort(vfull + sv, vph, abort_flag);
           const uint64_t dV = dV0 + sv * kStageStep;
-          if (ok) ok = mbar_wait_or_abort(pfull, i & 1, abort_flag);
+          if (ok) ok = mbar_wait_or_abort(pfull + (i & 1), (i >> 1) & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
@@ -917,7 +926,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
               tc_mma_f16_ts(tO, tP + 32 * hf + 8 * ks, dV + hf * kRegionStep + 2 * ks, kIdescBF16,
                             (i > 0 || ks > 0) ? 1u : 0u);
           }
-          tc_commit(pvdone);
+          tc_commit(pvdone + (i & 1));
           tc_commit(vempty + sv);
           if (++sv == kVStages) {
             sv = 0;
