@@ -199,6 +199,17 @@ def test_select_mass_parity(hyq, seed, B, HQ, HKV, Lc, W, ppm):
     check_mass(c, got, Lc, W, ppm)
 
 
+def test_select_mass_two_row_groups_from_strided_proxies(hyq):
+    """g = 8 query heads and 40 of the 64 proxy slots: 320 rows, not one
+    contiguous block of the proxy buffer, so the rows are staged thread by
+    thread; the second 256-row group is only partly filled (rows past 320
+    weigh nothing), and the two groups' column sums are added by the
+    group-sum kernel."""
+    c = decode_case(27, 1, 16, 2, 1800, window=128, n_proxy=64, sink_frac=0.02, outlier_channels=3)
+    got = run_select_mass(c, 1800, 128, 50_000, n_proxy=40)
+    check_mass(c, got, 1800, 128, 50_000, n_proxy=40)
+
+
 def test_select_mass_uses_only_the_first_n_proxies(hyq):
     c = decode_case(25, 1, 8, 2, 1500, window=128, n_proxy=64, sink_frac=0.02)
     got = run_select_mass(c, 1500, 128, 50_000, n_proxy=17)
