@@ -31,6 +31,8 @@ namespace {
 
 constexpr int kScoreThreads = 256;
 constexpr int kScoreRowsPerCta = 64;
+constexpr int kScoreRowsPerStep = 2 * (kScoreThreads / 32);  // one row per half-warp
+constexpr int kScoreSteps = kScoreRowsPerCta / kScoreRowsPerStep;
 constexpr int kTopkThreads = 1024;
 
 struct SelectWs {
@@ -67,16 +69,29 @@ __global__ void __launch_bounds__(kProxyThreads) proxy_sum_kernel(const __nv_bfl
   const int r0 = threadIdx.x >> 4, c = threadIdx.x & 15;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   const int rows = gq * n_proxy;
-  for (int r = r0; r < rows; r += 32) {
-    const int j = r / n_proxy, t = r - j * n_proxy;
-    const __nv_bfloat16* row = qp + (((size_t)b * HKV * gq + (size_t)h * gq + j) * n_ld + t) * HYQ_D;
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(row) + c);
-    const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&v);
+  // rows r0, r0 + 32, ... in order; eight of them loaded at a time
+  for (int rb = r0; rb < rows; rb += 8 * 32) {
+    uint4 v[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 f = __bfloat1622float2(p2[i]);
-      acc[2 * i] += f.x;
-      acc[2 * i + 1] += f.y;
+    for (int u = 0; u < 8; ++u) {
+      const int r = rb + 32 * u;
+      v[u] = make_uint4(0, 0, 0, 0);
+      if (r < rows) {
+        const int j = r / n_proxy, t = r - j * n_proxy;
+        const __nv_bfloat16* row = qp + (((size_t)b * HKV * gq + (size_t)h * gq + j) * n_ld + t) * HYQ_D;
+        v[u] = __ldg(reinterpret_cast<const uint4*>(row) + c);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (rb + 32 * u >= rows) break;
+      const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&v[u]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(p2[i]);
+        acc[2 * i] += f.x;
+        acc[2 * i + 1] += f.y;
+      }
     }
   }
 #pragma unroll
@@ -112,15 +127,22 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(
   for (int i = 0; i < 8; ++i) uu[i] = u[bh * HYQ_D + 8 * sub + i];
   const __nv_bfloat16* kb = k_src + bh * ld * HYQ_D;
   const int end = min(P, (int)(blockIdx.x + 1) * kScoreRowsPerCta);
-  // The trip count is uniform across the warp (both half-warps run every
-  // iteration) so the full-mask shuffles below are always complete.
-  for (int r0 = blockIdx.x * kScoreRowsPerCta + 2 * warp; r0 < end; r0 += 2 * (kScoreThreads / 32)) {
-    const int r = r0 + half;
+  // A thread's rows (every 16th of the block's) are all loaded before the
+  // first is reduced, so that they are in flight together.  Every lane runs
+  // every step, so the full-mask shuffles below are always complete.
+  uint4 raw[kScoreSteps];
+#pragma unroll
+  for (int it = 0; it < kScoreSteps; ++it) {
+    const int r = blockIdx.x * kScoreRowsPerCta + it * kScoreRowsPerStep + 2 * warp + half;
+    raw[it] = r < end ? *reinterpret_cast<const uint4*>(kb + (size_t)r * HYQ_D + 8 * sub) : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int it = 0; it < kScoreSteps; ++it) {
+    const int r = blockIdx.x * kScoreRowsPerCta + it * kScoreRowsPerStep + 2 * warp + half;
     const bool valid = r < end;
     float s = 0.f;
     if (valid) {
-      uint4 raw = *reinterpret_cast<const uint4*>(kb + (size_t)r * HYQ_D + 8 * sub);
-      const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&raw);
+      const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&raw[it]);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         float2 f = __bfloat1622float2(pr[i]);
@@ -155,15 +177,21 @@ __global__ void __launch_bounds__(kScoreThreads) score_heads_kernel(
   }
   const __nv_bfloat16* kb = k_src + bh * ld * HYQ_D;
   const int end = min(P, (int)(blockIdx.x + 1) * kScoreRowsPerCta);
-  for (int r0 = blockIdx.x * kScoreRowsPerCta + 2 * warp; r0 < end; r0 += 2 * (kScoreThreads / 32)) {
-    const int r = r0 + half;
+  uint4 raw[kScoreSteps];  // loaded together, as in score_kernel
+#pragma unroll
+  for (int it = 0; it < kScoreSteps; ++it) {
+    const int r = blockIdx.x * kScoreRowsPerCta + it * kScoreRowsPerStep + 2 * warp + half;
+    raw[it] = r < end ? *reinterpret_cast<const uint4*>(kb + (size_t)r * HYQ_D + 8 * sub) : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int it = 0; it < kScoreSteps; ++it) {
+    const int r = blockIdx.x * kScoreRowsPerCta + it * kScoreRowsPerStep + 2 * warp + half;
     const bool valid = r < end;
     float s[G + 1];
 #pragma unroll
     for (int q = 0; q <= G; ++q) s[q] = 0.f;
     if (valid) {
-      uint4 raw = *reinterpret_cast<const uint4*>(kb + (size_t)r * HYQ_D + 8 * sub);
-      const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&raw);
+      const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&raw[it]);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         float2 f = __bfloat1622float2(pr[i]);
